@@ -1,0 +1,91 @@
+"""CPU oracle of the BF16DLT1 delta format -- TEST INFRASTRUCTURE ONLY.
+
+A plain single-threaded C implementation (``bd_oracle.c``) of what the delta path computes,
+wrapped with ctypes for numpy arrays.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+``bench.py`` (its ``cpu_baseline`` leg and ``--impl reference`` arm) may import this package.
+The CUDA library never imports, links or executes anything here, and this package imports
+nothing from the library.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "bd_oracle.c")
+_LIB = os.path.join(_HERE, "libbd_oracle.so")
+
+OK, ERR_ARG, ERR_CAPACITY, ERR_FORMAT, ERR_CHECKSUM = 0, 1, 2, 3, 4
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compiles bd_oracle.c into libbd_oracle.so next to it (plain gcc, portable flags)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-o", tmp, _SRC],
+                       check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        u64, p = ctypes.c_uint64, ctypes.c_void_p
+        lib.orc_checksum.argtypes = [p, u64]
+        lib.orc_checksum.restype = u64
+        lib.orc_encode.argtypes = [p, p, u64, p, u64, ctypes.POINTER(u64), ctypes.POINTER(u64)]
+        lib.orc_encode.restype = ctypes.c_int
+        lib.orc_decode.argtypes = [p, u64, p, u64, u64, p]
+        lib.orc_decode.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _u16(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        a = a.view(np.uint16) if a.dtype.itemsize == 2 else a.astype(np.uint16)
+    return a.reshape(-1)
+
+
+def checksum(w) -> int:
+    """Checksum of a BF16 tensor given as any 16-bit numpy array."""
+    w = _u16(w)
+    return int(_load().orc_checksum(w.ctypes.data, w.size))
+
+
+def encode(old, new) -> tuple[np.ndarray, int]:
+    """Returns (payload bytes as a uint8 array, checksum of new)."""
+    old, new = _u16(old), _u16(new)
+    if old.size != new.size:
+        raise ValueError("old and new must have the same number of elements")
+    lib = _load()
+    size, ck = ctypes.c_uint64(), ctypes.c_uint64()
+    rc = lib.orc_encode(old.ctypes.data, new.ctypes.data, old.size, None, 0,
+                        ctypes.byref(size), ctypes.byref(ck))
+    if rc not in (OK, ERR_CAPACITY):
+        raise RuntimeError(f"orc_encode failed with {rc}")
+    out = np.zeros(size.value, dtype=np.uint8)
+    rc = lib.orc_encode(old.ctypes.data, new.ctypes.data, old.size, out.ctypes.data,
+                        out.size, ctypes.byref(size), ctypes.byref(ck))
+    if rc != OK:
+        raise RuntimeError(f"orc_encode failed with {rc}")
+    return out, int(ck.value)
+
+
+def decode(old, payload, expected_checksum: int) -> tuple[int, np.ndarray]:
+    """Returns (status, restored).  status is OK, ERR_FORMAT or ERR_CHECKSUM."""
+    old = _u16(old)
+    payload = np.ascontiguousarray(payload, dtype=np.uint8).reshape(-1)
+    out = np.empty_like(old)
+    rc = _load().orc_decode(old.ctypes.data, old.size, payload.ctypes.data, payload.size,
+                            ctypes.c_uint64(expected_checksum & (2**64 - 1)),
+                            out.ctypes.data)
+    return int(rc), out

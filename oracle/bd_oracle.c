@@ -1,0 +1,356 @@
+/*
+ * bd_oracle.c -- plain, slow, single-threaded CPU oracle of the BF16DLT1 v1 delta format.
+ *
+ * TEST INFRASTRUCTURE ONLY (see bd_oracle.h): never part of the product path.
+ *
+ * The steps follow the pages in their order:
+ *   1. XOR every old/new BF16 pair ([WT] "Delta update algebra"; [ARCv3] figure "How ARCv3
+ *      encodes a block of weights": each prev/next pair is XORed).
+ *   2. Classify each XOR by the field that changed ([ARCv3] same figure): zero (unchanged),
+ *      mantissa-only, or exponent/sign ("rare").
+ *   3. Omit unchanged elements: only the positions of changed elements are recorded, per
+ *      4096-element chunk, as a delta list or a bitmap, whichever is smaller.
+ *   4. Mantissa-only changes contribute just their 7 mantissa bits ([ARCv3] paragraph on
+ *      encoding the asymmetry: "mantissa-only changes contribute just their mantissa bits").
+ *   5. Rare changes are packed separately, each as one 16-bit block holding all changed
+ *      fields (sign, exponent and mantissa XOR together).
+ *   6. A checksum of the new weights is returned beside the payload ([ARCv3] API listing;
+ *      "the result is checksummed against the trainer's original").
+ * Decoding XORs both streams back into old ([WT]: old XOR mask = new) and verifies the
+ * checksum.  Readings where the pages are silent are the library's written format spec.
+ *
+ * Payload layout (all integers little-endian, no padding between sections):
+ *   header (64 bytes) | count table (C x {u16 M_c, u16 R_c}) | R stream (u16 per rare
+ *   element) | position section (per chunk: M block then R block) | M stream (7 bits per
+ *   mantissa-only element, LSB-first bit packing, pad bits zero)
+ */
+#include "bd_oracle.h"
+
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_CHUNK 4096u
+#define ORC_HEADER 64u
+
+/* Field masks of a BF16 word: sign bit 15, exponent bits 14..7, mantissa bits 6..0. */
+#define ORC_SIGN_EXP_BITS 0xFF80u
+#define ORC_MANT_BITS 0x007Fu
+
+/* Class of one XOR value. */
+enum { CLASS_ZERO = 0, CLASS_MANT = 1, CLASS_RARE = 2 };
+
+static int classify(uint16_t x) {
+  if (x == 0) return CLASS_ZERO;
+  if ((x & ORC_SIGN_EXP_BITS) == 0) return CLASS_MANT;
+  return CLASS_RARE;
+}
+
+/* ---- little-endian helpers ---------------------------------------------------------- */
+
+static void put_u16(uint8_t* p, uint16_t v) {
+  p[0] = (uint8_t)(v & 0xFF);
+  p[1] = (uint8_t)(v >> 8);
+}
+static void put_u32(uint8_t* p, uint32_t v) {
+  for (int b = 0; b < 4; b++) p[b] = (uint8_t)(v >> (8 * b));
+}
+static void put_u64(uint8_t* p, uint64_t v) {
+  for (int b = 0; b < 8; b++) p[b] = (uint8_t)(v >> (8 * b));
+}
+static uint16_t get_u16(const uint8_t* p) { return (uint16_t)(p[0] | (p[1] << 8)); }
+static uint32_t get_u32(const uint8_t* p) {
+  uint32_t v = 0;
+  for (int b = 0; b < 4; b++) v |= (uint32_t)p[b] << (8 * b);
+  return v;
+}
+static uint64_t get_u64(const uint8_t* p) {
+  uint64_t v = 0;
+  for (int b = 0; b < 8; b++) v |= (uint64_t)p[b] << (8 * b);
+  return v;
+}
+
+/* ---- checksum ----------------------------------------------------------------------- */
+/*
+ * The pages only say the result is "checksummed".  Definition used here: view the n BF16
+ * values as W = ceil(n/4) little-endian 64-bit words (word j holds elements 4j..4j+3,
+ * element 4j+e in bits 16e..16e+15, zero past n).  Each word is keyed by its position and
+ * mixed with the SplitMix64 output function (Steele, Lea & Flood, "Fast splittable
+ * pseudorandom number generators", OOPSLA 2014):
+ *   checksum = sum over j of  mix64( word_j XOR (j+1)*GAMMA )   (mod 2^64)
+ * For an all-zero tensor the terms are exactly the SplitMix64 outputs for seed 0.
+ */
+static const uint64_t GAMMA = 0x9E3779B97F4A7C15ull;
+
+static uint64_t mix64(uint64_t z) {
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+uint64_t orc_checksum(const uint16_t* w, uint64_t n) {
+  uint64_t sum = 0;
+  uint64_t words = (n + 3) / 4;
+  for (uint64_t j = 0; j < words; j++) {
+    uint64_t word = 0;
+    for (uint64_t e = 0; e < 4; e++) {
+      uint64_t i = 4 * j + e;
+      if (i < n) word |= (uint64_t)w[i] << (16 * e);
+    }
+    sum += mix64(word ^ ((j + 1) * GAMMA));
+  }
+  return sum;
+}
+
+/* ---- position blocks ---------------------------------------------------------------- */
+
+/* Length of chunk c of an n-element tensor. */
+static uint64_t chunk_len(uint64_t n, uint64_t c) {
+  uint64_t start = c * ORC_CHUNK;
+  uint64_t left = n - start;
+  return left < ORC_CHUNK ? left : ORC_CHUNK;
+}
+
+/* Bytes of a position block holding k positions of a chunk of length L:
+ * a delta list of k u16 values when 2k < ceil(L/8), otherwise a ceil(L/8)-byte bitmap. */
+static uint64_t block_bytes(uint64_t k, uint64_t L) {
+  uint64_t bitmap = (L + 7) / 8;
+  if (2 * k < bitmap) return 2 * k;
+  return bitmap;
+}
+
+/* Writes the block for the k ascending positions pos[0..k) of a chunk of length L at dst. */
+static void write_block(uint8_t* dst, const uint16_t* pos, uint64_t k, uint64_t L) {
+  uint64_t bitmap = (L + 7) / 8;
+  if (2 * k < bitmap) {
+    for (uint64_t j = 0; j < k; j++) {
+      uint16_t d = (uint16_t)(j == 0 ? pos[0] : pos[j] - pos[j - 1]);
+      put_u16(dst + 2 * j, d);
+    }
+  } else {
+    memset(dst, 0, bitmap);
+    for (uint64_t j = 0; j < k; j++) dst[pos[j] / 8] |= (uint8_t)(1u << (pos[j] % 8));
+  }
+}
+
+/* Reads a block with k positions of a chunk of length L from src into pos[0..k).
+ * Returns 0 when the block is canonical, -1 otherwise. */
+static int read_block(const uint8_t* src, uint16_t* pos, uint64_t k, uint64_t L) {
+  uint64_t bitmap = (L + 7) / 8;
+  if (2 * k < bitmap) {
+    uint64_t p = 0;
+    for (uint64_t j = 0; j < k; j++) {
+      uint64_t d = get_u16(src + 2 * j);
+      if (j > 0 && d == 0) return -1; /* positions must be strictly increasing */
+      p = (j == 0) ? d : p + d;
+      if (p >= L) return -1;
+      pos[j] = (uint16_t)p;
+    }
+    return 0;
+  }
+  uint64_t found = 0;
+  for (uint64_t p = 0; p < bitmap * 8; p++) {
+    if ((src[p / 8] >> (p % 8)) & 1) {
+      if (p >= L) return -1; /* unused tail bits must be zero */
+      if (found == k) return -1;
+      pos[found++] = (uint16_t)p;
+    }
+  }
+  return found == k ? 0 : -1;
+}
+
+/* ---- encode ------------------------------------------------------------------------- */
+
+int orc_encode(const uint16_t* old, const uint16_t* neu, uint64_t n, uint8_t* out,
+               uint64_t cap, uint64_t* size_out, uint64_t* checksum_out) {
+  if ((n > 0 && (old == NULL || neu == NULL)) || size_out == NULL || checksum_out == NULL)
+    return ORC_ERR_ARG;
+  uint64_t C = (n + ORC_CHUNK - 1) / ORC_CHUNK;
+
+  /* Steps 1-2: XOR and classify; count each class per chunk. */
+  uint64_t* mcount = (uint64_t*)calloc(C ? C : 1, sizeof(uint64_t));
+  uint64_t* rcount = (uint64_t*)calloc(C ? C : 1, sizeof(uint64_t));
+  if (!mcount || !rcount) { free(mcount); free(rcount); return ORC_ERR_ARG; }
+  for (uint64_t i = 0; i < n; i++) {
+    int cls = classify((uint16_t)(old[i] ^ neu[i]));
+    if (cls == CLASS_MANT) mcount[i / ORC_CHUNK]++;
+    if (cls == CLASS_RARE) rcount[i / ORC_CHUNK]++;
+  }
+
+  /* Section sizes. */
+  uint64_t sum_m = 0, sum_r = 0, pos_bytes = 0;
+  for (uint64_t c = 0; c < C; c++) {
+    uint64_t L = chunk_len(n, c);
+    sum_m += mcount[c];
+    sum_r += rcount[c];
+    pos_bytes += block_bytes(mcount[c], L) + block_bytes(rcount[c], L);
+  }
+  uint64_t m_bytes = (7 * sum_m + 7) / 8;
+  uint64_t size = ORC_HEADER + 4 * C + 2 * sum_r + pos_bytes + m_bytes;
+
+  /* Step 6: checksum of the new weights. */
+  *size_out = size;
+  *checksum_out = orc_checksum(neu, n);
+  if (out == NULL || cap < size) { free(mcount); free(rcount); return ORC_ERR_CAPACITY; }
+
+  memset(out, 0, size);
+  /* Header. */
+  memcpy(out, "BF16DLT1", 8);
+  put_u32(out + 8, 1);           /* version */
+  put_u32(out + 12, ORC_CHUNK);  /* chunk_elems */
+  put_u64(out + 16, n);
+  put_u64(out + 24, C);
+  put_u64(out + 32, sum_m);
+  put_u64(out + 40, sum_r);
+  put_u64(out + 48, pos_bytes);
+  put_u64(out + 56, size);
+
+  /* Count table. */
+  for (uint64_t c = 0; c < C; c++) {
+    put_u16(out + ORC_HEADER + 4 * c, (uint16_t)mcount[c]);
+    put_u16(out + ORC_HEADER + 4 * c + 2, (uint16_t)rcount[c]);
+  }
+
+  uint64_t r_off = ORC_HEADER + 4 * C;
+  uint64_t p_off = r_off + 2 * sum_r;
+  uint64_t m_off = p_off + pos_bytes;
+
+  /* Step 5: the rare stream -- the full 16-bit XOR of every exponent/sign change. */
+  for (uint64_t i = 0; i < n; i++) {
+    uint16_t x = (uint16_t)(old[i] ^ neu[i]);
+    if (classify(x) == CLASS_RARE) {
+      put_u16(out + r_off, x);
+      r_off += 2;
+    }
+  }
+
+  /* Step 3: positions of the changed elements, chunk by chunk (M block, then R block). */
+  uint16_t* mpos = (uint16_t*)malloc(ORC_CHUNK * sizeof(uint16_t));
+  uint16_t* rpos = (uint16_t*)malloc(ORC_CHUNK * sizeof(uint16_t));
+  for (uint64_t c = 0; c < C; c++) {
+    uint64_t L = chunk_len(n, c);
+    uint64_t km = 0, kr = 0;
+    for (uint64_t p = 0; p < L; p++) {
+      uint64_t i = c * ORC_CHUNK + p;
+      int cls = classify((uint16_t)(old[i] ^ neu[i]));
+      if (cls == CLASS_MANT) mpos[km++] = (uint16_t)p;
+      if (cls == CLASS_RARE) rpos[kr++] = (uint16_t)p;
+    }
+    write_block(out + p_off, mpos, km, L);
+    p_off += block_bytes(km, L);
+    write_block(out + p_off, rpos, kr, L);
+    p_off += block_bytes(kr, L);
+  }
+  free(mpos);
+  free(rpos);
+
+  /* Step 4: the mantissa stream -- 7 bits (x & 0x7F) per mantissa-only change, element j of
+   * the stream in bits [7j, 7j+7), stream bit b = bit (b % 8) of byte (b / 8). */
+  uint64_t j = 0;
+  for (uint64_t i = 0; i < n; i++) {
+    uint16_t x = (uint16_t)(old[i] ^ neu[i]);
+    if (classify(x) != CLASS_MANT) continue;
+    uint16_t v = (uint16_t)(x & ORC_MANT_BITS);
+    for (uint64_t b = 0; b < 7; b++) {
+      uint64_t bit = 7 * j + b;
+      if ((v >> b) & 1) out[m_off + bit / 8] |= (uint8_t)(1u << (bit % 8));
+    }
+    j++;
+  }
+
+  free(mcount);
+  free(rcount);
+  return ORC_OK;
+}
+
+/* ---- decode ------------------------------------------------------------------------- */
+
+int orc_decode(const uint16_t* old, uint64_t n, const uint8_t* payload, uint64_t size,
+               uint64_t expected, uint16_t* out) {
+  if ((n > 0 && (old == NULL || out == NULL)) || (size > 0 && payload == NULL))
+    return ORC_ERR_ARG;
+  if (size < ORC_HEADER) return ORC_ERR_FORMAT;
+  if (memcmp(payload, "BF16DLT1", 8) != 0) return ORC_ERR_FORMAT;
+  if (get_u32(payload + 8) != 1) return ORC_ERR_FORMAT;
+  if (get_u32(payload + 12) != ORC_CHUNK) return ORC_ERR_FORMAT;
+  uint64_t C = (n + ORC_CHUNK - 1) / ORC_CHUNK;
+  if (get_u64(payload + 16) != n) return ORC_ERR_FORMAT;
+  if (get_u64(payload + 24) != C) return ORC_ERR_FORMAT;
+  uint64_t hdr_m = get_u64(payload + 32), hdr_r = get_u64(payload + 40);
+  uint64_t hdr_pos = get_u64(payload + 48), hdr_size = get_u64(payload + 56);
+  if (hdr_size != size) return ORC_ERR_FORMAT;
+  if ((size - ORC_HEADER) / 4 < C) return ORC_ERR_FORMAT; /* count table must fit */
+
+  /* Count table: per-chunk counts, their totals and the closed-form size. */
+  uint64_t sum_m = 0, sum_r = 0, pos_bytes = 0;
+  for (uint64_t c = 0; c < C; c++) {
+    uint64_t L = chunk_len(n, c);
+    uint64_t km = get_u16(payload + ORC_HEADER + 4 * c);
+    uint64_t kr = get_u16(payload + ORC_HEADER + 4 * c + 2);
+    if (km + kr > L) return ORC_ERR_FORMAT;
+    sum_m += km;
+    sum_r += kr;
+    pos_bytes += block_bytes(km, L) + block_bytes(kr, L);
+  }
+  if (sum_m != hdr_m || sum_r != hdr_r || pos_bytes != hdr_pos) return ORC_ERR_FORMAT;
+  uint64_t m_bytes = (7 * sum_m + 7) / 8;
+  if (ORC_HEADER + 4 * C + 2 * sum_r + pos_bytes + m_bytes != size) return ORC_ERR_FORMAT;
+
+  uint64_t r_off = ORC_HEADER + 4 * C;
+  uint64_t p_off = r_off + 2 * sum_r;
+  uint64_t m_off = p_off + pos_bytes;
+
+  if (n > 0) memcpy(out, old, n * sizeof(uint16_t));
+  uint16_t* mpos = (uint16_t*)malloc(ORC_CHUNK * sizeof(uint16_t));
+  uint16_t* rpos = (uint16_t*)malloc(ORC_CHUNK * sizeof(uint16_t));
+  uint8_t* seen = (uint8_t*)malloc(ORC_CHUNK);
+  int status = ORC_OK;
+  uint64_t mj = 0, rj = 0;
+  for (uint64_t c = 0; c < C && status == ORC_OK; c++) {
+    uint64_t L = chunk_len(n, c);
+    uint64_t km = get_u16(payload + ORC_HEADER + 4 * c);
+    uint64_t kr = get_u16(payload + ORC_HEADER + 4 * c + 2);
+    if (read_block(payload + p_off, mpos, km, L) != 0) { status = ORC_ERR_FORMAT; break; }
+    p_off += block_bytes(km, L);
+    if (read_block(payload + p_off, rpos, kr, L) != 0) { status = ORC_ERR_FORMAT; break; }
+    p_off += block_bytes(kr, L);
+
+    /* A position belongs to at most one class. */
+    memset(seen, 0, ORC_CHUNK);
+    for (uint64_t j = 0; j < km; j++) seen[mpos[j]] = 1;
+    for (uint64_t j = 0; j < kr; j++) {
+      if (seen[rpos[j]]) { status = ORC_ERR_FORMAT; break; }
+    }
+    if (status != ORC_OK) break;
+
+    /* Mantissa-only changes: XOR the next 7-bit value into the mantissa. */
+    for (uint64_t j = 0; j < km; j++, mj++) {
+      uint16_t v = 0;
+      for (uint64_t b = 0; b < 7; b++) {
+        uint64_t bit = 7 * mj + b;
+        v |= (uint16_t)(((payload[m_off + bit / 8] >> (bit % 8)) & 1) << b);
+      }
+      if (v == 0) { status = ORC_ERR_FORMAT; break; }
+      out[c * ORC_CHUNK + mpos[j]] ^= v;
+    }
+    if (status != ORC_OK) break;
+
+    /* Rare changes: XOR the next full 16-bit block. */
+    for (uint64_t j = 0; j < kr; j++, rj++) {
+      uint16_t v = get_u16(payload + r_off + 2 * rj);
+      if ((v & ORC_SIGN_EXP_BITS) == 0) { status = ORC_ERR_FORMAT; break; }
+      out[c * ORC_CHUNK + rpos[j]] ^= v;
+    }
+  }
+  free(mpos);
+  free(rpos);
+  free(seen);
+  if (status != ORC_OK) return status;
+
+  /* Pad bits after the last mantissa value must be zero. */
+  for (uint64_t bit = 7 * sum_m; bit < 8 * m_bytes; bit++) {
+    if ((payload[m_off + bit / 8] >> (bit % 8)) & 1) return ORC_ERR_FORMAT;
+  }
+
+  if (orc_checksum(out, n) != expected) return ORC_ERR_CHECKSUM;
+  return ORC_OK;
+}

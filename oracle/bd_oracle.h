@@ -1,0 +1,60 @@
+/*
+ * bd_oracle.h -- plain single-threaded CPU oracle of the BF16 field-split delta format.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and the cpu_baseline /
+ * reference arm of bench.py may call, link or execute this code.  The product path (the
+ * CUDA library) never uses it and shares no code, header, table or constant with it.
+ *
+ * What it computes follows
+ *   [ARCv3]  "Every byte counts: ARCv3 and the case for cross-region RL" -- the paragraph on
+ *            how ARCv3 encodes the mantissa/exponent asymmetry and the figure "How ARCv3
+ *            encodes a block of weights" (XOR each prev/next pair, classify by changed field,
+ *            omit unchanged, keep only mantissa bits of mantissa-only changes, pack the rarer
+ *            exponent/sign changes separately as one block, checksum the result);
+ *            the API listing (delta_compress returns (compressed_diff, checksum);
+ *            delta_decompress(src, compressed_diff, checksum) restores dst bit for bit).
+ *   [WT]     "GPU-accelerated Weight Teleportation", section "Delta update algebra"
+ *            (mask = old XOR new; old XOR mask = new; bits only, no floating point).
+ * Everything below the field split (chunking, position coding, byte layout, checksum
+ * formula) is not on the pages; it is this library's format "BF16DLT1" version 1, whose
+ * written specification the oracle follows step by step.
+ */
+#ifndef BD_ORACLE_H
+#define BD_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Oracle status codes (numerically equal to the library's, but defined independently). */
+enum {
+  ORC_OK = 0,
+  ORC_ERR_ARG = 1,
+  ORC_ERR_CAPACITY = 2,
+  ORC_ERR_FORMAT = 3,
+  ORC_ERR_CHECKSUM = 4
+};
+
+/* 64-bit checksum of n BF16 words (see bd_oracle.c for the definition). */
+uint64_t orc_checksum(const uint16_t* w, uint64_t n);
+
+/* Encodes the delta old -> neu (n elements).  Always stores the exact payload size in
+ * *size_out and the checksum of neu in *checksum_out.  Writes the payload into out only when
+ * cap >= size; otherwise returns ORC_ERR_CAPACITY and leaves out untouched. */
+int orc_encode(const uint16_t* old, const uint16_t* neu, uint64_t n, uint8_t* out,
+               uint64_t cap, uint64_t* size_out, uint64_t* checksum_out);
+
+/* Decodes payload[0..size) against old (n elements) into out (n elements, must not alias
+ * old), then verifies checksum(out) == expected.  Returns ORC_OK, ORC_ERR_FORMAT (payload
+ * is not a canonical BF16DLT1 v1 payload for n elements) or ORC_ERR_CHECKSUM.  On an error
+ * the contents of out are unspecified. */
+int orc_decode(const uint16_t* old, uint64_t n, const uint8_t* payload, uint64_t size,
+               uint64_t expected, uint16_t* out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BD_ORACLE_H */
