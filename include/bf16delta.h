@@ -1,0 +1,165 @@
+/*
+ * bf16delta.h -- C ABI of libbf16delta, lossless delta sync of BF16 weights on one GB300.
+ *
+ * The operations are the ones described in
+ *   [ARCv3] "Every byte counts: ARCv3 and the case for cross-region RL"
+ *     - the paragraph on encoding the mantissa/exponent asymmetry and the figure
+ *       "How ARCv3 encodes a block of weights": each old/new BF16 pair is XORed and
+ *       classified by the field that changed; unchanged values are omitted; mantissa-only
+ *       changes contribute just their mantissa bits; the rarer exponent/sign changes are
+ *       packed separately, all their changed fields as one block; on the rollout side both
+ *       streams are applied to the previous checkpoint and the result is checksummed
+ *       against the trainer's original;
+ *     - the API listing: delta_compress(src, dst) -> (compressed_diff, checksum) and
+ *       delta_decompress(src, compressed_diff, checksum) -> restored, bit-identical to dst.
+ *   [WT] "GPU-accelerated Weight Teleportation", section "Delta update algebra":
+ *       mask = old XOR new on the trainer; old XOR mask = new on the rollout side; the
+ *       weights are plain bits (no floating-point arithmetic, no rounding).
+ *
+ * Payload format "BF16DLT1" version 1 (the pages fix only the field split; the rest is this
+ * library's format).  x = old ^ new as u16.  A change is mantissa-only (M) when x != 0 and
+ * (x & 0xFF80) == 0, rare (R) when (x & 0xFF80) != 0.  Tensors are cut into chunks of
+ * 4096 elements (C = ceil(n/4096), the last chunk may be shorter, length L_c).
+ * Little-endian, no padding between sections:
+ *   [header 64 B] [count table: C x {u16 M_c, u16 R_c}] [R stream: u16 x per R element]
+ *   [positions: per chunk, the M block then the R block] [M stream: 7 bits (x & 0x7F) per
+ *   M element, element j in stream bits [7j, 7j+7), bit b = bit b%8 of byte b/8, pad 0]
+ * A position block with k entries for a chunk of length L is a delta list of k u16
+ * (d_0 = p_0, d_j = p_j - p_{j-1}) when 2k < ceil(L/8), else a ceil(L/8)-byte bitmap
+ * (bit p = bit p%8 of byte p/8).  Elements inside every stream are in ascending position.
+ * Header: "BF16DLT1", u32 version=1, u32 chunk_elems=4096, u64 n, u64 C, u64 sum M,
+ * u64 sum R, u64 position bytes, u64 total size.
+ * Checksum (returned beside the payload, not stored in it): with word_j the little-endian
+ * 64-bit word of elements 4j..4j+3 (zero past n),
+ *   checksum = sum_j mix64(word_j ^ (j+1) * 0x9E3779B97F4A7C15)  mod 2^64,
+ * mix64 being the SplitMix64 output function (Steele, Lea & Flood 2014).
+ *
+ * Conventions for every call:
+ *   - "d_" pointers are device memory, "h_" pointers host memory, all owned by the caller.
+ *     The library allocates nothing; scratch comes from a caller-provided workspace.
+ *   - BF16 tensors are arrays of uint16_t bit patterns, 16-byte aligned.  Payload
+ *     buffers are 16-byte aligned; workspaces 256-byte aligned.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy default
+ *     stream).  Results are written to device memory in stream order.
+ *   - The return value reports argument and launch errors only (BD_ERR_INVALID_ARG,
+ *     BD_ERR_CUDA); nothing has been enqueued when it is not BD_OK.  Errors found on the
+ *     device (capacity, format, checksum) arrive in the int32 status words.
+ *   - The same workspace must not be used by two calls that may overlap on the GPU.
+ */
+#ifndef BF16DELTA_H
+#define BF16DELTA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Exported symbols (the library is built with hidden visibility otherwise). */
+#if defined(__GNUC__)
+#define BD_API __attribute__((visibility("default")))
+#else
+#define BD_API
+#endif
+
+typedef enum bd_status {
+  BD_OK = 0,
+  BD_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment, overlap or workspace size */
+  BD_ERR_CAPACITY = 2,    /* compress: payload larger than the capacity given */
+  BD_ERR_FORMAT = 3,      /* decompress: not a canonical BF16DLT1 v1 payload for n elements */
+  BD_ERR_CHECKSUM = 4,    /* decompress: checksum of the result differs from the expected */
+  BD_ERR_CUDA = 5         /* a CUDA runtime call or kernel launch failed */
+} bd_status;
+
+#define BD_CHUNK_ELEMS 4096u
+#define BD_HEADER_BYTES 64u
+/* Largest tensor accepted, in elements (2^40, i.e. 2 TiB of BF16). */
+#define BD_MAX_ELEMS (1ull << 40)
+
+/* One tensor of a batched compress.  All device pointers; d_status may be NULL. */
+typedef struct bd_compress_item {
+  const uint16_t* d_old;  /* trainer weights before the step (n elements) */
+  const uint16_t* d_new;  /* trainer weights after the step (n elements) */
+  uint64_t n;             /* elements */
+  void* d_payload;        /* output buffer of cap bytes */
+  uint64_t cap;           /* capacity of d_payload in bytes */
+  uint64_t* d_size;       /* out: exact payload size (also when it exceeds cap) */
+  uint64_t* d_checksum;   /* out: checksum of d_new */
+  int32_t* d_status;      /* out (optional): BD_OK or BD_ERR_CAPACITY */
+} bd_compress_item;
+
+/* One tensor of a batched decompress.  All device pointers; d_status may be NULL. */
+typedef struct bd_decompress_item {
+  const uint16_t* d_old;         /* rollout weights before the step (n elements) */
+  uint16_t* d_out;               /* result (n elements); == d_old for an in-place apply */
+  uint64_t n;                    /* elements */
+  const void* d_payload;         /* payload produced by compress for this tensor */
+  uint64_t size;                 /* payload bytes */
+  const uint64_t* d_expected;    /* expected checksum of the result (from compress) */
+  int32_t* d_status;             /* out (optional): BD_OK, BD_ERR_FORMAT or BD_ERR_CHECKSUM */
+} bd_decompress_item;
+
+/* Parsed payload header (host side). */
+typedef struct bd_payload_info_t {
+  uint64_t n, chunks, n_mant, n_rare, position_bytes, total_size;
+  uint32_t version, chunk_elems;
+} bd_payload_info_t;
+
+/* Largest payload compress can produce for n elements (every chunk at its worst split).
+ * Returns 0 for n > BD_MAX_ELEMS. */
+BD_API uint64_t bd_compress_bound(uint64_t n);
+
+/* Workspace bytes needed by bd_compress_batch / bd_decompress_batch for k tensors of
+ * h_n[0..k) elements (k = 1 for the single-tensor calls).  Returns 0 on bad arguments. */
+BD_API uint64_t bd_compress_workspace_size(const uint64_t* h_n, uint32_t k);
+BD_API uint64_t bd_decompress_workspace_size(const uint64_t* h_n, uint32_t k);
+
+/* [ARCv3] delta_compress: encodes old -> new into d_payload and returns the checksum of new.
+ * Writes the exact payload size to *d_size and the checksum to *d_checksum.  If the payload
+ * does not fit in cap bytes, the status is BD_ERR_CAPACITY, *d_size still holds the size
+ * needed and the payload bytes are unspecified.  d_status (optional, may be NULL) receives
+ * BD_OK or BD_ERR_CAPACITY.  d_old and d_new may not overlap d_payload or d_ws. */
+BD_API int bd_compress(const uint16_t* d_old, const uint16_t* d_new, uint64_t n, void* d_payload,
+                uint64_t cap, void* d_ws, uint64_t ws_bytes, uint64_t* d_size,
+                uint64_t* d_checksum, int32_t* d_status, void* stream);
+
+/* Batched compress: one launch per phase for k tensors; each tensor's payload, size and
+ * checksum are byte-identical to a single-tensor call.  h_items is read during the call
+ * only.  d_status (optional) receives the largest status code over the tensors. */
+BD_API int bd_compress_batch(const bd_compress_item* h_items, uint32_t k, void* d_ws,
+                      uint64_t ws_bytes, int32_t* d_status, void* stream);
+
+/* [ARCv3] delta_decompress, [WT] weights_updated = weights_old XOR mask: applies the payload
+ * to d_old, writing the result to d_out (d_out == d_old applies in place; any other overlap
+ * is BD_ERR_INVALID_ARG), then verifies checksum(result) == *d_expected.  *d_status receives
+ * BD_OK, BD_ERR_FORMAT or BD_ERR_CHECKSUM.  Chunks found malformed are left unwritten; on
+ * any error an in-place apply can be undone by applying the same payload again (XOR is an
+ * involution and decoding depends on the payload only). */
+BD_API int bd_decompress(const uint16_t* d_old, uint64_t n, const void* d_payload, uint64_t size,
+                  const uint64_t* d_expected, uint16_t* d_out, void* d_ws,
+                  uint64_t ws_bytes, int32_t* d_status, void* stream);
+
+/* Batched decompress: one launch per phase for k tensors.  *d_status (required) receives
+ * the largest status code over the tensors; per-tensor codes go to the items' d_status. */
+BD_API int bd_decompress_batch(const bd_decompress_item* h_items, uint32_t k, void* d_ws,
+                        uint64_t ws_bytes, int32_t* d_status, void* stream);
+
+/* The checksum above of n BF16 values, written to *d_out.  Needs no workspace. */
+BD_API int bd_checksum(const uint16_t* d_w, uint64_t n, uint64_t* d_out, void* stream);
+
+/* Parses and checks a payload header held in host memory (bytes >= 64).  Checks magic,
+ * version, chunk size and the internal consistency of the header fields; returns BD_OK,
+ * BD_ERR_FORMAT or BD_ERR_INVALID_ARG.  Does not touch the GPU. */
+BD_API int bd_payload_info(const void* h_header, uint64_t bytes, bd_payload_info_t* out);
+
+/* Waits for `stream` and returns the int32 status word at d_status (or BD_ERR_CUDA). */
+BD_API int bd_status_sync(const int32_t* d_status, void* stream);
+
+/* Static description of a status code. */
+BD_API const char* bd_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BF16DELTA_H */

@@ -1,0 +1,369 @@
+// bd_api.cu -- the C ABI of libbf16delta (include/bf16delta.h): argument checks, workspace
+// layout, the per-call tensor table and the kernel sequence of each operation.
+//
+// Operations follow "Every byte counts: ARCv3 and the case for cross-region RL" (API listing:
+// delta_compress(src, dst) -> (compressed_diff, checksum); delta_decompress(src,
+// compressed_diff, checksum) -> restored) and "GPU-accelerated Weight Teleportation",
+// section "Delta update algebra" (old XOR mask = new).
+#include <cstring>
+#include <memory>
+#include <vector>
+
+#include "bd_internal.cuh"
+
+namespace bd {
+namespace {
+
+constexpr uint64_t kAlign = 256;
+inline uint64_t up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
+
+struct Sizes {
+  uint64_t chunks = 0, tiles = 0, mbytes = 0;
+};
+
+bool sizes_of(const uint64_t* ns, uint32_t k, Sizes& s) {
+  s = Sizes{};
+  for (uint32_t i = 0; i < k; i++) {
+    const uint64_t n = ns[i];
+    if (n > BD_MAX_ELEMS) return false;
+    const uint64_t C = (n + kChunk - 1) / kChunk;
+    s.chunks += C;
+    s.tiles += (C + kTileChunks - 1) / kTileChunks;
+    s.mbytes += up(n, 16);
+  }
+  return true;
+}
+
+WsLayout make_layout(uint32_t k, const Sizes& s, bool compress) {
+  WsLayout L{};
+  uint64_t off = 0;
+  L.state = off;
+  L.ck = off;
+  off = up(off + (uint64_t)k * kCkBytes, kAlign);
+  L.info = off;
+  off = up(off + (uint64_t)k * sizeof(JobInfo), kAlign);
+  L.state_bytes = off - L.state;
+  L.jobs = off;
+  off = up(off + (uint64_t)k * 128, kAlign);
+  L.chunk_start = off;
+  off = up(off + ((uint64_t)k + 1) * 8, kAlign);
+  L.tile_start = off;
+  off = up(off + ((uint64_t)k + 1) * 8, kAlign);
+  L.loc = off;
+  off = up(off + s.chunks * 16, kAlign);
+  L.tile_tot = off;
+  off = up(off + s.tiles * sizeof(TileSum), kAlign);
+  L.tile_pre = off;
+  off = up(off + s.tiles * sizeof(TileSum), kAlign);
+  if (compress) {
+    L.counts = off;
+    off = up(off + s.chunks * 4, kAlign);
+    L.slots = off;
+    off = up(off + s.chunks * kSlotBytes, kAlign);
+    L.mbytes = off;
+    off = up(off + s.mbytes, kAlign);
+  }
+  L.total = off;
+  return L;
+}
+
+// ---- host -> device upload of the tensor table through kernel parameters -----------------
+// Kernel parameters are copied at launch, so the host table may be released as soon as the
+// call returns and no pageable-memory copy (which may synchronise) is involved.
+constexpr uint32_t kBlobWords = 30 * 1024 / 16;
+struct Blob {
+  uint32_t words;
+  uint32_t pad[3];
+  uint4 data[kBlobWords];
+};
+
+__global__ void k_put(const __grid_constant__ Blob b, uint4* __restrict__ dst) {
+  for (uint32_t i = threadIdx.x; i < b.words; i += blockDim.x) dst[i] = b.data[i];
+}
+
+cudaError_t upload(const std::vector<uint8_t>& host, uint8_t* dst, cudaStream_t s) {
+  static_assert(sizeof(Blob) <= 32000, "kernel parameter limit");
+  const uint64_t words = host.size() / 16;
+  std::unique_ptr<Blob> b(new Blob);
+  for (uint64_t w0 = 0; w0 < words; w0 += kBlobWords) {
+    const uint32_t cnt = (uint32_t)((words - w0) < kBlobWords ? (words - w0) : kBlobWords);
+    b->words = cnt;
+    std::memcpy(b->data, host.data() + w0 * 16, (size_t)cnt * 16);
+    k_put<<<1, 256, 0, s>>>(*b, reinterpret_cast<uint4*>(dst) + w0);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+int sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return sms;
+}
+
+inline bool aligned(const void* p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+// [a, a+na) and [b, b+nb) intersect
+inline bool overlaps(const void* a, uint64_t na, const void* b, uint64_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return na > 0 && nb > 0 && x < y + nb && y < x + na;
+}
+
+int check(cudaError_t e) { return e == cudaSuccess ? BD_OK : BD_ERR_CUDA; }
+
+// -------------------------------------------------------------------------------- compress
+int compress_impl(const bd_compress_item* items, uint32_t k, void* ws, uint64_t ws_bytes,
+                  int32_t* status_all, cudaStream_t s) {
+  if (k > 0 && items == nullptr) return BD_ERR_INVALID_ARG;
+  std::vector<uint64_t> ns(k);
+  for (uint32_t i = 0; i < k; i++) {
+    const bd_compress_item& it = items[i];
+    if (it.n > BD_MAX_ELEMS) return BD_ERR_INVALID_ARG;
+    if (it.n > 0 && (!it.d_old || !it.d_new || !aligned(it.d_old, 16) || !aligned(it.d_new, 16)))
+      return BD_ERR_INVALID_ARG;
+    if (it.cap > 0 && (!it.d_payload || !aligned(it.d_payload, 16))) return BD_ERR_INVALID_ARG;
+    if (!it.d_size || !it.d_checksum) return BD_ERR_INVALID_ARG;
+    if (overlaps(it.d_payload, it.cap, it.d_old, 2 * it.n) ||
+        overlaps(it.d_payload, it.cap, it.d_new, 2 * it.n))
+      return BD_ERR_INVALID_ARG;
+    ns[i] = it.n;
+  }
+  Sizes sz;
+  if (!sizes_of(ns.data(), k, sz)) return BD_ERR_INVALID_ARG;
+  const WsLayout lay = make_layout(k, sz, true);
+  if (!ws || !aligned(ws, kAlign) || ws_bytes < lay.total) return BD_ERR_INVALID_ARG;
+  for (uint32_t i = 0; i < k; i++)
+    if (overlaps(items[i].d_payload, items[i].cap, ws, lay.total)) return BD_ERR_INVALID_ARG;
+  const int sms = sm_count();
+  if (sms <= 0) return BD_ERR_CUDA;
+
+  // tensor table
+  std::vector<uint8_t> host(lay.loc - lay.jobs, 0);
+  CJob* jobs = reinterpret_cast<CJob*>(host.data());
+  uint64_t* cstart = reinterpret_cast<uint64_t*>(host.data() + (lay.chunk_start - lay.jobs));
+  uint64_t* tstart = reinterpret_cast<uint64_t*>(host.data() + (lay.tile_start - lay.jobs));
+  uint64_t cb = 0, tb = 0, mb = 0;
+  for (uint32_t i = 0; i < k; i++) {
+    const bd_compress_item& it = items[i];
+    CJob& J = jobs[i];
+    J.old = it.d_old;
+    J.neu = it.d_new;
+    J.payload = static_cast<uint8_t*>(it.d_payload);
+    J.n = it.n;
+    J.cap = it.cap;
+    J.d_size = it.d_size;
+    J.d_checksum = it.d_checksum;
+    J.d_status = it.d_status;
+    J.nchunks = (it.n + kChunk - 1) / kChunk;
+    J.chunk_base = cb;
+    J.tile_base = tb;
+    J.m_base = mb;
+    cstart[i] = cb;
+    tstart[i] = tb;
+    cb += J.nchunks;
+    tb += (J.nchunks + kTileChunks - 1) / kTileChunks;
+    mb += up(it.n, 16);
+  }
+  cstart[k] = cb;
+  tstart[k] = tb;
+
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  LaunchCtx c{s, sms, w, lay, k, sz.chunks, sz.tiles};
+  int rc;
+  if ((rc = check(cudaMemsetAsync(w + lay.state, 0, lay.state_bytes, s)))) return rc;
+  if (status_all && (rc = check(cudaMemsetAsync(status_all, 0, sizeof(int32_t), s)))) return rc;
+  if (k == 0) return BD_OK;
+  if ((rc = check(upload(host, w + lay.jobs, s)))) return rc;
+  if ((rc = check(launch_encode_slots(c)))) return rc;
+  if ((rc = check(launch_scan_tiles(c, false)))) return rc;
+  if ((rc = check(launch_scan_jobs(c, false, status_all)))) return rc;
+  if ((rc = check(launch_emit(c)))) return rc;
+  return check(launch_pack_mant(c));
+}
+
+// ------------------------------------------------------------------------------ decompress
+int decompress_impl(const bd_decompress_item* items, uint32_t k, void* ws, uint64_t ws_bytes,
+                    int32_t* status_all, cudaStream_t s) {
+  if (k > 0 && items == nullptr) return BD_ERR_INVALID_ARG;
+  if (!status_all || !aligned(status_all, 4)) return BD_ERR_INVALID_ARG;
+  std::vector<uint64_t> ns(k);
+  for (uint32_t i = 0; i < k; i++) {
+    const bd_decompress_item& it = items[i];
+    if (it.n > BD_MAX_ELEMS) return BD_ERR_INVALID_ARG;
+    if (it.n > 0 && (!it.d_old || !it.d_out || !aligned(it.d_old, 16) || !aligned(it.d_out, 16)))
+      return BD_ERR_INVALID_ARG;
+    if (it.d_out != it.d_old && overlaps(it.d_out, 2 * it.n, it.d_old, 2 * it.n))
+      return BD_ERR_INVALID_ARG;
+    if (it.size > 0 && (!it.d_payload || !aligned(it.d_payload, 16))) return BD_ERR_INVALID_ARG;
+    if (overlaps(it.d_out, 2 * it.n, it.d_payload, it.size)) return BD_ERR_INVALID_ARG;
+    if (!it.d_expected) return BD_ERR_INVALID_ARG;
+    ns[i] = it.n;
+  }
+  Sizes sz;
+  if (!sizes_of(ns.data(), k, sz)) return BD_ERR_INVALID_ARG;
+  const WsLayout lay = make_layout(k, sz, false);
+  if (!ws || !aligned(ws, kAlign) || ws_bytes < lay.total) return BD_ERR_INVALID_ARG;
+  for (uint32_t i = 0; i < k; i++)
+    if (overlaps(items[i].d_out, 2 * items[i].n, ws, lay.total)) return BD_ERR_INVALID_ARG;
+  const int sms = sm_count();
+  if (sms <= 0) return BD_ERR_CUDA;
+
+  std::vector<uint8_t> host(lay.loc - lay.jobs, 0);
+  DJob* jobs = reinterpret_cast<DJob*>(host.data());
+  uint64_t* cstart = reinterpret_cast<uint64_t*>(host.data() + (lay.chunk_start - lay.jobs));
+  uint64_t* tstart = reinterpret_cast<uint64_t*>(host.data() + (lay.tile_start - lay.jobs));
+  uint64_t cb = 0, tb = 0;
+  for (uint32_t i = 0; i < k; i++) {
+    const bd_decompress_item& it = items[i];
+    DJob& J = jobs[i];
+    J.old = it.d_old;
+    J.out = it.d_out;
+    J.payload = static_cast<const uint8_t*>(it.d_payload);
+    J.n = it.n;
+    J.size = it.size;
+    J.d_expected = it.d_expected;
+    J.d_status = it.d_status;
+    J.nchunks = (it.n + kChunk - 1) / kChunk;
+    J.chunk_base = cb;
+    J.tile_base = tb;
+    cstart[i] = cb;
+    tstart[i] = tb;
+    cb += J.nchunks;
+    tb += (J.nchunks + kTileChunks - 1) / kTileChunks;
+  }
+  cstart[k] = cb;
+  tstart[k] = tb;
+
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  LaunchCtx c{s, sms, w, lay, k, sz.chunks, sz.tiles};
+  int rc;
+  if ((rc = check(cudaMemsetAsync(w + lay.state, 0, lay.state_bytes, s)))) return rc;
+  if ((rc = check(cudaMemsetAsync(status_all, 0, sizeof(int32_t), s)))) return rc;
+  if (k == 0) return BD_OK;
+  if ((rc = check(upload(host, w + lay.jobs, s)))) return rc;
+  if ((rc = check(launch_scan_tiles(c, true)))) return rc;
+  if ((rc = check(launch_scan_jobs(c, true, nullptr)))) return rc;
+  if ((rc = check(launch_apply(c)))) return rc;
+  return check(launch_apply_finish(c, status_all));
+}
+
+uint64_t le64(const uint8_t* p) {
+  uint64_t v = 0;
+  for (int i = 0; i < 8; i++) v |= (uint64_t)p[i] << (8 * i);
+  return v;
+}
+
+}  // namespace
+}  // namespace bd
+
+using namespace bd;
+
+extern "C" {
+
+uint64_t bd_compress_bound(uint64_t n) {
+  if (n > BD_MAX_ELEMS) return 0;
+  const uint64_t C = (n + kChunk - 1) / kChunk;
+  const uint64_t full = n / kChunk, tail = n % kChunk;
+  const uint64_t bitmaps = full * kChunkBitmap + (tail + 7) / 8;
+  // per chunk: 2 bytes per R element + 7/8 byte per M element <= 2 bytes per element, and
+  // at most two bitmaps of position bytes; one byte of M-stream rounding
+  return kHeader + 4 * C + 2 * n + 2 * bitmaps + 1;
+}
+
+uint64_t bd_compress_workspace_size(const uint64_t* h_n, uint32_t k) {
+  if (k > 0 && !h_n) return 0;
+  Sizes s;
+  if (!sizes_of(h_n, k, s)) return 0;
+  return make_layout(k, s, true).total;
+}
+
+uint64_t bd_decompress_workspace_size(const uint64_t* h_n, uint32_t k) {
+  if (k > 0 && !h_n) return 0;
+  Sizes s;
+  if (!sizes_of(h_n, k, s)) return 0;
+  return make_layout(k, s, false).total;
+}
+
+int bd_compress(const uint16_t* d_old, const uint16_t* d_new, uint64_t n, void* d_payload,
+                uint64_t cap, void* d_ws, uint64_t ws_bytes, uint64_t* d_size,
+                uint64_t* d_checksum, int32_t* d_status, void* stream) {
+  bd_compress_item it{d_old, d_new, n, d_payload, cap, d_size, d_checksum, nullptr};
+  return compress_impl(&it, 1, d_ws, ws_bytes, d_status, static_cast<cudaStream_t>(stream));
+}
+
+int bd_compress_batch(const bd_compress_item* h_items, uint32_t k, void* d_ws,
+                      uint64_t ws_bytes, int32_t* d_status, void* stream) {
+  return compress_impl(h_items, k, d_ws, ws_bytes, d_status, static_cast<cudaStream_t>(stream));
+}
+
+int bd_decompress(const uint16_t* d_old, uint64_t n, const void* d_payload, uint64_t size,
+                  const uint64_t* d_expected, uint16_t* d_out, void* d_ws, uint64_t ws_bytes,
+                  int32_t* d_status, void* stream) {
+  bd_decompress_item it{d_old, d_out, n, d_payload, size, d_expected, nullptr};
+  return decompress_impl(&it, 1, d_ws, ws_bytes, d_status, static_cast<cudaStream_t>(stream));
+}
+
+int bd_decompress_batch(const bd_decompress_item* h_items, uint32_t k, void* d_ws,
+                        uint64_t ws_bytes, int32_t* d_status, void* stream) {
+  return decompress_impl(h_items, k, d_ws, ws_bytes, d_status,
+                         static_cast<cudaStream_t>(stream));
+}
+
+int bd_checksum(const uint16_t* d_w, uint64_t n, uint64_t* d_out, void* stream) {
+  if (!d_out || !aligned(d_out, 8) || n > BD_MAX_ELEMS) return BD_ERR_INVALID_ARG;
+  if (n > 0 && (!d_w || !aligned(d_w, 16))) return BD_ERR_INVALID_ARG;
+  const int sms = sm_count();
+  if (sms <= 0) return BD_ERR_CUDA;
+  return check(launch_checksum(d_w, n, d_out, static_cast<cudaStream_t>(stream), sms));
+}
+
+int bd_payload_info(const void* h_header, uint64_t bytes, bd_payload_info_t* out) {
+  if (!h_header || !out || bytes < kHeader) return BD_ERR_INVALID_ARG;
+  const uint8_t* p = static_cast<const uint8_t*>(h_header);
+  if (std::memcmp(p, "BF16DLT1", 8) != 0) return BD_ERR_FORMAT;
+  bd_payload_info_t I;
+  I.version = (uint32_t)(le64(p + 8) & 0xFFFFFFFFu);
+  I.chunk_elems = (uint32_t)(le64(p + 8) >> 32);
+  I.n = le64(p + 16);
+  I.chunks = le64(p + 24);
+  I.n_mant = le64(p + 32);
+  I.n_rare = le64(p + 40);
+  I.position_bytes = le64(p + 48);
+  I.total_size = le64(p + 56);
+  if (I.version != 1 || I.chunk_elems != kChunk || I.n > BD_MAX_ELEMS) return BD_ERR_FORMAT;
+  if (I.chunks != (I.n + kChunk - 1) / kChunk) return BD_ERR_FORMAT;
+  if (I.n_mant > I.n || I.n_rare > I.n - I.n_mant) return BD_ERR_FORMAT;
+  if (I.position_bytes > 2 * (uint64_t)kChunkBitmap * I.chunks) return BD_ERR_FORMAT;
+  const uint64_t want = kHeader + 4 * I.chunks + 2 * I.n_rare + I.position_bytes +
+                        (7 * I.n_mant + 7) / 8;
+  if (want != I.total_size) return BD_ERR_FORMAT;
+  *out = I;
+  return BD_OK;
+}
+
+int bd_status_sync(const int32_t* d_status, void* stream) {
+  if (!d_status) return BD_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return BD_ERR_CUDA;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, d_status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return BD_ERR_CUDA;
+  return v;
+}
+
+const char* bd_status_string(int code) {
+  switch (code) {
+    case BD_OK: return "ok";
+    case BD_ERR_INVALID_ARG: return "invalid argument";
+    case BD_ERR_CAPACITY: return "payload larger than the capacity given";
+    case BD_ERR_FORMAT: return "malformed payload";
+    case BD_ERR_CHECKSUM: return "checksum mismatch";
+    case BD_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,249 @@
+// bd_internal.cuh -- device-side definitions shared by the kernels of libbf16delta.
+//
+// Everything here follows the BF16DLT1 v1 format described in include/bf16delta.h.
+// The field split comes from "Every byte counts: ARCv3 and the case for cross-region RL"
+// (figure "How ARCv3 encodes a block of weights"); the XOR algebra from "GPU-accelerated
+// Weight Teleportation", section "Delta update algebra".
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "bf16delta.h"
+
+namespace bd {
+
+// ---------------------------------------------------------------------------- format
+constexpr uint32_t kChunk = 4096;          // elements per chunk
+constexpr uint32_t kChunkBitmap = 512;     // bitmap bytes of a full chunk
+constexpr uint32_t kHeader = 64;           // header bytes
+constexpr uint16_t kSignExp = 0xFF80;      // sign + exponent field of a BF16 word
+constexpr uint16_t kMant = 0x007F;         // mantissa field
+constexpr uint64_t kGamma = 0x9E3779B97F4A7C15ull;
+
+// Bytes of a position block holding k positions of a chunk whose bitmap has B bytes:
+// a delta list (2k bytes) when 2k < B, otherwise the B-byte bitmap.
+__host__ __device__ __forceinline__ uint32_t block_bytes(uint32_t k, uint32_t B) {
+  return (2 * k < B) ? 2 * k : B;
+}
+
+// SplitMix64 output function (Steele, Lea & Flood 2014) applied to a position-keyed word.
+__device__ __forceinline__ uint64_t mix64(uint64_t z) {
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+// Checksum terms of the 8 BF16 values in v, whose first element is element 8*q of the
+// tensor (q = group index) -- words 2q and 2q+1; `words` is the number of words of the
+// tensor (ceil(n/4)), so a group straddling the end contributes only its real words.
+__device__ __forceinline__ uint64_t group_hash(uint4 v, uint64_t q, uint64_t words) {
+  uint64_t j0 = 2 * q;
+  uint64_t w0 = (uint64_t)v.x | ((uint64_t)v.y << 32);
+  uint64_t w1 = (uint64_t)v.z | ((uint64_t)v.w << 32);
+  uint64_t k0 = (j0 + 1) * kGamma;
+  uint64_t h = 0;
+  if (j0 < words) h += mix64(w0 ^ k0);
+  if (j0 + 1 < words) h += mix64(w1 ^ (k0 + kGamma));
+  return h;
+}
+
+// Per-element class masks of the 8 XOR values in x (bit e <-> element e of the group).
+__device__ __forceinline__ void classify8(uint4 x, uint32_t& mmask, uint32_t& rmask) {
+  mmask = 0;
+  rmask = 0;
+  if ((x.x | x.y | x.z | x.w) == 0) return;
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    uint32_t lo = w[i] & 0xFFFFu, hi = w[i] >> 16;
+    if (lo) { if (lo & kSignExp) rmask |= 1u << (2 * i); else mmask |= 1u << (2 * i); }
+    if (hi) { if (hi & kSignExp) rmask |= 2u << (2 * i); else mmask |= 2u << (2 * i); }
+  }
+}
+
+__device__ __forceinline__ uint32_t elem_of(uint4 v, int e) {
+  uint32_t w = (e < 2) ? v.x : (e < 4) ? v.y : (e < 6) ? v.z : v.w;
+  return (e & 1) ? (w >> 16) : (w & 0xFFFFu);
+}
+
+// Loads 8 BF16 values starting at element e of p (16-byte aligned when e % 8 == 0);
+// elements at or past n read as zero.
+__device__ __forceinline__ uint4 load8(const uint16_t* __restrict__ p, uint64_t e, uint64_t n) {
+  if (e + 8 <= n) return __ldg(reinterpret_cast<const uint4*>(p + e));
+  uint32_t w[4] = {0, 0, 0, 0};
+  for (int i = 0; i < 8; i++)
+    if (e + i < n) w[i >> 1] |= (uint32_t)p[e + i] << (16 * (i & 1));
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Little-endian u16 at a possibly odd address (position blocks after an odd-length bitmap).
+__device__ __forceinline__ void store_u16(uint8_t* p, uint16_t v) {
+  if ((reinterpret_cast<uintptr_t>(p) & 1) == 0) {
+    *reinterpret_cast<uint16_t*>(p) = v;
+  } else {
+    p[0] = (uint8_t)(v & 0xFF);
+    p[1] = (uint8_t)(v >> 8);
+  }
+}
+__device__ __forceinline__ uint32_t load_u16(const uint8_t* p) {
+  if ((reinterpret_cast<uintptr_t>(p) & 1) == 0) return *reinterpret_cast<const uint16_t*>(p);
+  return (uint32_t)p[0] | ((uint32_t)p[1] << 8);
+}
+
+// Streaming variant (data read once): bypasses L1.
+__device__ __forceinline__ uint4 load8_stream(const uint16_t* __restrict__ p, uint64_t e,
+                                              uint64_t n) {
+  if (e + 8 <= n) return __ldcs(reinterpret_cast<const uint4*>(p + e));
+  return load8(p, e, n);
+}
+
+// ---------------------------------------------------------------------------- jobs
+
+// One tensor of a compress call, as the kernels see it (written into the workspace).
+struct CJob {
+  const uint16_t* old;
+  const uint16_t* neu;
+  uint8_t* payload;
+  uint64_t n;
+  uint64_t cap;
+  uint64_t* d_size;
+  uint64_t* d_checksum;
+  int32_t* d_status;
+  uint64_t chunk_base;  // global index of this tensor's chunk 0
+  uint64_t nchunks;     // C = ceil(n / 4096)
+  uint64_t tile_base;   // global index of this tensor's first scan tile
+  uint64_t m_base;      // byte offset of this tensor's M-byte staging area
+  uint64_t pad[4];
+};
+static_assert(sizeof(CJob) == 128, "CJob layout");
+
+// One tensor of a decompress call.
+struct DJob {
+  const uint16_t* old;
+  uint16_t* out;
+  const uint8_t* payload;
+  uint64_t n;
+  uint64_t size;
+  const uint64_t* d_expected;
+  int32_t* d_status;
+  uint64_t chunk_base;
+  uint64_t nchunks;
+  uint64_t tile_base;
+  uint64_t pad[6];
+};
+static_assert(sizeof(DJob) == 128, "DJob layout");
+
+// Per-tensor results of the scan phase (workspace).
+struct JobInfo {
+  uint64_t sum_m, sum_r, sum_p;   // totals
+  uint64_t r_start, p_start, m_start, total;
+  int32_t status;      // set by the scan phase; constant while later kernels run
+  int32_t chunk_err;   // set by the apply kernel when a chunk is malformed
+};
+static_assert(sizeof(JobInfo) == 64, "JobInfo layout");
+
+// Checksum accumulators per tensor: kCkSlots u64 spaced one 64-byte line apart so that
+// atomics from different warps spread over L2.
+constexpr int kCkSlots = 8;
+constexpr int kCkStride = 8;  // u64 per slot
+constexpr int kCkBytes = kCkSlots * kCkStride * 8;
+
+// Scan tiles: chunks per tile of the count scan.
+constexpr uint32_t kTileChunks = 1024;
+
+struct TileSum {   // totals of one scan tile (or their exclusive prefix)
+  uint64_t p, m, r, pad;
+};
+
+// Per-chunk slot written by the encode pass: u32 header (entry count, bit 31 = overflow)
+// followed by up to kSlotEntries entries (pos << 16 | x) in ascending position.
+constexpr uint32_t kSlotBytes = 1024;
+constexpr uint32_t kSlotEntries = kSlotBytes / 4 - 1;
+constexpr uint32_t kSlotOverflow = 0x80000000u;
+
+// Workspace layout of one call (byte offsets from the workspace base, 256-aligned).
+struct WsLayout {
+  uint64_t state;        // memset to zero at the start of a call: ck slots, job info
+  uint64_t state_bytes;
+  uint64_t ck;           // k * kCkBytes
+  uint64_t info;         // k * JobInfo
+  uint64_t jobs;         // k * CJob / DJob
+  uint64_t chunk_start;  // (k+1) u64: global chunk index where job j starts
+  uint64_t tile_start;   // (k+1) u64
+  uint64_t counts;       // Ctot u32 (compress only)
+  uint64_t slots;        // Ctot * kSlotBytes (compress only)
+  uint64_t loc;          // Ctot uint4: chunk exclusive prefix inside its tile (p, m, r)
+  uint64_t tile_tot;     // Utot TileSum
+  uint64_t tile_pre;     // Utot TileSum
+  uint64_t mbytes;       // sum over jobs of round_up(n, 16) (compress only)
+  uint64_t total;
+};
+
+// Index of the job containing global index g, given starts[0..k] (starts[k] = total).
+__device__ __forceinline__ uint32_t find_job(const uint64_t* __restrict__ starts, uint32_t k,
+                                             uint64_t g) {
+  uint32_t lo = 0, hi = k;  // invariant: starts[lo] <= g < starts[hi]
+  while (hi - lo > 1) {
+    uint32_t mid = (lo + hi) >> 1;
+    if (__ldg(starts + mid) <= g) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// Warp-level inclusive scan (sum) of a 32-bit value.
+__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    uint32_t o = __shfl_up_sync(0xFFFFFFFFu, v, d);
+    if (lane >= d) v += o;
+  }
+  return v;
+}
+
+__device__ __forceinline__ int32_t warp_incl_max(int32_t v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    int32_t o = __shfl_up_sync(0xFFFFFFFFu, v, d);
+    if (lane >= d) v = max(v, o);
+  }
+  return v;
+}
+
+__device__ __forceinline__ uint64_t warp_sum64(uint64_t v) {
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, d);
+  return v;
+}
+
+__device__ __forceinline__ void record_status(int32_t* info_status, int32_t code) {
+  atomicMax(reinterpret_cast<int*>(info_status), code);
+}
+
+}  // namespace bd
+
+// ---------------------------------------------------------------------------- launchers
+// Host-side launch functions of each translation unit (internal linkage to the library).
+namespace bd {
+struct LaunchCtx {
+  cudaStream_t stream;
+  int sms;             // multiprocessors of the current device
+  uint8_t* ws;         // workspace base
+  WsLayout lay;
+  uint32_t k;          // jobs
+  uint64_t chunks;     // total chunks
+  uint64_t tiles;      // total scan tiles
+};
+
+cudaError_t launch_encode_slots(const LaunchCtx& c);
+cudaError_t launch_scan_tiles(const LaunchCtx& c, bool decompress);
+cudaError_t launch_scan_jobs(const LaunchCtx& c, bool decompress, int32_t* d_status_all);
+cudaError_t launch_emit(const LaunchCtx& c);
+cudaError_t launch_pack_mant(const LaunchCtx& c);
+cudaError_t launch_apply(const LaunchCtx& c);
+cudaError_t launch_apply_finish(const LaunchCtx& c, int32_t* d_status_all);
+cudaError_t launch_checksum(const uint16_t* w, uint64_t n, uint64_t* out, cudaStream_t s,
+                            int sms);
+}  // namespace bd

@@ -1,0 +1,125 @@
+"""CPU tests of the C-ABI boundary: the library builds for sm_103a, loads without a GPU,
+exports exactly what include/bf16delta.h declares, and its host-only logic (size bounds,
+workspace sizes, header parsing, argument checks) behaves as documented.  No call here
+launches GPU work."""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+from lossless_bf16_weight_old_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bf16delta.h")
+
+
+def _declared() -> set[str]:
+    src = open(HEADER).read()
+    return set(re.findall(r"^BD_API\s+[\w\s\*]*?\b(bd_\w+)\s*\(", src, flags=re.M))
+
+
+def test_library_exports_every_declared_symbol(cuda_lib):
+    names = _declared()
+    assert len(names) == 11
+    for name in names:
+        assert hasattr(cuda_lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if l.split()[-1].startswith("bd_")}
+    assert exported == names
+
+
+def test_python_signatures_cover_header():
+    assert set(_lib.SIGNATURES) == _declared()
+
+
+def test_compress_bound_is_an_upper_bound(cuda_lib):
+    rng = np.random.default_rng(3)
+    for n in (0, 1, 7, 24, 4095, 4096, 4097, 20000):
+        old = rng.integers(0, 1 << 16, n).astype(np.uint16)
+        # worst cases: every element rare; and a mantissa/rare mix near the list/bitmap edge
+        cases = [old ^ np.uint16(0x8000), old ^ rng.integers(1, 1 << 16, n).astype(np.uint16)]
+        mix = old.copy()
+        mix[: n // 20] ^= np.uint16(0x0001)
+        mix[n // 20:] ^= np.uint16(0x0080)
+        cases.append(mix)
+        bound = cuda_lib.bd_compress_bound(n)
+        for new in cases:
+            payload, _ = oracle.encode(old, new)
+            assert payload.size <= bound
+    assert cuda_lib.bd_compress_bound((1 << 40) + 1) == 0
+
+
+def test_workspace_sizes(cuda_lib):
+    def ws(fn, ns):
+        arr = (ctypes.c_uint64 * max(1, len(ns)))(*ns)
+        return fn(arr, len(ns))
+    a = ws(cuda_lib.bd_compress_workspace_size, [1 << 20])
+    b = ws(cuda_lib.bd_compress_workspace_size, [1 << 21])
+    assert 0 < a < b
+    assert a % 256 == 0
+    # decompress needs only O(chunks) scratch, far less than compress
+    d = ws(cuda_lib.bd_decompress_workspace_size, [1 << 24])
+    assert 0 < d < (1 << 24) // 64
+    assert ws(cuda_lib.bd_compress_workspace_size, [(1 << 40) + 1]) == 0
+    assert ws(cuda_lib.bd_decompress_workspace_size, [1, 2, 3]) > 0
+
+
+def test_payload_info_parses_oracle_headers(cuda_lib):
+    rng = np.random.default_rng(9)
+    old = rng.integers(0, 1 << 16, 10000).astype(np.uint16)
+    new = old.copy()
+    new[::50] ^= np.uint16(3)
+    new[7::400] ^= np.uint16(0x4000)
+    payload, _ = oracle.encode(old, new)
+    info = _lib.PayloadInfo()
+    hdr = (ctypes.c_uint8 * 64).from_buffer_copy(payload[:64].tobytes())
+    assert cuda_lib.bd_payload_info(hdr, 64, ctypes.byref(info)) == 0
+    assert info.n == 10000 and info.chunks == 3 and info.version == 1
+    assert info.chunk_elems == 4096 and info.total_size == payload.size
+    assert info.n_mant == 200 and info.n_rare == 25
+    # flips that break a checked relation (n -> n + 65536 changes C; M, R, size change total)
+    for off in (0, 8, 12, 18, 24, 32, 40, 48, 56):
+        bad = bytearray(payload[:64].tobytes())
+        bad[off] ^= 1
+        b = (ctypes.c_uint8 * 64).from_buffer_copy(bytes(bad))
+        assert cuda_lib.bd_payload_info(b, 64, ctypes.byref(info)) == 3, off
+    assert cuda_lib.bd_payload_info(hdr, 63, ctypes.byref(info)) == 1
+
+
+def test_argument_checks_need_no_gpu(cuda_lib):
+    """Bad arguments are rejected before any CUDA call."""
+    one = ctypes.c_uint64(1)
+    dummy = ctypes.c_void_p(4096)
+    # null tensors
+    assert cuda_lib.bd_compress(None, None, 10, dummy, 100, dummy, 1 << 20, dummy, dummy,
+                                None, None) == 1
+    # misaligned tensor
+    assert cuda_lib.bd_compress(ctypes.c_void_p(4098), dummy, 10, ctypes.c_void_p(1 << 20),
+                                100, dummy, 1 << 20, dummy, dummy, None, None) == 1
+    # workspace too small
+    assert cuda_lib.bd_compress(dummy, dummy, 10, ctypes.c_void_p(1 << 20), 100,
+                                ctypes.c_void_p(1 << 24), 16, dummy, dummy, None, None) == 1
+    # decompress needs a status word and an expected checksum
+    assert cuda_lib.bd_decompress(dummy, 10, dummy, 100, dummy, dummy, dummy, 1 << 20, None,
+                                  None) == 1
+    # partially overlapping out-of-place output
+    assert cuda_lib.bd_decompress(ctypes.c_void_p(1 << 20), 1000, ctypes.c_void_p(1 << 24),
+                                  100, dummy, ctypes.c_void_p((1 << 20) + 16),
+                                  ctypes.c_void_p(1 << 26), 1 << 20, dummy, None) == 1
+    assert cuda_lib.bd_checksum(None, 5, dummy, None) == 1
+    assert cuda_lib.bd_status_sync(None, None) == 1
+    del one
+
+
+def test_status_strings(cuda_lib):
+    for code, word in [(0, b"ok"), (2, b"capacity"), (3, b"malformed"), (4, b"checksum")]:
+        assert word in cuda_lib.bd_status_string(code)
+
+
+def test_build_targets_sm103a():
+    assert "arch=compute_103a,code=sm_103a" in " ".join(build.ARCH)
