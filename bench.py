@@ -1,0 +1,492 @@
+"""Benchmark of the delta-sync hot path on GB300: compress (trainer side) + verified in-place
+apply (rollout side) of a synthetic BF16 checkpoint pair.
+
+One step = bd_compress_batch over every tensor (XOR, classify, pack, checksum of new) followed
+by bd_decompress_batch over every tensor (decode, scatter-XOR into the rollout copy, verify the
+checksum).  The rollout copy alternates between old and new from step to step (XOR is an
+involution), so every step is a full compress + a full verified apply, against checksum(new)
+on odd steps and checksum(old) on even ones.
+
+Prints one JSON line.  `value` is raw BF16 GB/s through the whole step (2 bytes per element
+of one checkpoint divided by compress+apply time), summed over ranks for N > 1 (independent
+replicas, weak scaling).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload dense7b] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "compress & apply GB/s of raw BF16 weights (% of HBM roofline); payload % raw"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _peak_hbm() -> tuple[float, str]:
+    try:
+        with open(PEAKS_FILE) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _workload_specs(name: str) -> list[W.Spec]:
+    if "@" in name:  # one tensor of a workload, e.g. sweep14336@rate0.02
+        base, which = name.split("@", 1)
+        return [s for s in W.specs(base) if s.name == which]
+    return W.specs(name)
+
+
+def _describe(name: str, specs: list[W.Spec]) -> str:
+    n = sum(s.numel for s in specs)
+    return f"{name}: {len(specs)} BF16 tensors, {n:,} elements ({2 * n / 1e9:.2f} GB per checkpoint)"
+
+
+def _source_hash() -> str:
+    """Hash of the CUDA sources, to tell whether stored ncu counters still apply."""
+    import hashlib
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "lossless_bf16_weight_old_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(f.encode())
+            with open(os.path.join(d, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(workload: str, phase: str):
+    """DRAM bytes (read + write) per call of `phase` from the committed ncu summary, or None
+    when there is none for this workload or the kernels changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            data = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if data.get("source_hash") != _source_hash():
+        return None
+    entry = data.get("phases", {}).get(phase, {})
+    if entry.get("workload") != workload:
+        return None
+    return entry.get("dram_bytes_per_call")
+
+
+# ------------------------------------------------------------------------ multi-rank helpers
+
+def dist_env() -> tuple[int, int, int]:
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max of a float over all ranks (identity when world == 1)."""
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ------------------------------------------------------------------------ clocks
+
+def _smi_id(dev, local: int) -> str:
+    """nvidia-smi -i argument for this device: its UUID when torch exposes it."""
+    props = torch.cuda.get_device_properties(dev)
+    uuid = getattr(props, "uuid", None)
+    if uuid:
+        u = str(uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if local < len(ids):
+            return ids[local]
+    return str(local)
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------ oracle baseline
+
+def _sample(specs: list[W.Spec], budget: int) -> list[W.Spec]:
+    """Tensors of the workload in order, skipping any larger than the budget, until the
+    budget of elements is reached (at least one tensor)."""
+    out, tot = [], 0
+    for s in specs:
+        if tot + s.numel > budget:
+            continue
+        out.append(s)
+        tot += s.numel
+    return out or [min(specs, key=lambda s: s.numel)]
+
+
+def oracle_baseline(specs: list[W.Spec], budget_elems: int, device) -> dict:
+    """Times the CPU oracle (single thread) on a bounded sample of the workload's tensors."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    sample = _sample(specs, budget_elems)
+    t_enc = t_dec = 0.0
+    elems = 0
+    for s in sample:
+        old, new = W.make_pair(s, device=device)
+        o = old.reshape(-1).view(torch.int16).cpu().numpy().view(np.uint16)
+        nw = new.reshape(-1).view(torch.int16).cpu().numpy().view(np.uint16)
+        del old, new
+        t0 = time.perf_counter()
+        payload, ck = oracle.encode(o, nw)
+        t1 = time.perf_counter()
+        st, restored = oracle.decode(o, payload, ck)
+        t2 = time.perf_counter()
+        if st != oracle.OK or not np.array_equal(restored, nw):
+            raise RuntimeError("oracle roundtrip failed")
+        t_enc += t1 - t0
+        t_dec += t2 - t1
+        elems += o.size
+    gbs = 2 * elems / (t_enc + t_dec) / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{len(sample)} tensors ({elems:,} elements) of the workload: "
+                      f"encode {t_enc:.2f} s + decode {t_dec:.2f} s, single thread",
+            "encode_gbs": round(2 * elems / t_enc / 1e9, 4),
+            "decode_gbs": round(2 * elems / t_dec / 1e9, 4)}
+
+
+def run_reference(args) -> None:
+    """The reference arm: the CPU oracle as it stands, on host cores, same metric/unit."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    oracle.build()
+    specs = _workload_specs(args.workload)
+    # each step: one bounded sample of the workload's tensors, generated on the CPU
+    sample = _sample(specs, args.ref_sample_elems)
+    pairs = []
+    for s in sample:
+        old, new = W.make_pair(s, device="cpu")
+        pairs.append((old.reshape(-1).view(torch.int16).numpy().view(np.uint16),
+                      new.reshape(-1).view(torch.int16).numpy().view(np.uint16)))
+    elems = sum(p[0].size for p in pairs)
+
+    def step():
+        for o, nw in pairs:
+            payload, ck = oracle.encode(o, nw)
+            st, _ = oracle.decode(o, payload, ck)
+            if st != oracle.OK:
+                raise RuntimeError("oracle roundtrip failed")
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    gbs = 2 * elems / dt / 1e9
+    desc = f"{len(sample)} tensors ({elems:,} elements) of {_describe(args.workload, specs)}"
+    line = {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "u16", "data": "synthetic",
+            "config": {"workload": desc, "where": "host CPU, CPU oracle, single thread"},
+            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1,
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------ GPU arm
+
+def run_ours(args) -> None:
+    import lossless_bf16_weight_old_gb300 as bd
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    bd._lib.load()
+
+    specs = _workload_specs(args.workload)
+    ns = [s.numel for s in specs]
+    n_total = sum(ns)
+    # flat buffers: old (trainer before), new (trainer after), rollout copy
+    offs, o = [], 0
+    for n in ns:
+        offs.append(o)
+        o += (n + 127) // 128 * 128
+    O = torch.empty(o, dtype=torch.bfloat16, device=dev)
+    N = torch.empty(o, dtype=torch.bfloat16, device=dev)
+    for s, off, n in zip(specs, offs, ns):
+        a, b = W.make_pair(s, device=dev)
+        O[off:off + n].copy_(a.reshape(-1))
+        N[off:off + n].copy_(b.reshape(-1))
+        del a, b
+    olds = [O[off:off + n] for off, n in zip(offs, ns)]
+    news = [N[off:off + n] for off, n in zip(offs, ns)]
+    Rb = O.clone()
+    rolls = [Rb[off:off + n] for off, n in zip(offs, ns)]
+    torch.cuda.synchronize()
+
+    # touched 32-byte sectors (16 elements) -- algorithmic write bytes of the in-place apply
+    touched = 0
+    for a, b in zip(olds, news):
+        m = len(a) // 16 * 16
+        diff = a.view(torch.int16) != b.view(torch.int16)
+        touched += int(diff[:m].view(-1, 16).any(1).sum().item()) + int(diff[m:].any().item())
+
+    stream = torch.cuda.current_stream()
+    comp = bd.CompressBatch(olds, news)
+    comp.run(stream)
+    torch.cuda.synchronize()
+    if int(comp.status.item()) != bd.OK:
+        raise RuntimeError(f"compress status {int(comp.status.item())}")
+    sizes = [int(v) for v in comp.sizes.tolist()]
+    payload_bytes = sum(sizes)
+    ck_new = comp.checksums.clone()
+    ck_old = torch.empty_like(ck_new)
+    for i, a in enumerate(olds):
+        ck_old[i:i + 1].copy_(bd.checksum(a))
+    dec_to_new = bd.DecompressBatch(rolls, comp.payloads, sizes, ck_new)
+    dec_to_old = bd.DecompressBatch(rolls, comp.payloads, sizes, ck_old)
+    torch.cuda.synchronize()
+
+    state = {"new": False}
+
+    def step(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        comp.run(stream)
+        if evs is not None:
+            evs[1].record(stream)
+        d = dec_to_old if state["new"] else dec_to_new
+        d.run(stream)
+        state["new"] = not state["new"]
+        if evs is not None:
+            evs[2].record(stream)
+        return d
+
+    clocks = ClockSampler(_smi_id(dev, local))
+    clocks.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world, dev)
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    last = None
+    for i in range(args.steps):
+        last = step(evs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world, dev)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    total_ms = start.elapsed_time(end)
+    t_comp = [e[0].elapsed_time(e[1]) for e in evs]
+    t_app = [e[1].elapsed_time(e[2]) for e in evs]
+
+    # correctness of the timed work (outside the timed region)
+    st_c, st_d = int(comp.status.item()), int(last.status.item())
+    want = N if state["new"] else O
+    if st_c != bd.OK or st_d != bd.OK or not torch.equal(Rb.view(torch.int16), want.view(torch.int16)):
+        raise RuntimeError(f"timed steps did not verify: compress {st_c}, apply {st_d}")
+
+    total_ms = reduce_max(total_ms, world, dev)
+    ms_step = total_ms / args.steps
+    raw = 2 * n_total
+    value = world * raw / (ms_step * 1e-3) / 1e9
+    peak, peak_kind = _peak_hbm()
+    mc, ma = statistics.mean(t_comp), statistics.mean(t_app)
+    comp_bytes = 4 * n_total + payload_bytes
+    app_bytes = 2 * n_total + payload_bytes + 32 * touched
+    comp_ach = comp_bytes / (mc * 1e-3) / 1e9
+    app_ach = app_bytes / (ma * 1e-3) / 1e9
+    dom = "compress" if mc >= ma else "apply"
+    roof = {"bound": "hbm",
+            "kernel": ("compress phase (bd_compress_batch: encode_slots + count scan + emit)"
+                       if dom == "compress" else
+                       "apply phase (bd_decompress_batch: count scan + decode + apply_stream + "
+                       "apply_dense + apply_finish)"),
+            "achieved": round(comp_ach if dom == "compress" else app_ach, 1),
+            "peak": peak, "unit": "GB/s",
+            "frac": round((comp_ach if dom == "compress" else app_ach) / peak, 4),
+            "traffic": _traffic(args.workload, dom), "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+            if peak_kind == "measured" else "fallback"}
+
+    # e2e through the public API with host buffers: H2D old+new from pinned memory, compress,
+    # verified apply, D2H of payloads + checksums + statuses
+    e2e = None
+    if True:
+        hO = torch.empty(O.shape, dtype=O.dtype, pin_memory=True)
+        hN = torch.empty(N.shape, dtype=N.dtype, pin_memory=True)
+        hO.copy_(O)
+        hN.copy_(N)
+        hP = torch.empty(max(payload_bytes, 1), dtype=torch.uint8, pin_memory=True)
+        hS = torch.empty(len(specs) * 3, dtype=torch.int64, pin_memory=True)
+        torch.cuda.synchronize()
+        # payload bytes of every tensor, packed one after another in host memory
+        regions, hoff = [], 0
+        for p, sz in zip(comp.payloads, sizes):
+            regions.append((p, hoff, sz))
+            hoff += sz
+
+        def e2e_step():
+            O.copy_(hO, non_blocking=True)
+            N.copy_(hN, non_blocking=True)
+            d = step()
+            for p, hoff, sz in regions:
+                hP[hoff:hoff + sz].copy_(p[:sz], non_blocking=True)
+            hS[:len(specs)].copy_(comp.sizes, non_blocking=True)
+            hS[len(specs):2 * len(specs)].copy_(comp.checksums, non_blocking=True)
+            hS[2 * len(specs):2 * len(specs) + 1].copy_(d.status.to(torch.int64), non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world, dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e2e_steps = max(3, min(args.steps, 10))
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = reduce_max(e0.elapsed_time(e1), world, dev) / e2e_steps
+        if int(hS[2 * len(specs)].item()) != bd.OK:
+            raise RuntimeError("e2e apply did not verify")
+        e2e = {"value": round(world * raw / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "ms_per_step": round(e_ms, 3), "steps": e2e_steps,
+               "h2d_bytes_per_step": 4 * n_total, "d2h_bytes_per_step":
+               payload_bytes + 8 * 2 * len(specs) + 8}
+        del hO, hN, hP
+
+    cpu = None
+    if rank == 0:
+        cpu = oracle_baseline(specs, args.cpu_sample_elems, dev)
+
+    blobs_c = -(-(128 * len(specs) + 2 * 8 * (len(specs) + 1) + 1024) // 30720)
+    launches_per_step = (blobs_c + 4) + (blobs_c + 6)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "u16", "data": "synthetic",
+                "config": {"workload": _describe(args.workload, specs),
+                           "l2": "inputs larger than L2 (no flush needed)"
+                           if 4 * n_total > 129e6 else "inputs fit in L2",
+                           "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+                "compress_gbs": round(raw / (mc * 1e-3) / 1e9, 2),
+                "apply_gbs": round(raw / (ma * 1e-3) / 1e9, 2),
+                "compress_ms": round(mc, 4), "apply_ms": round(ma, 4),
+                "compress_roofline_frac": round(comp_ach / peak, 4),
+                "apply_roofline_frac": round(app_ach / peak, 4),
+                "compress_algorithmic_bytes": comp_bytes, "apply_algorithmic_bytes": app_bytes,
+                "payload_pct": round(100 * payload_bytes / raw, 4),
+                "touched_sector_pct": round(100 * touched / (raw / 32), 3),
+                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
+                "gpu_launches": launches_per_step * args.steps}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="dense7b")
+    p.add_argument("--cpu-sample-elems", type=int, default=1_000_000_000,
+                   help="elements of the workload the CPU oracle baseline encodes+decodes")
+    p.add_argument("--ref-sample-elems", type=int, default=40_000_000,
+                   help="elements per step of the --impl reference arm")
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -18,7 +18,7 @@ constexpr uint64_t kAlign = 256;
 inline uint64_t up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
 
 struct Sizes {
-  uint64_t chunks = 0, tiles = 0, mbytes = 0;
+  uint64_t chunks = 0, tiles = 0;
 };
 
 bool sizes_of(const uint64_t* ns, uint32_t k, Sizes& s) {
@@ -29,7 +29,6 @@ bool sizes_of(const uint64_t* ns, uint32_t k, Sizes& s) {
     const uint64_t C = (n + kChunk - 1) / kChunk;
     s.chunks += C;
     s.tiles += (C + kTileChunks - 1) / kTileChunks;
-    s.mbytes += up(n, 16);
   }
   return true;
 }
@@ -42,6 +41,8 @@ WsLayout make_layout(uint32_t k, const Sizes& s, bool compress) {
   off = up(off + (uint64_t)k * kCkBytes, kAlign);
   L.info = off;
   off = up(off + (uint64_t)k * sizeof(JobInfo), kAlign);
+  L.overflow = off;  // decompress: count of chunks listed for the dense apply
+  off = up(off + 16, kAlign);
   L.state_bytes = off - L.state;
   L.jobs = off;
   off = up(off + (uint64_t)k * 128, kAlign);
@@ -55,13 +56,14 @@ WsLayout make_layout(uint32_t k, const Sizes& s, bool compress) {
   off = up(off + s.tiles * sizeof(TileSum), kAlign);
   L.tile_pre = off;
   off = up(off + s.tiles * sizeof(TileSum), kAlign);
+  L.slots = off;
+  off = up(off + s.chunks * kSlotBytes, kAlign);
   if (compress) {
     L.counts = off;
     off = up(off + s.chunks * 4, kAlign);
-    L.slots = off;
-    off = up(off + s.chunks * kSlotBytes, kAlign);
-    L.mbytes = off;
-    off = up(off + s.mbytes, kAlign);
+  } else {
+    L.ovf_list = off;
+    off = up(off + s.chunks * 4, kAlign);
   }
   L.total = off;
   return L;
@@ -146,7 +148,7 @@ int compress_impl(const bd_compress_item* items, uint32_t k, void* ws, uint64_t 
   CJob* jobs = reinterpret_cast<CJob*>(host.data());
   uint64_t* cstart = reinterpret_cast<uint64_t*>(host.data() + (lay.chunk_start - lay.jobs));
   uint64_t* tstart = reinterpret_cast<uint64_t*>(host.data() + (lay.tile_start - lay.jobs));
-  uint64_t cb = 0, tb = 0, mb = 0;
+  uint64_t cb = 0, tb = 0;
   for (uint32_t i = 0; i < k; i++) {
     const bd_compress_item& it = items[i];
     CJob& J = jobs[i];
@@ -161,12 +163,10 @@ int compress_impl(const bd_compress_item* items, uint32_t k, void* ws, uint64_t 
     J.nchunks = (it.n + kChunk - 1) / kChunk;
     J.chunk_base = cb;
     J.tile_base = tb;
-    J.m_base = mb;
     cstart[i] = cb;
     tstart[i] = tb;
     cb += J.nchunks;
     tb += (J.nchunks + kTileChunks - 1) / kTileChunks;
-    mb += up(it.n, 16);
   }
   cstart[k] = cb;
   tstart[k] = tb;
@@ -181,8 +181,7 @@ int compress_impl(const bd_compress_item* items, uint32_t k, void* ws, uint64_t 
   if ((rc = check(launch_encode_slots(c)))) return rc;
   if ((rc = check(launch_scan_tiles(c, false)))) return rc;
   if ((rc = check(launch_scan_jobs(c, false, status_all)))) return rc;
-  if ((rc = check(launch_emit(c)))) return rc;
-  return check(launch_pack_mant(c));
+  return check(launch_emit(c));
 }
 
 // ------------------------------------------------------------------------------ decompress
@@ -247,6 +246,8 @@ int decompress_impl(const bd_decompress_item* items, uint32_t k, void* ws, uint6
   if ((rc = check(upload(host, w + lay.jobs, s)))) return rc;
   if ((rc = check(launch_scan_tiles(c, true)))) return rc;
   if ((rc = check(launch_scan_jobs(c, true, nullptr)))) return rc;
+  if ((rc = check(launch_decode(c)))) return rc;
+  if ((rc = check(launch_apply_stream(c)))) return rc;
   if ((rc = check(launch_apply(c)))) return rc;
   return check(launch_apply_finish(c, status_all));
 }

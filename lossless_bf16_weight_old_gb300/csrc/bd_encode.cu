@@ -5,17 +5,18 @@
 // values, keep only the mantissa bits of mantissa-only changes and pack exponent/sign changes
 // separately as one block; the API returns a checksum beside the payload.
 //
-// Three passes, none of which waits on another CTA:
-//   encode_slots  reads old and new once (the only full-size read): per 4096-element chunk
-//                 it counts the M and R classes, accumulates the checksum of new and stores
-//                 the chunk's nonzero XORs (position, value) in a fixed 1 KiB slot of the
-//                 workspace; a chunk with more changes than a slot holds is marked overflow.
-//   (count scan in bd_scan.cu: per-chunk offsets of every section, header, size.)
-//   emit          writes the count table, the R stream and the position blocks straight to
-//                 their final payload offsets and stages the 7-bit M values as bytes;
-//                 overflow chunks re-read old/new instead of the slot.
-//   pack_mant     packs the staged M bytes into the 7-bit stream; each output byte is
-//                 written by the chunk that holds the element its first bit belongs to.
+// Two passes around the count scan (bd_scan.cu), neither of which waits on another CTA:
+//   encode_slots  the only full-size read of old and new.  One warp per 4096-element chunk:
+//                 branch-free classification, per-chunk class counts, the checksum of new,
+//                 and the chunk's nonzero XORs (position, value) in a fixed 1 KiB workspace
+//                 slot (a chunk with more changes than a slot holds is marked overflow and is
+//                 read again by emit).  The slot also records the chunk's first mantissa value.
+//   emit          one warp per chunk, after the scan: writes the count-table entry, the rare
+//                 stream, the position blocks and the chunk's share of the 7-bit mantissa
+//                 stream, all at their final payload offsets.  A mantissa-stream byte is
+//                 written by the chunk holding the element its first bit belongs to; when the
+//                 byte reaches into the next chunk that has mantissa values, the first of
+//                 them comes from that chunk's slot.
 #include "bd_internal.cuh"
 
 namespace bd {
@@ -24,12 +25,116 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 
-__device__ __forceinline__ uint64_t* ck_slot(uint8_t* ck_base, uint32_t job, uint64_t salt) {
-  return reinterpret_cast<uint64_t*>(ck_base + (uint64_t)job * kCkBytes) +
+__device__ __forceinline__ unsigned long long* ck_slot(uint8_t* ck_base, uint32_t job,
+                                                       uint64_t salt) {
+  return reinterpret_cast<unsigned long long*>(ck_base + (uint64_t)job * kCkBytes) +
          (salt & (kCkSlots - 1)) * kCkStride;
 }
 
+__device__ __forceinline__ uint4 xor4(uint4 a, uint4 b) {
+  return make_uint4(a.x ^ b.x, a.y ^ b.y, a.z ^ b.z, a.w ^ b.w);
+}
+
+// 16-bit element-order mask of the nonzero values among the 16 of (x0, x1).
+__device__ __forceinline__ uint32_t nz_mask16(uint4 x0, uint4 x1) {
+  const uint32_t a = flags_to_mask8(nz_flags(x0.x), nz_flags(x0.y), nz_flags(x0.z), nz_flags(x0.w));
+  const uint32_t b = flags_to_mask8(nz_flags(x1.x), nz_flags(x1.y), nz_flags(x1.z), nz_flags(x1.w));
+  return a | (b << 8);
+}
+
+__device__ __forceinline__ uint32_t rare_mask16(uint4 x0, uint4 x1) {
+  const uint32_t a = flags_to_mask8(rare_flags(x0.x), rare_flags(x0.y), rare_flags(x0.z),
+                                    rare_flags(x0.w));
+  const uint32_t b = flags_to_mask8(rare_flags(x1.x), rare_flags(x1.y), rare_flags(x1.z),
+                                    rare_flags(x1.w));
+  return a | (b << 8);
+}
+
+// Checksum terms of a full group of 8 values; key = (index of its first word + 1) * gamma.
+__device__ __forceinline__ uint64_t hash_group_full(uint4 v, uint64_t key) {
+  const uint64_t w0 = (uint64_t)v.x | ((uint64_t)v.y << 32);
+  const uint64_t w1 = (uint64_t)v.z | ((uint64_t)v.w << 32);
+  return mix64(w0 ^ key) + mix64(w1 ^ (key + kGamma));
+}
+
 // ------------------------------------------------------------------------ encode_slots
+template <bool FULL>
+__device__ __forceinline__ void encode_chunk(const uint16_t* __restrict__ old,
+                                             const uint16_t* __restrict__ neu, uint64_t n,
+                                             uint64_t e0, uint32_t* __restrict__ slot,
+                                             uint32_t& mcnt, uint32_t& rcnt, uint64_t& ck) {
+  const int lane = threadIdx.x & 31;
+  const uint64_t words = (n + 3) >> 2;
+  uint32_t* __restrict__ entries = slot + kSlotHeader / 4;
+  uint32_t running = 0;
+  uint32_t fm = 0;  // first mantissa value | kAuxHasM once found
+  uint64_t e = e0 + lane * 16;
+  uint4 o0, o1, n0, n1;
+  if (FULL) {
+    o0 = __ldcs(reinterpret_cast<const uint4*>(old + e));
+    o1 = __ldcs(reinterpret_cast<const uint4*>(old + e + 8));
+    n0 = __ldcs(reinterpret_cast<const uint4*>(neu + e));
+    n1 = __ldcs(reinterpret_cast<const uint4*>(neu + e + 8));
+  } else {
+    o0 = load8(old, e, n); o1 = load8(old, e + 8, n);
+    n0 = load8(neu, e, n); n1 = load8(neu, e + 8, n);
+  }
+  uint64_t key = ((e >> 2) + 1) * kGamma;  // key of this lane's first word
+#pragma unroll 1
+  for (int s = 0; s < 8; s++) {
+    const uint4 po0 = o0, po1 = o1, pn0 = n0, pn1 = n1;
+    if (s < 7) {
+      const uint64_t en = e + 512;
+      if (FULL) {
+        o0 = __ldcs(reinterpret_cast<const uint4*>(old + en));
+        o1 = __ldcs(reinterpret_cast<const uint4*>(old + en + 8));
+        n0 = __ldcs(reinterpret_cast<const uint4*>(neu + en));
+        n1 = __ldcs(reinterpret_cast<const uint4*>(neu + en + 8));
+      } else {
+        o0 = load8(old, en, n); o1 = load8(old, en + 8, n);
+        n0 = load8(neu, en, n); n1 = load8(neu, en + 8, n);
+      }
+    }
+    const uint32_t eloc = (uint32_t)(e - e0);
+    if (FULL) {
+      ck += hash_group_full(pn0, key) + hash_group_full(pn1, key + 2 * kGamma);
+    } else {
+      ck += group_hash(pn0, e >> 3, words) + group_hash(pn1, (e >> 3) + 1, words);
+    }
+    const uint4 x0 = xor4(po0, pn0), x1 = xor4(po1, pn1);
+    const uint32_t nz = nz_mask16(x0, x1);
+    const uint32_t cnt = __popc(nz);
+    const uint32_t incl = warp_incl_scan(cnt);
+    const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    uint32_t idx = running + incl - cnt;
+    uint32_t bits = nz, lane_fm = 0;
+    while (bits) {
+      const int b = __ffs(bits) - 1;
+      bits &= bits - 1;
+      const uint32_t xv = elem_of(b < 8 ? x0 : x1, b & 7);
+      if (xv & kSignExp) {
+        rcnt++;
+      } else {
+        mcnt++;
+        if (lane_fm == 0) lane_fm = xv | kAuxHasM;
+      }
+      if (idx < kSlotEntries) entries[idx] = ((eloc + b) << 16) | xv;
+      idx++;
+    }
+    if (fm == 0) {
+      const uint32_t has = __ballot_sync(0xFFFFFFFFu, lane_fm != 0);
+      if (has) fm = __shfl_sync(0xFFFFFFFFu, lane_fm, __ffs(has) - 1);
+    }
+    running += tot;
+    e += 512;
+    key += 128 * kGamma;  // 512 elements = 128 words per step
+  }
+  if (lane == 0) {
+    slot[0] = running > kSlotEntries ? (kSlotOverflow | kSlotEntries) : running;
+    slot[1] = fm;
+  }
+}
+
 __global__ void __launch_bounds__(kThreads)
 k_encode_slots(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
                uint32_t k, uint64_t total_chunks, uint32_t* __restrict__ counts,
@@ -38,91 +143,52 @@ k_encode_slots(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
   const uint64_t gwarp = ((uint64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
   const uint64_t nwarps = ((uint64_t)gridDim.x * kThreads) >> 5;
 
-  uint32_t cur_job = 0xFFFFFFFFu;
+  uint32_t j = 0xFFFFFFFFu, cur = 0xFFFFFFFFu;
   uint64_t ck = 0;
   for (uint64_t g = gwarp; g < total_chunks; g += nwarps) {
-    const uint32_t j = find_job(chunk_start, k, g);
-    if (j != cur_job) {
-      if (cur_job != 0xFFFFFFFFu) {
-        uint64_t s = warp_sum64(ck);
-        if (lane == 0) atomicAdd(reinterpret_cast<unsigned long long*>(ck_slot(ck_base, cur_job, gwarp)),
-                                 (unsigned long long)s);
+    j = advance_job(chunk_start, k, j, g);
+    if (j != cur) {
+      if (cur != 0xFFFFFFFFu) {
+        const uint64_t s = warp_sum64(ck);
+        if (lane == 0) atomicAdd(ck_slot(ck_base, cur, gwarp), (unsigned long long)s);
       }
-      cur_job = j;
+      cur = j;
       ck = 0;
     }
-    const uint16_t* __restrict__ old = jobs[j].old;
-    const uint16_t* __restrict__ neu = jobs[j].neu;
     const uint64_t n = jobs[j].n;
-    const uint64_t c = g - chunk_start[j];
-    const uint64_t e0 = c * kChunk;
-    const uint64_t words = (n + 3) >> 2;
-    uint32_t* __restrict__ slot = reinterpret_cast<uint32_t*>(slots + g * kSlotBytes);
-
-    uint32_t running = 0, mcnt = 0, rcnt = 0;
-    // two-stage register pipeline over the 8 steps of 512 elements
-    uint64_t e = e0 + lane * 16;
-    uint4 o0 = load8_stream(old, e, n), o1 = load8_stream(old, e + 8, n);
-    uint4 n0 = load8_stream(neu, e, n), n1 = load8_stream(neu, e + 8, n);
-#pragma unroll 1
-    for (int s = 0; s < 8; s++) {
-      uint4 po0 = o0, po1 = o1, pn0 = n0, pn1 = n1;
-      if (s < 7) {
-        const uint64_t en = e0 + (s + 1) * 512 + lane * 16;
-        o0 = load8_stream(old, en, n); o1 = load8_stream(old, en + 8, n);
-        n0 = load8_stream(neu, en, n); n1 = load8_stream(neu, en + 8, n);
-      }
-      const uint32_t eloc = s * 512 + lane * 16;
-      const uint64_t q = (e0 + eloc) >> 3;
-      ck += group_hash(pn0, q, words) + group_hash(pn1, q + 1, words);
-      const uint4 x0 = make_uint4(po0.x ^ pn0.x, po0.y ^ pn0.y, po0.z ^ pn0.z, po0.w ^ pn0.w);
-      const uint4 x1 = make_uint4(po1.x ^ pn1.x, po1.y ^ pn1.y, po1.z ^ pn1.z, po1.w ^ pn1.w);
-      uint32_t m0, r0, m1, r1;
-      classify8(x0, m0, r0);
-      classify8(x1, m1, r1);
-      const uint32_t mm = m0 | (m1 << 8), rm = r0 | (r1 << 8), nz = mm | rm;
-      mcnt += __popc(mm);
-      rcnt += __popc(rm);
-      const uint32_t cnt = __popc(nz);
-      const uint32_t incl = warp_incl_scan(cnt);
-      const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
-      uint32_t idx = running + incl - cnt;
-      uint32_t bits = nz;
-      while (bits) {
-        const int b = __ffs(bits) - 1;
-        bits &= bits - 1;
-        if (idx < kSlotEntries) {
-          const uint32_t xv = elem_of(b < 8 ? x0 : x1, b & 7);
-          slot[1 + idx] = ((eloc + b) << 16) | xv;
-        }
-        idx++;
-      }
-      running += tot;
-    }
+    const uint64_t e0 = (g - chunk_start[j]) * kChunk;
+    uint32_t* slot = reinterpret_cast<uint32_t*>(slots + g * kSlotBytes);
+    uint32_t mcnt = 0, rcnt = 0;
+    if (e0 + kChunk <= n)
+      encode_chunk<true>(jobs[j].old, jobs[j].neu, n, e0, slot, mcnt, rcnt, ck);
+    else
+      encode_chunk<false>(jobs[j].old, jobs[j].neu, n, e0, slot, mcnt, rcnt, ck);
     mcnt = warp_incl_scan(mcnt);
     rcnt = warp_incl_scan(rcnt);
-    if (lane == 31) {
-      counts[g] = mcnt | (rcnt << 16);
-      slot[0] = running > kSlotEntries ? (kSlotOverflow | kSlotEntries) : running;
-    }
+    if (lane == 31) counts[g] = mcnt | (rcnt << 16);
   }
-  if (cur_job != 0xFFFFFFFFu) {
-    uint64_t s = warp_sum64(ck);
-    if (lane == 0) atomicAdd(reinterpret_cast<unsigned long long*>(ck_slot(ck_base, cur_job, gwarp)),
-                             (unsigned long long)s);
+  if (cur != 0xFFFFFFFFu) {
+    const uint64_t s = warp_sum64(ck);
+    if (lane == 0) atomicAdd(ck_slot(ck_base, cur, gwarp), (unsigned long long)s);
   }
 }
 
 // ------------------------------------------------------------------------ emit
+
+// Per-warp shared scratch of emit.
+struct EmitSmem {
+  uint32_t bm[256];   // bitmaps: [0..128) mantissa-only, [128..256) rare
+  uint8_t mv[528];    // window of the chunk's 7-bit mantissa values, by chunk-local rank
+};
 
 // Where one chunk's output goes.
 struct EmitCtx {
   uint8_t* mblk;       // M position block
   uint8_t* rblk;       // R position block
   uint16_t* rstream;   // R stream at this chunk's first R element
-  uint8_t* mbytes;     // staged M bytes at this chunk's first M element
-  uint32_t* bm;        // shared bitmaps of this warp: [0..128) M, [128..256) R
+  EmitSmem* sm;
   uint32_t M, R;       // the chunk's counts: no write goes past them
+  uint32_t wbase;      // chunk-local rank of the value held in sm->mv[0]
   bool listM, listR;
 };
 
@@ -162,21 +228,15 @@ __device__ __forceinline__ void emit_batch(uint32_t p0, uint32_t mmask, uint32_t
     const uint32_t x = xf(b);
     if ((mmask >> b) & 1) {
       if (rm >= cx.M) continue;  // never taken when counts and data agree
-      if (cx.listM) {
-        store_u16(cx.mblk + 2 * rm, (uint16_t)(pos - (uint32_t)prevM));
-      } else {
-        atomicOr(&cx.bm[pos >> 5], 1u << (pos & 31));
-      }
-      cx.mbytes[rm] = (uint8_t)(x & kMant);
+      if (cx.listM) store_u16(cx.mblk + 2 * rm, (uint16_t)(pos - (uint32_t)prevM));
+      else atomicOr(&cx.sm->bm[pos >> 5], 1u << (pos & 31));
+      cx.sm->mv[rm - cx.wbase] = (uint8_t)(x & kMant);
       prevM = (int32_t)pos;
       rm++;
     } else {
       if (rr >= cx.R) continue;
-      if (cx.listR) {
-        store_u16(cx.rblk + 2 * rr, (uint16_t)(pos - (uint32_t)prevR));
-      } else {
-        atomicOr(&cx.bm[128 + (pos >> 5)], 1u << (pos & 31));
-      }
+      if (cx.listR) store_u16(cx.rblk + 2 * rr, (uint16_t)(pos - (uint32_t)prevR));
+      else atomicOr(&cx.sm->bm[128 + (pos >> 5)], 1u << (pos & 31));
       cx.rstream[rr] = (uint16_t)x;
       prevR = (int32_t)pos;
       rr++;
@@ -186,6 +246,23 @@ __device__ __forceinline__ void emit_batch(uint32_t p0, uint32_t mmask, uint32_t
   st.rankR += tot >> 16;
   st.lastM = max(st.lastM, __shfl_sync(0xFFFFFFFFu, inclM, 31));
   st.lastR = max(st.lastR, __shfl_sync(0xFFFFFFFFu, inclR, 31));
+}
+
+// Writes the mantissa-stream bytes b in [b_lo, b_hi) owned by this chunk.  Byte b starts in
+// global element floor(8b/7) (chunk-local jl) at bit s = 8b - 7*floor(8b/7); it takes the top
+// 7-s bits of value jl and the low s+1 bits of value jl+1 (`after` when jl+1 == M).
+__device__ __forceinline__ void put_mant_bytes(uint8_t* __restrict__ mout, uint64_t b_lo,
+                                               uint64_t b_hi, uint64_t Mex, uint32_t M,
+                                               uint32_t after, const EmitCtx& cx) {
+  const int lane = threadIdx.x & 31;
+  for (uint64_t b = b_lo + lane; b < b_hi; b += 32) {
+    const uint64_t jg = (8 * b) / 7;
+    const uint32_t s = (uint32_t)(8 * b - 7 * jg);
+    const uint32_t jl = (uint32_t)(jg - Mex);
+    const uint32_t v0 = cx.sm->mv[jl - cx.wbase];
+    const uint32_t v1 = (jl + 1 < M) ? cx.sm->mv[jl + 1 - cx.wbase] : after;
+    mout[b] = (uint8_t)((v0 >> s) | (v1 << (7 - s)));
+  }
 }
 
 // Copies a shared bitmap of B bytes to dst.  Every block of a tensor starts at an even
@@ -207,119 +284,123 @@ k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
        const uint64_t* __restrict__ tile_start, uint32_t k, uint64_t total_chunks,
        const uint32_t* __restrict__ counts, const uint8_t* __restrict__ slots,
        const uint4* __restrict__ loc, const TileSum* __restrict__ tile_pre,
-       const JobInfo* __restrict__ info, uint8_t* __restrict__ mbytes) {
-  __shared__ uint32_t s_bm[kWarps][256];
+       const JobInfo* __restrict__ info) {
+  __shared__ EmitSmem s_em[kWarps];
   const int lane = threadIdx.x & 31;
-  const int wib = threadIdx.x >> 5;
   const uint64_t gwarp = ((uint64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
   const uint64_t nwarps = ((uint64_t)gridDim.x * kThreads) >> 5;
-  uint32_t* bm = s_bm[wib];
+  EmitSmem* sm = &s_em[threadIdx.x >> 5];
 
+  uint32_t j = 0xFFFFFFFFu;
   for (uint64_t g = gwarp; g < total_chunks; g += nwarps) {
-    const uint32_t j = find_job(chunk_start, k, g);
+    j = advance_job(chunk_start, k, j, g);
+    const uint32_t cnt = counts[g];
+    const uint4 lc = loc[g];
+    const uint32_t* slot = reinterpret_cast<const uint32_t*>(slots + g * kSlotBytes);
+    const uint32_t hdr = slot[0];
     if (info[j].status != BD_OK) continue;
     const CJob& J = jobs[j];
     const uint64_t n = J.n;
     const uint64_t c = g - chunk_start[j];
     const uint64_t e0 = c * kChunk;
-    const uint32_t L = (uint32_t)((n - e0) < kChunk ? (n - e0) : kChunk);
+    const uint32_t L = (n - e0) < kChunk ? (uint32_t)(n - e0) : kChunk;
     const uint32_t B = (L + 7) >> 3;
-    const uint32_t cnt = counts[g];
     const uint32_t M = cnt & 0xFFFFu, R = cnt >> 16;
     const TileSum pre = tile_pre[tile_start[j] + c / kTileChunks];
-    const uint4 lc = loc[g];
     const uint64_t Pex = pre.p + lc.x, Mex = pre.m + lc.y, Rex = pre.r + lc.z;
+    const JobInfo& I = info[j];
     uint8_t* payload = J.payload;
     if (lane == 0) reinterpret_cast<uint32_t*>(payload + kHeader)[c] = cnt;
 
     EmitCtx cx;
     cx.listM = 2 * M < B;
     cx.listR = 2 * R < B;
-    cx.mblk = payload + info[j].p_start + Pex;
+    cx.mblk = payload + I.p_start + Pex;
     cx.rblk = cx.mblk + block_bytes(M, B);
-    cx.rstream = reinterpret_cast<uint16_t*>(payload + info[j].r_start) + Rex;
-    cx.mbytes = mbytes + J.m_base + Mex;
-    cx.bm = bm;
+    cx.rstream = reinterpret_cast<uint16_t*>(payload + I.r_start) + Rex;
+    cx.sm = sm;
     cx.M = M;
     cx.R = R;
+    cx.wbase = 0;
     if (!cx.listM || !cx.listR) {
-      for (int i = lane; i < 256; i += 32) bm[i] = 0;
+      for (int i = lane; i < 256; i += 32) sm->bm[i] = 0;
       __syncwarp();
     }
+    uint8_t* mout = payload + I.m_start;
+    // mantissa-stream bytes owned by this chunk: those whose first bit is in one of its values
+    const uint64_t b_lo = (7 * Mex + 7) >> 3, b_hi = (7 * (Mex + M) + 7) >> 3;
+    uint64_t b_next = b_lo;
     EmitState st{0, 0, 0, 0};
 
-    const uint32_t* slot = reinterpret_cast<const uint32_t*>(slots + g * kSlotBytes);
-    const uint32_t hdr = slot[0];
     if (!(hdr & kSlotOverflow)) {
-      const uint32_t kk = hdr;
+      const uint32_t kk = hdr & 0xFFFFu;
+      const uint32_t* entries = slot + kSlotHeader / 4;
       for (uint32_t base = 0; base < kk; base += 32) {
         const uint32_t i = base + lane;
         uint32_t ent = 0, mm = 0, rmk = 0;
         if (i < kk) {
-          ent = slot[1 + i];
-          const uint32_t x = ent & 0xFFFFu;
-          if (x & kSignExp) rmk = 1; else mm = 1;
+          ent = entries[i];
+          if (ent & kSignExp) rmk = 1; else mm = 1;
         }
         emit_batch(ent >> 16, mm, rmk, [ent](int) { return ent & 0xFFFFu; }, st, cx);
       }
     } else {
-      // Overflow: derive the chunk's changes again from old and new.
+      // Overflow: derive the chunk's changes again from old and new, 512 elements per step.
+      // After each step the bytes whose two values are known are written and the window of
+      // mantissa values keeps only its last value.
       const uint16_t* __restrict__ old = J.old;
       const uint16_t* __restrict__ neu = J.neu;
       for (int s = 0; s < 8; s++) {
         const uint32_t eloc = s * 512 + lane * 16;
         const uint64_t e = e0 + eloc;
-        const uint4 o0 = load8(old, e, n), o1 = load8(old, e + 8, n);
-        const uint4 n0 = load8(neu, e, n), n1 = load8(neu, e + 8, n);
-        const uint4 x0 = make_uint4(o0.x ^ n0.x, o0.y ^ n0.y, o0.z ^ n0.z, o0.w ^ n0.w);
-        const uint4 x1 = make_uint4(o1.x ^ n1.x, o1.y ^ n1.y, o1.z ^ n1.z, o1.w ^ n1.w);
-        uint32_t m0, r0, m1, r1;
-        classify8(x0, m0, r0);
-        classify8(x1, m1, r1);
-        emit_batch(eloc, m0 | (m1 << 8), r0 | (r1 << 8),
+        const uint4 x0 = xor4(load8(old, e, n), load8(neu, e, n));
+        const uint4 x1 = xor4(load8(old, e + 8, n), load8(neu, e + 8, n));
+        const uint32_t rare = rare_mask16(x0, x1);
+        emit_batch(eloc, nz_mask16(x0, x1) & ~rare, rare,
                    [x0, x1](int b) { return elem_of(b < 8 ? x0 : x1, b & 7); }, st, cx);
+        __syncwarp();
+        const uint32_t known = min(st.rankM, M);  // values with rank < known are in the window
+        if (known > cx.wbase) {
+          // byte b is complete when floor(8b/7) + 1 <= Mex + known - 1
+          const uint64_t b_full = (7 * (Mex + known - 1) + 7) >> 3;
+          const uint64_t b_end = min(b_full, b_hi);
+          if (b_end > b_next) {
+            put_mant_bytes(mout, b_next, b_end, Mex, M, 0, cx);
+            b_next = b_end;
+          }
+          __syncwarp();
+          if (lane == 0) sm->mv[0] = sm->mv[known - 1 - cx.wbase];
+          __syncwarp();
+          cx.wbase = known - 1;
+        }
       }
+    }
+    __syncwarp();
+    if (b_hi > b_next) {
+      // the last owned byte may reach into the next chunk of this tensor with mantissa values
+      uint32_t after = 0;
+      const uint64_t jg_last = (8 * (b_hi - 1)) / 7;
+      if (jg_last + 1 == Mex + M && Mex + M < I.sum_m) {
+        const uint64_t g_end = chunk_start[j + 1];
+        for (uint64_t gg = g + 1; gg < g_end; gg += 32) {
+          const uint64_t q = gg + lane;
+          const bool has = q < g_end && (counts[q] & 0xFFFFu) != 0;
+          const uint32_t bal = __ballot_sync(0xFFFFFFFFu, has);
+          if (bal) {
+            const uint64_t gn = gg + __ffs(bal) - 1;
+            after = reinterpret_cast<const uint32_t*>(slots + gn * kSlotBytes)[1] & kMant;
+            break;
+          }
+        }
+      }
+      put_mant_bytes(mout, b_next, b_hi, Mex, M, after, cx);
     }
     if (!cx.listM || !cx.listR) {
       __syncwarp();
-      if (!cx.listM) store_bitmap(cx.mblk, bm, B);
-      if (!cx.listR) store_bitmap(cx.rblk, bm + 128, B);
-      __syncwarp();
+      if (!cx.listM) store_bitmap(cx.mblk, sm->bm, B);
+      if (!cx.listR) store_bitmap(cx.rblk, sm->bm + 128, B);
     }
-  }
-}
-
-// ------------------------------------------------------------------------ pack_mant
-__global__ void __launch_bounds__(kThreads)
-k_pack_mant(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
-            const uint64_t* __restrict__ tile_start, uint32_t k, uint64_t total_chunks,
-            const uint32_t* __restrict__ counts, const uint4* __restrict__ loc,
-            const TileSum* __restrict__ tile_pre, const JobInfo* __restrict__ info,
-            const uint8_t* __restrict__ mbytes) {
-  const int lane = threadIdx.x & 31;
-  const uint64_t gwarp = ((uint64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
-  const uint64_t nwarps = ((uint64_t)gridDim.x * kThreads) >> 5;
-  for (uint64_t g = gwarp; g < total_chunks; g += nwarps) {
-    const uint32_t M = counts[g] & 0xFFFFu;
-    if (M == 0) continue;
-    const uint32_t j = find_job(chunk_start, k, g);
-    if (info[j].status != BD_OK) continue;
-    const uint64_t c = g - chunk_start[j];
-    const TileSum pre = tile_pre[tile_start[j] + c / kTileChunks];
-    const uint64_t Mex = pre.m + loc[g].y;
-    const uint64_t sum_m = info[j].sum_m;
-    const uint8_t* __restrict__ mb = mbytes + jobs[j].m_base;
-    uint8_t* out = jobs[j].payload + info[j].m_start;
-    // this chunk owns the bytes whose first bit lies in one of its elements
-    const uint64_t b0 = (7 * Mex + 7) >> 3;
-    const uint64_t b1 = (7 * (Mex + M) + 7) >> 3;
-    for (uint64_t b = b0 + lane; b < b1; b += 32) {
-      const uint64_t jj = (8 * b) / 7;
-      const uint32_t s = (uint32_t)(8 * b - 7 * jj);
-      const uint32_t v0 = mb[jj];
-      const uint32_t v1 = (jj + 1 < sum_m) ? mb[jj + 1] : 0u;
-      out[b] = (uint8_t)((v0 >> s) | (v1 << (7 - s)));
-    }
+    __syncwarp();
   }
 }
 
@@ -361,22 +442,7 @@ cudaError_t launch_emit(const LaunchCtx& c) {
       reinterpret_cast<const uint32_t*>(c.ws + c.lay.counts), c.ws + c.lay.slots,
       reinterpret_cast<const uint4*>(c.ws + c.lay.loc),
       reinterpret_cast<const TileSum*>(c.ws + c.lay.tile_pre),
-      reinterpret_cast<const JobInfo*>(c.ws + c.lay.info), c.ws + c.lay.mbytes);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_pack_mant(const LaunchCtx& c) {
-  if (c.chunks == 0) return cudaSuccess;
-  static const int per_sm = blocks_per_sm(k_pack_mant, kThreads);
-  const uint64_t grid = cap_grid((uint64_t)per_sm * c.sms, kWarps, c.chunks);
-  k_pack_mant<<<(unsigned)grid, kThreads, 0, c.stream>>>(
-      reinterpret_cast<const CJob*>(c.ws + c.lay.jobs),
-      reinterpret_cast<const uint64_t*>(c.ws + c.lay.chunk_start),
-      reinterpret_cast<const uint64_t*>(c.ws + c.lay.tile_start), c.k, c.chunks,
-      reinterpret_cast<const uint32_t*>(c.ws + c.lay.counts),
-      reinterpret_cast<const uint4*>(c.ws + c.lay.loc),
-      reinterpret_cast<const TileSum*>(c.ws + c.lay.tile_pre),
-      reinterpret_cast<const JobInfo*>(c.ws + c.lay.info), c.ws + c.lay.mbytes);
+      reinterpret_cast<const JobInfo*>(c.ws + c.lay.info));
   return cudaGetLastError();
 }
 

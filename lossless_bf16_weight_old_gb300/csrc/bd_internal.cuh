@@ -113,8 +113,7 @@ struct CJob {
   uint64_t chunk_base;  // global index of this tensor's chunk 0
   uint64_t nchunks;     // C = ceil(n / 4096)
   uint64_t tile_base;   // global index of this tensor's first scan tile
-  uint64_t m_base;      // byte offset of this tensor's M-byte staging area
-  uint64_t pad[4];
+  uint64_t pad[5];
 };
 static_assert(sizeof(CJob) == 128, "CJob layout");
 
@@ -156,11 +155,36 @@ struct TileSum {   // totals of one scan tile (or their exclusive prefix)
   uint64_t p, m, r, pad;
 };
 
-// Per-chunk slot written by the encode pass: u32 header (entry count, bit 31 = overflow)
-// followed by up to kSlotEntries entries (pos << 16 | x) in ascending position.
+// Per-chunk slot (workspace), written by the encode pass (compress) or the decode pass
+// (decompress); entries are in ascending position:
+//   u32 info     bits 0..15 entry count, bit 30 malformed chunk, bit 31 overflow (the chunk
+//                has more changed elements than kSlotEntries)
+//   u32 aux      compress: first mantissa-only XOR value of the chunk (bits 0..6), bit 7 set
+//                when the chunk has one
+//   u8 step_end[8]  decompress: entries with position < 512 (s + 1), s = 0..7
+//   u32 entry[kSlotEntries]  pos << 16 | x
 constexpr uint32_t kSlotBytes = 1024;
-constexpr uint32_t kSlotEntries = kSlotBytes / 4 - 1;
+constexpr uint32_t kSlotHeader = 16;
+constexpr uint32_t kSlotEntries = (kSlotBytes - kSlotHeader) / 4;
 constexpr uint32_t kSlotOverflow = 0x80000000u;
+constexpr uint32_t kSlotBad = 0x40000000u;
+constexpr uint32_t kAuxHasM = 0x80u;
+
+// Branch-free field flags of the two BF16 values in a 32-bit word: bit 15 (low value) and
+// bit 31 (high value) are set when the value is nonzero (nz) / has a sign or exponent bit set
+// (rare).  The add carries a nonzero masked field into bit 15 without crossing into bit 16.
+__device__ __forceinline__ uint32_t nz_flags(uint32_t w) {
+  return (((w & 0x7FFF7FFFu) + 0x7FFF7FFFu) | w) & 0x80008000u;
+}
+__device__ __forceinline__ uint32_t rare_flags(uint32_t w) {
+  return (((w & 0x7F807F80u) + 0x7F807F80u) | w) & 0x80008000u;
+}
+// 8-bit element-order mask (bit e <-> element e) from the flags of the 4 words of a group.
+__device__ __forceinline__ uint32_t flags_to_mask8(uint32_t f0, uint32_t f1, uint32_t f2,
+                                                   uint32_t f3) {
+  const uint32_t t = (f0 >> 15) | (f1 >> 13) | (f2 >> 11) | (f3 >> 9);  // even at 0,2,4,6; odd at 16..22
+  return (t | (t >> 15)) & 0xFFu;
+}
 
 // Workspace layout of one call (byte offsets from the workspace base, 256-aligned).
 struct WsLayout {
@@ -172,11 +196,12 @@ struct WsLayout {
   uint64_t chunk_start;  // (k+1) u64: global chunk index where job j starts
   uint64_t tile_start;   // (k+1) u64
   uint64_t counts;       // Ctot u32 (compress only)
-  uint64_t slots;        // Ctot * kSlotBytes (compress only)
+  uint64_t slots;        // Ctot * kSlotBytes
   uint64_t loc;          // Ctot uint4: chunk exclusive prefix inside its tile (p, m, r)
   uint64_t tile_tot;     // Utot TileSum
   uint64_t tile_pre;     // Utot TileSum
-  uint64_t mbytes;       // sum over jobs of round_up(n, 16) (compress only)
+  uint64_t overflow;     // decompress: u32 count (in the zeroed state) ...
+  uint64_t ovf_list;     // ... and Ctot u32 chunk indices handled by the block-level apply
   uint64_t total;
 };
 
@@ -189,6 +214,15 @@ __device__ __forceinline__ uint32_t find_job(const uint64_t* __restrict__ starts
     if (__ldg(starts + mid) <= g) lo = mid; else hi = mid;
   }
   return lo;
+}
+
+// Job of global index g when the previous index of this thread was in job j (g only grows).
+__device__ __forceinline__ uint32_t advance_job(const uint64_t* __restrict__ starts, uint32_t k,
+                                                uint32_t j, uint64_t g) {
+  if (j >= k) return find_job(starts, k, g);
+  if (__ldg(starts + j + 1) > g) return j;
+  if (j + 2 <= k && __ldg(starts + j + 2) > g) return j + 1;
+  return find_job(starts, k, g);
 }
 
 // Warp-level inclusive scan (sum) of a 32-bit value.
@@ -241,7 +275,8 @@ cudaError_t launch_encode_slots(const LaunchCtx& c);
 cudaError_t launch_scan_tiles(const LaunchCtx& c, bool decompress);
 cudaError_t launch_scan_jobs(const LaunchCtx& c, bool decompress, int32_t* d_status_all);
 cudaError_t launch_emit(const LaunchCtx& c);
-cudaError_t launch_pack_mant(const LaunchCtx& c);
+cudaError_t launch_decode(const LaunchCtx& c);
+cudaError_t launch_apply_stream(const LaunchCtx& c);
 cudaError_t launch_apply(const LaunchCtx& c);
 cudaError_t launch_apply_finish(const LaunchCtx& c, int32_t* d_status_all);
 cudaError_t launch_checksum(const uint16_t* w, uint64_t n, uint64_t* out, cudaStream_t s,
