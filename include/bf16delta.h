@@ -144,6 +144,36 @@ BD_API int bd_decompress(const uint16_t* d_old, uint64_t n, const void* d_payloa
 BD_API int bd_decompress_batch(const bd_decompress_item* h_items, uint32_t k, void* d_ws,
                         uint64_t ws_bytes, int32_t* d_status, void* stream);
 
+/* Largest tensor bd_decompress_noalloc accepts, in elements (2^27 = 128 Mi elements,
+ * 256 MiB of BF16), and the size of the device array it uses as scratch. */
+#define BD_NOALLOC_MAX_ELEMS (1ull << 27)
+#define BD_NOALLOC_SCRATCH_BYTES (1ull << 20)
+
+/* bd_decompress for callers that cannot allocate device memory.  The pages have no
+ * counterpart of this call; it exists for users of this library, not for the method.
+ *
+ * Who needs it: a rollout or inference engine whose allocator already holds almost all of
+ * HBM (weights plus a pre-reserved KV cache) cannot hand out a workspace, and calling
+ * cudaMalloc / cudaFree from such a process either fails, fragments the engine's pool or
+ * stalls the device at the wrong moment.  This entry point needs no workspace argument: its
+ * scratch is a fixed BD_NOALLOC_SCRATCH_BYTES array in the library's device memory, which
+ * every GPU that loads the library holds until the process exits.
+ *
+ * Arguments, result and status are those of bd_decompress.  Differences:
+ *   - n above BD_NOALLOC_MAX_ELEMS is rejected with BD_ERR_INVALID_ARG before anything is
+ *     enqueued;
+ *   - it decodes every chunk with the block-level decoder, so it is slower than
+ *     bd_decompress with a workspace;
+ *   - all calls share the one scratch array (it keeps the last call's contents; each call
+ *     clears what must start at zero), so two calls that may overlap on the GPU race:
+ *     issue them on one stream, or order them with events;
+ *   - the first call on a device looks up the array's device address (once per device, with
+ *     that device current); make that first call before any stream capture begins.
+ * It allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine. */
+BD_API int bd_decompress_noalloc(const uint16_t* d_old, uint64_t n, const void* d_payload,
+                                 uint64_t size, const uint64_t* d_expected, uint16_t* d_out,
+                                 int32_t* d_status, void* stream);
+
 /* The checksum above of n BF16 values, written to *d_out.  Needs no workspace. */
 BD_API int bd_checksum(const uint16_t* d_w, uint64_t n, uint64_t* d_out, void* stream);
 

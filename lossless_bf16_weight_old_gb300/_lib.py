@@ -37,6 +37,7 @@ SIGNATURES = {
     "bd_compress_batch": (c_int, [c_p, c_u32, c_p, c_u64, c_p, c_p]),
     "bd_decompress": (c_int, [c_p, c_u64, c_p, c_u64, c_p, c_p, c_p, c_u64, c_p, c_p]),
     "bd_decompress_batch": (c_int, [c_p, c_u32, c_p, c_u64, c_p, c_p]),
+    "bd_decompress_noalloc": (c_int, [c_p, c_u64, c_p, c_u64, c_p, c_p, c_p, c_p]),
     "bd_checksum": (c_int, [c_p, c_u64, c_p, c_p]),
     "bd_payload_info": (c_int, [c_p, c_u64, ctypes.POINTER(PayloadInfo)]),
     "bd_status_sync": (c_int, [c_p, c_p]),

@@ -16,7 +16,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libbf16delta.so")
 
-SOURCES = ["bd_api.cu", "bd_encode.cu", "bd_scan.cu", "bd_apply.cu", "bd_checksum.cu"]
+SOURCES = ["bd_api.cu", "bd_encode.cu", "bd_scan.cu", "bd_apply.cu", "bd_checksum.cu",
+           "bd_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
          f"-I{INCLUDE}"]
