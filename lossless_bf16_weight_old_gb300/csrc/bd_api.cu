@@ -58,11 +58,10 @@ WsLayout make_layout(uint32_t k, const Sizes& s, bool compress) {
   off = up(off + s.tiles * sizeof(TileSum), kAlign);
   L.slots = off;
   off = up(off + s.chunks * kSlotBytes, kAlign);
+  L.ovf_list = off;  // chunks too dense for a slot
+  off = up(off + s.chunks * 4, kAlign);
   if (compress) {
     L.counts = off;
-    off = up(off + s.chunks * 4, kAlign);
-  } else {
-    L.ovf_list = off;
     off = up(off + s.chunks * 4, kAlign);
   }
   L.total = off;
@@ -181,7 +180,8 @@ int compress_impl(const bd_compress_item* items, uint32_t k, void* ws, uint64_t 
   if ((rc = check(launch_encode_slots(c)))) return rc;
   if ((rc = check(launch_scan_tiles(c, false)))) return rc;
   if ((rc = check(launch_scan_jobs(c, false, status_all)))) return rc;
-  return check(launch_emit(c));
+  if ((rc = check(launch_emit(c)))) return rc;
+  return check(launch_emit_dense(c));
 }
 
 // ------------------------------------------------------------------------------ decompress

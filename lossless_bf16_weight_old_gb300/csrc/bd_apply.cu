@@ -6,15 +6,19 @@
 // result is checksummed against the trainer's original.
 //
 // After the count scan (bd_scan.cu):
-//   decode        one warp per chunk: decodes the chunk's position blocks (delta list -> prefix
-//                 sum, or bitmap -> popcount rank) and gathers its 7-bit and 16-bit XOR values
-//                 into a position-sorted entry list in the chunk's workspace slot, checking
-//                 every rule of the format.  Chunks with more changes than a slot holds are
-//                 listed for apply_dense.
-//   apply_stream  one warp per chunk, the streaming pass over old: per 512-element step it
-//                 scatters the step's entries into a 1 KiB shared mask, XORs, checksums the
-//                 result and writes back only the 16-byte groups that changed (in place) or
-//                 every group (out of place).
+//   decode        one warp per chunk: requests the chunk's position blocks and values in one
+//                 round, decodes the positions (delta list -> prefix sum, or bitmap ->
+//                 popcount rank) and writes (position, XOR) entries into the chunk's workspace
+//                 slot, mantissa-only from the front and rare from the back, checking the
+//                 format rules.  Chunks with more changes than a slot holds are listed for
+//                 apply_dense.
+//   apply_stream  two warps per chunk, the streaming pass over old: the chunk's 8 KiB of old are
+//                 copied into shared memory with cp.async while the previous chunk is processed
+//                 (double buffer) and its slot is prefetched into registers; the entries are
+//                 XORed into the staged data with shared-memory atomics (a position taken
+//                 twice is malformed), then each warp checksums half of the result, two steps
+//                 at a time, and writes back only the 16-byte groups that changed (in place)
+//                 or every group (out of place).
 //   apply_dense   one CTA per listed chunk: decodes straight from the payload into an 8 KiB
 //                 shared mask (dense chunks, bitmap positions).
 //   apply_finish  one thread per tensor: checks the mantissa-stream pad bits, compares the
@@ -253,24 +257,52 @@ k_apply_dense(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_
 
 // ------------------------------------------------------------------------ decode
 
-struct DecodeSmem {
-  uint16_t posM[256], valM[256], posR[256], valR[256];
-};
-
-// Number of values < x in the ascending array a[0..k).
-__device__ __forceinline__ uint32_t lower_bound16(const uint16_t* a, uint32_t k, uint32_t x) {
-  uint32_t lo = 0, hi = k;
-  while (lo < hi) {
-    const uint32_t mid = (lo + hi) >> 1;
-    if (a[mid] < x) lo = mid + 1; else hi = mid;
-  }
-  return lo;
+// 16-byte asynchronous global -> shared copy; src_bytes < 16 zero-fills the rest.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, uint32_t src_bytes) {
+  const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
-// Decodes the k ascending positions of one class (block at blk, chunk of length L whose
-// bitmap has B bytes) into pos[0..k).  Returns true when the block is malformed.
-__device__ __forceinline__ bool decode_positions(const uint8_t* __restrict__ blk, uint32_t k,
-                                                 uint32_t L, uint32_t B, uint16_t* pos) {
+// 4-byte asynchronous global -> shared copy; src_bytes < 4 zero-fills the rest.
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem, uint32_t src_bytes) {
+  const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(s), "l"(gmem),
+               "r"(src_bytes)
+               : "memory");
+}
+
+
+// Staging capacity per warp, in 32-bit words, of the three payload byte ranges of one chunk
+// whose changes fit a slot (M + R <= kSlotEntries): position blocks (delta lists up to 504
+// bytes, or bitmaps of a ragged last chunk up to 2 x 511 bytes), mantissa bytes (up to 221)
+// and rare values (up to 504 bytes), each widened to whole aligned words.
+constexpr int kStageP = 9, kStageM = 2, kStageR = 4;   // words per lane
+struct DecodeSmem {
+  uint32_t wp[32 * kStageP], wm[32 * kStageM], wr[32 * kStageR];
+};
+
+__device__ __forceinline__ uint32_t sbyte(const uint32_t* w, uint32_t i) {
+  return (w[i >> 2] >> (8 * (i & 3))) & 0xFFu;
+}
+__device__ __forceinline__ uint32_t su16(const uint32_t* w, uint32_t i) {
+  return sbyte(w, i) | (sbyte(w, i + 1) << 8);
+}
+
+// Decodes the k ascending positions of one class from the staged block (byte offset `boff`
+// in the word buffer w; chunk of length L whose bitmap has B bytes) and hands each one to
+// sink(rank, position).  Returns true when the block is malformed.
+template <typename SINK>
+__device__ __forceinline__ bool decode_positions(const uint32_t* w, uint32_t boff, uint32_t k,
+                                                 uint32_t L, uint32_t B, SINK sink) {
   const int lane = threadIdx.x & 31;
   bool bad = false;
   if (2 * k < B) {  // delta list: d_0 = p_0, d_i = p_i - p_{i-1} >= 1
@@ -279,22 +311,23 @@ __device__ __forceinline__ bool decode_positions(const uint8_t* __restrict__ blk
       const uint32_t i = base + lane;
       uint32_t d = 0;
       if (i < k) {
-        d = load_u16(blk + 2 * i);
+        d = su16(w, boff + 2 * i);
         if (i > 0 && d == 0) bad = true;
       }
       const uint32_t p = carry + warp_incl_scan(d);
       if (i < k) {
         if (p >= L) bad = true;
-        pos[i] = (uint16_t)(p < L ? p : 0);
+        else sink(i, p);
       }
       carry = __shfl_sync(0xFFFFFFFFu, p, 31);
     }
   } else {  // bitmap: lane handles bytes [16 lane, 16 lane + 16)
     uint32_t bytes[4] = {0, 0, 0, 0};
     uint32_t cnt = 0;
+#pragma unroll
     for (int q = 0; q < 16; q++) {
       const uint32_t bi = 16 * lane + q;
-      const uint32_t v = bi < B ? blk[bi] : 0u;
+      const uint32_t v = bi < B ? sbyte(w, boff + bi) : 0u;
       bytes[q >> 2] |= v << (8 * (q & 3));
       cnt += __popc(v);
     }
@@ -303,13 +336,36 @@ __device__ __forceinline__ bool decode_positions(const uint8_t* __restrict__ blk
     uint32_t r = incl - cnt;
     for (int q = 0; q < 4; q++) {
       for (uint32_t bits = bytes[q]; bits; bits &= bits - 1) {
-        const uint32_t p = 16 * 8 * lane + 32 * q + __ffs(bits) - 1;
+        const uint32_t p = 128 * lane + 32 * q + __ffs(bits) - 1;
         if (p >= L || r >= k) { bad = true; break; }
-        pos[r++] = (uint16_t)p;
+        sink(r++, p);
       }
     }
   }
   return bad;
+}
+
+// One chunk's payload pieces, as aligned word ranges.
+struct WordRange {
+  uint64_t first;   // byte offset (multiple of 4) of the first word
+  uint32_t words;   // words to stage
+  uint32_t skip;    // offset of the range's first byte inside the first word
+};
+__device__ __forceinline__ WordRange word_range(uint64_t a, uint64_t b) {
+  WordRange r;
+  r.first = a & ~3ull;
+  r.skip = (uint32_t)(a - r.first);
+  r.words = b > a ? (uint32_t)((((b + 3) & ~3ull) - r.first) >> 2) : 0u;
+  return r;
+}
+
+// Starts the asynchronous copy of word w of range r (payload of `size` bytes) to dst.
+__device__ __forceinline__ void stage_word(uint32_t* dst, const uint8_t* __restrict__ payload,
+                                           const WordRange& r, uint32_t w, uint64_t size) {
+  if (w >= r.words) return;
+  const uint64_t off = r.first + 4ull * w;
+  const uint32_t bytes = off + 4 <= size ? 4u : (off < size ? (uint32_t)(size - off) : 0u);
+  cp_async4(dst, bytes ? payload + off : payload, bytes);
 }
 
 __global__ void __launch_bounds__(kThreads)
@@ -326,15 +382,20 @@ k_decode(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start
   uint32_t j = 0xFFFFFFFFu;
   for (uint64_t g = gwarp; g < total_chunks; g += nwarps) {
     j = advance_job(chunk_start, k, j, g);
-    const uint4 lc = loc[g];
-    if (info[j].status != BD_OK) continue;
+    // level 1: everything addressed by g and j alone
     const DJob& J = jobs[j];
+    const JobInfo& I = info[j];
     const uint64_t c = g - chunk_start[j];
-    const uint64_t e0 = c * kChunk;
-    const uint32_t L = (J.n - e0) < kChunk ? (uint32_t)(J.n - e0) : kChunk;
-    const uint32_t B = (L + 7) >> 3;
+    const uint4 lc = loc[g];
+    const TileSum pre = tile_pre[tile_start[j] + c / kTileChunks];
+    const int32_t status = I.status;
     const uint8_t* __restrict__ payload = J.payload;
+    if (status != BD_OK) continue;
     const uint32_t cnt = reinterpret_cast<const uint32_t*>(payload + kHeader)[c];
+    const uint64_t n = J.n, size = J.size;
+    const uint64_t e0 = c * kChunk;
+    const uint32_t L = (n - e0) < kChunk ? (uint32_t)(n - e0) : kChunk;
+    const uint32_t B = (L + 7) >> 3;
     const uint32_t M = cnt & 0xFFFFu, R = cnt >> 16;
     uint32_t* slot = reinterpret_cast<uint32_t*>(slots + g * kSlotBytes);
     if (M + R > kSlotEntries) {
@@ -344,56 +405,47 @@ k_decode(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start
       }
       continue;
     }
-    const TileSum pre = tile_pre[tile_start[j] + c / kTileChunks];
     const uint64_t Pex = pre.p + lc.x, Mex = pre.m + lc.y, Rex = pre.r + lc.z;
-    const JobInfo& I = info[j];
-    const uint8_t* mblk = payload + I.p_start + Pex;
-    const uint8_t* rblk = mblk + block_bytes(M, B);
-    const uint8_t* mstream = payload + I.m_start;
-    const uint8_t* rstream = payload + I.r_start + 2 * Rex;
-
-    bool bad = decode_positions(mblk, M, L, B, sm->posM);
-    bad |= decode_positions(rblk, R, L, B, sm->posR);
-    for (uint32_t r = lane; r < M; r += 32) {
-      const uint32_t v = mant_value(mstream, Mex + r);
-      if (v == 0) bad = true;
-      sm->valM[r] = (uint16_t)v;
-    }
-    for (uint32_t r = lane; r < R; r += 32) {
-      const uint32_t v = load_u16(rstream + 2 * r);
-      if ((v & kSignExp) == 0) bad = true;
-      sm->valR[r] = (uint16_t)v;
-    }
-    __syncwarp();
-    // merge the two ascending lists into position order; a shared position is malformed
-    uint32_t* entries = slot + kSlotHeader / 4;
-    for (uint32_t r = lane; r < M; r += 32) {
-      const uint32_t p = sm->posM[r];
-      const uint32_t less = lower_bound16(sm->posR, R, p);
-      if (less < R && sm->posR[less] == p) bad = true;
-      entries[r + less] = (p << 16) | sm->valM[r];
-    }
-    for (uint32_t r = lane; r < R; r += 32) {
-      const uint32_t p = sm->posR[r];
-      entries[r + lower_bound16(sm->posM, M, p)] = (p << 16) | sm->valR[r];
-    }
-    // step_end[s]: entries with position < 512 (s + 1)
-    uint32_t se = 0;
-    if (lane < 8) {
-      const uint32_t bound = 512u * (lane + 1);
-      se = lower_bound16(sm->posM, M, bound) + lower_bound16(sm->posR, R, bound);
-    }
-    uint32_t w0 = 0, w1 = 0;
+    const uint32_t blkM = block_bytes(M, B), blkR = block_bytes(R, B);
+    // level 2: the chunk's three payload ranges, all words requested before any is used
+    const uint64_t pa = I.p_start + Pex;
+    const WordRange wp = word_range(pa, pa + blkM + blkR);
+    const uint64_t ma = I.m_start + ((7 * Mex) >> 3);
+    const WordRange wm = word_range(ma, I.m_start + ((7 * (Mex + M) + 7) >> 3));
+    const uint64_t ra = I.r_start + 2 * Rex;
+    const WordRange wr = word_range(ra, ra + 2 * R);
 #pragma unroll
-    for (int q = 0; q < 4; q++) {
-      w0 |= __shfl_sync(0xFFFFFFFFu, se, q) << (8 * q);
-      w1 |= __shfl_sync(0xFFFFFFFFu, se, q + 4) << (8 * q);
-    }
+    for (int q = 0; q < kStageP; q++) stage_word(&sm->wp[lane + 32 * q], payload, wp, lane + 32 * q, size);
+#pragma unroll
+    for (int q = 0; q < kStageM; q++) stage_word(&sm->wm[lane + 32 * q], payload, wm, lane + 32 * q, size);
+#pragma unroll
+    for (int q = 0; q < kStageR; q++) stage_word(&sm->wr[lane + 32 * q], payload, wr, lane + 32 * q, size);
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncwarp();
+
+    // entries: mantissa-only at [0, M), rare at [M, M+R) (collisions are checked when the
+    // chunk is applied)
+    uint32_t* entries = slot + kSlotHeader / 4;
+    bool bad = false;
+    const uint32_t mbit0 = 8 * wm.skip + (uint32_t)((7 * Mex) & 7);
+    const uint32_t* wmv = sm->wm;
+    bad |= decode_positions(sm->wp, wp.skip, M, L, B, [&](uint32_t r, uint32_t p) {
+      const uint32_t bit = mbit0 + 7 * r;
+      const uint32_t v = (su16(wmv, bit >> 3) >> (bit & 7)) & kMant;
+      if (v == 0) bad = true;
+      entries[r] = (p << 16) | v;
+    });
+    const uint32_t* wrv = sm->wr;
+    const uint32_t rskip = wr.skip;
+    bad |= decode_positions(sm->wp, wp.skip + blkM, R, L, B, [&](uint32_t r, uint32_t p) {
+      const uint32_t v = su16(wrv, rskip + 2 * r);
+      if ((v & kSignExp) == 0) bad = true;
+      entries[M + r] = (p << 16) | v;
+    });
     bad = __any_sync(0xFFFFFFFFu, bad);
     if (lane == 0) {
-      slot[0] = (M + R) | (bad ? kSlotBad : 0u);
-      slot[2] = w0;
-      slot[3] = w1;
+      slot[0] = slot_info(M, R) | (bad ? kSlotBad : 0u);
       if (bad) record_status(&info[j].chunk_err, BD_ERR_FORMAT);
     }
     __syncwarp();
@@ -402,101 +454,140 @@ k_decode(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start
 
 // ------------------------------------------------------------------------ apply_stream
 
-struct StreamSmem {
-  uint32_t ent[kSlotEntries + 4];
-  uint4 mask4[64];   // 512 u16: the XOR mask of one step
+constexpr int kStreamThreads = 256;  // 4 pairs of warps, one chunk per pair
+constexpr int kStreamPairs = kStreamThreads / 64;
+struct PairSmem {
+  uint4 buf[2][kChunk / 8];       // two 8 KiB chunk buffers (double-buffered old data)
+  uint32_t touched[kChunk / 32];  // 512 B: positions written in the current chunk
+  uint32_t flag;                  // a position was taken twice
+  uint32_t pad[3];
 };
 
-template <bool FULL>
-__device__ __forceinline__ void stream_chunk(const uint16_t* __restrict__ old,
-                                             uint16_t* __restrict__ out, bool inplace,
-                                             uint64_t n, uint64_t e0, uint32_t w0, uint32_t w1,
-                                             StreamSmem* sm, uint64_t& ck) {
-  const int lane = threadIdx.x & 31;
-  const uint64_t words = (n + 3) >> 2;
-  uint16_t* mask = reinterpret_cast<uint16_t*>(sm->mask4);
-  uint64_t e = e0 + lane * 16;
-  uint4 o0, o1;
-  if (FULL) {
-    o0 = __ldg(reinterpret_cast<const uint4*>(old + e));
-    o1 = __ldg(reinterpret_cast<const uint4*>(old + e + 8));
-  } else {
-    o0 = load8(old, e, n);
-    o1 = load8(old, e + 8, n);
-  }
-  uint64_t key = ((e >> 2) + 1) * kGamma;
-  uint32_t lo = 0;
-#pragma unroll 1
-  for (int s = 0; s < 8; s++) {
-    const uint4 c0 = o0, c1 = o1;
-    if (s < 7) {
-      if (FULL) {
-        o0 = __ldg(reinterpret_cast<const uint4*>(old + e + 512));
-        o1 = __ldg(reinterpret_cast<const uint4*>(old + e + 520));
-      } else {
-        o0 = load8(old, e + 512, n);
-        o1 = load8(old, e + 520, n);
-      }
-    }
-    const uint32_t hi = ((s < 4 ? w0 : w1) >> (8 * (s & 3))) & 0xFFu;
-    uint4 m0 = make_uint4(0, 0, 0, 0), m1 = m0;
-    if (__any_sync(0xFFFFFFFFu, hi > lo)) {
-      sm->mask4[2 * lane] = m0;
-      sm->mask4[2 * lane + 1] = m1;
-      __syncwarp();
-      for (uint32_t i = lo + lane; i < hi; i += 32) {
-        const uint32_t en = sm->ent[i];
-        mask[(en >> 16) & 511] = (uint16_t)(en & 0xFFFFu);
-      }
-      __syncwarp();
-      m0 = sm->mask4[2 * lane];
-      m1 = sm->mask4[2 * lane + 1];
-      __syncwarp();
-    }
-    lo = hi;
-    const uint4 r0 = make_uint4(c0.x ^ m0.x, c0.y ^ m0.y, c0.z ^ m0.z, c0.w ^ m0.w);
-    const uint4 r1 = make_uint4(c1.x ^ m1.x, c1.y ^ m1.y, c1.z ^ m1.z, c1.w ^ m1.w);
-    const bool ch0 = (m0.x | m0.y | m0.z | m0.w) != 0, ch1 = (m1.x | m1.y | m1.z | m1.w) != 0;
-    if (FULL) {
-      const uint64_t a0 = (uint64_t)r0.x | ((uint64_t)r0.y << 32);
-      const uint64_t a1 = (uint64_t)r0.z | ((uint64_t)r0.w << 32);
-      const uint64_t a2 = (uint64_t)r1.x | ((uint64_t)r1.y << 32);
-      const uint64_t a3 = (uint64_t)r1.z | ((uint64_t)r1.w << 32);
-      ck += mix64(a0 ^ key) + mix64(a1 ^ (key + kGamma)) + mix64(a2 ^ (key + 2 * kGamma)) +
-            mix64(a3 ^ (key + 3 * kGamma));
-      if (!inplace || ch0) *reinterpret_cast<uint4*>(out + e) = r0;
-      if (!inplace || ch1) *reinterpret_cast<uint4*>(out + e + 8) = r1;
-    } else {
-      ck += group_hash(r0, e >> 3, words) + group_hash(r1, (e >> 3) + 1, words);
-      if (e < n && (!inplace || ch0)) {
-        if (e + 8 <= n) *reinterpret_cast<uint4*>(out + e) = r0;
-        else for (int i = 0; e + i < n; i++) out[e + i] = (uint16_t)elem_of(r0, i);
-      }
-      if (e + 8 < n && (!inplace || ch1)) {
-        if (e + 16 <= n) *reinterpret_cast<uint4*>(out + e + 8) = r1;
-        else for (int i = 0; e + 8 + i < n; i++) out[e + 8 + i] = (uint16_t)elem_of(r1, i);
-      }
-    }
-    e += 512;
-    key += 128 * kGamma;
+// Barrier over the 64 threads of one warp pair (ids 1..4; 0 is __syncthreads).
+__device__ __forceinline__ void pair_sync(int pair) {
+  asm volatile("bar.sync %0, 64;\n" ::"r"(pair + 1) : "memory");
+}
+
+// Starts copying chunk [e0, e0 + 4096) of old into buf: pair thread pt copies groups
+// 64 t + pt (group q = elements e0 + 8q .. +8), elements past n read as zero.
+__device__ __forceinline__ void issue_chunk(uint4* buf, const uint16_t* __restrict__ old,
+                                            uint64_t n, uint64_t e0, uint32_t pt) {
+#pragma unroll
+  for (int t = 0; t < 8; t++) {
+    const uint32_t q = 64 * t + pt;
+    const uint64_t e = e0 + 8 * q;
+    const uint32_t bytes = e + 8 <= n ? 16u : (e < n ? (uint32_t)(2 * (n - e)) : 0u);
+    cp_async16(&buf[q], bytes ? old + e : old, bytes);
   }
 }
 
-__global__ void __launch_bounds__(kThreads)
-k_apply_stream(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
-               uint32_t k, uint64_t total_chunks, const JobInfo* __restrict__ info,
-               const uint8_t* __restrict__ slots, uint8_t* __restrict__ ck_base) {
-  __shared__ StreamSmem s_st[kWarps];
+// XORs one entry into the staged chunk; returns true when its position was already taken.
+__device__ __forceinline__ bool xor_entry(uint32_t* data32, uint32_t* touched, uint32_t e) {
+  const uint32_t pos = (e >> 16) & (kChunk - 1);
+  atomicXor(&data32[pos >> 1], (e & 0xFFFFu) << (16 * (pos & 1)));
+  return (atomicOr(&touched[pos >> 5], 1u << (pos & 31)) >> (pos & 31)) & 1u;
+}
+
+// Checksums and writes back the two 16-byte groups of this lane in step s (elements
+// e0 + 512 s + 16 lane ..); tmask = the 16 touched bits of those elements.
+template <bool FULL>
+__device__ __forceinline__ void put_groups(uint4 r0, uint4 r1, uint32_t tmask, uint64_t e,
+                                           uint64_t key, uint64_t n, uint64_t words,
+                                           uint16_t* __restrict__ out, bool inplace,
+                                           uint64_t& ck) {
+  if (FULL) {
+    const uint64_t a0 = (uint64_t)r0.x | ((uint64_t)r0.y << 32);
+    const uint64_t a1 = (uint64_t)r0.z | ((uint64_t)r0.w << 32);
+    const uint64_t a2 = (uint64_t)r1.x | ((uint64_t)r1.y << 32);
+    const uint64_t a3 = (uint64_t)r1.z | ((uint64_t)r1.w << 32);
+    ck += mix64(a0 ^ key) + mix64(a1 ^ (key + kGamma)) + mix64(a2 ^ (key + 2 * kGamma)) +
+          mix64(a3 ^ (key + 3 * kGamma));
+    if (!inplace || (tmask & 0xFFu)) *reinterpret_cast<uint4*>(out + e) = r0;
+    if (!inplace || (tmask >> 8)) *reinterpret_cast<uint4*>(out + e + 8) = r1;
+  } else {
+    ck += group_hash(r0, e >> 3, words) + group_hash(r1, (e >> 3) + 1, words);
+    if (e < n && (!inplace || (tmask & 0xFFu))) {
+      if (e + 8 <= n) *reinterpret_cast<uint4*>(out + e) = r0;
+      else for (int i = 0; e + i < n; i++) out[e + i] = (uint16_t)elem_of(r0, i);
+    }
+    if (e + 8 < n && (!inplace || (tmask >> 8))) {
+      if (e + 16 <= n) *reinterpret_cast<uint4*>(out + e + 8) = r1;
+      else for (int i = 0; e + 8 + i < n; i++) out[e + 8 + i] = (uint16_t)elem_of(r1, i);
+    }
+  }
+}
+
+// Steps s0 and s0 + 1 of a staged chunk, interleaved (eight independent hash chains per lane).
+template <bool FULL>
+__device__ __forceinline__ void stream_two_steps(const uint4* buf, const uint32_t* touched,
+                                                 int s0, uint64_t e0, uint64_t n,
+                                                 uint16_t* __restrict__ out, bool inplace,
+                                                 uint64_t& ck) {
   const int lane = threadIdx.x & 31;
-  const uint64_t gwarp = ((uint64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
-  const uint64_t nwarps = ((uint64_t)gridDim.x * kThreads) >> 5;
-  StreamSmem* sm = &s_st[threadIdx.x >> 5];
+  const uint64_t words = (n + 3) >> 2;
+  const uint4 a0 = buf[64 * s0 + 2 * lane], a1 = buf[64 * s0 + 2 * lane + 1];
+  const uint4 b0 = buf[64 * (s0 + 1) + 2 * lane], b1 = buf[64 * (s0 + 1) + 2 * lane + 1];
+  const uint32_t ta = (touched[16 * s0 + (lane >> 1)] >> (16 * (lane & 1))) & 0xFFFFu;
+  const uint32_t tb = (touched[16 * (s0 + 1) + (lane >> 1)] >> (16 * (lane & 1))) & 0xFFFFu;
+  const uint64_t ea = e0 + 512 * s0 + 16 * lane, eb = ea + 512;
+  const uint64_t ka = ((ea >> 2) + 1) * kGamma, kb = ka + 128 * kGamma;
+  uint64_t c0 = 0, c1 = 0;
+  put_groups<FULL>(a0, a1, ta, ea, ka, n, words, out, inplace, c0);
+  put_groups<FULL>(b0, b1, tb, eb, kb, n, words, out, inplace, c1);
+  ck += c0 + c1;
+}
+
+__global__ void __launch_bounds__(kStreamThreads)
+k_apply_stream(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
+               uint32_t k, uint64_t total_chunks, JobInfo* __restrict__ info,
+               const uint8_t* __restrict__ slots, uint8_t* __restrict__ ck_base) {
+  extern __shared__ uint4 s_dyn[];
+  const int lane = threadIdx.x & 31;
+  const int pair = threadIdx.x >> 6, half = (threadIdx.x >> 5) & 1;
+  const uint32_t pt = threadIdx.x & 63;
+  const uint64_t gpair = (uint64_t)blockIdx.x * kStreamPairs + pair;
+  const uint64_t npairs = (uint64_t)gridDim.x * kStreamPairs;
+  const uint64_t gwarp = 2 * gpair + half;
+  PairSmem* sm = reinterpret_cast<PairSmem*>(s_dyn) + pair;
+  sm->touched[2 * pt] = 0;
+  sm->touched[2 * pt + 1] = 0;
+  if (pt == 0) sm->flag = 0;
+
   uint32_t j = 0xFFFFFFFFu, cur = 0xFFFFFFFFu;
   uint64_t ck = 0;
-  for (uint64_t g = gwarp; g < total_chunks; g += nwarps) {
+  int b = 0;
+  // prologue: the first chunk's old data and slot (the pair's 64 threads hold its 64
+  // 16-byte pieces: the header in piece 0, entries 4 p - 4 .. 4 p - 1 in piece p)
+  uint4 pre = make_uint4(0, 0, 0, 0);
+  uint32_t pre_hdr = 0;
+  if (gpair < total_chunks) {
+    const uint32_t j0 = find_job(chunk_start, k, gpair);
+    issue_chunk(sm->buf[0], jobs[j0].old, jobs[j0].n, (gpair - chunk_start[j0]) * kChunk, pt);
+    pre = reinterpret_cast<const uint4*>(slots + gpair * kSlotBytes)[pt];
+    pre_hdr = *reinterpret_cast<const uint32_t*>(slots + gpair * kSlotBytes);
+  }
+  cp_async_commit();
+  for (uint64_t g = gpair; g < total_chunks; g += npairs, b ^= 1) {
     j = advance_job(chunk_start, k, j, g);
-    const uint4 hdr = *reinterpret_cast<const uint4*>(slots + g * kSlotBytes);
-    if (info[j].status != BD_OK || (hdr.x & (kSlotOverflow | kSlotBad))) continue;
+    const uint4 cur_pre = pre;
+    const uint32_t hdr = pre_hdr;
+    // the next chunk's old data goes into the other buffer, its slot into registers
+    const uint64_t gn = g + npairs;
+    if (gn < total_chunks) {
+      const uint32_t jn = advance_job(chunk_start, k, j, gn);
+      issue_chunk(sm->buf[b ^ 1], jobs[jn].old, jobs[jn].n, (gn - chunk_start[jn]) * kChunk, pt);
+      pre = reinterpret_cast<const uint4*>(slots + gn * kSlotBytes)[pt];
+      pre_hdr = *reinterpret_cast<const uint32_t*>(slots + gn * kSlotBytes);
+    }
+    cp_async_commit();
+    const DJob& J = jobs[j];
+    const uint64_t n = J.n;
+    const uint64_t e0 = (g - chunk_start[j]) * kChunk;
+    // this chunk's copies (every group but the one just issued) must land before its buffer
+    // is read, or reused two iterations later when the chunk is skipped
+    cp_async_wait<1>();
+    pair_sync(pair);
+    if (info[j].status != BD_OK || (hdr & (kSlotOverflow | kSlotBad))) continue;
     if (j != cur) {
       if (cur != 0xFFFFFFFFu) {
         const uint64_t s = warp_sum64(ck);
@@ -508,19 +599,37 @@ k_apply_stream(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
       cur = j;
       ck = 0;
     }
-    const uint32_t kk = hdr.x & 0xFFFFu;
-    const uint32_t* ent = reinterpret_cast<const uint32_t*>(slots + g * kSlotBytes + kSlotHeader);
-    for (uint32_t i = lane; i < kk; i += 32) sm->ent[i] = ent[i];
-    __syncwarp();
-    const DJob& J = jobs[j];
-    const uint64_t e0 = (g - chunk_start[j]) * kChunk;
-    const bool inplace = J.out == J.old;
-    if (e0 + kChunk <= J.n)
-      stream_chunk<true>(J.old, J.out, inplace, J.n, e0, hdr.z, hdr.w, sm, ck);
-    else
-      stream_chunk<false>(J.old, J.out, inplace, J.n, e0, hdr.z, hdr.w, sm, ck);
-    __syncwarp();
+    const uint32_t kk = (hdr & 0xFFFu) + ((hdr >> 12) & 0xFFFu);  // M + R entries
+    uint32_t* data32 = reinterpret_cast<uint32_t*>(sm->buf[b]);
+    bool taken = false;
+    if (pt > 0) {
+      const uint32_t i0 = 4 * pt - 4;  // entries held in this thread's piece of the slot
+      if (i0 + 0 < kk) taken |= xor_entry(data32, sm->touched, cur_pre.x);
+      if (i0 + 1 < kk) taken |= xor_entry(data32, sm->touched, cur_pre.y);
+      if (i0 + 2 < kk) taken |= xor_entry(data32, sm->touched, cur_pre.z);
+      if (i0 + 3 < kk) taken |= xor_entry(data32, sm->touched, cur_pre.w);
+    }
+    if (taken) sm->flag = 1;
+    pair_sync(pair);
+    if (sm->flag == 0) {
+      uint16_t* __restrict__ out = J.out;
+      const bool inplace = out == J.old;
+      if (e0 + kChunk <= n) {
+        stream_two_steps<true>(sm->buf[b], sm->touched, 4 * half, e0, n, out, inplace, ck);
+        stream_two_steps<true>(sm->buf[b], sm->touched, 4 * half + 2, e0, n, out, inplace, ck);
+      } else {
+        stream_two_steps<false>(sm->buf[b], sm->touched, 4 * half, e0, n, out, inplace, ck);
+        stream_two_steps<false>(sm->buf[b], sm->touched, 4 * half + 2, e0, n, out, inplace, ck);
+      }
+    } else if (pt == 0) {
+      record_status(&info[j].chunk_err, BD_ERR_FORMAT);
+    }
+    pair_sync(pair);
+    sm->touched[2 * pt] = 0;
+    sm->touched[2 * pt + 1] = 0;
+    if (pt == 0) sm->flag = 0;
   }
+  cp_async_wait<0>();
   if (cur != 0xFFFFFFFFu) {
     const uint64_t s = warp_sum64(ck);
     if (lane == 0)
@@ -586,12 +695,24 @@ cudaError_t launch_decode(const LaunchCtx& c) {
 
 cudaError_t launch_apply_stream(const LaunchCtx& c) {
   if (c.chunks == 0) return cudaSuccess;
-  static const int per_sm = blocks_per_sm(k_apply_stream);
-  const uint64_t grid = std::min<uint64_t>((c.chunks + kWarps - 1) / kWarps, (uint64_t)per_sm * c.sms);
-  k_apply_stream<<<(unsigned)grid, kThreads, 0, c.stream>>>(
+  constexpr size_t smem = kStreamPairs * sizeof(PairSmem);  // ~66 KiB
+  static const int per_sm = [] {
+    if (cudaFuncSetAttribute(k_apply_stream, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+      return 0;
+    int v = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, k_apply_stream, kStreamThreads, smem) !=
+            cudaSuccess || v < 1)
+      v = 1;
+    return v;
+  }();
+  if (per_sm == 0) return cudaErrorInvalidValue;
+  const uint64_t grid = std::min<uint64_t>((c.chunks + kStreamPairs - 1) / kStreamPairs,
+                                           (uint64_t)per_sm * c.sms);
+  k_apply_stream<<<(unsigned)grid, kStreamThreads, smem, c.stream>>>(
       reinterpret_cast<const DJob*>(c.ws + c.lay.jobs),
       reinterpret_cast<const uint64_t*>(c.ws + c.lay.chunk_start), c.k, c.chunks,
-      reinterpret_cast<const JobInfo*>(c.ws + c.lay.info), c.ws + c.lay.slots, c.ws + c.lay.ck);
+      reinterpret_cast<JobInfo*>(c.ws + c.lay.info), c.ws + c.lay.slots, c.ws + c.lay.ck);
   return cudaGetLastError();
 }
 

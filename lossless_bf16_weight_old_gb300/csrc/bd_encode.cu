@@ -16,7 +16,10 @@
 //                 stream, all at their final payload offsets.  A mantissa-stream byte is
 //                 written by the chunk holding the element its first bit belongs to; when the
 //                 byte reaches into the next chunk that has mantissa values, the first of
-//                 them comes from that chunk's slot.
+//                 them comes from that chunk's slot.  Each warp requests all of a chunk's
+//                 inputs in two rounds (metadata and the first slot entries, then the rest).
+//   emit_dense    the same for the chunks listed by encode_slots as too dense for a slot:
+//                 their changes are derived again from old and new.
 #include "bd_internal.cuh"
 
 namespace bd {
@@ -62,12 +65,16 @@ template <bool FULL>
 __device__ __forceinline__ void encode_chunk(const uint16_t* __restrict__ old,
                                              const uint16_t* __restrict__ neu, uint64_t n,
                                              uint64_t e0, uint32_t* __restrict__ slot,
-                                             uint32_t& mcnt, uint32_t& rcnt, uint64_t& ck) {
+                                             uint64_t& ck, uint64_t g,
+                                             uint32_t* __restrict__ counts,
+                                             uint32_t* __restrict__ list_count,
+                                             uint32_t* __restrict__ list) {
   const int lane = threadIdx.x & 31;
   const uint64_t words = (n + 3) >> 2;
   uint32_t* __restrict__ entries = slot + kSlotHeader / 4;
-  uint32_t running = 0;
-  uint32_t fm = 0;  // first mantissa value | kAuxHasM once found
+  uint32_t running = 0;        // changes in the steps done so far
+  uint32_t nl = 0, rl = 0;     // this lane's changes, and its rare ones
+  uint32_t fm = 0;             // first mantissa value | kAuxHasM once found
   uint64_t e = e0 + lane * 16;
   uint4 o0, o1, n0, n1;
   if (FULL) {
@@ -105,40 +112,47 @@ __device__ __forceinline__ void encode_chunk(const uint16_t* __restrict__ old,
     const uint32_t nz = nz_mask16(x0, x1);
     const uint32_t cnt = __popc(nz);
     const uint32_t incl = warp_incl_scan(cnt);
-    const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
     uint32_t idx = running + incl - cnt;
-    uint32_t bits = nz, lane_fm = 0;
-    while (bits) {
+    uint32_t lane_fm = 0;
+    for (uint32_t bits = nz; bits; bits &= bits - 1) {
       const int b = __ffs(bits) - 1;
-      bits &= bits - 1;
       const uint32_t xv = elem_of(b < 8 ? x0 : x1, b & 7);
       if (xv & kSignExp) {
-        rcnt++;
-      } else {
-        mcnt++;
-        if (lane_fm == 0) lane_fm = xv | kAuxHasM;
+        rl++;
+      } else if (lane_fm == 0) {
+        lane_fm = xv | kAuxHasM;
       }
       if (idx < kSlotEntries) entries[idx] = ((eloc + b) << 16) | xv;
       idx++;
     }
+    nl += cnt;
     if (fm == 0) {
       const uint32_t has = __ballot_sync(0xFFFFFFFFu, lane_fm != 0);
       if (has) fm = __shfl_sync(0xFFFFFFFFu, lane_fm, __ffs(has) - 1);
     }
-    running += tot;
+    running += __shfl_sync(0xFFFFFFFFu, incl, 31);
     e += 512;
     key += 128 * kGamma;  // 512 elements = 128 words per step
   }
+  // per-chunk class counts
+  nl = warp_incl_scan(nl);
+  rl = warp_incl_scan(rl);
+  const uint32_t runR = __shfl_sync(0xFFFFFFFFu, rl, 31);
+  const uint32_t runM = __shfl_sync(0xFFFFFFFFu, nl, 31) - runR;
   if (lane == 0) {
-    slot[0] = running > kSlotEntries ? (kSlotOverflow | kSlotEntries) : running;
+    const bool overflow = runM + runR > kSlotEntries;
+    slot[0] = overflow ? kSlotOverflow : slot_info(runM, runR);
     slot[1] = fm;
+    counts[g] = runM | (runR << 16);
+    if (overflow) list[atomicAdd(list_count, 1u)] = (uint32_t)g;
   }
 }
 
 __global__ void __launch_bounds__(kThreads)
 k_encode_slots(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
                uint32_t k, uint64_t total_chunks, uint32_t* __restrict__ counts,
-               uint8_t* __restrict__ slots, uint8_t* __restrict__ ck_base) {
+               uint8_t* __restrict__ slots, uint8_t* __restrict__ ck_base,
+               uint32_t* __restrict__ list_count, uint32_t* __restrict__ list) {
   const int lane = threadIdx.x & 31;
   const uint64_t gwarp = ((uint64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
   const uint64_t nwarps = ((uint64_t)gridDim.x * kThreads) >> 5;
@@ -158,14 +172,10 @@ k_encode_slots(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
     const uint64_t n = jobs[j].n;
     const uint64_t e0 = (g - chunk_start[j]) * kChunk;
     uint32_t* slot = reinterpret_cast<uint32_t*>(slots + g * kSlotBytes);
-    uint32_t mcnt = 0, rcnt = 0;
     if (e0 + kChunk <= n)
-      encode_chunk<true>(jobs[j].old, jobs[j].neu, n, e0, slot, mcnt, rcnt, ck);
+      encode_chunk<true>(jobs[j].old, jobs[j].neu, n, e0, slot, ck, g, counts, list_count, list);
     else
-      encode_chunk<false>(jobs[j].old, jobs[j].neu, n, e0, slot, mcnt, rcnt, ck);
-    mcnt = warp_incl_scan(mcnt);
-    rcnt = warp_incl_scan(rcnt);
-    if (lane == 31) counts[g] = mcnt | (rcnt << 16);
+      encode_chunk<false>(jobs[j].old, jobs[j].neu, n, e0, slot, ck, g, counts, list_count, list);
   }
   if (cur != 0xFFFFFFFFu) {
     const uint64_t s = warp_sum64(ck);
@@ -279,6 +289,46 @@ __device__ __forceinline__ void store_bitmap(uint8_t* dst, const uint32_t* bm, u
   }
 }
 
+// Position of the first mantissa value after chunk g (in g's tensor, ending at g_end) and
+// its value, for the last owned byte of g that reaches past g's own values.  `cnt_next` and
+// `aux_next` are the counts and slot aux word of chunk g + 1, already loaded.
+__device__ __forceinline__ uint32_t next_mant_value(uint64_t g, uint64_t g_end, uint32_t cnt_next,
+                                                    uint32_t aux_next,
+                                                    const uint32_t* __restrict__ counts,
+                                                    const uint8_t* __restrict__ slots) {
+  const int lane = threadIdx.x & 31;
+  if (g + 1 < g_end && (cnt_next & 0xFFFFu) != 0) return aux_next & kMant;
+  for (uint64_t gg = g + 2; gg < g_end; gg += 32) {  // rare: chunks without mantissa values
+    const uint64_t q = gg + lane;
+    const bool has = q < g_end && (counts[q] & 0xFFFFu) != 0;
+    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, has);
+    if (bal) {
+      const uint64_t gn = gg + __ffs(bal) - 1;
+      return reinterpret_cast<const uint32_t*>(slots + gn * kSlotBytes)[1] & kMant;
+    }
+  }
+  return 0;
+}
+
+// Sets up the output pointers of chunk c (counts cnt, exclusive prefixes Pex / Rex).
+__device__ __forceinline__ void emit_ctx(EmitCtx& cx, uint8_t* payload, const JobInfo& I,
+                                         uint32_t cnt, uint32_t B, uint64_t Pex, uint64_t Rex,
+                                         EmitSmem* sm) {
+  const uint32_t M = cnt & 0xFFFFu, R = cnt >> 16;
+  cx.listM = 2 * M < B;
+  cx.listR = 2 * R < B;
+  cx.mblk = payload + I.p_start + Pex;
+  cx.rblk = cx.mblk + block_bytes(M, B);
+  cx.rstream = reinterpret_cast<uint16_t*>(payload + I.r_start) + Rex;
+  cx.sm = sm;
+  cx.M = M;
+  cx.R = R;
+  cx.wbase = 0;
+}
+
+// Chunks whose changes fit their slot: the slot's single position-ordered list is split by
+// class 32 entries at a time with ballots (rank = set lanes below; the previous element of
+// the same class, for the delta, is the nearest such lane below or the carry).
 __global__ void __launch_bounds__(kThreads)
 k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
        const uint64_t* __restrict__ tile_start, uint32_t k, uint64_t total_chunks,
@@ -287,6 +337,7 @@ k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
        const JobInfo* __restrict__ info) {
   __shared__ EmitSmem s_em[kWarps];
   const int lane = threadIdx.x & 31;
+  const uint32_t lt = (1u << lane) - 1;
   const uint64_t gwarp = ((uint64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
   const uint64_t nwarps = ((uint64_t)gridDim.x * kThreads) >> 5;
   EmitSmem* sm = &s_em[threadIdx.x >> 5];
@@ -294,104 +345,177 @@ k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
   uint32_t j = 0xFFFFFFFFu;
   for (uint64_t g = gwarp; g < total_chunks; g += nwarps) {
     j = advance_job(chunk_start, k, j, g);
-    const uint32_t cnt = counts[g];
+    // level 1: everything addressed by g and j alone, requested together
+    const uint8_t* slot = slots + g * kSlotBytes;
+    const uint32_t* E = reinterpret_cast<const uint32_t*>(slot + kSlotHeader);
+    const uint32_t hdr = *reinterpret_cast<const uint32_t*>(slot);
+    uint32_t ent[8];
+    ent[0] = E[lane];
     const uint4 lc = loc[g];
-    const uint32_t* slot = reinterpret_cast<const uint32_t*>(slots + g * kSlotBytes);
-    const uint32_t hdr = slot[0];
-    if (info[j].status != BD_OK) continue;
-    const CJob& J = jobs[j];
-    const uint64_t n = J.n;
     const uint64_t c = g - chunk_start[j];
+    const uint64_t g_end = chunk_start[j + 1];
+    const TileSum pre = tile_pre[tile_start[j] + c / kTileChunks];
+    const uint32_t cnt_next = g + 1 < g_end ? counts[g + 1] : 0u;
+    const uint32_t aux_next =
+        g + 1 < g_end ? reinterpret_cast<const uint32_t*>(slot + kSlotBytes)[1] : 0u;
+    const JobInfo I = info[j];
+    uint8_t* payload = jobs[j].payload;
+    const uint64_t n = jobs[j].n;
+    if (I.status != BD_OK || (hdr & kSlotOverflow)) continue;
+
+    // level 2: the rest of the list
+    const uint32_t M = hdr & 0xFFFu, R = (hdr >> 12) & 0xFFFu, kk = M + R;
+#pragma unroll
+    for (int q = 1; q < 8; q++) {
+      const uint32_t i = 32 * q + lane;
+      ent[q] = i < kk ? E[i] : 0u;
+    }
+
     const uint64_t e0 = c * kChunk;
     const uint32_t L = (n - e0) < kChunk ? (uint32_t)(n - e0) : kChunk;
     const uint32_t B = (L + 7) >> 3;
-    const uint32_t M = cnt & 0xFFFFu, R = cnt >> 16;
-    const TileSum pre = tile_pre[tile_start[j] + c / kTileChunks];
+    const uint32_t cnt = M | (R << 16);
     const uint64_t Pex = pre.p + lc.x, Mex = pre.m + lc.y, Rex = pre.r + lc.z;
-    const JobInfo& I = info[j];
+    if (lane == 0) reinterpret_cast<uint32_t*>(payload + kHeader)[c] = cnt;
+    EmitCtx cx;
+    emit_ctx(cx, payload, I, cnt, B, Pex, Rex, sm);
+    if (!cx.listM || !cx.listR) {
+      for (int i = lane; i < 256; i += 32) sm->bm[i] = 0;
+      __syncwarp();
+    }
+    uint32_t baseM = 0, baseR = 0, carryM = 0, carryR = 0;
+#pragma unroll
+    for (int q = 0; q < 8; q++) {
+      if (32u * q >= kk) break;
+      const uint32_t e = ent[q], pos = e >> 16, x = e & 0xFFFFu;
+      const bool valid = 32u * q + lane < kk;
+      const bool isR = valid && (x & kSignExp);
+      const bool isM = valid && !(x & kSignExp);
+      const uint32_t bM = __ballot_sync(0xFFFFFFFFu, isM), bR = __ballot_sync(0xFFFFFFFFu, isR);
+      const uint32_t lowM = bM & lt, lowR = bR & lt;
+      const uint32_t pM = __shfl_sync(0xFFFFFFFFu, pos, lowM ? 31 - __clz(lowM) : lane);
+      const uint32_t pR = __shfl_sync(0xFFFFFFFFu, pos, lowR ? 31 - __clz(lowR) : lane);
+      if (isM) {
+        const uint32_t r = baseM + __popc(lowM);
+        const uint32_t prev = lowM ? pM : carryM;
+        if (cx.listM) store_u16(cx.mblk + 2 * r, (uint16_t)(pos - prev));
+        else atomicOr(&sm->bm[pos >> 5], 1u << (pos & 31));
+        sm->mv[r] = (uint8_t)(x & kMant);
+      }
+      if (isR) {
+        const uint32_t r = baseR + __popc(lowR);
+        const uint32_t prev = lowR ? pR : carryR;
+        if (cx.listR) store_u16(cx.rblk + 2 * r, (uint16_t)(pos - prev));
+        else atomicOr(&sm->bm[128 + (pos >> 5)], 1u << (pos & 31));
+        cx.rstream[r] = (uint16_t)x;
+      }
+      // carries: position of the last element of each class so far
+      const uint32_t topM = __shfl_sync(0xFFFFFFFFu, pos, bM ? 31 - __clz(bM) : 0);
+      const uint32_t topR = __shfl_sync(0xFFFFFFFFu, pos, bR ? 31 - __clz(bR) : 0);
+      if (bM) carryM = topM;
+      if (bR) carryR = topR;
+      baseM += __popc(bM);
+      baseR += __popc(bR);
+    }
+    __syncwarp();
+    // the mantissa-stream bytes owned by this chunk (first bit in one of its values)
+    const uint64_t b_lo = (7 * Mex + 7) >> 3, b_hi = (7 * (Mex + M) + 7) >> 3;
+    if (b_hi > b_lo) {
+      uint32_t after = 0;
+      const uint64_t jg_last = (8 * (b_hi - 1)) / 7;
+      if (jg_last + 1 == Mex + M && Mex + M < I.sum_m)
+        after = next_mant_value(g, g_end, cnt_next, aux_next, counts, slots);
+      put_mant_bytes(payload + I.m_start, b_lo, b_hi, Mex, M, after, cx);
+    }
+    if (!cx.listM || !cx.listR) {
+      __syncwarp();
+      if (!cx.listM) store_bitmap(cx.mblk, sm->bm, B);
+      if (!cx.listR) store_bitmap(cx.rblk, sm->bm + 128, B);
+    }
+    __syncwarp();
+  }
+}
+
+// Chunks with more changes than a slot holds (listed by encode_slots): the changes are derived
+// again from old and new, 512 elements per step; after each step the mantissa-stream bytes
+// whose two values are known are written and the value window keeps only its last value.
+__global__ void __launch_bounds__(kThreads)
+k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
+             const uint64_t* __restrict__ tile_start, uint32_t k,
+             const uint32_t* __restrict__ list_count, const uint32_t* __restrict__ list,
+             const uint32_t* __restrict__ counts, const uint8_t* __restrict__ slots,
+             const uint4* __restrict__ loc, const TileSum* __restrict__ tile_pre,
+             const JobInfo* __restrict__ info) {
+  __shared__ EmitSmem s_em[kWarps];
+  const int lane = threadIdx.x & 31;
+  const uint64_t gwarp = ((uint64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+  const uint64_t nwarps = ((uint64_t)gridDim.x * kThreads) >> 5;
+  EmitSmem* sm = &s_em[threadIdx.x >> 5];
+  const uint32_t listed = *list_count;
+  for (uint64_t li = gwarp; li < listed; li += nwarps) {
+    const uint64_t g = list[li];
+    const uint32_t j = find_job(chunk_start, k, g);
+    const JobInfo I = info[j];
+    if (I.status != BD_OK) continue;
+    const CJob& J = jobs[j];
+    const uint64_t n = J.n;
+    const uint64_t c = g - chunk_start[j];
+    const uint64_t g_end = chunk_start[j + 1];
+    const uint64_t e0 = c * kChunk;
+    const uint32_t L = (n - e0) < kChunk ? (uint32_t)(n - e0) : kChunk;
+    const uint32_t B = (L + 7) >> 3;
+    const uint32_t cnt = counts[g];
+    const uint32_t M = cnt & 0xFFFFu;
+    const TileSum pre = tile_pre[tile_start[j] + c / kTileChunks];
+    const uint4 lc = loc[g];
+    const uint64_t Pex = pre.p + lc.x, Mex = pre.m + lc.y, Rex = pre.r + lc.z;
     uint8_t* payload = J.payload;
     if (lane == 0) reinterpret_cast<uint32_t*>(payload + kHeader)[c] = cnt;
-
     EmitCtx cx;
-    cx.listM = 2 * M < B;
-    cx.listR = 2 * R < B;
-    cx.mblk = payload + I.p_start + Pex;
-    cx.rblk = cx.mblk + block_bytes(M, B);
-    cx.rstream = reinterpret_cast<uint16_t*>(payload + I.r_start) + Rex;
-    cx.sm = sm;
-    cx.M = M;
-    cx.R = R;
-    cx.wbase = 0;
+    emit_ctx(cx, payload, I, cnt, B, Pex, Rex, sm);
     if (!cx.listM || !cx.listR) {
       for (int i = lane; i < 256; i += 32) sm->bm[i] = 0;
       __syncwarp();
     }
     uint8_t* mout = payload + I.m_start;
-    // mantissa-stream bytes owned by this chunk: those whose first bit is in one of its values
     const uint64_t b_lo = (7 * Mex + 7) >> 3, b_hi = (7 * (Mex + M) + 7) >> 3;
     uint64_t b_next = b_lo;
     EmitState st{0, 0, 0, 0};
-
-    if (!(hdr & kSlotOverflow)) {
-      const uint32_t kk = hdr & 0xFFFFu;
-      const uint32_t* entries = slot + kSlotHeader / 4;
-      for (uint32_t base = 0; base < kk; base += 32) {
-        const uint32_t i = base + lane;
-        uint32_t ent = 0, mm = 0, rmk = 0;
-        if (i < kk) {
-          ent = entries[i];
-          if (ent & kSignExp) rmk = 1; else mm = 1;
+    const uint16_t* __restrict__ old = J.old;
+    const uint16_t* __restrict__ neu = J.neu;
+    for (int s = 0; s < 8; s++) {
+      const uint32_t eloc = s * 512 + lane * 16;
+      const uint64_t e = e0 + eloc;
+      const uint4 x0 = xor4(load8(old, e, n), load8(neu, e, n));
+      const uint4 x1 = xor4(load8(old, e + 8, n), load8(neu, e + 8, n));
+      const uint32_t rare = rare_mask16(x0, x1);
+      emit_batch(eloc, nz_mask16(x0, x1) & ~rare, rare,
+                 [x0, x1](int b) { return elem_of(b < 8 ? x0 : x1, b & 7); }, st, cx);
+      __syncwarp();
+      const uint32_t known = min(st.rankM, M);  // values with rank < known are in the window
+      if (known > cx.wbase) {
+        // byte b is complete when floor(8b/7) + 1 <= Mex + known - 1
+        const uint64_t b_full = (7 * (Mex + known - 1) + 7) >> 3;
+        const uint64_t b_end = min(b_full, b_hi);
+        if (b_end > b_next) {
+          put_mant_bytes(mout, b_next, b_end, Mex, M, 0, cx);
+          b_next = b_end;
         }
-        emit_batch(ent >> 16, mm, rmk, [ent](int) { return ent & 0xFFFFu; }, st, cx);
-      }
-    } else {
-      // Overflow: derive the chunk's changes again from old and new, 512 elements per step.
-      // After each step the bytes whose two values are known are written and the window of
-      // mantissa values keeps only its last value.
-      const uint16_t* __restrict__ old = J.old;
-      const uint16_t* __restrict__ neu = J.neu;
-      for (int s = 0; s < 8; s++) {
-        const uint32_t eloc = s * 512 + lane * 16;
-        const uint64_t e = e0 + eloc;
-        const uint4 x0 = xor4(load8(old, e, n), load8(neu, e, n));
-        const uint4 x1 = xor4(load8(old, e + 8, n), load8(neu, e + 8, n));
-        const uint32_t rare = rare_mask16(x0, x1);
-        emit_batch(eloc, nz_mask16(x0, x1) & ~rare, rare,
-                   [x0, x1](int b) { return elem_of(b < 8 ? x0 : x1, b & 7); }, st, cx);
         __syncwarp();
-        const uint32_t known = min(st.rankM, M);  // values with rank < known are in the window
-        if (known > cx.wbase) {
-          // byte b is complete when floor(8b/7) + 1 <= Mex + known - 1
-          const uint64_t b_full = (7 * (Mex + known - 1) + 7) >> 3;
-          const uint64_t b_end = min(b_full, b_hi);
-          if (b_end > b_next) {
-            put_mant_bytes(mout, b_next, b_end, Mex, M, 0, cx);
-            b_next = b_end;
-          }
-          __syncwarp();
-          if (lane == 0) sm->mv[0] = sm->mv[known - 1 - cx.wbase];
-          __syncwarp();
-          cx.wbase = known - 1;
-        }
+        if (lane == 0) sm->mv[0] = sm->mv[known - 1 - cx.wbase];
+        __syncwarp();
+        cx.wbase = known - 1;
       }
     }
     __syncwarp();
     if (b_hi > b_next) {
-      // the last owned byte may reach into the next chunk of this tensor with mantissa values
       uint32_t after = 0;
       const uint64_t jg_last = (8 * (b_hi - 1)) / 7;
       if (jg_last + 1 == Mex + M && Mex + M < I.sum_m) {
-        const uint64_t g_end = chunk_start[j + 1];
-        for (uint64_t gg = g + 1; gg < g_end; gg += 32) {
-          const uint64_t q = gg + lane;
-          const bool has = q < g_end && (counts[q] & 0xFFFFu) != 0;
-          const uint32_t bal = __ballot_sync(0xFFFFFFFFu, has);
-          if (bal) {
-            const uint64_t gn = gg + __ffs(bal) - 1;
-            after = reinterpret_cast<const uint32_t*>(slots + gn * kSlotBytes)[1] & kMant;
-            break;
-          }
-        }
+        const uint32_t cnt_next = g + 1 < g_end ? counts[g + 1] : 0u;
+        const uint32_t aux_next =
+            g + 1 < g_end ? reinterpret_cast<const uint32_t*>(slots + (g + 1) * kSlotBytes)[1] : 0u;
+        after = next_mant_value(g, g_end, cnt_next, aux_next, counts, slots);
       }
       put_mant_bytes(mout, b_next, b_hi, Mex, M, after, cx);
     }
@@ -427,7 +551,26 @@ cudaError_t launch_encode_slots(const LaunchCtx& c) {
   k_encode_slots<<<(unsigned)grid, kThreads, 0, c.stream>>>(
       reinterpret_cast<const CJob*>(c.ws + c.lay.jobs),
       reinterpret_cast<const uint64_t*>(c.ws + c.lay.chunk_start), c.k, c.chunks,
-      reinterpret_cast<uint32_t*>(c.ws + c.lay.counts), c.ws + c.lay.slots, c.ws + c.lay.ck);
+      reinterpret_cast<uint32_t*>(c.ws + c.lay.counts), c.ws + c.lay.slots, c.ws + c.lay.ck,
+      reinterpret_cast<uint32_t*>(c.ws + c.lay.overflow),
+      reinterpret_cast<uint32_t*>(c.ws + c.lay.ovf_list));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_emit_dense(const LaunchCtx& c) {
+  if (c.chunks == 0) return cudaSuccess;
+  static const int per_sm = blocks_per_sm(k_emit_dense, kThreads);
+  const uint64_t grid = cap_grid((uint64_t)per_sm * c.sms, kWarps, c.chunks);
+  k_emit_dense<<<(unsigned)grid, kThreads, 0, c.stream>>>(
+      reinterpret_cast<const CJob*>(c.ws + c.lay.jobs),
+      reinterpret_cast<const uint64_t*>(c.ws + c.lay.chunk_start),
+      reinterpret_cast<const uint64_t*>(c.ws + c.lay.tile_start), c.k,
+      reinterpret_cast<const uint32_t*>(c.ws + c.lay.overflow),
+      reinterpret_cast<const uint32_t*>(c.ws + c.lay.ovf_list),
+      reinterpret_cast<const uint32_t*>(c.ws + c.lay.counts), c.ws + c.lay.slots,
+      reinterpret_cast<const uint4*>(c.ws + c.lay.loc),
+      reinterpret_cast<const TileSum*>(c.ws + c.lay.tile_pre),
+      reinterpret_cast<const JobInfo*>(c.ws + c.lay.info));
   return cudaGetLastError();
 }
 

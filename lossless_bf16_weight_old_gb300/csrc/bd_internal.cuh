@@ -155,20 +155,25 @@ struct TileSum {   // totals of one scan tile (or their exclusive prefix)
   uint64_t p, m, r, pad;
 };
 
-// Per-chunk slot (workspace), written by the encode pass (compress) or the decode pass
-// (decompress); entries are in ascending position:
-//   u32 info     bits 0..15 entry count, bit 30 malformed chunk, bit 31 overflow (the chunk
-//                has more changed elements than kSlotEntries)
-//   u32 aux      compress: first mantissa-only XOR value of the chunk (bits 0..6), bit 7 set
-//                when the chunk has one
-//   u8 step_end[8]  decompress: entries with position < 512 (s + 1), s = 0..7
-//   u32 entry[kSlotEntries]  pos << 16 | x
+// Per-chunk slot (workspace).  Entries are pos << 16 | x.
+//   u32 info   bits 0..11 mantissa-only count M, bits 12..23 rare count R, bit 30 malformed
+//              chunk, bit 31 overflow (more changes than kSlotEntries: entries incomplete)
+//   u32 aux    compress: first mantissa-only XOR value of the chunk (bits 0..6), bit 7 set
+//              when the chunk has one (valid even on overflow)
+//   u32 pad[2]
+//   u32 entry[kSlotEntries]
+// Compress (encode_slots -> emit): one list of all changes in ascending position at [0, M+R).
+// Decompress (decode -> apply_stream): mantissa-only entries at [0, M), then rare entries at
+// [M, M+R), each class in ascending position.
 constexpr uint32_t kSlotBytes = 1024;
 constexpr uint32_t kSlotHeader = 16;
 constexpr uint32_t kSlotEntries = (kSlotBytes - kSlotHeader) / 4;
 constexpr uint32_t kSlotOverflow = 0x80000000u;
 constexpr uint32_t kSlotBad = 0x40000000u;
 constexpr uint32_t kAuxHasM = 0x80u;
+__host__ __device__ __forceinline__ uint32_t slot_info(uint32_t M, uint32_t R) {
+  return (M & 0xFFFu) | ((R & 0xFFFu) << 12);
+}
 
 // Branch-free field flags of the two BF16 values in a 32-bit word: bit 15 (low value) and
 // bit 31 (high value) are set when the value is nonzero (nz) / has a sign or exponent bit set
@@ -275,6 +280,7 @@ cudaError_t launch_encode_slots(const LaunchCtx& c);
 cudaError_t launch_scan_tiles(const LaunchCtx& c, bool decompress);
 cudaError_t launch_scan_jobs(const LaunchCtx& c, bool decompress, int32_t* d_status_all);
 cudaError_t launch_emit(const LaunchCtx& c);
+cudaError_t launch_emit_dense(const LaunchCtx& c);
 cudaError_t launch_decode(const LaunchCtx& c);
 cudaError_t launch_apply_stream(const LaunchCtx& c);
 cudaError_t launch_apply(const LaunchCtx& c);
