@@ -379,10 +379,10 @@ def run_ours(args) -> None:
     app_ach = app_bytes / (ma * 1e-3) / 1e9
     dom = "compress" if mc >= ma else "apply"
     roof = {"bound": "hbm",
-            "kernel": ("compress phase (bd_compress_batch: encode_slots + count scan + emit)"
-                       if dom == "compress" else
-                       "apply phase (bd_decompress_batch: count scan + decode + apply_stream + "
-                       "apply_dense + apply_finish)"),
+            "kernel": ("compress phase (bd_compress_batch: encode_slots + count scan + emit + "
+                       "emit_dense)" if dom == "compress" else
+                       "apply phase (bd_decompress_batch: count scan + apply_chunks + apply_dense "
+                       "+ apply_finish)"),
             "achieved": round(comp_ach if dom == "compress" else app_ach, 1),
             "peak": peak, "unit": "GB/s",
             "frac": round((comp_ach if dom == "compress" else app_ach) / peak, 4),
@@ -441,7 +441,7 @@ def run_ours(args) -> None:
         cpu = oracle_baseline(specs, args.cpu_sample_elems, dev)
 
     blobs_c = -(-(128 * len(specs) + 2 * 8 * (len(specs) + 1) + 1024) // 30720)
-    launches_per_step = (blobs_c + 4) + (blobs_c + 6)
+    launches_per_step = (blobs_c + 5) + (blobs_c + 5)
 
     if rank == 0:
         line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,

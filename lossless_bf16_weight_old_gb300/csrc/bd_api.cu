@@ -56,11 +56,11 @@ WsLayout make_layout(uint32_t k, const Sizes& s, bool compress) {
   off = up(off + s.tiles * sizeof(TileSum), kAlign);
   L.tile_pre = off;
   off = up(off + s.tiles * sizeof(TileSum), kAlign);
-  L.slots = off;
-  off = up(off + s.chunks * kSlotBytes, kAlign);
-  L.ovf_list = off;  // chunks too dense for a slot
+  L.ovf_list = off;  // chunks too dense for a slot / for the thread-level apply
   off = up(off + s.chunks * 4, kAlign);
   if (compress) {
+    L.slots = off;
+    off = up(off + s.chunks * kSlotBytes, kAlign);
     L.counts = off;
     off = up(off + s.chunks * 4, kAlign);
   }
@@ -216,8 +216,10 @@ int decompress_impl(const bd_decompress_item* items, uint32_t k, void* ws, uint6
   uint64_t* cstart = reinterpret_cast<uint64_t*>(host.data() + (lay.chunk_start - lay.jobs));
   uint64_t* tstart = reinterpret_cast<uint64_t*>(host.data() + (lay.tile_start - lay.jobs));
   uint64_t cb = 0, tb = 0;
+  bool any_out_of_place = false;
   for (uint32_t i = 0; i < k; i++) {
     const bd_decompress_item& it = items[i];
+    if (it.d_out != it.d_old) any_out_of_place = true;
     DJob& J = jobs[i];
     J.old = it.d_old;
     J.out = it.d_out;
@@ -246,8 +248,8 @@ int decompress_impl(const bd_decompress_item* items, uint32_t k, void* ws, uint6
   if ((rc = check(upload(host, w + lay.jobs, s)))) return rc;
   if ((rc = check(launch_scan_tiles(c, true)))) return rc;
   if ((rc = check(launch_scan_jobs(c, true, nullptr)))) return rc;
-  if ((rc = check(launch_decode(c)))) return rc;
-  if ((rc = check(launch_apply_stream(c)))) return rc;
+  if (any_out_of_place && (rc = check(launch_copy_jobs(c)))) return rc;
+  if ((rc = check(launch_apply_chunks(c)))) return rc;
   if ((rc = check(launch_apply(c)))) return rc;
   return check(launch_apply_finish(c, status_all));
 }

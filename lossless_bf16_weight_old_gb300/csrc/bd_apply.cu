@@ -6,24 +6,22 @@
 // result is checksummed against the trainer's original.
 //
 // After the count scan (bd_scan.cu):
-//   decode        one warp per chunk: requests the chunk's position blocks and values in one
-//                 round, decodes the positions (delta list -> prefix sum, or bitmap ->
-//                 popcount rank) and writes (position, XOR) entries into the chunk's workspace
-//                 slot, mantissa-only from the front and rare from the back, checking the
-//                 format rules.  Chunks with more changes than a slot holds are listed for
-//                 apply_dense.
-//   apply_stream  two warps per chunk, the streaming pass over old: the chunk's 8 KiB of old are
-//                 copied into shared memory with cp.async while the previous chunk is processed
-//                 (double buffer) and its slot is prefetched into registers; the entries are
-//                 XORed into the staged data with shared-memory atomics (a position taken
-//                 twice is malformed), then each warp checksums half of the result, two steps
-//                 at a time, and writes back only the 16-byte groups that changed (in place)
-//                 or every group (out of place).
-//   apply_dense   one CTA per listed chunk: decodes straight from the payload into an 8 KiB
-//                 shared mask (dense chunks, bitmap positions).
-//   apply_finish  one thread per tensor: checks the mantissa-stream pad bits, compares the
-//                 checksum with the expected value and publishes the status.
-// Malformed chunks are detected before any write to them and are left unwritten.
+//   copy_jobs      out-of-place only: out = old (warp per chunk), so the passes below work on
+//                  out in place.
+//   apply_chunks   one warp per chunk whose two position blocks are delta lists (the common
+//                  case for sparse deltas): decodes and checks the whole chunk into shared
+//                  memory, XORs each change into out with a 32-bit atomic XOR performed in L2,
+//                  then reads the chunk back through L2 for its checksum terms.  The atomics
+//                  bring the touched sectors into L2 where the read-back finds them, so each
+//                  sector of out crosses HBM at most once each way.  Chunks with a bitmap
+//                  block are listed.
+//   apply_dense    one CTA per listed chunk: decodes into an 8 KiB shared mask, XORs the
+//                  chunk, writes the changed 16-byte groups and adds their checksum terms.
+//   apply_finish   one thread per tensor: checks the mantissa-stream pad bits, compares the
+//                  checksum with the expected value and publishes the status.
+// A malformed chunk is checked in full before anything is written and is left unwritten, so on
+// any error applying the same payload again undoes the other chunks (XOR involution; decoding
+// depends on the payload only).
 #include <algorithm>
 
 #include "bd_internal.cuh"
@@ -44,6 +42,20 @@ __device__ __forceinline__ uint32_t mant_value(const uint8_t* __restrict__ ms, u
   return v & kMant;
 }
 
+// Adds a warp's checksum partial sum to tensor j's accumulators (one slot per warp parity
+// class, so that the atomics of different warps spread over L2 lines).
+__device__ __forceinline__ void flush_ck(uint8_t* ck_base, uint32_t j, uint64_t gwarp,
+                                         uint64_t ck) {
+  const uint64_t s = warp_sum64(ck);
+  if ((threadIdx.x & 31) == 0)
+    atomicAdd(reinterpret_cast<unsigned long long*>(ck_base + (uint64_t)j * kCkBytes) +
+                  (gwarp & (kCkSlots - 1)) * kCkStride,
+              (unsigned long long)s);
+}
+
+// One CTA per listed chunk (a chunk with a bitmap block): decodes the chunk into an 8 KiB
+// shared XOR mask, applies it, writes the changed 16-byte groups and adds the checksum terms
+// of the result.
 __global__ void __launch_bounds__(kThreads)
 k_apply_dense(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
               const uint64_t* __restrict__ tile_start, uint32_t k,
@@ -53,37 +65,25 @@ k_apply_dense(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_
   __shared__ uint4 s_mask4[kChunk / 8];       // the chunk's XOR mask, 8 KiB
   __shared__ uint32_t s_tot[kWarps][4];
   __shared__ int s_bad;
-  __shared__ uint64_t s_ck[kWarps];
   uint16_t* s_mask = reinterpret_cast<uint16_t*>(s_mask4);
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
 
-  if (t == 0) s_bad = 0;
-  uint32_t cur_job = 0xFFFFFFFFu;
+  const uint64_t gwarp = ((uint64_t)blockIdx.x * kThreads + t) >> 5;
+  uint32_t cur = 0xFFFFFFFFu;
   uint64_t ck = 0;
+  if (t == 0) s_bad = 0;
   __syncthreads();
 
   const uint32_t listed = *list_count;
   for (uint32_t li = blockIdx.x; li < listed; li += gridDim.x) {
     const uint64_t g = list[li];
     const uint32_t j = find_job(chunk_start, k, g);
-    if (j != cur_job) {
-      if (cur_job != 0xFFFFFFFFu) {
-        const uint64_t s = warp_sum64(ck);
-        if (lane == 0) s_ck[w] = s;
-        __syncthreads();
-        if (t == 0) {
-          uint64_t tot = 0;
-          for (int q = 0; q < kWarps; q++) tot += s_ck[q];
-          atomicAdd(reinterpret_cast<unsigned long long*>(ck_base + (uint64_t)cur_job * kCkBytes) +
-                        (blockIdx.x & (kCkSlots - 1)) * kCkStride,
-                    (unsigned long long)tot);
-        }
-        __syncthreads();
-      }
-      cur_job = j;
+    if (info[j].status != BD_OK) continue;
+    if (j != cur) {   // block-uniform
+      if (cur != 0xFFFFFFFFu) flush_ck(ck_base, cur, gwarp, ck);
+      cur = j;
       ck = 0;
     }
-    if (info[j].status != BD_OK) continue;
 
     const DJob& J = jobs[j];
     const uint64_t n = J.n;
@@ -105,9 +105,9 @@ k_apply_dense(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_
     const uint8_t* mstream = payload + m_start;
     const uint8_t* rstream = payload + r_start + 2 * Rex;
 
-    // the old chunk: groups t and t + 256 (8 elements each)
+    // the chunk of `out` (which holds old at this point): groups t and t + 256
     const uint64_t ea = e0 + 8 * (uint64_t)t, eb = ea + 2048;
-    const uint4 oa = load8(J.old, ea, n), ob = load8(J.old, eb, n);
+    const uint4 oa = load8(J.out, ea, n), ob = load8(J.out, eb, n);
     s_mask4[t] = make_uint4(0, 0, 0, 0);
     s_mask4[t + 256] = make_uint4(0, 0, 0, 0);
 
@@ -220,19 +220,18 @@ k_apply_dense(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_
       const uint4 ma = s_mask4[t], mb = s_mask4[t + 256];
       const uint4 ra = make_uint4(oa.x ^ ma.x, oa.y ^ ma.y, oa.z ^ ma.z, oa.w ^ ma.w);
       const uint4 rb = make_uint4(ob.x ^ mb.x, ob.y ^ mb.y, ob.z ^ mb.z, ob.w ^ mb.w);
-      const uint64_t words = (n + 3) >> 2;
-      ck += group_hash(ra, ea >> 3, words) + group_hash(rb, eb >> 3, words);
-      const bool inplace = J.out == J.old;
       const bool cha = (ma.x | ma.y | ma.z | ma.w) != 0, chb = (mb.x | mb.y | mb.z | mb.w) != 0;
       uint16_t* out = J.out;
-      if (ea < n && (!inplace || cha)) {
+      if (ea < n && cha) {
         if (ea + 8 <= n) *reinterpret_cast<uint4*>(out + ea) = ra;
         else for (int i = 0; ea + i < n; i++) out[ea + i] = (uint16_t)elem_of(ra, i);
       }
-      if (eb < n && (!inplace || chb)) {
+      if (eb < n && chb) {
         if (eb + 8 <= n) *reinterpret_cast<uint4*>(out + eb) = rb;
         else for (int i = 0; eb + i < n; i++) out[eb + i] = (uint16_t)elem_of(rb, i);
       }
+      const uint64_t words = (n + 3) >> 2;
+      ck += group_hash(ra, ea >> 3, words) + group_hash(rb, eb >> 3, words);
     }
     __syncthreads();
     if (t == 0 && chunk_bad) {
@@ -241,401 +240,219 @@ k_apply_dense(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_
     }
     __syncthreads();
   }
-  if (cur_job != 0xFFFFFFFFu) {
-    const uint64_t s = warp_sum64(ck);
-    if (lane == 0) s_ck[w] = s;
-    __syncthreads();
-    if (t == 0) {
-      uint64_t tot = 0;
-      for (int q = 0; q < kWarps; q++) tot += s_ck[q];
-      atomicAdd(reinterpret_cast<unsigned long long*>(ck_base + (uint64_t)cur_job * kCkBytes) +
-                    (blockIdx.x & (kCkSlots - 1)) * kCkStride,
-                (unsigned long long)tot);
-    }
-  }
+  if (cur != 0xFFFFFFFFu) flush_ck(ck_base, cur, gwarp, ck);
 }
 
-// ------------------------------------------------------------------------ decode
+// ------------------------------------------------------------------------ apply_chunks
 
-// 16-byte asynchronous global -> shared copy; src_bytes < 16 zero-fills the rest.
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, uint32_t src_bytes) {
-  const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem),
-               "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;\n" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
-}
+// Longest delta list of a chunk: a block is a list only while 2k < 512 bytes.
+constexpr uint32_t kListMax = 255;
+constexpr uint32_t kEntMax = 2 * kListMax + 2;
+constexpr uint32_t kNone = 0xFFFFFFFFu;
+constexpr unsigned kFull = 0xFFFFFFFFu;
 
-// 4-byte asynchronous global -> shared copy; src_bytes < 4 zero-fills the rest.
-__device__ __forceinline__ void cp_async4(void* smem, const void* gmem, uint32_t src_bytes) {
-  const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(s), "l"(gmem),
-               "r"(src_bytes)
-               : "memory");
+// Loads served by L2 only (never by L1): `out` is changed by L2 atomics while the kernel runs.
+// Volatile so that the compiler keeps them after the atomics and the fence that precede them.
+__device__ __forceinline__ uint4 ld_l2(const uint16_t* p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
 }
-
-
-// Staging capacity per warp, in 32-bit words, of the three payload byte ranges of one chunk
-// whose changes fit a slot (M + R <= kSlotEntries): position blocks (delta lists up to 504
-// bytes, or bitmaps of a ragged last chunk up to 2 x 511 bytes), mantissa bytes (up to 221)
-// and rare values (up to 504 bytes), each widened to whole aligned words.
-constexpr int kStageP = 9, kStageM = 2, kStageR = 4;   // words per lane
-struct DecodeSmem {
-  uint32_t wp[32 * kStageP], wm[32 * kStageM], wr[32 * kStageR];
-};
-
-__device__ __forceinline__ uint32_t sbyte(const uint32_t* w, uint32_t i) {
-  return (w[i >> 2] >> (8 * (i & 3))) & 0xFFu;
+__device__ __forceinline__ uint32_t ld_l2_u16(const uint16_t* p) {
+  unsigned short v;
+  asm volatile("ld.global.cg.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
 }
-__device__ __forceinline__ uint32_t su16(const uint32_t* w, uint32_t i) {
-  return sbyte(w, i) | (sbyte(w, i + 1) << 8);
+__device__ __forceinline__ uint4 load8_l2(const uint16_t* p, uint64_t e, uint64_t n) {
+  if (e + 8 <= n) return ld_l2(p + e);
+  uint32_t w[4] = {0, 0, 0, 0};
+  for (int i = 0; i < 8; i++)
+    if (e + i < n) w[i >> 1] |= ld_l2_u16(p + e + i) << (16 * (i & 1));
+  return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Decodes the k ascending positions of one class from the staged block (byte offset `boff`
-// in the word buffer w; chunk of length L whose bitmap has B bytes) and hands each one to
-// sink(rank, position).  Returns true when the block is malformed.
-template <typename SINK>
-__device__ __forceinline__ bool decode_positions(const uint32_t* w, uint32_t boff, uint32_t k,
-                                                 uint32_t L, uint32_t B, SINK sink) {
-  const int lane = threadIdx.x & 31;
-  bool bad = false;
-  if (2 * k < B) {  // delta list: d_0 = p_0, d_i = p_i - p_{i-1} >= 1
-    uint32_t carry = 0;
-    for (uint32_t base = 0; base < k; base += 32) {
-      const uint32_t i = base + lane;
-      uint32_t d = 0;
-      if (i < k) {
-        d = su16(w, boff + 2 * i);
-        if (i > 0 && d == 0) bad = true;
-      }
-      const uint32_t p = carry + warp_incl_scan(d);
-      if (i < k) {
-        if (p >= L) bad = true;
-        else sink(i, p);
-      }
-      carry = __shfl_sync(0xFFFFFFFFu, p, 31);
-    }
-  } else {  // bitmap: lane handles bytes [16 lane, 16 lane + 16)
-    uint32_t bytes[4] = {0, 0, 0, 0};
-    uint32_t cnt = 0;
-#pragma unroll
-    for (int q = 0; q < 16; q++) {
-      const uint32_t bi = 16 * lane + q;
-      const uint32_t v = bi < B ? sbyte(w, boff + bi) : 0u;
-      bytes[q >> 2] |= v << (8 * (q & 3));
-      cnt += __popc(v);
-    }
-    const uint32_t incl = warp_incl_scan(cnt);
-    if (__shfl_sync(0xFFFFFFFFu, incl, 31) != k) bad = true;
-    uint32_t r = incl - cnt;
-    for (int q = 0; q < 4; q++) {
-      for (uint32_t bits = bytes[q]; bits; bits &= bits - 1) {
-        const uint32_t p = 128 * lane + 32 * q + __ffs(bits) - 1;
-        if (p >= L || r >= k) { bad = true; break; }
-        sink(r++, p);
-      }
-    }
-  }
-  return bad;
-}
-
-// One chunk's payload pieces, as aligned word ranges.
-struct WordRange {
-  uint64_t first;   // byte offset (multiple of 4) of the first word
-  uint32_t words;   // words to stage
-  uint32_t skip;    // offset of the range's first byte inside the first word
-};
-__device__ __forceinline__ WordRange word_range(uint64_t a, uint64_t b) {
-  WordRange r;
-  r.first = a & ~3ull;
-  r.skip = (uint32_t)(a - r.first);
-  r.words = b > a ? (uint32_t)((((b + 3) & ~3ull) - r.first) >> 2) : 0u;
-  return r;
-}
-
-// Starts the asynchronous copy of word w of range r (payload of `size` bytes) to dst.
-__device__ __forceinline__ void stage_word(uint32_t* dst, const uint8_t* __restrict__ payload,
-                                           const WordRange& r, uint32_t w, uint64_t size) {
-  if (w >= r.words) return;
-  const uint64_t off = r.first + 4ull * w;
-  const uint32_t bytes = off + 4 <= size ? 4u : (off < size ? (uint32_t)(size - off) : 0u);
-  cp_async4(dst, bytes ? payload + off : payload, bytes);
-}
-
-__global__ void __launch_bounds__(kThreads)
-k_decode(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
-         const uint64_t* __restrict__ tile_start, uint32_t k, uint64_t total_chunks,
-         const uint4* __restrict__ loc, const TileSum* __restrict__ tile_pre,
-         JobInfo* __restrict__ info, uint8_t* __restrict__ slots,
-         uint32_t* __restrict__ list_count, uint32_t* __restrict__ list) {
-  __shared__ DecodeSmem s_dec[kWarps];
-  const int lane = threadIdx.x & 31;
-  const uint64_t gwarp = ((uint64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
-  const uint64_t nwarps = ((uint64_t)gridDim.x * kThreads) >> 5;
-  DecodeSmem* sm = &s_dec[threadIdx.x >> 5];
-  uint32_t j = 0xFFFFFFFFu;
-  for (uint64_t g = gwarp; g < total_chunks; g += nwarps) {
-    j = advance_job(chunk_start, k, j, g);
-    // level 1: everything addressed by g and j alone
-    const DJob& J = jobs[j];
-    const JobInfo& I = info[j];
-    const uint64_t c = g - chunk_start[j];
-    const uint4 lc = loc[g];
-    const TileSum pre = tile_pre[tile_start[j] + c / kTileChunks];
-    const int32_t status = I.status;
-    const uint8_t* __restrict__ payload = J.payload;
-    if (status != BD_OK) continue;
-    const uint32_t cnt = reinterpret_cast<const uint32_t*>(payload + kHeader)[c];
-    const uint64_t n = J.n, size = J.size;
-    const uint64_t e0 = c * kChunk;
-    const uint32_t L = (n - e0) < kChunk ? (uint32_t)(n - e0) : kChunk;
-    const uint32_t B = (L + 7) >> 3;
-    const uint32_t M = cnt & 0xFFFFu, R = cnt >> 16;
-    uint32_t* slot = reinterpret_cast<uint32_t*>(slots + g * kSlotBytes);
-    if (M + R > kSlotEntries) {
-      if (lane == 0) {
-        slot[0] = kSlotOverflow;
-        list[atomicAdd(list_count, 1u)] = (uint32_t)g;
-      }
-      continue;
-    }
-    const uint64_t Pex = pre.p + lc.x, Mex = pre.m + lc.y, Rex = pre.r + lc.z;
-    const uint32_t blkM = block_bytes(M, B), blkR = block_bytes(R, B);
-    // level 2: the chunk's three payload ranges, all words requested before any is used
-    const uint64_t pa = I.p_start + Pex;
-    const WordRange wp = word_range(pa, pa + blkM + blkR);
-    const uint64_t ma = I.m_start + ((7 * Mex) >> 3);
-    const WordRange wm = word_range(ma, I.m_start + ((7 * (Mex + M) + 7) >> 3));
-    const uint64_t ra = I.r_start + 2 * Rex;
-    const WordRange wr = word_range(ra, ra + 2 * R);
-#pragma unroll
-    for (int q = 0; q < kStageP; q++) stage_word(&sm->wp[lane + 32 * q], payload, wp, lane + 32 * q, size);
-#pragma unroll
-    for (int q = 0; q < kStageM; q++) stage_word(&sm->wm[lane + 32 * q], payload, wm, lane + 32 * q, size);
-#pragma unroll
-    for (int q = 0; q < kStageR; q++) stage_word(&sm->wr[lane + 32 * q], payload, wr, lane + 32 * q, size);
-    cp_async_commit();
-    cp_async_wait<0>();
-    __syncwarp();
-
-    // entries: mantissa-only at [0, M), rare at [M, M+R) (collisions are checked when the
-    // chunk is applied)
-    uint32_t* entries = slot + kSlotHeader / 4;
-    bool bad = false;
-    const uint32_t mbit0 = 8 * wm.skip + (uint32_t)((7 * Mex) & 7);
-    const uint32_t* wmv = sm->wm;
-    bad |= decode_positions(sm->wp, wp.skip, M, L, B, [&](uint32_t r, uint32_t p) {
-      const uint32_t bit = mbit0 + 7 * r;
-      const uint32_t v = (su16(wmv, bit >> 3) >> (bit & 7)) & kMant;
-      if (v == 0) bad = true;
-      entries[r] = (p << 16) | v;
-    });
-    const uint32_t* wrv = sm->wr;
-    const uint32_t rskip = wr.skip;
-    bad |= decode_positions(sm->wp, wp.skip + blkM, R, L, B, [&](uint32_t r, uint32_t p) {
-      const uint32_t v = su16(wrv, rskip + 2 * r);
-      if ((v & kSignExp) == 0) bad = true;
-      entries[M + r] = (p << 16) | v;
-    });
-    bad = __any_sync(0xFFFFFFFFu, bad);
-    if (lane == 0) {
-      slot[0] = slot_info(M, R) | (bad ? kSlotBad : 0u);
-      if (bad) record_status(&info[j].chunk_err, BD_ERR_FORMAT);
-    }
-    __syncwarp();
-  }
-}
-
-// ------------------------------------------------------------------------ apply_stream
-
-constexpr int kStreamThreads = 256;  // 4 pairs of warps, one chunk per pair
-constexpr int kStreamPairs = kStreamThreads / 64;
-struct PairSmem {
-  uint4 buf[2][kChunk / 8];       // two 8 KiB chunk buffers (double-buffered old data)
-  uint32_t touched[kChunk / 32];  // 512 B: positions written in the current chunk
-  uint32_t flag;                  // a position was taken twice
-  uint32_t pad[3];
-};
-
-// Barrier over the 64 threads of one warp pair (ids 1..4; 0 is __syncthreads).
-__device__ __forceinline__ void pair_sync(int pair) {
-  asm volatile("bar.sync %0, 64;\n" ::"r"(pair + 1) : "memory");
-}
-
-// Starts copying chunk [e0, e0 + 4096) of old into buf: pair thread pt copies groups
-// 64 t + pt (group q = elements e0 + 8q .. +8), elements past n read as zero.
-__device__ __forceinline__ void issue_chunk(uint4* buf, const uint16_t* __restrict__ old,
-                                            uint64_t n, uint64_t e0, uint32_t pt) {
-#pragma unroll
-  for (int t = 0; t < 8; t++) {
-    const uint32_t q = 64 * t + pt;
-    const uint64_t e = e0 + 8 * q;
-    const uint32_t bytes = e + 8 <= n ? 16u : (e < n ? (uint32_t)(2 * (n - e)) : 0u);
-    cp_async16(&buf[q], bytes ? old + e : old, bytes);
-  }
-}
-
-// XORs one entry into the staged chunk; returns true when its position was already taken.
-__device__ __forceinline__ bool xor_entry(uint32_t* data32, uint32_t* touched, uint32_t e) {
-  const uint32_t pos = (e >> 16) & (kChunk - 1);
-  atomicXor(&data32[pos >> 1], (e & 0xFFFFu) << (16 * (pos & 1)));
-  return (atomicOr(&touched[pos >> 5], 1u << (pos & 31)) >> (pos & 31)) & 1u;
-}
-
-// Checksums and writes back the two 16-byte groups of this lane in step s (elements
-// e0 + 512 s + 16 lane ..); tmask = the 16 touched bits of those elements.
+// Checksum terms of one chunk of w (elements e0 .. e0+4095, clipped at n), one warp: two
+// 512-element steps at a time per lane, so eight independent hash chains per lane, with the
+// next two steps' loads in flight.
 template <bool FULL>
-__device__ __forceinline__ void put_groups(uint4 r0, uint4 r1, uint32_t tmask, uint64_t e,
-                                           uint64_t key, uint64_t n, uint64_t words,
-                                           uint16_t* __restrict__ out, bool inplace,
-                                           uint64_t& ck) {
-  if (FULL) {
-    const uint64_t a0 = (uint64_t)r0.x | ((uint64_t)r0.y << 32);
-    const uint64_t a1 = (uint64_t)r0.z | ((uint64_t)r0.w << 32);
-    const uint64_t a2 = (uint64_t)r1.x | ((uint64_t)r1.y << 32);
-    const uint64_t a3 = (uint64_t)r1.z | ((uint64_t)r1.w << 32);
-    ck += mix64(a0 ^ key) + mix64(a1 ^ (key + kGamma)) + mix64(a2 ^ (key + 2 * kGamma)) +
-          mix64(a3 ^ (key + 3 * kGamma));
-    if (!inplace || (tmask & 0xFFu)) *reinterpret_cast<uint4*>(out + e) = r0;
-    if (!inplace || (tmask >> 8)) *reinterpret_cast<uint4*>(out + e + 8) = r1;
-  } else {
-    ck += group_hash(r0, e >> 3, words) + group_hash(r1, (e >> 3) + 1, words);
-    if (e < n && (!inplace || (tmask & 0xFFu))) {
-      if (e + 8 <= n) *reinterpret_cast<uint4*>(out + e) = r0;
-      else for (int i = 0; e + i < n; i++) out[e + i] = (uint16_t)elem_of(r0, i);
-    }
-    if (e + 8 < n && (!inplace || (tmask >> 8))) {
-      if (e + 16 <= n) *reinterpret_cast<uint4*>(out + e + 8) = r1;
-      else for (int i = 0; e + 8 + i < n; i++) out[e + 8 + i] = (uint16_t)elem_of(r1, i);
-    }
-  }
-}
-
-// Steps s0 and s0 + 1 of a staged chunk, interleaved (eight independent hash chains per lane).
-template <bool FULL>
-__device__ __forceinline__ void stream_two_steps(const uint4* buf, const uint32_t* touched,
-                                                 int s0, uint64_t e0, uint64_t n,
-                                                 uint16_t* __restrict__ out, bool inplace,
-                                                 uint64_t& ck) {
+__device__ __forceinline__ uint64_t hash_chunk(const uint16_t* w, uint64_t n, uint64_t e0) {
   const int lane = threadIdx.x & 31;
   const uint64_t words = (n + 3) >> 2;
-  const uint4 a0 = buf[64 * s0 + 2 * lane], a1 = buf[64 * s0 + 2 * lane + 1];
-  const uint4 b0 = buf[64 * (s0 + 1) + 2 * lane], b1 = buf[64 * (s0 + 1) + 2 * lane + 1];
-  const uint32_t ta = (touched[16 * s0 + (lane >> 1)] >> (16 * (lane & 1))) & 0xFFFFu;
-  const uint32_t tb = (touched[16 * (s0 + 1) + (lane >> 1)] >> (16 * (lane & 1))) & 0xFFFFu;
-  const uint64_t ea = e0 + 512 * s0 + 16 * lane, eb = ea + 512;
-  const uint64_t ka = ((ea >> 2) + 1) * kGamma, kb = ka + 128 * kGamma;
-  uint64_t c0 = 0, c1 = 0;
-  put_groups<FULL>(a0, a1, ta, ea, ka, n, words, out, inplace, c0);
-  put_groups<FULL>(b0, b1, tb, eb, kb, n, words, out, inplace, c1);
-  ck += c0 + c1;
+  uint64_t ck = 0;
+  uint64_t e = e0 + 16 * lane;
+  uint4 a0, a1, b0, b1;
+  if (FULL) {
+    a0 = ld_l2(w + e); a1 = ld_l2(w + e + 8);
+    b0 = ld_l2(w + e + 512); b1 = ld_l2(w + e + 520);
+  } else {
+    a0 = load8_l2(w, e, n); a1 = load8_l2(w, e + 8, n);
+    b0 = load8_l2(w, e + 512, n); b1 = load8_l2(w, e + 520, n);
+  }
+  uint64_t key = ((e >> 2) + 1) * kGamma;
+#pragma unroll 1
+  for (int s = 0; s < 8; s += 2) {
+    const uint4 c0 = a0, c1 = a1, d0 = b0, d1 = b1;
+    if (s < 6) {
+      const uint64_t en = e + 1024;
+      if (FULL) {
+        a0 = ld_l2(w + en); a1 = ld_l2(w + en + 8);
+        b0 = ld_l2(w + en + 512); b1 = ld_l2(w + en + 520);
+      } else {
+        a0 = load8_l2(w, en, n); a1 = load8_l2(w, en + 8, n);
+        b0 = load8_l2(w, en + 512, n); b1 = load8_l2(w, en + 520, n);
+      }
+    }
+    if (FULL) {
+      const uint64_t kb = key + 128 * kGamma;
+      ck += mix64(((uint64_t)c0.x | ((uint64_t)c0.y << 32)) ^ key) +
+            mix64(((uint64_t)c0.z | ((uint64_t)c0.w << 32)) ^ (key + kGamma)) +
+            mix64(((uint64_t)c1.x | ((uint64_t)c1.y << 32)) ^ (key + 2 * kGamma)) +
+            mix64(((uint64_t)c1.z | ((uint64_t)c1.w << 32)) ^ (key + 3 * kGamma)) +
+            mix64(((uint64_t)d0.x | ((uint64_t)d0.y << 32)) ^ kb) +
+            mix64(((uint64_t)d0.z | ((uint64_t)d0.w << 32)) ^ (kb + kGamma)) +
+            mix64(((uint64_t)d1.x | ((uint64_t)d1.y << 32)) ^ (kb + 2 * kGamma)) +
+            mix64(((uint64_t)d1.z | ((uint64_t)d1.w << 32)) ^ (kb + 3 * kGamma));
+    } else {
+      ck += group_hash(c0, e >> 3, words) + group_hash(c1, (e >> 3) + 1, words) +
+            group_hash(d0, (e + 512) >> 3, words) + group_hash(d1, ((e + 512) >> 3) + 1, words);
+    }
+    e += 1024;
+    key += 256 * kGamma;
+  }
+  return ck;
 }
 
-__global__ void __launch_bounds__(kStreamThreads)
-k_apply_stream(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
-               uint32_t k, uint64_t total_chunks, JobInfo* __restrict__ info,
-               const uint8_t* __restrict__ slots, uint8_t* __restrict__ ck_base) {
-  extern __shared__ uint4 s_dyn[];
-  const int lane = threadIdx.x & 31;
-  const int pair = threadIdx.x >> 6, half = (threadIdx.x >> 5) & 1;
-  const uint32_t pt = threadIdx.x & 63;
-  const uint64_t gpair = (uint64_t)blockIdx.x * kStreamPairs + pair;
-  const uint64_t npairs = (uint64_t)gridDim.x * kStreamPairs;
-  const uint64_t gwarp = 2 * gpair + half;
-  PairSmem* sm = reinterpret_cast<PairSmem*>(s_dyn) + pair;
-  sm->touched[2 * pt] = 0;
-  sm->touched[2 * pt + 1] = 0;
-  if (pt == 0) sm->flag = 0;
-
-  uint32_t j = 0xFFFFFFFFu, cur = 0xFFFFFFFFu;
+// One warp per chunk of every tensor whose scan status is BD_OK.  A chunk whose two position
+// blocks are delta lists is decoded and checked in full into shared memory (positions from
+// the prefix sums of the deltas, 7-bit values from the mantissa stream at bit 7*(M prefix +
+// i), 16-bit values from the rare stream; a position in both classes, a zero delta after the
+// first, a position past the chunk, a zero mantissa value or a rare value without a sign or
+// exponent bit marks the chunk malformed).  A well-formed chunk is then XORed into `out` by
+// one 32-bit atomic XOR per change, performed in L2 without a reply, and read back through
+// L2 for its checksum terms.  Chunks with a bitmap block are listed for apply_dense, which
+// also adds their checksum terms.
+__global__ void __launch_bounds__(kThreads, 4)
+k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
+               const uint64_t* __restrict__ tile_start, uint32_t k, uint64_t total_chunks,
+               const uint4* __restrict__ loc, const TileSum* __restrict__ tile_pre,
+               JobInfo* __restrict__ info, uint32_t* __restrict__ list_count,
+               uint32_t* __restrict__ list, uint8_t* __restrict__ ck_base) {
+  __shared__ uint32_t s_ent[kWarps][kEntMax];       // pos << 16 | XOR value
+  __shared__ uint4 s_bits[kWarps][kChunk / 128];    // mantissa-only positions, 512 B
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  uint32_t* ent = s_ent[w];
+  uint32_t* bits = reinterpret_cast<uint32_t*>(s_bits[w]);
+  const uint64_t gwarp = ((uint64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+  const uint64_t nwarps = ((uint64_t)gridDim.x * kThreads) >> 5;
+  uint32_t j = kNone, cur = kNone;
   uint64_t ck = 0;
-  int b = 0;
-  // prologue: the first chunk's old data and slot (the pair's 64 threads hold its 64
-  // 16-byte pieces: the header in piece 0, entries 4 p - 4 .. 4 p - 1 in piece p)
-  uint4 pre = make_uint4(0, 0, 0, 0);
-  uint32_t pre_hdr = 0;
-  if (gpair < total_chunks) {
-    const uint32_t j0 = find_job(chunk_start, k, gpair);
-    issue_chunk(sm->buf[0], jobs[j0].old, jobs[j0].n, (gpair - chunk_start[j0]) * kChunk, pt);
-    pre = reinterpret_cast<const uint4*>(slots + gpair * kSlotBytes)[pt];
-    pre_hdr = *reinterpret_cast<const uint32_t*>(slots + gpair * kSlotBytes);
-  }
-  cp_async_commit();
-  for (uint64_t g = gpair; g < total_chunks; g += npairs, b ^= 1) {
+  for (uint64_t g = gwarp; g < total_chunks; g += nwarps) {
     j = advance_job(chunk_start, k, j, g);
-    const uint4 cur_pre = pre;
-    const uint32_t hdr = pre_hdr;
-    // the next chunk's old data goes into the other buffer, its slot into registers
-    const uint64_t gn = g + npairs;
-    if (gn < total_chunks) {
-      const uint32_t jn = advance_job(chunk_start, k, j, gn);
-      issue_chunk(sm->buf[b ^ 1], jobs[jn].old, jobs[jn].n, (gn - chunk_start[jn]) * kChunk, pt);
-      pre = reinterpret_cast<const uint4*>(slots + gn * kSlotBytes)[pt];
-      pre_hdr = *reinterpret_cast<const uint32_t*>(slots + gn * kSlotBytes);
-    }
-    cp_async_commit();
-    const DJob& J = jobs[j];
-    const uint64_t n = J.n;
-    const uint64_t e0 = (g - chunk_start[j]) * kChunk;
-    // this chunk's copies (every group but the one just issued) must land before its buffer
-    // is read, or reused two iterations later when the chunk is skipped
-    cp_async_wait<1>();
-    pair_sync(pair);
-    if (info[j].status != BD_OK || (hdr & (kSlotOverflow | kSlotBad))) continue;
+    const JobInfo& I = info[j];
+    if (I.status != BD_OK) continue;
     if (j != cur) {
-      if (cur != 0xFFFFFFFFu) {
-        const uint64_t s = warp_sum64(ck);
-        if (lane == 0)
-          atomicAdd(reinterpret_cast<unsigned long long*>(ck_base + (uint64_t)cur * kCkBytes) +
-                        (gwarp & (kCkSlots - 1)) * kCkStride,
-                    (unsigned long long)s);
-      }
+      if (cur != kNone) flush_ck(ck_base, cur, gwarp, ck);
       cur = j;
       ck = 0;
     }
-    const uint32_t kk = (hdr & 0xFFFu) + ((hdr >> 12) & 0xFFFu);  // M + R entries
-    uint32_t* data32 = reinterpret_cast<uint32_t*>(sm->buf[b]);
-    bool taken = false;
-    if (pt > 0) {
-      const uint32_t i0 = 4 * pt - 4;  // entries held in this thread's piece of the slot
-      if (i0 + 0 < kk) taken |= xor_entry(data32, sm->touched, cur_pre.x);
-      if (i0 + 1 < kk) taken |= xor_entry(data32, sm->touched, cur_pre.y);
-      if (i0 + 2 < kk) taken |= xor_entry(data32, sm->touched, cur_pre.z);
-      if (i0 + 3 < kk) taken |= xor_entry(data32, sm->touched, cur_pre.w);
+    const DJob& J = jobs[j];
+    const uint64_t n = J.n, c = g - chunk_start[j], e0 = c * kChunk;
+    const uint32_t L = (n - e0) < kChunk ? (uint32_t)(n - e0) : kChunk;
+    const uint32_t B = (L + 7) >> 3;
+    const uint8_t* __restrict__ payload = J.payload;
+    const uint32_t cnt = reinterpret_cast<const uint32_t*>(payload + kHeader)[c];
+    const uint32_t M = cnt & 0xFFFFu, R = cnt >> 16;
+    if (2 * M >= B || 2 * R >= B) {
+      if (lane == 0) list[atomicAdd(list_count, 1u)] = (uint32_t)g;
+      continue;
     }
-    if (taken) sm->flag = 1;
-    pair_sync(pair);
-    if (sm->flag == 0) {
-      uint16_t* __restrict__ out = J.out;
-      const bool inplace = out == J.old;
-      if (e0 + kChunk <= n) {
-        stream_two_steps<true>(sm->buf[b], sm->touched, 4 * half, e0, n, out, inplace, ck);
-        stream_two_steps<true>(sm->buf[b], sm->touched, 4 * half + 2, e0, n, out, inplace, ck);
-      } else {
-        stream_two_steps<false>(sm->buf[b], sm->touched, 4 * half, e0, n, out, inplace, ck);
-        stream_two_steps<false>(sm->buf[b], sm->touched, 4 * half + 2, e0, n, out, inplace, ck);
+    if (M + R > 0) {
+      const TileSum pre = tile_pre[tile_start[j] + c / kTileChunks];
+      const uint4 lc = loc[g];
+      const uint64_t Pex = pre.p + lc.x, Mex = pre.m + lc.y, Rex = pre.r + lc.z;
+      const uint8_t* mblk = payload + I.p_start + Pex;
+      const uint8_t* rblk = mblk + 2 * M;
+      const uint8_t* ms = payload + I.m_start;
+      const uint8_t* rs = payload + I.r_start + 2 * Rex;
+      const bool both = M > 0 && R > 0;
+      bool bad = false;
+      if (both) s_bits[w][lane] = make_uint4(0, 0, 0, 0);
+      __syncwarp();
+      uint32_t carry = 0;
+      for (uint32_t b0 = 0; b0 < M; b0 += 32) {
+        const uint32_t i = b0 + lane;
+        const bool in = i < M;
+        const uint32_t d = in ? load_u16(mblk + 2 * i) : 0u;
+        if (in && i > 0 && d == 0) bad = true;
+        const uint32_t p = carry + warp_incl_scan(d);
+        carry = __shfl_sync(kFull, p, 31);
+        if (in) {
+          const uint32_t v = mant_value(ms, Mex + i);
+          if (p >= L || v == 0) {
+            bad = true;
+          } else {
+            ent[i] = (p << 16) | v;
+            if (both) atomicOr(&bits[p >> 5], 1u << (p & 31));
+          }
+        }
       }
-    } else if (pt == 0) {
-      record_status(&info[j].chunk_err, BD_ERR_FORMAT);
+      __syncwarp();
+      carry = 0;
+      for (uint32_t b0 = 0; b0 < R; b0 += 32) {
+        const uint32_t i = b0 + lane;
+        const bool in = i < R;
+        const uint32_t d = in ? load_u16(rblk + 2 * i) : 0u;
+        if (in && i > 0 && d == 0) bad = true;
+        const uint32_t p = carry + warp_incl_scan(d);
+        carry = __shfl_sync(kFull, p, 31);
+        if (in) {
+          const uint32_t v = load_u16(rs + 2 * i);
+          if (p >= L || (v & kSignExp) == 0) bad = true;
+          else if (both && ((bits[p >> 5] >> (p & 31)) & 1u)) bad = true;
+          else ent[M + i] = (p << 16) | v;
+        }
+      }
+      if (__any_sync(kFull, bad)) {
+        if (lane == 0) record_status(&info[j].chunk_err, BD_ERR_FORMAT);
+        __syncwarp();
+        continue;
+      }
+      __syncwarp();
+      uint16_t* base = J.out + e0;   // 4-byte aligned: out is 16-byte aligned, e0 % 4096 == 0
+      for (uint32_t i = lane; i < M + R; i += 32) {
+        const uint32_t e = ent[i], p = e >> 16;
+        atomicXor(reinterpret_cast<unsigned int*>(base + (p & ~1u)),
+                  (e & 0xFFFFu) << (16 * (p & 1)));
+      }
+      // every lane's atomics are performed before any lane reads the chunk back
+      __threadfence_block();
+      __syncwarp();
     }
-    pair_sync(pair);
-    sm->touched[2 * pt] = 0;
-    sm->touched[2 * pt + 1] = 0;
-    if (pt == 0) sm->flag = 0;
+    if (e0 + kChunk <= n) ck += hash_chunk<true>(J.out, n, e0);
+    else ck += hash_chunk<false>(J.out, n, e0);
   }
-  cp_async_wait<0>();
-  if (cur != 0xFFFFFFFFu) {
-    const uint64_t s = warp_sum64(ck);
-    if (lane == 0)
-      atomicAdd(reinterpret_cast<unsigned long long*>(ck_base + (uint64_t)cur * kCkBytes) +
-                    (gwarp & (kCkSlots - 1)) * kCkStride,
-                (unsigned long long)s);
+  if (cur != kNone) flush_ck(ck_base, cur, gwarp, ck);
+}
+
+// Out-of-place apply: copies old to out (warp per chunk) for the tensors with out != old.
+__global__ void __launch_bounds__(kThreads)
+k_copy_jobs(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start, uint32_t k,
+            uint64_t total_chunks, const JobInfo* __restrict__ info) {
+  const int lane = threadIdx.x & 31;
+  const uint64_t gwarp = ((uint64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+  const uint64_t nwarps = ((uint64_t)gridDim.x * kThreads) >> 5;
+  uint32_t j = 0xFFFFFFFFu;
+  for (uint64_t g = gwarp; g < total_chunks; g += nwarps) {
+    j = advance_job(chunk_start, k, j, g);
+    const DJob& J = jobs[j];
+    if (J.out == J.old || info[j].status != BD_OK) continue;
+    const uint64_t n = J.n, e0 = (g - chunk_start[j]) * kChunk;
+    for (uint64_t e = e0 + 8 * lane; e < e0 + kChunk && e < n; e += 256) {
+      if (e + 8 <= n) *reinterpret_cast<uint4*>(J.out + e) = __ldcs(reinterpret_cast<const uint4*>(J.old + e));
+      else for (uint64_t i = e; i < n; i++) J.out[i] = J.old[i];
+    }
   }
 }
 
@@ -677,42 +494,30 @@ int blocks_per_sm(K kernel) {
 
 }  // namespace
 
-cudaError_t launch_decode(const LaunchCtx& c) {
+cudaError_t launch_apply_chunks(const LaunchCtx& c) {
   if (c.chunks == 0) return cudaSuccess;
-  static const int per_sm = blocks_per_sm(k_decode);
+  static const int per_sm = blocks_per_sm(k_apply_chunks);
   const uint64_t grid = std::min<uint64_t>((c.chunks + kWarps - 1) / kWarps, (uint64_t)per_sm * c.sms);
-  k_decode<<<(unsigned)grid, kThreads, 0, c.stream>>>(
+  k_apply_chunks<<<(unsigned)grid, kThreads, 0, c.stream>>>(
       reinterpret_cast<const DJob*>(c.ws + c.lay.jobs),
       reinterpret_cast<const uint64_t*>(c.ws + c.lay.chunk_start),
       reinterpret_cast<const uint64_t*>(c.ws + c.lay.tile_start), c.k, c.chunks,
       reinterpret_cast<const uint4*>(c.ws + c.lay.loc),
       reinterpret_cast<const TileSum*>(c.ws + c.lay.tile_pre),
-      reinterpret_cast<JobInfo*>(c.ws + c.lay.info), c.ws + c.lay.slots,
+      reinterpret_cast<JobInfo*>(c.ws + c.lay.info),
       reinterpret_cast<uint32_t*>(c.ws + c.lay.overflow),
-      reinterpret_cast<uint32_t*>(c.ws + c.lay.ovf_list));
+      reinterpret_cast<uint32_t*>(c.ws + c.lay.ovf_list), c.ws + c.lay.ck);
   return cudaGetLastError();
 }
 
-cudaError_t launch_apply_stream(const LaunchCtx& c) {
+cudaError_t launch_copy_jobs(const LaunchCtx& c) {
   if (c.chunks == 0) return cudaSuccess;
-  constexpr size_t smem = kStreamPairs * sizeof(PairSmem);  // ~66 KiB
-  static const int per_sm = [] {
-    if (cudaFuncSetAttribute(k_apply_stream, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
-      return 0;
-    int v = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, k_apply_stream, kStreamThreads, smem) !=
-            cudaSuccess || v < 1)
-      v = 1;
-    return v;
-  }();
-  if (per_sm == 0) return cudaErrorInvalidValue;
-  const uint64_t grid = std::min<uint64_t>((c.chunks + kStreamPairs - 1) / kStreamPairs,
-                                           (uint64_t)per_sm * c.sms);
-  k_apply_stream<<<(unsigned)grid, kStreamThreads, smem, c.stream>>>(
+  static const int per_sm = blocks_per_sm(k_copy_jobs);
+  const uint64_t grid = std::min<uint64_t>((c.chunks + kWarps - 1) / kWarps, (uint64_t)per_sm * c.sms);
+  k_copy_jobs<<<(unsigned)grid, kThreads, 0, c.stream>>>(
       reinterpret_cast<const DJob*>(c.ws + c.lay.jobs),
       reinterpret_cast<const uint64_t*>(c.ws + c.lay.chunk_start), c.k, c.chunks,
-      reinterpret_cast<JobInfo*>(c.ws + c.lay.info), c.ws + c.lay.slots, c.ws + c.lay.ck);
+      reinterpret_cast<const JobInfo*>(c.ws + c.lay.info));
   return cudaGetLastError();
 }
 

@@ -13,11 +13,11 @@
 //                 read again by emit).  The slot also records the chunk's first mantissa value.
 //   emit          one warp per chunk, after the scan: writes the count-table entry, the rare
 //                 stream, the position blocks and the chunk's share of the 7-bit mantissa
-//                 stream, all at their final payload offsets.  A mantissa-stream byte is
-//                 written by the chunk holding the element its first bit belongs to; when the
-//                 byte reaches into the next chunk that has mantissa values, the first of
-//                 them comes from that chunk's slot.  Each warp requests all of a chunk's
-//                 inputs in two rounds (metadata and the first slot entries, then the rest).
+//                 stream, all at their final payload offsets, 32 slot entries at a time with
+//                 the classes split by ballots.  A mantissa-stream byte is written by the
+//                 chunk holding the element its first bit belongs to; when the byte reaches
+//                 into the next chunk that has mantissa values, the first of them comes from
+//                 that chunk's slot.
 //   emit_dense    the same for the chunks listed by encode_slots as too dense for a slot:
 //                 their changes are derived again from old and new.
 #include "bd_internal.cuh"

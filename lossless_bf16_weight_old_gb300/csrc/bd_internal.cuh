@@ -281,8 +281,8 @@ cudaError_t launch_scan_tiles(const LaunchCtx& c, bool decompress);
 cudaError_t launch_scan_jobs(const LaunchCtx& c, bool decompress, int32_t* d_status_all);
 cudaError_t launch_emit(const LaunchCtx& c);
 cudaError_t launch_emit_dense(const LaunchCtx& c);
-cudaError_t launch_decode(const LaunchCtx& c);
-cudaError_t launch_apply_stream(const LaunchCtx& c);
+cudaError_t launch_apply_chunks(const LaunchCtx& c);
+cudaError_t launch_copy_jobs(const LaunchCtx& c);
 cudaError_t launch_apply(const LaunchCtx& c);
 cudaError_t launch_apply_finish(const LaunchCtx& c, int32_t* d_status_all);
 cudaError_t launch_checksum(const uint16_t* w, uint64_t n, uint64_t* out, cudaStream_t s,

@@ -159,6 +159,7 @@ extern "C" int bd_decompress_noalloc(const uint16_t* d_old, uint64_t n, const vo
   if ((rc = check(cudaGetLastError()))) return rc;
   if ((rc = check(launch_scan_tiles(c, true)))) return rc;
   if ((rc = check(launch_scan_jobs(c, true, nullptr)))) return rc;
+  if (d_out != d_old && (rc = check(launch_copy_jobs(c)))) return rc;
   if ((rc = check(launch_apply(c)))) return rc;
   return check(launch_apply_finish(c, d_status));
 }

@@ -62,11 +62,12 @@ def test_workspace_sizes(cuda_lib):
     b = ws(cuda_lib.bd_compress_workspace_size, [1 << 21])
     assert 0 < a < b
     assert a % 256 == 0
-    # both need O(chunks) scratch: a 1 KiB slot plus ~20 bytes per 4096-element chunk
+    # O(chunks) scratch: compress a 1 KiB slot plus ~30 bytes per 4096-element chunk,
+    # decompress ~20 bytes per chunk
     d = ws(cuda_lib.bd_decompress_workspace_size, [1 << 24])
     c = ws(cuda_lib.bd_compress_workspace_size, [1 << 24])
     chunks = (1 << 24) // 4096
-    assert 1024 * chunks < d <= 1100 * chunks + 4096
+    assert 16 * chunks < d <= 32 * chunks + 4096
     assert 1024 * chunks < c <= 1100 * chunks + 4096
     assert ws(cuda_lib.bd_compress_workspace_size, [(1 << 40) + 1]) == 0
     assert ws(cuda_lib.bd_decompress_workspace_size, [1, 2, 3]) > 0
