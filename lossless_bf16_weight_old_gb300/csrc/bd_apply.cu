@@ -324,15 +324,15 @@ __device__ __forceinline__ uint64_t hash_chunk(const uint16_t* w, uint64_t n, ui
   return ck;
 }
 
-// One warp per chunk of every tensor whose scan status is BD_OK.  A chunk whose two position
-// blocks are delta lists is decoded and checked in full into shared memory (positions from
-// the prefix sums of the deltas, 7-bit values from the mantissa stream at bit 7*(M prefix +
-// i), 16-bit values from the rare stream; a position in both classes, a zero delta after the
-// first, a position past the chunk, a zero mantissa value or a rare value without a sign or
-// exponent bit marks the chunk malformed).  A well-formed chunk is then XORed into `out` by
-// one 32-bit atomic XOR per change, performed in L2 without a reply, and read back through
-// L2 for its checksum terms.  Chunks with a bitmap block are listed for apply_dense, which
-// also adds their checksum terms.
+// One warp per chunk of every tensor whose scan status is BD_OK, each warp taking a contiguous
+// range of chunks.  A chunk whose two position blocks are delta lists is decoded and checked
+// in full into shared memory (positions from the prefix sums of the deltas, 7-bit values from
+// the mantissa stream at bit 7*(M prefix + i), 16-bit values from the rare stream; a position
+// in both classes, a zero delta after the first, a position past the chunk, a zero mantissa
+// value or a rare value without a sign or exponent bit marks the chunk malformed).  A
+// well-formed chunk is then XORed into `out` by one 32-bit atomic XOR per change, performed
+// in L2 without a reply, and read back through L2 for its checksum terms.  Chunks with a
+// bitmap block are listed for apply_dense, which also adds their checksum terms.
 __global__ void __launch_bounds__(kThreads, 4)
 k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
                const uint64_t* __restrict__ tile_start, uint32_t k, uint64_t total_chunks,
@@ -348,7 +348,9 @@ k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
   const uint64_t nwarps = ((uint64_t)gridDim.x * kThreads) >> 5;
   uint32_t j = kNone, cur = kNone;
   uint64_t ck = 0;
-  for (uint64_t g = gwarp; g < total_chunks; g += nwarps) {
+  uint64_t g_begin, g_end;
+  warp_range(total_chunks, gwarp, nwarps, g_begin, g_end);
+  for (uint64_t g = g_begin; g < g_end; g++) {
     j = advance_job(chunk_start, k, j, g);
     const JobInfo& I = info[j];
     if (I.status != BD_OK) continue;
@@ -372,10 +374,15 @@ k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
       const TileSum pre = tile_pre[tile_start[j] + c / kTileChunks];
       const uint4 lc = loc[g];
       const uint64_t Pex = pre.p + lc.x, Mex = pre.m + lc.y, Rex = pre.r + lc.z;
-      const uint8_t* mblk = payload + I.p_start + Pex;
-      const uint8_t* rblk = mblk + 2 * M;
-      const uint8_t* ms = payload + I.m_start;
-      const uint8_t* rs = payload + I.r_start + 2 * Rex;
+      // Every position block before a tensor's last chunk has an even length (2k or 512
+      // bytes) and the position section starts at 64 + 4C + 2*sum(R), so both lists and the
+      // rare values are 2-byte aligned.
+      const uint16_t* mlist = reinterpret_cast<const uint16_t*>(payload + I.p_start + Pex);
+      const uint16_t* rlist = mlist + M;
+      const uint16_t* rvals = reinterpret_cast<const uint16_t*>(payload + I.r_start) + Rex;
+      const uint64_t mbit0 = 7 * Mex;
+      const uint8_t* mbytes = payload + I.m_start + (mbit0 >> 3);
+      const uint32_t s0 = (uint32_t)(mbit0 & 7);
       const bool both = M > 0 && R > 0;
       bool bad = false;
       if (both) s_bits[w][lane] = make_uint4(0, 0, 0, 0);
@@ -384,12 +391,15 @@ k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
       for (uint32_t b0 = 0; b0 < M; b0 += 32) {
         const uint32_t i = b0 + lane;
         const bool in = i < M;
-        const uint32_t d = in ? load_u16(mblk + 2 * i) : 0u;
+        const uint32_t d = in ? (uint32_t)mlist[i] : 0u;
         if (in && i > 0 && d == 0) bad = true;
         const uint32_t p = carry + warp_incl_scan(d);
         carry = __shfl_sync(kFull, p, 31);
         if (in) {
-          const uint32_t v = mant_value(ms, Mex + i);
+          const uint32_t bit = s0 + 7 * i, sh = bit & 7;
+          uint32_t v = (uint32_t)mbytes[bit >> 3] >> sh;
+          if (sh > 1) v |= (uint32_t)mbytes[(bit >> 3) + 1] << (8 - sh);
+          v &= kMant;
           if (p >= L || v == 0) {
             bad = true;
           } else {
@@ -403,12 +413,12 @@ k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
       for (uint32_t b0 = 0; b0 < R; b0 += 32) {
         const uint32_t i = b0 + lane;
         const bool in = i < R;
-        const uint32_t d = in ? load_u16(rblk + 2 * i) : 0u;
+        const uint32_t d = in ? (uint32_t)rlist[i] : 0u;
         if (in && i > 0 && d == 0) bad = true;
         const uint32_t p = carry + warp_incl_scan(d);
         carry = __shfl_sync(kFull, p, 31);
         if (in) {
-          const uint32_t v = load_u16(rs + 2 * i);
+          const uint32_t v = rvals[i];
           if (p >= L || (v & kSignExp) == 0) bad = true;
           else if (both && ((bits[p >> 5] >> (p & 31)) & 1u)) bad = true;
           else ent[M + i] = (p << 16) | v;

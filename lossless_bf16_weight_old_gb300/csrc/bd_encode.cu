@@ -159,7 +159,9 @@ k_encode_slots(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
 
   uint32_t j = 0xFFFFFFFFu, cur = 0xFFFFFFFFu;
   uint64_t ck = 0;
-  for (uint64_t g = gwarp; g < total_chunks; g += nwarps) {
+  uint64_t g_begin, g_end;
+  warp_range(total_chunks, gwarp, nwarps, g_begin, g_end);
+  for (uint64_t g = g_begin; g < g_end; g++) {
     j = advance_job(chunk_start, k, j, g);
     if (j != cur) {
       if (cur != 0xFFFFFFFFu) {
@@ -343,7 +345,9 @@ k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
   EmitSmem* sm = &s_em[threadIdx.x >> 5];
 
   uint32_t j = 0xFFFFFFFFu;
-  for (uint64_t g = gwarp; g < total_chunks; g += nwarps) {
+  uint64_t g_begin, g_end;
+  warp_range(total_chunks, gwarp, nwarps, g_begin, g_end);
+  for (uint64_t g = g_begin; g < g_end; g++) {
     j = advance_job(chunk_start, k, j, g);
     // level 1: everything addressed by g and j alone, requested together
     const uint8_t* slot = slots + g * kSlotBytes;

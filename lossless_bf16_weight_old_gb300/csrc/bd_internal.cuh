@@ -230,6 +230,16 @@ __device__ __forceinline__ uint32_t advance_job(const uint64_t* __restrict__ sta
   return find_job(starts, k, g);
 }
 
+// The contiguous range [begin, end) of `total` items that warp `gwarp` of `nwarps` takes:
+// consecutive chunks of one warp read consecutive memory, and its job index and count-table
+// reads advance by one step at a time.
+__device__ __forceinline__ void warp_range(uint64_t total, uint64_t gwarp, uint64_t nwarps,
+                                           uint64_t& begin, uint64_t& end) {
+  const uint64_t per = (total + nwarps - 1) / nwarps;
+  begin = gwarp * per;
+  end = begin + per < total ? begin + per : total;
+}
+
 // Warp-level inclusive scan (sum) of a 32-bit value.
 __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
   const int lane = threadIdx.x & 31;
