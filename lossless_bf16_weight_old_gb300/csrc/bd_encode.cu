@@ -148,7 +148,7 @@ __device__ __forceinline__ void encode_chunk(const uint16_t* __restrict__ old,
   }
 }
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 4)
 k_encode_slots(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
                uint32_t k, uint64_t total_chunks, uint32_t* __restrict__ counts,
                uint8_t* __restrict__ slots, uint8_t* __restrict__ ck_base,
@@ -267,13 +267,15 @@ __device__ __forceinline__ void put_mant_bytes(uint8_t* __restrict__ mout, uint6
                                                uint64_t b_hi, uint64_t Mex, uint32_t M,
                                                uint32_t after, const EmitCtx& cx) {
   const int lane = threadIdx.x & 31;
-  for (uint64_t b = b_lo + lane; b < b_hi; b += 32) {
-    const uint64_t jg = (8 * b) / 7;
-    const uint32_t s = (uint32_t)(8 * b - 7 * jg);
-    const uint32_t jl = (uint32_t)(jg - Mex);
+  // bit offsets relative to the chunk's first mantissa bit 7*Mex fit in 32 bits
+  const uint32_t nb = (uint32_t)(b_hi - b_lo);
+  const uint32_t rel0 = (uint32_t)(8 * b_lo - 7 * Mex);
+  for (uint32_t t = lane; t < nb; t += 32) {
+    const uint32_t rel = rel0 + 8 * t;
+    const uint32_t jl = rel / 7, s = rel - 7 * jl;
     const uint32_t v0 = cx.sm->mv[jl - cx.wbase];
     const uint32_t v1 = (jl + 1 < M) ? cx.sm->mv[jl + 1 - cx.wbase] : after;
-    mout[b] = (uint8_t)((v0 >> s) | (v1 << (7 - s)));
+    mout[b_lo + t] = (uint8_t)((v0 >> s) | (v1 << (7 - s)));
   }
 }
 
@@ -354,14 +356,18 @@ k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
     const uint32_t* E = reinterpret_cast<const uint32_t*>(slot + kSlotHeader);
     const uint32_t hdr = *reinterpret_cast<const uint32_t*>(slot);
     uint32_t ent[8];
+    // the first 96 entries are read with the header (a slot always has room for them); they
+    // cover the whole list of most sparse chunks
     ent[0] = E[lane];
+    ent[1] = E[32 + lane];
+    ent[2] = E[64 + lane];
     const uint4 lc = loc[g];
     const uint64_t c = g - chunk_start[j];
-    const uint64_t g_end = chunk_start[j + 1];
+    const uint64_t g_job_end = chunk_start[j + 1];
     const TileSum pre = tile_pre[tile_start[j] + c / kTileChunks];
-    const uint32_t cnt_next = g + 1 < g_end ? counts[g + 1] : 0u;
+    const uint32_t cnt_next = g + 1 < g_job_end ? counts[g + 1] : 0u;
     const uint32_t aux_next =
-        g + 1 < g_end ? reinterpret_cast<const uint32_t*>(slot + kSlotBytes)[1] : 0u;
+        g + 1 < g_job_end ? reinterpret_cast<const uint32_t*>(slot + kSlotBytes)[1] : 0u;
     const JobInfo I = info[j];
     uint8_t* payload = jobs[j].payload;
     const uint64_t n = jobs[j].n;
@@ -370,7 +376,7 @@ k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
     // level 2: the rest of the list
     const uint32_t M = hdr & 0xFFFu, R = (hdr >> 12) & 0xFFFu, kk = M + R;
 #pragma unroll
-    for (int q = 1; q < 8; q++) {
+    for (int q = 3; q < 8; q++) {
       const uint32_t i = 32 * q + lane;
       ent[q] = i < kk ? E[i] : 0u;
     }
@@ -428,7 +434,7 @@ k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
       uint32_t after = 0;
       const uint64_t jg_last = (8 * (b_hi - 1)) / 7;
       if (jg_last + 1 == Mex + M && Mex + M < I.sum_m)
-        after = next_mant_value(g, g_end, cnt_next, aux_next, counts, slots);
+        after = next_mant_value(g, g_job_end, cnt_next, aux_next, counts, slots);
       put_mant_bytes(payload + I.m_start, b_lo, b_hi, Mex, M, after, cx);
     }
     if (!cx.listM || !cx.listR) {
@@ -464,7 +470,7 @@ k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
     const CJob& J = jobs[j];
     const uint64_t n = J.n;
     const uint64_t c = g - chunk_start[j];
-    const uint64_t g_end = chunk_start[j + 1];
+    const uint64_t g_job_end = chunk_start[j + 1];
     const uint64_t e0 = c * kChunk;
     const uint32_t L = (n - e0) < kChunk ? (uint32_t)(n - e0) : kChunk;
     const uint32_t B = (L + 7) >> 3;
@@ -516,10 +522,10 @@ k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
       uint32_t after = 0;
       const uint64_t jg_last = (8 * (b_hi - 1)) / 7;
       if (jg_last + 1 == Mex + M && Mex + M < I.sum_m) {
-        const uint32_t cnt_next = g + 1 < g_end ? counts[g + 1] : 0u;
+        const uint32_t cnt_next = g + 1 < g_job_end ? counts[g + 1] : 0u;
         const uint32_t aux_next =
-            g + 1 < g_end ? reinterpret_cast<const uint32_t*>(slots + (g + 1) * kSlotBytes)[1] : 0u;
-        after = next_mant_value(g, g_end, cnt_next, aux_next, counts, slots);
+            g + 1 < g_job_end ? reinterpret_cast<const uint32_t*>(slots + (g + 1) * kSlotBytes)[1] : 0u;
+        after = next_mant_value(g, g_job_end, cnt_next, aux_next, counts, slots);
       }
       put_mant_bytes(mout, b_next, b_hi, Mex, M, after, cx);
     }

@@ -1,0 +1,116 @@
+"""Parity at full size on the 7B-shaped dense checkpoint and the 30B-shaped MoE checkpoint, in
+the launch configuration the benchmark times: one batched compress over every tensor of the
+checkpoint (held in one flat buffer per checkpoint, tensors at 256-byte aligned offsets), then
+one batched in-place apply on a copy of old.
+
+The oracle checks a sample of tensors one by one (payload bytes, size, checksum; integer work,
+tolerance 0).  Every tensor is checked by properties that hold at any size: each status is OK,
+the restored checkpoint equals new bit for bit, and applying the same payloads again with the
+checksums of old restores old exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from tests.gpu_util import oracle_pair
+
+pytestmark = pytest.mark.gpu
+
+bd = pytest.importorskip("lossless_bf16_weight_old_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    bd._lib.load()
+
+
+def _flat(specs, dev):
+    ns = [s.numel for s in specs]
+    offs, o = [], 0
+    for n in ns:
+        offs.append(o)
+        o += (n + 127) // 128 * 128
+    O = torch.empty(o, dtype=torch.bfloat16, device=dev)
+    N = torch.empty(o, dtype=torch.bfloat16, device=dev)
+    for s, off, n in zip(specs, offs, ns):
+        a, b = W.make_pair(s, device=dev)
+        O[off:off + n].copy_(a.reshape(-1))
+        N[off:off + n].copy_(b.reshape(-1))
+        del a, b
+    return O, N, offs, ns
+
+
+def _cap_estimate(spec) -> int:
+    """Generous payload room for a tensor with the spec's change rate (not a bound)."""
+    n = spec.numel
+    C = (n + 4095) // 4096
+    lam = spec.rate * 4096
+    per_chunk = 1024 if lam > 100 else int(6 * lam) + 256
+    return min(bd.compress_bound(n), 64 + 4 * C + per_chunk * C + int(3 * spec.rate * n) + 4096)
+
+
+def _check_workload(specs, sample):
+    dev = torch.device("cuda")
+    O, N, offs, ns = _flat(specs, dev)
+    olds = [O[off:off + n] for off, n in zip(offs, ns)]
+    news = [N[off:off + n] for off, n in zip(offs, ns)]
+    # payload room from the change rate (the worst-case bound of a 30B checkpoint would not fit
+    # beside it); a tensor that needs more reports its size and the batch is run again
+    caps = [_cap_estimate(s) for s in specs]
+    comp = bd.CompressBatch(olds, news, caps)
+    comp.run()
+    torch.cuda.synchronize()
+    if int(comp.status.item()) == bd.ERR_CAPACITY:
+        need = [int(v) for v in comp.sizes.tolist()]
+        del comp
+        comp = bd.CompressBatch(olds, news, need)
+        comp.run()
+        torch.cuda.synchronize()
+    assert int(comp.status.item()) == bd.OK
+    sizes = [int(v) for v in comp.sizes.tolist()]
+    cks = bd.u64(comp.checksums)
+
+    # sampled tensors against the oracle, byte for byte
+    for i in sample:
+        ref, ref_ck = oracle_pair(olds[i], news[i])
+        assert sizes[i] == ref.size, specs[i].name
+        assert cks[i] == ref_ck, specs[i].name
+        got = comp.payloads[i][:sizes[i]].cpu().numpy()
+        assert np.array_equal(got, ref), specs[i].name
+
+    # every tensor: in-place apply restores new, applying again with checksum(old) restores old
+    R = O.clone()
+    rolls = [R[off:off + n] for off, n in zip(offs, ns)]
+    fwd = bd.DecompressBatch(rolls, comp.payloads, sizes, comp.checksums)
+    fwd.run()
+    torch.cuda.synchronize()
+    assert int(fwd.status.item()) == bd.OK
+    assert all(int(s) == bd.OK for s in fwd.statuses.tolist())
+    assert torch.equal(R.view(torch.int16), N.view(torch.int16))
+    ck_old = torch.cat([bd.checksum(a).reshape(1) for a in olds])
+    back = bd.DecompressBatch(rolls, comp.payloads, sizes, ck_old)
+    back.run()
+    torch.cuda.synchronize()
+    assert int(back.status.item()) == bd.OK
+    assert torch.equal(R.view(torch.int16), O.view(torch.int16))
+
+
+def test_dense7b_full_size_batched():
+    specs = W.dense7b()
+    names = {s.name: i for i, s in enumerate(specs)}
+    sample = [names[x] for x in ("embed", "layers.0.q", "layers.0.gate", "layers.0.down",
+                                 "layers.0.norm1", "layers.31.up", "norm", "lm_head")]
+    _check_workload(specs, sample)
+
+
+def test_moe30b_full_size_batched():
+    specs = W.moe30b()
+    names = {s.name: i for i, s in enumerate(specs)}
+    hot = max(range(len(specs)), key=lambda i: specs[i].rate)   # a hot expert (bitmap chunks)
+    cold = next(i for i, s in enumerate(specs) if ".experts." in s.name and s.rate < specs[hot].rate)
+    sample = [names["embed"], hot, cold, names["layers.0.q"], names["layers.0.k"],
+              names["layers.47.router"], names["lm_head"]]
+    _check_workload(specs, sample)
