@@ -331,7 +331,9 @@ __device__ __forceinline__ uint64_t hash_chunk(const uint16_t* w, uint64_t n, ui
 // in both classes, a zero delta after the first, a position past the chunk, a zero mantissa
 // value or a rare value without a sign or exponent bit marks the chunk malformed).  A
 // well-formed chunk is then XORed into `out` by one 32-bit atomic XOR per change, performed
-// in L2 without a reply, and read back through L2 for its checksum terms.  Chunks with a
+// in L2 without a reply, and read back through L2 for its checksum terms.  The chunk is
+// prefetched into L2 before the decode starts, so that the atomics and the read-back find it
+// there (prefetching a later chunk instead thrashes L2 and was much slower).  Chunks with a
 // bitmap block are listed for apply_dense, which also adds their checksum terms.
 __global__ void __launch_bounds__(kThreads, 4)
 k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
@@ -370,6 +372,8 @@ k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
       if (lane == 0) list[atomicAdd(list_count, 1u)] = (uint32_t)g;
       continue;
     }
+    if (e0 + kChunk <= n) prefetch_chunk_l2(J.out + e0);   // in L2 by the time it is read
+
     if (M + R > 0) {
       const TileSum pre = tile_pre[tile_start[j] + c / kTileChunks];
       const uint4 lc = loc[g];

@@ -6,11 +6,13 @@
 // separately as one block; the API returns a checksum beside the payload.
 //
 // Two passes around the count scan (bd_scan.cu), neither of which waits on another CTA:
-//   encode_slots  the only full-size read of old and new.  One warp per 4096-element chunk:
-//                 branch-free classification, per-chunk class counts, the checksum of new,
-//                 and the chunk's nonzero XORs (position, value) in a fixed 1 KiB workspace
-//                 slot (a chunk with more changes than a slot holds is marked overflow and is
-//                 read again by emit).  The slot also records the chunk's first mantissa value.
+//   encode_slots  the only full-size read of old and new.  One warp per 4096-element chunk
+//                 (each warp a contiguous range of chunks, each chunk prefetched into L2 as
+//                 the warp starts it): branch-free classification, per-chunk class counts,
+//                 the checksum of new, and the chunk's nonzero XORs (position, value) in a
+//                 fixed 1 KiB workspace slot (a chunk with more changes than a slot holds is
+//                 marked overflow and is read again by emit_dense).  The slot also records the
+//                 chunk's first mantissa value.
 //   emit          one warp per chunk, after the scan: writes the count-table entry, the rare
 //                 stream, the position blocks and the chunk's share of the 7-bit mantissa
 //                 stream, all at their final payload offsets, 32 slot entries at a time with
@@ -174,6 +176,10 @@ k_encode_slots(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
     const uint64_t n = jobs[j].n;
     const uint64_t e0 = (g - chunk_start[j]) * kChunk;
     uint32_t* slot = reinterpret_cast<uint32_t*>(slots + g * kSlotBytes);
+    if (e0 + kChunk <= n) {   // the chunk of old and new into L2 ahead of the step loads
+      prefetch_chunk_l2(jobs[j].old + e0);
+      prefetch_chunk_l2(jobs[j].neu + e0);
+    }
     if (e0 + kChunk <= n)
       encode_chunk<true>(jobs[j].old, jobs[j].neu, n, e0, slot, ck, g, counts, list_count, list);
     else
@@ -402,6 +408,20 @@ k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
       const bool isR = valid && (x & kSignExp);
       const bool isM = valid && !(x & kSignExp);
       const uint32_t bM = __ballot_sync(0xFFFFFFFFu, isM), bR = __ballot_sync(0xFFFFFFFFu, isR);
+      if (bR == 0 && cx.listM) {
+        // no rare entry in this batch: the mantissa-only entries are the first lanes in order
+        const uint32_t prevL = __shfl_up_sync(0xFFFFFFFFu, pos, 1);
+        if (isM) {
+          const uint32_t r = baseM + lane;
+          const uint32_t prev = lane ? prevL : carryM;
+          store_u16(cx.mblk + 2 * r, (uint16_t)(pos - prev));
+          sm->mv[r] = (uint8_t)(x & kMant);
+        }
+        const uint32_t cntM = __popc(bM);
+        carryM = __shfl_sync(0xFFFFFFFFu, pos, cntM - 1);
+        baseM += cntM;
+        continue;
+      }
       const uint32_t lowM = bM & lt, lowR = bR & lt;
       const uint32_t pM = __shfl_sync(0xFFFFFFFFu, pos, lowM ? 31 - __clz(lowM) : lane);
       const uint32_t pR = __shfl_sync(0xFFFFFFFFu, pos, lowR ? 31 - __clz(lowR) : lane);

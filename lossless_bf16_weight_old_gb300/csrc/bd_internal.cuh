@@ -98,6 +98,16 @@ __device__ __forceinline__ uint4 load8_stream(const uint16_t* __restrict__ p, ui
   return load8(p, e, n);
 }
 
+// Asks L2 to fetch the 8 KiB at p (one full 4096-element chunk of BF16 values), one 128-byte
+// line per lane and half, so that the loads of the chunk that follow find it in L2 while the
+// warp is still busy with the chunk's other work.  A hint only: nothing waits for it.
+__device__ __forceinline__ void prefetch_chunk_l2(const uint16_t* p) {
+  const char* c = reinterpret_cast<const char*>(p);
+  const int lane = threadIdx.x & 31;
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(c + 128 * lane));
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(c + 128 * (lane + 32)));
+}
+
 // ---------------------------------------------------------------------------- jobs
 
 // One tensor of a compress call, as the kernels see it (written into the workspace).
