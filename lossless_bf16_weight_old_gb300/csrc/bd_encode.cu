@@ -42,9 +42,14 @@ __device__ __forceinline__ uint4 xor4(uint4 a, uint4 b) {
 
 // 16-bit element-order mask of the nonzero values among the 16 of (x0, x1).
 __device__ __forceinline__ uint32_t nz_mask16(uint4 x0, uint4 x1) {
-  const uint32_t a = flags_to_mask8(nz_flags(x0.x), nz_flags(x0.y), nz_flags(x0.z), nz_flags(x0.w));
-  const uint32_t b = flags_to_mask8(nz_flags(x1.x), nz_flags(x1.y), nz_flags(x1.z), nz_flags(x1.w));
-  return a | (b << 8);
+  // per group: low values' flags at even bits 0..6, high values' at 16..22; the second group's
+  // at 8..14 and 24..30; one fold moves every high value's flag next to its low neighbour
+  const uint32_t ta = (nz_flags(x0.x) >> 15) | (nz_flags(x0.y) >> 13) | (nz_flags(x0.z) >> 11) |
+                      (nz_flags(x0.w) >> 9);
+  const uint32_t tb = (nz_flags(x1.x) >> 7) | (nz_flags(x1.y) >> 5) | (nz_flags(x1.z) >> 3) |
+                      (nz_flags(x1.w) >> 1);
+  const uint32_t u = ta | tb;
+  return (u | (u >> 15)) & 0xFFFFu;
 }
 
 __device__ __forceinline__ uint32_t rare_mask16(uint4 x0, uint4 x1) {
@@ -70,8 +75,10 @@ __device__ __forceinline__ void encode_chunk(const uint16_t* __restrict__ old,
                                              uint64_t& ck, uint64_t g,
                                              uint32_t* __restrict__ counts,
                                              uint32_t* __restrict__ list_count,
-                                             uint32_t* __restrict__ list) {
+                                             uint32_t* __restrict__ list,
+                                             uint4* __restrict__ xs) {
   const int lane = threadIdx.x & 31;
+  const uint16_t* xs16 = reinterpret_cast<const uint16_t*>(xs);
   const uint64_t words = (n + 3) >> 2;
   uint32_t* __restrict__ entries = slot + kSlotHeader / 4;
   uint32_t running = 0;        // changes in the steps done so far
@@ -112,13 +119,17 @@ __device__ __forceinline__ void encode_chunk(const uint16_t* __restrict__ old,
     }
     const uint4 x0 = xor4(po0, pn0), x1 = xor4(po1, pn1);
     const uint32_t nz = nz_mask16(x0, x1);
+    if (nz) {   // the lane's 16 XOR values, read back by position in the loop below
+      xs[0] = x0;
+      xs[1] = x1;
+    }
     const uint32_t cnt = __popc(nz);
     const uint32_t incl = warp_incl_scan(cnt);
     uint32_t idx = running + incl - cnt;
     uint32_t lane_fm = 0;
     for (uint32_t bits = nz; bits; bits &= bits - 1) {
       const int b = __ffs(bits) - 1;
-      const uint32_t xv = elem_of(b < 8 ? x0 : x1, b & 7);
+      const uint32_t xv = xs16[b];
       if (xv & kSignExp) {
         rl++;
       } else if (lane_fm == 0) {
@@ -155,6 +166,7 @@ k_encode_slots(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
                uint32_t k, uint64_t total_chunks, uint32_t* __restrict__ counts,
                uint8_t* __restrict__ slots, uint8_t* __restrict__ ck_base,
                uint32_t* __restrict__ list_count, uint32_t* __restrict__ list) {
+  __shared__ uint4 s_xs[kThreads][2];   // per thread: the 16 XOR values of its current step
   const int lane = threadIdx.x & 31;
   const uint64_t gwarp = ((uint64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
   const uint64_t nwarps = ((uint64_t)gridDim.x * kThreads) >> 5;
@@ -181,9 +193,11 @@ k_encode_slots(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
       prefetch_chunk_l2(jobs[j].neu + e0);
     }
     if (e0 + kChunk <= n)
-      encode_chunk<true>(jobs[j].old, jobs[j].neu, n, e0, slot, ck, g, counts, list_count, list);
+      encode_chunk<true>(jobs[j].old, jobs[j].neu, n, e0, slot, ck, g, counts, list_count, list,
+                         s_xs[threadIdx.x]);
     else
-      encode_chunk<false>(jobs[j].old, jobs[j].neu, n, e0, slot, ck, g, counts, list_count, list);
+      encode_chunk<false>(jobs[j].old, jobs[j].neu, n, e0, slot, ck, g, counts, list_count, list,
+                          s_xs[threadIdx.x]);
   }
   if (cur != 0xFFFFFFFFu) {
     const uint64_t s = warp_sum64(ck);
@@ -382,9 +396,13 @@ k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
     // level 2: the rest of the list
     const uint32_t M = hdr & 0xFFFu, R = (hdr >> 12) & 0xFFFu, kk = M + R;
 #pragma unroll
-    for (int q = 3; q < 8; q++) {
-      const uint32_t i = 32 * q + lane;
-      ent[q] = i < kk ? E[i] : 0u;
+    for (int q = 3; q < 8; q++) ent[q] = 0u;
+    if (kk > 96) {
+#pragma unroll
+      for (int q = 3; q < 8; q++) {
+        const uint32_t i = 32 * q + lane;
+        if (i < kk) ent[q] = E[i];
+      }
     }
 
     const uint64_t e0 = c * kChunk;
@@ -408,13 +426,16 @@ k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
       const bool isR = valid && (x & kSignExp);
       const bool isM = valid && !(x & kSignExp);
       const uint32_t bM = __ballot_sync(0xFFFFFFFFu, isM), bR = __ballot_sync(0xFFFFFFFFu, isR);
+        // (A chunk's M block starts at an even offset: the position section starts at
+      // 64 + 4C + 2*sum(R) and every block before it in the tensor has an even length, so the
+      // delta list is written with plain 2-byte stores.)
       if (bR == 0 && cx.listM) {
         // no rare entry in this batch: the mantissa-only entries are the first lanes in order
         const uint32_t prevL = __shfl_up_sync(0xFFFFFFFFu, pos, 1);
         if (isM) {
           const uint32_t r = baseM + lane;
           const uint32_t prev = lane ? prevL : carryM;
-          store_u16(cx.mblk + 2 * r, (uint16_t)(pos - prev));
+          reinterpret_cast<uint16_t*>(cx.mblk)[r] = (uint16_t)(pos - prev);
           sm->mv[r] = (uint8_t)(x & kMant);
         }
         const uint32_t cntM = __popc(bM);
@@ -428,7 +449,7 @@ k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
       if (isM) {
         const uint32_t r = baseM + __popc(lowM);
         const uint32_t prev = lowM ? pM : carryM;
-        if (cx.listM) store_u16(cx.mblk + 2 * r, (uint16_t)(pos - prev));
+        if (cx.listM) reinterpret_cast<uint16_t*>(cx.mblk)[r] = (uint16_t)(pos - prev);
         else atomicOr(&sm->bm[pos >> 5], 1u << (pos & 31));
         sm->mv[r] = (uint8_t)(x & kMant);
       }
@@ -452,8 +473,10 @@ k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
     const uint64_t b_lo = (7 * Mex + 7) >> 3, b_hi = (7 * (Mex + M) + 7) >> 3;
     if (b_hi > b_lo) {
       uint32_t after = 0;
-      const uint64_t jg_last = (8 * (b_hi - 1)) / 7;
-      if (jg_last + 1 == Mex + M && Mex + M < I.sum_m)
+      // chunk-local value holding the first bit of the last owned byte (32-bit: the offset
+      // from the chunk's first mantissa bit is below 7*M + 8)
+      const uint32_t jl_last = (uint32_t)(8 * (b_hi - 1) - 7 * Mex) / 7;
+      if (jl_last + 1 == M && Mex + M < I.sum_m)
         after = next_mant_value(g, g_job_end, cnt_next, aux_next, counts, slots);
       put_mant_bytes(payload + I.m_start, b_lo, b_hi, Mex, M, after, cx);
     }
