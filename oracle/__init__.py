@@ -44,6 +44,9 @@ def _load():
         lib.orc_encode.restype = ctypes.c_int
         lib.orc_decode.argtypes = [p, u64, p, u64, u64, p]
         lib.orc_decode.restype = ctypes.c_int
+        lib.orc_decode_incremental.argtypes = [p, u64, p, u64, u64, u64, p,
+                                               ctypes.POINTER(u64)]
+        lib.orc_decode_incremental.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -89,3 +92,19 @@ def decode(old, payload, expected_checksum: int) -> tuple[int, np.ndarray]:
                             ctypes.c_uint64(expected_checksum & (2**64 - 1)),
                             out.ctypes.data)
     return int(rc), out
+
+
+def decode_incremental(old, payload, ck_old: int, expected_checksum: int
+                       ) -> tuple[int, np.ndarray, int]:
+    """Incremental verification: returns (status, restored, ck) where ck = ck_old plus the
+    new-minus-old checksum terms of the changed words (ck is 0 when the payload is
+    malformed)."""
+    old = _u16(old)
+    payload = np.ascontiguousarray(payload, dtype=np.uint8).reshape(-1)
+    out = np.empty_like(old)
+    ck = ctypes.c_uint64(0)
+    rc = _load().orc_decode_incremental(old.ctypes.data, old.size, payload.ctypes.data,
+                                        payload.size, ctypes.c_uint64(ck_old & (2**64 - 1)),
+                                        ctypes.c_uint64(expected_checksum & (2**64 - 1)),
+                                        out.ctypes.data, ctypes.byref(ck))
+    return int(rc), out, int(ck.value)

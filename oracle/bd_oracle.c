@@ -264,8 +264,9 @@ int orc_encode(const uint16_t* old, const uint16_t* neu, uint64_t n, uint8_t* ou
 
 /* ---- decode ------------------------------------------------------------------------- */
 
-int orc_decode(const uint16_t* old, uint64_t n, const uint8_t* payload, uint64_t size,
-               uint64_t expected, uint16_t* out) {
+/* Applies payload[0..size) to old into out and checks every format rule; no checksum. */
+static int decode_into(const uint16_t* old, uint64_t n, const uint8_t* payload, uint64_t size,
+                       uint16_t* out) {
   if ((n > 0 && (old == NULL || out == NULL)) || (size > 0 && payload == NULL))
     return ORC_ERR_ARG;
   if (size < ORC_HEADER) return ORC_ERR_FORMAT;
@@ -350,7 +351,41 @@ int orc_decode(const uint16_t* old, uint64_t n, const uint8_t* payload, uint64_t
   for (uint64_t bit = 7 * sum_m; bit < 8 * m_bytes; bit++) {
     if ((payload[m_off + bit / 8] >> (bit % 8)) & 1) return ORC_ERR_FORMAT;
   }
+  return ORC_OK;
+}
 
+int orc_decode(const uint16_t* old, uint64_t n, const uint8_t* payload, uint64_t size,
+               uint64_t expected, uint16_t* out) {
+  int status = decode_into(old, n, payload, size, out);
+  if (status != ORC_OK) return status;
   if (orc_checksum(out, n) != expected) return ORC_ERR_CHECKSUM;
   return ORC_OK;
+}
+
+/* ---- incremental verification -------------------------------------------------------- */
+
+/* Word j of w (elements 4j..4j+3, zero past n), as in the checksum definition. */
+static uint64_t word_of(const uint16_t* w, uint64_t n, uint64_t j) {
+  uint64_t word = 0;
+  for (uint64_t e = 0; e < 4; e++) {
+    uint64_t i = 4 * j + e;
+    if (i < n) word |= (uint64_t)w[i] << (16 * e);
+  }
+  return word;
+}
+
+int orc_decode_incremental(const uint16_t* old, uint64_t n, const uint8_t* payload,
+                           uint64_t size, uint64_t ck_old, uint64_t expected, uint16_t* out,
+                           uint64_t* ck_out) {
+  int status = decode_into(old, n, payload, size, out);
+  if (status != ORC_OK) return status;
+  /* ck_old plus, for every word the payload changed, its new term minus its old term */
+  uint64_t ck = ck_old;
+  uint64_t words = (n + 3) / 4;
+  for (uint64_t j = 0; j < words; j++) {
+    uint64_t wo = word_of(old, n, j), wn = word_of(out, n, j);
+    if (wo != wn) ck += mix64(wn ^ ((j + 1) * GAMMA)) - mix64(wo ^ ((j + 1) * GAMMA));
+  }
+  if (ck_out) *ck_out = ck;
+  return ck == expected ? ORC_OK : ORC_ERR_CHECKSUM;
 }

@@ -53,6 +53,18 @@ int orc_encode(const uint16_t* old, const uint16_t* neu, uint64_t n, uint8_t* ou
 int orc_decode(const uint16_t* old, uint64_t n, const uint8_t* payload, uint64_t size,
                uint64_t expected, uint16_t* out);
 
+/* Incremental verification (not on the pages; the rollout side often knows the checksum of
+ * the weights it holds from its previous verified update).  Decodes like orc_decode (same
+ * format rules), then computes
+ *   ck = ck_old + sum over the words j where out differs from old of
+ *          mix64(out_word_j ^ (j+1)*GAMMA) - mix64(old_word_j ^ (j+1)*GAMMA)   (mod 2^64)
+ * which equals checksum(out) whenever ck_old == checksum(old).  Stores ck in *ck_out (when
+ * not NULL and the payload is well formed) and returns ORC_OK when ck == expected, else
+ * ORC_ERR_CHECKSUM (or ORC_ERR_FORMAT / ORC_ERR_ARG as orc_decode). */
+int orc_decode_incremental(const uint16_t* old, uint64_t n, const uint8_t* payload,
+                           uint64_t size, uint64_t ck_old, uint64_t expected, uint16_t* out,
+                           uint64_t* ck_out);
+
 #ifdef __cplusplus
 }
 #endif
