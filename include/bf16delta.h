@@ -99,6 +99,19 @@ typedef struct bd_decompress_item {
   int32_t* d_status;             /* out (optional): BD_OK, BD_ERR_FORMAT or BD_ERR_CHECKSUM */
 } bd_decompress_item;
 
+/* One tensor of a batched incremental apply (bd_decompress_incremental_batch).  All device
+ * pointers; d_ck_out and d_status may be NULL. */
+typedef struct bd_incremental_item {
+  uint16_t* d_w;                 /* rollout weights, updated in place (n elements) */
+  uint64_t n;                    /* elements */
+  const void* d_payload;         /* payload produced by compress for this tensor */
+  uint64_t size;                 /* payload bytes */
+  const uint64_t* d_ck_old;      /* checksum of d_w before the call */
+  const uint64_t* d_expected;    /* expected checksum of the result (from compress) */
+  uint64_t* d_ck_out;            /* out (optional): the result's checksum, computed as below */
+  int32_t* d_status;             /* out (optional): BD_OK, BD_ERR_FORMAT or BD_ERR_CHECKSUM */
+} bd_incremental_item;
+
 /* Parsed payload header (host side). */
 typedef struct bd_payload_info_t {
   uint64_t n, chunks, n_mant, n_rare, position_bytes, total_size;
@@ -143,6 +156,33 @@ BD_API int bd_decompress(const uint16_t* d_old, uint64_t n, const void* d_payloa
  * the largest status code over the tensors; per-tensor codes go to the items' d_status. */
 BD_API int bd_decompress_batch(const bd_decompress_item* h_items, uint32_t k, void* d_ws,
                         uint64_t ws_bytes, int32_t* d_status, void* stream);
+
+/* In-place apply verified incrementally.  Not on the pages, which verify by checksumming the
+ * restored weights: a rollout process that applies updates one after another already holds
+ * a verified checksum of its current weights (the expected checksum of its previous update),
+ * so the terms of the unchanged words are known and only the changed words need new terms:
+ *   ck = *d_ck_old + sum over the words the payload changes of
+ *          mix64(new_word_j ^ (j+1)*G) - mix64(old_word_j ^ (j+1)*G)     (mod 2^64)
+ * which equals the checksum of the result whenever *d_ck_old is the checksum of d_w before
+ * the call.  The status is BD_OK when ck == *d_expected, else BD_ERR_CHECKSUM (format errors
+ * as bd_decompress); ck goes to *d_ck_out when given.  Only the 32-byte sectors holding
+ * changes are read and written (plus the payload), against a full read of the tensor for
+ * bd_decompress.  What it does not verify: a word of d_w that differs from the trainer's
+ * old copy but is not touched by the payload (bd_decompress's full read catches that).
+ * The workspace is bd_decompress_workspace_size's for the same tensors.  Malformed chunks
+ * are left unwritten; applying the same payload again (with the checksums swapped) undoes
+ * the call. */
+BD_API int bd_decompress_incremental(uint16_t* d_w, uint64_t n, const void* d_payload,
+                                     uint64_t size, const uint64_t* d_ck_old,
+                                     const uint64_t* d_expected, uint64_t* d_ck_out,
+                                     void* d_ws, uint64_t ws_bytes, int32_t* d_status,
+                                     void* stream);
+
+/* Batched bd_decompress_incremental: one launch per phase for k tensors.  *d_status
+ * (required) receives the largest status code over the tensors. */
+BD_API int bd_decompress_incremental_batch(const bd_incremental_item* h_items, uint32_t k,
+                                           void* d_ws, uint64_t ws_bytes, int32_t* d_status,
+                                           void* stream);
 
 /* Largest tensor bd_decompress_noalloc accepts, in elements (2^27 = 128 Mi elements,
  * 256 MiB of BF16), and the size of the device array it uses as scratch. */

@@ -28,8 +28,9 @@ _U64 = (1 << 64) - 1
 
 __all__ = [
     "delta_compress", "delta_decompress", "compress", "decompress", "compress_batch",
-    "decompress_batch", "checksum", "compress_bound", "compress_workspace_size",
-    "decompress_workspace_size", "payload_info", "DeltaError", "status_name",
+    "decompress_batch", "decompress_incremental", "IncrementalBatch", "checksum",
+    "compress_bound", "compress_workspace_size", "decompress_workspace_size", "payload_info",
+    "DeltaError", "status_name",
 ]
 
 
@@ -147,6 +148,28 @@ def decompress(old: torch.Tensor, payload: torch.Tensor, size: int, expected,
     return st
 
 
+def decompress_incremental(w: torch.Tensor, payload: torch.Tensor, size: int, ck_old, expected,
+                           *, workspace: torch.Tensor | None = None, stream=None
+                           ) -> tuple[torch.Tensor, torch.Tensor]:
+    """Applies payload[:size] to w in place, verifying incrementally from ck_old, the checksum
+    of w before the call (see bd_decompress_incremental).  ck_old and expected are ints or
+    int64[1] device tensors.  Returns (int32[1] status, int64[1] computed checksum)."""
+    pw, n = _bits(w, "w")
+    if not isinstance(ck_old, torch.Tensor):
+        ck_old = _u64_tensor([ck_old], w.device)
+    if not isinstance(expected, torch.Tensor):
+        expected = _u64_tensor([expected], w.device)
+    ws = _workspace(decompress_workspace_size([n]), w.device, workspace)
+    st = torch.empty(1, dtype=torch.int32, device=w.device)
+    ck = torch.zeros(1, dtype=torch.int64, device=w.device)
+    rc = _lib.load().bd_decompress_incremental(pw, n, payload.data_ptr(), int(size),
+                                               ck_old.data_ptr(), expected.data_ptr(),
+                                               ck.data_ptr(), ws.data_ptr(), ws.numel(),
+                                               st.data_ptr(), _stream(stream))
+    _check(rc, "bd_decompress_incremental")
+    return st, ck
+
+
 def checksum(w: torch.Tensor, *, stream=None) -> torch.Tensor:
     """Checksum of a BF16 tensor as an int64[1] device tensor (unsigned bits)."""
     pw, n = _bits(w, "w")
@@ -240,6 +263,39 @@ class DecompressBatch:
                                              self.workspace.numel(), self.status.data_ptr(),
                                              _stream(stream))
         _check(rc, "bd_decompress_batch")
+
+
+class IncrementalBatch:
+    """Item table of one batched incremental apply over fixed tensors (in place)."""
+
+    def __init__(self, ws: Sequence[torch.Tensor], payloads: Sequence[torch.Tensor],
+                 sizes: Sequence[int], ck_old: torch.Tensor, expected: torch.Tensor):
+        k = len(ws)
+        dev = ws[0].device
+        ns = [w.numel() for w in ws]
+        self.statuses = torch.zeros(k, dtype=torch.int32, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.checksums = torch.zeros(k, dtype=torch.int64, device=dev)
+        self.workspace = torch.empty(max(decompress_workspace_size(ns), 256),
+                                     dtype=torch.uint8, device=dev)
+        items = (_lib.IncrementalItem * max(1, k))()
+        for i in range(k):
+            items[i].d_w = _bits(ws[i], "w")[0]
+            items[i].n = ns[i]
+            items[i].d_payload = payloads[i].data_ptr()
+            items[i].size = int(sizes[i])
+            items[i].d_ck_old = ck_old.data_ptr() + 8 * i
+            items[i].d_expected = expected.data_ptr() + 8 * i
+            items[i].d_ck_out = self.checksums.data_ptr() + 8 * i
+            items[i].d_status = self.statuses.data_ptr() + 4 * i
+        self._keep = (list(ws), list(payloads), ck_old, expected)
+        self.items, self.k = items, k
+
+    def run(self, stream=None) -> None:
+        rc = _lib.load().bd_decompress_incremental_batch(
+            self.items, self.k, self.workspace.data_ptr(), self.workspace.numel(),
+            self.status.data_ptr(), _stream(stream))
+        _check(rc, "bd_decompress_incremental_batch")
 
 
 def compress_batch(olds, news, caps=None, stream=None) -> CompressBatch:

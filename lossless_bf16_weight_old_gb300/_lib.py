@@ -22,6 +22,11 @@ class DecompressItem(ctypes.Structure):
                 ("size", c_u64), ("d_expected", c_p), ("d_status", c_p)]
 
 
+class IncrementalItem(ctypes.Structure):
+    _fields_ = [("d_w", c_p), ("n", c_u64), ("d_payload", c_p), ("size", c_u64),
+                ("d_ck_old", c_p), ("d_expected", c_p), ("d_ck_out", c_p), ("d_status", c_p)]
+
+
 class PayloadInfo(ctypes.Structure):
     _fields_ = [("n", c_u64), ("chunks", c_u64), ("n_mant", c_u64), ("n_rare", c_u64),
                 ("position_bytes", c_u64), ("total_size", c_u64), ("version", c_u32),
@@ -38,6 +43,9 @@ SIGNATURES = {
     "bd_decompress": (c_int, [c_p, c_u64, c_p, c_u64, c_p, c_p, c_p, c_u64, c_p, c_p]),
     "bd_decompress_batch": (c_int, [c_p, c_u32, c_p, c_u64, c_p, c_p]),
     "bd_decompress_noalloc": (c_int, [c_p, c_u64, c_p, c_u64, c_p, c_p, c_p, c_p]),
+    "bd_decompress_incremental": (c_int, [c_p, c_u64, c_p, c_u64, c_p, c_p, c_p, c_p, c_u64, c_p,
+                                          c_p]),
+    "bd_decompress_incremental_batch": (c_int, [c_p, c_u32, c_p, c_u64, c_p, c_p]),
     "bd_checksum": (c_int, [c_p, c_u64, c_p, c_p]),
     "bd_payload_info": (c_int, [c_p, c_u64, ctypes.POINTER(PayloadInfo)]),
     "bd_status_sync": (c_int, [c_p, c_p]),

@@ -185,21 +185,38 @@ int compress_impl(const bd_compress_item* items, uint32_t k, void* ws, uint64_t 
 }
 
 // ------------------------------------------------------------------------------ decompress
-int decompress_impl(const bd_decompress_item* items, uint32_t k, void* ws, uint64_t ws_bytes,
-                    int32_t* status_all, cudaStream_t s) {
+// One tensor of a decompress call, from either public item type.
+struct DecItem {
+  const uint16_t* old;
+  uint16_t* out;
+  uint64_t n;
+  const void* payload;
+  uint64_t size;
+  const uint64_t* expected;
+  const uint64_t* ck_old;   // incremental verification only
+  uint64_t* ck_out;         // incremental verification only (optional)
+  int32_t* status;
+};
+
+int decompress_impl(const DecItem* items, uint32_t k, void* ws, uint64_t ws_bytes,
+                    int32_t* status_all, cudaStream_t s, bool incremental) {
   if (k > 0 && items == nullptr) return BD_ERR_INVALID_ARG;
   if (!status_all || !aligned(status_all, 4)) return BD_ERR_INVALID_ARG;
   std::vector<uint64_t> ns(k);
   for (uint32_t i = 0; i < k; i++) {
-    const bd_decompress_item& it = items[i];
+    const DecItem& it = items[i];
     if (it.n > BD_MAX_ELEMS) return BD_ERR_INVALID_ARG;
-    if (it.n > 0 && (!it.d_old || !it.d_out || !aligned(it.d_old, 16) || !aligned(it.d_out, 16)))
+    if (it.n > 0 && (!it.old || !it.out || !aligned(it.old, 16) || !aligned(it.out, 16)))
       return BD_ERR_INVALID_ARG;
-    if (it.d_out != it.d_old && overlaps(it.d_out, 2 * it.n, it.d_old, 2 * it.n))
+    if (it.out != it.old && overlaps(it.out, 2 * it.n, it.old, 2 * it.n))
       return BD_ERR_INVALID_ARG;
-    if (it.size > 0 && (!it.d_payload || !aligned(it.d_payload, 16))) return BD_ERR_INVALID_ARG;
-    if (overlaps(it.d_out, 2 * it.n, it.d_payload, it.size)) return BD_ERR_INVALID_ARG;
-    if (!it.d_expected) return BD_ERR_INVALID_ARG;
+    if (it.size > 0 && (!it.payload || !aligned(it.payload, 16))) return BD_ERR_INVALID_ARG;
+    if (overlaps(it.out, 2 * it.n, it.payload, it.size)) return BD_ERR_INVALID_ARG;
+    if (!it.expected || !aligned(it.expected, 8)) return BD_ERR_INVALID_ARG;
+    if (incremental) {
+      if (it.out != it.old || !it.ck_old || !aligned(it.ck_old, 8)) return BD_ERR_INVALID_ARG;
+      if (it.ck_out && !aligned(it.ck_out, 8)) return BD_ERR_INVALID_ARG;
+    }
     ns[i] = it.n;
   }
   Sizes sz;
@@ -207,7 +224,7 @@ int decompress_impl(const bd_decompress_item* items, uint32_t k, void* ws, uint6
   const WsLayout lay = make_layout(k, sz, false);
   if (!ws || !aligned(ws, kAlign) || ws_bytes < lay.total) return BD_ERR_INVALID_ARG;
   for (uint32_t i = 0; i < k; i++)
-    if (overlaps(items[i].d_out, 2 * items[i].n, ws, lay.total)) return BD_ERR_INVALID_ARG;
+    if (overlaps(items[i].out, 2 * items[i].n, ws, lay.total)) return BD_ERR_INVALID_ARG;
   const int sms = sm_count();
   if (sms <= 0) return BD_ERR_CUDA;
 
@@ -218,16 +235,18 @@ int decompress_impl(const bd_decompress_item* items, uint32_t k, void* ws, uint6
   uint64_t cb = 0, tb = 0;
   bool any_out_of_place = false;
   for (uint32_t i = 0; i < k; i++) {
-    const bd_decompress_item& it = items[i];
-    if (it.d_out != it.d_old) any_out_of_place = true;
+    const DecItem& it = items[i];
+    if (it.out != it.old) any_out_of_place = true;
     DJob& J = jobs[i];
-    J.old = it.d_old;
-    J.out = it.d_out;
-    J.payload = static_cast<const uint8_t*>(it.d_payload);
+    J.old = it.old;
+    J.out = it.out;
+    J.payload = static_cast<const uint8_t*>(it.payload);
     J.n = it.n;
     J.size = it.size;
-    J.d_expected = it.d_expected;
-    J.d_status = it.d_status;
+    J.d_expected = it.expected;
+    J.d_status = it.status;
+    J.d_ck_old = incremental ? it.ck_old : nullptr;
+    J.d_ck_out = incremental ? it.ck_out : nullptr;
     J.nchunks = (it.n + kChunk - 1) / kChunk;
     J.chunk_base = cb;
     J.tile_base = tb;
@@ -249,8 +268,12 @@ int decompress_impl(const bd_decompress_item* items, uint32_t k, void* ws, uint6
   if ((rc = check(launch_scan_tiles(c, true)))) return rc;
   if ((rc = check(launch_scan_jobs(c, true, nullptr)))) return rc;
   if (any_out_of_place && (rc = check(launch_copy_jobs(c)))) return rc;
-  if ((rc = check(launch_apply_chunks(c)))) return rc;
-  if ((rc = check(launch_apply(c)))) return rc;
+  if (incremental) {
+    if ((rc = check(launch_apply_incremental(c)))) return rc;
+  } else {
+    if ((rc = check(launch_apply_chunks(c)))) return rc;
+  }
+  if ((rc = check(launch_apply(c, incremental)))) return rc;
   return check(launch_apply_finish(c, status_all));
 }
 
@@ -306,14 +329,44 @@ int bd_compress_batch(const bd_compress_item* h_items, uint32_t k, void* d_ws,
 int bd_decompress(const uint16_t* d_old, uint64_t n, const void* d_payload, uint64_t size,
                   const uint64_t* d_expected, uint16_t* d_out, void* d_ws, uint64_t ws_bytes,
                   int32_t* d_status, void* stream) {
-  bd_decompress_item it{d_old, d_out, n, d_payload, size, d_expected, nullptr};
-  return decompress_impl(&it, 1, d_ws, ws_bytes, d_status, static_cast<cudaStream_t>(stream));
+  DecItem it{d_old, d_out, n, d_payload, size, d_expected, nullptr, nullptr, nullptr};
+  return decompress_impl(&it, 1, d_ws, ws_bytes, d_status, static_cast<cudaStream_t>(stream),
+                         false);
 }
 
 int bd_decompress_batch(const bd_decompress_item* h_items, uint32_t k, void* d_ws,
                         uint64_t ws_bytes, int32_t* d_status, void* stream) {
-  return decompress_impl(h_items, k, d_ws, ws_bytes, d_status,
-                         static_cast<cudaStream_t>(stream));
+  if (k > 0 && !h_items) return BD_ERR_INVALID_ARG;
+  std::vector<DecItem> it(k);
+  for (uint32_t i = 0; i < k; i++) {
+    const bd_decompress_item& x = h_items[i];
+    it[i] = DecItem{x.d_old, x.d_out, x.n, x.d_payload, x.size, x.d_expected, nullptr, nullptr,
+                    x.d_status};
+  }
+  return decompress_impl(it.data(), k, d_ws, ws_bytes, d_status,
+                         static_cast<cudaStream_t>(stream), false);
+}
+
+int bd_decompress_incremental(uint16_t* d_w, uint64_t n, const void* d_payload, uint64_t size,
+                              const uint64_t* d_ck_old, const uint64_t* d_expected,
+                              uint64_t* d_ck_out, void* d_ws, uint64_t ws_bytes,
+                              int32_t* d_status, void* stream) {
+  DecItem it{d_w, d_w, n, d_payload, size, d_expected, d_ck_old, d_ck_out, nullptr};
+  return decompress_impl(&it, 1, d_ws, ws_bytes, d_status, static_cast<cudaStream_t>(stream),
+                         true);
+}
+
+int bd_decompress_incremental_batch(const bd_incremental_item* h_items, uint32_t k, void* d_ws,
+                                    uint64_t ws_bytes, int32_t* d_status, void* stream) {
+  if (k > 0 && !h_items) return BD_ERR_INVALID_ARG;
+  std::vector<DecItem> it(k);
+  for (uint32_t i = 0; i < k; i++) {
+    const bd_incremental_item& x = h_items[i];
+    it[i] = DecItem{x.d_w, x.d_w, x.n, x.d_payload, x.size, x.d_expected, x.d_ck_old,
+                    x.d_ck_out, x.d_status};
+  }
+  return decompress_impl(it.data(), k, d_ws, ws_bytes, d_status,
+                         static_cast<cudaStream_t>(stream), true);
 }
 
 int bd_checksum(const uint16_t* d_w, uint64_t n, uint64_t* d_out, void* stream) {

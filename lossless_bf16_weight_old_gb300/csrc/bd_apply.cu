@@ -55,7 +55,8 @@ __device__ __forceinline__ void flush_ck(uint8_t* ck_base, uint32_t j, uint64_t 
 
 // One CTA per listed chunk (a chunk with a bitmap block): decodes the chunk into an 8 KiB
 // shared XOR mask, applies it, writes the changed 16-byte groups and adds the checksum terms
-// of the result.
+// of the result (INCR: the new-minus-old terms of the changed groups only).
+template <bool INCR>
 __global__ void __launch_bounds__(kThreads)
 k_apply_dense(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
               const uint64_t* __restrict__ tile_start, uint32_t k,
@@ -231,7 +232,12 @@ k_apply_dense(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_
         else for (int i = 0; eb + i < n; i++) out[eb + i] = (uint16_t)elem_of(rb, i);
       }
       const uint64_t words = (n + 3) >> 2;
-      ck += group_hash(ra, ea >> 3, words) + group_hash(rb, eb >> 3, words);
+      if (INCR) {
+        if (cha) ck += group_hash(ra, ea >> 3, words) - group_hash(oa, ea >> 3, words);
+        if (chb) ck += group_hash(rb, eb >> 3, words) - group_hash(ob, eb >> 3, words);
+      } else {
+        ck += group_hash(ra, ea >> 3, words) + group_hash(rb, eb >> 3, words);
+      }
     }
     __syncthreads();
     if (t == 0 && chunk_bad) {
@@ -450,6 +456,150 @@ k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
   if (cur != kNone) flush_ck(ck_base, cur, gwarp, ck);
 }
 
+// Incremental verification, one warp per chunk (each warp a contiguous range of chunks) of
+// every tensor whose scan status is BD_OK.  A chunk whose two position blocks are delta lists
+// is decoded and checked exactly as in apply_chunks; a well-formed chunk then applies each
+// change with a 64-bit atomic XOR that returns the word before it, and adds the word's
+// checksum term after the change minus its term before (elements past n count as zero).
+// Changes to the same word are serialised by the atomics, so their terms telescope to the
+// word's final term minus its original one.  Nothing else of the chunk is read.  Chunks with
+// a bitmap block are listed for apply_dense<true>.
+__global__ void __launch_bounds__(kThreads, 4)
+k_apply_incr(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
+             const uint64_t* __restrict__ tile_start, uint32_t k, uint64_t total_chunks,
+             const uint4* __restrict__ loc, const TileSum* __restrict__ tile_pre,
+             JobInfo* __restrict__ info, uint32_t* __restrict__ list_count,
+             uint32_t* __restrict__ list, uint8_t* __restrict__ ck_base) {
+  __shared__ uint32_t s_ent[kWarps][kEntMax];       // pos << 16 | XOR value
+  __shared__ uint4 s_bits[kWarps][kChunk / 128];    // mantissa-only positions, 512 B
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  uint32_t* ent = s_ent[w];
+  uint32_t* bits = reinterpret_cast<uint32_t*>(s_bits[w]);
+  const uint64_t gwarp = ((uint64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+  const uint64_t nwarps = ((uint64_t)gridDim.x * kThreads) >> 5;
+  uint32_t j = kNone, cur = kNone;
+  uint64_t ck = 0;
+  uint64_t g_begin, g_end;
+  warp_range(total_chunks, gwarp, nwarps, g_begin, g_end);
+  for (uint64_t g = g_begin; g < g_end; g++) {
+    j = advance_job(chunk_start, k, j, g);
+    const JobInfo& I = info[j];
+    if (I.status != BD_OK) continue;
+    if (j != cur) {
+      if (cur != kNone) flush_ck(ck_base, cur, gwarp, ck);
+      cur = j;
+      ck = 0;
+    }
+    const DJob& J = jobs[j];
+    const uint64_t n = J.n, c = g - chunk_start[j], e0 = c * kChunk;
+    const uint32_t L = (n - e0) < kChunk ? (uint32_t)(n - e0) : kChunk;
+    const uint32_t B = (L + 7) >> 3;
+    const uint8_t* __restrict__ payload = J.payload;
+    const uint32_t cnt = reinterpret_cast<const uint32_t*>(payload + kHeader)[c];
+    const uint32_t M = cnt & 0xFFFFu, R = cnt >> 16;
+    if (2 * M >= B || 2 * R >= B) {
+      if (lane == 0) list[atomicAdd(list_count, 1u)] = (uint32_t)g;
+      continue;
+    }
+    if (M + R == 0) continue;
+    const TileSum pre = tile_pre[tile_start[j] + c / kTileChunks];
+    const uint4 lc = loc[g];
+    const uint64_t Pex = pre.p + lc.x, Mex = pre.m + lc.y, Rex = pre.r + lc.z;
+    // both lists and the rare values are 2-byte aligned (see apply_chunks)
+    const uint16_t* mlist = reinterpret_cast<const uint16_t*>(payload + I.p_start + Pex);
+    const uint16_t* rlist = mlist + M;
+    const uint16_t* rvals = reinterpret_cast<const uint16_t*>(payload + I.r_start) + Rex;
+    const uint64_t mbit0 = 7 * Mex;
+    const uint8_t* mbytes = payload + I.m_start + (mbit0 >> 3);
+    const uint32_t s0 = (uint32_t)(mbit0 & 7);
+    const bool both = M > 0 && R > 0;
+    bool bad = false;
+    if (both) s_bits[w][lane] = make_uint4(0, 0, 0, 0);
+    __syncwarp();
+    uint32_t carry = 0;
+    for (uint32_t b0 = 0; b0 < M; b0 += 32) {
+      const uint32_t i = b0 + lane;
+      const bool in = i < M;
+      const uint32_t d = in ? (uint32_t)mlist[i] : 0u;
+      if (in && i > 0 && d == 0) bad = true;
+      const uint32_t p = carry + warp_incl_scan(d);
+      carry = __shfl_sync(kFull, p, 31);
+      if (in) {
+        const uint32_t bit = s0 + 7 * i, sh = bit & 7;
+        uint32_t v = (uint32_t)mbytes[bit >> 3] >> sh;
+        if (sh > 1) v |= (uint32_t)mbytes[(bit >> 3) + 1] << (8 - sh);
+        v &= kMant;
+        if (p >= L || v == 0) {
+          bad = true;
+        } else {
+          ent[i] = (p << 16) | v;
+          if (both) atomicOr(&bits[p >> 5], 1u << (p & 31));
+        }
+      }
+    }
+    __syncwarp();
+    carry = 0;
+    for (uint32_t b0 = 0; b0 < R; b0 += 32) {
+      const uint32_t i = b0 + lane;
+      const bool in = i < R;
+      const uint32_t d = in ? (uint32_t)rlist[i] : 0u;
+      if (in && i > 0 && d == 0) bad = true;
+      const uint32_t p = carry + warp_incl_scan(d);
+      carry = __shfl_sync(kFull, p, 31);
+      if (in) {
+        const uint32_t v = rvals[i];
+        if (p >= L || (v & kSignExp) == 0) bad = true;
+        else if (both && ((bits[p >> 5] >> (p & 31)) & 1u)) bad = true;
+        else ent[M + i] = (p << 16) | v;
+      }
+    }
+    if (__any_sync(kFull, bad)) {
+      if (lane == 0) record_status(&info[j].chunk_err, BD_ERR_FORMAT);
+      __syncwarp();
+      continue;
+    }
+    __syncwarp();
+    // 8-byte aligned: out is 16-byte aligned and e0 % 4096 == 0.  The last word of a tensor
+    // whose n is not a multiple of 4 also covers up to 3 values past n: they are XORed with
+    // zero (the atomic leaves them as they are) and count as zero in the checksum terms.
+    unsigned long long* base = reinterpret_cast<unsigned long long*>(J.out + e0);
+    const uint64_t wlast = (n - 1) >> 2;
+    const uint32_t in_last = (uint32_t)(n - 4 * wlast);   // values of the last word, 1..4
+    const uint64_t last_mask = in_last == 4 ? ~0ull : ((1ull << (16 * in_last)) - 1);
+    // 4 entries per lane per round: their atomics are issued back to back, then the terms
+    for (uint32_t r0 = 0; r0 < M + R; r0 += 128) {
+      uint64_t before[4], dd[4];
+      uint32_t pp[4];
+#pragma unroll
+      for (int u = 0; u < 4; u++) {
+        const uint32_t i = r0 + 32 * u + lane;
+        pp[u] = 0xFFFFFFFFu;
+        if (i < M + R) {
+          const uint32_t e = ent[i], p = e >> 16;
+          pp[u] = p;
+          dd[u] = (uint64_t)(e & 0xFFFFu) << (16 * (p & 3));
+          before[u] = atomicXor(base + (p >> 2), (unsigned long long)dd[u]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; u++) {
+        if (pp[u] != 0xFFFFFFFFu) {
+          uint64_t b = before[u], a = before[u] ^ dd[u];
+          const uint64_t wj = (e0 >> 2) + (pp[u] >> 2);
+          if (wj == wlast) {
+            b &= last_mask;
+            a &= last_mask;
+          }
+          const uint64_t key = (wj + 1) * kGamma;
+          ck += mix64(a ^ key) - mix64(b ^ key);
+        }
+      }
+    }
+    __syncwarp();
+  }
+  if (cur != kNone) flush_ck(ck_base, cur, gwarp, ck);
+}
+
 // Out-of-place apply: copies old to out (warp per chunk) for the tensors with out != old.
 __global__ void __launch_bounds__(kThreads)
 k_copy_jobs(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start, uint32_t k,
@@ -488,9 +638,12 @@ __global__ void k_apply_finish(const DJob* __restrict__ jobs, uint32_t k,
     }
   }
   if (st == BD_OK) {
+    // incremental verification starts from the checksum of out before the call; the slots
+    // then hold the new-minus-old terms of the changed words
     const uint64_t* ck = reinterpret_cast<const uint64_t*>(ck_base + j * kCkBytes);
-    uint64_t sum = 0;
+    uint64_t sum = J.d_ck_old ? *J.d_ck_old : 0;
     for (int s = 0; s < kCkSlots; s++) sum += ck[s * kCkStride];
+    if (J.d_ck_out) *J.d_ck_out = sum;
     if (sum != *J.d_expected) st = BD_ERR_CHECKSUM;
   }
   info[j].status = st;
@@ -535,11 +688,28 @@ cudaError_t launch_copy_jobs(const LaunchCtx& c) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_apply(const LaunchCtx& c) {
+cudaError_t launch_apply_incremental(const LaunchCtx& c) {
   if (c.chunks == 0) return cudaSuccess;
-  static const int per_sm = blocks_per_sm(k_apply_dense);
+  static const int per_sm = blocks_per_sm(k_apply_incr);
+  const uint64_t grid = std::min<uint64_t>((c.chunks + kWarps - 1) / kWarps, (uint64_t)per_sm * c.sms);
+  k_apply_incr<<<(unsigned)grid, kThreads, 0, c.stream>>>(
+      reinterpret_cast<const DJob*>(c.ws + c.lay.jobs),
+      reinterpret_cast<const uint64_t*>(c.ws + c.lay.chunk_start),
+      reinterpret_cast<const uint64_t*>(c.ws + c.lay.tile_start), c.k, c.chunks,
+      reinterpret_cast<const uint4*>(c.ws + c.lay.loc),
+      reinterpret_cast<const TileSum*>(c.ws + c.lay.tile_pre),
+      reinterpret_cast<JobInfo*>(c.ws + c.lay.info),
+      reinterpret_cast<uint32_t*>(c.ws + c.lay.overflow),
+      reinterpret_cast<uint32_t*>(c.ws + c.lay.ovf_list), c.ws + c.lay.ck);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_apply(const LaunchCtx& c, bool incremental) {
+  if (c.chunks == 0) return cudaSuccess;
+  static const int per_sm = blocks_per_sm(k_apply_dense<false>);
   const uint64_t grid = std::min<uint64_t>(c.chunks, (uint64_t)per_sm * c.sms);
-  k_apply_dense<<<(unsigned)grid, kThreads, 0, c.stream>>>(
+  auto kernel = incremental ? k_apply_dense<true> : k_apply_dense<false>;
+  kernel<<<(unsigned)grid, kThreads, 0, c.stream>>>(
       reinterpret_cast<const DJob*>(c.ws + c.lay.jobs),
       reinterpret_cast<const uint64_t*>(c.ws + c.lay.chunk_start),
       reinterpret_cast<const uint64_t*>(c.ws + c.lay.tile_start), c.k,

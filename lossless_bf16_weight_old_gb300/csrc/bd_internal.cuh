@@ -139,7 +139,9 @@ struct DJob {
   uint64_t chunk_base;
   uint64_t nchunks;
   uint64_t tile_base;
-  uint64_t pad[6];
+  const uint64_t* d_ck_old;   // incremental verification: checksum of out before the call
+  uint64_t* d_ck_out;         // incremental verification (optional): the computed checksum
+  uint64_t pad[4];
 };
 static_assert(sizeof(DJob) == 128, "DJob layout");
 
@@ -302,8 +304,9 @@ cudaError_t launch_scan_jobs(const LaunchCtx& c, bool decompress, int32_t* d_sta
 cudaError_t launch_emit(const LaunchCtx& c);
 cudaError_t launch_emit_dense(const LaunchCtx& c);
 cudaError_t launch_apply_chunks(const LaunchCtx& c);
+cudaError_t launch_apply_incremental(const LaunchCtx& c);
 cudaError_t launch_copy_jobs(const LaunchCtx& c);
-cudaError_t launch_apply(const LaunchCtx& c);
+cudaError_t launch_apply(const LaunchCtx& c, bool incremental = false);
 cudaError_t launch_apply_finish(const LaunchCtx& c, int32_t* d_status_all);
 cudaError_t launch_checksum(const uint16_t* w, uint64_t n, uint64_t* out, cudaStream_t s,
                             int sms);

@@ -24,7 +24,7 @@ def _declared() -> set[str]:
 
 def test_library_exports_every_declared_symbol(cuda_lib):
     names = _declared()
-    assert len(names) == 12
+    assert len(names) == 14
     for name in names:
         assert hasattr(cuda_lib, name), name
     out = subprocess.run(["nm", "-D", "--defined-only", _lib.path()], capture_output=True,

@@ -97,6 +97,20 @@ def _check_workload(specs, sample):
     assert int(back.status.item()) == bd.OK
     assert torch.equal(R.view(torch.int16), O.view(torch.int16))
 
+    # incremental verification: forward from the checksums of old, then back from those of new
+    inc = bd.IncrementalBatch(rolls, comp.payloads, sizes, ck_old, comp.checksums)
+    inc.run()
+    torch.cuda.synchronize()
+    assert int(inc.status.item()) == bd.OK
+    assert bd.u64(inc.checksums) == cks
+    assert torch.equal(R.view(torch.int16), N.view(torch.int16))
+    inc_back = bd.IncrementalBatch(rolls, comp.payloads, sizes, comp.checksums, ck_old)
+    inc_back.run()
+    torch.cuda.synchronize()
+    assert int(inc_back.status.item()) == bd.OK
+    assert bd.u64(inc_back.checksums) == bd.u64(ck_old)
+    assert torch.equal(R.view(torch.int16), O.view(torch.int16))
+
 
 def test_dense7b_full_size_batched():
     specs = W.dense7b()
