@@ -30,7 +30,7 @@ __all__ = [
     "delta_compress", "delta_decompress", "compress", "decompress", "compress_batch",
     "decompress_batch", "decompress_incremental", "IncrementalBatch", "checksum",
     "compress_bound", "compress_workspace_size", "decompress_workspace_size", "payload_info",
-    "DeltaError", "status_name",
+    "DeltaError", "status_name", "MappedHostBuffer",
 ]
 
 
@@ -62,6 +62,71 @@ def _bits(t: torch.Tensor, name: str) -> tuple[int, int]:
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     return t.data_ptr(), t.numel()
+
+
+def _addr(payload) -> int:
+    """Device address of a payload: a CUDA uint8 tensor, or an int address the device can read
+    (for example MappedHostBuffer.device_ptr plus an offset)."""
+    if isinstance(payload, torch.Tensor):
+        if not payload.is_cuda:
+            raise ValueError("a payload tensor must be a CUDA tensor; for host memory pass a "
+                             "MappedHostBuffer device address")
+        return payload.data_ptr()
+    return int(payload)
+
+
+_cudart_lib = None
+
+
+def _cudart():
+    """The CUDA runtime library, loaded once (used only for mapped host allocations)."""
+    global _cudart_lib
+    if _cudart_lib is None:
+        for name in ("libcudart.so.13", "/usr/local/cuda/lib64/libcudart.so.13", "libcudart.so"):
+            try:
+                _cudart_lib = ctypes.CDLL(name)
+                break
+            except OSError:
+                continue
+        if _cudart_lib is None:
+            raise RuntimeError("the CUDA runtime library was not found")
+    return _cudart_lib
+
+
+class MappedHostBuffer:
+    """Pinned host memory mapped into the device's address space (cudaHostAlloc with
+    cudaHostAllocMapped).  Kernels read it over the CPU-GPU link through `device_ptr`; host
+    code fills it through `numpy()`.  A payload received into such a buffer can be applied
+    without a separate host-to-device copy: pass `device_ptr + offset` as the payload."""
+
+    _MAPPED = 0x02   # cudaHostAllocMapped
+
+    def __init__(self, nbytes: int):
+        rt = _cudart()
+        self.nbytes = int(nbytes)
+        self._host = ctypes.c_void_p()
+        rc = rt.cudaHostAlloc(ctypes.byref(self._host), ctypes.c_size_t(max(self.nbytes, 1)),
+                              ctypes.c_uint(self._MAPPED))
+        if rc != 0:
+            self._host = None
+            raise RuntimeError(f"cudaHostAlloc failed ({rc})")
+        dev = ctypes.c_void_p()
+        rc = rt.cudaHostGetDevicePointer(ctypes.byref(dev), self._host, ctypes.c_uint(0))
+        if rc != 0:
+            rt.cudaFreeHost(self._host)
+            self._host = None
+            raise RuntimeError(f"cudaHostGetDevicePointer failed ({rc})")
+        self.device_ptr = int(dev.value)
+
+    def numpy(self):
+        import numpy as np
+        buf = (ctypes.c_uint8 * max(self.nbytes, 1)).from_address(self._host.value)
+        return np.frombuffer(buf, dtype=np.uint8, count=self.nbytes)
+
+    def __del__(self):
+        if getattr(self, "_host", None):
+            _cudart().cudaFreeHost(self._host)
+            self._host = None
 
 
 def _u64_tensor(values, device) -> torch.Tensor:
@@ -141,7 +206,7 @@ def decompress(old: torch.Tensor, payload: torch.Tensor, size: int, expected,
         expected = _u64_tensor([expected], old.device)
     ws = _workspace(decompress_workspace_size([n]), old.device, workspace)
     st = torch.empty(1, dtype=torch.int32, device=old.device)
-    rc = _lib.load().bd_decompress(po, n, payload.data_ptr(), int(size), expected.data_ptr(),
+    rc = _lib.load().bd_decompress(po, n, _addr(payload), int(size), expected.data_ptr(),
                                    pout, ws.data_ptr(), ws.numel(), st.data_ptr(),
                                    _stream(stream))
     _check(rc, "bd_decompress")
@@ -162,7 +227,7 @@ def decompress_incremental(w: torch.Tensor, payload: torch.Tensor, size: int, ck
     ws = _workspace(decompress_workspace_size([n]), w.device, workspace)
     st = torch.empty(1, dtype=torch.int32, device=w.device)
     ck = torch.zeros(1, dtype=torch.int64, device=w.device)
-    rc = _lib.load().bd_decompress_incremental(pw, n, payload.data_ptr(), int(size),
+    rc = _lib.load().bd_decompress_incremental(pw, n, _addr(payload), int(size),
                                                ck_old.data_ptr(), expected.data_ptr(),
                                                ck.data_ptr(), ws.data_ptr(), ws.numel(),
                                                st.data_ptr(), _stream(stream))
@@ -246,7 +311,7 @@ class DecompressBatch:
             items[i].d_old = _bits(olds[i], "old")[0]
             items[i].d_out = _bits(outs[i], "out")[0]
             items[i].n = ns[i]
-            items[i].d_payload = payloads[i].data_ptr()
+            items[i].d_payload = _addr(payloads[i])
             items[i].size = int(sizes[i])
             items[i].d_expected = expected.data_ptr() + 8 * i
             items[i].d_status = self.statuses.data_ptr() + 4 * i
@@ -282,7 +347,7 @@ class IncrementalBatch:
         for i in range(k):
             items[i].d_w = _bits(ws[i], "w")[0]
             items[i].n = ns[i]
-            items[i].d_payload = payloads[i].data_ptr()
+            items[i].d_payload = _addr(payloads[i])
             items[i].size = int(sizes[i])
             items[i].d_ck_old = ck_old.data_ptr() + 8 * i
             items[i].d_expected = expected.data_ptr() + 8 * i
