@@ -19,6 +19,7 @@ _SRC = os.path.join(_HERE, "bd_oracle.c")
 _LIB = os.path.join(_HERE, "libbd_oracle.so")
 
 OK, ERR_ARG, ERR_CAPACITY, ERR_FORMAT, ERR_CHECKSUM = 0, 1, 2, 3, 4
+ERR_BASE = 6
 
 _lib = None
 
@@ -42,6 +43,9 @@ def _load():
         lib.orc_checksum.restype = u64
         lib.orc_encode.argtypes = [p, p, u64, p, u64, ctypes.POINTER(u64), ctypes.POINTER(u64)]
         lib.orc_encode.restype = ctypes.c_int
+        lib.orc_encode_versioned.argtypes = [p, p, u64, u64, p, u64, ctypes.POINTER(u64),
+                                             ctypes.POINTER(u64)]
+        lib.orc_encode_versioned.restype = ctypes.c_int
         lib.orc_decode.argtypes = [p, u64, p, u64, u64, p]
         lib.orc_decode.restype = ctypes.c_int
         lib.orc_decode_incremental.argtypes = [p, u64, p, u64, u64, u64, p,
@@ -64,20 +68,27 @@ def checksum(w) -> int:
     return int(_load().orc_checksum(w.ctypes.data, w.size))
 
 
-def encode(old, new) -> tuple[np.ndarray, int]:
-    """Returns (payload bytes as a uint8 array, checksum of new)."""
+def encode(old, new, base: int | None = None) -> tuple[np.ndarray, int]:
+    """Returns (payload bytes as a uint8 array, checksum of new).  With `base` (the checksum of
+    old as the caller knows it) the payload is version 2, bound to that base."""
     old, new = _u16(old), _u16(new)
     if old.size != new.size:
         raise ValueError("old and new must have the same number of elements")
     lib = _load()
     size, ck = ctypes.c_uint64(), ctypes.c_uint64()
-    rc = lib.orc_encode(old.ctypes.data, new.ctypes.data, old.size, None, 0,
-                        ctypes.byref(size), ctypes.byref(ck))
+    if base is None:
+        call = lambda out, cap: lib.orc_encode(old.ctypes.data, new.ctypes.data, old.size, out,
+                                               cap, ctypes.byref(size), ctypes.byref(ck))
+    else:
+        b = ctypes.c_uint64(int(base) & (2**64 - 1))
+        call = lambda out, cap: lib.orc_encode_versioned(old.ctypes.data, new.ctypes.data,
+                                                         old.size, b, out, cap,
+                                                         ctypes.byref(size), ctypes.byref(ck))
+    rc = call(None, 0)
     if rc not in (OK, ERR_CAPACITY):
         raise RuntimeError(f"orc_encode failed with {rc}")
     out = np.zeros(size.value, dtype=np.uint8)
-    rc = lib.orc_encode(old.ctypes.data, new.ctypes.data, old.size, out.ctypes.data,
-                        out.size, ctypes.byref(size), ctypes.byref(ck))
+    rc = call(out.ctypes.data, out.size)
     if rc != OK:
         raise RuntimeError(f"orc_encode failed with {rc}")
     return out, int(ck.value)

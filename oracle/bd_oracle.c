@@ -23,6 +23,11 @@
  *   header (64 bytes) | count table (C x {u16 M_c, u16 R_c}) | R stream (u16 per rare
  *   element) | position section (per chunk: M block then R block) | M stream (7 bits per
  *   mantissa-only element, LSB-first bit packing, pad bits zero)
+ * Version 2 (a payload bound to its base version; not on the pages, which only say that a
+ * joint commit binds the installed weights to the baseline of the next delta): the version-1
+ * header with version 2, followed by u64 base checksum (the checksum of the weights the
+ * payload applies to) and u64 reserved = 0, i.e. an 80-byte header; the sections after it are
+ * the same.
  */
 #include "bd_oracle.h"
 
@@ -30,7 +35,8 @@
 #include <string.h>
 
 #define ORC_CHUNK 4096u
-#define ORC_HEADER 64u
+#define ORC_HEADER 64u      /* version 1 */
+#define ORC_HEADER_V2 80u   /* version 2: + base checksum + reserved */
 
 /* Field masks of a BF16 word: sign bit 15, exponent bits 14..7, mantissa bits 6..0. */
 #define ORC_SIGN_EXP_BITS 0xFF80u
@@ -160,10 +166,12 @@ static int read_block(const uint8_t* src, uint16_t* pos, uint64_t k, uint64_t L)
 
 /* ---- encode ------------------------------------------------------------------------- */
 
-int orc_encode(const uint16_t* old, const uint16_t* neu, uint64_t n, uint8_t* out,
-               uint64_t cap, uint64_t* size_out, uint64_t* checksum_out) {
+static int encode_impl(const uint16_t* old, const uint16_t* neu, uint64_t n, int bound,
+                       uint64_t base, uint8_t* out, uint64_t cap, uint64_t* size_out,
+                       uint64_t* checksum_out) {
   if ((n > 0 && (old == NULL || neu == NULL)) || size_out == NULL || checksum_out == NULL)
     return ORC_ERR_ARG;
+  const uint64_t hdr = bound ? ORC_HEADER_V2 : ORC_HEADER;
   uint64_t C = (n + ORC_CHUNK - 1) / ORC_CHUNK;
 
   /* Steps 1-2: XOR and classify; count each class per chunk. */
@@ -185,7 +193,7 @@ int orc_encode(const uint16_t* old, const uint16_t* neu, uint64_t n, uint8_t* ou
     pos_bytes += block_bytes(mcount[c], L) + block_bytes(rcount[c], L);
   }
   uint64_t m_bytes = (7 * sum_m + 7) / 8;
-  uint64_t size = ORC_HEADER + 4 * C + 2 * sum_r + pos_bytes + m_bytes;
+  uint64_t size = hdr + 4 * C + 2 * sum_r + pos_bytes + m_bytes;
 
   /* Step 6: checksum of the new weights. */
   *size_out = size;
@@ -195,7 +203,7 @@ int orc_encode(const uint16_t* old, const uint16_t* neu, uint64_t n, uint8_t* ou
   memset(out, 0, size);
   /* Header. */
   memcpy(out, "BF16DLT1", 8);
-  put_u32(out + 8, 1);           /* version */
+  put_u32(out + 8, bound ? 2 : 1);   /* version */
   put_u32(out + 12, ORC_CHUNK);  /* chunk_elems */
   put_u64(out + 16, n);
   put_u64(out + 24, C);
@@ -203,14 +211,18 @@ int orc_encode(const uint16_t* old, const uint16_t* neu, uint64_t n, uint8_t* ou
   put_u64(out + 40, sum_r);
   put_u64(out + 48, pos_bytes);
   put_u64(out + 56, size);
+  if (bound) {
+    put_u64(out + 64, base);   /* base checksum */
+    put_u64(out + 72, 0);      /* reserved */
+  }
 
   /* Count table. */
   for (uint64_t c = 0; c < C; c++) {
-    put_u16(out + ORC_HEADER + 4 * c, (uint16_t)mcount[c]);
-    put_u16(out + ORC_HEADER + 4 * c + 2, (uint16_t)rcount[c]);
+    put_u16(out + hdr + 4 * c, (uint16_t)mcount[c]);
+    put_u16(out + hdr + 4 * c + 2, (uint16_t)rcount[c]);
   }
 
-  uint64_t r_off = ORC_HEADER + 4 * C;
+  uint64_t r_off = hdr + 4 * C;
   uint64_t p_off = r_off + 2 * sum_r;
   uint64_t m_off = p_off + pos_bytes;
 
@@ -262,16 +274,33 @@ int orc_encode(const uint16_t* old, const uint16_t* neu, uint64_t n, uint8_t* ou
   return ORC_OK;
 }
 
+int orc_encode(const uint16_t* old, const uint16_t* neu, uint64_t n, uint8_t* out,
+               uint64_t cap, uint64_t* size_out, uint64_t* checksum_out) {
+  return encode_impl(old, neu, n, 0, 0, out, cap, size_out, checksum_out);
+}
+
+int orc_encode_versioned(const uint16_t* old, const uint16_t* neu, uint64_t n, uint64_t base,
+                         uint8_t* out, uint64_t cap, uint64_t* size_out,
+                         uint64_t* checksum_out) {
+  return encode_impl(old, neu, n, 1, base, out, cap, size_out, checksum_out);
+}
+
 /* ---- decode ------------------------------------------------------------------------- */
 
-/* Applies payload[0..size) to old into out and checks every format rule; no checksum. */
+/* Applies payload[0..size) to old into out and checks every format rule; no checksum.  When
+ * required_base is not NULL and the payload is version 2, its base checksum must equal
+ * *required_base (checked after the header and count table, before any chunk is decoded). */
 static int decode_into(const uint16_t* old, uint64_t n, const uint8_t* payload, uint64_t size,
-                       uint16_t* out) {
+                       uint16_t* out, const uint64_t* required_base) {
   if ((n > 0 && (old == NULL || out == NULL)) || (size > 0 && payload == NULL))
     return ORC_ERR_ARG;
   if (size < ORC_HEADER) return ORC_ERR_FORMAT;
   if (memcmp(payload, "BF16DLT1", 8) != 0) return ORC_ERR_FORMAT;
-  if (get_u32(payload + 8) != 1) return ORC_ERR_FORMAT;
+  uint32_t version = get_u32(payload + 8);
+  if (version != 1 && version != 2) return ORC_ERR_FORMAT;
+  const uint64_t hdr = version == 2 ? ORC_HEADER_V2 : ORC_HEADER;
+  if (size < hdr) return ORC_ERR_FORMAT;
+  if (version == 2 && get_u64(payload + 72) != 0) return ORC_ERR_FORMAT;
   if (get_u32(payload + 12) != ORC_CHUNK) return ORC_ERR_FORMAT;
   uint64_t C = (n + ORC_CHUNK - 1) / ORC_CHUNK;
   if (get_u64(payload + 16) != n) return ORC_ERR_FORMAT;
@@ -279,14 +308,14 @@ static int decode_into(const uint16_t* old, uint64_t n, const uint8_t* payload, 
   uint64_t hdr_m = get_u64(payload + 32), hdr_r = get_u64(payload + 40);
   uint64_t hdr_pos = get_u64(payload + 48), hdr_size = get_u64(payload + 56);
   if (hdr_size != size) return ORC_ERR_FORMAT;
-  if ((size - ORC_HEADER) / 4 < C) return ORC_ERR_FORMAT; /* count table must fit */
+  if ((size - hdr) / 4 < C) return ORC_ERR_FORMAT; /* count table must fit */
 
   /* Count table: per-chunk counts, their totals and the closed-form size. */
   uint64_t sum_m = 0, sum_r = 0, pos_bytes = 0;
   for (uint64_t c = 0; c < C; c++) {
     uint64_t L = chunk_len(n, c);
-    uint64_t km = get_u16(payload + ORC_HEADER + 4 * c);
-    uint64_t kr = get_u16(payload + ORC_HEADER + 4 * c + 2);
+    uint64_t km = get_u16(payload + hdr + 4 * c);
+    uint64_t kr = get_u16(payload + hdr + 4 * c + 2);
     if (km + kr > L) return ORC_ERR_FORMAT;
     sum_m += km;
     sum_r += kr;
@@ -294,9 +323,13 @@ static int decode_into(const uint16_t* old, uint64_t n, const uint8_t* payload, 
   }
   if (sum_m != hdr_m || sum_r != hdr_r || pos_bytes != hdr_pos) return ORC_ERR_FORMAT;
   uint64_t m_bytes = (7 * sum_m + 7) / 8;
-  if (ORC_HEADER + 4 * C + 2 * sum_r + pos_bytes + m_bytes != size) return ORC_ERR_FORMAT;
+  if (hdr + 4 * C + 2 * sum_r + pos_bytes + m_bytes != size) return ORC_ERR_FORMAT;
 
-  uint64_t r_off = ORC_HEADER + 4 * C;
+  /* A payload bound to a base version is applied to that version only. */
+  if (version == 2 && required_base != NULL && get_u64(payload + 64) != *required_base)
+    return ORC_ERR_BASE;
+
+  uint64_t r_off = hdr + 4 * C;
   uint64_t p_off = r_off + 2 * sum_r;
   uint64_t m_off = p_off + pos_bytes;
 
@@ -308,8 +341,8 @@ static int decode_into(const uint16_t* old, uint64_t n, const uint8_t* payload, 
   uint64_t mj = 0, rj = 0;
   for (uint64_t c = 0; c < C && status == ORC_OK; c++) {
     uint64_t L = chunk_len(n, c);
-    uint64_t km = get_u16(payload + ORC_HEADER + 4 * c);
-    uint64_t kr = get_u16(payload + ORC_HEADER + 4 * c + 2);
+    uint64_t km = get_u16(payload + hdr + 4 * c);
+    uint64_t kr = get_u16(payload + hdr + 4 * c + 2);
     if (read_block(payload + p_off, mpos, km, L) != 0) { status = ORC_ERR_FORMAT; break; }
     p_off += block_bytes(km, L);
     if (read_block(payload + p_off, rpos, kr, L) != 0) { status = ORC_ERR_FORMAT; break; }
@@ -356,7 +389,7 @@ static int decode_into(const uint16_t* old, uint64_t n, const uint8_t* payload, 
 
 int orc_decode(const uint16_t* old, uint64_t n, const uint8_t* payload, uint64_t size,
                uint64_t expected, uint16_t* out) {
-  int status = decode_into(old, n, payload, size, out);
+  int status = decode_into(old, n, payload, size, out, NULL);
   if (status != ORC_OK) return status;
   if (orc_checksum(out, n) != expected) return ORC_ERR_CHECKSUM;
   return ORC_OK;
@@ -377,7 +410,7 @@ static uint64_t word_of(const uint16_t* w, uint64_t n, uint64_t j) {
 int orc_decode_incremental(const uint16_t* old, uint64_t n, const uint8_t* payload,
                            uint64_t size, uint64_t ck_old, uint64_t expected, uint16_t* out,
                            uint64_t* ck_out) {
-  int status = decode_into(old, n, payload, size, out);
+  int status = decode_into(old, n, payload, size, out, &ck_old);
   if (status != ORC_OK) return status;
   /* ck_old plus, for every word the payload changed, its new term minus its old term */
   uint64_t ck = ck_old;

@@ -34,7 +34,8 @@ enum {
   ORC_ERR_ARG = 1,
   ORC_ERR_CAPACITY = 2,
   ORC_ERR_FORMAT = 3,
-  ORC_ERR_CHECKSUM = 4
+  ORC_ERR_CHECKSUM = 4,
+  ORC_ERR_BASE = 6      /* a version-2 payload applied to weights of another base version */
 };
 
 /* 64-bit checksum of n BF16 words (see bd_oracle.c for the definition). */
@@ -46,7 +47,14 @@ uint64_t orc_checksum(const uint16_t* w, uint64_t n);
 int orc_encode(const uint16_t* old, const uint16_t* neu, uint64_t n, uint8_t* out,
                uint64_t cap, uint64_t* size_out, uint64_t* checksum_out);
 
-/* Decodes payload[0..size) against old (n elements) into out (n elements, must not alias
+/* orc_encode writing a version-2 payload bound to its base version: the 80-byte header
+ * carries `base` (the checksum of old, as the caller knows it) and 8 reserved zero bytes;
+ * everything after the header is as in version 1. */
+int orc_encode_versioned(const uint16_t* old, const uint16_t* neu, uint64_t n, uint64_t base,
+                         uint8_t* out, uint64_t cap, uint64_t* size_out, uint64_t* checksum_out);
+
+/* Decodes payload[0..size) (version 1 or 2; the base of a version-2 payload is not checked
+ * here) against old (n elements) into out (n elements, must not alias
  * old), then verifies checksum(out) == expected.  Returns ORC_OK, ORC_ERR_FORMAT (payload
  * is not a canonical BF16DLT1 v1 payload for n elements) or ORC_ERR_CHECKSUM.  On an error
  * the contents of out are unspecified. */
@@ -60,7 +68,9 @@ int orc_decode(const uint16_t* old, uint64_t n, const uint8_t* payload, uint64_t
  *          mix64(out_word_j ^ (j+1)*GAMMA) - mix64(old_word_j ^ (j+1)*GAMMA)   (mod 2^64)
  * which equals checksum(out) whenever ck_old == checksum(old).  Stores ck in *ck_out (when
  * not NULL and the payload is well formed) and returns ORC_OK when ck == expected, else
- * ORC_ERR_CHECKSUM (or ORC_ERR_FORMAT / ORC_ERR_ARG as orc_decode). */
+ * ORC_ERR_CHECKSUM (or ORC_ERR_FORMAT / ORC_ERR_ARG as orc_decode).  A version-2 payload whose
+ * base checksum differs from ck_old gives ORC_ERR_BASE (after the header and count table are
+ * checked, before any chunk is decoded). */
 int orc_decode_incremental(const uint16_t* old, uint64_t n, const uint8_t* payload,
                            uint64_t size, uint64_t ck_old, uint64_t expected, uint16_t* out,
                            uint64_t* ck_out);
