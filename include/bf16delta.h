@@ -29,6 +29,10 @@
  * (bit p = bit p%8 of byte p/8).  Elements inside every stream are in ascending position.
  * Header: "BF16DLT1", u32 version=1, u32 chunk_elems=4096, u64 n, u64 C, u64 sum M,
  * u64 sum R, u64 position bytes, u64 total size.
+ * Version 2 (bd_compress_versioned): the same payload with an 80-byte header -- version 2,
+ * the 64 bytes above, then u64 base checksum (the checksum of the weights the payload applies
+ * to) and u64 0 -- so every section starts 16 bytes later.  Every decompress call accepts
+ * both versions.
  * Checksum (returned beside the payload, not stored in it): with word_j the little-endian
  * 64-bit word of elements 4j..4j+3 (zero past n),
  *   checksum = sum_j mix64(word_j ^ (j+1) * 0x9E3779B97F4A7C15)  mod 2^64,
@@ -68,7 +72,9 @@ typedef enum bd_status {
   BD_ERR_CAPACITY = 2,    /* compress: payload larger than the capacity given */
   BD_ERR_FORMAT = 3,      /* decompress: not a canonical BF16DLT1 v1 payload for n elements */
   BD_ERR_CHECKSUM = 4,    /* decompress: checksum of the result differs from the expected */
-  BD_ERR_CUDA = 5         /* a CUDA runtime call or kernel launch failed */
+  BD_ERR_CUDA = 5,        /* a CUDA runtime call or kernel launch failed */
+  BD_ERR_BASE = 6         /* incremental apply: a version-2 payload whose base checksum is not
+                             the checksum of the weights it is applied to */
 } bd_status;
 
 #define BD_CHUNK_ELEMS 4096u
@@ -112,14 +118,15 @@ typedef struct bd_incremental_item {
   int32_t* d_status;             /* out (optional): BD_OK, BD_ERR_FORMAT or BD_ERR_CHECKSUM */
 } bd_incremental_item;
 
-/* Parsed payload header (host side). */
+/* Parsed payload header (host side).  base_checksum is 0 for a version-1 payload. */
 typedef struct bd_payload_info_t {
   uint64_t n, chunks, n_mant, n_rare, position_bytes, total_size;
   uint32_t version, chunk_elems;
+  uint64_t base_checksum;
 } bd_payload_info_t;
 
-/* Largest payload compress can produce for n elements (every chunk at its worst split).
- * Returns 0 for n > BD_MAX_ELEMS. */
+/* Largest payload compress can produce for n elements (every chunk at its worst split, with
+ * the version-2 header).  Returns 0 for n > BD_MAX_ELEMS. */
 BD_API uint64_t bd_compress_bound(uint64_t n);
 
 /* Workspace bytes needed by bd_compress_batch / bd_decompress_batch for k tensors of
@@ -141,6 +148,27 @@ BD_API int bd_compress(const uint16_t* d_old, const uint16_t* d_new, uint64_t n,
  * only.  d_status (optional) receives the largest status code over the tensors. */
 BD_API int bd_compress_batch(const bd_compress_item* h_items, uint32_t k, void* d_ws,
                       uint64_t ws_bytes, int32_t* d_status, void* stream);
+
+/* bd_compress writing a version-2 payload bound to its base version.  Not on the pages: the
+ * NeMo-DCR page binds the installed weights to the baseline of the next delta so that
+ * mismatched versions cannot enter silently.  *d_base_checksum (device, required) is the
+ * checksum of d_old as the caller knows it -- in a steady update loop, the checksum of the
+ * previous update's new weights; it is stored in the header, not recomputed.  The
+ * incremental apply refuses the payload with BD_ERR_BASE when the receiver's checksum of its
+ * weights differs; bd_payload_info exposes the base for a check on the host before a full
+ * apply.  Payload otherwise as bd_compress (16 bytes longer). */
+BD_API int bd_compress_versioned(const uint16_t* d_old, const uint16_t* d_new, uint64_t n,
+                                 void* d_payload, uint64_t cap, void* d_ws, uint64_t ws_bytes,
+                                 uint64_t* d_size, uint64_t* d_checksum,
+                                 const uint64_t* d_base_checksum, int32_t* d_status,
+                                 void* stream);
+
+/* Batched bd_compress_versioned: h_base_checksums[i] (host array of k device pointers, each
+ * required) is the base checksum of item i. */
+BD_API int bd_compress_versioned_batch(const bd_compress_item* h_items,
+                                       const uint64_t* const* h_base_checksums, uint32_t k,
+                                       void* d_ws, uint64_t ws_bytes, int32_t* d_status,
+                                       void* stream);
 
 /* [ARCv3] delta_decompress, [WT] weights_updated = weights_old XOR mask: applies the payload
  * to d_old, writing the result to d_out (d_out == d_old applies in place; any other overlap
@@ -165,7 +193,8 @@ BD_API int bd_decompress_batch(const bd_decompress_item* h_items, uint32_t k, vo
  *          mix64(new_word_j ^ (j+1)*G) - mix64(old_word_j ^ (j+1)*G)     (mod 2^64)
  * which equals the checksum of the result whenever *d_ck_old is the checksum of d_w before
  * the call.  The status is BD_OK when ck == *d_expected, else BD_ERR_CHECKSUM (format errors
- * as bd_decompress); ck goes to *d_ck_out when given.  Only the 32-byte sectors holding
+ * as bd_decompress); ck goes to *d_ck_out when given.  A version-2 payload whose base checksum
+ * differs from *d_ck_old is refused with BD_ERR_BASE and nothing is written.  Only the 32-byte sectors holding
  * changes are read and written (plus the payload), against a full read of the tensor for
  * bd_decompress.  What it does not verify: a word of d_w that differs from the trainer's
  * old copy but is not touched by the payload (bd_decompress's full read catches that).

@@ -20,7 +20,7 @@ import torch
 
 from . import _lib
 
-OK, ERR_INVALID_ARG, ERR_CAPACITY, ERR_FORMAT, ERR_CHECKSUM, ERR_CUDA = range(6)
+OK, ERR_INVALID_ARG, ERR_CAPACITY, ERR_FORMAT, ERR_CHECKSUM, ERR_CUDA, ERR_BASE = range(7)
 FORMAT_NAME = "bf16_xor_v1"
 CHUNK_ELEMS = 4096
 HEADER_BYTES = 64
@@ -169,10 +169,12 @@ def _workspace(nbytes: int, device, workspace) -> torch.Tensor:
 
 
 def compress(old: torch.Tensor, new: torch.Tensor, *, payload: torch.Tensor | None = None,
-             workspace: torch.Tensor | None = None, stream=None):
+             workspace: torch.Tensor | None = None, base_checksum=None, stream=None):
     """Encodes old -> new on the GPU.  Returns device tensors
     (payload uint8[cap], size int64[1], checksum int64[1] (unsigned bits), status int32[1]),
-    all written asynchronously on the stream."""
+    all written asynchronously on the stream.  With base_checksum (an int or int64[1] device
+    tensor: the checksum of old as the caller knows it) the payload is version 2, bound to
+    that base (bd_compress_versioned)."""
     po, n = _bits(old, "old")
     pn, n2 = _bits(new, "new")
     if n != n2:
@@ -184,10 +186,19 @@ def compress(old: torch.Tensor, new: torch.Tensor, *, payload: torch.Tensor | No
     size = torch.empty(1, dtype=torch.int64, device=dev)
     ck = torch.empty(1, dtype=torch.int64, device=dev)
     st = torch.empty(1, dtype=torch.int32, device=dev)
-    rc = _lib.load().bd_compress(po, pn, n, payload.data_ptr(), payload.numel(), ws.data_ptr(),
-                                 ws.numel(), size.data_ptr(), ck.data_ptr(), st.data_ptr(),
-                                 _stream(stream))
-    _check(rc, "bd_compress")
+    if base_checksum is None:
+        rc = _lib.load().bd_compress(po, pn, n, payload.data_ptr(), payload.numel(),
+                                     ws.data_ptr(), ws.numel(), size.data_ptr(), ck.data_ptr(),
+                                     st.data_ptr(), _stream(stream))
+        _check(rc, "bd_compress")
+    else:
+        if not isinstance(base_checksum, torch.Tensor):
+            base_checksum = _u64_tensor([base_checksum], dev)
+        rc = _lib.load().bd_compress_versioned(po, pn, n, payload.data_ptr(), payload.numel(),
+                                               ws.data_ptr(), ws.numel(), size.data_ptr(),
+                                               ck.data_ptr(), base_checksum.data_ptr(),
+                                               st.data_ptr(), _stream(stream))
+        _check(rc, "bd_compress_versioned")
     return payload, size, ck, st
 
 
@@ -247,7 +258,9 @@ class CompressBatch:
     """Device buffers and the C item table of one batched compress over fixed tensors."""
 
     def __init__(self, olds: Sequence[torch.Tensor], news: Sequence[torch.Tensor],
-                 caps: Sequence[int] | None = None):
+                 caps: Sequence[int] | None = None, base_checksums: torch.Tensor | None = None):
+        """base_checksums (int64[k] device tensor, optional): version-2 payloads bound to
+        these base checksums (bd_compress_versioned_batch)."""
         if len(olds) != len(news):
             raise ValueError("olds and news differ in length")
         k = len(olds)
@@ -281,10 +294,20 @@ class CompressBatch:
             items[i].d_size = self.sizes.data_ptr() + 8 * i
             items[i].d_checksum = self.checksums.data_ptr() + 8 * i
             items[i].d_status = self.statuses.data_ptr() + 4 * i
-        self._keep = (list(olds), list(news))
+        self._keep = (list(olds), list(news), base_checksums)
         self.items, self.k = items, k
+        self.bases = None
+        if base_checksums is not None:
+            self.bases = (ctypes.c_void_p * max(1, k))(
+                *[base_checksums.data_ptr() + 8 * i for i in range(k)])
 
     def run(self, stream=None) -> None:
+        if self.bases is not None:
+            rc = _lib.load().bd_compress_versioned_batch(
+                self.items, self.bases, self.k, self.workspace.data_ptr(),
+                self.workspace.numel(), self.status.data_ptr(), _stream(stream))
+            _check(rc, "bd_compress_versioned_batch")
+            return
         rc = _lib.load().bd_compress_batch(self.items, self.k, self.workspace.data_ptr(),
                                            self.workspace.numel(), self.status.data_ptr(),
                                            _stream(stream))

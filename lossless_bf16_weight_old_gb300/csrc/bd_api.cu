@@ -117,9 +117,12 @@ inline bool overlaps(const void* a, uint64_t na, const void* b, uint64_t nb) {
 int check(cudaError_t e) { return e == cudaSuccess ? BD_OK : BD_ERR_CUDA; }
 
 // -------------------------------------------------------------------------------- compress
-int compress_impl(const bd_compress_item* items, uint32_t k, void* ws, uint64_t ws_bytes,
-                  int32_t* status_all, cudaStream_t s) {
+int compress_impl(const bd_compress_item* items, const uint64_t* const* bases, uint32_t k,
+                  void* ws, uint64_t ws_bytes, int32_t* status_all, cudaStream_t s) {
   if (k > 0 && items == nullptr) return BD_ERR_INVALID_ARG;
+  if (bases)
+    for (uint32_t i = 0; i < k; i++)
+      if (!bases[i] || !aligned(bases[i], 8)) return BD_ERR_INVALID_ARG;
   std::vector<uint64_t> ns(k);
   for (uint32_t i = 0; i < k; i++) {
     const bd_compress_item& it = items[i];
@@ -159,6 +162,7 @@ int compress_impl(const bd_compress_item* items, uint32_t k, void* ws, uint64_t 
     J.d_size = it.d_size;
     J.d_checksum = it.d_checksum;
     J.d_status = it.d_status;
+    J.d_base = bases ? bases[i] : nullptr;
     J.nchunks = (it.n + kChunk - 1) / kChunk;
     J.chunk_base = cb;
     J.tile_base = tb;
@@ -297,7 +301,7 @@ uint64_t bd_compress_bound(uint64_t n) {
   const uint64_t bitmaps = full * kChunkBitmap + (tail + 7) / 8;
   // per chunk: 2 bytes per R element + 7/8 byte per M element <= 2 bytes per element, and
   // at most two bitmaps of position bytes; one byte of M-stream rounding
-  return kHeader + 4 * C + 2 * n + 2 * bitmaps + 1;
+  return kHeaderV2 + 4 * C + 2 * n + 2 * bitmaps + 1;
 }
 
 uint64_t bd_compress_workspace_size(const uint64_t* h_n, uint32_t k) {
@@ -318,12 +322,32 @@ int bd_compress(const uint16_t* d_old, const uint16_t* d_new, uint64_t n, void* 
                 uint64_t cap, void* d_ws, uint64_t ws_bytes, uint64_t* d_size,
                 uint64_t* d_checksum, int32_t* d_status, void* stream) {
   bd_compress_item it{d_old, d_new, n, d_payload, cap, d_size, d_checksum, nullptr};
-  return compress_impl(&it, 1, d_ws, ws_bytes, d_status, static_cast<cudaStream_t>(stream));
+  return compress_impl(&it, nullptr, 1, d_ws, ws_bytes, d_status,
+                       static_cast<cudaStream_t>(stream));
 }
 
 int bd_compress_batch(const bd_compress_item* h_items, uint32_t k, void* d_ws,
                       uint64_t ws_bytes, int32_t* d_status, void* stream) {
-  return compress_impl(h_items, k, d_ws, ws_bytes, d_status, static_cast<cudaStream_t>(stream));
+  return compress_impl(h_items, nullptr, k, d_ws, ws_bytes, d_status,
+                       static_cast<cudaStream_t>(stream));
+}
+
+int bd_compress_versioned(const uint16_t* d_old, const uint16_t* d_new, uint64_t n,
+                          void* d_payload, uint64_t cap, void* d_ws, uint64_t ws_bytes,
+                          uint64_t* d_size, uint64_t* d_checksum,
+                          const uint64_t* d_base_checksum, int32_t* d_status, void* stream) {
+  bd_compress_item it{d_old, d_new, n, d_payload, cap, d_size, d_checksum, nullptr};
+  const uint64_t* bases[1] = {d_base_checksum};
+  return compress_impl(&it, bases, 1, d_ws, ws_bytes, d_status,
+                       static_cast<cudaStream_t>(stream));
+}
+
+int bd_compress_versioned_batch(const bd_compress_item* h_items,
+                                const uint64_t* const* h_base_checksums, uint32_t k, void* d_ws,
+                                uint64_t ws_bytes, int32_t* d_status, void* stream) {
+  if (k > 0 && !h_base_checksums) return BD_ERR_INVALID_ARG;
+  return compress_impl(h_items, h_base_checksums, k, d_ws, ws_bytes, d_status,
+                       static_cast<cudaStream_t>(stream));
 }
 
 int bd_decompress(const uint16_t* d_old, uint64_t n, const void* d_payload, uint64_t size,
@@ -390,11 +414,19 @@ int bd_payload_info(const void* h_header, uint64_t bytes, bd_payload_info_t* out
   I.n_rare = le64(p + 40);
   I.position_bytes = le64(p + 48);
   I.total_size = le64(p + 56);
-  if (I.version != 1 || I.chunk_elems != kChunk || I.n > BD_MAX_ELEMS) return BD_ERR_FORMAT;
+  I.base_checksum = 0;
+  if ((I.version != 1 && I.version != 2) || I.chunk_elems != kChunk || I.n > BD_MAX_ELEMS)
+    return BD_ERR_FORMAT;
+  const uint64_t hdr = I.version == 2 ? kHeaderV2 : kHeader;
+  if (I.version == 2) {
+    if (bytes < kHeaderV2) return BD_ERR_INVALID_ARG;
+    I.base_checksum = le64(p + 64);
+    if (le64(p + 72) != 0) return BD_ERR_FORMAT;
+  }
   if (I.chunks != (I.n + kChunk - 1) / kChunk) return BD_ERR_FORMAT;
   if (I.n_mant > I.n || I.n_rare > I.n - I.n_mant) return BD_ERR_FORMAT;
   if (I.position_bytes > 2 * (uint64_t)kChunkBitmap * I.chunks) return BD_ERR_FORMAT;
-  const uint64_t want = kHeader + 4 * I.chunks + 2 * I.n_rare + I.position_bytes +
+  const uint64_t want = hdr + 4 * I.chunks + 2 * I.n_rare + I.position_bytes +
                         (7 * I.n_mant + 7) / 8;
   if (want != I.total_size) return BD_ERR_FORMAT;
   *out = I;
@@ -418,6 +450,7 @@ const char* bd_status_string(int code) {
     case BD_ERR_FORMAT: return "malformed payload";
     case BD_ERR_CHECKSUM: return "checksum mismatch";
     case BD_ERR_CUDA: return "CUDA error";
+    case BD_ERR_BASE: return "payload bound to another base version";
     default: return "unknown status";
   }
 }

@@ -93,7 +93,8 @@ k_apply_dense(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_
     const uint32_t L = (n - e0) < kChunk ? (uint32_t)(n - e0) : kChunk;
     const uint32_t B = (L + 7) >> 3;
     const uint8_t* __restrict__ payload = J.payload;
-    const uint32_t cnt = reinterpret_cast<const uint32_t*>(payload + kHeader)[c];
+    const uint32_t cnt = reinterpret_cast<const uint32_t*>(
+        payload + count_table_offset(info[j].r_start, J.nchunks))[c];
     const uint32_t M = cnt & 0xFFFFu, R = cnt >> 16;
     const TileSum pre = tile_pre[tile_start[j] + c / kTileChunks];
     const uint4 lc = loc[g];
@@ -279,11 +280,11 @@ __device__ __forceinline__ uint4 load8_l2(const uint16_t* p, uint64_t e, uint64_
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Checksum terms of one chunk of w (elements e0 .. e0+4095, clipped at n), one warp: two
-// 512-element steps at a time per lane, so eight independent hash chains per lane, with the
+// Checksum terms of one chunk of w (elements e0 .. e0+4095, clipped at n; used for the last,
+// partial chunk of a tensor), one warp: two 512-element steps at a time per lane, with the
 // next two steps' loads in flight.
 template <bool FULL>
-__device__ __forceinline__ uint64_t hash_chunk(const uint16_t* w, uint64_t n, uint64_t e0) {
+__device__ __forceinline__ uint64_t hash_chunk_r(const uint16_t* w, uint64_t n, uint64_t e0) {
   const int lane = threadIdx.x & 31;
   const uint64_t words = (n + 3) >> 2;
   uint64_t ck = 0;
@@ -330,6 +331,34 @@ __device__ __forceinline__ uint64_t hash_chunk(const uint16_t* w, uint64_t n, ui
   return ck;
 }
 
+// Checksum terms of one full chunk, one warp: the lane's 16 loads (its 8 KiB share of the
+// chunk, 256 bytes) are all issued before the first term is formed.  The chunk was prefetched
+// into L2, so the whole read-back costs one L2 round trip; this needs 76 registers, i.e. three
+// blocks per SM, which measured faster than four blocks with two steps in flight.
+template <bool FULL>
+__device__ __forceinline__ uint64_t hash_chunk(const uint16_t* w, uint64_t n, uint64_t e0) {
+  if (!FULL) return hash_chunk_r<false>(w, n, e0);
+  const int lane = threadIdx.x & 31;
+  const uint64_t e = e0 + 16 * lane;
+  uint4 v[16];
+#pragma unroll
+  for (int s = 0; s < 8; s++) {
+    v[2 * s] = ld_l2(w + e + 512 * s);
+    v[2 * s + 1] = ld_l2(w + e + 512 * s + 8);
+  }
+  uint64_t key = ((e >> 2) + 1) * kGamma, ck = 0;
+#pragma unroll
+  for (int s = 0; s < 8; s++) {
+    const uint4 c0 = v[2 * s], c1 = v[2 * s + 1];
+    ck += mix64(((uint64_t)c0.x | ((uint64_t)c0.y << 32)) ^ key) +
+          mix64(((uint64_t)c0.z | ((uint64_t)c0.w << 32)) ^ (key + kGamma)) +
+          mix64(((uint64_t)c1.x | ((uint64_t)c1.y << 32)) ^ (key + 2 * kGamma)) +
+          mix64(((uint64_t)c1.z | ((uint64_t)c1.w << 32)) ^ (key + 3 * kGamma));
+    key += 128 * kGamma;
+  }
+  return ck;
+}
+
 // One warp per chunk of every tensor whose scan status is BD_OK, each warp taking a contiguous
 // range of chunks.  A chunk whose two position blocks are delta lists is decoded and checked
 // in full into shared memory (positions from the prefix sums of the deltas, 7-bit values from
@@ -341,7 +370,7 @@ __device__ __forceinline__ uint64_t hash_chunk(const uint16_t* w, uint64_t n, ui
 // prefetched into L2 before the decode starts, so that the atomics and the read-back find it
 // there (prefetching a later chunk instead thrashes L2 and was much slower).  Chunks with a
 // bitmap block are listed for apply_dense, which also adds their checksum terms.
-__global__ void __launch_bounds__(kThreads, 4)
+__global__ void __launch_bounds__(kThreads, 3)
 k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
                const uint64_t* __restrict__ tile_start, uint32_t k, uint64_t total_chunks,
                const uint4* __restrict__ loc, const TileSum* __restrict__ tile_pre,
@@ -372,7 +401,8 @@ k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
     const uint32_t L = (n - e0) < kChunk ? (uint32_t)(n - e0) : kChunk;
     const uint32_t B = (L + 7) >> 3;
     const uint8_t* __restrict__ payload = J.payload;
-    const uint32_t cnt = reinterpret_cast<const uint32_t*>(payload + kHeader)[c];
+    const uint32_t cnt = reinterpret_cast<const uint32_t*>(
+        payload + count_table_offset(info[j].r_start, J.nchunks))[c];
     const uint32_t M = cnt & 0xFFFFu, R = cnt >> 16;
     if (2 * M >= B || 2 * R >= B) {
       if (lane == 0) list[atomicAdd(list_count, 1u)] = (uint32_t)g;
@@ -495,7 +525,8 @@ k_apply_incr(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
     const uint32_t L = (n - e0) < kChunk ? (uint32_t)(n - e0) : kChunk;
     const uint32_t B = (L + 7) >> 3;
     const uint8_t* __restrict__ payload = J.payload;
-    const uint32_t cnt = reinterpret_cast<const uint32_t*>(payload + kHeader)[c];
+    const uint32_t cnt = reinterpret_cast<const uint32_t*>(
+        payload + count_table_offset(info[j].r_start, J.nchunks))[c];
     const uint32_t M = cnt & 0xFFFFu, R = cnt >> 16;
     if (2 * M >= B || 2 * R >= B) {
       if (lane == 0) list[atomicAdd(list_count, 1u)] = (uint32_t)g;

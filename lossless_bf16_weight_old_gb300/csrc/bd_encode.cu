@@ -410,7 +410,9 @@ k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
     const uint32_t B = (L + 7) >> 3;
     const uint32_t cnt = M | (R << 16);
     const uint64_t Pex = pre.p + lc.x, Mex = pre.m + lc.y, Rex = pre.r + lc.z;
-    if (lane == 0) reinterpret_cast<uint32_t*>(payload + kHeader)[c] = cnt;
+    if (lane == 0)
+      reinterpret_cast<uint32_t*>(payload + count_table_offset(I.r_start, jobs[j].nchunks))[c] =
+          cnt;
     EmitCtx cx;
     emit_ctx(cx, payload, I, cnt, B, Pex, Rex, sm);
     if (!cx.listM || !cx.listR) {
@@ -523,7 +525,9 @@ k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
     const uint4 lc = loc[g];
     const uint64_t Pex = pre.p + lc.x, Mex = pre.m + lc.y, Rex = pre.r + lc.z;
     uint8_t* payload = J.payload;
-    if (lane == 0) reinterpret_cast<uint32_t*>(payload + kHeader)[c] = cnt;
+    if (lane == 0)
+      reinterpret_cast<uint32_t*>(payload + count_table_offset(I.r_start, jobs[j].nchunks))[c] =
+          cnt;
     EmitCtx cx;
     emit_ctx(cx, payload, I, cnt, B, Pex, Rex, sm);
     if (!cx.listM || !cx.listR) {

@@ -16,7 +16,15 @@ namespace bd {
 // ---------------------------------------------------------------------------- format
 constexpr uint32_t kChunk = 4096;          // elements per chunk
 constexpr uint32_t kChunkBitmap = 512;     // bitmap bytes of a full chunk
-constexpr uint32_t kHeader = 64;           // header bytes
+constexpr uint32_t kHeader = 64;           // header bytes, version 1
+constexpr uint32_t kHeaderV2 = 80;         // version 2: + base checksum + reserved u64
+
+// Count table of a tensor's payload: it ends where the R stream starts (r_start, known once
+// the scan has run), so its place does not depend on the header version.
+__host__ __device__ __forceinline__ uint64_t count_table_offset(uint64_t r_start,
+                                                                uint64_t nchunks) {
+  return r_start - 4 * nchunks;
+}
 constexpr uint16_t kSignExp = 0xFF80;      // sign + exponent field of a BF16 word
 constexpr uint16_t kMant = 0x007F;         // mantissa field
 constexpr uint64_t kGamma = 0x9E3779B97F4A7C15ull;
@@ -123,7 +131,8 @@ struct CJob {
   uint64_t chunk_base;  // global index of this tensor's chunk 0
   uint64_t nchunks;     // C = ceil(n / 4096)
   uint64_t tile_base;   // global index of this tensor's first scan tile
-  uint64_t pad[5];
+  const uint64_t* d_base;   // version 2: the base checksum to bind to (NULL: version 1)
+  uint64_t pad[4];
 };
 static_assert(sizeof(CJob) == 128, "CJob layout");
 

@@ -54,11 +54,15 @@ k_scan_tiles(const void* __restrict__ jobs, const uint64_t* __restrict__ tile_st
     const uint64_t c1 = min(c0 + kTileChunks, J.nchunks);
     const uint32_t* cnt;
     if (DEC) {
-      if (J.size < kHeader + 4 * J.nchunks) {  // count table not inside the payload
+      // the header length follows the version (checked again with the whole header in
+      // scan_jobs); the count table must lie inside the payload
+      const uint32_t version = J.size >= 16 ? reinterpret_cast<const uint32_t*>(J.payload)[2] : 0;
+      const uint64_t hdr = version == 2 ? kHeaderV2 : kHeader;
+      if (J.size < hdr + 4 * J.nchunks) {
         if (t == 0) record_status(&info[j].status, BD_ERR_FORMAT);
         continue;
       }
-      cnt = reinterpret_cast<const uint32_t*>(J.payload + kHeader);
+      cnt = reinterpret_cast<const uint32_t*>(J.payload + hdr);
     } else {
       cnt = counts_ws + J.chunk_base;
     }
@@ -146,7 +150,7 @@ k_scan_jobs(const void* __restrict__ jobs, const uint64_t* __restrict__ tile_sta
     I.chunk_err = 0;
     if (!DEC) {
       const CJob& J = reinterpret_cast<const CJob*>(jobs)[j];
-      I.r_start = kHeader + 4 * J.nchunks;
+      I.r_start = (J.d_base ? kHeaderV2 : kHeader) + 4 * J.nchunks;
       I.p_start = I.r_start + 2 * rR;
       I.m_start = I.p_start + rP;
       I.total = I.m_start + (7 * rM + 7) / 8;
@@ -159,13 +163,17 @@ k_scan_jobs(const void* __restrict__ jobs, const uint64_t* __restrict__ tile_sta
       if (I.status == BD_OK) {
         uint64_t* h = reinterpret_cast<uint64_t*>(J.payload);
         h[0] = kMagic;
-        h[1] = 1ull | ((uint64_t)kChunk << 32);
+        h[1] = (J.d_base ? 2ull : 1ull) | ((uint64_t)kChunk << 32);
         h[2] = J.n;
         h[3] = J.nchunks;
         h[4] = rM;
         h[5] = rR;
         h[6] = rP;
         h[7] = I.total;
+        if (J.d_base) {   // version 2: the base this payload applies to, and a reserved zero
+          h[8] = *J.d_base;
+          h[9] = 0;
+        }
       }
       if (J.d_status) *J.d_status = I.status;
       info[j] = I;
@@ -173,18 +181,24 @@ k_scan_jobs(const void* __restrict__ jobs, const uint64_t* __restrict__ tile_sta
     } else {
       const DJob& J = reinterpret_cast<const DJob*>(jobs)[j];
       int32_t st = info[j].status;
-      I.r_start = kHeader + 4 * J.nchunks;
+      const uint32_t version = J.size >= 16 ? reinterpret_cast<const uint32_t*>(J.payload)[2] : 0;
+      const uint64_t hdr = version == 2 ? kHeaderV2 : kHeader;
+      I.r_start = hdr + 4 * J.nchunks;
       I.p_start = I.r_start + 2 * rR;
       I.m_start = I.p_start + rP;
       I.total = I.m_start + (7 * rM + 7) / 8;
-      if (J.size < kHeader) {
+      if (J.size < hdr) {
         st = BD_ERR_FORMAT;
       } else if (st == BD_OK) {
         const uint64_t* h = reinterpret_cast<const uint64_t*>(J.payload);
-        const bool ok = h[0] == kMagic && h[1] == (1ull | ((uint64_t)kChunk << 32)) &&
+        const bool ok = h[0] == kMagic && (version == 1 || version == 2) &&
+                        h[1] == ((uint64_t)version | ((uint64_t)kChunk << 32)) &&
                         h[2] == J.n && h[3] == J.nchunks && h[4] == rM && h[5] == rR &&
-                        h[6] == rP && h[7] == J.size && I.total == J.size;
+                        h[6] == rP && h[7] == J.size && I.total == J.size &&
+                        (version == 1 || h[9] == 0);
         if (!ok) st = BD_ERR_FORMAT;
+        // a payload bound to a base version is applied incrementally to that version only
+        else if (version == 2 && J.d_ck_old && h[8] != *J.d_ck_old) st = BD_ERR_BASE;
       }
       I.status = st;
       info[j] = I;

@@ -24,7 +24,7 @@ def _declared() -> set[str]:
 
 def test_library_exports_every_declared_symbol(cuda_lib):
     names = _declared()
-    assert len(names) == 14
+    assert len(names) == 16
     for name in names:
         assert hasattr(cuda_lib, name), name
     out = subprocess.run(["nm", "-D", "--defined-only", _lib.path()], capture_output=True,
@@ -51,6 +51,8 @@ def test_compress_bound_is_an_upper_bound(cuda_lib):
         for new in cases:
             payload, _ = oracle.encode(old, new)
             assert payload.size <= bound
+            payload2, _ = oracle.encode(old, new, base=12345)   # version 2: 16 bytes longer
+            assert payload2.size == payload.size + 16 <= bound
     assert cuda_lib.bd_compress_bound((1 << 40) + 1) == 0
 
 
@@ -93,6 +95,31 @@ def test_payload_info_parses_oracle_headers(cuda_lib):
         b = (ctypes.c_uint8 * 64).from_buffer_copy(bytes(bad))
         assert cuda_lib.bd_payload_info(b, 64, ctypes.byref(info)) == 3, off
     assert cuda_lib.bd_payload_info(hdr, 63, ctypes.byref(info)) == 1
+
+
+def test_payload_info_parses_version_2_headers(cuda_lib):
+    rng = np.random.default_rng(10)
+    old = rng.integers(0, 1 << 16, 9000).astype(np.uint16)
+    new = old.copy()
+    new[::30] ^= np.uint16(5)
+    base = 0xFEDCBA9876543210
+    payload, _ = oracle.encode(old, new, base=base)
+    info = _lib.PayloadInfo()
+    hdr = (ctypes.c_uint8 * 80).from_buffer_copy(payload[:80].tobytes())
+    assert cuda_lib.bd_payload_info(hdr, 80, ctypes.byref(info)) == 0
+    assert info.version == 2 and info.base_checksum == base
+    assert info.n == 9000 and info.total_size == payload.size
+    # a version-2 header needs all 80 bytes; the reserved word must be zero
+    assert cuda_lib.bd_payload_info(hdr, 64, ctypes.byref(info)) == 1
+    bad = bytearray(payload[:80].tobytes())
+    bad[75] = 1
+    b = (ctypes.c_uint8 * 80).from_buffer_copy(bytes(bad))
+    assert cuda_lib.bd_payload_info(b, 80, ctypes.byref(info)) == 3
+    # a version-1 header reports base 0
+    p1, _ = oracle.encode(old, new)
+    h1 = (ctypes.c_uint8 * 64).from_buffer_copy(p1[:64].tobytes())
+    assert cuda_lib.bd_payload_info(h1, 64, ctypes.byref(info)) == 0
+    assert info.version == 1 and info.base_checksum == 0
 
 
 def test_argument_checks_need_no_gpu(cuda_lib):
