@@ -28,6 +28,18 @@
  * header with version 2, followed by u64 base checksum (the checksum of the weights the
  * payload applies to) and u64 reserved = 0, i.e. an 80-byte header; the sections after it are
  * the same.
+ * Version 3 (compact positions; a byte-aligned code of the position gaps standing in for the
+ * entropy stage of the pages' codecs): the version-2 header with version 3, then
+ *   count table (C x u32) | R stream | X stream (u16 per escaped gap, chunks in order) |
+ *   position section | M stream
+ * Count entry: bit 31 set -- a compact chunk, M in bits 0..8, R in bits 9..17, E (escaped
+ * gaps) in bits 18..26, bits 27..30 zero; bit 31 clear -- M in bits 0..14, R in bits 15..29,
+ * bit 30 zero, blocks exactly as in version 1.  A compact chunk (k = M + R <= 508) has one
+ * merged list of all its changes in ascending position: k gap bytes (g_0 = p_0 + 1,
+ * g_i = p_i - p_{i-1}; the byte is g when g <= 255, else 0 and g is the chunk's next X value)
+ * then ceil(k/8) class bytes (bit i, LSB-first, is 1 when change i is rare; pad bits 0).  The
+ * encoder makes a chunk compact when k <= 508 and k + ceil(k/8) + 2E is smaller than its
+ * version-1 blocks; decoders accept either coding of a chunk.
  */
 #include "bd_oracle.h"
 
@@ -36,7 +48,8 @@
 
 #define ORC_CHUNK 4096u
 #define ORC_HEADER 64u      /* version 1 */
-#define ORC_HEADER_V2 80u   /* version 2: + base checksum + reserved */
+#define ORC_HEADER_V2 80u   /* version 2 and 3: + base checksum + reserved */
+#define ORC_COMPACT_MAX 508u /* version 3: most changes of a compact chunk */
 
 /* Field masks of a BF16 word: sign bit 15, exponent bits 14..7, mantissa bits 6..0. */
 #define ORC_SIGN_EXP_BITS 0xFF80u
@@ -285,6 +298,284 @@ int orc_encode_versioned(const uint16_t* old, const uint16_t* neu, uint64_t n, u
   return encode_impl(old, neu, n, 1, base, out, cap, size_out, checksum_out);
 }
 
+/* ---- version 3: compact positions ---------------------------------------------------- */
+
+#define ORC_COMPACT_FLAG 0x80000000u
+
+/* Escaped gaps of a chunk's merged list (gaps above 255). */
+static uint64_t chunk_escapes(const uint16_t* old, const uint16_t* neu, uint64_t c, uint64_t L) {
+  int64_t prev = -1;
+  uint64_t e = 0;
+  for (uint64_t p = 0; p < L; p++) {
+    uint64_t i = c * ORC_CHUNK + p;
+    if (classify((uint16_t)(old[i] ^ neu[i])) == CLASS_ZERO) continue;
+    if ((int64_t)p - prev > 255) e++;
+    prev = (int64_t)p;
+  }
+  return e;
+}
+
+int orc_encode_compact(const uint16_t* old, const uint16_t* neu, uint64_t n, uint64_t base,
+                       uint8_t* out, uint64_t cap, uint64_t* size_out, uint64_t* checksum_out) {
+  if ((n > 0 && (old == NULL || neu == NULL)) || size_out == NULL || checksum_out == NULL)
+    return ORC_ERR_ARG;
+  uint64_t C = (n + ORC_CHUNK - 1) / ORC_CHUNK;
+
+  /* XOR and classify: per-chunk counts; the coding of each chunk (compact when smaller). */
+  uint64_t* mcount = (uint64_t*)calloc(C ? C : 1, sizeof(uint64_t));
+  uint64_t* rcount = (uint64_t*)calloc(C ? C : 1, sizeof(uint64_t));
+  uint64_t* ecount = (uint64_t*)calloc(C ? C : 1, sizeof(uint64_t));
+  uint8_t* compact = (uint8_t*)calloc(C ? C : 1, 1);
+  if (!mcount || !rcount || !ecount || !compact) {
+    free(mcount); free(rcount); free(ecount); free(compact);
+    return ORC_ERR_ARG;
+  }
+  for (uint64_t i = 0; i < n; i++) {
+    int cls = classify((uint16_t)(old[i] ^ neu[i]));
+    if (cls == CLASS_MANT) mcount[i / ORC_CHUNK]++;
+    if (cls == CLASS_RARE) rcount[i / ORC_CHUNK]++;
+  }
+  uint64_t sum_m = 0, sum_r = 0, sum_e = 0, pos_bytes = 0;
+  for (uint64_t c = 0; c < C; c++) {
+    uint64_t L = chunk_len(n, c), k = mcount[c] + rcount[c];
+    uint64_t plain = block_bytes(mcount[c], L) + block_bytes(rcount[c], L);
+    if (k > 0 && k <= ORC_COMPACT_MAX) {
+      uint64_t e = chunk_escapes(old, neu, c, L);
+      if (k + (k + 7) / 8 + 2 * e < plain) {
+        compact[c] = 1;
+        ecount[c] = e;
+      }
+    }
+    sum_m += mcount[c];
+    sum_r += rcount[c];
+    sum_e += ecount[c];
+    pos_bytes += compact[c] ? k + (k + 7) / 8 : plain;
+  }
+  uint64_t m_bytes = (7 * sum_m + 7) / 8;
+  uint64_t size = ORC_HEADER_V2 + 4 * C + 2 * sum_r + 2 * sum_e + pos_bytes + m_bytes;
+  *size_out = size;
+  *checksum_out = orc_checksum(neu, n);
+  if (out == NULL || cap < size) {
+    free(mcount); free(rcount); free(ecount); free(compact);
+    return ORC_ERR_CAPACITY;
+  }
+
+  memset(out, 0, size);
+  memcpy(out, "BF16DLT1", 8);
+  put_u32(out + 8, 3);
+  put_u32(out + 12, ORC_CHUNK);
+  put_u64(out + 16, n);
+  put_u64(out + 24, C);
+  put_u64(out + 32, sum_m);
+  put_u64(out + 40, sum_r);
+  put_u64(out + 48, pos_bytes);
+  put_u64(out + 56, size);
+  put_u64(out + 64, base);
+  put_u64(out + 72, 0);
+  for (uint64_t c = 0; c < C; c++) {
+    uint32_t v = compact[c] ? ORC_COMPACT_FLAG | (uint32_t)mcount[c] | ((uint32_t)rcount[c] << 9) |
+                                  ((uint32_t)ecount[c] << 18)
+                            : (uint32_t)mcount[c] | ((uint32_t)rcount[c] << 15);
+    put_u32(out + ORC_HEADER_V2 + 4 * c, v);
+  }
+  uint64_t r_off = ORC_HEADER_V2 + 4 * C;
+  uint64_t x_off = r_off + 2 * sum_r;
+  uint64_t p_off = x_off + 2 * sum_e;
+  uint64_t m_off = p_off + pos_bytes;
+
+  /* R stream: every rare change's 16-bit XOR, in position order. */
+  for (uint64_t i = 0; i < n; i++) {
+    uint16_t x = (uint16_t)(old[i] ^ neu[i]);
+    if (classify(x) == CLASS_RARE) { put_u16(out + r_off, x); r_off += 2; }
+  }
+  /* X stream and position blocks, chunk by chunk. */
+  uint16_t* mpos = (uint16_t*)malloc(ORC_CHUNK * sizeof(uint16_t));
+  uint16_t* rpos = (uint16_t*)malloc(ORC_CHUNK * sizeof(uint16_t));
+  for (uint64_t c = 0; c < C; c++) {
+    uint64_t L = chunk_len(n, c), k = mcount[c] + rcount[c];
+    if (compact[c]) {
+      int64_t prev = -1;
+      uint64_t j = 0;
+      for (uint64_t p = 0; p < L; p++) {
+        uint64_t i = c * ORC_CHUNK + p;
+        int cls = classify((uint16_t)(old[i] ^ neu[i]));
+        if (cls == CLASS_ZERO) continue;
+        uint64_t g = (uint64_t)((int64_t)p - prev);
+        if (g > 255) {
+          out[p_off + j] = 0;
+          put_u16(out + x_off, (uint16_t)g);
+          x_off += 2;
+        } else {
+          out[p_off + j] = (uint8_t)g;
+        }
+        if (cls == CLASS_RARE) out[p_off + k + j / 8] |= (uint8_t)(1u << (j % 8));
+        prev = (int64_t)p;
+        j++;
+      }
+      p_off += k + (k + 7) / 8;
+    } else {
+      uint64_t km = 0, kr = 0;
+      for (uint64_t p = 0; p < L; p++) {
+        uint64_t i = c * ORC_CHUNK + p;
+        int cls = classify((uint16_t)(old[i] ^ neu[i]));
+        if (cls == CLASS_MANT) mpos[km++] = (uint16_t)p;
+        if (cls == CLASS_RARE) rpos[kr++] = (uint16_t)p;
+      }
+      write_block(out + p_off, mpos, km, L);
+      p_off += block_bytes(km, L);
+      write_block(out + p_off, rpos, kr, L);
+      p_off += block_bytes(kr, L);
+    }
+  }
+  free(mpos);
+  free(rpos);
+  /* M stream: as in version 1. */
+  uint64_t j = 0;
+  for (uint64_t i = 0; i < n; i++) {
+    uint16_t x = (uint16_t)(old[i] ^ neu[i]);
+    if (classify(x) != CLASS_MANT) continue;
+    for (uint64_t b = 0; b < 7; b++) {
+      uint64_t bit = 7 * j + b;
+      if (((x & ORC_MANT_BITS) >> b) & 1) out[m_off + bit / 8] |= (uint8_t)(1u << (bit % 8));
+    }
+    j++;
+  }
+  free(mcount); free(rcount); free(ecount); free(compact);
+  return ORC_OK;
+}
+
+/* Splits a version-3 count entry; returns -1 when its unused bits are not zero. */
+static int v3_entry(uint32_t v, uint64_t* km, uint64_t* kr, uint64_t* ke, int* is_compact) {
+  *is_compact = (v & ORC_COMPACT_FLAG) != 0;
+  if (*is_compact) {
+    if (v & 0x78000000u) return -1;
+    *km = v & 0x1FF;
+    *kr = (v >> 9) & 0x1FF;
+    *ke = (v >> 18) & 0x1FF;
+    if (*km + *kr == 0 || *km + *kr > ORC_COMPACT_MAX || *ke > *km + *kr) return -1;
+  } else {
+    if (v & 0x40000000u) return -1;
+    *km = v & 0x7FFF;
+    *kr = (v >> 15) & 0x7FFF;
+    *ke = 0;
+  }
+  return 0;
+}
+
+/* The 7-bit value j of the M stream starting at m. */
+static uint16_t mant_at(const uint8_t* m, uint64_t j) {
+  uint16_t v = 0;
+  for (uint64_t b = 0; b < 7; b++) {
+    uint64_t bit = 7 * j + b;
+    v |= (uint16_t)(((m[bit / 8] >> (bit % 8)) & 1) << b);
+  }
+  return v;
+}
+
+/* Decodes a version-3 payload (header fields n, C, version and reserved already checked,
+ * size >= 80) into out; the base is checked against required_base as in decode_into. */
+static int decode_v3(const uint16_t* old, uint64_t n, const uint8_t* payload, uint64_t size,
+                     uint16_t* out, const uint64_t* required_base) {
+  uint64_t C = (n + ORC_CHUNK - 1) / ORC_CHUNK;
+  uint64_t hdr_m = get_u64(payload + 32), hdr_r = get_u64(payload + 40);
+  uint64_t hdr_pos = get_u64(payload + 48), hdr_size = get_u64(payload + 56);
+  if (hdr_size != size) return ORC_ERR_FORMAT;
+  if ((size - ORC_HEADER_V2) / 4 < C) return ORC_ERR_FORMAT;
+  uint64_t sum_m = 0, sum_r = 0, sum_e = 0, pos_bytes = 0;
+  for (uint64_t c = 0; c < C; c++) {
+    uint64_t L = chunk_len(n, c), km, kr, ke;
+    int cmp;
+    if (v3_entry(get_u32(payload + ORC_HEADER_V2 + 4 * c), &km, &kr, &ke, &cmp) != 0)
+      return ORC_ERR_FORMAT;
+    if (km + kr > L) return ORC_ERR_FORMAT;
+    sum_m += km;
+    sum_r += kr;
+    sum_e += ke;
+    pos_bytes += cmp ? km + kr + (km + kr + 7) / 8 : block_bytes(km, L) + block_bytes(kr, L);
+  }
+  if (sum_m != hdr_m || sum_r != hdr_r || pos_bytes != hdr_pos) return ORC_ERR_FORMAT;
+  uint64_t m_bytes = (7 * sum_m + 7) / 8;
+  if (ORC_HEADER_V2 + 4 * C + 2 * sum_r + 2 * sum_e + pos_bytes + m_bytes != size)
+    return ORC_ERR_FORMAT;
+  if (required_base != NULL && get_u64(payload + 64) != *required_base) return ORC_ERR_BASE;
+
+  uint64_t r_off = ORC_HEADER_V2 + 4 * C;
+  uint64_t x_off = r_off + 2 * sum_r;
+  uint64_t p_off = x_off + 2 * sum_e;
+  uint64_t m_off = p_off + pos_bytes;
+  if (n > 0) memcpy(out, old, n * sizeof(uint16_t));
+  uint16_t* mpos = (uint16_t*)malloc(ORC_CHUNK * sizeof(uint16_t));
+  uint16_t* rpos = (uint16_t*)malloc(ORC_CHUNK * sizeof(uint16_t));
+  uint64_t mj = 0, rj = 0, xj = 0;
+  int status = ORC_OK;
+  for (uint64_t c = 0; c < C && status == ORC_OK; c++) {
+    uint64_t L = chunk_len(n, c), km, kr, ke;
+    int cmp;
+    v3_entry(get_u32(payload + ORC_HEADER_V2 + 4 * c), &km, &kr, &ke, &cmp);
+    const uint8_t* blk = payload + p_off;
+    uint64_t nm = 0, nr = 0;
+    if (cmp) {
+      /* the merged list: positions from the gaps, classes from the class bits */
+      uint64_t k = km + kr, p = 0, esc = 0;
+      for (uint64_t i = 0; i < k && status == ORC_OK; i++) {
+        uint64_t g = blk[i];
+        if (g == 0) {
+          if (esc == ke) { status = ORC_ERR_FORMAT; break; }
+          g = get_u16(payload + x_off + 2 * (xj + esc));
+          esc++;
+          if (g <= 255) { status = ORC_ERR_FORMAT; break; }   /* only gaps above 255 */
+        }
+        p = (i == 0) ? g - 1 : p + g;
+        if (p >= L) { status = ORC_ERR_FORMAT; break; }
+        if ((blk[k + i / 8] >> (i % 8)) & 1) {
+          if (nr == kr) { status = ORC_ERR_FORMAT; break; }
+          rpos[nr++] = (uint16_t)p;
+        } else {
+          if (nm == km) { status = ORC_ERR_FORMAT; break; }
+          mpos[nm++] = (uint16_t)p;
+        }
+      }
+      if (status == ORC_OK && (esc != ke || nm != km || nr != kr)) status = ORC_ERR_FORMAT;
+      for (uint64_t i = k; status == ORC_OK && i < 8 * ((k + 7) / 8); i++)
+        if ((blk[k + i / 8] >> (i % 8)) & 1) status = ORC_ERR_FORMAT;   /* class pad bits */
+      p_off += k + (k + 7) / 8;
+    } else {
+      /* version-1 blocks; a position may not be in both */
+      if (read_block(blk, mpos, km, L) != 0) status = ORC_ERR_FORMAT;
+      blk += block_bytes(km, L);
+      if (status == ORC_OK && read_block(blk, rpos, kr, L) != 0) status = ORC_ERR_FORMAT;
+      for (uint64_t a = 0, b = 0; status == ORC_OK && a < km && b < kr;) {
+        if (mpos[a] == rpos[b]) status = ORC_ERR_FORMAT;
+        else if (mpos[a] < rpos[b]) a++;
+        else b++;
+      }
+      nm = km;
+      nr = kr;
+      p_off += block_bytes(km, L) + block_bytes(kr, L);
+    }
+    if (status != ORC_OK) break;
+    for (uint64_t i = 0; i < nm; i++) {
+      uint16_t v = mant_at(payload + m_off, mj + i);
+      if (v == 0) { status = ORC_ERR_FORMAT; break; }
+      out[c * ORC_CHUNK + mpos[i]] ^= v;
+    }
+    for (uint64_t i = 0; status == ORC_OK && i < nr; i++) {
+      uint16_t v = get_u16(payload + r_off + 2 * (rj + i));
+      if ((v & ORC_SIGN_EXP_BITS) == 0) { status = ORC_ERR_FORMAT; break; }
+      out[c * ORC_CHUNK + rpos[i]] ^= v;
+    }
+    mj += km;
+    rj += kr;
+    xj += ke;
+  }
+  free(mpos);
+  free(rpos);
+  if (status != ORC_OK) return status;
+  for (uint64_t bit = 7 * sum_m; bit < 8 * m_bytes; bit++)
+    if ((payload[m_off + bit / 8] >> (bit % 8)) & 1) return ORC_ERR_FORMAT;
+  return ORC_OK;
+}
+
 /* ---- decode ------------------------------------------------------------------------- */
 
 /* Applies payload[0..size) to old into out and checks every format rule; no checksum.  When
@@ -297,14 +588,15 @@ static int decode_into(const uint16_t* old, uint64_t n, const uint8_t* payload, 
   if (size < ORC_HEADER) return ORC_ERR_FORMAT;
   if (memcmp(payload, "BF16DLT1", 8) != 0) return ORC_ERR_FORMAT;
   uint32_t version = get_u32(payload + 8);
-  if (version != 1 && version != 2) return ORC_ERR_FORMAT;
-  const uint64_t hdr = version == 2 ? ORC_HEADER_V2 : ORC_HEADER;
+  if (version != 1 && version != 2 && version != 3) return ORC_ERR_FORMAT;
+  const uint64_t hdr = version >= 2 ? ORC_HEADER_V2 : ORC_HEADER;
   if (size < hdr) return ORC_ERR_FORMAT;
-  if (version == 2 && get_u64(payload + 72) != 0) return ORC_ERR_FORMAT;
+  if (version >= 2 && get_u64(payload + 72) != 0) return ORC_ERR_FORMAT;
   if (get_u32(payload + 12) != ORC_CHUNK) return ORC_ERR_FORMAT;
   uint64_t C = (n + ORC_CHUNK - 1) / ORC_CHUNK;
   if (get_u64(payload + 16) != n) return ORC_ERR_FORMAT;
   if (get_u64(payload + 24) != C) return ORC_ERR_FORMAT;
+  if (version == 3) return decode_v3(old, n, payload, size, out, required_base);
   uint64_t hdr_m = get_u64(payload + 32), hdr_r = get_u64(payload + 40);
   uint64_t hdr_pos = get_u64(payload + 48), hdr_size = get_u64(payload + 56);
   if (hdr_size != size) return ORC_ERR_FORMAT;

@@ -53,7 +53,12 @@ int orc_encode(const uint16_t* old, const uint16_t* neu, uint64_t n, uint8_t* ou
 int orc_encode_versioned(const uint16_t* old, const uint16_t* neu, uint64_t n, uint64_t base,
                          uint8_t* out, uint64_t cap, uint64_t* size_out, uint64_t* checksum_out);
 
-/* Decodes payload[0..size) (version 1 or 2; the base of a version-2 payload is not checked
+/* orc_encode_versioned writing a version-3 payload (compact positions: a merged gap-byte
+ * list with escapes and class bits per chunk, see bd_oracle.c). */
+int orc_encode_compact(const uint16_t* old, const uint16_t* neu, uint64_t n, uint64_t base,
+                       uint8_t* out, uint64_t cap, uint64_t* size_out, uint64_t* checksum_out);
+
+/* Decodes payload[0..size) (version 1, 2 or 3; the base of a bound payload is not checked
  * here) against old (n elements) into out (n elements, must not alias
  * old), then verifies checksum(out) == expected.  Returns ORC_OK, ORC_ERR_FORMAT (payload
  * is not a canonical BF16DLT1 v1 payload for n elements) or ORC_ERR_CHECKSUM.  On an error
