@@ -540,6 +540,58 @@ def run_ours(args) -> None:
     state["new"] = h_state["new"]
     del hd_new, hd_old, hbuf
 
+    # version 3 (compact position blocks) of the same update: compress bound to checksum(old),
+    # the full verified apply, and the incremental apply -- backwards from a second payload of
+    # the reverse update bound to checksum(new), so that both directions pass the base check
+    c3 = bd.CompressBatch(olds, news, base_checksums=ck_old, compact=True)
+    c3.run(stream)
+    torch.cuda.synchronize()
+    s3 = [int(v) for v in c3.sizes.tolist()]
+    c3b = bd.CompressBatch(news, olds, caps=s3, base_checksums=ck_new, compact=True)
+    c3b.run(stream)
+    torch.cuda.synchronize()
+    if int(c3.status.item()) != bd.OK or int(c3b.status.item()) != bd.OK:
+        raise RuntimeError("version-3 compress failed")
+    p3_bytes = sum(s3)
+
+    def timed(fn, steps):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(steps):
+            out = fn()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        return reduce_max(t0.elapsed_time(t1), world, dev) / steps, out
+
+    c3_ms, _ = timed(lambda: c3.run(stream), args.steps)
+    d3 = {True: bd.DecompressBatch(rolls, c3.payloads, s3, ck_old),
+          False: bd.DecompressBatch(rolls, c3.payloads, s3, ck_new)}
+    i3 = {True: bd.IncrementalBatch(rolls, c3b.payloads, s3, ck_new, ck_old),
+          False: bd.IncrementalBatch(rolls, c3.payloads, s3, ck_old, ck_new)}
+
+    def alternate(table):
+        def run():
+            b = table[state["new"]]
+            b.run(stream)
+            state["new"] = not state["new"]
+            return b
+        return run
+
+    for name, table in (("apply", d3), ("incremental", i3)):
+        ms, last3 = timed(alternate(table), args.steps)
+        want = N if state["new"] else O
+        if int(last3.status.item()) != bd.OK or not torch.equal(Rb.view(torch.int16),
+                                                                 want.view(torch.int16)):
+            raise RuntimeError(f"version-3 {name} did not verify")
+        if name == "apply":
+            a3_ms = ms
+        else:
+            i3_ms = ms
+    del c3b, d3, i3
+
     total_ms = reduce_max(total_ms, world, dev)
     ms_step = total_ms / args.steps
     raw = 2 * n_total
@@ -645,6 +697,18 @@ def run_ours(args) -> None:
                     "what": "bd_decompress_incremental_batch in place: verified from the "
                             "checksums of the resident weights; algorithmic bytes = payload + "
                             "read and write of each touched 32-byte sector"},
+                "compact": {
+                    "payload_pct": round(100 * p3_bytes / raw, 4),
+                    "payload_vs_v1": round(p3_bytes / payload_bytes, 4),
+                    "compress_ms": round(c3_ms, 4), "apply_ms": round(a3_ms, 4),
+                    "incremental_ms": round(i3_ms, 4),
+                    "compress_roofline_frac": round((4 * n_total + p3_bytes) / (c3_ms * 1e-3)
+                                                    / 1e9 / peak, 4),
+                    "apply_roofline_frac": round((2 * n_total + p3_bytes + 32 * touched)
+                                                 / (a3_ms * 1e-3) / 1e9 / peak, 4),
+                    "what": "version-3 payloads (compact position blocks) of the same update: "
+                            "bd_compress_versioned_batch format 3, bd_decompress_batch in "
+                            "place, bd_decompress_incremental_batch in place"},
                 "compress_algorithmic_bytes": comp_bytes, "apply_algorithmic_bytes": app_bytes,
                 "payload_pct": round(100 * payload_bytes / raw, 4),
                 "touched_sector_pct": round(100 * touched / (raw / 32), 3),

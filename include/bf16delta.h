@@ -29,10 +29,25 @@
  * (bit p = bit p%8 of byte p/8).  Elements inside every stream are in ascending position.
  * Header: "BF16DLT1", u32 version=1, u32 chunk_elems=4096, u64 n, u64 C, u64 sum M,
  * u64 sum R, u64 position bytes, u64 total size.
- * Version 2 (bd_compress_versioned): the same payload with an 80-byte header -- version 2,
- * the 64 bytes above, then u64 base checksum (the checksum of the weights the payload applies
- * to) and u64 0 -- so every section starts 16 bytes later.  Every decompress call accepts
- * both versions.
+ * Version 2 (bd_compress_versioned, format 2): the same payload with an 80-byte header --
+ * version 2, the 64 bytes above, then u64 base checksum (the checksum of the weights the
+ * payload applies to) and u64 0 -- so every section starts 16 bytes later.
+ * Version 3 (format 3): the version-2 header with version 3, and compact position blocks
+ * standing in for the entropy stage the ARCv3 page applies to the sparse positions (which it
+ * does not specify).  Sections:
+ *   [header 80 B] [count table: C x u32] [R stream] [X stream: u16 per escaped gap]
+ *   [positions] [M stream]
+ * A count entry with bit 31 set marks a compact chunk: M in bits 0..8, R in 9..17, E in
+ * 18..26, bits 27..30 zero, 1 <= M + R <= 508, E <= M + R.  Its block merges the chunk's
+ * changes into one ascending list: M + R gap bytes (gap_0 = p_0 + 1, gap_i = p_i - p_{i-1};
+ * a gap above 255 is written as 0 and its value taken from the X stream, E of them in order)
+ * then ceil((M+R)/8) class bytes (bit i set: change i is rare; pad bits 0).  An entry with
+ * bit 31 clear has M in bits 0..14, R in 15..29, bit 30 zero, and version-1 blocks.  Compress
+ * codes a chunk compactly exactly when it has 1..508 changes and M + R + ceil((M+R)/8) + 2E
+ * is below the bytes of its two version-1 blocks, so a version-3 payload is never longer
+ * than the version-2 payload of the same update.  The header's position-bytes field counts
+ * the position section only; the X stream is what the other sections leave of the total.
+ * Every decompress call accepts all three versions.
  * Checksum (returned beside the payload, not stored in it): with word_j the little-endian
  * 64-bit word of elements 4j..4j+3 (zero past n),
  *   checksum = sum_j mix64(word_j ^ (j+1) * 0x9E3779B97F4A7C15)  mod 2^64,
@@ -70,11 +85,11 @@ typedef enum bd_status {
   BD_OK = 0,
   BD_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment, overlap or workspace size */
   BD_ERR_CAPACITY = 2,    /* compress: payload larger than the capacity given */
-  BD_ERR_FORMAT = 3,      /* decompress: not a canonical BF16DLT1 v1 payload for n elements */
+  BD_ERR_FORMAT = 3,      /* decompress: not a canonical BF16DLT1 payload for n elements */
   BD_ERR_CHECKSUM = 4,    /* decompress: checksum of the result differs from the expected */
   BD_ERR_CUDA = 5,        /* a CUDA runtime call or kernel launch failed */
-  BD_ERR_BASE = 6         /* incremental apply: a version-2 payload whose base checksum is not
-                             the checksum of the weights it is applied to */
+  BD_ERR_BASE = 6         /* incremental apply: a version-2 or -3 payload whose base checksum
+                             is not the checksum of the weights it is applied to */
 } bd_status;
 
 #define BD_CHUNK_ELEMS 4096u
@@ -118,11 +133,13 @@ typedef struct bd_incremental_item {
   int32_t* d_status;             /* out (optional): BD_OK, BD_ERR_FORMAT or BD_ERR_CHECKSUM */
 } bd_incremental_item;
 
-/* Parsed payload header (host side).  base_checksum is 0 for a version-1 payload. */
+/* Parsed payload header (host side).  base_checksum is 0 for a version-1 payload;
+ * n_escapes (X-stream values) is 0 below version 3. */
 typedef struct bd_payload_info_t {
   uint64_t n, chunks, n_mant, n_rare, position_bytes, total_size;
   uint32_t version, chunk_elems;
   uint64_t base_checksum;
+  uint64_t n_escapes;
 } bd_payload_info_t;
 
 /* Largest payload compress can produce for n elements (every chunk at its worst split, with
@@ -149,26 +166,28 @@ BD_API int bd_compress(const uint16_t* d_old, const uint16_t* d_new, uint64_t n,
 BD_API int bd_compress_batch(const bd_compress_item* h_items, uint32_t k, void* d_ws,
                       uint64_t ws_bytes, int32_t* d_status, void* stream);
 
-/* bd_compress writing a version-2 payload bound to its base version.  Not on the pages: the
- * NeMo-DCR page binds the installed weights to the baseline of the next delta so that
- * mismatched versions cannot enter silently.  *d_base_checksum (device, required) is the
- * checksum of d_old as the caller knows it -- in a steady update loop, the checksum of the
- * previous update's new weights; it is stored in the header, not recomputed.  The
- * incremental apply refuses the payload with BD_ERR_BASE when the receiver's checksum of its
- * weights differs; bd_payload_info exposes the base for a check on the host before a full
- * apply.  Payload otherwise as bd_compress (16 bytes longer). */
+/* bd_compress writing a payload bound to its base version: format 2 (the version-1 payload
+ * with the 80-byte header) or 3 (compact position blocks, see above); any other format is
+ * BD_ERR_INVALID_ARG.  Not on the pages: the NeMo-DCR page binds the installed weights to
+ * the baseline of the next delta so that mismatched versions cannot enter silently.
+ * *d_base_checksum (device, required) is the checksum of d_old as the caller knows it -- in
+ * a steady update loop, the checksum of the previous update's new weights; it is stored in
+ * the header, not recomputed.  The incremental apply refuses the payload with BD_ERR_BASE
+ * when the receiver's checksum of its weights differs; bd_payload_info exposes the base for
+ * a check on the host before a full apply.  Sizes, capacity and workspace as bd_compress
+ * (bd_compress_bound covers both formats). */
 BD_API int bd_compress_versioned(const uint16_t* d_old, const uint16_t* d_new, uint64_t n,
                                  void* d_payload, uint64_t cap, void* d_ws, uint64_t ws_bytes,
                                  uint64_t* d_size, uint64_t* d_checksum,
-                                 const uint64_t* d_base_checksum, int32_t* d_status,
-                                 void* stream);
+                                 const uint64_t* d_base_checksum, uint32_t format,
+                                 int32_t* d_status, void* stream);
 
-/* Batched bd_compress_versioned: h_base_checksums[i] (host array of k device pointers, each
- * required) is the base checksum of item i. */
+/* Batched bd_compress_versioned, every item in the same format: h_base_checksums[i] (host
+ * array of k device pointers, each required) is the base checksum of item i. */
 BD_API int bd_compress_versioned_batch(const bd_compress_item* h_items,
                                        const uint64_t* const* h_base_checksums, uint32_t k,
-                                       void* d_ws, uint64_t ws_bytes, int32_t* d_status,
-                                       void* stream);
+                                       uint32_t format, void* d_ws, uint64_t ws_bytes,
+                                       int32_t* d_status, void* stream);
 
 /* [ARCv3] delta_decompress, [WT] weights_updated = weights_old XOR mask: applies the payload
  * to d_old, writing the result to d_out (d_out == d_old applies in place; any other overlap
@@ -193,8 +212,8 @@ BD_API int bd_decompress_batch(const bd_decompress_item* h_items, uint32_t k, vo
  *          mix64(new_word_j ^ (j+1)*G) - mix64(old_word_j ^ (j+1)*G)     (mod 2^64)
  * which equals the checksum of the result whenever *d_ck_old is the checksum of d_w before
  * the call.  The status is BD_OK when ck == *d_expected, else BD_ERR_CHECKSUM (format errors
- * as bd_decompress); ck goes to *d_ck_out when given.  A version-2 payload whose base checksum
- * differs from *d_ck_old is refused with BD_ERR_BASE and nothing is written.  Only the 32-byte sectors holding
+ * as bd_decompress); ck goes to *d_ck_out when given.  A version-2 or -3 payload whose base
+ * checksum differs from *d_ck_old is refused with BD_ERR_BASE and nothing is written.  Only the 32-byte sectors holding
  * changes are read and written (plus the payload), against a full read of the tensor for
  * bd_decompress.  What it does not verify: a word of d_w that differs from the trainer's
  * old copy but is not touched by the payload (bd_decompress's full read catches that).
@@ -246,9 +265,11 @@ BD_API int bd_decompress_noalloc(const uint16_t* d_old, uint64_t n, const void* 
 /* The checksum above of n BF16 values, written to *d_out.  Needs no workspace. */
 BD_API int bd_checksum(const uint16_t* d_w, uint64_t n, uint64_t* d_out, void* stream);
 
-/* Parses and checks a payload header held in host memory (bytes >= 64).  Checks magic,
- * version, chunk size and the internal consistency of the header fields; returns BD_OK,
- * BD_ERR_FORMAT or BD_ERR_INVALID_ARG.  Does not touch the GPU. */
+/* Parses and checks a payload header held in host memory (bytes >= 64; >= 80 for versions 2
+ * and 3).  Checks magic, version, chunk size and the internal consistency of the header
+ * fields (for version 3 the total leaves an even number of bytes, at most 2 * 508 per chunk,
+ * for the X stream); returns BD_OK, BD_ERR_FORMAT or BD_ERR_INVALID_ARG.  Does not touch the
+ * GPU. */
 BD_API int bd_payload_info(const void* h_header, uint64_t bytes, bd_payload_info_t* out);
 
 /* Waits for `stream` and returns the int32 status word at d_status (or BD_ERR_CUDA). */

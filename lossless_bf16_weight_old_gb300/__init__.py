@@ -169,12 +169,16 @@ def _workspace(nbytes: int, device, workspace) -> torch.Tensor:
 
 
 def compress(old: torch.Tensor, new: torch.Tensor, *, payload: torch.Tensor | None = None,
-             workspace: torch.Tensor | None = None, base_checksum=None, stream=None):
+             workspace: torch.Tensor | None = None, base_checksum=None, compact: bool = False,
+             stream=None):
     """Encodes old -> new on the GPU.  Returns device tensors
     (payload uint8[cap], size int64[1], checksum int64[1] (unsigned bits), status int32[1]),
     all written asynchronously on the stream.  With base_checksum (an int or int64[1] device
-    tensor: the checksum of old as the caller knows it) the payload is version 2, bound to
-    that base (bd_compress_versioned)."""
+    tensor: the checksum of old as the caller knows it) the payload is bound to that base
+    (bd_compress_versioned): version 2, or version 3 (compact position blocks) when
+    `compact` is set."""
+    if compact and base_checksum is None:
+        raise ValueError("compact payloads (version 3) are bound to a base: pass base_checksum")
     po, n = _bits(old, "old")
     pn, n2 = _bits(new, "new")
     if n != n2:
@@ -197,7 +201,8 @@ def compress(old: torch.Tensor, new: torch.Tensor, *, payload: torch.Tensor | No
         rc = _lib.load().bd_compress_versioned(po, pn, n, payload.data_ptr(), payload.numel(),
                                                ws.data_ptr(), ws.numel(), size.data_ptr(),
                                                ck.data_ptr(), base_checksum.data_ptr(),
-                                               st.data_ptr(), _stream(stream))
+                                               3 if compact else 2, st.data_ptr(),
+                                               _stream(stream))
         _check(rc, "bd_compress_versioned")
     return payload, size, ck, st
 
@@ -258,9 +263,14 @@ class CompressBatch:
     """Device buffers and the C item table of one batched compress over fixed tensors."""
 
     def __init__(self, olds: Sequence[torch.Tensor], news: Sequence[torch.Tensor],
-                 caps: Sequence[int] | None = None, base_checksums: torch.Tensor | None = None):
-        """base_checksums (int64[k] device tensor, optional): version-2 payloads bound to
-        these base checksums (bd_compress_versioned_batch)."""
+                 caps: Sequence[int] | None = None, base_checksums: torch.Tensor | None = None,
+                 compact: bool = False):
+        """base_checksums (int64[k] device tensor, optional): payloads bound to these base
+        checksums (bd_compress_versioned_batch), version 2, or version 3 (compact position
+        blocks) when `compact` is set."""
+        if compact and base_checksums is None:
+            raise ValueError("compact payloads (version 3) are bound to a base: pass base_checksums")
+        self.format = 3 if compact else 2
         if len(olds) != len(news):
             raise ValueError("olds and news differ in length")
         k = len(olds)
@@ -304,7 +314,7 @@ class CompressBatch:
     def run(self, stream=None) -> None:
         if self.bases is not None:
             rc = _lib.load().bd_compress_versioned_batch(
-                self.items, self.bases, self.k, self.workspace.data_ptr(),
+                self.items, self.bases, self.k, self.format, self.workspace.data_ptr(),
                 self.workspace.numel(), self.status.data_ptr(), _stream(stream))
             _check(rc, "bd_compress_versioned_batch")
             return

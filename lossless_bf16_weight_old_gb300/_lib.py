@@ -30,7 +30,7 @@ class IncrementalItem(ctypes.Structure):
 class PayloadInfo(ctypes.Structure):
     _fields_ = [("n", c_u64), ("chunks", c_u64), ("n_mant", c_u64), ("n_rare", c_u64),
                 ("position_bytes", c_u64), ("total_size", c_u64), ("version", c_u32),
-                ("chunk_elems", c_u32), ("base_checksum", c_u64)]
+                ("chunk_elems", c_u32), ("base_checksum", c_u64), ("n_escapes", c_u64)]
 
 
 # name -> (restype, argtypes); must match include/bf16delta.h
@@ -40,9 +40,9 @@ SIGNATURES = {
     "bd_decompress_workspace_size": (c_u64, [c_p, c_u32]),
     "bd_compress": (c_int, [c_p, c_p, c_u64, c_p, c_u64, c_p, c_u64, c_p, c_p, c_p, c_p]),
     "bd_compress_batch": (c_int, [c_p, c_u32, c_p, c_u64, c_p, c_p]),
-    "bd_compress_versioned": (c_int, [c_p, c_p, c_u64, c_p, c_u64, c_p, c_u64, c_p, c_p, c_p, c_p,
-                                      c_p]),
-    "bd_compress_versioned_batch": (c_int, [c_p, c_p, c_u32, c_p, c_u64, c_p, c_p]),
+    "bd_compress_versioned": (c_int, [c_p, c_p, c_u64, c_p, c_u64, c_p, c_u64, c_p, c_p, c_p, c_u32,
+                                      c_p, c_p]),
+    "bd_compress_versioned_batch": (c_int, [c_p, c_p, c_u32, c_u32, c_p, c_u64, c_p, c_p]),
     "bd_decompress": (c_int, [c_p, c_u64, c_p, c_u64, c_p, c_p, c_p, c_u64, c_p, c_p]),
     "bd_decompress_batch": (c_int, [c_p, c_u32, c_p, c_u64, c_p, c_p]),
     "bd_decompress_noalloc": (c_int, [c_p, c_u64, c_p, c_u64, c_p, c_p, c_p, c_p]),

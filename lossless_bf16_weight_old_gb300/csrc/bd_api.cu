@@ -117,9 +117,12 @@ inline bool overlaps(const void* a, uint64_t na, const void* b, uint64_t nb) {
 int check(cudaError_t e) { return e == cudaSuccess ? BD_OK : BD_ERR_CUDA; }
 
 // -------------------------------------------------------------------------------- compress
-int compress_impl(const bd_compress_item* items, const uint64_t* const* bases, uint32_t k,
-                  void* ws, uint64_t ws_bytes, int32_t* status_all, cudaStream_t s) {
+// bases == nullptr: version 1; else version `format` (2, or 3 with compact position blocks).
+int compress_impl(const bd_compress_item* items, const uint64_t* const* bases, uint32_t format,
+                  uint32_t k, void* ws, uint64_t ws_bytes, int32_t* status_all, cudaStream_t s) {
   if (k > 0 && items == nullptr) return BD_ERR_INVALID_ARG;
+  if (bases && format != 2 && format != 3) return BD_ERR_INVALID_ARG;
+  const uint32_t version = bases ? format : 1;
   if (bases)
     for (uint32_t i = 0; i < k; i++)
       if (!bases[i] || !aligned(bases[i], 8)) return BD_ERR_INVALID_ARG;
@@ -163,6 +166,7 @@ int compress_impl(const bd_compress_item* items, const uint64_t* const* bases, u
     J.d_checksum = it.d_checksum;
     J.d_status = it.d_status;
     J.d_base = bases ? bases[i] : nullptr;
+    J.version = version;
     J.nchunks = (it.n + kChunk - 1) / kChunk;
     J.chunk_base = cb;
     J.tile_base = tb;
@@ -181,10 +185,10 @@ int compress_impl(const bd_compress_item* items, const uint64_t* const* bases, u
   if (status_all && (rc = check(cudaMemsetAsync(status_all, 0, sizeof(int32_t), s)))) return rc;
   if (k == 0) return BD_OK;
   if ((rc = check(upload(host, w + lay.jobs, s)))) return rc;
-  if ((rc = check(launch_encode_slots(c)))) return rc;
+  if ((rc = check(launch_encode_slots(c, version == 3)))) return rc;
   if ((rc = check(launch_scan_tiles(c, false)))) return rc;
   if ((rc = check(launch_scan_jobs(c, false, status_all)))) return rc;
-  if ((rc = check(launch_emit(c)))) return rc;
+  if ((rc = check(launch_emit(c, version == 3)))) return rc;
   return check(launch_emit_dense(c));
 }
 
@@ -322,31 +326,33 @@ int bd_compress(const uint16_t* d_old, const uint16_t* d_new, uint64_t n, void* 
                 uint64_t cap, void* d_ws, uint64_t ws_bytes, uint64_t* d_size,
                 uint64_t* d_checksum, int32_t* d_status, void* stream) {
   bd_compress_item it{d_old, d_new, n, d_payload, cap, d_size, d_checksum, nullptr};
-  return compress_impl(&it, nullptr, 1, d_ws, ws_bytes, d_status,
+  return compress_impl(&it, nullptr, 1, 1, d_ws, ws_bytes, d_status,
                        static_cast<cudaStream_t>(stream));
 }
 
 int bd_compress_batch(const bd_compress_item* h_items, uint32_t k, void* d_ws,
                       uint64_t ws_bytes, int32_t* d_status, void* stream) {
-  return compress_impl(h_items, nullptr, k, d_ws, ws_bytes, d_status,
+  return compress_impl(h_items, nullptr, 1, k, d_ws, ws_bytes, d_status,
                        static_cast<cudaStream_t>(stream));
 }
 
 int bd_compress_versioned(const uint16_t* d_old, const uint16_t* d_new, uint64_t n,
                           void* d_payload, uint64_t cap, void* d_ws, uint64_t ws_bytes,
                           uint64_t* d_size, uint64_t* d_checksum,
-                          const uint64_t* d_base_checksum, int32_t* d_status, void* stream) {
+                          const uint64_t* d_base_checksum, uint32_t format, int32_t* d_status,
+                          void* stream) {
   bd_compress_item it{d_old, d_new, n, d_payload, cap, d_size, d_checksum, nullptr};
   const uint64_t* bases[1] = {d_base_checksum};
-  return compress_impl(&it, bases, 1, d_ws, ws_bytes, d_status,
+  return compress_impl(&it, bases, format, 1, d_ws, ws_bytes, d_status,
                        static_cast<cudaStream_t>(stream));
 }
 
 int bd_compress_versioned_batch(const bd_compress_item* h_items,
-                                const uint64_t* const* h_base_checksums, uint32_t k, void* d_ws,
-                                uint64_t ws_bytes, int32_t* d_status, void* stream) {
+                                const uint64_t* const* h_base_checksums, uint32_t k,
+                                uint32_t format, void* d_ws, uint64_t ws_bytes,
+                                int32_t* d_status, void* stream) {
   if (k > 0 && !h_base_checksums) return BD_ERR_INVALID_ARG;
-  return compress_impl(h_items, h_base_checksums, k, d_ws, ws_bytes, d_status,
+  return compress_impl(h_items, h_base_checksums, format, k, d_ws, ws_bytes, d_status,
                        static_cast<cudaStream_t>(stream));
 }
 
@@ -415,10 +421,11 @@ int bd_payload_info(const void* h_header, uint64_t bytes, bd_payload_info_t* out
   I.position_bytes = le64(p + 48);
   I.total_size = le64(p + 56);
   I.base_checksum = 0;
-  if ((I.version != 1 && I.version != 2) || I.chunk_elems != kChunk || I.n > BD_MAX_ELEMS)
+  I.n_escapes = 0;
+  if (I.version < 1 || I.version > 3 || I.chunk_elems != kChunk || I.n > BD_MAX_ELEMS)
     return BD_ERR_FORMAT;
-  const uint64_t hdr = I.version == 2 ? kHeaderV2 : kHeader;
-  if (I.version == 2) {
+  const uint64_t hdr = I.version >= 2 ? kHeaderV2 : kHeader;
+  if (I.version >= 2) {
     if (bytes < kHeaderV2) return BD_ERR_INVALID_ARG;
     I.base_checksum = le64(p + 64);
     if (le64(p + 72) != 0) return BD_ERR_FORMAT;
@@ -428,7 +435,16 @@ int bd_payload_info(const void* h_header, uint64_t bytes, bd_payload_info_t* out
   if (I.position_bytes > 2 * (uint64_t)kChunkBitmap * I.chunks) return BD_ERR_FORMAT;
   const uint64_t want = hdr + 4 * I.chunks + 2 * I.n_rare + I.position_bytes +
                         (7 * I.n_mant + 7) / 8;
-  if (want != I.total_size) return BD_ERR_FORMAT;
+  if (I.version == 3) {
+    // the X stream's length is not in the header: whatever the other sections leave, in u16
+    // values, at most kCompactMax per chunk
+    if (I.total_size < want || (I.total_size - want) % 2 != 0 ||
+        (I.total_size - want) / 2 > (uint64_t)kCompactMax * I.chunks)
+      return BD_ERR_FORMAT;
+    I.n_escapes = (I.total_size - want) / 2;
+  } else if (want != I.total_size) {
+    return BD_ERR_FORMAT;
+  }
   *out = I;
   return BD_OK;
 }

@@ -9,8 +9,10 @@
 //   copy_jobs      out-of-place only: out = old (warp per chunk), so the passes below work on
 //                  out in place.
 //   apply_chunks   one warp per chunk whose two position blocks are delta lists (the common
-//                  case for sparse deltas): decodes and checks the whole chunk into shared
-//                  memory, XORs each change into out with a 32-bit atomic XOR performed in L2,
+//                  case for sparse deltas) or whose block is a version-3 compact block (one
+//                  ascending list of gap bytes with class bits): decodes and checks the whole
+//                  chunk into shared memory, XORs each change into out with a 32-bit atomic
+//                  XOR performed in L2,
 //                  then reads the chunk back through L2 for its checksum terms.  The atomics
 //                  bring the touched sectors into L2 where the read-back finds them, so each
 //                  sector of out crosses HBM at most once each way.  Chunks with a bitmap
@@ -53,9 +55,37 @@ __device__ __forceinline__ void flush_ck(uint8_t* ck_base, uint32_t j, uint64_t 
               (unsigned long long)s);
 }
 
-// One CTA per listed chunk (a chunk with a bitmap block): decodes the chunk into an 8 KiB
-// shared XOR mask, applies it, writes the changed 16-byte groups and adds the checksum terms
-// of the result (INCR: the new-minus-old terms of the changed groups only).
+// Block-wide exclusive prefix sums of two quantities (0 and 1), each held in two slots per
+// thread and ordered slot a of threads 0..255, then slot b of threads 0..255; tot0 / tot1 are
+// the totals.  Starts and ends with a barrier, so s_tot may be reused by the next call.
+__device__ __forceinline__ void block_scan_ab(uint32_t a0, uint32_t b0, uint32_t a1, uint32_t b1,
+                                              uint32_t (*s_tot)[4], uint32_t& xa0,
+                                              uint32_t& xb0, uint32_t& xa1, uint32_t& xb1,
+                                              uint32_t& tot0, uint32_t& tot1) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const uint32_t ia0 = warp_incl_scan(a0), ib0 = warp_incl_scan(b0);
+  const uint32_t ia1 = warp_incl_scan(a1), ib1 = warp_incl_scan(b1);
+  __syncthreads();
+  if (lane == 31) { s_tot[w][0] = ia0; s_tot[w][1] = ib0; s_tot[w][2] = ia1; s_tot[w][3] = ib1; }
+  __syncthreads();
+  uint32_t pa0 = 0, pb0 = 0, pa1 = 0, pb1 = 0, ta0 = 0, tb0 = 0, ta1 = 0, tb1 = 0;
+  for (int q = 0; q < kWarps; q++) {
+    if (q < w) { pa0 += s_tot[q][0]; pb0 += s_tot[q][1]; pa1 += s_tot[q][2]; pb1 += s_tot[q][3]; }
+    ta0 += s_tot[q][0]; tb0 += s_tot[q][1]; ta1 += s_tot[q][2]; tb1 += s_tot[q][3];
+  }
+  xa0 = pa0 + ia0 - a0;
+  xb0 = ta0 + pb0 + ib0 - b0;
+  xa1 = pa1 + ia1 - a1;
+  xb1 = ta1 + pb1 + ib1 - b1;
+  tot0 = ta0 + tb0;
+  tot1 = ta1 + tb1;
+  __syncthreads();
+}
+
+// One CTA per listed chunk (a chunk with a bitmap block, or any chunk on the path without a
+// workspace, including version-3 compact chunks): decodes the chunk into an 8 KiB shared XOR
+// mask, applies it, writes the changed 16-byte groups and adds the checksum terms of the
+// result (INCR: the new-minus-old terms of the changed groups only).
 template <bool INCR>
 __global__ void __launch_bounds__(kThreads)
 k_apply_dense(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
@@ -93,9 +123,9 @@ k_apply_dense(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_
     const uint32_t L = (n - e0) < kChunk ? (uint32_t)(n - e0) : kChunk;
     const uint32_t B = (L + 7) >> 3;
     const uint8_t* __restrict__ payload = J.payload;
-    const uint32_t cnt = reinterpret_cast<const uint32_t*>(
-        payload + count_table_offset(info[j].r_start, J.nchunks))[c];
-    const uint32_t M = cnt & 0xFFFFu, R = cnt >> 16;
+    const ChunkCount cc = parse_count(reinterpret_cast<const uint32_t*>(
+        payload + count_table_offset(info[j].r_start, J.nchunks))[c], info[j].version);
+    const uint32_t M = cc.M, R = cc.R;
     const TileSum pre = tile_pre[tile_start[j] + c / kTileChunks];
     const uint4 lc = loc[g];
     const uint64_t Pex = pre.p + lc.x, Mex = pre.m + lc.y, Rex = pre.r + lc.z;
@@ -113,106 +143,150 @@ k_apply_dense(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_
     s_mask4[t] = make_uint4(0, 0, 0, 0);
     s_mask4[t + 256] = make_uint4(0, 0, 0, 0);
 
-    // per-thread scan inputs: list entry t (slot a) or bitmap bytes t, t+256 (slots a, b)
     bool bad = false;
-    uint32_t aM = 0, bM = 0, aR = 0, bR = 0;
-    uint32_t byteMa = 0, byteMb = 0, byteRa = 0, byteRb = 0;
-    if (listM) {
-      if ((uint32_t)t < M) {
-        aM = load_u16(mblk + 2 * t);
-        if (t > 0 && aM == 0) bad = true;
+    if (cc.compact) {
+      // changes t (slot a) and t + 256 (slot b) of the merged list; first the escapes and the
+      // rare flags, then the gaps with the escaped values in place
+      const uint32_t k = M + R, ia = t, ib = t + 256;
+      const uint8_t* blk = mblk;
+      const uint8_t* cls = blk + k;
+      const uint16_t* xs =
+          reinterpret_cast<const uint16_t*>(payload + info[j].x_start) + pre.e + lc.w;
+      uint32_t ga = ia < k ? blk[ia] : 0u, gb = ib < k ? blk[ib] : 0u;
+      const uint32_t escA = ia < k && ga == 0, escB = ib < k && gb == 0;
+      const uint32_t rA = ia < k ? (cls[ia >> 3] >> (ia & 7)) & 1u : 0u;
+      const uint32_t rB = ib < k ? (cls[ib >> 3] >> (ib & 7)) & 1u : 0u;
+      uint32_t xEa, xEb, xRa, xRb, totE, totR;
+      block_scan_ab(escA, escB, rA, rB, s_tot, xEa, xEb, xRa, xRb, totE, totR);
+      if (escA) {
+        if (xEa < cc.E) ga = xs[xEa];
+        if (ga <= 255) bad = true;
+      }
+      if (escB) {
+        if (xEb < cc.E) gb = xs[xEb];
+        if (gb <= 255) bad = true;
+      }
+      if (totE != cc.E || totR != R) bad = true;
+      if (t == 0 && (k & 7) != 0 && (cls[(k - 1) >> 3] >> (k & 7)) != 0) bad = true;
+      uint32_t pa, pb, unused0, unused1, tg, unused2;
+      block_scan_ab(ga, gb, 0u, 0u, s_tot, pa, pb, unused0, unused1, tg, unused2);
+      pa += ga - 1;   // inclusive prefix of the gaps, minus one
+      pb += gb - 1;
+      if (ia < k) {
+        uint32_t v = 0;
+        if (rA) { if (xRa < R) v = load_u16(rstream + 2 * xRa); if ((v & kSignExp) == 0) bad = true; }
+        else { if (ia - xRa < M) v = mant_value(mstream, Mex + ia - xRa); if (v == 0) bad = true; }
+        if (pa >= L) bad = true;
+        if (!bad) s_mask[pa] = (uint16_t)v;
+      }
+      if (ib < k) {
+        uint32_t v = 0;
+        if (rB) { if (xRb < R) v = load_u16(rstream + 2 * xRb); if ((v & kSignExp) == 0) bad = true; }
+        else { if (ib - xRb < M) v = mant_value(mstream, Mex + ib - xRb); if (v == 0) bad = true; }
+        if (pb >= L) bad = true;
+        if (!bad) s_mask[pb] = (uint16_t)v;
       }
     } else {
-      if ((uint32_t)t < B) byteMa = mblk[t];
-      if ((uint32_t)t + 256 < B) byteMb = mblk[t + 256];
-      aM = __popc(byteMa);
-      bM = __popc(byteMb);
-    }
-    if (listR) {
-      if ((uint32_t)t < R) {
-        aR = load_u16(rblk + 2 * t);
-        if (t > 0 && aR == 0) bad = true;
+      // per-thread scan inputs: list entry t (slot a) or bitmap bytes t, t+256 (slots a, b)
+      uint32_t aM = 0, bM = 0, aR = 0, bR = 0;
+      uint32_t byteMa = 0, byteMb = 0, byteRa = 0, byteRb = 0;
+      if (listM) {
+        if ((uint32_t)t < M) {
+          aM = load_u16(mblk + 2 * t);
+          if (t > 0 && aM == 0) bad = true;
+        }
+      } else {
+        if ((uint32_t)t < B) byteMa = mblk[t];
+        if ((uint32_t)t + 256 < B) byteMb = mblk[t + 256];
+        aM = __popc(byteMa);
+        bM = __popc(byteMb);
       }
-    } else {
-      if ((uint32_t)t < B) byteRa = rblk[t];
-      if ((uint32_t)t + 256 < B) byteRb = rblk[t + 256];
-      aR = __popc(byteRa);
-      bR = __popc(byteRb);
-    }
-    // bitmap bits for positions >= L must be zero (only the byte holding position L-1 and
-    // later ones can have them)
-    if ((L & 7) != 0) {
-      const uint32_t lastb = B - 1, keep = (1u << (L & 7)) - 1;
-      if (!listM && (((uint32_t)t == lastb && (byteMa & ~keep)) ||
-                     ((uint32_t)t + 256 == lastb && (byteMb & ~keep)))) bad = true;
-      if (!listR && (((uint32_t)t == lastb && (byteRa & ~keep)) ||
-                     ((uint32_t)t + 256 == lastb && (byteRb & ~keep)))) bad = true;
-    }
+      if (listR) {
+        if ((uint32_t)t < R) {
+          aR = load_u16(rblk + 2 * t);
+          if (t > 0 && aR == 0) bad = true;
+        }
+      } else {
+        if ((uint32_t)t < B) byteRa = rblk[t];
+        if ((uint32_t)t + 256 < B) byteRb = rblk[t + 256];
+        aR = __popc(byteRa);
+        bR = __popc(byteRb);
+      }
+      // bitmap bits for positions >= L must be zero (only the byte holding position L-1 and
+      // later ones can have them)
+      if ((L & 7) != 0) {
+        const uint32_t lastb = B - 1, keep = (1u << (L & 7)) - 1;
+        if (!listM && (((uint32_t)t == lastb && (byteMa & ~keep)) ||
+                       ((uint32_t)t + 256 == lastb && (byteMb & ~keep)))) bad = true;
+        if (!listR && (((uint32_t)t == lastb && (byteRa & ~keep)) ||
+                       ((uint32_t)t + 256 == lastb && (byteRb & ~keep)))) bad = true;
+      }
 
-    // block scan over slots in order [a: t = 0..255][b: t = 0..255]
-    const uint32_t iaM = warp_incl_scan(aM), ibM = warp_incl_scan(bM);
-    const uint32_t iaR = warp_incl_scan(aR), ibR = warp_incl_scan(bR);
-    if (lane == 31) { s_tot[w][0] = iaM; s_tot[w][1] = ibM; s_tot[w][2] = iaR; s_tot[w][3] = ibR; }
-    __syncthreads();
-    uint32_t xaM = 0, xbM = 0, xaR = 0, xbR = 0, totaM = 0, totaR = 0, totbM = 0, totbR = 0;
-    for (int q = 0; q < kWarps; q++) {
-      if (q < w) { xaM += s_tot[q][0]; xbM += s_tot[q][1]; xaR += s_tot[q][2]; xbR += s_tot[q][3]; }
-      totaM += s_tot[q][0]; totbM += s_tot[q][1]; totaR += s_tot[q][2]; totbR += s_tot[q][3];
-    }
-    xaM += iaM - aM;
-    xbM += totaM + ibM - bM;
-    xaR += iaR - aR;
-    xbR += totaR + ibR - bR;
+      // block scan over slots in order [a: t = 0..255][b: t = 0..255]
+      const uint32_t iaM = warp_incl_scan(aM), ibM = warp_incl_scan(bM);
+      const uint32_t iaR = warp_incl_scan(aR), ibR = warp_incl_scan(bR);
+      if (lane == 31) { s_tot[w][0] = iaM; s_tot[w][1] = ibM; s_tot[w][2] = iaR; s_tot[w][3] = ibR; }
+      __syncthreads();
+      uint32_t xaM = 0, xbM = 0, xaR = 0, xbR = 0, totaM = 0, totaR = 0, totbM = 0, totbR = 0;
+      for (int q = 0; q < kWarps; q++) {
+        if (q < w) { xaM += s_tot[q][0]; xbM += s_tot[q][1]; xaR += s_tot[q][2]; xbR += s_tot[q][3]; }
+        totaM += s_tot[q][0]; totbM += s_tot[q][1]; totaR += s_tot[q][2]; totbR += s_tot[q][3];
+      }
+      xaM += iaM - aM;
+      xbM += totaM + ibM - bM;
+      xaR += iaR - aR;
+      xbR += totaR + ibR - bR;
 
-    // scatter the mantissa-only values
-    if (listM) {
-      if ((uint32_t)t < M) {
-        const uint32_t pos = xaM + aM;   // inclusive prefix of the deltas
-        const uint32_t v = mant_value(mstream, Mex + t);
-        if (pos >= L || v == 0) bad = true;
-        else s_mask[pos] = (uint16_t)v;
+      // scatter the mantissa-only values
+      if (listM) {
+        if ((uint32_t)t < M) {
+          const uint32_t pos = xaM + aM;   // inclusive prefix of the deltas
+          const uint32_t v = mant_value(mstream, Mex + t);
+          if (pos >= L || v == 0) bad = true;
+          else s_mask[pos] = (uint16_t)v;
+        }
+      } else {
+        if (totaM + totbM != M) bad = true;
+        uint32_t r = xaM;
+        for (uint32_t bits = byteMa; bits; bits &= bits - 1, r++) {
+          const uint32_t pos = 8 * t + __ffs(bits) - 1;
+          if (r >= M || pos >= L) { bad = true; break; }
+          const uint32_t v = mant_value(mstream, Mex + r);
+          if (v == 0) bad = true; else s_mask[pos] = (uint16_t)v;
+        }
+        r = xbM;
+        for (uint32_t bits = byteMb; bits; bits &= bits - 1, r++) {
+          const uint32_t pos = 8 * (t + 256) + __ffs(bits) - 1;
+          if (r >= M || pos >= L) { bad = true; break; }
+          const uint32_t v = mant_value(mstream, Mex + r);
+          if (v == 0) bad = true; else s_mask[pos] = (uint16_t)v;
+        }
       }
-    } else {
-      if (totaM + totbM != M) bad = true;
-      uint32_t r = xaM;
-      for (uint32_t bits = byteMa; bits; bits &= bits - 1, r++) {
-        const uint32_t pos = 8 * t + __ffs(bits) - 1;
-        if (r >= M || pos >= L) { bad = true; break; }
-        const uint32_t v = mant_value(mstream, Mex + r);
-        if (v == 0) bad = true; else s_mask[pos] = (uint16_t)v;
-      }
-      r = xbM;
-      for (uint32_t bits = byteMb; bits; bits &= bits - 1, r++) {
-        const uint32_t pos = 8 * (t + 256) + __ffs(bits) - 1;
-        if (r >= M || pos >= L) { bad = true; break; }
-        const uint32_t v = mant_value(mstream, Mex + r);
-        if (v == 0) bad = true; else s_mask[pos] = (uint16_t)v;
-      }
-    }
-    __syncthreads();
-    // scatter the rare values; a position already holding a mantissa value is malformed
-    if (listR) {
-      if ((uint32_t)t < R) {
-        const uint32_t pos = xaR + aR;
-        const uint32_t v = load_u16(rstream + 2 * t);
-        if (pos >= L || (v & kSignExp) == 0 || s_mask[pos] != 0) bad = true;
-        else s_mask[pos] = (uint16_t)v;
-      }
-    } else {
-      if (totaR + totbR != R) bad = true;
-      uint32_t r = xaR;
-      for (uint32_t bits = byteRa; bits; bits &= bits - 1, r++) {
-        const uint32_t pos = 8 * t + __ffs(bits) - 1;
-        if (r >= R || pos >= L) { bad = true; break; }
-        const uint32_t v = load_u16(rstream + 2 * r);
-        if ((v & kSignExp) == 0 || s_mask[pos] != 0) bad = true; else s_mask[pos] = (uint16_t)v;
-      }
-      r = xbR;
-      for (uint32_t bits = byteRb; bits; bits &= bits - 1, r++) {
-        const uint32_t pos = 8 * (t + 256) + __ffs(bits) - 1;
-        if (r >= R || pos >= L) { bad = true; break; }
-        const uint32_t v = load_u16(rstream + 2 * r);
-        if ((v & kSignExp) == 0 || s_mask[pos] != 0) bad = true; else s_mask[pos] = (uint16_t)v;
+      __syncthreads();
+      // scatter the rare values; a position already holding a mantissa value is malformed
+      if (listR) {
+        if ((uint32_t)t < R) {
+          const uint32_t pos = xaR + aR;
+          const uint32_t v = load_u16(rstream + 2 * t);
+          if (pos >= L || (v & kSignExp) == 0 || s_mask[pos] != 0) bad = true;
+          else s_mask[pos] = (uint16_t)v;
+        }
+      } else {
+        if (totaR + totbR != R) bad = true;
+        uint32_t r = xaR;
+        for (uint32_t bits = byteRa; bits; bits &= bits - 1, r++) {
+          const uint32_t pos = 8 * t + __ffs(bits) - 1;
+          if (r >= R || pos >= L) { bad = true; break; }
+          const uint32_t v = load_u16(rstream + 2 * r);
+          if ((v & kSignExp) == 0 || s_mask[pos] != 0) bad = true; else s_mask[pos] = (uint16_t)v;
+        }
+        r = xbR;
+        for (uint32_t bits = byteRb; bits; bits &= bits - 1, r++) {
+          const uint32_t pos = 8 * (t + 256) + __ffs(bits) - 1;
+          if (r >= R || pos >= L) { bad = true; break; }
+          const uint32_t v = load_u16(rstream + 2 * r);
+          if ((v & kSignExp) == 0 || s_mask[pos] != 0) bad = true; else s_mask[pos] = (uint16_t)v;
+        }
       }
     }
     if (bad) s_bad = 1;
@@ -359,6 +433,80 @@ __device__ __forceinline__ uint64_t hash_chunk(const uint16_t* w, uint64_t n, ui
   return ck;
 }
 
+// 7-bit value m of the M stream whose first value starts at bit s0 of mbytes; the caller
+// guarantees m < the chunk's M, so the second byte is read only when the value crosses into it.
+__device__ __forceinline__ uint32_t mant_at(const uint8_t* __restrict__ mbytes, uint32_t s0,
+                                            uint32_t m) {
+  const uint32_t bit = s0 + 7 * m, sh = bit & 7;
+  uint32_t v = (uint32_t)mbytes[bit >> 3] >> sh;
+  if (sh > 1) v |= (uint32_t)mbytes[(bit >> 3) + 1] << (8 - sh);
+  return v & kMant;
+}
+
+// Decodes a version-3 compact chunk (one warp) into ent[0..M+R) as pos << 16 | XOR value in
+// ascending position, 32 changes at a time: gap bytes from blk (a zero byte takes the next
+// X-stream value, which must exceed 255; at most E of them, and exactly E), positions from
+// the prefix sums of the gaps (first position = first gap - 1, all below L), classes from the
+// class bits at blk + M + R (exactly R set, pad bits zero), mantissa-only values from the M
+// stream (nonzero), rare values from the R stream (a sign or exponent bit set).  Returns
+// whether the chunk is malformed (the same on every lane).
+__device__ __forceinline__ bool decode_compact(const uint8_t* __restrict__ blk,
+                                               const uint16_t* __restrict__ xs, uint32_t E,
+                                               const uint8_t* __restrict__ mbytes, uint32_t s0,
+                                               const uint16_t* __restrict__ rvals, uint32_t M,
+                                               uint32_t R, uint32_t L, uint32_t* __restrict__ ent) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t lt = (1u << lane) - 1;
+  const uint32_t k = M + R;
+  const uint8_t* __restrict__ cls = blk + k;
+  bool bad = false;
+  uint32_t carry = 0xFFFFFFFFu, xr = 0, mr = 0, rr = 0;
+  for (uint32_t b0 = 0; b0 < k; b0 += 32) {
+    const uint32_t i = b0 + lane;
+    const bool in = i < k;
+    uint32_t g = in ? (uint32_t)blk[i] : 0u;
+    const bool esc = in && g == 0;
+    const uint32_t bE = __ballot_sync(kFull, esc);
+    if (esc) {
+      const uint32_t xi = xr + __popc(bE & lt);
+      if (xi < E) g = xs[xi];
+      if (g <= 255) bad = true;
+    }
+    xr += __popc(bE);
+    const uint32_t p = carry + warp_incl_scan(g);
+    carry = __shfl_sync(kFull, p, 31);
+    const bool isR = in && ((cls[i >> 3] >> (i & 7)) & 1u);
+    const uint32_t bR = __ballot_sync(kFull, isR), bM = __ballot_sync(kFull, in && !isR);
+    if (in) {
+      uint32_t v = 0;
+      if (isR) {
+        const uint32_t r = rr + __popc(bR & lt);
+        if (r < R) v = rvals[r];
+        if ((v & kSignExp) == 0) bad = true;
+      } else {
+        const uint32_t m = mr + __popc(bM & lt);
+        if (m < M) v = mant_at(mbytes, s0, m);
+        if (v == 0) bad = true;
+      }
+      if (p >= L) bad = true;
+      if (!bad) ent[i] = (p << 16) | v;
+    }
+    mr += __popc(bM);
+    rr += __popc(bR);
+  }
+  if (xr != E || rr != R) bad = true;
+  if (lane == 0 && (k & 7) != 0 && (cls[(k - 1) >> 3] >> (k & 7)) != 0) bad = true;
+  return __any_sync(kFull, bad);
+}
+
+// Entry i of a u16 delta list.  Versions 1 and 2 place every list at an even offset; after an
+// odd-length compact block of version 3 one may start at an odd offset.
+template <bool V3>
+__device__ __forceinline__ uint32_t list_entry(const uint8_t* __restrict__ list, uint32_t i) {
+  if (V3) return load_u16(list + 2 * i);
+  return reinterpret_cast<const uint16_t*>(list)[i];
+}
+
 // One warp per chunk of every tensor whose scan status is BD_OK, each warp taking a contiguous
 // range of chunks.  A chunk whose two position blocks are delta lists is decoded and checked
 // in full into shared memory (positions from the prefix sums of the deltas, 7-bit values from
@@ -370,12 +518,14 @@ __device__ __forceinline__ uint64_t hash_chunk(const uint16_t* w, uint64_t n, ui
 // prefetched into L2 before the decode starts, so that the atomics and the read-back find it
 // there (prefetching a later chunk instead thrashes L2 and was much slower).  Chunks with a
 // bitmap block are listed for apply_dense, which also adds their checksum terms.
+template <bool V3>
 __global__ void __launch_bounds__(kThreads, 3)
 k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
                const uint64_t* __restrict__ tile_start, uint32_t k, uint64_t total_chunks,
                const uint4* __restrict__ loc, const TileSum* __restrict__ tile_pre,
                JobInfo* __restrict__ info, uint32_t* __restrict__ list_count,
                uint32_t* __restrict__ list, uint8_t* __restrict__ ck_base) {
+  if ((list_count[kFlagV3Word] != 0) != V3) return;   // the other build runs this call
   __shared__ uint32_t s_ent[kWarps][kEntMax];       // pos << 16 | XOR value
   __shared__ uint4 s_bits[kWarps][kChunk / 128];    // mantissa-only positions, 512 B
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -401,10 +551,10 @@ k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
     const uint32_t L = (n - e0) < kChunk ? (uint32_t)(n - e0) : kChunk;
     const uint32_t B = (L + 7) >> 3;
     const uint8_t* __restrict__ payload = J.payload;
-    const uint32_t cnt = reinterpret_cast<const uint32_t*>(
-        payload + count_table_offset(info[j].r_start, J.nchunks))[c];
-    const uint32_t M = cnt & 0xFFFFu, R = cnt >> 16;
-    if (2 * M >= B || 2 * R >= B) {
+    const ChunkCount cc = parse_count(reinterpret_cast<const uint32_t*>(
+        payload + count_table_offset(info[j].r_start, J.nchunks))[c], V3 ? I.version : 1u);
+    const uint32_t M = cc.M, R = cc.R;
+    if (!cc.compact && (2 * M >= B || 2 * R >= B)) {
       if (lane == 0) list[atomicAdd(list_count, 1u)] = (uint32_t)g;
       continue;
     }
@@ -414,54 +564,60 @@ k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
       const TileSum pre = tile_pre[tile_start[j] + c / kTileChunks];
       const uint4 lc = loc[g];
       const uint64_t Pex = pre.p + lc.x, Mex = pre.m + lc.y, Rex = pre.r + lc.z;
-      // Every position block before a tensor's last chunk has an even length (2k or 512
-      // bytes) and the position section starts at 64 + 4C + 2*sum(R), so both lists and the
-      // rare values are 2-byte aligned.
-      const uint16_t* mlist = reinterpret_cast<const uint16_t*>(payload + I.p_start + Pex);
-      const uint16_t* rlist = mlist + M;
+      // The rare values are 2-byte aligned (the R stream starts at the even offset
+      // header + 4C); the delta lists are too in versions 1 and 2, but may start at an odd
+      // offset after a compact block of version 3, hence the alignment-checking loads.
+      const uint8_t* mlist = payload + I.p_start + Pex;
+      const uint8_t* rlist = mlist + 2 * M;
       const uint16_t* rvals = reinterpret_cast<const uint16_t*>(payload + I.r_start) + Rex;
       const uint64_t mbit0 = 7 * Mex;
       const uint8_t* mbytes = payload + I.m_start + (mbit0 >> 3);
       const uint32_t s0 = (uint32_t)(mbit0 & 7);
       const bool both = M > 0 && R > 0;
       bool bad = false;
-      if (both) s_bits[w][lane] = make_uint4(0, 0, 0, 0);
-      __syncwarp();
-      uint32_t carry = 0;
-      for (uint32_t b0 = 0; b0 < M; b0 += 32) {
-        const uint32_t i = b0 + lane;
-        const bool in = i < M;
-        const uint32_t d = in ? (uint32_t)mlist[i] : 0u;
-        if (in && i > 0 && d == 0) bad = true;
-        const uint32_t p = carry + warp_incl_scan(d);
-        carry = __shfl_sync(kFull, p, 31);
-        if (in) {
-          const uint32_t bit = s0 + 7 * i, sh = bit & 7;
-          uint32_t v = (uint32_t)mbytes[bit >> 3] >> sh;
-          if (sh > 1) v |= (uint32_t)mbytes[(bit >> 3) + 1] << (8 - sh);
-          v &= kMant;
-          if (p >= L || v == 0) {
-            bad = true;
-          } else {
-            ent[i] = (p << 16) | v;
-            if (both) atomicOr(&bits[p >> 5], 1u << (p & 31));
+      if (V3 && cc.compact) {
+        bad = decode_compact(mlist,
+                             reinterpret_cast<const uint16_t*>(payload + I.x_start) + pre.e + lc.w,
+                             cc.E, mbytes, s0, rvals, M, R, L, ent);
+      } else {
+        if (both) s_bits[w][lane] = make_uint4(0, 0, 0, 0);
+        __syncwarp();
+        uint32_t carry = 0;
+        for (uint32_t b0 = 0; b0 < M; b0 += 32) {
+          const uint32_t i = b0 + lane;
+          const bool in = i < M;
+          const uint32_t d = in ? list_entry<V3>(mlist, i) : 0u;
+          if (in && i > 0 && d == 0) bad = true;
+          const uint32_t p = carry + warp_incl_scan(d);
+          carry = __shfl_sync(kFull, p, 31);
+          if (in) {
+            const uint32_t bit = s0 + 7 * i, sh = bit & 7;
+            uint32_t v = (uint32_t)mbytes[bit >> 3] >> sh;
+            if (sh > 1) v |= (uint32_t)mbytes[(bit >> 3) + 1] << (8 - sh);
+            v &= kMant;
+            if (p >= L || v == 0) {
+              bad = true;
+            } else {
+              ent[i] = (p << 16) | v;
+              if (both) atomicOr(&bits[p >> 5], 1u << (p & 31));
+            }
           }
         }
-      }
-      __syncwarp();
-      carry = 0;
-      for (uint32_t b0 = 0; b0 < R; b0 += 32) {
-        const uint32_t i = b0 + lane;
-        const bool in = i < R;
-        const uint32_t d = in ? (uint32_t)rlist[i] : 0u;
-        if (in && i > 0 && d == 0) bad = true;
-        const uint32_t p = carry + warp_incl_scan(d);
-        carry = __shfl_sync(kFull, p, 31);
-        if (in) {
-          const uint32_t v = rvals[i];
-          if (p >= L || (v & kSignExp) == 0) bad = true;
-          else if (both && ((bits[p >> 5] >> (p & 31)) & 1u)) bad = true;
-          else ent[M + i] = (p << 16) | v;
+        __syncwarp();
+        carry = 0;
+        for (uint32_t b0 = 0; b0 < R; b0 += 32) {
+          const uint32_t i = b0 + lane;
+          const bool in = i < R;
+          const uint32_t d = in ? list_entry<V3>(rlist, i) : 0u;
+          if (in && i > 0 && d == 0) bad = true;
+          const uint32_t p = carry + warp_incl_scan(d);
+          carry = __shfl_sync(kFull, p, 31);
+          if (in) {
+            const uint32_t v = rvals[i];
+            if (p >= L || (v & kSignExp) == 0) bad = true;
+            else if (both && ((bits[p >> 5] >> (p & 31)) & 1u)) bad = true;
+            else ent[M + i] = (p << 16) | v;
+          }
         }
       }
       if (__any_sync(kFull, bad)) {
@@ -494,12 +650,14 @@ k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
 // Changes to the same word are serialised by the atomics, so their terms telescope to the
 // word's final term minus its original one.  Nothing else of the chunk is read.  Chunks with
 // a bitmap block are listed for apply_dense<true>.
-__global__ void __launch_bounds__(kThreads, 4)
+template <bool V3>
+__global__ void __launch_bounds__(kThreads, V3 ? 3 : 4)
 k_apply_incr(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
              const uint64_t* __restrict__ tile_start, uint32_t k, uint64_t total_chunks,
              const uint4* __restrict__ loc, const TileSum* __restrict__ tile_pre,
              JobInfo* __restrict__ info, uint32_t* __restrict__ list_count,
              uint32_t* __restrict__ list, uint8_t* __restrict__ ck_base) {
+  if ((list_count[kFlagV3Word] != 0) != V3) return;   // the other build runs this call
   __shared__ uint32_t s_ent[kWarps][kEntMax];       // pos << 16 | XOR value
   __shared__ uint4 s_bits[kWarps][kChunk / 128];    // mantissa-only positions, 512 B
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -525,10 +683,10 @@ k_apply_incr(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
     const uint32_t L = (n - e0) < kChunk ? (uint32_t)(n - e0) : kChunk;
     const uint32_t B = (L + 7) >> 3;
     const uint8_t* __restrict__ payload = J.payload;
-    const uint32_t cnt = reinterpret_cast<const uint32_t*>(
-        payload + count_table_offset(info[j].r_start, J.nchunks))[c];
-    const uint32_t M = cnt & 0xFFFFu, R = cnt >> 16;
-    if (2 * M >= B || 2 * R >= B) {
+    const ChunkCount cc = parse_count(reinterpret_cast<const uint32_t*>(
+        payload + count_table_offset(info[j].r_start, J.nchunks))[c], V3 ? I.version : 1u);
+    const uint32_t M = cc.M, R = cc.R;
+    if (!cc.compact && (2 * M >= B || 2 * R >= B)) {
       if (lane == 0) list[atomicAdd(list_count, 1u)] = (uint32_t)g;
       continue;
     }
@@ -536,52 +694,58 @@ k_apply_incr(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
     const TileSum pre = tile_pre[tile_start[j] + c / kTileChunks];
     const uint4 lc = loc[g];
     const uint64_t Pex = pre.p + lc.x, Mex = pre.m + lc.y, Rex = pre.r + lc.z;
-    // both lists and the rare values are 2-byte aligned (see apply_chunks)
-    const uint16_t* mlist = reinterpret_cast<const uint16_t*>(payload + I.p_start + Pex);
-    const uint16_t* rlist = mlist + M;
+    // the rare values are 2-byte aligned, the delta lists not always (see apply_chunks)
+    const uint8_t* mlist = payload + I.p_start + Pex;
+    const uint8_t* rlist = mlist + 2 * M;
     const uint16_t* rvals = reinterpret_cast<const uint16_t*>(payload + I.r_start) + Rex;
     const uint64_t mbit0 = 7 * Mex;
     const uint8_t* mbytes = payload + I.m_start + (mbit0 >> 3);
     const uint32_t s0 = (uint32_t)(mbit0 & 7);
     const bool both = M > 0 && R > 0;
     bool bad = false;
-    if (both) s_bits[w][lane] = make_uint4(0, 0, 0, 0);
-    __syncwarp();
-    uint32_t carry = 0;
-    for (uint32_t b0 = 0; b0 < M; b0 += 32) {
-      const uint32_t i = b0 + lane;
-      const bool in = i < M;
-      const uint32_t d = in ? (uint32_t)mlist[i] : 0u;
-      if (in && i > 0 && d == 0) bad = true;
-      const uint32_t p = carry + warp_incl_scan(d);
-      carry = __shfl_sync(kFull, p, 31);
-      if (in) {
-        const uint32_t bit = s0 + 7 * i, sh = bit & 7;
-        uint32_t v = (uint32_t)mbytes[bit >> 3] >> sh;
-        if (sh > 1) v |= (uint32_t)mbytes[(bit >> 3) + 1] << (8 - sh);
-        v &= kMant;
-        if (p >= L || v == 0) {
-          bad = true;
-        } else {
-          ent[i] = (p << 16) | v;
-          if (both) atomicOr(&bits[p >> 5], 1u << (p & 31));
+    if (V3 && cc.compact) {
+      bad = decode_compact(mlist,
+                           reinterpret_cast<const uint16_t*>(payload + I.x_start) + pre.e + lc.w,
+                           cc.E, mbytes, s0, rvals, M, R, L, ent);
+    } else {
+      if (both) s_bits[w][lane] = make_uint4(0, 0, 0, 0);
+      __syncwarp();
+      uint32_t carry = 0;
+      for (uint32_t b0 = 0; b0 < M; b0 += 32) {
+        const uint32_t i = b0 + lane;
+        const bool in = i < M;
+        const uint32_t d = in ? list_entry<V3>(mlist, i) : 0u;
+        if (in && i > 0 && d == 0) bad = true;
+        const uint32_t p = carry + warp_incl_scan(d);
+        carry = __shfl_sync(kFull, p, 31);
+        if (in) {
+          const uint32_t bit = s0 + 7 * i, sh = bit & 7;
+          uint32_t v = (uint32_t)mbytes[bit >> 3] >> sh;
+          if (sh > 1) v |= (uint32_t)mbytes[(bit >> 3) + 1] << (8 - sh);
+          v &= kMant;
+          if (p >= L || v == 0) {
+            bad = true;
+          } else {
+            ent[i] = (p << 16) | v;
+            if (both) atomicOr(&bits[p >> 5], 1u << (p & 31));
+          }
         }
       }
-    }
-    __syncwarp();
-    carry = 0;
-    for (uint32_t b0 = 0; b0 < R; b0 += 32) {
-      const uint32_t i = b0 + lane;
-      const bool in = i < R;
-      const uint32_t d = in ? (uint32_t)rlist[i] : 0u;
-      if (in && i > 0 && d == 0) bad = true;
-      const uint32_t p = carry + warp_incl_scan(d);
-      carry = __shfl_sync(kFull, p, 31);
-      if (in) {
-        const uint32_t v = rvals[i];
-        if (p >= L || (v & kSignExp) == 0) bad = true;
-        else if (both && ((bits[p >> 5] >> (p & 31)) & 1u)) bad = true;
-        else ent[M + i] = (p << 16) | v;
+      __syncwarp();
+      carry = 0;
+      for (uint32_t b0 = 0; b0 < R; b0 += 32) {
+        const uint32_t i = b0 + lane;
+        const bool in = i < R;
+        const uint32_t d = in ? list_entry<V3>(rlist, i) : 0u;
+        if (in && i > 0 && d == 0) bad = true;
+        const uint32_t p = carry + warp_incl_scan(d);
+        carry = __shfl_sync(kFull, p, 31);
+        if (in) {
+          const uint32_t v = rvals[i];
+          if (p >= L || (v & kSignExp) == 0) bad = true;
+          else if (both && ((bits[p >> 5] >> (p & 31)) & 1u)) bad = true;
+          else ent[M + i] = (p << 16) | v;
+        }
       }
     }
     if (__any_sync(kFull, bad)) {
@@ -692,20 +856,33 @@ int blocks_per_sm(K kernel) {
 
 }  // namespace
 
+// Launches both builds of a thread-level apply kernel (versions 1-2 only, any version); the
+// scan's version-3 word decides on the device which of them works.
+template <typename K>
+cudaError_t launch_both(const LaunchCtx& c, K k12, int per_sm12, K k3, int per_sm3) {
+  const uint64_t want = (c.chunks + kWarps - 1) / kWarps;
+  for (int b = 0; b < 2; b++) {
+    const uint64_t grid = std::min<uint64_t>(want, (uint64_t)(b ? per_sm3 : per_sm12) * c.sms);
+    (b ? k3 : k12)<<<(unsigned)grid, kThreads, 0, c.stream>>>(
+        reinterpret_cast<const DJob*>(c.ws + c.lay.jobs),
+        reinterpret_cast<const uint64_t*>(c.ws + c.lay.chunk_start),
+        reinterpret_cast<const uint64_t*>(c.ws + c.lay.tile_start), c.k, c.chunks,
+        reinterpret_cast<const uint4*>(c.ws + c.lay.loc),
+        reinterpret_cast<const TileSum*>(c.ws + c.lay.tile_pre),
+        reinterpret_cast<JobInfo*>(c.ws + c.lay.info),
+        reinterpret_cast<uint32_t*>(c.ws + c.lay.overflow),
+        reinterpret_cast<uint32_t*>(c.ws + c.lay.ovf_list), c.ws + c.lay.ck);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 cudaError_t launch_apply_chunks(const LaunchCtx& c) {
   if (c.chunks == 0) return cudaSuccess;
-  static const int per_sm = blocks_per_sm(k_apply_chunks);
-  const uint64_t grid = std::min<uint64_t>((c.chunks + kWarps - 1) / kWarps, (uint64_t)per_sm * c.sms);
-  k_apply_chunks<<<(unsigned)grid, kThreads, 0, c.stream>>>(
-      reinterpret_cast<const DJob*>(c.ws + c.lay.jobs),
-      reinterpret_cast<const uint64_t*>(c.ws + c.lay.chunk_start),
-      reinterpret_cast<const uint64_t*>(c.ws + c.lay.tile_start), c.k, c.chunks,
-      reinterpret_cast<const uint4*>(c.ws + c.lay.loc),
-      reinterpret_cast<const TileSum*>(c.ws + c.lay.tile_pre),
-      reinterpret_cast<JobInfo*>(c.ws + c.lay.info),
-      reinterpret_cast<uint32_t*>(c.ws + c.lay.overflow),
-      reinterpret_cast<uint32_t*>(c.ws + c.lay.ovf_list), c.ws + c.lay.ck);
-  return cudaGetLastError();
+  static const int per_sm12 = blocks_per_sm(k_apply_chunks<false>);
+  static const int per_sm3 = blocks_per_sm(k_apply_chunks<true>);
+  return launch_both(c, k_apply_chunks<false>, per_sm12, k_apply_chunks<true>, per_sm3);
 }
 
 cudaError_t launch_copy_jobs(const LaunchCtx& c) {
@@ -721,18 +898,9 @@ cudaError_t launch_copy_jobs(const LaunchCtx& c) {
 
 cudaError_t launch_apply_incremental(const LaunchCtx& c) {
   if (c.chunks == 0) return cudaSuccess;
-  static const int per_sm = blocks_per_sm(k_apply_incr);
-  const uint64_t grid = std::min<uint64_t>((c.chunks + kWarps - 1) / kWarps, (uint64_t)per_sm * c.sms);
-  k_apply_incr<<<(unsigned)grid, kThreads, 0, c.stream>>>(
-      reinterpret_cast<const DJob*>(c.ws + c.lay.jobs),
-      reinterpret_cast<const uint64_t*>(c.ws + c.lay.chunk_start),
-      reinterpret_cast<const uint64_t*>(c.ws + c.lay.tile_start), c.k, c.chunks,
-      reinterpret_cast<const uint4*>(c.ws + c.lay.loc),
-      reinterpret_cast<const TileSum*>(c.ws + c.lay.tile_pre),
-      reinterpret_cast<JobInfo*>(c.ws + c.lay.info),
-      reinterpret_cast<uint32_t*>(c.ws + c.lay.overflow),
-      reinterpret_cast<uint32_t*>(c.ws + c.lay.ovf_list), c.ws + c.lay.ck);
-  return cudaGetLastError();
+  static const int per_sm12 = blocks_per_sm(k_apply_incr<false>);
+  static const int per_sm3 = blocks_per_sm(k_apply_incr<true>);
+  return launch_both(c, k_apply_incr<false>, per_sm12, k_apply_incr<true>, per_sm3);
 }
 
 cudaError_t launch_apply(const LaunchCtx& c, bool incremental) {

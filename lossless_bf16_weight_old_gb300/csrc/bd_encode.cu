@@ -68,7 +68,7 @@ __device__ __forceinline__ uint64_t hash_group_full(uint4 v, uint64_t key) {
 }
 
 // ------------------------------------------------------------------------ encode_slots
-template <bool FULL>
+template <bool FULL, bool COMPACT>
 __device__ __forceinline__ void encode_chunk(const uint16_t* __restrict__ old,
                                              const uint16_t* __restrict__ neu, uint64_t n,
                                              uint64_t e0, uint32_t* __restrict__ slot,
@@ -84,6 +84,8 @@ __device__ __forceinline__ void encode_chunk(const uint16_t* __restrict__ old,
   uint32_t running = 0;        // changes in the steps done so far
   uint32_t nl = 0, rl = 0;     // this lane's changes, and its rare ones
   uint32_t fm = 0;             // first mantissa value | kAuxHasM once found
+  int32_t lastp = -1;          // COMPACT: position of the chunk's last change so far
+  uint32_t esc = 0;            // COMPACT: gaps above 255 in the chunk's merged position list
   uint64_t e = e0 + lane * 16;
   uint4 o0, o1, n0, n1;
   if (FULL) {
@@ -123,6 +125,18 @@ __device__ __forceinline__ void encode_chunk(const uint16_t* __restrict__ old,
       xs[0] = x0;
       xs[1] = x1;
     }
+    if (COMPACT) {
+      // only a lane's first change can follow a gap above 255 (its others are < 16 apart); its
+      // predecessor is the last change of the lanes below or of the steps before
+      const int32_t last = nz ? (int32_t)(eloc + 31 - __clz(nz)) : -1;
+      const int32_t incl_last = warp_incl_max(last);
+      int32_t prev = __shfl_up_sync(0xFFFFFFFFu, incl_last, 1);
+      if (lane == 0) prev = -1;
+      prev = max(prev, lastp);
+      const bool big = nz != 0 && (int32_t)(eloc + __ffs(nz) - 1) - prev > 255;
+      esc += __popc(__ballot_sync(0xFFFFFFFFu, big));
+      lastp = max(lastp, __shfl_sync(0xFFFFFFFFu, incl_last, 31));
+    }
     const uint32_t cnt = __popc(nz);
     const uint32_t incl = warp_incl_scan(cnt);
     uint32_t idx = running + incl - cnt;
@@ -156,11 +170,12 @@ __device__ __forceinline__ void encode_chunk(const uint16_t* __restrict__ old,
     const bool overflow = runM + runR > kSlotEntries;
     slot[0] = overflow ? kSlotOverflow : slot_info(runM, runR);
     slot[1] = fm;
-    counts[g] = runM | (runR << 16);
+    counts[g] = wcount(runM, runR, esc);
     if (overflow) list[atomicAdd(list_count, 1u)] = (uint32_t)g;
   }
 }
 
+template <bool COMPACT>
 __global__ void __launch_bounds__(kThreads, 4)
 k_encode_slots(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
                uint32_t k, uint64_t total_chunks, uint32_t* __restrict__ counts,
@@ -193,11 +208,11 @@ k_encode_slots(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
       prefetch_chunk_l2(jobs[j].neu + e0);
     }
     if (e0 + kChunk <= n)
-      encode_chunk<true>(jobs[j].old, jobs[j].neu, n, e0, slot, ck, g, counts, list_count, list,
-                         s_xs[threadIdx.x]);
+      encode_chunk<true, COMPACT>(jobs[j].old, jobs[j].neu, n, e0, slot, ck, g, counts,
+                                  list_count, list, s_xs[threadIdx.x]);
     else
-      encode_chunk<false>(jobs[j].old, jobs[j].neu, n, e0, slot, ck, g, counts, list_count, list,
-                          s_xs[threadIdx.x]);
+      encode_chunk<false, COMPACT>(jobs[j].old, jobs[j].neu, n, e0, slot, ck, g, counts,
+                                   list_count, list, s_xs[threadIdx.x]);
   }
   if (cur != 0xFFFFFFFFu) {
     const uint64_t s = warp_sum64(ck);
@@ -321,10 +336,10 @@ __device__ __forceinline__ uint32_t next_mant_value(uint64_t g, uint64_t g_end, 
                                                     const uint32_t* __restrict__ counts,
                                                     const uint8_t* __restrict__ slots) {
   const int lane = threadIdx.x & 31;
-  if (g + 1 < g_end && (cnt_next & 0xFFFFu) != 0) return aux_next & kMant;
+  if (g + 1 < g_end && wcount_m(cnt_next) != 0) return aux_next & kMant;
   for (uint64_t gg = g + 2; gg < g_end; gg += 32) {  // rare: chunks without mantissa values
     const uint64_t q = gg + lane;
-    const bool has = q < g_end && (counts[q] & 0xFFFFu) != 0;
+    const bool has = q < g_end && wcount_m(counts[q]) != 0;
     const uint32_t bal = __ballot_sync(0xFFFFFFFFu, has);
     if (bal) {
       const uint64_t gn = gg + __ffs(bal) - 1;
@@ -334,11 +349,56 @@ __device__ __forceinline__ uint32_t next_mant_value(uint64_t g, uint64_t g_end, 
   return 0;
 }
 
-// Sets up the output pointers of chunk c (counts cnt, exclusive prefixes Pex / Rex).
+// Output of a version-3 compact chunk.
+struct CompactOut {
+  uint8_t* blk;        // the chunk's k gap bytes; its class bytes follow at blk + k
+  uint16_t* xs;        // X stream at the chunk's first escaped gap
+  uint16_t* rstream;   // R stream at the chunk's first rare value
+  uint8_t* mv;         // shared: the chunk's 7-bit mantissa values by chunk-local rank
+  uint32_t k;          // changes of the chunk
+};
+struct CompactState {
+  uint32_t prev;           // position of the last change emitted (0xFFFFFFFF before the first)
+  uint32_t i, m, r, x;     // changes, mantissa-only values, rare values, escapes emitted
+};
+
+// Emits the 32 changes cs.i .. cs.i+31 of a compact chunk in position order, lane l holding
+// change cs.i + l as pos << 16 | x when `valid` (the valid lanes are a prefix; cs.i is a
+// multiple of 32).  Gap g = pos - previous position (pos + 1 for the first change) goes to
+// byte cs.i + l, or 0 there and g to the X stream when g > 255; the class bits of the batch
+// are 4 whole bytes of the class section, written by lanes 0..3.
+__device__ __forceinline__ void compact_batch(uint32_t e, bool valid, CompactState& cs,
+                                              const CompactOut& o) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t lt = (1u << lane) - 1;
+  const uint32_t pos = e >> 16, x = e & 0xFFFFu;
+  uint32_t prev = __shfl_up_sync(0xFFFFFFFFu, pos, 1);
+  if (lane == 0) prev = cs.prev;
+  const uint32_t gap = pos - prev;
+  const bool isR = valid && (x & kSignExp) != 0;
+  const bool isM = valid && (x & kSignExp) == 0;
+  const bool esc = valid && gap > 255;
+  const uint32_t bM = __ballot_sync(0xFFFFFFFFu, isM), bR = __ballot_sync(0xFFFFFFFFu, isR),
+                 bE = __ballot_sync(0xFFFFFFFFu, esc);
+  if (valid) {
+    o.blk[cs.i + lane] = esc ? (uint8_t)0 : (uint8_t)gap;
+    if (esc) o.xs[cs.x + __popc(bE & lt)] = (uint16_t)gap;
+    if (isM) o.mv[cs.m + __popc(bM & lt)] = (uint8_t)(x & kMant);
+    else o.rstream[cs.r + __popc(bR & lt)] = (uint16_t)x;
+  }
+  const uint32_t b0 = cs.i >> 3, nbytes = (o.k + 7) >> 3;
+  if (lane < 4 && b0 + lane < nbytes) o.blk[o.k + b0 + lane] = (uint8_t)(bR >> (8 * lane));
+  cs.prev = __shfl_sync(0xFFFFFFFFu, pos, 31);
+  cs.i += 32;
+  cs.m += __popc(bM);
+  cs.r += __popc(bR);
+  cs.x += __popc(bE);
+}
+
+// Sets up the output pointers of chunk c (counts M, R, exclusive prefixes Pex / Rex).
 __device__ __forceinline__ void emit_ctx(EmitCtx& cx, uint8_t* payload, const JobInfo& I,
-                                         uint32_t cnt, uint32_t B, uint64_t Pex, uint64_t Rex,
-                                         EmitSmem* sm) {
-  const uint32_t M = cnt & 0xFFFFu, R = cnt >> 16;
+                                         uint32_t M, uint32_t R, uint32_t B, uint64_t Pex,
+                                         uint64_t Rex, EmitSmem* sm) {
   cx.listM = 2 * M < B;
   cx.listR = 2 * R < B;
   cx.mblk = payload + I.p_start + Pex;
@@ -353,6 +413,7 @@ __device__ __forceinline__ void emit_ctx(EmitCtx& cx, uint8_t* payload, const Jo
 // Chunks whose changes fit their slot: the slot's single position-ordered list is split by
 // class 32 entries at a time with ballots (rank = set lanes below; the previous element of
 // the same class, for the delta, is the nearest such lane below or the carry).
+template <bool V3>
 __global__ void __launch_bounds__(kThreads)
 k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
        const uint64_t* __restrict__ tile_start, uint32_t k, uint64_t total_chunks,
@@ -385,6 +446,7 @@ k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
     const uint64_t c = g - chunk_start[j];
     const uint64_t g_job_end = chunk_start[j + 1];
     const TileSum pre = tile_pre[tile_start[j] + c / kTileChunks];
+    const uint32_t cnt_here = V3 ? counts[g] : 0u;
     const uint32_t cnt_next = g + 1 < g_job_end ? counts[g + 1] : 0u;
     const uint32_t aux_next =
         g + 1 < g_job_end ? reinterpret_cast<const uint32_t*>(slot + kSlotBytes)[1] : 0u;
@@ -408,13 +470,26 @@ k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
     const uint64_t e0 = c * kChunk;
     const uint32_t L = (n - e0) < kChunk ? (uint32_t)(n - e0) : kChunk;
     const uint32_t B = (L + 7) >> 3;
-    const uint32_t cnt = M | (R << 16);
     const uint64_t Pex = pre.p + lc.x, Mex = pre.m + lc.y, Rex = pre.r + lc.z;
+    const uint32_t nesc = wcount_e(cnt_here);
+    const bool compact = V3 && I.version == 3 && choose_compact(M, R, nesc, B);
     if (lane == 0)
       reinterpret_cast<uint32_t*>(payload + count_table_offset(I.r_start, jobs[j].nchunks))[c] =
-          cnt;
+          count_entry(V3 ? I.version : 1u, M, R, nesc, compact);
     EmitCtx cx;
-    emit_ctx(cx, payload, I, cnt, B, Pex, Rex, sm);
+    emit_ctx(cx, payload, I, M, R, B, Pex, Rex, sm);
+    if (V3 && compact) {
+      cx.listM = cx.listR = true;   // no bitmap
+      const CompactOut o{payload + I.p_start + Pex,
+                         reinterpret_cast<uint16_t*>(payload + I.x_start) + pre.e + lc.w,
+                         cx.rstream, sm->mv, kk};
+      CompactState cs{0xFFFFFFFFu, 0, 0, 0, 0};
+#pragma unroll
+      for (int q = 0; q < 8; q++) {
+        if (32u * q >= kk) break;
+        compact_batch(ent[q], 32u * q + lane < kk, cs, o);
+      }
+    }
     if (!cx.listM || !cx.listR) {
       for (int i = lane; i < 256; i += 32) sm->bm[i] = 0;
       __syncwarp();
@@ -422,22 +497,22 @@ k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
     uint32_t baseM = 0, baseR = 0, carryM = 0, carryR = 0;
 #pragma unroll
     for (int q = 0; q < 8; q++) {
-      if (32u * q >= kk) break;
+      if (compact || 32u * q >= kk) break;
       const uint32_t e = ent[q], pos = e >> 16, x = e & 0xFFFFu;
       const bool valid = 32u * q + lane < kk;
       const bool isR = valid && (x & kSignExp);
       const bool isM = valid && !(x & kSignExp);
       const uint32_t bM = __ballot_sync(0xFFFFFFFFu, isM), bR = __ballot_sync(0xFFFFFFFFu, isR);
-        // (A chunk's M block starts at an even offset: the position section starts at
-      // 64 + 4C + 2*sum(R) and every block before it in the tensor has an even length, so the
-      // delta list is written with plain 2-byte stores.)
+      // (In versions 1 and 2 every M block starts at an even offset; after an odd-length
+      // compact block of version 3 it may not, hence the alignment-checking stores there.)
       if (bR == 0 && cx.listM) {
         // no rare entry in this batch: the mantissa-only entries are the first lanes in order
         const uint32_t prevL = __shfl_up_sync(0xFFFFFFFFu, pos, 1);
         if (isM) {
           const uint32_t r = baseM + lane;
           const uint32_t prev = lane ? prevL : carryM;
-          reinterpret_cast<uint16_t*>(cx.mblk)[r] = (uint16_t)(pos - prev);
+          if (V3) store_u16(cx.mblk + 2 * r, (uint16_t)(pos - prev));
+          else reinterpret_cast<uint16_t*>(cx.mblk)[r] = (uint16_t)(pos - prev);
           sm->mv[r] = (uint8_t)(x & kMant);
         }
         const uint32_t cntM = __popc(bM);
@@ -451,7 +526,8 @@ k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
       if (isM) {
         const uint32_t r = baseM + __popc(lowM);
         const uint32_t prev = lowM ? pM : carryM;
-        if (cx.listM) reinterpret_cast<uint16_t*>(cx.mblk)[r] = (uint16_t)(pos - prev);
+        if (cx.listM && V3) store_u16(cx.mblk + 2 * r, (uint16_t)(pos - prev));
+        else if (cx.listM) reinterpret_cast<uint16_t*>(cx.mblk)[r] = (uint16_t)(pos - prev);
         else atomicOr(&sm->bm[pos >> 5], 1u << (pos & 31));
         sm->mv[r] = (uint8_t)(x & kMant);
       }
@@ -494,6 +570,8 @@ k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
 // Chunks with more changes than a slot holds (listed by encode_slots): the changes are derived
 // again from old and new, 512 elements per step; after each step the mantissa-stream bytes
 // whose two values are known are written and the value window keeps only its last value.
+// A version-3 compact chunk (at most kCompactMax changes) first gathers its changes in
+// position order into a shared list, then emits them 32 at a time as emit does.
 __global__ void __launch_bounds__(kThreads)
 k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
              const uint64_t* __restrict__ tile_start, uint32_t k,
@@ -502,10 +580,12 @@ k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
              const uint4* __restrict__ loc, const TileSum* __restrict__ tile_pre,
              const JobInfo* __restrict__ info) {
   __shared__ EmitSmem s_em[kWarps];
+  __shared__ uint32_t s_list[kWarps][kCompactMax];   // compact chunks: pos << 16 | x
   const int lane = threadIdx.x & 31;
   const uint64_t gwarp = ((uint64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
   const uint64_t nwarps = ((uint64_t)gridDim.x * kThreads) >> 5;
   EmitSmem* sm = &s_em[threadIdx.x >> 5];
+  uint32_t* lst = s_list[threadIdx.x >> 5];
   const uint32_t listed = *list_count;
   for (uint64_t li = gwarp; li < listed; li += nwarps) {
     const uint64_t g = list[li];
@@ -520,16 +600,18 @@ k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
     const uint32_t L = (n - e0) < kChunk ? (uint32_t)(n - e0) : kChunk;
     const uint32_t B = (L + 7) >> 3;
     const uint32_t cnt = counts[g];
-    const uint32_t M = cnt & 0xFFFFu;
+    const uint32_t M = wcount_m(cnt), R = wcount_r(cnt), E = wcount_e(cnt);
     const TileSum pre = tile_pre[tile_start[j] + c / kTileChunks];
     const uint4 lc = loc[g];
     const uint64_t Pex = pre.p + lc.x, Mex = pre.m + lc.y, Rex = pre.r + lc.z;
+    const bool compact = I.version == 3 && choose_compact(M, R, E, B);
     uint8_t* payload = J.payload;
     if (lane == 0)
       reinterpret_cast<uint32_t*>(payload + count_table_offset(I.r_start, jobs[j].nchunks))[c] =
-          cnt;
+          count_entry(I.version, M, R, E, compact);
     EmitCtx cx;
-    emit_ctx(cx, payload, I, cnt, B, Pex, Rex, sm);
+    emit_ctx(cx, payload, I, M, R, B, Pex, Rex, sm);
+    if (compact) cx.listM = cx.listR = true;   // no bitmap
     if (!cx.listM || !cx.listR) {
       for (int i = lane; i < 256; i += 32) sm->bm[i] = 0;
       __syncwarp();
@@ -540,7 +622,35 @@ k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
     EmitState st{0, 0, 0, 0};
     const uint16_t* __restrict__ old = J.old;
     const uint16_t* __restrict__ neu = J.neu;
-    for (int s = 0; s < 8; s++) {
+    if (compact) {
+      // the chunk's changes in position order (M + R <= kCompactMax of them)
+      uint32_t base = 0;
+      for (int s = 0; s < 8; s++) {
+        const uint32_t eloc = s * 512 + lane * 16;
+        const uint64_t e = e0 + eloc;
+        const uint4 x0 = xor4(load8(old, e, n), load8(neu, e, n));
+        const uint4 x1 = xor4(load8(old, e + 8, n), load8(neu, e + 8, n));
+        const uint32_t nz = nz_mask16(x0, x1);
+        const uint32_t cntl = __popc(nz), incl = warp_incl_scan(cntl);
+        uint32_t idx = base + incl - cntl;
+        for (uint32_t bits = nz; bits; bits &= bits - 1, idx++) {
+          const int b = __ffs(bits) - 1;
+          if (idx < kCompactMax) lst[idx] = ((eloc + b) << 16) | elem_of(b < 8 ? x0 : x1, b & 7);
+        }
+        base += __shfl_sync(0xFFFFFFFFu, incl, 31);
+      }
+      __syncwarp();
+      const uint32_t kk = M + R;
+      const CompactOut o{payload + I.p_start + Pex,
+                         reinterpret_cast<uint16_t*>(payload + I.x_start) + pre.e + lc.w,
+                         cx.rstream, sm->mv, kk};
+      CompactState cs{0xFFFFFFFFu, 0, 0, 0, 0};
+      for (uint32_t i0 = 0; i0 < kk; i0 += 32) {
+        const bool valid = i0 + lane < kk;
+        compact_batch(valid ? lst[i0 + lane] : 0u, valid, cs, o);
+      }
+    }
+    for (int s = 0; s < 8 && !compact; s++) {
       const uint32_t eloc = s * 512 + lane * 16;
       const uint64_t e = e0 + eloc;
       const uint4 x0 = xor4(load8(old, e, n), load8(neu, e, n));
@@ -601,11 +711,13 @@ uint64_t cap_grid(uint64_t want, uint64_t work_items_per_block, uint64_t items) 
 
 }  // namespace
 
-cudaError_t launch_encode_slots(const LaunchCtx& c) {
+cudaError_t launch_encode_slots(const LaunchCtx& c, bool compact) {
   if (c.chunks == 0) return cudaSuccess;
-  static const int per_sm = blocks_per_sm(k_encode_slots, kThreads);
-  const uint64_t grid = cap_grid((uint64_t)per_sm * c.sms, kWarps, c.chunks);
-  k_encode_slots<<<(unsigned)grid, kThreads, 0, c.stream>>>(
+  static const int per_sm = blocks_per_sm(k_encode_slots<false>, kThreads);
+  static const int per_sm_c = blocks_per_sm(k_encode_slots<true>, kThreads);
+  const uint64_t grid = cap_grid((uint64_t)(compact ? per_sm_c : per_sm) * c.sms, kWarps, c.chunks);
+  auto kernel = compact ? k_encode_slots<true> : k_encode_slots<false>;
+  kernel<<<(unsigned)grid, kThreads, 0, c.stream>>>(
       reinterpret_cast<const CJob*>(c.ws + c.lay.jobs),
       reinterpret_cast<const uint64_t*>(c.ws + c.lay.chunk_start), c.k, c.chunks,
       reinterpret_cast<uint32_t*>(c.ws + c.lay.counts), c.ws + c.lay.slots, c.ws + c.lay.ck,
@@ -631,11 +743,13 @@ cudaError_t launch_emit_dense(const LaunchCtx& c) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_emit(const LaunchCtx& c) {
+cudaError_t launch_emit(const LaunchCtx& c, bool v3) {
   if (c.chunks == 0) return cudaSuccess;
-  static const int per_sm = blocks_per_sm(k_emit, kThreads);
-  const uint64_t grid = cap_grid((uint64_t)per_sm * c.sms, kWarps, c.chunks);
-  k_emit<<<(unsigned)grid, kThreads, 0, c.stream>>>(
+  static const int per_sm = blocks_per_sm(k_emit<false>, kThreads);
+  static const int per_sm3 = blocks_per_sm(k_emit<true>, kThreads);
+  const uint64_t grid = cap_grid((uint64_t)(v3 ? per_sm3 : per_sm) * c.sms, kWarps, c.chunks);
+  auto kernel = v3 ? k_emit<true> : k_emit<false>;
+  kernel<<<(unsigned)grid, kThreads, 0, c.stream>>>(
       reinterpret_cast<const CJob*>(c.ws + c.lay.jobs),
       reinterpret_cast<const uint64_t*>(c.ws + c.lay.chunk_start),
       reinterpret_cast<const uint64_t*>(c.ws + c.lay.tile_start), c.k, c.chunks,

@@ -1,6 +1,6 @@
 // bd_internal.cuh -- device-side definitions shared by the kernels of libbf16delta.
 //
-// Everything here follows the BF16DLT1 v1 format described in include/bf16delta.h.
+// Everything here follows the BF16DLT1 format (versions 1 to 3) described in include/bf16delta.h.
 // The field split comes from "Every byte counts: ARCv3 and the case for cross-region RL"
 // (figure "How ARCv3 encodes a block of weights"); the XOR algebra from "GPU-accelerated
 // Weight Teleportation", section "Delta update algebra".
@@ -34,6 +34,72 @@ constexpr uint64_t kGamma = 0x9E3779B97F4A7C15ull;
 __host__ __device__ __forceinline__ uint32_t block_bytes(uint32_t k, uint32_t B) {
   return (2 * k < B) ? 2 * k : B;
 }
+
+// Version 3: compact position blocks.  A compact block holds the chunk's k = M + R changes as
+// one ascending list -- k gap bytes (first gap = position + 1; a gap above 255 is written as a
+// zero byte and its u16 value goes to the X stream) then ceil(k/8) class bytes (bit i set:
+// change i is rare).  A count-table entry is a u32: compact (bit 31) with M in bits 0..8, R in
+// 9..17 and E (escaped gaps) in 18..26, or plain (bit 31 clear) with M in bits 0..14 and R in
+// 15..29 and version-1 blocks.  Positions of a chunk are below 4096 and every escaped gap is
+// above 255, so a well-formed chunk has E <= 16.
+constexpr uint32_t kCompactMax = 508;          // most changes of a compact chunk
+constexpr uint32_t kCompactFlag = 0x80000000u;
+__host__ __device__ __forceinline__ uint32_t compact_bytes(uint32_t k) { return k + (k + 7) / 8; }
+
+// The encoder's choice: compact when the chunk has changes, at most kCompactMax of them, and
+// the compact block plus its X-stream values is smaller than the two version-1 blocks.
+__host__ __device__ __forceinline__ bool choose_compact(uint32_t M, uint32_t R, uint32_t E,
+                                                        uint32_t B) {
+  const uint32_t k = M + R;
+  return k > 0 && k <= kCompactMax &&
+         compact_bytes(k) + 2 * E < block_bytes(M, B) + block_bytes(R, B);
+}
+
+// One count-table entry, decoded for the payload's version.
+struct ChunkCount {
+  uint32_t M, R, E;   // mantissa-only and rare changes, escaped gaps (compact only)
+  bool compact;
+  bool bad;           // unused bits set, or a compact entry out of range
+};
+__host__ __device__ __forceinline__ ChunkCount parse_count(uint32_t v, uint32_t version) {
+  ChunkCount c{0, 0, 0, false, false};
+  if (version < 3) {
+    c.M = v & 0xFFFFu;
+    c.R = v >> 16;
+  } else if (v & kCompactFlag) {
+    c.compact = true;
+    c.M = v & 0x1FFu;
+    c.R = (v >> 9) & 0x1FFu;
+    c.E = (v >> 18) & 0x1FFu;
+    c.bad = (v & 0x78000000u) != 0 || c.M + c.R == 0 || c.M + c.R > kCompactMax ||
+            c.E > c.M + c.R;
+  } else {
+    c.M = v & 0x7FFFu;
+    c.R = (v >> 15) & 0x7FFFu;
+    c.bad = (v & 0x40000000u) != 0;
+  }
+  return c;
+}
+// Position-section bytes of a chunk whose bitmap has B bytes.
+__host__ __device__ __forceinline__ uint32_t chunk_pos_bytes(const ChunkCount& c, uint32_t B) {
+  return c.compact ? compact_bytes(c.M + c.R) : block_bytes(c.M, B) + block_bytes(c.R, B);
+}
+// The count-table entry written by compress.
+__host__ __device__ __forceinline__ uint32_t count_entry(uint32_t version, uint32_t M,
+                                                         uint32_t R, uint32_t E, bool compact) {
+  if (version < 3) return M | (R << 16);
+  if (compact) return kCompactFlag | M | (R << 9) | (E << 18);
+  return M | (R << 15);
+}
+
+// Compress workspace word of a chunk's counts: M in bits 0..12, R in 13..25, E (gaps above 255
+// in the merged position list, counted only for version 3) in 26..30.
+__host__ __device__ __forceinline__ uint32_t wcount(uint32_t M, uint32_t R, uint32_t E) {
+  return M | (R << 13) | (E << 26);
+}
+__host__ __device__ __forceinline__ uint32_t wcount_m(uint32_t v) { return v & 0x1FFFu; }
+__host__ __device__ __forceinline__ uint32_t wcount_r(uint32_t v) { return (v >> 13) & 0x1FFFu; }
+__host__ __device__ __forceinline__ uint32_t wcount_e(uint32_t v) { return (v >> 26) & 0x1Fu; }
 
 // SplitMix64 output function (Steele, Lea & Flood 2014) applied to a position-keyed word.
 __device__ __forceinline__ uint64_t mix64(uint64_t z) {
@@ -131,8 +197,10 @@ struct CJob {
   uint64_t chunk_base;  // global index of this tensor's chunk 0
   uint64_t nchunks;     // C = ceil(n / 4096)
   uint64_t tile_base;   // global index of this tensor's first scan tile
-  const uint64_t* d_base;   // version 2: the base checksum to bind to (NULL: version 1)
-  uint64_t pad[4];
+  const uint64_t* d_base;   // versions 2 and 3: the base checksum to bind to (NULL: version 1)
+  uint32_t version;         // payload version written: 1, 2 or 3 (compact position blocks)
+  uint32_t pad32;
+  uint64_t pad[3];
 };
 static_assert(sizeof(CJob) == 128, "CJob layout");
 
@@ -156,12 +224,15 @@ static_assert(sizeof(DJob) == 128, "DJob layout");
 
 // Per-tensor results of the scan phase (workspace).
 struct JobInfo {
-  uint64_t sum_m, sum_r, sum_p;   // totals
-  uint64_t r_start, p_start, m_start, total;
+  uint64_t sum_m, sum_r, sum_p, sum_e;   // totals
+  uint64_t r_start, x_start, p_start, m_start, total;   // section offsets, payload size
   int32_t status;      // set by the scan phase; constant while later kernels run
   int32_t chunk_err;   // set by the apply kernel when a chunk is malformed
+  uint32_t version;    // payload version (set by the scan phase)
+  uint32_t pad32;
+  uint64_t pad;
 };
-static_assert(sizeof(JobInfo) == 64, "JobInfo layout");
+static_assert(sizeof(JobInfo) == 96, "JobInfo layout");
 
 // Checksum accumulators per tensor: kCkSlots u64 spaced one 64-byte line apart so that
 // atomics from different warps spread over L2.
@@ -173,7 +244,7 @@ constexpr int kCkBytes = kCkSlots * kCkStride * 8;
 constexpr uint32_t kTileChunks = 1024;
 
 struct TileSum {   // totals of one scan tile (or their exclusive prefix)
-  uint64_t p, m, r, pad;
+  uint64_t p, m, r, e;   // position bytes, M, R, escaped gaps (X-stream values)
 };
 
 // Per-chunk slot (workspace).  Entries are pos << 16 | x.
@@ -223,13 +294,20 @@ struct WsLayout {
   uint64_t tile_start;   // (k+1) u64
   uint64_t counts;       // Ctot u32 (compress only)
   uint64_t slots;        // Ctot * kSlotBytes
-  uint64_t loc;          // Ctot uint4: chunk exclusive prefix inside its tile (p, m, r)
+  uint64_t loc;          // Ctot uint4: chunk exclusive prefix inside its tile (p, m, r, e)
   uint64_t tile_tot;     // Utot TileSum
   uint64_t tile_pre;     // Utot TileSum
-  uint64_t overflow;     // decompress: u32 count (in the zeroed state) ...
+  uint64_t overflow;     // decompress: u32 words in the zeroed state -- the count of listed
+                         // chunks, then kFlagV3Word ...
   uint64_t ovf_list;     // ... and Ctot u32 chunk indices handled by the block-level apply
   uint64_t total;
 };
+
+// Decompress: word of the zeroed `overflow` state that the scan sets when a payload of the
+// call is version 3.  The thread-level apply kernels come in two builds, one for versions 1
+// and 2 only (no compact blocks: fewer registers, aligned list loads) and one for any
+// version; both are launched and the one that does not match this word returns at once.
+constexpr uint32_t kFlagV3Word = 1;
 
 // Index of the job containing global index g, given starts[0..k] (starts[k] = total).
 __device__ __forceinline__ uint32_t find_job(const uint64_t* __restrict__ starts, uint32_t k,
@@ -307,10 +385,10 @@ struct LaunchCtx {
   uint64_t tiles;      // total scan tiles
 };
 
-cudaError_t launch_encode_slots(const LaunchCtx& c);
+cudaError_t launch_encode_slots(const LaunchCtx& c, bool compact);
 cudaError_t launch_scan_tiles(const LaunchCtx& c, bool decompress);
 cudaError_t launch_scan_jobs(const LaunchCtx& c, bool decompress, int32_t* d_status_all);
-cudaError_t launch_emit(const LaunchCtx& c);
+cudaError_t launch_emit(const LaunchCtx& c, bool v3);
 cudaError_t launch_emit_dense(const LaunchCtx& c);
 cudaError_t launch_apply_chunks(const LaunchCtx& c);
 cudaError_t launch_apply_incremental(const LaunchCtx& c);

@@ -122,6 +122,50 @@ def test_payload_info_parses_version_2_headers(cuda_lib):
     assert info.version == 1 and info.base_checksum == 0
 
 
+def test_payload_info_parses_version_3_headers(cuda_lib):
+    rng = np.random.default_rng(12)
+    old = rng.integers(0, 1 << 16, 7 * 4096 + 7).astype(np.uint16)
+    new = old.copy()
+    new[:5 * 4096:40] ^= np.uint16(3)                   # compact chunks
+    new[3 * 4096:5 * 4096:1500] ^= np.uint16(0x4001)
+    new[5 * 4096 + 600:6 * 4096:10] ^= np.uint16(5)     # compact, first gap escaped
+    base = 0x0102030405060708
+    payload, _ = oracle.encode(old, new, base=base, compact=True)
+    C = 8
+    table = payload[80:80 + 4 * C].view(np.uint32)
+    compact = (table >> 31) == 1
+    n_esc = int(np.where(compact, (table >> 18) & 0x1FF, 0).sum())
+    assert compact.any() and (~compact).any() and n_esc > 0
+    info = _lib.PayloadInfo()
+    hdr = (ctypes.c_uint8 * 80).from_buffer_copy(payload[:80].tobytes())
+    assert cuda_lib.bd_payload_info(hdr, 80, ctypes.byref(info)) == 0
+    assert info.version == 3 and info.base_checksum == base and info.n_escapes == n_esc
+    assert info.total_size == payload.size and info.chunks == C
+    # a total that leaves an odd number of bytes (or fewer than the other sections) is refused
+    for delta in (1, -2 * n_esc - 2):
+        bad = bytearray(payload[:80].tobytes())
+        bad[56:64] = (payload.size + delta).to_bytes(8, "little")
+        b = (ctypes.c_uint8 * 80).from_buffer_copy(bytes(bad))
+        assert cuda_lib.bd_payload_info(b, 80, ctypes.byref(info)) == 3, delta
+    # version 2 and 1 report no escapes
+    p2, _ = oracle.encode(old, new, base=base)
+    h2 = (ctypes.c_uint8 * 80).from_buffer_copy(p2[:80].tobytes())
+    assert cuda_lib.bd_payload_info(h2, 80, ctypes.byref(info)) == 0
+    assert info.version == 2 and info.n_escapes == 0
+
+
+def test_version_3_bound(cuda_lib):
+    """bd_compress_bound covers version 3: never longer than version 2 of the same update."""
+    rng = np.random.default_rng(13)
+    for n in (1, 4097, 3 * 4096 + 5):
+        old = rng.integers(0, 1 << 16, n).astype(np.uint16)
+        for rate in (0.001, 0.05, 0.5, 1.0):
+            new = old ^ np.where(rng.random(n) < rate, rng.integers(1, 1 << 16, n), 0).astype(np.uint16)
+            p3, _ = oracle.encode(old, new, base=1, compact=True)
+            p2, _ = oracle.encode(old, new, base=1)
+            assert p3.size <= p2.size <= cuda_lib.bd_compress_bound(n)
+
+
 def test_argument_checks_need_no_gpu(cuda_lib):
     """Bad arguments are rejected before any CUDA call."""
     one = ctypes.c_uint64(1)
@@ -142,6 +186,14 @@ def test_argument_checks_need_no_gpu(cuda_lib):
     assert cuda_lib.bd_decompress(ctypes.c_void_p(1 << 20), 1000, ctypes.c_void_p(1 << 24),
                                   100, dummy, ctypes.c_void_p((1 << 20) + 16),
                                   ctypes.c_void_p(1 << 26), 1 << 20, dummy, None) == 1
+    # the versioned compress takes format 2 or 3 only
+    for fmt in (0, 1, 4):
+        assert cuda_lib.bd_compress_versioned(dummy, dummy, 10, ctypes.c_void_p(1 << 20), 100,
+                                              ctypes.c_void_p(1 << 24), 1 << 20, dummy, dummy,
+                                              dummy, fmt, None, None) == 1
+    base_ptrs = (ctypes.c_void_p * 1)(4096)
+    assert cuda_lib.bd_compress_versioned_batch(None, base_ptrs, 0, 7, ctypes.c_void_p(1 << 24),
+                                                1 << 20, None, None) == 1
     assert cuda_lib.bd_checksum(None, 5, dummy, None) == 1
     assert cuda_lib.bd_status_sync(None, None) == 1
     del one

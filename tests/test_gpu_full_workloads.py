@@ -1,7 +1,8 @@
 """Parity at full size on the 7B-shaped dense checkpoint and the 30B-shaped MoE checkpoint, in
 the launch configuration the benchmark times: one batched compress over every tensor of the
 checkpoint (held in one flat buffer per checkpoint, tensors at 256-byte aligned offsets), then
-one batched in-place apply on a copy of old.
+one batched in-place apply on a copy of old; the dense checkpoint also in version 3 (compact
+position blocks).
 
 The oracle checks a sample of tensors one by one (payload bytes, size, checksum; integer work,
 tolerance 0).  Every tensor is checked by properties that hold at any size: each status is OK,
@@ -12,8 +13,9 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as W
-from tests.gpu_util import oracle_pair
+from tests.gpu_util import oracle_pair, to_np_u16
 
 pytestmark = pytest.mark.gpu
 
@@ -52,21 +54,23 @@ def _cap_estimate(spec) -> int:
     return min(bd.compress_bound(n), 64 + 4 * C + per_chunk * C + int(3 * spec.rate * n) + 4096)
 
 
-def _check_workload(specs, sample):
+def _check_workload(specs, sample, compact=False):
     dev = torch.device("cuda")
     O, N, offs, ns = _flat(specs, dev)
     olds = [O[off:off + n] for off, n in zip(offs, ns)]
     news = [N[off:off + n] for off, n in zip(offs, ns)]
+    ck_old = torch.cat([bd.checksum(a).reshape(1) for a in olds])
+    bases = ck_old if compact else None   # version 3 payloads are bound to checksum(old)
     # payload room from the change rate (the worst-case bound of a 30B checkpoint would not fit
     # beside it); a tensor that needs more reports its size and the batch is run again
     caps = [_cap_estimate(s) for s in specs]
-    comp = bd.CompressBatch(olds, news, caps)
+    comp = bd.CompressBatch(olds, news, caps, base_checksums=bases, compact=compact)
     comp.run()
     torch.cuda.synchronize()
     if int(comp.status.item()) == bd.ERR_CAPACITY:
         need = [int(v) for v in comp.sizes.tolist()]
         del comp
-        comp = bd.CompressBatch(olds, news, need)
+        comp = bd.CompressBatch(olds, news, need, base_checksums=bases, compact=compact)
         comp.run()
         torch.cuda.synchronize()
     assert int(comp.status.item()) == bd.OK
@@ -74,8 +78,13 @@ def _check_workload(specs, sample):
     cks = bd.u64(comp.checksums)
 
     # sampled tensors against the oracle, byte for byte
+    ck_old_list = bd.u64(ck_old)
     for i in sample:
-        ref, ref_ck = oracle_pair(olds[i], news[i])
+        if compact:
+            ref, ref_ck = oracle.encode(to_np_u16(olds[i]), to_np_u16(news[i]),
+                                        base=ck_old_list[i], compact=True)
+        else:
+            ref, ref_ck = oracle_pair(olds[i], news[i])
         assert sizes[i] == ref.size, specs[i].name
         assert cks[i] == ref_ck, specs[i].name
         got = comp.payloads[i][:sizes[i]].cpu().numpy()
@@ -90,7 +99,6 @@ def _check_workload(specs, sample):
     assert int(fwd.status.item()) == bd.OK
     assert all(int(s) == bd.OK for s in fwd.statuses.tolist())
     assert torch.equal(R.view(torch.int16), N.view(torch.int16))
-    ck_old = torch.cat([bd.checksum(a).reshape(1) for a in olds])
     back = bd.DecompressBatch(rolls, comp.payloads, sizes, ck_old)
     back.run()
     torch.cuda.synchronize()
@@ -118,6 +126,15 @@ def test_dense7b_full_size_batched():
     sample = [names[x] for x in ("embed", "layers.0.q", "layers.0.gate", "layers.0.down",
                                  "layers.0.norm1", "layers.31.up", "norm", "lm_head")]
     _check_workload(specs, sample)
+
+
+def test_dense7b_full_size_compact():
+    """The same checkpoint in version 3 (compact position blocks), bound to checksum(old)."""
+    specs = W.dense7b()
+    names = {s.name: i for i, s in enumerate(specs)}
+    sample = [names[x] for x in ("embed", "layers.0.q", "layers.0.down", "layers.0.norm1",
+                                 "norm", "lm_head")]
+    _check_workload(specs, sample, compact=True)
 
 
 def test_moe30b_full_size_batched():
