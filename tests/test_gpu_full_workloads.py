@@ -112,7 +112,22 @@ def _check_workload(specs, sample, compact=False):
     assert int(inc.status.item()) == bd.OK
     assert bd.u64(inc.checksums) == cks
     assert torch.equal(R.view(torch.int16), N.view(torch.int16))
-    inc_back = bd.IncrementalBatch(rolls, comp.payloads, sizes, comp.checksums, ck_old)
+    back_payloads, back_sizes = comp.payloads, sizes
+    if compact:
+        # a payload bound to checksum(old) is refused from new, leaving the weights alone; the
+        # way back is the reverse update's payload, bound to checksum(new)
+        refused = bd.IncrementalBatch(rolls, comp.payloads, sizes, comp.checksums, ck_old)
+        refused.run()
+        torch.cuda.synchronize()
+        assert all(int(s) == bd.ERR_BASE for s in refused.statuses.tolist())
+        assert torch.equal(R.view(torch.int16), N.view(torch.int16))
+        rev = bd.CompressBatch(news, olds, sizes, base_checksums=comp.checksums, compact=True)
+        rev.run()
+        torch.cuda.synchronize()
+        assert int(rev.status.item()) == bd.OK
+        assert [int(v) for v in rev.sizes.tolist()] == sizes
+        back_payloads = rev.payloads
+    inc_back = bd.IncrementalBatch(rolls, back_payloads, back_sizes, comp.checksums, ck_old)
     inc_back.run()
     torch.cuda.synchronize()
     assert int(inc_back.status.item()) == bd.OK
