@@ -668,7 +668,9 @@ def run_ours(args) -> None:
         cpu["fanout"] = oracle_fanout(specs, args.cpu_sample_elems)
 
     blobs_c = -(-(128 * len(specs) + 2 * 8 * (len(specs) + 1) + 1024) // 30720)
-    launches_per_step = (blobs_c + 5) + (blobs_c + 5)
+    # compress: tensor-table uploads + encode, scan x2, emit, emit_dense; decompress: uploads +
+    # scan x2, both builds of apply_chunks (one returns at once), apply_dense, apply_finish
+    launches_per_step = (blobs_c + 5) + (blobs_c + 6)
 
     if rank == 0:
         line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,

@@ -651,7 +651,7 @@ k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
 // word's final term minus its original one.  Nothing else of the chunk is read.  Chunks with
 // a bitmap block are listed for apply_dense<true>.
 template <bool V3>
-__global__ void __launch_bounds__(kThreads, V3 ? 3 : 4)
+__global__ void __launch_bounds__(kThreads, 4)
 k_apply_incr(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
              const uint64_t* __restrict__ tile_start, uint32_t k, uint64_t total_chunks,
              const uint4* __restrict__ loc, const TileSum* __restrict__ tile_pre,
@@ -761,12 +761,15 @@ k_apply_incr(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
     const uint64_t wlast = (n - 1) >> 2;
     const uint32_t in_last = (uint32_t)(n - 4 * wlast);   // values of the last word, 1..4
     const uint64_t last_mask = in_last == 4 ? ~0ull : ((1ull << (16 * in_last)) - 1);
-    // 4 entries per lane per round: their atomics are issued back to back, then the terms
-    for (uint32_t r0 = 0; r0 < M + R; r0 += 128) {
-      uint64_t before[4], dd[4];
-      uint32_t pp[4];
+    // kB entries per lane per round: their atomics are issued back to back, then the terms
+    // (3 in the build for any version, whose compact decoder leaves fewer registers: with 4
+    // it spilled at 64 registers, and 3 blocks per SM instead was slower)
+    constexpr int kB = V3 ? 3 : 4;
+    for (uint32_t r0 = 0; r0 < M + R; r0 += 32 * kB) {
+      uint64_t before[kB], dd[kB];
+      uint32_t pp[kB];
 #pragma unroll
-      for (int u = 0; u < 4; u++) {
+      for (int u = 0; u < kB; u++) {
         const uint32_t i = r0 + 32 * u + lane;
         pp[u] = 0xFFFFFFFFu;
         if (i < M + R) {
@@ -777,7 +780,7 @@ k_apply_incr(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
         }
       }
 #pragma unroll
-      for (int u = 0; u < 4; u++) {
+      for (int u = 0; u < kB; u++) {
         if (pp[u] != 0xFFFFFFFFu) {
           uint64_t b = before[u], a = before[u] ^ dd[u];
           const uint64_t wj = (e0 >> 2) + (pp[u] >> 2);

@@ -68,6 +68,64 @@ __device__ __forceinline__ uint64_t hash_group_full(uint4 v, uint64_t key) {
 }
 
 // ------------------------------------------------------------------------ encode_slots
+
+// Gaps above 255 in a chunk's merged position list, counted from its k slot entries (position
+// order, pos << 16 | x): the first gap is p_0 + 1, then p_i - p_{i-1}.
+__device__ __forceinline__ uint32_t slot_escapes(const uint32_t* __restrict__ entries,
+                                                 uint32_t k) {
+  const int lane = threadIdx.x & 31;
+  int32_t carry = -1;
+  uint32_t esc = 0;
+  for (uint32_t i0 = 0; i0 < k; i0 += 32) {
+    const uint32_t i = i0 + lane;
+    const int32_t pos = i < k ? (int32_t)(entries[i] >> 16) : 0;
+    int32_t prev = __shfl_up_sync(0xFFFFFFFFu, pos, 1);
+    if (lane == 0) prev = carry;
+    esc += __popc(__ballot_sync(0xFFFFFFFFu, i < k && pos - prev > 255));
+    carry = __shfl_sync(0xFFFFFFFFu, pos, 31);
+  }
+  return esc;
+}
+
+// The same count for a chunk whose changes did not fit its slot, from old and new again (512
+// elements per step, 16 per lane).  Only a lane's first change can follow a gap above 255 --
+// its others are under 16 apart -- and its predecessor is the last change of the nearest lower
+// lane that has one, or of the steps before.
+template <bool FULL>
+__device__ __noinline__ uint32_t chunk_escapes(const uint16_t* __restrict__ old,
+                                               const uint16_t* __restrict__ neu, uint64_t n,
+                                               uint64_t e0) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t lt = (1u << lane) - 1;
+  int32_t lastp = -1;
+  uint32_t esc = 0;
+  for (int s = 0; s < 8; s++) {
+    const uint32_t eloc = s * 512 + lane * 16;
+    const uint64_t e = e0 + eloc;
+    uint4 o0, o1, n0, n1;
+    if (FULL) {
+      o0 = __ldg(reinterpret_cast<const uint4*>(old + e));
+      o1 = __ldg(reinterpret_cast<const uint4*>(old + e + 8));
+      n0 = __ldg(reinterpret_cast<const uint4*>(neu + e));
+      n1 = __ldg(reinterpret_cast<const uint4*>(neu + e + 8));
+    } else {
+      o0 = load8(old, e, n); o1 = load8(old, e + 8, n);
+      n0 = load8(neu, e, n); n1 = load8(neu, e + 8, n);
+    }
+    const uint32_t nz = nz_mask16(xor4(o0, n0), xor4(o1, n1));
+    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, nz != 0);
+    if (bal == 0) continue;
+    const int32_t last = (int32_t)(eloc + 31 - __clz(nz));   // meaningful where nz != 0
+    const uint32_t lower = bal & lt;
+    const int32_t below = __shfl_sync(0xFFFFFFFFu, last, lower ? 31 - __clz(lower) : 0);
+    const int32_t prev = lower ? below : lastp;
+    const bool big = nz != 0 && (int32_t)(eloc + __ffs(nz) - 1) - prev > 255;
+    esc += __popc(__ballot_sync(0xFFFFFFFFu, big));
+    lastp = __shfl_sync(0xFFFFFFFFu, last, 31 - __clz(bal));
+  }
+  return esc;
+}
+
 template <bool FULL, bool COMPACT>
 __device__ __forceinline__ void encode_chunk(const uint16_t* __restrict__ old,
                                              const uint16_t* __restrict__ neu, uint64_t n,
@@ -84,8 +142,6 @@ __device__ __forceinline__ void encode_chunk(const uint16_t* __restrict__ old,
   uint32_t running = 0;        // changes in the steps done so far
   uint32_t nl = 0, rl = 0;     // this lane's changes, and its rare ones
   uint32_t fm = 0;             // first mantissa value | kAuxHasM once found
-  int32_t lastp = -1;          // COMPACT: position of the chunk's last change so far
-  uint32_t esc = 0;            // COMPACT: gaps above 255 in the chunk's merged position list
   uint64_t e = e0 + lane * 16;
   uint4 o0, o1, n0, n1;
   if (FULL) {
@@ -125,18 +181,6 @@ __device__ __forceinline__ void encode_chunk(const uint16_t* __restrict__ old,
       xs[0] = x0;
       xs[1] = x1;
     }
-    if (COMPACT) {
-      // only a lane's first change can follow a gap above 255 (its others are < 16 apart); its
-      // predecessor is the last change of the lanes below or of the steps before
-      const int32_t last = nz ? (int32_t)(eloc + 31 - __clz(nz)) : -1;
-      const int32_t incl_last = warp_incl_max(last);
-      int32_t prev = __shfl_up_sync(0xFFFFFFFFu, incl_last, 1);
-      if (lane == 0) prev = -1;
-      prev = max(prev, lastp);
-      const bool big = nz != 0 && (int32_t)(eloc + __ffs(nz) - 1) - prev > 255;
-      esc += __popc(__ballot_sync(0xFFFFFFFFu, big));
-      lastp = max(lastp, __shfl_sync(0xFFFFFFFFu, incl_last, 31));
-    }
     const uint32_t cnt = __popc(nz);
     const uint32_t incl = warp_incl_scan(cnt);
     uint32_t idx = running + incl - cnt;
@@ -166,8 +210,17 @@ __device__ __forceinline__ void encode_chunk(const uint16_t* __restrict__ old,
   rl = warp_incl_scan(rl);
   const uint32_t runR = __shfl_sync(0xFFFFFFFFu, rl, 31);
   const uint32_t runM = __shfl_sync(0xFFFFFFFFu, nl, 31) - runR;
+  const bool overflow = runM + runR > kSlotEntries;
+  uint32_t esc = 0;   // COMPACT: gaps above 255 in the chunk's merged position list
+  if (COMPACT && runM + runR <= kCompactMax) {
+    if (!overflow) {
+      __syncwarp();   // the slot entries written by every lane are visible to the warp
+      esc = slot_escapes(entries, runM + runR);
+    } else {
+      esc = chunk_escapes<FULL>(old, neu, n, e0);
+    }
+  }
   if (lane == 0) {
-    const bool overflow = runM + runR > kSlotEntries;
     slot[0] = overflow ? kSlotOverflow : slot_info(runM, runR);
     slot[1] = fm;
     counts[g] = wcount(runM, runR, esc);
@@ -414,7 +467,7 @@ __device__ __forceinline__ void emit_ctx(EmitCtx& cx, uint8_t* payload, const Jo
 // class 32 entries at a time with ballots (rank = set lanes below; the previous element of
 // the same class, for the delta, is the nearest such lane below or the carry).
 template <bool V3>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 4)
 k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
        const uint64_t* __restrict__ tile_start, uint32_t k, uint64_t total_chunks,
        const uint32_t* __restrict__ counts, const uint8_t* __restrict__ slots,
