@@ -49,6 +49,10 @@ def _load():
         lib.orc_encode_compact.argtypes = [p, p, u64, u64, p, u64, ctypes.POINTER(u64),
                                            ctypes.POINTER(u64)]
         lib.orc_encode_compact.restype = ctypes.c_int
+        for name in ("orc_encode_overwrite", "orc_encode_compact_overwrite"):
+            fn = getattr(lib, name)
+            fn.argtypes = [p, p, u64, u64, p, u64, ctypes.POINTER(u64), ctypes.POINTER(u64)]
+            fn.restype = ctypes.c_int
         lib.orc_decode.argtypes = [p, u64, p, u64, u64, p]
         lib.orc_decode.restype = ctypes.c_int
         lib.orc_decode_incremental.argtypes = [p, u64, p, u64, u64, u64, p,
@@ -71,30 +75,29 @@ def checksum(w) -> int:
     return int(_load().orc_checksum(w.ctypes.data, w.size))
 
 
-def encode(old, new, base: int | None = None, compact: bool = False) -> tuple[np.ndarray, int]:
+def encode(old, new, base: int | None = None, compact: bool = False,
+           overwrite: bool = False) -> tuple[np.ndarray, int]:
     """Returns (payload bytes as a uint8 array, checksum of new).  With `base` (the checksum of
     old as the caller knows it) the payload is version 2, bound to that base; with compact=True
-    (which needs a base) it is version 3, with compact position lists."""
+    (which needs a base) it is version 3, with compact position lists; with overwrite=True
+    (which needs a base) its streams hold new values instead of XOR masks."""
     old, new = _u16(old), _u16(new)
     if old.size != new.size:
         raise ValueError("old and new must have the same number of elements")
     lib = _load()
     size, ck = ctypes.c_uint64(), ctypes.c_uint64()
-    if compact and base is None:
-        raise ValueError("compact payloads are bound to a base: give base")
+    if (compact or overwrite) and base is None:
+        raise ValueError("compact and overwrite payloads are bound to a base: give base")
     if base is None:
         call = lambda out, cap: lib.orc_encode(old.ctypes.data, new.ctypes.data, old.size, out,
                                                cap, ctypes.byref(size), ctypes.byref(ck))
-    elif compact:
-        b = ctypes.c_uint64(int(base) & (2**64 - 1))
-        call = lambda out, cap: lib.orc_encode_compact(old.ctypes.data, new.ctypes.data,
-                                                       old.size, b, out, cap,
-                                                       ctypes.byref(size), ctypes.byref(ck))
     else:
         b = ctypes.c_uint64(int(base) & (2**64 - 1))
-        call = lambda out, cap: lib.orc_encode_versioned(old.ctypes.data, new.ctypes.data,
-                                                         old.size, b, out, cap,
-                                                         ctypes.byref(size), ctypes.byref(ck))
+        fn = {(False, False): lib.orc_encode_versioned, (True, False): lib.orc_encode_compact,
+              (False, True): lib.orc_encode_overwrite,
+              (True, True): lib.orc_encode_compact_overwrite}[(bool(compact), bool(overwrite))]
+        call = lambda out, cap: fn(old.ctypes.data, new.ctypes.data, old.size, b, out, cap,
+                                   ctypes.byref(size), ctypes.byref(ck))
     rc = call(None, 0)
     if rc not in (OK, ERR_CAPACITY):
         raise RuntimeError(f"orc_encode failed with {rc}")

@@ -1,5 +1,5 @@
 /*
- * bd_oracle.c -- plain, slow, single-threaded CPU oracle of the BF16DLT1 v1 delta format.
+ * bd_oracle.c -- plain, slow, single-threaded CPU oracle of the BF16DLT1 delta format.
  *
  * TEST INFRASTRUCTURE ONLY (see bd_oracle.h): never part of the product path.
  *
@@ -26,8 +26,14 @@
  * Version 2 (a payload bound to its base version; not on the pages, which only say that a
  * joint commit binds the installed weights to the baseline of the next delta): the version-1
  * header with version 2, followed by u64 base checksum (the checksum of the weights the
- * payload applies to) and u64 reserved = 0, i.e. an 80-byte header; the sections after it are
- * the same.
+ * payload applies to) and u64 flags, i.e. an 80-byte header; the sections after it are the
+ * same.  Flags bit 0 (versions 2 and 3; every other bit zero) marks an overwrite payload
+ * ("Two forms of update payload": changes carried as absolute overwrites; "Retry-safe
+ * versioning": partial writes retried through overwrites): the R stream holds each rare
+ * element's new value and the M stream each mantissa-only element's new mantissa, and the
+ * decoder writes them into place instead of XORing, so applying the payload again to weights
+ * it has already (partly) updated leaves the same result.  Positions and classes are those of
+ * the XOR payload of the same update.
  * Version 3 (compact positions; a byte-aligned code of the position gaps standing in for the
  * entropy stage of the pages' codecs): the version-2 header with version 3, then
  *   count table (C x u32) | R stream | X stream (u16 per escaped gap, chunks in order) |
@@ -50,6 +56,9 @@
 #define ORC_HEADER 64u      /* version 1 */
 #define ORC_HEADER_V2 80u   /* version 2 and 3: + base checksum + reserved */
 #define ORC_COMPACT_MAX 508u /* version 3: most changes of a compact chunk */
+/* Header flags (versions 2 and 3, the u64 at byte 72): bit 0 = the streams carry new field
+ * values to overwrite instead of XOR masks.  Every other bit is zero. */
+#define ORC_FLAG_OVERWRITE 1u
 
 /* Field masks of a BF16 word: sign bit 15, exponent bits 14..7, mantissa bits 6..0. */
 #define ORC_SIGN_EXP_BITS 0xFF80u
@@ -179,9 +188,11 @@ static int read_block(const uint8_t* src, uint16_t* pos, uint64_t k, uint64_t L)
 
 /* ---- encode ------------------------------------------------------------------------- */
 
+/* bound: write the 80-byte header (version 2) with base; overwrite (version 2 only): the
+ * streams carry the new field values instead of XOR masks and the header flags say so. */
 static int encode_impl(const uint16_t* old, const uint16_t* neu, uint64_t n, int bound,
-                       uint64_t base, uint8_t* out, uint64_t cap, uint64_t* size_out,
-                       uint64_t* checksum_out) {
+                       uint64_t base, int overwrite, uint8_t* out, uint64_t cap,
+                       uint64_t* size_out, uint64_t* checksum_out) {
   if ((n > 0 && (old == NULL || neu == NULL)) || size_out == NULL || checksum_out == NULL)
     return ORC_ERR_ARG;
   const uint64_t hdr = bound ? ORC_HEADER_V2 : ORC_HEADER;
@@ -225,8 +236,8 @@ static int encode_impl(const uint16_t* old, const uint16_t* neu, uint64_t n, int
   put_u64(out + 48, pos_bytes);
   put_u64(out + 56, size);
   if (bound) {
-    put_u64(out + 64, base);   /* base checksum */
-    put_u64(out + 72, 0);      /* reserved */
+    put_u64(out + 64, base);                      /* base checksum */
+    put_u64(out + 72, overwrite ? ORC_FLAG_OVERWRITE : 0);   /* flags */
   }
 
   /* Count table. */
@@ -239,11 +250,12 @@ static int encode_impl(const uint16_t* old, const uint16_t* neu, uint64_t n, int
   uint64_t p_off = r_off + 2 * sum_r;
   uint64_t m_off = p_off + pos_bytes;
 
-  /* Step 5: the rare stream -- the full 16-bit XOR of every exponent/sign change. */
+  /* Step 5: the rare stream -- the full 16-bit XOR of every exponent/sign change (with
+   * overwrite: the full new value). */
   for (uint64_t i = 0; i < n; i++) {
     uint16_t x = (uint16_t)(old[i] ^ neu[i]);
     if (classify(x) == CLASS_RARE) {
-      put_u16(out + r_off, x);
+      put_u16(out + r_off, overwrite ? neu[i] : x);
       r_off += 2;
     }
   }
@@ -268,13 +280,14 @@ static int encode_impl(const uint16_t* old, const uint16_t* neu, uint64_t n, int
   free(mpos);
   free(rpos);
 
-  /* Step 4: the mantissa stream -- 7 bits (x & 0x7F) per mantissa-only change, element j of
-   * the stream in bits [7j, 7j+7), stream bit b = bit (b % 8) of byte (b / 8). */
+  /* Step 4: the mantissa stream -- 7 bits (x & 0x7F; with overwrite: the new mantissa) per
+   * mantissa-only change, element j of the stream in bits [7j, 7j+7), stream bit b = bit
+   * (b % 8) of byte (b / 8). */
   uint64_t j = 0;
   for (uint64_t i = 0; i < n; i++) {
     uint16_t x = (uint16_t)(old[i] ^ neu[i]);
     if (classify(x) != CLASS_MANT) continue;
-    uint16_t v = (uint16_t)(x & ORC_MANT_BITS);
+    uint16_t v = (uint16_t)((overwrite ? neu[i] : x) & ORC_MANT_BITS);
     for (uint64_t b = 0; b < 7; b++) {
       uint64_t bit = 7 * j + b;
       if ((v >> b) & 1) out[m_off + bit / 8] |= (uint8_t)(1u << (bit % 8));
@@ -289,13 +302,19 @@ static int encode_impl(const uint16_t* old, const uint16_t* neu, uint64_t n, int
 
 int orc_encode(const uint16_t* old, const uint16_t* neu, uint64_t n, uint8_t* out,
                uint64_t cap, uint64_t* size_out, uint64_t* checksum_out) {
-  return encode_impl(old, neu, n, 0, 0, out, cap, size_out, checksum_out);
+  return encode_impl(old, neu, n, 0, 0, 0, out, cap, size_out, checksum_out);
 }
 
 int orc_encode_versioned(const uint16_t* old, const uint16_t* neu, uint64_t n, uint64_t base,
                          uint8_t* out, uint64_t cap, uint64_t* size_out,
                          uint64_t* checksum_out) {
-  return encode_impl(old, neu, n, 1, base, out, cap, size_out, checksum_out);
+  return encode_impl(old, neu, n, 1, base, 0, out, cap, size_out, checksum_out);
+}
+
+int orc_encode_overwrite(const uint16_t* old, const uint16_t* neu, uint64_t n, uint64_t base,
+                         uint8_t* out, uint64_t cap, uint64_t* size_out,
+                         uint64_t* checksum_out) {
+  return encode_impl(old, neu, n, 1, base, 1, out, cap, size_out, checksum_out);
 }
 
 /* ---- version 3: compact positions ---------------------------------------------------- */
@@ -315,8 +334,9 @@ static uint64_t chunk_escapes(const uint16_t* old, const uint16_t* neu, uint64_t
   return e;
 }
 
-int orc_encode_compact(const uint16_t* old, const uint16_t* neu, uint64_t n, uint64_t base,
-                       uint8_t* out, uint64_t cap, uint64_t* size_out, uint64_t* checksum_out) {
+static int compact_impl(const uint16_t* old, const uint16_t* neu, uint64_t n, uint64_t base,
+                        int overwrite, uint8_t* out, uint64_t cap, uint64_t* size_out,
+                        uint64_t* checksum_out) {
   if ((n > 0 && (old == NULL || neu == NULL)) || size_out == NULL || checksum_out == NULL)
     return ORC_ERR_ARG;
   uint64_t C = (n + ORC_CHUNK - 1) / ORC_CHUNK;
@@ -371,7 +391,7 @@ int orc_encode_compact(const uint16_t* old, const uint16_t* neu, uint64_t n, uin
   put_u64(out + 48, pos_bytes);
   put_u64(out + 56, size);
   put_u64(out + 64, base);
-  put_u64(out + 72, 0);
+  put_u64(out + 72, overwrite ? ORC_FLAG_OVERWRITE : 0);
   for (uint64_t c = 0; c < C; c++) {
     uint32_t v = compact[c] ? ORC_COMPACT_FLAG | (uint32_t)mcount[c] | ((uint32_t)rcount[c] << 9) |
                                   ((uint32_t)ecount[c] << 18)
@@ -386,7 +406,7 @@ int orc_encode_compact(const uint16_t* old, const uint16_t* neu, uint64_t n, uin
   /* R stream: every rare change's 16-bit XOR, in position order. */
   for (uint64_t i = 0; i < n; i++) {
     uint16_t x = (uint16_t)(old[i] ^ neu[i]);
-    if (classify(x) == CLASS_RARE) { put_u16(out + r_off, x); r_off += 2; }
+    if (classify(x) == CLASS_RARE) { put_u16(out + r_off, overwrite ? neu[i] : x); r_off += 2; }
   }
   /* X stream and position blocks, chunk by chunk. */
   uint16_t* mpos = (uint16_t*)malloc(ORC_CHUNK * sizeof(uint16_t));
@@ -436,12 +456,24 @@ int orc_encode_compact(const uint16_t* old, const uint16_t* neu, uint64_t n, uin
     if (classify(x) != CLASS_MANT) continue;
     for (uint64_t b = 0; b < 7; b++) {
       uint64_t bit = 7 * j + b;
-      if (((x & ORC_MANT_BITS) >> b) & 1) out[m_off + bit / 8] |= (uint8_t)(1u << (bit % 8));
+      if ((((overwrite ? neu[i] : x) & ORC_MANT_BITS) >> b) & 1)
+        out[m_off + bit / 8] |= (uint8_t)(1u << (bit % 8));
     }
     j++;
   }
   free(mcount); free(rcount); free(ecount); free(compact);
   return ORC_OK;
+}
+
+int orc_encode_compact(const uint16_t* old, const uint16_t* neu, uint64_t n, uint64_t base,
+                       uint8_t* out, uint64_t cap, uint64_t* size_out, uint64_t* checksum_out) {
+  return compact_impl(old, neu, n, base, 0, out, cap, size_out, checksum_out);
+}
+
+int orc_encode_compact_overwrite(const uint16_t* old, const uint16_t* neu, uint64_t n,
+                                 uint64_t base, uint8_t* out, uint64_t cap, uint64_t* size_out,
+                                 uint64_t* checksum_out) {
+  return compact_impl(old, neu, n, base, 1, out, cap, size_out, checksum_out);
 }
 
 /* Splits a version-3 count entry; returns -1 when its unused bits are not zero. */
@@ -462,6 +494,20 @@ static int v3_entry(uint32_t v, uint64_t* km, uint64_t* kr, uint64_t* ke, int* i
   return 0;
 }
 
+/* Applying one change to the element at w.  An XOR payload flips the bits its value holds
+ * ("Delta update algebra": old XOR mask = new).  An overwrite payload carries the new
+ * field instead ("Two forms of update payload": absolute overwrites): a mantissa-only change
+ * replaces the mantissa and keeps the sign and exponent, which it did not change; a rare
+ * change replaces the whole value.  Applying an overwrite twice leaves the same result. */
+static void apply_mant(uint16_t* w, uint16_t v, int overwrite) {
+  if (overwrite) *w = (uint16_t)((*w & ORC_SIGN_EXP_BITS) | v);
+  else *w ^= v;
+}
+static void apply_rare(uint16_t* w, uint16_t v, int overwrite) {
+  if (overwrite) *w = v;
+  else *w ^= v;
+}
+
 /* The 7-bit value j of the M stream starting at m. */
 static uint16_t mant_at(const uint8_t* m, uint64_t j) {
   uint16_t v = 0;
@@ -472,10 +518,10 @@ static uint16_t mant_at(const uint8_t* m, uint64_t j) {
   return v;
 }
 
-/* Decodes a version-3 payload (header fields n, C, version and reserved already checked,
+/* Decodes a version-3 payload (header fields n, C, version and flags already checked,
  * size >= 80) into out; the base is checked against required_base as in decode_into. */
 static int decode_v3(const uint16_t* old, uint64_t n, const uint8_t* payload, uint64_t size,
-                     uint16_t* out, const uint64_t* required_base) {
+                     uint16_t* out, const uint64_t* required_base, int overwrite) {
   uint64_t C = (n + ORC_CHUNK - 1) / ORC_CHUNK;
   uint64_t hdr_m = get_u64(payload + 32), hdr_r = get_u64(payload + 40);
   uint64_t hdr_pos = get_u64(payload + 48), hdr_size = get_u64(payload + 56);
@@ -556,13 +602,13 @@ static int decode_v3(const uint16_t* old, uint64_t n, const uint8_t* payload, ui
     if (status != ORC_OK) break;
     for (uint64_t i = 0; i < nm; i++) {
       uint16_t v = mant_at(payload + m_off, mj + i);
-      if (v == 0) { status = ORC_ERR_FORMAT; break; }
-      out[c * ORC_CHUNK + mpos[i]] ^= v;
+      if (!overwrite && v == 0) { status = ORC_ERR_FORMAT; break; }
+      apply_mant(&out[c * ORC_CHUNK + mpos[i]], v, overwrite);
     }
     for (uint64_t i = 0; status == ORC_OK && i < nr; i++) {
       uint16_t v = get_u16(payload + r_off + 2 * (rj + i));
-      if ((v & ORC_SIGN_EXP_BITS) == 0) { status = ORC_ERR_FORMAT; break; }
-      out[c * ORC_CHUNK + rpos[i]] ^= v;
+      if (!overwrite && (v & ORC_SIGN_EXP_BITS) == 0) { status = ORC_ERR_FORMAT; break; }
+      apply_rare(&out[c * ORC_CHUNK + rpos[i]], v, overwrite);
     }
     mj += km;
     rj += kr;
@@ -591,12 +637,14 @@ static int decode_into(const uint16_t* old, uint64_t n, const uint8_t* payload, 
   if (version != 1 && version != 2 && version != 3) return ORC_ERR_FORMAT;
   const uint64_t hdr = version >= 2 ? ORC_HEADER_V2 : ORC_HEADER;
   if (size < hdr) return ORC_ERR_FORMAT;
-  if (version >= 2 && get_u64(payload + 72) != 0) return ORC_ERR_FORMAT;
+  const uint64_t flags = version >= 2 ? get_u64(payload + 72) : 0;
+  if ((flags & ~(uint64_t)ORC_FLAG_OVERWRITE) != 0) return ORC_ERR_FORMAT;
+  const int overwrite = (flags & ORC_FLAG_OVERWRITE) != 0;
   if (get_u32(payload + 12) != ORC_CHUNK) return ORC_ERR_FORMAT;
   uint64_t C = (n + ORC_CHUNK - 1) / ORC_CHUNK;
   if (get_u64(payload + 16) != n) return ORC_ERR_FORMAT;
   if (get_u64(payload + 24) != C) return ORC_ERR_FORMAT;
-  if (version == 3) return decode_v3(old, n, payload, size, out, required_base);
+  if (version == 3) return decode_v3(old, n, payload, size, out, required_base, overwrite);
   uint64_t hdr_m = get_u64(payload + 32), hdr_r = get_u64(payload + 40);
   uint64_t hdr_pos = get_u64(payload + 48), hdr_size = get_u64(payload + 56);
   if (hdr_size != size) return ORC_ERR_FORMAT;
@@ -648,23 +696,25 @@ static int decode_into(const uint16_t* old, uint64_t n, const uint8_t* payload, 
     }
     if (status != ORC_OK) break;
 
-    /* Mantissa-only changes: XOR the next 7-bit value into the mantissa. */
+    /* Mantissa-only changes: XOR the next 7-bit value into the mantissa (overwrite: the
+     * value replaces the mantissa). */
     for (uint64_t j = 0; j < km; j++, mj++) {
       uint16_t v = 0;
       for (uint64_t b = 0; b < 7; b++) {
         uint64_t bit = 7 * mj + b;
         v |= (uint16_t)(((payload[m_off + bit / 8] >> (bit % 8)) & 1) << b);
       }
-      if (v == 0) { status = ORC_ERR_FORMAT; break; }
-      out[c * ORC_CHUNK + mpos[j]] ^= v;
+      if (!overwrite && v == 0) { status = ORC_ERR_FORMAT; break; }
+      apply_mant(&out[c * ORC_CHUNK + mpos[j]], v, overwrite);
     }
     if (status != ORC_OK) break;
 
-    /* Rare changes: XOR the next full 16-bit block. */
+    /* Rare changes: XOR the next full 16-bit block (overwrite: the block replaces the
+     * value). */
     for (uint64_t j = 0; j < kr; j++, rj++) {
       uint16_t v = get_u16(payload + r_off + 2 * rj);
-      if ((v & ORC_SIGN_EXP_BITS) == 0) { status = ORC_ERR_FORMAT; break; }
-      out[c * ORC_CHUNK + rpos[j]] ^= v;
+      if (!overwrite && (v & ORC_SIGN_EXP_BITS) == 0) { status = ORC_ERR_FORMAT; break; }
+      apply_rare(&out[c * ORC_CHUNK + rpos[j]], v, overwrite);
     }
   }
   free(mpos);

@@ -58,10 +58,18 @@ int orc_encode_versioned(const uint16_t* old, const uint16_t* neu, uint64_t n, u
 int orc_encode_compact(const uint16_t* old, const uint16_t* neu, uint64_t n, uint64_t base,
                        uint8_t* out, uint64_t cap, uint64_t* size_out, uint64_t* checksum_out);
 
+/* orc_encode_versioned / orc_encode_compact writing an overwrite payload (header flags bit 0):
+ * the same positions and classes, the streams holding new values instead of XOR masks. */
+int orc_encode_overwrite(const uint16_t* old, const uint16_t* neu, uint64_t n, uint64_t base,
+                         uint8_t* out, uint64_t cap, uint64_t* size_out, uint64_t* checksum_out);
+int orc_encode_compact_overwrite(const uint16_t* old, const uint16_t* neu, uint64_t n,
+                                 uint64_t base, uint8_t* out, uint64_t cap, uint64_t* size_out,
+                                 uint64_t* checksum_out);
+
 /* Decodes payload[0..size) (version 1, 2 or 3; the base of a bound payload is not checked
  * here) against old (n elements) into out (n elements, must not alias
  * old), then verifies checksum(out) == expected.  Returns ORC_OK, ORC_ERR_FORMAT (payload
- * is not a canonical BF16DLT1 v1 payload for n elements) or ORC_ERR_CHECKSUM.  On an error
+ * is not a canonical BF16DLT1 payload for n elements) or ORC_ERR_CHECKSUM.  On an error
  * the contents of out are unspecified. */
 int orc_decode(const uint16_t* old, uint64_t n, const uint8_t* payload, uint64_t size,
                uint64_t expected, uint16_t* out);

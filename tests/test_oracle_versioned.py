@@ -86,7 +86,7 @@ def test_base_mismatch_and_order_of_checks():
     assert oracle.decode(old, p2, ck)[0] == oracle.OK
     # a header format error comes first
     bad = p2.copy()
-    bad[72] = 1     # reserved byte
+    bad[72] = 2     # a flag bit with no meaning (bit 0 marks an overwrite payload)
     assert oracle.decode_incremental(old, bad, base ^ 1, ck)[0] == oracle.ERR_FORMAT
     assert oracle.decode(old, bad, ck)[0] == oracle.ERR_FORMAT
     # a malformed chunk comes after the base: a zero delta after the first in chunk 0's list
