@@ -592,6 +592,31 @@ def run_ours(args) -> None:
             i3_ms = ms
     del c3b, d3, i3
 
+    # overwrite payloads (version 3, header flag bit 0) of the same update, both directions
+    cof = bd.CompressBatch(olds, news, caps=s3, base_checksums=ck_old, compact=True,
+                           overwrite=True)
+    cob = bd.CompressBatch(news, olds, caps=s3, base_checksums=ck_new, compact=True,
+                           overwrite=True)
+    cof.run(stream)
+    cob.run(stream)
+    torch.cuda.synchronize()
+    if int(cof.status.item()) != bd.OK or int(cob.status.item()) != bd.OK:
+        raise RuntimeError("overwrite compress failed")
+    ow_ms, _ = timed(lambda: cof.run(stream), args.steps)
+    dow = {True: bd.DecompressBatch(rolls, cob.payloads, s3, ck_old),
+           False: bd.DecompressBatch(rolls, cof.payloads, s3, ck_new)}
+    iow = {True: bd.IncrementalBatch(rolls, cob.payloads, s3, ck_new, ck_old),
+           False: bd.IncrementalBatch(rolls, cof.payloads, s3, ck_old, ck_new)}
+    ow_res = {}
+    for name, table in (("apply", dow), ("incremental", iow)):
+        ms, lastw = timed(alternate(table), args.steps)
+        want = N if state["new"] else O
+        if int(lastw.status.item()) != bd.OK or not torch.equal(Rb.view(torch.int16),
+                                                                 want.view(torch.int16)):
+            raise RuntimeError(f"overwrite {name} did not verify")
+        ow_res[name] = ms
+    del cof, cob, dow, iow
+
     total_ms = reduce_max(total_ms, world, dev)
     ms_step = total_ms / args.steps
     raw = 2 * n_total
@@ -711,6 +736,14 @@ def run_ours(args) -> None:
                     "what": "version-3 payloads (compact position blocks) of the same update: "
                             "bd_compress_versioned_batch format 3, bd_decompress_batch in "
                             "place, bd_decompress_incremental_batch in place"},
+                "overwrite": {
+                    "compress_ms": round(ow_ms, 4), "apply_ms": round(ow_res["apply"], 4),
+                    "incremental_ms": round(ow_res["incremental"], 4),
+                    "what": "version-3 overwrite payloads (new field values instead of XOR "
+                            "masks; same size as the version-3 XOR payload) of the same update "
+                            "and of its reverse: bd_compress_versioned_batch format 3 | "
+                            "BD_FORMAT_OVERWRITE, bd_decompress_batch and "
+                            "bd_decompress_incremental_batch in place"},
                 "compress_algorithmic_bytes": comp_bytes, "apply_algorithmic_bytes": app_bytes,
                 "payload_pct": round(100 * payload_bytes / raw, 4),
                 "touched_sector_pct": round(100 * touched / (raw / 32), 3),

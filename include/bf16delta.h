@@ -31,7 +31,8 @@
  * u64 sum R, u64 position bytes, u64 total size.
  * Version 2 (bd_compress_versioned, format 2): the same payload with an 80-byte header --
  * version 2, the 64 bytes above, then u64 base checksum (the checksum of the weights the
- * payload applies to) and u64 0 -- so every section starts 16 bytes later.
+ * payload applies to) and u64 flags (0 for an XOR payload) -- so every section starts 16
+ * bytes later.
  * Version 3 (format 3): the version-2 header with version 3, and compact position blocks
  * standing in for the entropy stage the ARCv3 page applies to the sparse positions (which it
  * does not specify).  Sections:
@@ -48,6 +49,16 @@
  * than the version-2 payload of the same update.  The header's position-bytes field counts
  * the position section only; the X stream is what the other sections leave of the total.
  * Every decompress call accepts all three versions.
+ * Overwrite payloads (versions 2 and 3 with header flags bit 0 = BD_FLAG_OVERWRITE; the u64 at
+ * byte 72, whose other bits are zero): the NeMo-DCR page's second form of update payload,
+ * absolute overwrites, through which partial writes are retried.  Positions, classes and
+ * sizes are those of the XOR payload of the same update; the R stream holds each rare
+ * element's new value and the M stream each mantissa-only element's new mantissa.  Applying
+ * one writes those fields into place -- the new value, or the new mantissa under the element's
+ * own sign and exponent (which a mantissa-only change does not alter) -- so applying it again,
+ * to weights it has already updated wholly or in part, gives the same result.  The XOR
+ * payload's value rules (a nonzero mantissa mask, a rare mask with a sign or exponent bit) do
+ * not apply to it.
  * Checksum (returned beside the payload, not stored in it): with word_j the little-endian
  * 64-bit word of elements 4j..4j+3 (zero past n),
  *   checksum = sum_j mix64(word_j ^ (j+1) * 0x9E3779B97F4A7C15)  mod 2^64,
@@ -134,13 +145,20 @@ typedef struct bd_incremental_item {
 } bd_incremental_item;
 
 /* Parsed payload header (host side).  base_checksum is 0 for a version-1 payload;
- * n_escapes (X-stream values) is 0 below version 3. */
+ * n_escapes (X-stream values) is 0 below version 3; flags is the header flags word of versions
+ * 2 and 3 (BD_FLAG_OVERWRITE: an overwrite payload), 0 for version 1. */
 typedef struct bd_payload_info_t {
   uint64_t n, chunks, n_mant, n_rare, position_bytes, total_size;
   uint32_t version, chunk_elems;
   uint64_t base_checksum;
   uint64_t n_escapes;
+  uint64_t flags;
 } bd_payload_info_t;
+
+/* Header flag of an overwrite payload, and the bit of bd_compress_versioned's format argument
+ * that asks for one. */
+#define BD_FLAG_OVERWRITE 1u
+#define BD_FORMAT_OVERWRITE 0x100u
 
 /* Largest payload compress can produce for n elements (every chunk at its worst split, with
  * the version-2 header).  Returns 0 for n > BD_MAX_ELEMS. */
@@ -167,8 +185,8 @@ BD_API int bd_compress_batch(const bd_compress_item* h_items, uint32_t k, void* 
                       uint64_t ws_bytes, int32_t* d_status, void* stream);
 
 /* bd_compress writing a payload bound to its base version: format 2 (the version-1 payload
- * with the 80-byte header) or 3 (compact position blocks, see above); any other format is
- * BD_ERR_INVALID_ARG.  Not on the pages: the NeMo-DCR page binds the installed weights to
+ * with the 80-byte header) or 3 (compact position blocks, see above), either optionally OR-ed
+ * with BD_FORMAT_OVERWRITE for an overwrite payload; any other format is BD_ERR_INVALID_ARG.  Not on the pages: the NeMo-DCR page binds the installed weights to
  * the baseline of the next delta so that mismatched versions cannot enter silently.
  * *d_base_checksum (device, required) is the checksum of d_old as the caller knows it -- in
  * a steady update loop, the checksum of the previous update's new weights; it is stored in

@@ -30,7 +30,8 @@ class IncrementalItem(ctypes.Structure):
 class PayloadInfo(ctypes.Structure):
     _fields_ = [("n", c_u64), ("chunks", c_u64), ("n_mant", c_u64), ("n_rare", c_u64),
                 ("position_bytes", c_u64), ("total_size", c_u64), ("version", c_u32),
-                ("chunk_elems", c_u32), ("base_checksum", c_u64), ("n_escapes", c_u64)]
+                ("chunk_elems", c_u32), ("base_checksum", c_u64), ("n_escapes", c_u64),
+                ("flags", c_u64)]
 
 
 # name -> (restype, argtypes); must match include/bf16delta.h

@@ -117,12 +117,16 @@ inline bool overlaps(const void* a, uint64_t na, const void* b, uint64_t nb) {
 int check(cudaError_t e) { return e == cudaSuccess ? BD_OK : BD_ERR_CUDA; }
 
 // -------------------------------------------------------------------------------- compress
-// bases == nullptr: version 1; else version `format` (2, or 3 with compact position blocks).
+// bases == nullptr: version 1; else version `format & 0xFF` (2, or 3 with compact position
+// blocks), an overwrite payload when format has BD_FORMAT_OVERWRITE.
 int compress_impl(const bd_compress_item* items, const uint64_t* const* bases, uint32_t format,
                   uint32_t k, void* ws, uint64_t ws_bytes, int32_t* status_all, cudaStream_t s) {
   if (k > 0 && items == nullptr) return BD_ERR_INVALID_ARG;
-  if (bases && format != 2 && format != 3) return BD_ERR_INVALID_ARG;
-  const uint32_t version = bases ? format : 1;
+  const uint32_t vfmt = format & 0xFFu;
+  const bool overwrite = bases && (format & BD_FORMAT_OVERWRITE) != 0;
+  if (bases && ((vfmt != 2 && vfmt != 3) || (format & ~(0xFFu | BD_FORMAT_OVERWRITE)) != 0))
+    return BD_ERR_INVALID_ARG;
+  const uint32_t version = bases ? vfmt : 1;
   if (bases)
     for (uint32_t i = 0; i < k; i++)
       if (!bases[i] || !aligned(bases[i], 8)) return BD_ERR_INVALID_ARG;
@@ -167,6 +171,7 @@ int compress_impl(const bd_compress_item* items, const uint64_t* const* bases, u
     J.d_status = it.d_status;
     J.d_base = bases ? bases[i] : nullptr;
     J.version = version;
+    J.flags = overwrite ? kFlagOverwrite : 0;
     J.nchunks = (it.n + kChunk - 1) / kChunk;
     J.chunk_base = cb;
     J.tile_base = tb;
@@ -185,10 +190,11 @@ int compress_impl(const bd_compress_item* items, const uint64_t* const* bases, u
   if (status_all && (rc = check(cudaMemsetAsync(status_all, 0, sizeof(int32_t), s)))) return rc;
   if (k == 0) return BD_OK;
   if ((rc = check(upload(host, w + lay.jobs, s)))) return rc;
-  if ((rc = check(launch_encode_slots(c, version == 3)))) return rc;
+  const bool general = version == 3 || overwrite;   // the general kernel builds
+  if ((rc = check(launch_encode_slots(c, general, overwrite)))) return rc;
   if ((rc = check(launch_scan_tiles(c, false)))) return rc;
   if ((rc = check(launch_scan_jobs(c, false, status_all)))) return rc;
-  if ((rc = check(launch_emit(c, version == 3)))) return rc;
+  if ((rc = check(launch_emit(c, general, overwrite)))) return rc;
   return check(launch_emit_dense(c));
 }
 
@@ -422,13 +428,15 @@ int bd_payload_info(const void* h_header, uint64_t bytes, bd_payload_info_t* out
   I.total_size = le64(p + 56);
   I.base_checksum = 0;
   I.n_escapes = 0;
+  I.flags = 0;
   if (I.version < 1 || I.version > 3 || I.chunk_elems != kChunk || I.n > BD_MAX_ELEMS)
     return BD_ERR_FORMAT;
   const uint64_t hdr = I.version >= 2 ? kHeaderV2 : kHeader;
   if (I.version >= 2) {
     if (bytes < kHeaderV2) return BD_ERR_INVALID_ARG;
     I.base_checksum = le64(p + 64);
-    if (le64(p + 72) != 0) return BD_ERR_FORMAT;
+    I.flags = le64(p + 72);
+    if ((I.flags & ~(uint64_t)kFlagOverwrite) != 0) return BD_ERR_FORMAT;
   }
   if (I.chunks != (I.n + kChunk - 1) / kChunk) return BD_ERR_FORMAT;
   if (I.n_mant > I.n || I.n_rare > I.n - I.n_mant) return BD_ERR_FORMAT;

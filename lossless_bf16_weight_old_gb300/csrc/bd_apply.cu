@@ -55,6 +55,41 @@ __device__ __forceinline__ void flush_ck(uint8_t* ck_base, uint32_t j, uint64_t 
               (unsigned long long)s);
 }
 
+// Records the value of one change at chunk position pos in the shared mask (and, for an
+// overwrite payload, the position in the record bitmap of its class).
+__device__ __forceinline__ void put_record(uint16_t* s_mask, uint32_t* rec, uint32_t pos,
+                                           uint32_t v, bool ow) {
+  s_mask[pos] = (uint16_t)v;
+  if (ow) atomicOr(&rec[pos >> 5], 1u << (pos & 31));
+}
+
+// Whether a rare change with value v may go to pos: not a position of a mantissa-only change,
+// and for an XOR payload a value with a sign or exponent bit.  (An XOR payload's mantissa masks
+// are nonzero, so a nonzero mask at pos marks one; an overwrite payload's may be zero, so
+// its record bitmap does.)
+__device__ __forceinline__ bool rare_ok(const uint16_t* s_mask, const uint32_t* rec_m,
+                                        uint32_t pos, uint32_t v, bool ow) {
+  if (ow) return ((rec_m[pos >> 5] >> (pos & 31)) & 1u) == 0;
+  return (v & kSignExp) != 0 && s_mask[pos] == 0;
+}
+
+// Overwrite payloads: the XOR mask that takes the 8 current values o of a group to their
+// targets -- a rare record's target is the new value, a mantissa-only record's the new
+// mantissa under the current sign and exponent -- from the targets t and the group's record
+// bits (bit i: element i); elements without a record keep their value.
+__device__ __forceinline__ uint4 overwrite_mask(uint4 t, uint4 o, uint32_t rec_m, uint32_t rec_r) {
+  uint32_t w[4] = {0, 0, 0, 0};
+#pragma unroll
+  for (int i = 0; i < 8; i++) {
+    const uint32_t now = elem_of(o, i), to = elem_of(t, i);
+    uint32_t x = 0;
+    if ((rec_r >> i) & 1u) x = now ^ to;
+    else if ((rec_m >> i) & 1u) x = (now & kMant) ^ to;
+    w[i >> 1] |= x << (16 * (i & 1));
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // Block-wide exclusive prefix sums of two quantities (0 and 1), each held in two slots per
 // thread and ordered slot a of threads 0..255, then slot b of threads 0..255; tot0 / tot1 are
 // the totals.  Starts and ends with a barrier, so s_tot may be reused by the next call.
@@ -93,7 +128,8 @@ k_apply_dense(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_
               const uint32_t* __restrict__ list_count, const uint32_t* __restrict__ list,
               const uint4* __restrict__ loc, const TileSum* __restrict__ tile_pre,
               JobInfo* __restrict__ info, uint8_t* __restrict__ ck_base) {
-  __shared__ uint4 s_mask4[kChunk / 8];       // the chunk's XOR mask, 8 KiB
+  __shared__ uint4 s_mask4[kChunk / 8];       // the chunk's XOR mask (overwrite: targets), 8 KiB
+  __shared__ uint32_t s_rec[2][kChunk / 32];  // overwrite: positions with M / R records
   __shared__ uint32_t s_tot[kWarps][4];
   __shared__ int s_bad;
   uint16_t* s_mask = reinterpret_cast<uint16_t*>(s_mask4);
@@ -142,6 +178,12 @@ k_apply_dense(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_
     const uint4 oa = load8(J.out, ea, n), ob = load8(J.out, eb, n);
     s_mask4[t] = make_uint4(0, 0, 0, 0);
     s_mask4[t + 256] = make_uint4(0, 0, 0, 0);
+    const bool ow = (info[j].flags & kFlagOverwrite) != 0;   // block-uniform
+    if (ow && t < 128) {
+      s_rec[0][t] = 0;
+      s_rec[1][t] = 0;
+    }
+    // (the first block scan below orders these stores before every scatter)
 
     bool bad = false;
     if (cc.compact) {
@@ -174,17 +216,25 @@ k_apply_dense(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_
       pb += gb - 1;
       if (ia < k) {
         uint32_t v = 0;
-        if (rA) { if (xRa < R) v = load_u16(rstream + 2 * xRa); if ((v & kSignExp) == 0) bad = true; }
-        else { if (ia - xRa < M) v = mant_value(mstream, Mex + ia - xRa); if (v == 0) bad = true; }
+        if (rA) { if (xRa < R) v = load_u16(rstream + 2 * xRa); else bad = true; }
+        else { if (ia - xRa < M) v = mant_value(mstream, Mex + ia - xRa); else bad = true; }
+        if (!ow && (rA ? (v & kSignExp) == 0 : v == 0)) bad = true;
         if (pa >= L) bad = true;
-        if (!bad) s_mask[pa] = (uint16_t)v;
+        if (!bad) {
+          s_mask[pa] = (uint16_t)v;
+          if (ow) atomicOr(&s_rec[rA][pa >> 5], 1u << (pa & 31));
+        }
       }
       if (ib < k) {
         uint32_t v = 0;
-        if (rB) { if (xRb < R) v = load_u16(rstream + 2 * xRb); if ((v & kSignExp) == 0) bad = true; }
-        else { if (ib - xRb < M) v = mant_value(mstream, Mex + ib - xRb); if (v == 0) bad = true; }
+        if (rB) { if (xRb < R) v = load_u16(rstream + 2 * xRb); else bad = true; }
+        else { if (ib - xRb < M) v = mant_value(mstream, Mex + ib - xRb); else bad = true; }
+        if (!ow && (rB ? (v & kSignExp) == 0 : v == 0)) bad = true;
         if (pb >= L) bad = true;
-        if (!bad) s_mask[pb] = (uint16_t)v;
+        if (!bad) {
+          s_mask[pb] = (uint16_t)v;
+          if (ow) atomicOr(&s_rec[rB][pb >> 5], 1u << (pb & 31));
+        }
       }
     } else {
       // per-thread scan inputs: list entry t (slot a) or bitmap bytes t, t+256 (slots a, b)
@@ -242,8 +292,8 @@ k_apply_dense(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_
         if ((uint32_t)t < M) {
           const uint32_t pos = xaM + aM;   // inclusive prefix of the deltas
           const uint32_t v = mant_value(mstream, Mex + t);
-          if (pos >= L || v == 0) bad = true;
-          else s_mask[pos] = (uint16_t)v;
+          if (pos >= L || (!ow && v == 0)) bad = true;
+          else put_record(s_mask, s_rec[0], pos, v, ow);
         }
       } else {
         if (totaM + totbM != M) bad = true;
@@ -252,14 +302,14 @@ k_apply_dense(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_
           const uint32_t pos = 8 * t + __ffs(bits) - 1;
           if (r >= M || pos >= L) { bad = true; break; }
           const uint32_t v = mant_value(mstream, Mex + r);
-          if (v == 0) bad = true; else s_mask[pos] = (uint16_t)v;
+          if (!ow && v == 0) bad = true; else put_record(s_mask, s_rec[0], pos, v, ow);
         }
         r = xbM;
         for (uint32_t bits = byteMb; bits; bits &= bits - 1, r++) {
           const uint32_t pos = 8 * (t + 256) + __ffs(bits) - 1;
           if (r >= M || pos >= L) { bad = true; break; }
           const uint32_t v = mant_value(mstream, Mex + r);
-          if (v == 0) bad = true; else s_mask[pos] = (uint16_t)v;
+          if (!ow && v == 0) bad = true; else put_record(s_mask, s_rec[0], pos, v, ow);
         }
       }
       __syncthreads();
@@ -268,8 +318,8 @@ k_apply_dense(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_
         if ((uint32_t)t < R) {
           const uint32_t pos = xaR + aR;
           const uint32_t v = load_u16(rstream + 2 * t);
-          if (pos >= L || (v & kSignExp) == 0 || s_mask[pos] != 0) bad = true;
-          else s_mask[pos] = (uint16_t)v;
+          if (pos >= L || !rare_ok(s_mask, s_rec[0], pos, v, ow)) bad = true;
+          else put_record(s_mask, s_rec[1], pos, v, ow);
         }
       } else {
         if (totaR + totbR != R) bad = true;
@@ -278,14 +328,16 @@ k_apply_dense(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_
           const uint32_t pos = 8 * t + __ffs(bits) - 1;
           if (r >= R || pos >= L) { bad = true; break; }
           const uint32_t v = load_u16(rstream + 2 * r);
-          if ((v & kSignExp) == 0 || s_mask[pos] != 0) bad = true; else s_mask[pos] = (uint16_t)v;
+          if (!rare_ok(s_mask, s_rec[0], pos, v, ow)) bad = true;
+          else put_record(s_mask, s_rec[1], pos, v, ow);
         }
         r = xbR;
         for (uint32_t bits = byteRb; bits; bits &= bits - 1, r++) {
           const uint32_t pos = 8 * (t + 256) + __ffs(bits) - 1;
           if (r >= R || pos >= L) { bad = true; break; }
           const uint32_t v = load_u16(rstream + 2 * r);
-          if ((v & kSignExp) == 0 || s_mask[pos] != 0) bad = true; else s_mask[pos] = (uint16_t)v;
+          if (!rare_ok(s_mask, s_rec[0], pos, v, ow)) bad = true;
+          else put_record(s_mask, s_rec[1], pos, v, ow);
         }
       }
     }
@@ -293,7 +345,13 @@ k_apply_dense(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_
     __syncthreads();
     const bool chunk_bad = s_bad != 0;
     if (!chunk_bad) {
-      const uint4 ma = s_mask4[t], mb = s_mask4[t + 256];
+      uint4 ma = s_mask4[t], mb = s_mask4[t + 256];
+      if (ow) {   // targets -> XOR masks against the current values of groups t and t + 256
+        const uint32_t sh = (8 * t) & 31;
+        ma = overwrite_mask(ma, oa, (s_rec[0][t >> 2] >> sh) & 0xFFu, (s_rec[1][t >> 2] >> sh) & 0xFFu);
+        mb = overwrite_mask(mb, ob, (s_rec[0][(t + 256) >> 2] >> sh) & 0xFFu,
+                            (s_rec[1][(t + 256) >> 2] >> sh) & 0xFFu);
+      }
       const uint4 ra = make_uint4(oa.x ^ ma.x, oa.y ^ ma.y, oa.z ^ ma.z, oa.w ^ ma.w);
       const uint4 rb = make_uint4(ob.x ^ mb.x, ob.y ^ mb.y, ob.z ^ mb.z, ob.w ^ mb.w);
       const bool cha = (ma.x | ma.y | ma.z | ma.w) != 0, chb = (mb.x | mb.y | mb.z | mb.w) != 0;
@@ -443,18 +501,20 @@ __device__ __forceinline__ uint32_t mant_at(const uint8_t* __restrict__ mbytes, 
   return v & kMant;
 }
 
-// Decodes a version-3 compact chunk (one warp) into ent[0..M+R) as pos << 16 | XOR value in
-// ascending position, 32 changes at a time: gap bytes from blk (a zero byte takes the next
+// Decodes a version-3 compact chunk (one warp) into ent[0..M+R) in the general entry layout,
+// in ascending position, 32 changes at a time: gap bytes from blk (a zero byte takes the next
 // X-stream value, which must exceed 255; at most E of them, and exactly E), positions from
 // the prefix sums of the gaps (first position = first gap - 1, all below L), classes from the
 // class bits at blk + M + R (exactly R set, pad bits zero), mantissa-only values from the M
-// stream (nonzero), rare values from the R stream (a sign or exponent bit set).  Returns
+// stream, rare values from the R stream (XOR payloads: a mantissa mask is nonzero, a rare mask
+// has a sign or exponent bit; an overwrite payload's values are unrestricted).  Returns
 // whether the chunk is malformed (the same on every lane).
 __device__ __forceinline__ bool decode_compact(const uint8_t* __restrict__ blk,
                                                const uint16_t* __restrict__ xs, uint32_t E,
                                                const uint8_t* __restrict__ mbytes, uint32_t s0,
                                                const uint16_t* __restrict__ rvals, uint32_t M,
-                                               uint32_t R, uint32_t L, uint32_t* __restrict__ ent) {
+                                               uint32_t R, uint32_t L, bool ow,
+                                               uint32_t* __restrict__ ent) {
   const int lane = threadIdx.x & 31;
   const uint32_t lt = (1u << lane) - 1;
   const uint32_t k = M + R;
@@ -482,14 +542,16 @@ __device__ __forceinline__ bool decode_compact(const uint8_t* __restrict__ blk,
       if (isR) {
         const uint32_t r = rr + __popc(bR & lt);
         if (r < R) v = rvals[r];
-        if ((v & kSignExp) == 0) bad = true;
+        else bad = true;
+        if (!ow && (v & kSignExp) == 0) bad = true;
       } else {
         const uint32_t m = mr + __popc(bM & lt);
         if (m < M) v = mant_at(mbytes, s0, m);
-        if (v == 0) bad = true;
+        else bad = true;
+        if (!ow && v == 0) bad = true;
       }
       if (p >= L) bad = true;
-      if (!bad) ent[i] = (p << 16) | v;
+      if (!bad) ent[i] = (isR ? kEntRare : 0u) | (p << 16) | v;
     }
     mr += __popc(bM);
     rr += __popc(bR);
@@ -497,6 +559,26 @@ __device__ __forceinline__ bool decode_compact(const uint8_t* __restrict__ blk,
   if (xr != E || rr != R) bad = true;
   if (lane == 0 && (k & 7) != 0 && (cls[(k - 1) >> 3] >> (k & 7)) != 0) bad = true;
   return __any_sync(kFull, bad);
+}
+
+// Asks L2 for the 128-byte line holding p when p lies before end (a hint: nothing waits for
+// it, and nothing is asked past the end of the payload).
+__device__ __forceinline__ void prefetch_l2_before(const uint8_t* p, const uint8_t* end) {
+  if (p < end) asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// The payload bytes of the chunk after this one in a warp's range follow this chunk's bytes in
+// each section: ask L2 for their first lines (4 of the position section, 2 of the M stream, 1
+// each of the R and X streams) while this chunk is decoded.
+__device__ __forceinline__ void prefetch_next_payload(const uint8_t* pos_next,
+                                                      const uint8_t* m_next,
+                                                      const uint8_t* r_next,
+                                                      const uint8_t* x_next, const uint8_t* end) {
+  const int lane = threadIdx.x & 31;
+  if (lane < 4) prefetch_l2_before(pos_next + 128 * lane, end);
+  else if (lane < 6) prefetch_l2_before(m_next + 128 * (lane - 4), end);
+  else if (lane == 6) prefetch_l2_before(r_next, end);
+  else if (lane == 7) prefetch_l2_before(x_next, end);
 }
 
 // Entry i of a u16 delta list.  Versions 1 and 2 place every list at an even offset; after an
@@ -574,11 +656,12 @@ k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
       const uint8_t* mbytes = payload + I.m_start + (mbit0 >> 3);
       const uint32_t s0 = (uint32_t)(mbit0 & 7);
       const bool both = M > 0 && R > 0;
+      const bool ow = V3 && (I.flags & kFlagOverwrite) != 0;
       bool bad = false;
       if (V3 && cc.compact) {
         bad = decode_compact(mlist,
                              reinterpret_cast<const uint16_t*>(payload + I.x_start) + pre.e + lc.w,
-                             cc.E, mbytes, s0, rvals, M, R, L, ent);
+                             cc.E, mbytes, s0, rvals, M, R, L, ow, ent);
       } else {
         if (both) s_bits[w][lane] = make_uint4(0, 0, 0, 0);
         __syncwarp();
@@ -595,7 +678,7 @@ k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
             uint32_t v = (uint32_t)mbytes[bit >> 3] >> sh;
             if (sh > 1) v |= (uint32_t)mbytes[(bit >> 3) + 1] << (8 - sh);
             v &= kMant;
-            if (p >= L || v == 0) {
+            if (p >= L || (!ow && v == 0)) {
               bad = true;
             } else {
               ent[i] = (p << 16) | v;
@@ -614,9 +697,9 @@ k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
           carry = __shfl_sync(kFull, p, 31);
           if (in) {
             const uint32_t v = rvals[i];
-            if (p >= L || (v & kSignExp) == 0) bad = true;
+            if (p >= L || (!ow && (v & kSignExp) == 0)) bad = true;
             else if (both && ((bits[p >> 5] >> (p & 31)) & 1u)) bad = true;
-            else ent[M + i] = (p << 16) | v;
+            else ent[M + i] = (V3 ? kEntRare : 0u) | (p << 16) | v;
           }
         }
       }
@@ -628,9 +711,13 @@ k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
       __syncwarp();
       uint16_t* base = J.out + e0;   // 4-byte aligned: out is 16-byte aligned, e0 % 4096 == 0
       for (uint32_t i = lane; i < M + R; i += 32) {
-        const uint32_t e = ent[i], p = e >> 16;
-        atomicXor(reinterpret_cast<unsigned int*>(base + (p & ~1u)),
-                  (e & 0xFFFFu) << (16 * (p & 1)));
+        const uint32_t e = ent[i], p = V3 ? ent_pos(e) : e >> 16;
+        uint32_t x = e & 0xFFFFu;
+        if (ow) {   // the new value or mantissa, XORed in against the element's current bits
+          const uint32_t now = ld_l2_u16(base + p);
+          x = (e & kEntRare) ? (now ^ x) : ((now & kMant) ^ x);
+        }
+        if (x) atomicXor(reinterpret_cast<unsigned int*>(base + (p & ~1u)), x << (16 * (p & 1)));
       }
       // every lane's atomics are performed before any lane reads the chunk back
       __threadfence_block();
@@ -650,14 +737,15 @@ k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
 // Changes to the same word are serialised by the atomics, so their terms telescope to the
 // word's final term minus its original one.  Nothing else of the chunk is read.  Chunks with
 // a bitmap block are listed for apply_dense<true>.
-template <bool V3>
+template <bool V3, bool OW>
 __global__ void __launch_bounds__(kThreads, 4)
 k_apply_incr(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
              const uint64_t* __restrict__ tile_start, uint32_t k, uint64_t total_chunks,
              const uint4* __restrict__ loc, const TileSum* __restrict__ tile_pre,
              JobInfo* __restrict__ info, uint32_t* __restrict__ list_count,
              uint32_t* __restrict__ list, uint8_t* __restrict__ ck_base) {
-  if ((list_count[kFlagV3Word] != 0) != V3) return;   // the other build runs this call
+  // another build runs this call
+  if ((list_count[kFlagV3Word] != 0) != V3 || (list_count[kFlagOwWord] != 0) != OW) return;
   __shared__ uint32_t s_ent[kWarps][kEntMax];       // pos << 16 | XOR value
   __shared__ uint4 s_bits[kWarps][kChunk / 128];    // mantissa-only positions, 512 B
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -701,12 +789,17 @@ k_apply_incr(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
     const uint64_t mbit0 = 7 * Mex;
     const uint8_t* mbytes = payload + I.m_start + (mbit0 >> 3);
     const uint32_t s0 = (uint32_t)(mbit0 & 7);
+    prefetch_next_payload(mlist + chunk_pos_bytes(cc, B),
+                          payload + I.m_start + ((7 * (Mex + M)) >> 3),
+                          reinterpret_cast<const uint8_t*>(rvals + R),
+                          payload + I.x_start + 2 * (pre.e + lc.w + cc.E), payload + J.size);
     const bool both = M > 0 && R > 0;
+    const bool ow = OW && (I.flags & kFlagOverwrite) != 0;
     bool bad = false;
     if (V3 && cc.compact) {
       bad = decode_compact(mlist,
                            reinterpret_cast<const uint16_t*>(payload + I.x_start) + pre.e + lc.w,
-                           cc.E, mbytes, s0, rvals, M, R, L, ent);
+                           cc.E, mbytes, s0, rvals, M, R, L, ow, ent);
     } else {
       if (both) s_bits[w][lane] = make_uint4(0, 0, 0, 0);
       __syncwarp();
@@ -723,7 +816,7 @@ k_apply_incr(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
           uint32_t v = (uint32_t)mbytes[bit >> 3] >> sh;
           if (sh > 1) v |= (uint32_t)mbytes[(bit >> 3) + 1] << (8 - sh);
           v &= kMant;
-          if (p >= L || v == 0) {
+          if (p >= L || (!ow && v == 0)) {
             bad = true;
           } else {
             ent[i] = (p << 16) | v;
@@ -742,9 +835,9 @@ k_apply_incr(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
         carry = __shfl_sync(kFull, p, 31);
         if (in) {
           const uint32_t v = rvals[i];
-          if (p >= L || (v & kSignExp) == 0) bad = true;
+          if (p >= L || (!ow && (v & kSignExp) == 0)) bad = true;
           else if (both && ((bits[p >> 5] >> (p & 31)) & 1u)) bad = true;
-          else ent[M + i] = (p << 16) | v;
+          else ent[M + i] = (V3 ? kEntRare : 0u) | (p << 16) | v;
         }
       }
     }
@@ -762,21 +855,58 @@ k_apply_incr(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
     const uint32_t in_last = (uint32_t)(n - 4 * wlast);   // values of the last word, 1..4
     const uint64_t last_mask = in_last == 4 ? ~0ull : ((1ull << (16 * in_last)) - 1);
     // kB entries per lane per round: their atomics are issued back to back, then the terms
-    // (3 in the build for any version, whose compact decoder leaves fewer registers: with 4
-    // it spilled at 64 registers, and 3 blocks per SM instead was slower)
-    constexpr int kB = V3 ? 3 : 4;
+    // (3 in the general build, whose compact decoder leaves fewer registers: with 4 it
+    // spilled at 64 registers, and 3 blocks per SM instead was slower; 2 in the build that
+    // also applies overwrites, which spilled with 3)
+    constexpr int kB = V3 ? (OW ? 2 : 3) : 4;
     for (uint32_t r0 = 0; r0 < M + R; r0 += 32 * kB) {
       uint64_t before[kB], dd[kB];
       uint32_t pp[kB];
+      if (!ow) {
 #pragma unroll
-      for (int u = 0; u < kB; u++) {
-        const uint32_t i = r0 + 32 * u + lane;
-        pp[u] = 0xFFFFFFFFu;
-        if (i < M + R) {
-          const uint32_t e = ent[i], p = e >> 16;
-          pp[u] = p;
-          dd[u] = (uint64_t)(e & 0xFFFFu) << (16 * (p & 3));
-          before[u] = atomicXor(base + (p >> 2), (unsigned long long)dd[u]);
+        for (int u = 0; u < kB; u++) {
+          const uint32_t i = r0 + 32 * u + lane;
+          pp[u] = 0xFFFFFFFFu;
+          if (i < M + R) {
+            const uint32_t e = ent[i], p = V3 ? ent_pos(e) : e >> 16;
+            pp[u] = p;
+            dd[u] = (uint64_t)(e & 0xFFFFu) << (16 * (p & 3));
+            before[u] = atomicXor(base + (p >> 2), (unsigned long long)dd[u]);
+          }
+        }
+      } else {
+        // overwrite: the new value or mantissa, XORed in against the element's current bits
+        // (the round's reads are issued before the first is used); an element that already
+        // holds its new bits is left alone.  The word after the change is formed below from
+        // the word before it, which holds this element's bits as read.
+        uint32_t now[kB];
+#pragma unroll
+        for (int u = 0; u < kB; u++) {
+          const uint32_t i = r0 + 32 * u + lane;
+          pp[u] = 0xFFFFFFFFu;
+          if (i < M + R) {
+            pp[u] = ent_pos(ent[i]);
+            now[u] = ld_l2_u16(J.out + e0 + pp[u]);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kB; u++) {
+          if (pp[u] != 0xFFFFFFFFu) {
+            const uint32_t e = ent[r0 + 32 * u + lane], t = e & 0xFFFFu;
+            const uint32_t x = (e & kEntRare) ? (now[u] ^ t) : ((now[u] & kMant) ^ t);
+            if (x == 0) pp[u] = 0xFFFFFFFFu;
+            else before[u] = atomicXor(base + (pp[u] >> 2),
+                                       (unsigned long long)x << (16 * (pp[u] & 3)));
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kB; u++) {
+          if (pp[u] != 0xFFFFFFFFu) {
+            const uint32_t e = ent[r0 + 32 * u + lane], t = e & 0xFFFFu, sh = 16 * (pp[u] & 3);
+            const uint32_t was = (uint32_t)(before[u] >> sh) & 0xFFFFu;
+            const uint32_t to = (e & kEntRare) ? t : ((was & kSignExp) | t);
+            dd[u] = (uint64_t)(was ^ to) << sh;
+          }
         }
       }
 #pragma unroll
@@ -859,12 +989,13 @@ int blocks_per_sm(K kernel) {
 
 }  // namespace
 
-// Launches both builds of a thread-level apply kernel (versions 1-2 only, any version); the
-// scan's version-3 word decides on the device which of them works.
+// Launches the builds of a thread-level apply kernel (XOR payloads of versions 1-2 only, the
+// general one; from `first`); the scan's selection words decide on the device which works.
 template <typename K>
-cudaError_t launch_both(const LaunchCtx& c, K k12, int per_sm12, K k3, int per_sm3) {
+cudaError_t launch_both(const LaunchCtx& c, K k12, int per_sm12, K k3, int per_sm3,
+                        int first = 0) {
   const uint64_t want = (c.chunks + kWarps - 1) / kWarps;
-  for (int b = 0; b < 2; b++) {
+  for (int b = first; b < 2; b++) {
     const uint64_t grid = std::min<uint64_t>(want, (uint64_t)(b ? per_sm3 : per_sm12) * c.sms);
     (b ? k3 : k12)<<<(unsigned)grid, kThreads, 0, c.stream>>>(
         reinterpret_cast<const DJob*>(c.ws + c.lay.jobs),
@@ -901,9 +1032,13 @@ cudaError_t launch_copy_jobs(const LaunchCtx& c) {
 
 cudaError_t launch_apply_incremental(const LaunchCtx& c) {
   if (c.chunks == 0) return cudaSuccess;
-  static const int per_sm12 = blocks_per_sm(k_apply_incr<false>);
-  static const int per_sm3 = blocks_per_sm(k_apply_incr<true>);
-  return launch_both(c, k_apply_incr<false>, per_sm12, k_apply_incr<true>, per_sm3);
+  static const int per_sm12 = blocks_per_sm(k_apply_incr<false, false>);
+  static const int per_sm3 = blocks_per_sm(k_apply_incr<true, false>);
+  static const int per_smo = blocks_per_sm(k_apply_incr<true, true>);
+  cudaError_t e = launch_both(c, k_apply_incr<false, false>, per_sm12, k_apply_incr<true, false>,
+                              per_sm3);
+  if (e != cudaSuccess) return e;
+  return launch_both(c, k_apply_incr<true, true>, per_smo, k_apply_incr<true, true>, per_smo, 1);
 }
 
 cudaError_t launch_apply(const LaunchCtx& c, bool incremental) {

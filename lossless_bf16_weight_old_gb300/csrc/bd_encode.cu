@@ -70,7 +70,7 @@ __device__ __forceinline__ uint64_t hash_group_full(uint4 v, uint64_t key) {
 // ------------------------------------------------------------------------ encode_slots
 
 // Gaps above 255 in a chunk's merged position list, counted from its k slot entries (position
-// order, pos << 16 | x): the first gap is p_0 + 1, then p_i - p_{i-1}.
+// order, either layout): the first gap is p_0 + 1, then p_i - p_{i-1}.
 __device__ __forceinline__ uint32_t slot_escapes(const uint32_t* __restrict__ entries,
                                                  uint32_t k) {
   const int lane = threadIdx.x & 31;
@@ -78,7 +78,7 @@ __device__ __forceinline__ uint32_t slot_escapes(const uint32_t* __restrict__ en
   uint32_t esc = 0;
   for (uint32_t i0 = 0; i0 < k; i0 += 32) {
     const uint32_t i = i0 + lane;
-    const int32_t pos = i < k ? (int32_t)(entries[i] >> 16) : 0;
+    const int32_t pos = i < k ? (int32_t)ent_pos(entries[i]) : 0;
     int32_t prev = __shfl_up_sync(0xFFFFFFFFu, pos, 1);
     if (lane == 0) prev = carry;
     esc += __popc(__ballot_sync(0xFFFFFFFFu, i < k && pos - prev > 255));
@@ -126,7 +126,12 @@ __device__ __noinline__ uint32_t chunk_escapes(const uint16_t* __restrict__ old,
   return esc;
 }
 
-template <bool FULL, bool COMPACT>
+// GEN: the general build (version 3, overwrite payloads): the chunk's escaped gaps counted.
+// OW: slot entries in the general layout (kEntRare | pos << 16 | value) with the new field
+// values (the new value of a rare change, the new mantissa of a mantissa-only one), read back
+// from a per-lane shared copy of the step's new values; otherwise pos << 16 | x (the class
+// follows from x).
+template <bool FULL, bool GEN, bool OW>
 __device__ __forceinline__ void encode_chunk(const uint16_t* __restrict__ old,
                                              const uint16_t* __restrict__ neu, uint64_t n,
                                              uint64_t e0, uint32_t* __restrict__ slot,
@@ -134,9 +139,10 @@ __device__ __forceinline__ void encode_chunk(const uint16_t* __restrict__ old,
                                              uint32_t* __restrict__ counts,
                                              uint32_t* __restrict__ list_count,
                                              uint32_t* __restrict__ list,
-                                             uint4* __restrict__ xs) {
+                                             uint4* __restrict__ xs, uint4* __restrict__ ns) {
   const int lane = threadIdx.x & 31;
   const uint16_t* xs16 = reinterpret_cast<const uint16_t*>(xs);
+  const uint16_t* ns16 = reinterpret_cast<const uint16_t*>(ns);
   const uint64_t words = (n + 3) >> 2;
   uint32_t* __restrict__ entries = slot + kSlotHeader / 4;
   uint32_t running = 0;        // changes in the steps done so far
@@ -180,6 +186,10 @@ __device__ __forceinline__ void encode_chunk(const uint16_t* __restrict__ old,
     if (nz) {   // the lane's 16 XOR values, read back by position in the loop below
       xs[0] = x0;
       xs[1] = x1;
+      if (OW) {
+        ns[0] = pn0;
+        ns[1] = pn1;
+      }
     }
     const uint32_t cnt = __popc(nz);
     const uint32_t incl = warp_incl_scan(cnt);
@@ -188,12 +198,17 @@ __device__ __forceinline__ void encode_chunk(const uint16_t* __restrict__ old,
     for (uint32_t bits = nz; bits; bits &= bits - 1) {
       const int b = __ffs(bits) - 1;
       const uint32_t xv = xs16[b];
-      if (xv & kSignExp) {
+      const bool rare = (xv & kSignExp) != 0;
+      uint32_t val = xv;
+      if (OW) val = rare ? (uint32_t)ns16[b] : (uint32_t)(ns16[b] & kMant);
+      if (rare) {
         rl++;
       } else if (lane_fm == 0) {
-        lane_fm = xv | kAuxHasM;
+        lane_fm = val | kAuxHasM;
       }
-      if (idx < kSlotEntries) entries[idx] = ((eloc + b) << 16) | xv;
+      if (idx < kSlotEntries)
+        entries[idx] = OW ? ((rare ? kEntRare : 0u) | ((eloc + b) << 16) | val)
+                          : (((eloc + b) << 16) | xv);
       idx++;
     }
     nl += cnt;
@@ -211,8 +226,8 @@ __device__ __forceinline__ void encode_chunk(const uint16_t* __restrict__ old,
   const uint32_t runR = __shfl_sync(0xFFFFFFFFu, rl, 31);
   const uint32_t runM = __shfl_sync(0xFFFFFFFFu, nl, 31) - runR;
   const bool overflow = runM + runR > kSlotEntries;
-  uint32_t esc = 0;   // COMPACT: gaps above 255 in the chunk's merged position list
-  if (COMPACT && runM + runR <= kCompactMax) {
+  uint32_t esc = 0;   // GEN: gaps above 255 in the chunk's merged position list
+  if (GEN && runM + runR <= kCompactMax) {
     if (!overflow) {
       __syncwarp();   // the slot entries written by every lane are visible to the warp
       esc = slot_escapes(entries, runM + runR);
@@ -228,13 +243,14 @@ __device__ __forceinline__ void encode_chunk(const uint16_t* __restrict__ old,
   }
 }
 
-template <bool COMPACT>
+template <bool GEN, bool OW>
 __global__ void __launch_bounds__(kThreads, 4)
 k_encode_slots(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
                uint32_t k, uint64_t total_chunks, uint32_t* __restrict__ counts,
                uint8_t* __restrict__ slots, uint8_t* __restrict__ ck_base,
                uint32_t* __restrict__ list_count, uint32_t* __restrict__ list) {
   __shared__ uint4 s_xs[kThreads][2];   // per thread: the 16 XOR values of its current step
+  __shared__ uint4 s_ns[OW ? kThreads : 1][2];   // OW: its 16 new values
   const int lane = threadIdx.x & 31;
   const uint64_t gwarp = ((uint64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
   const uint64_t nwarps = ((uint64_t)gridDim.x * kThreads) >> 5;
@@ -260,12 +276,13 @@ k_encode_slots(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
       prefetch_chunk_l2(jobs[j].old + e0);
       prefetch_chunk_l2(jobs[j].neu + e0);
     }
+    uint4* ns = s_ns[OW ? threadIdx.x : 0];
     if (e0 + kChunk <= n)
-      encode_chunk<true, COMPACT>(jobs[j].old, jobs[j].neu, n, e0, slot, ck, g, counts,
-                                  list_count, list, s_xs[threadIdx.x]);
+      encode_chunk<true, GEN, OW>(jobs[j].old, jobs[j].neu, n, e0, slot, ck, g, counts,
+                                  list_count, list, s_xs[threadIdx.x], ns);
     else
-      encode_chunk<false, COMPACT>(jobs[j].old, jobs[j].neu, n, e0, slot, ck, g, counts,
-                                   list_count, list, s_xs[threadIdx.x]);
+      encode_chunk<false, GEN, OW>(jobs[j].old, jobs[j].neu, n, e0, slot, ck, g, counts,
+                                   list_count, list, s_xs[threadIdx.x], ns);
   }
   if (cur != 0xFFFFFFFFu) {
     const uint64_t s = warp_sum64(ck);
@@ -416,20 +433,22 @@ struct CompactState {
 };
 
 // Emits the 32 changes cs.i .. cs.i+31 of a compact chunk in position order, lane l holding
-// change cs.i + l as pos << 16 | x when `valid` (the valid lanes are a prefix; cs.i is a
-// multiple of 32).  Gap g = pos - previous position (pos + 1 for the first change) goes to
+// change cs.i + l as a slot entry (OW: the general layout; else pos << 16 | x) when `valid`
+// (the valid lanes are a prefix; cs.i is a multiple of 32).  Gap g = pos - previous position (pos + 1 for the first change) goes to
 // byte cs.i + l, or 0 there and g to the X stream when g > 255; the class bits of the batch
 // are 4 whole bytes of the class section, written by lanes 0..3.
+template <bool OW>
 __device__ __forceinline__ void compact_batch(uint32_t e, bool valid, CompactState& cs,
                                               const CompactOut& o) {
   const int lane = threadIdx.x & 31;
   const uint32_t lt = (1u << lane) - 1;
-  const uint32_t pos = e >> 16, x = e & 0xFFFFu;
+  const uint32_t pos = ent_pos(e), x = e & 0xFFFFu;
   uint32_t prev = __shfl_up_sync(0xFFFFFFFFu, pos, 1);
   if (lane == 0) prev = cs.prev;
   const uint32_t gap = pos - prev;
-  const bool isR = valid && (x & kSignExp) != 0;
-  const bool isM = valid && (x & kSignExp) == 0;
+  const bool rare = OW ? (e & kEntRare) != 0 : (x & kSignExp) != 0;
+  const bool isR = valid && rare;
+  const bool isM = valid && !rare;
   const bool esc = valid && gap > 255;
   const uint32_t bM = __ballot_sync(0xFFFFFFFFu, isM), bR = __ballot_sync(0xFFFFFFFFu, isR),
                  bE = __ballot_sync(0xFFFFFFFFu, esc);
@@ -465,8 +484,9 @@ __device__ __forceinline__ void emit_ctx(EmitCtx& cx, uint8_t* payload, const Jo
 
 // Chunks whose changes fit their slot: the slot's single position-ordered list is split by
 // class 32 entries at a time with ballots (rank = set lanes below; the previous element of
-// the same class, for the delta, is the nearest such lane below or the carry).
-template <bool V3>
+// the same class, for the delta, is the nearest such lane below or the carry).  GEN: the
+// general build (version-3 compact blocks); OW: slot entries in the general layout.
+template <bool GEN, bool OW>
 __global__ void __launch_bounds__(kThreads, 4)
 k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
        const uint64_t* __restrict__ tile_start, uint32_t k, uint64_t total_chunks,
@@ -499,7 +519,7 @@ k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
     const uint64_t c = g - chunk_start[j];
     const uint64_t g_job_end = chunk_start[j + 1];
     const TileSum pre = tile_pre[tile_start[j] + c / kTileChunks];
-    const uint32_t cnt_here = V3 ? counts[g] : 0u;
+    const uint32_t cnt_here = GEN ? counts[g] : 0u;
     const uint32_t cnt_next = g + 1 < g_job_end ? counts[g + 1] : 0u;
     const uint32_t aux_next =
         g + 1 < g_job_end ? reinterpret_cast<const uint32_t*>(slot + kSlotBytes)[1] : 0u;
@@ -525,13 +545,13 @@ k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
     const uint32_t B = (L + 7) >> 3;
     const uint64_t Pex = pre.p + lc.x, Mex = pre.m + lc.y, Rex = pre.r + lc.z;
     const uint32_t nesc = wcount_e(cnt_here);
-    const bool compact = V3 && I.version == 3 && choose_compact(M, R, nesc, B);
+    const bool compact = GEN && I.version == 3 && choose_compact(M, R, nesc, B);
     if (lane == 0)
       reinterpret_cast<uint32_t*>(payload + count_table_offset(I.r_start, jobs[j].nchunks))[c] =
-          count_entry(V3 ? I.version : 1u, M, R, nesc, compact);
+          count_entry(GEN ? I.version : 1u, M, R, nesc, compact);
     EmitCtx cx;
     emit_ctx(cx, payload, I, M, R, B, Pex, Rex, sm);
-    if (V3 && compact) {
+    if (GEN && compact) {
       cx.listM = cx.listR = true;   // no bitmap
       const CompactOut o{payload + I.p_start + Pex,
                          reinterpret_cast<uint16_t*>(payload + I.x_start) + pre.e + lc.w,
@@ -540,7 +560,7 @@ k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
 #pragma unroll
       for (int q = 0; q < 8; q++) {
         if (32u * q >= kk) break;
-        compact_batch(ent[q], 32u * q + lane < kk, cs, o);
+        compact_batch<OW>(ent[q], 32u * q + lane < kk, cs, o);
       }
     }
     if (!cx.listM || !cx.listR) {
@@ -551,10 +571,11 @@ k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
 #pragma unroll
     for (int q = 0; q < 8; q++) {
       if (compact || 32u * q >= kk) break;
-      const uint32_t e = ent[q], pos = e >> 16, x = e & 0xFFFFu;
+      const uint32_t e = ent[q], pos = OW ? ent_pos(e) : e >> 16, x = e & 0xFFFFu;
       const bool valid = 32u * q + lane < kk;
-      const bool isR = valid && (x & kSignExp);
-      const bool isM = valid && !(x & kSignExp);
+      const bool rare = OW ? (e & kEntRare) != 0 : (x & kSignExp) != 0;
+      const bool isR = valid && rare;
+      const bool isM = valid && !rare;
       const uint32_t bM = __ballot_sync(0xFFFFFFFFu, isM), bR = __ballot_sync(0xFFFFFFFFu, isR);
       // (In versions 1 and 2 every M block starts at an even offset; after an odd-length
       // compact block of version 3 it may not, hence the alignment-checking stores there.)
@@ -564,7 +585,7 @@ k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
         if (isM) {
           const uint32_t r = baseM + lane;
           const uint32_t prev = lane ? prevL : carryM;
-          if (V3) store_u16(cx.mblk + 2 * r, (uint16_t)(pos - prev));
+          if (GEN) store_u16(cx.mblk + 2 * r, (uint16_t)(pos - prev));
           else reinterpret_cast<uint16_t*>(cx.mblk)[r] = (uint16_t)(pos - prev);
           sm->mv[r] = (uint8_t)(x & kMant);
         }
@@ -579,7 +600,7 @@ k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
       if (isM) {
         const uint32_t r = baseM + __popc(lowM);
         const uint32_t prev = lowM ? pM : carryM;
-        if (cx.listM && V3) store_u16(cx.mblk + 2 * r, (uint16_t)(pos - prev));
+        if (cx.listM && GEN) store_u16(cx.mblk + 2 * r, (uint16_t)(pos - prev));
         else if (cx.listM) reinterpret_cast<uint16_t*>(cx.mblk)[r] = (uint16_t)(pos - prev);
         else atomicOr(&sm->bm[pos >> 5], 1u << (pos & 31));
         sm->mv[r] = (uint8_t)(x & kMant);
@@ -658,6 +679,7 @@ k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
     const uint4 lc = loc[g];
     const uint64_t Pex = pre.p + lc.x, Mex = pre.m + lc.y, Rex = pre.r + lc.z;
     const bool compact = I.version == 3 && choose_compact(M, R, E, B);
+    const bool ow = (J.flags & kFlagOverwrite) != 0;
     uint8_t* payload = J.payload;
     if (lane == 0)
       reinterpret_cast<uint32_t*>(payload + count_table_offset(I.r_start, jobs[j].nchunks))[c] =
@@ -688,7 +710,16 @@ k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
         uint32_t idx = base + incl - cntl;
         for (uint32_t bits = nz; bits; bits &= bits - 1, idx++) {
           const int b = __ffs(bits) - 1;
-          if (idx < kCompactMax) lst[idx] = ((eloc + b) << 16) | elem_of(b < 8 ? x0 : x1, b & 7);
+          const uint32_t xv = elem_of(b < 8 ? x0 : x1, b & 7);
+          const bool rare = (xv & kSignExp) != 0;
+          uint32_t val = xv;
+          if (ow) {
+            const uint32_t nv = elem_of(load8(neu, e + (b & 8), n), b & 7);
+            val = rare ? nv : (nv & kMant);
+          }
+          if (idx < kCompactMax)
+            lst[idx] = ow ? ((rare ? kEntRare : 0u) | ((eloc + b) << 16) | val)
+                          : (((eloc + b) << 16) | xv);
         }
         base += __shfl_sync(0xFFFFFFFFu, incl, 31);
       }
@@ -700,17 +731,22 @@ k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
       CompactState cs{0xFFFFFFFFu, 0, 0, 0, 0};
       for (uint32_t i0 = 0; i0 < kk; i0 += 32) {
         const bool valid = i0 + lane < kk;
-        compact_batch(valid ? lst[i0 + lane] : 0u, valid, cs, o);
+        if (ow) compact_batch<true>(valid ? lst[i0 + lane] : 0u, valid, cs, o);
+        else compact_batch<false>(valid ? lst[i0 + lane] : 0u, valid, cs, o);
       }
     }
     for (int s = 0; s < 8 && !compact; s++) {
       const uint32_t eloc = s * 512 + lane * 16;
       const uint64_t e = e0 + eloc;
-      const uint4 x0 = xor4(load8(old, e, n), load8(neu, e, n));
-      const uint4 x1 = xor4(load8(old, e + 8, n), load8(neu, e + 8, n));
+      const uint4 n0 = load8(neu, e, n), n1 = load8(neu, e + 8, n);
+      const uint4 x0 = xor4(load8(old, e, n), n0);
+      const uint4 x1 = xor4(load8(old, e + 8, n), n1);
       const uint32_t rare = rare_mask16(x0, x1);
+      // the value emitted: the XOR mask, or with overwrite the new value (the M stream keeps
+      // its mantissa bits)
+      const uint4 v0 = ow ? n0 : x0, v1 = ow ? n1 : x1;
       emit_batch(eloc, nz_mask16(x0, x1) & ~rare, rare,
-                 [x0, x1](int b) { return elem_of(b < 8 ? x0 : x1, b & 7); }, st, cx);
+                 [v0, v1](int b) { return elem_of(b < 8 ? v0 : v1, b & 7); }, st, cx);
       __syncwarp();
       const uint32_t known = min(st.rankM, M);  // values with rank < known are in the window
       if (known > cx.wbase) {
@@ -764,12 +800,15 @@ uint64_t cap_grid(uint64_t want, uint64_t work_items_per_block, uint64_t items) 
 
 }  // namespace
 
-cudaError_t launch_encode_slots(const LaunchCtx& c, bool compact) {
+cudaError_t launch_encode_slots(const LaunchCtx& c, bool general, bool overwrite) {
   if (c.chunks == 0) return cudaSuccess;
-  static const int per_sm = blocks_per_sm(k_encode_slots<false>, kThreads);
-  static const int per_sm_c = blocks_per_sm(k_encode_slots<true>, kThreads);
-  const uint64_t grid = cap_grid((uint64_t)(compact ? per_sm_c : per_sm) * c.sms, kWarps, c.chunks);
-  auto kernel = compact ? k_encode_slots<true> : k_encode_slots<false>;
+  static const int per_sm = blocks_per_sm(k_encode_slots<false, false>, kThreads);
+  static const int per_sm_g = blocks_per_sm(k_encode_slots<true, false>, kThreads);
+  static const int per_sm_o = blocks_per_sm(k_encode_slots<true, true>, kThreads);
+  const int bps = overwrite ? per_sm_o : general ? per_sm_g : per_sm;
+  const uint64_t grid = cap_grid((uint64_t)bps * c.sms, kWarps, c.chunks);
+  auto kernel = overwrite ? k_encode_slots<true, true>
+                          : general ? k_encode_slots<true, false> : k_encode_slots<false, false>;
   kernel<<<(unsigned)grid, kThreads, 0, c.stream>>>(
       reinterpret_cast<const CJob*>(c.ws + c.lay.jobs),
       reinterpret_cast<const uint64_t*>(c.ws + c.lay.chunk_start), c.k, c.chunks,
@@ -796,12 +835,14 @@ cudaError_t launch_emit_dense(const LaunchCtx& c) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_emit(const LaunchCtx& c, bool v3) {
+cudaError_t launch_emit(const LaunchCtx& c, bool general, bool overwrite) {
   if (c.chunks == 0) return cudaSuccess;
-  static const int per_sm = blocks_per_sm(k_emit<false>, kThreads);
-  static const int per_sm3 = blocks_per_sm(k_emit<true>, kThreads);
-  const uint64_t grid = cap_grid((uint64_t)(v3 ? per_sm3 : per_sm) * c.sms, kWarps, c.chunks);
-  auto kernel = v3 ? k_emit<true> : k_emit<false>;
+  static const int per_sm = blocks_per_sm(k_emit<false, false>, kThreads);
+  static const int per_sm_g = blocks_per_sm(k_emit<true, false>, kThreads);
+  static const int per_sm_o = blocks_per_sm(k_emit<true, true>, kThreads);
+  const int bps = overwrite ? per_sm_o : general ? per_sm_g : per_sm;
+  const uint64_t grid = cap_grid((uint64_t)bps * c.sms, kWarps, c.chunks);
+  auto kernel = overwrite ? k_emit<true, true> : general ? k_emit<true, false> : k_emit<false, false>;
   kernel<<<(unsigned)grid, kThreads, 0, c.stream>>>(
       reinterpret_cast<const CJob*>(c.ws + c.lay.jobs),
       reinterpret_cast<const uint64_t*>(c.ws + c.lay.chunk_start),

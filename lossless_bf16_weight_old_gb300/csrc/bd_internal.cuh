@@ -92,6 +92,18 @@ __host__ __device__ __forceinline__ uint32_t count_entry(uint32_t version, uint3
   return M | (R << 15);
 }
 
+// Header flags (the u64 at byte 72 of a version-2 or -3 header).  kFlagOverwrite: the streams
+// carry new field values (the whole value of a rare change, the mantissa of a mantissa-only
+// change) that overwrite the weights instead of XOR masks; every other bit is zero.
+constexpr uint32_t kFlagOverwrite = 1;
+
+// Entries of the general layout -- compress slots of overwrite payloads, decoded changes in the
+// general apply builds: bit 31 set for a rare change, the chunk-local position in bits 16..27,
+// the value to emit or apply in bits 0..15.  XOR slots use pos << 16 | x (the class follows
+// from x); ent_pos reads the position of either.
+constexpr uint32_t kEntRare = 0x80000000u;
+__host__ __device__ __forceinline__ uint32_t ent_pos(uint32_t e) { return (e >> 16) & 0xFFFu; }
+
 // Compress workspace word of a chunk's counts: M in bits 0..12, R in 13..25, E (gaps above 255
 // in the merged position list, counted only for version 3) in 26..30.
 __host__ __device__ __forceinline__ uint32_t wcount(uint32_t M, uint32_t R, uint32_t E) {
@@ -199,7 +211,7 @@ struct CJob {
   uint64_t tile_base;   // global index of this tensor's first scan tile
   const uint64_t* d_base;   // versions 2 and 3: the base checksum to bind to (NULL: version 1)
   uint32_t version;         // payload version written: 1, 2 or 3 (compact position blocks)
-  uint32_t pad32;
+  uint32_t flags;           // header flags written (versions 2 and 3): kFlagOverwrite
   uint64_t pad[3];
 };
 static_assert(sizeof(CJob) == 128, "CJob layout");
@@ -229,7 +241,7 @@ struct JobInfo {
   int32_t status;      // set by the scan phase; constant while later kernels run
   int32_t chunk_err;   // set by the apply kernel when a chunk is malformed
   uint32_t version;    // payload version (set by the scan phase)
-  uint32_t pad32;
+  uint32_t flags;      // header flags (versions 2 and 3; set by the scan phase)
   uint64_t pad;
 };
 static_assert(sizeof(JobInfo) == 96, "JobInfo layout");
@@ -304,10 +316,14 @@ struct WsLayout {
 };
 
 // Decompress: word of the zeroed `overflow` state that the scan sets when a payload of the
-// call is version 3.  The thread-level apply kernels come in two builds, one for versions 1
-// and 2 only (no compact blocks: fewer registers, aligned list loads) and one for any
-// version; both are launched and the one that does not match this word returns at once.
+// call is version 3 or an overwrite payload.  The thread-level apply kernels come in two
+// builds, one for XOR payloads of versions 1 and 2 only (no compact blocks, no overwrites:
+// fewer registers, aligned list loads) and a general one; both are launched and the one that
+// does not match this word returns at once.
 constexpr uint32_t kFlagV3Word = 1;
+// ... and the word it sets when a payload of the call is an overwrite payload: the
+// incremental apply has a third build, the general one with the overwrite code, selected by it.
+constexpr uint32_t kFlagOwWord = 2;
 
 // Index of the job containing global index g, given starts[0..k] (starts[k] = total).
 __device__ __forceinline__ uint32_t find_job(const uint64_t* __restrict__ starts, uint32_t k,
@@ -385,10 +401,10 @@ struct LaunchCtx {
   uint64_t tiles;      // total scan tiles
 };
 
-cudaError_t launch_encode_slots(const LaunchCtx& c, bool compact);
+cudaError_t launch_encode_slots(const LaunchCtx& c, bool general, bool overwrite);
 cudaError_t launch_scan_tiles(const LaunchCtx& c, bool decompress);
 cudaError_t launch_scan_jobs(const LaunchCtx& c, bool decompress, int32_t* d_status_all);
-cudaError_t launch_emit(const LaunchCtx& c, bool v3);
+cudaError_t launch_emit(const LaunchCtx& c, bool general, bool overwrite);
 cudaError_t launch_emit_dense(const LaunchCtx& c);
 cudaError_t launch_apply_chunks(const LaunchCtx& c);
 cudaError_t launch_apply_incremental(const LaunchCtx& c);

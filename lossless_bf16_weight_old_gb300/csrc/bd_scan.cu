@@ -174,6 +174,7 @@ k_scan_jobs(const void* __restrict__ jobs, const uint64_t* __restrict__ tile_sta
     if (!DEC) {
       const CJob& J = reinterpret_cast<const CJob*>(jobs)[j];
       I.version = J.version;
+      I.flags = J.flags;
       I.r_start = header_bytes(J.version) + 4 * J.nchunks;
       I.x_start = I.r_start + 2 * rR;
       I.p_start = I.x_start + 2 * rE;
@@ -195,9 +196,9 @@ k_scan_jobs(const void* __restrict__ jobs, const uint64_t* __restrict__ tile_sta
         h[5] = rR;
         h[6] = rP;
         h[7] = I.total;
-        if (J.version >= 2) {   // the base this payload applies to, and a reserved zero
+        if (J.version >= 2) {   // the base this payload applies to, and the flags
           h[8] = *J.d_base;
-          h[9] = 0;
+          h[9] = J.flags;
         }
       }
       if (J.d_status) *J.d_status = I.status;
@@ -209,7 +210,12 @@ k_scan_jobs(const void* __restrict__ jobs, const uint64_t* __restrict__ tile_sta
       const uint32_t version = payload_version(J.payload, J.size);
       const uint64_t hdr = header_bytes(version);
       I.version = version;
-      if (version == 3) *v3_flag = 1u;   // selects the apply build that decodes compact blocks
+      const uint64_t flags = version >= 2 && J.size >= kHeaderV2
+                                 ? reinterpret_cast<const uint64_t*>(J.payload)[9] : 0;
+      I.flags = (uint32_t)(flags & kFlagOverwrite);
+      // the general apply build decodes compact blocks and applies overwrites
+      if (version == 3 || I.flags != 0) *v3_flag = 1u;
+      if (I.flags != 0) v3_flag[kFlagOwWord - kFlagV3Word] = 1u;
       I.r_start = hdr + 4 * J.nchunks;
       I.x_start = I.r_start + 2 * rR;
       I.p_start = I.x_start + 2 * rE;
@@ -223,7 +229,7 @@ k_scan_jobs(const void* __restrict__ jobs, const uint64_t* __restrict__ tile_sta
                         h[1] == ((uint64_t)version | ((uint64_t)kChunk << 32)) &&
                         h[2] == J.n && h[3] == J.nchunks && h[4] == rM && h[5] == rR &&
                         h[6] == rP && h[7] == J.size && I.total == J.size &&
-                        (version == 1 || h[9] == 0);
+                        (version == 1 || (h[9] & ~(uint64_t)kFlagOverwrite) == 0);
         if (!ok) st = BD_ERR_FORMAT;
         // a payload bound to a base version is applied incrementally to that version only
         else if (version >= 2 && J.d_ck_old && h[8] != *J.d_ck_old) st = BD_ERR_BASE;

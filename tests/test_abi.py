@@ -151,7 +151,24 @@ def test_payload_info_parses_version_3_headers(cuda_lib):
     p2, _ = oracle.encode(old, new, base=base)
     h2 = (ctypes.c_uint8 * 80).from_buffer_copy(p2[:80].tobytes())
     assert cuda_lib.bd_payload_info(h2, 80, ctypes.byref(info)) == 0
-    assert info.version == 2 and info.n_escapes == 0
+    assert info.version == 2 and info.n_escapes == 0 and info.flags == 0
+
+
+def test_payload_info_reports_overwrite_flag(cuda_lib):
+    rng = np.random.default_rng(14)
+    old = rng.integers(0, 1 << 16, 6000).astype(np.uint16)
+    new = old.copy()
+    new[::25] ^= np.uint16(9)
+    info = _lib.PayloadInfo()
+    for compact in (False, True):
+        p, _ = oracle.encode(old, new, base=77, compact=compact, overwrite=True)
+        h = (ctypes.c_uint8 * 80).from_buffer_copy(p[:80].tobytes())
+        assert cuda_lib.bd_payload_info(h, 80, ctypes.byref(info)) == 0
+        assert info.flags == 1 and info.version == (3 if compact else 2)
+        bad = bytearray(p[:80].tobytes())
+        bad[72] = 3
+        b = (ctypes.c_uint8 * 80).from_buffer_copy(bytes(bad))
+        assert cuda_lib.bd_payload_info(b, 80, ctypes.byref(info)) == 3
 
 
 def test_version_3_bound(cuda_lib):
@@ -186,8 +203,8 @@ def test_argument_checks_need_no_gpu(cuda_lib):
     assert cuda_lib.bd_decompress(ctypes.c_void_p(1 << 20), 1000, ctypes.c_void_p(1 << 24),
                                   100, dummy, ctypes.c_void_p((1 << 20) + 16),
                                   ctypes.c_void_p(1 << 26), 1 << 20, dummy, None) == 1
-    # the versioned compress takes format 2 or 3 only
-    for fmt in (0, 1, 4):
+    # the versioned compress takes format 2 or 3 only, optionally with the overwrite bit
+    for fmt in (0, 1, 4, 0x102 | 0x200, 0x101, 0x104):
         assert cuda_lib.bd_compress_versioned(dummy, dummy, 10, ctypes.c_void_p(1 << 20), 100,
                                               ctypes.c_void_p(1 << 24), 1 << 20, dummy, dummy,
                                               dummy, fmt, None, None) == 1
