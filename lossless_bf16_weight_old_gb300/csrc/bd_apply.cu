@@ -509,6 +509,7 @@ __device__ __forceinline__ uint32_t mant_at(const uint8_t* __restrict__ mbytes, 
 // stream, rare values from the R stream (XOR payloads: a mantissa mask is nonzero, a rare mask
 // has a sign or exponent bit; an overwrite payload's values are unrestricted).  Returns
 // whether the chunk is malformed (the same on every lane).
+template <int PRE>
 __device__ __forceinline__ bool decode_compact(const uint8_t* __restrict__ blk,
                                                const uint16_t* __restrict__ xs, uint32_t E,
                                                const uint8_t* __restrict__ mbytes, uint32_t s0,
@@ -521,7 +522,63 @@ __device__ __forceinline__ bool decode_compact(const uint8_t* __restrict__ blk,
   const uint8_t* __restrict__ cls = blk + k;
   bool bad = false;
   uint32_t carry = 0xFFFFFFFFu, xr = 0, mr = 0, rr = 0;
-  for (uint32_t b0 = 0; b0 < k; b0 += 32) {
+  // the checks and the entry of change i, gap g (escaped values in place), class isR, value v
+  auto finish = [&](uint32_t i, bool in, uint32_t g, bool isR, uint32_t v) {
+    const uint32_t p = carry + warp_incl_scan(g);
+    carry = __shfl_sync(kFull, p, 31);
+    if (in) {
+      if (!ow && (isR ? (v & kSignExp) == 0 : v == 0)) bad = true;
+      if (p >= L) bad = true;
+      if (!bad) ent[i] = (isR ? kEntRare : 0u) | (p << 16) | v;
+    }
+  };
+  if constexpr (PRE > 0) {
+    // the first PRE batches: gap bytes and class bits requested together, then -- their ranks
+    // known from ballots -- every escaped gap and value, before the first is used
+    constexpr int NQ = PRE > 0 ? PRE : 1;   // (arrays of size 0 are not allowed)
+    uint32_t gq[NQ], cq[NQ], vq[NQ];
+#pragma unroll
+    for (int q = 0; q < PRE; q++) {
+      const uint32_t i = 32 * q + lane;
+      gq[q] = i < k ? (uint32_t)blk[i] : 0u;
+      cq[q] = i < k ? (uint32_t)(cls[i >> 3] >> (i & 7)) & 1u : 0u;
+    }
+#pragma unroll
+    for (int q = 0; q < PRE; q++) {
+      const uint32_t i = 32 * q + lane;
+      const bool in = i < k;
+      const bool esc = in && gq[q] == 0;
+      const bool isR = in && cq[q] != 0;
+      const uint32_t bE = __ballot_sync(kFull, esc), bR = __ballot_sync(kFull, isR),
+                     bM = __ballot_sync(kFull, in && !isR);
+      if (esc) {
+        const uint32_t xi = xr + __popc(bE & lt);
+        if (xi < E) gq[q] = xs[xi];   // stays 0 past E: flagged below
+        cq[q] |= 2u;
+      }
+      vq[q] = 0;
+      if (isR) {
+        const uint32_t r = rr + __popc(bR & lt);
+        if (r < R) vq[q] = rvals[r];
+        else cq[q] |= 4u;
+      } else if (in) {
+        const uint32_t m = mr + __popc(bM & lt);
+        if (m < M) vq[q] = mant_at(mbytes, s0, m);
+        else cq[q] |= 4u;
+      }
+      xr += __popc(bE);
+      rr += __popc(bR);
+      mr += __popc(bM);
+    }
+#pragma unroll
+    for (int q = 0; q < PRE; q++) {
+      if (32u * q >= k) break;
+      const uint32_t i = 32 * q + lane;
+      if (((cq[q] & 2u) && gq[q] <= 255) || (cq[q] & 4u)) bad = true;
+      finish(i, i < k, gq[q], (cq[q] & 1u) != 0, vq[q]);
+    }
+  }
+  for (uint32_t b0 = 32 * PRE; b0 < k; b0 += 32) {
     const uint32_t i = b0 + lane;
     const bool in = i < k;
     uint32_t g = in ? (uint32_t)blk[i] : 0u;
@@ -533,28 +590,21 @@ __device__ __forceinline__ bool decode_compact(const uint8_t* __restrict__ blk,
       if (g <= 255) bad = true;
     }
     xr += __popc(bE);
-    const uint32_t p = carry + warp_incl_scan(g);
-    carry = __shfl_sync(kFull, p, 31);
     const bool isR = in && ((cls[i >> 3] >> (i & 7)) & 1u);
     const uint32_t bR = __ballot_sync(kFull, isR), bM = __ballot_sync(kFull, in && !isR);
-    if (in) {
-      uint32_t v = 0;
-      if (isR) {
-        const uint32_t r = rr + __popc(bR & lt);
-        if (r < R) v = rvals[r];
-        else bad = true;
-        if (!ow && (v & kSignExp) == 0) bad = true;
-      } else {
-        const uint32_t m = mr + __popc(bM & lt);
-        if (m < M) v = mant_at(mbytes, s0, m);
-        else bad = true;
-        if (!ow && v == 0) bad = true;
-      }
-      if (p >= L) bad = true;
-      if (!bad) ent[i] = (isR ? kEntRare : 0u) | (p << 16) | v;
+    uint32_t v = 0;
+    if (isR) {
+      const uint32_t r = rr + __popc(bR & lt);
+      if (r < R) v = rvals[r];
+      else bad = true;
+    } else if (in) {
+      const uint32_t m = mr + __popc(bM & lt);
+      if (m < M) v = mant_at(mbytes, s0, m);
+      else bad = true;
     }
     mr += __popc(bM);
     rr += __popc(bR);
+    finish(i, in, g, isR, v);
   }
   if (xr != E || rr != R) bad = true;
   if (lane == 0 && (k & 7) != 0 && (cls[(k - 1) >> 3] >> (k & 7)) != 0) bad = true;
@@ -659,25 +709,42 @@ k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
       const bool ow = V3 && (I.flags & kFlagOverwrite) != 0;
       bool bad = false;
       if (V3 && cc.compact) {
-        bad = decode_compact(mlist,
+        bad = decode_compact<4>(mlist,
                              reinterpret_cast<const uint16_t*>(payload + I.x_start) + pre.e + lc.w,
                              cc.E, mbytes, s0, rvals, M, R, L, ow, ent);
       } else {
         if (both) s_bits[w][lane] = make_uint4(0, 0, 0, 0);
+        // the payload of the first 128 mantissa-only and 32 rare changes, all requested before
+        // the first is used (one round trip for most chunks instead of one per 32 changes:
+        // -3% on the dense apply; in apply_incr, at 64 registers, the same spilled and was
+        // much slower)
+        uint32_t pd[4], pv[4];
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+          const uint32_t i = 32 * q + lane;
+          pd[q] = 0;
+          pv[q] = 0;
+          if (i < M) {
+            pd[q] = list_entry<V3>(mlist, i);
+            const uint32_t bit = s0 + 7 * i;
+            pv[q] = mbytes[bit >> 3];
+            if ((bit & 7) > 1) pv[q] |= (uint32_t)mbytes[(bit >> 3) + 1] << 8;
+          }
+        }
+        uint32_t rd0 = 0, rv0 = 0;
+        if ((uint32_t)lane < R) {
+          rd0 = list_entry<V3>(rlist, lane);
+          rv0 = rvals[lane];
+        }
         __syncwarp();
         uint32_t carry = 0;
-        for (uint32_t b0 = 0; b0 < M; b0 += 32) {
-          const uint32_t i = b0 + lane;
+        auto m_batch = [&](uint32_t i, uint32_t d, uint32_t raw) {
           const bool in = i < M;
-          const uint32_t d = in ? list_entry<V3>(mlist, i) : 0u;
           if (in && i > 0 && d == 0) bad = true;
           const uint32_t p = carry + warp_incl_scan(d);
           carry = __shfl_sync(kFull, p, 31);
           if (in) {
-            const uint32_t bit = s0 + 7 * i, sh = bit & 7;
-            uint32_t v = (uint32_t)mbytes[bit >> 3] >> sh;
-            if (sh > 1) v |= (uint32_t)mbytes[(bit >> 3) + 1] << (8 - sh);
-            v &= kMant;
+            const uint32_t v = (raw >> ((s0 + 7 * i) & 7)) & kMant;
             if (p >= L || (!ow && v == 0)) {
               bad = true;
             } else {
@@ -685,18 +752,37 @@ k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
               if (both) atomicOr(&bits[p >> 5], 1u << (p & 31));
             }
           }
+        };
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+          if (32u * q >= M) break;
+          m_batch(32 * q + lane, pd[q], pv[q]);
+        }
+        for (uint32_t b0 = 128; b0 < M; b0 += 32) {
+          const uint32_t i = b0 + lane;
+          uint32_t d = 0, raw = 0;
+          if (i < M) {
+            d = list_entry<V3>(mlist, i);
+            const uint32_t bit = s0 + 7 * i;
+            raw = mbytes[bit >> 3];
+            if ((bit & 7) > 1) raw |= (uint32_t)mbytes[(bit >> 3) + 1] << 8;
+          }
+          m_batch(i, d, raw);
         }
         __syncwarp();
         carry = 0;
         for (uint32_t b0 = 0; b0 < R; b0 += 32) {
           const uint32_t i = b0 + lane;
           const bool in = i < R;
-          const uint32_t d = in ? list_entry<V3>(rlist, i) : 0u;
+          uint32_t d = rd0, v = rv0;
+          if (b0 > 0) {
+            d = in ? list_entry<V3>(rlist, i) : 0u;
+            v = in ? (uint32_t)rvals[i] : 0u;
+          }
           if (in && i > 0 && d == 0) bad = true;
           const uint32_t p = carry + warp_incl_scan(d);
           carry = __shfl_sync(kFull, p, 31);
           if (in) {
-            const uint32_t v = rvals[i];
             if (p >= L || (!ow && (v & kSignExp) == 0)) bad = true;
             else if (both && ((bits[p >> 5] >> (p & 31)) & 1u)) bad = true;
             else ent[M + i] = (V3 ? kEntRare : 0u) | (p << 16) | v;
@@ -797,7 +883,7 @@ k_apply_incr(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
     const bool ow = OW && (I.flags & kFlagOverwrite) != 0;
     bool bad = false;
     if (V3 && cc.compact) {
-      bad = decode_compact(mlist,
+      bad = decode_compact<0>(mlist,
                            reinterpret_cast<const uint16_t*>(payload + I.x_start) + pre.e + lc.w,
                            cc.E, mbytes, s0, rvals, M, R, L, ow, ent);
     } else {

@@ -507,6 +507,9 @@ k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
     j = advance_job(chunk_start, k, j, g);
     // level 1: everything addressed by g and j alone, requested together
     const uint8_t* slot = slots + g * kSlotBytes;
+    // the next chunk's slot header and first 96 entries into L2 while this one is emitted
+    if (g + 1 < g_end && lane < 4)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(slot + kSlotBytes + 128 * lane));
     const uint32_t* E = reinterpret_cast<const uint32_t*>(slot + kSlotHeader);
     const uint32_t hdr = *reinterpret_cast<const uint32_t*>(slot);
     uint32_t ent[8];
