@@ -216,3 +216,34 @@ def test_compact_on_bf16_workload_tensor():
     torch.cuda.synchronize()
     assert int(st.item()) == bd.OK and int(size.item()) == ref.size
     assert np.array_equal(payload[:ref.size].cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("overwrite", [False, True])
+def test_full_size_1gib_and_sweep_workloads(overwrite):
+    """The 1 GiB N(0,1) tensor (about 22% changed: bitmap chunks, version-1 chunks among compact
+    ones, chunks of 253..508 changes) and the 14336x4096 tensor at every rate of the sweep, in
+    version 3 (XOR and overwrite): bytes identical to the oracle's, and every apply restores."""
+    specs = W.dense1g() + W.sweep14336()
+    for spec in specs:
+        old, new = W.make_pair(spec, device="cuda")
+        old, new = old.reshape(-1), new.reshape(-1)
+        o, nw = to_np_u16(old), to_np_u16(new)
+        base = oracle.checksum(o)
+        ref, ck_ref = oracle.encode(o, nw, base=base, compact=True, overwrite=overwrite)
+        payload, size, ck, st = bd.compress(old, new, base_checksum=base, compact=True,
+                                            overwrite=overwrite)
+        torch.cuda.synchronize()
+        assert int(st.item()) == bd.OK, spec.name
+        size = int(size.item())
+        assert size == ref.size and bd.u64(ck)[0] == ck_ref, spec.name
+        assert np.array_equal(payload[:size].cpu().numpy(), ref), spec.name
+        w = old.clone()
+        st2 = bd.decompress(w, payload, size, ck, out=w)
+        w2 = old.clone()
+        st3, ck3 = bd.decompress_incremental(w2, payload, size, base, ck)
+        torch.cuda.synchronize()
+        assert int(st2.item()) == bd.OK and int(st3.item()) == bd.OK, spec.name
+        assert bd.u64(ck3)[0] == ck_ref, spec.name
+        assert torch.equal(w.view(torch.int16), new.view(torch.int16)), spec.name
+        assert torch.equal(w2.view(torch.int16), new.view(torch.int16)), spec.name
+        del old, new, w, w2, payload

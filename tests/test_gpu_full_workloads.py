@@ -121,6 +121,8 @@ def _check_workload(specs, sample, compact=False):
         torch.cuda.synchronize()
         assert all(int(s) == bd.ERR_BASE for s in refused.statuses.tolist())
         assert torch.equal(R.view(torch.int16), N.view(torch.int16))
+        comp.workspace = None   # (the forward compress is done: room for the reverse one)
+        torch.cuda.empty_cache()
         rev = bd.CompressBatch(news, olds, sizes, base_checksums=comp.checksums, compact=True)
         rev.run()
         torch.cuda.synchronize()
@@ -149,6 +151,16 @@ def test_dense7b_full_size_compact():
     names = {s.name: i for i, s in enumerate(specs)}
     sample = [names[x] for x in ("embed", "layers.0.q", "layers.0.down", "layers.0.norm1",
                                  "norm", "lm_head")]
+    _check_workload(specs, sample, compact=True)
+
+
+def test_moe30b_full_size_compact():
+    """The MoE checkpoint in version 3: hot experts with dense chunks (version-1 bitmaps and
+    compact chunks of 253..508 changes through the dense emit) beside sparse cold experts."""
+    specs = W.moe30b()
+    names = {s.name: i for i, s in enumerate(specs)}
+    hot = max(range(len(specs)), key=lambda i: specs[i].rate)
+    sample = [names["embed"], hot, names["layers.0.q"], names["lm_head"]]
     _check_workload(specs, sample, compact=True)
 
 
