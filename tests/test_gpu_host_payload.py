@@ -78,3 +78,32 @@ def test_batched_apply_from_host_payloads():
     assert int(b.status.item()) == bd.OK
     for o, nw in zip(outs, news):
         assert torch.equal(o.view(torch.int16), nw.view(torch.int16))
+
+
+@pytest.mark.parametrize("overwrite", [False, True])
+def test_version_3_payloads_from_host_memory(overwrite):
+    """Version-3 payloads (XOR and overwrite) read from mapped host memory by the full, the
+    incremental and the no-workspace apply: the oracle's result in every case."""
+    old, new = W.make_pair(W.Spec("h3", (4096 * 90 + 321,), rate=0.04, tid=13), device="cuda")
+    old, new = old.reshape(-1), new.reshape(-1)
+    o, nw = to_np_u16(old), to_np_u16(new)
+    base = oracle.checksum(o)
+    ref, ck = oracle.encode(o, nw, base=base, compact=True, overwrite=overwrite)
+    buf = bd.MappedHostBuffer(ref.size)
+    buf.numpy()[:] = ref
+    out = torch.empty_like(old)
+    st = bd.decompress(old, buf.device_ptr, ref.size, ck, out=out)
+    w = old.clone()
+    st2, ck2 = bd.decompress_incremental(w, buf.device_ptr, ref.size, base, ck)
+    lib = bd._lib.load()
+    out3 = torch.empty_like(old)
+    st3 = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    ckt = bd._u64_tensor([ck], "cuda")
+    assert lib.bd_decompress_noalloc(old.data_ptr(), old.numel(), buf.device_ptr, ref.size,
+                                     ckt.data_ptr(), out3.data_ptr(), st3.data_ptr(),
+                                     torch.cuda.current_stream().cuda_stream) == bd.OK
+    torch.cuda.synchronize()
+    assert int(st.item()) == int(st2.item()) == int(st3.item()) == bd.OK
+    assert bd.u64(ck2)[0] == ck
+    for r in (out, w, out3):
+        assert torch.equal(r.view(torch.int16), new.view(torch.int16))
