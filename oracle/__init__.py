@@ -53,6 +53,9 @@ def _load():
             fn = getattr(lib, name)
             fn.argtypes = [p, p, u64, u64, p, u64, ctypes.POINTER(u64), ctypes.POINTER(u64)]
             fn.restype = ctypes.c_int
+        lib.orc_encode_rice.argtypes = [p, p, u64, u64, ctypes.c_int, p, u64,
+                                        ctypes.POINTER(u64), ctypes.POINTER(u64)]
+        lib.orc_encode_rice.restype = ctypes.c_int
         lib.orc_decode.argtypes = [p, u64, p, u64, u64, p]
         lib.orc_decode.restype = ctypes.c_int
         lib.orc_decode_incremental.argtypes = [p, u64, p, u64, u64, u64, p,
@@ -76,19 +79,28 @@ def checksum(w) -> int:
 
 
 def encode(old, new, base: int | None = None, compact: bool = False,
-           overwrite: bool = False) -> tuple[np.ndarray, int]:
+           overwrite: bool = False, rice: bool = False) -> tuple[np.ndarray, int]:
     """Returns (payload bytes as a uint8 array, checksum of new).  With `base` (the checksum of
     old as the caller knows it) the payload is version 2, bound to that base; with compact=True
-    (which needs a base) it is version 3, with compact position lists; with overwrite=True
-    (which needs a base) its streams hold new values instead of XOR masks."""
+    (which needs a base) it is version 3, with compact position lists; with rice=True (which
+    needs a base, and excludes compact) it is version 4, with Rice-coded compact position
+    blocks; with overwrite=True (which needs a base) its streams hold new values instead of XOR
+    masks."""
     old, new = _u16(old), _u16(new)
     if old.size != new.size:
         raise ValueError("old and new must have the same number of elements")
     lib = _load()
     size, ck = ctypes.c_uint64(), ctypes.c_uint64()
-    if (compact or overwrite) and base is None:
-        raise ValueError("compact and overwrite payloads are bound to a base: give base")
-    if base is None:
+    if (compact or overwrite or rice) and base is None:
+        raise ValueError("compact, Rice and overwrite payloads are bound to a base: give base")
+    if compact and rice:
+        raise ValueError("compact (version 3) and rice (version 4) exclude each other")
+    if rice:
+        b = ctypes.c_uint64(int(base) & (2**64 - 1))
+        call = lambda out, cap: lib.orc_encode_rice(old.ctypes.data, new.ctypes.data, old.size, b,
+                                                    int(bool(overwrite)), out, cap,
+                                                    ctypes.byref(size), ctypes.byref(ck))
+    elif base is None:
         call = lambda out, cap: lib.orc_encode(old.ctypes.data, new.ctypes.data, old.size, out,
                                                cap, ctypes.byref(size), ctypes.byref(ck))
     else:

@@ -46,6 +46,16 @@
  * then ceil(k/8) class bytes (bit i, LSB-first, is 1 when change i is rare; pad bits 0).  The
  * encoder makes a chunk compact when k <= 508 and k + ceil(k/8) + 2E is smaller than its
  * version-1 blocks; decoders accept either coding of a chunk.
+ * Version 4 (a Golomb-Rice code of the same gaps, the second stand-in for the entropy stage):
+ * the version-3 layout without the X stream.  Compact count entry: bit 31 set, M in bits
+ * 0..8, R in bits 9..17, the Rice parameter K in bits 18..20 and the block's bytes B in bits
+ * 21..30 (M + R between 1 and 508, B at least 1); plain entries as in version 3.  A compact
+ * block is a bit stream, LSB-first from its first byte: the R indices (within the merged
+ * list, ascending, 9 bits each) of the rare changes; then for each gap g_i its remainder
+ * g_i mod 2^K (K bits); then for each gap its quotient g_i >> K in unary (that many 1 bits,
+ * then a 0); then zero pad bits up to B = ceil(bits / 8).  The encoder takes the K in 0..7
+ * giving the fewest bits (the smallest such K) and makes a chunk compact when k <= 508 and B
+ * is smaller than its version-1 blocks.
  */
 #include "bd_oracle.h"
 
@@ -476,6 +486,191 @@ int orc_encode_compact_overwrite(const uint16_t* old, const uint16_t* neu, uint6
   return compact_impl(old, neu, n, base, 1, out, cap, size_out, checksum_out);
 }
 
+/* ---- version 4: Rice-coded positions --------------------------------------------------- */
+
+#define ORC_RICE_IDX_BITS 9u   /* bits of a rare change's index in its chunk's merged list */
+
+/* Changes of chunk c (length L) in ascending position: pos[i] and rare[i] (1: rare). */
+static uint64_t chunk_changes(const uint16_t* old, const uint16_t* neu, uint64_t c, uint64_t L,
+                              uint16_t* pos, uint8_t* rare) {
+  uint64_t k = 0;
+  for (uint64_t p = 0; p < L; p++) {
+    uint64_t i = c * ORC_CHUNK + p;
+    int cls = classify((uint16_t)(old[i] ^ neu[i]));
+    if (cls == CLASS_ZERO) continue;
+    pos[k] = (uint16_t)p;
+    rare[k] = cls == CLASS_RARE;
+    k++;
+  }
+  return k;
+}
+
+/* Bits of a Rice-coded block: R rare indices, k remainders of K bits, and for each gap its
+ * quotient (gap >> K) in unary, ones then a zero.  Gaps: pos[0] + 1, then pos[i] - pos[i-1]. */
+static uint64_t rice_bits(const uint16_t* pos, uint64_t k, uint64_t R, unsigned K) {
+  uint64_t bits = ORC_RICE_IDX_BITS * R + k * K + k;
+  int64_t prev = -1;
+  for (uint64_t i = 0; i < k; i++) {
+    bits += (uint64_t)((int64_t)pos[i] - prev) >> K;
+    prev = pos[i];
+  }
+  return bits;
+}
+
+/* The encoder's Rice parameter: the K in 0..7 giving the fewest bits, the smallest on a tie. */
+static unsigned rice_param(const uint16_t* pos, uint64_t k, uint64_t R) {
+  unsigned best = 0;
+  for (unsigned K = 1; K < 8; K++)
+    if (rice_bits(pos, k, R, K) < rice_bits(pos, k, R, best)) best = K;
+  return best;
+}
+
+static void put_bits(uint8_t* blk, uint64_t bit, uint32_t v, unsigned nbits) {
+  for (unsigned b = 0; b < nbits; b++)
+    if ((v >> b) & 1) blk[(bit + b) / 8] |= (uint8_t)(1u << ((bit + b) % 8));
+}
+static uint32_t get_bits(const uint8_t* blk, uint64_t bit, unsigned nbits) {
+  uint32_t v = 0;
+  for (unsigned b = 0; b < nbits; b++) v |= (uint32_t)((blk[(bit + b) / 8] >> ((bit + b) % 8)) & 1) << b;
+  return v;
+}
+
+/* Writes the block of k changes (R of them rare) with parameter K at blk (zeroed): the rare
+ * indices, ascending, 9 bits each; then the remainders gap mod 2^K, K bits each; then the
+ * quotients in unary. */
+static void write_rice(uint8_t* blk, const uint16_t* pos, const uint8_t* rare, uint64_t k,
+                       uint64_t R, unsigned K) {
+  uint64_t j = 0;
+  for (uint64_t i = 0; i < k; i++)
+    if (rare[i]) put_bits(blk, ORC_RICE_IDX_BITS * j++, (uint32_t)i, ORC_RICE_IDX_BITS);
+  uint64_t u = ORC_RICE_IDX_BITS * R + k * K;
+  int64_t prev = -1;
+  for (uint64_t i = 0; i < k; i++) {
+    uint64_t g = (uint64_t)((int64_t)pos[i] - prev);
+    put_bits(blk, ORC_RICE_IDX_BITS * R + K * i, (uint32_t)(g & ((1u << K) - 1)), K);
+    for (uint64_t q = g >> K; q > 0; q--) put_bits(blk, u++, 1, 1);
+    u++;   /* the zero that ends the quotient */
+    prev = pos[i];
+  }
+}
+
+static int rice_impl(const uint16_t* old, const uint16_t* neu, uint64_t n, uint64_t base,
+                     int overwrite, uint8_t* out, uint64_t cap, uint64_t* size_out,
+                     uint64_t* checksum_out) {
+  if ((n > 0 && (old == NULL || neu == NULL)) || size_out == NULL || checksum_out == NULL)
+    return ORC_ERR_ARG;
+  uint64_t C = (n + ORC_CHUNK - 1) / ORC_CHUNK;
+
+  /* XOR and classify per chunk; a chunk is compact when its Rice block is smaller than its
+   * two version-1 blocks. */
+  uint64_t* mcount = (uint64_t*)calloc(C ? C : 1, sizeof(uint64_t));
+  uint64_t* rcount = (uint64_t*)calloc(C ? C : 1, sizeof(uint64_t));
+  uint32_t* kparam = (uint32_t*)calloc(C ? C : 1, sizeof(uint32_t));
+  uint32_t* bbytes = (uint32_t*)calloc(C ? C : 1, sizeof(uint32_t));
+  uint16_t* pos = (uint16_t*)malloc(ORC_CHUNK * sizeof(uint16_t));
+  uint8_t* rare = (uint8_t*)malloc(ORC_CHUNK);
+  if (!mcount || !rcount || !kparam || !bbytes || !pos || !rare) {
+    free(mcount); free(rcount); free(kparam); free(bbytes); free(pos); free(rare);
+    return ORC_ERR_ARG;
+  }
+  uint64_t sum_m = 0, sum_r = 0, pos_bytes = 0;
+  for (uint64_t c = 0; c < C; c++) {
+    uint64_t L = chunk_len(n, c);
+    uint64_t k = chunk_changes(old, neu, c, L, pos, rare);
+    uint64_t R = 0;
+    for (uint64_t i = 0; i < k; i++) R += rare[i];
+    mcount[c] = k - R;
+    rcount[c] = R;
+    uint64_t plain = block_bytes(k - R, L) + block_bytes(R, L);
+    if (k > 0 && k <= ORC_COMPACT_MAX) {
+      unsigned K = rice_param(pos, k, R);
+      uint64_t B = (rice_bits(pos, k, R, K) + 7) / 8;
+      if (B < plain) {
+        kparam[c] = K;
+        bbytes[c] = (uint32_t)B;
+      }
+    }
+    sum_m += mcount[c];
+    sum_r += rcount[c];
+    pos_bytes += bbytes[c] ? bbytes[c] : plain;
+  }
+  uint64_t m_bytes = (7 * sum_m + 7) / 8;
+  uint64_t size = ORC_HEADER_V2 + 4 * C + 2 * sum_r + pos_bytes + m_bytes;
+  *size_out = size;
+  *checksum_out = orc_checksum(neu, n);
+  if (out == NULL || cap < size) {
+    free(mcount); free(rcount); free(kparam); free(bbytes); free(pos); free(rare);
+    return ORC_ERR_CAPACITY;
+  }
+
+  memset(out, 0, size);
+  memcpy(out, "BF16DLT1", 8);
+  put_u32(out + 8, 4);
+  put_u32(out + 12, ORC_CHUNK);
+  put_u64(out + 16, n);
+  put_u64(out + 24, C);
+  put_u64(out + 32, sum_m);
+  put_u64(out + 40, sum_r);
+  put_u64(out + 48, pos_bytes);
+  put_u64(out + 56, size);
+  put_u64(out + 64, base);
+  put_u64(out + 72, overwrite ? ORC_FLAG_OVERWRITE : 0);
+  for (uint64_t c = 0; c < C; c++) {
+    uint32_t v = bbytes[c] ? ORC_COMPACT_FLAG | (uint32_t)mcount[c] | ((uint32_t)rcount[c] << 9) |
+                                 (kparam[c] << 18) | (bbytes[c] << 21)
+                           : (uint32_t)mcount[c] | ((uint32_t)rcount[c] << 15);
+    put_u32(out + ORC_HEADER_V2 + 4 * c, v);
+  }
+  uint64_t r_off = ORC_HEADER_V2 + 4 * C;
+  uint64_t p_off = r_off + 2 * sum_r;
+  uint64_t m_off = p_off + pos_bytes;
+
+  /* R stream: every rare change's XOR (overwrite: its new value), in position order. */
+  for (uint64_t i = 0; i < n; i++) {
+    uint16_t x = (uint16_t)(old[i] ^ neu[i]);
+    if (classify(x) == CLASS_RARE) { put_u16(out + r_off, overwrite ? neu[i] : x); r_off += 2; }
+  }
+  /* Position blocks, chunk by chunk. */
+  uint16_t* mpos = (uint16_t*)malloc(ORC_CHUNK * sizeof(uint16_t));
+  uint16_t* rpos = (uint16_t*)malloc(ORC_CHUNK * sizeof(uint16_t));
+  for (uint64_t c = 0; c < C; c++) {
+    uint64_t L = chunk_len(n, c);
+    uint64_t k = chunk_changes(old, neu, c, L, pos, rare);
+    if (bbytes[c]) {
+      write_rice(out + p_off, pos, rare, k, rcount[c], kparam[c]);
+      p_off += bbytes[c];
+    } else {
+      uint64_t km = 0, kr = 0;
+      for (uint64_t i = 0; i < k; i++) {
+        if (rare[i]) rpos[kr++] = pos[i];
+        else mpos[km++] = pos[i];
+      }
+      write_block(out + p_off, mpos, km, L);
+      p_off += block_bytes(km, L);
+      write_block(out + p_off, rpos, kr, L);
+      p_off += block_bytes(kr, L);
+    }
+  }
+  free(mpos);
+  free(rpos);
+  /* M stream: as in version 1 (overwrite: the new mantissas). */
+  uint64_t j = 0;
+  for (uint64_t i = 0; i < n; i++) {
+    uint16_t x = (uint16_t)(old[i] ^ neu[i]);
+    if (classify(x) != CLASS_MANT) continue;
+    put_bits(out + m_off, 7 * j, (uint32_t)((overwrite ? neu[i] : x) & ORC_MANT_BITS), 7);
+    j++;
+  }
+  free(mcount); free(rcount); free(kparam); free(bbytes); free(pos); free(rare);
+  return ORC_OK;
+}
+
+int orc_encode_rice(const uint16_t* old, const uint16_t* neu, uint64_t n, uint64_t base,
+                    int overwrite, uint8_t* out, uint64_t cap, uint64_t* size_out,
+                    uint64_t* checksum_out) {
+  return rice_impl(old, neu, n, base, overwrite != 0, out, cap, size_out, checksum_out);
+}
+
 /* Splits a version-3 count entry; returns -1 when its unused bits are not zero. */
 static int v3_entry(uint32_t v, uint64_t* km, uint64_t* kr, uint64_t* ke, int* is_compact) {
   *is_compact = (v & ORC_COMPACT_FLAG) != 0;
@@ -518,10 +713,72 @@ static uint16_t mant_at(const uint8_t* m, uint64_t j) {
   return v;
 }
 
-/* Decodes a version-3 payload (header fields n, C, version and flags already checked,
- * size >= 80) into out; the base is checked against required_base as in decode_into. */
-static int decode_v3(const uint16_t* old, uint64_t n, const uint8_t* payload, uint64_t size,
-                     uint16_t* out, const uint64_t* required_base, int overwrite) {
+/* Splits a version-4 count entry: a compact entry gives M, R, the Rice parameter K and the
+ * block's bytes B; a plain entry M and R as in version 3.  Returns -1 on a malformed entry. */
+static int v4_entry(uint32_t v, uint64_t* km, uint64_t* kr, unsigned* K, uint64_t* B,
+                    int* is_compact) {
+  *is_compact = (v & ORC_COMPACT_FLAG) != 0;
+  *K = 0;
+  *B = 0;
+  if (*is_compact) {
+    *km = v & 0x1FF;
+    *kr = (v >> 9) & 0x1FF;
+    *K = (v >> 18) & 0x7;
+    *B = (v >> 21) & 0x3FF;
+    if (*km + *kr == 0 || *km + *kr > ORC_COMPACT_MAX || *B == 0) return -1;
+  } else {
+    if (v & 0x40000000u) return -1;
+    *km = v & 0x7FFF;
+    *kr = (v >> 15) & 0x7FFF;
+  }
+  return 0;
+}
+
+/* Reads the B-byte Rice block of a compact version-4 chunk of length L with k changes, R of
+ * them rare, parameter K: the merged list's positions into pos[0..k) and classes into
+ * rare[0..k).  Returns 0 when the block is the canonical coding of such a list: rare indices
+ * strictly ascending and below k; every gap (quotient << K | remainder) at least 1 and every
+ * position below L; the k-th unary zero inside the block; B = ceil(bits used / 8), the pad
+ * bits after them zero.  Otherwise -1. */
+static int read_rice(const uint8_t* blk, uint64_t B, uint64_t k, uint64_t R, unsigned K,
+                     uint64_t L, uint16_t* pos, uint8_t* rare) {
+  uint64_t fixed = ORC_RICE_IDX_BITS * R + k * K;
+  if (fixed > 8 * B) return -1;
+  memset(rare, 0, k);
+  for (uint64_t j = 0; j < R; j++) {
+    uint64_t idx = get_bits(blk, ORC_RICE_IDX_BITS * j, ORC_RICE_IDX_BITS);
+    uint64_t prev = j == 0 ? 0 : get_bits(blk, ORC_RICE_IDX_BITS * (j - 1), ORC_RICE_IDX_BITS);
+    if (idx >= k || (j > 0 && idx <= prev)) return -1;
+    rare[idx] = 1;
+  }
+  uint64_t u = fixed, p = 0;
+  for (uint64_t i = 0; i < k; i++) {
+    uint64_t q = 0;
+    for (;;) {
+      if (u >= 8 * B) return -1;           /* the quotient runs past the block */
+      uint32_t bit = get_bits(blk, u++, 1);
+      if (bit == 0) break;
+      q++;
+    }
+    uint64_t g = (q << K) | get_bits(blk, ORC_RICE_IDX_BITS * R + K * i, K);
+    if (g == 0) return -1;
+    p = i == 0 ? g - 1 : p + g;
+    if (p >= L) return -1;
+    pos[i] = (uint16_t)p;
+  }
+  if ((u + 7) / 8 != B) return -1;
+  for (uint64_t bit = u; bit < 8 * B; bit++)
+    if (get_bits(blk, bit, 1)) return -1;
+  return 0;
+}
+
+/* Decodes a version-3 or version-4 payload (header fields n, C, version and flags already
+ * checked, size >= 80) into out; the base is checked against required_base as in
+ * decode_into.  The two versions differ in the count entry of a compact chunk, the X stream
+ * (version 3 only) and the coding of a compact chunk's merged list. */
+static int decode_v3_v4(const uint16_t* old, uint64_t n, const uint8_t* payload, uint64_t size,
+                     uint16_t* out, const uint64_t* required_base, int overwrite,
+                     uint32_t version) {
   uint64_t C = (n + ORC_CHUNK - 1) / ORC_CHUNK;
   uint64_t hdr_m = get_u64(payload + 32), hdr_r = get_u64(payload + 40);
   uint64_t hdr_pos = get_u64(payload + 48), hdr_size = get_u64(payload + 56);
@@ -529,15 +786,18 @@ static int decode_v3(const uint16_t* old, uint64_t n, const uint8_t* payload, ui
   if ((size - ORC_HEADER_V2) / 4 < C) return ORC_ERR_FORMAT;
   uint64_t sum_m = 0, sum_r = 0, sum_e = 0, pos_bytes = 0;
   for (uint64_t c = 0; c < C; c++) {
-    uint64_t L = chunk_len(n, c), km, kr, ke;
+    uint64_t L = chunk_len(n, c), km, kr, ke = 0, B = 0;
+    unsigned K;
     int cmp;
-    if (v3_entry(get_u32(payload + ORC_HEADER_V2 + 4 * c), &km, &kr, &ke, &cmp) != 0)
+    uint32_t v = get_u32(payload + ORC_HEADER_V2 + 4 * c);
+    if (version == 3 ? v3_entry(v, &km, &kr, &ke, &cmp) : v4_entry(v, &km, &kr, &K, &B, &cmp))
       return ORC_ERR_FORMAT;
     if (km + kr > L) return ORC_ERR_FORMAT;
     sum_m += km;
     sum_r += kr;
     sum_e += ke;
-    pos_bytes += cmp ? km + kr + (km + kr + 7) / 8 : block_bytes(km, L) + block_bytes(kr, L);
+    if (!cmp) pos_bytes += block_bytes(km, L) + block_bytes(kr, L);
+    else pos_bytes += version == 3 ? km + kr + (km + kr + 7) / 8 : B;
   }
   if (sum_m != hdr_m || sum_r != hdr_r || pos_bytes != hdr_pos) return ORC_ERR_FORMAT;
   uint64_t m_bytes = (7 * sum_m + 7) / 8;
@@ -552,15 +812,29 @@ static int decode_v3(const uint16_t* old, uint64_t n, const uint8_t* payload, ui
   if (n > 0) memcpy(out, old, n * sizeof(uint16_t));
   uint16_t* mpos = (uint16_t*)malloc(ORC_CHUNK * sizeof(uint16_t));
   uint16_t* rpos = (uint16_t*)malloc(ORC_CHUNK * sizeof(uint16_t));
+  uint16_t* kpos = (uint16_t*)malloc(ORC_COMPACT_MAX * sizeof(uint16_t));
+  uint8_t* krare = (uint8_t*)malloc(ORC_COMPACT_MAX);
   uint64_t mj = 0, rj = 0, xj = 0;
   int status = ORC_OK;
   for (uint64_t c = 0; c < C && status == ORC_OK; c++) {
-    uint64_t L = chunk_len(n, c), km, kr, ke;
+    uint64_t L = chunk_len(n, c), km, kr, ke = 0, B = 0;
+    unsigned K = 0;
     int cmp;
-    v3_entry(get_u32(payload + ORC_HEADER_V2 + 4 * c), &km, &kr, &ke, &cmp);
+    uint32_t v = get_u32(payload + ORC_HEADER_V2 + 4 * c);
+    if (version == 3) v3_entry(v, &km, &kr, &ke, &cmp);
+    else v4_entry(v, &km, &kr, &K, &B, &cmp);
     const uint8_t* blk = payload + p_off;
     uint64_t nm = 0, nr = 0;
-    if (cmp) {
+    if (cmp && version == 4) {
+      /* the merged list from the Rice block, split by class */
+      if (read_rice(blk, B, km + kr, kr, K, L, kpos, krare) != 0) { status = ORC_ERR_FORMAT; break; }
+      for (uint64_t i = 0; i < km + kr; i++) {
+        if (krare[i]) rpos[nr++] = kpos[i];
+        else mpos[nm++] = kpos[i];
+      }
+      if (nm != km) { status = ORC_ERR_FORMAT; break; }   /* cannot differ: R indices distinct */
+      p_off += B;
+    } else if (cmp) {
       /* the merged list: positions from the gaps, classes from the class bits */
       uint64_t k = km + kr, p = 0, esc = 0;
       for (uint64_t i = 0; i < k && status == ORC_OK; i++) {
@@ -616,6 +890,8 @@ static int decode_v3(const uint16_t* old, uint64_t n, const uint8_t* payload, ui
   }
   free(mpos);
   free(rpos);
+  free(kpos);
+  free(krare);
   if (status != ORC_OK) return status;
   for (uint64_t bit = 7 * sum_m; bit < 8 * m_bytes; bit++)
     if ((payload[m_off + bit / 8] >> (bit % 8)) & 1) return ORC_ERR_FORMAT;
@@ -634,7 +910,7 @@ static int decode_into(const uint16_t* old, uint64_t n, const uint8_t* payload, 
   if (size < ORC_HEADER) return ORC_ERR_FORMAT;
   if (memcmp(payload, "BF16DLT1", 8) != 0) return ORC_ERR_FORMAT;
   uint32_t version = get_u32(payload + 8);
-  if (version != 1 && version != 2 && version != 3) return ORC_ERR_FORMAT;
+  if (version < 1 || version > 4) return ORC_ERR_FORMAT;
   const uint64_t hdr = version >= 2 ? ORC_HEADER_V2 : ORC_HEADER;
   if (size < hdr) return ORC_ERR_FORMAT;
   const uint64_t flags = version >= 2 ? get_u64(payload + 72) : 0;
@@ -644,7 +920,8 @@ static int decode_into(const uint16_t* old, uint64_t n, const uint8_t* payload, 
   uint64_t C = (n + ORC_CHUNK - 1) / ORC_CHUNK;
   if (get_u64(payload + 16) != n) return ORC_ERR_FORMAT;
   if (get_u64(payload + 24) != C) return ORC_ERR_FORMAT;
-  if (version == 3) return decode_v3(old, n, payload, size, out, required_base, overwrite);
+  if (version >= 3)
+    return decode_v3_v4(old, n, payload, size, out, required_base, overwrite, version);
   uint64_t hdr_m = get_u64(payload + 32), hdr_r = get_u64(payload + 40);
   uint64_t hdr_pos = get_u64(payload + 48), hdr_size = get_u64(payload + 56);
   if (hdr_size != size) return ORC_ERR_FORMAT;

@@ -66,7 +66,13 @@ int orc_encode_compact_overwrite(const uint16_t* old, const uint16_t* neu, uint6
                                  uint64_t base, uint8_t* out, uint64_t cap, uint64_t* size_out,
                                  uint64_t* checksum_out);
 
-/* Decodes payload[0..size) (version 1, 2 or 3; the base of a bound payload is not checked
+/* orc_encode_versioned writing a version-4 payload (Rice-coded compact position blocks, see
+ * bd_oracle.c); overwrite != 0 gives an overwrite payload as above. */
+int orc_encode_rice(const uint16_t* old, const uint16_t* neu, uint64_t n, uint64_t base,
+                    int overwrite, uint8_t* out, uint64_t cap, uint64_t* size_out,
+                    uint64_t* checksum_out);
+
+/* Decodes payload[0..size) (version 1, 2, 3 or 4; the base of a bound payload is not checked
  * here) against old (n elements) into out (n elements, must not alias
  * old), then verifies checksum(out) == expected.  Returns ORC_OK, ORC_ERR_FORMAT (payload
  * is not a canonical BF16DLT1 payload for n elements) or ORC_ERR_CHECKSUM.  On an error

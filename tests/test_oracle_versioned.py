@@ -103,7 +103,7 @@ def test_unknown_version_rejected():
     new = old.copy()
     new[3] = 1
     p2, ck = oracle.encode(old, new, base=0)
-    for version in (0, 4, 255):
+    for version in (0, 5, 255):
         bad = p2.copy()
         bad[8] = version
         assert oracle.decode(old, bad, ck)[0] == oracle.ERR_FORMAT, version
