@@ -48,8 +48,22 @@
  * is below the bytes of its two version-1 blocks, so a version-3 payload is never longer
  * than the version-2 payload of the same update.  The header's position-bytes field counts
  * the position section only; the X stream is what the other sections leave of the total.
- * Every decompress call accepts all three versions.
- * Overwrite payloads (versions 2 and 3 with header flags bit 0 = BD_FLAG_OVERWRITE; the u64 at
+ * Version 4 (format 4): version 3 with the compact blocks coded by a Golomb-Rice code of the
+ * same gaps instead (a second stand-in for the unspecified entropy stage), and no X stream:
+ *   [header 80 B] [count table: C x u32] [R stream] [positions] [M stream]
+ * A compact count entry (bit 31 set) holds M in bits 0..8, R in 9..17, the Rice parameter K
+ * in 18..20 and the block's length B in bytes in 21..30 (1 <= M + R <= 508, B >= 1); plain
+ * entries are as in version 3.  The block is a bit stream, bit b = bit b%8 of byte b/8: the
+ * indices of the R rare changes in the merged list (9 bits each, strictly ascending, below
+ * M + R), then each gap's remainder gap mod 2^K (K bits), then each gap's quotient gap >> K
+ * in unary (that many 1 bits, then a 0), then 0 bits up to the end of byte B - 1, which must
+ * be the byte holding the last used bit.  Every gap is at least 1 and every position below L.
+ * Compress takes the K in 0..7 giving the fewest bits (the smallest on a tie) and codes a
+ * chunk compactly exactly when it has 1..508 changes and B is below the bytes of its two
+ * version-1 blocks, so a version-4 payload is never longer than the version-2 payload of the
+ * same update.
+ * Every decompress call accepts all four versions.
+ * Overwrite payloads (versions 2 to 4 with header flags bit 0 = BD_FLAG_OVERWRITE; the u64 at
  * byte 72, whose other bits are zero): the NeMo-DCR page's second form of update payload,
  * absolute overwrites, through which partial writes are retried.  Positions, classes and
  * sizes are those of the XOR payload of the same update; the R stream holds each rare
@@ -99,7 +113,7 @@ typedef enum bd_status {
   BD_ERR_FORMAT = 3,      /* decompress: not a canonical BF16DLT1 payload for n elements */
   BD_ERR_CHECKSUM = 4,    /* decompress: checksum of the result differs from the expected */
   BD_ERR_CUDA = 5,        /* a CUDA runtime call or kernel launch failed */
-  BD_ERR_BASE = 6         /* incremental apply: a version-2 or -3 payload whose base checksum
+  BD_ERR_BASE = 6         /* incremental apply: a payload of version 2 or later whose base checksum
                              is not the checksum of the weights it is applied to */
 } bd_status;
 
@@ -145,8 +159,8 @@ typedef struct bd_incremental_item {
 } bd_incremental_item;
 
 /* Parsed payload header (host side).  base_checksum is 0 for a version-1 payload;
- * n_escapes (X-stream values) is 0 below version 3; flags is the header flags word of versions
- * 2 and 3 (BD_FLAG_OVERWRITE: an overwrite payload), 0 for version 1. */
+ * n_escapes (X-stream values) is 0 except in version 3; flags is the header flags word of
+ * versions 2 to 4 (BD_FLAG_OVERWRITE: an overwrite payload), 0 for version 1. */
 typedef struct bd_payload_info_t {
   uint64_t n, chunks, n_mant, n_rare, position_bytes, total_size;
   uint32_t version, chunk_elems;
@@ -230,7 +244,7 @@ BD_API int bd_decompress_batch(const bd_decompress_item* h_items, uint32_t k, vo
  *          mix64(new_word_j ^ (j+1)*G) - mix64(old_word_j ^ (j+1)*G)     (mod 2^64)
  * which equals the checksum of the result whenever *d_ck_old is the checksum of d_w before
  * the call.  The status is BD_OK when ck == *d_expected, else BD_ERR_CHECKSUM (format errors
- * as bd_decompress); ck goes to *d_ck_out when given.  A version-2 or -3 payload whose base
+ * as bd_decompress); ck goes to *d_ck_out when given.  A payload of version 2 or later whose base
  * checksum differs from *d_ck_old is refused with BD_ERR_BASE and nothing is written.  Only the 32-byte sectors holding
  * changes are read and written (plus the payload), against a full read of the tensor for
  * bd_decompress.  What it does not verify: a word of d_w that differs from the trainer's
@@ -284,7 +298,7 @@ BD_API int bd_decompress_noalloc(const uint16_t* d_old, uint64_t n, const void* 
 BD_API int bd_checksum(const uint16_t* d_w, uint64_t n, uint64_t* d_out, void* stream);
 
 /* Parses and checks a payload header held in host memory (bytes >= 64; >= 80 for versions 2
- * and 3).  Checks magic, version, chunk size and the internal consistency of the header
+ * to 4).  Checks magic, version, chunk size and the internal consistency of the header
  * fields (for version 3 the total leaves an even number of bytes, at most 2 * 508 per chunk,
  * for the X stream); returns BD_OK, BD_ERR_FORMAT or BD_ERR_INVALID_ARG.  Does not touch the
  * GPU. */

@@ -429,7 +429,7 @@ int bd_payload_info(const void* h_header, uint64_t bytes, bd_payload_info_t* out
   I.base_checksum = 0;
   I.n_escapes = 0;
   I.flags = 0;
-  if (I.version < 1 || I.version > 3 || I.chunk_elems != kChunk || I.n > BD_MAX_ELEMS)
+  if (I.version < 1 || I.version > 4 || I.chunk_elems != kChunk || I.n > BD_MAX_ELEMS)
     return BD_ERR_FORMAT;
   const uint64_t hdr = I.version >= 2 ? kHeaderV2 : kHeader;
   if (I.version >= 2) {

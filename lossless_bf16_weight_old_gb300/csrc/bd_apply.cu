@@ -9,11 +9,12 @@
 //   copy_jobs      out-of-place only: out = old (warp per chunk), so the passes below work on
 //                  out in place.
 //   apply_chunks   one warp per chunk whose two position blocks are delta lists (the common
-//                  case for sparse deltas) or whose block is a version-3 compact block (one
-//                  ascending list of gap bytes with class bits): decodes and checks the whole
+//                  case for sparse deltas) or whose block is a compact block (one ascending
+//                  list of changes: gap bytes with class bits in version 3, a Rice code of the
+//                  gaps with the rare indices in version 4): decodes and checks the whole
 //                  chunk into shared memory, XORs each change into out with a 32-bit atomic
-//                  XOR performed in L2,
-//                  then reads the chunk back through L2 for its checksum terms.  The atomics
+//                  XOR performed in L2, then reads the chunk back through L2 for its checksum
+//                  terms.  The atomics
 //                  bring the touched sectors into L2 where the read-back finds them, so each
 //                  sector of out crosses HBM at most once each way.  Chunks with a bitmap
 //                  block are listed.
@@ -33,6 +34,28 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
+// Words of a warp's staging area for a version-4 block: the block (at most 1023 bytes, 256
+// words) and a zero guard word, then the 512-bit class bitmap of the merged list.
+constexpr uint32_t kRiceCls = 260;
+constexpr uint32_t kRiceWords = kRiceCls + 16;
+
+__device__ __forceinline__ bool decode_rice(const uint8_t* __restrict__ blk, uint32_t nb,
+                                            uint32_t K, const uint8_t* __restrict__ mbytes,
+                                            uint32_t s0, const uint16_t* __restrict__ rvals,
+                                            uint32_t M, uint32_t R, uint32_t L, bool ow,
+                                            uint32_t* __restrict__ sw,
+                                            uint32_t* __restrict__ ent);
+// The same as a called function: the block-level kernel holds more registers of its own
+// across the decode (inlined there, it needed 128 registers and spilled; the warp-level
+// kernels inline it).
+__device__ __noinline__ bool decode_rice_call(const uint8_t* blk, uint32_t nb, uint32_t K,
+                                              const uint8_t* mbytes, uint32_t s0,
+                                              const uint16_t* rvals, uint32_t M, uint32_t R,
+                                              uint32_t L, bool ow, uint32_t* sw, uint32_t* ent) {
+  return decode_rice(blk, nb, K, mbytes, s0, rvals, M, R, L, ow, sw, ent);
+}
 
 // 7-bit value j of an M stream.  The caller guarantees j < number of M values, so the
 // second byte is read only when the value crosses into it (and then it exists).
@@ -131,6 +154,8 @@ k_apply_dense(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_
   __shared__ uint4 s_mask4[kChunk / 8];       // the chunk's XOR mask (overwrite: targets), 8 KiB
   __shared__ uint32_t s_rec[2][kChunk / 32];  // overwrite: positions with M / R records
   __shared__ uint32_t s_tot[kWarps][4];
+  __shared__ uint32_t s_rice[kRiceWords];     // version 4: warp 0's staging area ...
+  __shared__ uint32_t s_rent[kCompactMax];    // ... and the decoded changes
   __shared__ int s_bad;
   uint16_t* s_mask = reinterpret_cast<uint16_t*>(s_mask4);
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
@@ -186,7 +211,24 @@ k_apply_dense(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_
     // (the first block scan below orders these stores before every scatter)
 
     bool bad = false;
-    if (cc.compact) {
+    if (cc.rice) {
+      // warp 0 decodes and checks the Rice block, then every thread records two changes
+      if (w == 0) {
+        const uint64_t mbit0 = 7 * Mex;
+        const bool b = decode_rice_call(mblk, cc.nb, cc.K, mstream + (mbit0 >> 3),
+                                   (uint32_t)(mbit0 & 7),
+                                   reinterpret_cast<const uint16_t*>(rstream), M, R, L, ow,
+                                   s_rice, s_rent);
+        if (lane == 0 && b) s_bad = 1;
+      }
+      __syncthreads();
+      if (s_bad == 0) {
+        for (uint32_t i = t; i < M + R; i += kThreads) {
+          const uint32_t e = s_rent[i];
+          put_record(s_mask, s_rec[e >> 31], ent_pos(e), e & 0xFFFFu, ow);
+        }
+      }
+    } else if (cc.compact) {
       // changes t (slot a) and t + 256 (slot b) of the merged list; first the escapes and the
       // rare flags, then the gaps with the escaped values in place
       const uint32_t k = M + R, ia = t, ib = t + 256;
@@ -388,7 +430,6 @@ k_apply_dense(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_
 constexpr uint32_t kListMax = 255;
 constexpr uint32_t kEntMax = 2 * kListMax + 2;
 constexpr uint32_t kNone = 0xFFFFFFFFu;
-constexpr unsigned kFull = 0xFFFFFFFFu;
 
 // Loads served by L2 only (never by L1): `out` is changed by L2 atomics while the kernel runs.
 // Volatile so that the compiler keeps them after the atomics and the fence that precede them.
@@ -611,6 +652,120 @@ __device__ __forceinline__ bool decode_compact(const uint8_t* __restrict__ blk,
   return __any_sync(kFull, bad);
 }
 
+// Decodes a version-4 compact chunk (one warp) into ent[0..M+R) in the general entry layout,
+// in ascending position: the nb-byte Rice block at blk with parameter K is staged as words in
+// sw (kRiceWords, per warp), the rare indices set the class bitmap, each lane finds the zeros
+// of one 32-bit window of the unary section (their offsets go to ent[rank] for rank < k), and
+// the changes are then formed 32 at a time -- gap (quotient << K | remainder, quotient from
+// two consecutive zeros), position from the prefix sums of the gaps, value from the M or R
+// stream by class.  Checks, as the format requires: the fixed fields fit in the block; the
+// rare indices strictly ascend below k; k zeros in the unary section; the bits used end in
+// the block's last byte and the pad bits after them are zero (the ones of the section are
+// exactly the quotients' ones); every gap is at least 1 and every position below L; the value
+// rules of apply_chunks.  Returns whether the chunk is malformed (the same on every lane).
+__device__ __forceinline__ bool decode_rice(const uint8_t* __restrict__ blk, uint32_t nb,
+                                            uint32_t K, const uint8_t* __restrict__ mbytes,
+                                            uint32_t s0, const uint16_t* __restrict__ rvals,
+                                            uint32_t M, uint32_t R, uint32_t L, bool ow,
+                                            uint32_t* __restrict__ sw,
+                                            uint32_t* __restrict__ ent) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t lt = (1u << lane) - 1;
+  const uint32_t k = M + R, nbits = 8 * nb, nw = (nb + 3) >> 2;   // nw <= 256
+  uint32_t* __restrict__ cls = sw + kRiceCls;
+  // the block as little-endian words, bytes past it zero, and the guard word
+  for (uint32_t i = lane; i <= nw; i += 32) {
+    uint32_t v = 0;
+#pragma unroll
+    for (int b = 0; b < 4; b++)
+      if (4 * i + b < nb) v |= (uint32_t)blk[4 * i + b] << (8 * b);
+    sw[i] = v;
+  }
+  if (lane < 16) cls[lane] = 0;
+  __syncwarp();
+  // nbits-bit field at bit `at` of the block (at < 32 * nw, so the second word exists)
+  auto field = [&](uint32_t at, uint32_t bits) -> uint32_t {
+    const uint32_t wd = at >> 5;
+    return __funnelshift_r(sw[wd], sw[wd + 1], at & 31) & ((1u << bits) - 1u);
+  };
+  const uint32_t fixed = kRiceIdxBits * R + K * k;
+  if (fixed >= nbits) return true;   // no room for the k unary zeros (the same on every lane)
+  bool bad = false;
+  // rare indices: strictly ascending, below k
+  uint32_t last = 0;
+  for (uint32_t j0 = 0; j0 < R; j0 += 32) {
+    const uint32_t jj = j0 + lane;
+    const bool in = jj < R;
+    const uint32_t idx = in ? field(kRiceIdxBits * jj, kRiceIdxBits) : 0u;
+    uint32_t before = __shfl_up_sync(kFull, idx, 1);
+    if (lane == 0) before = last;
+    if (in) {
+      if (idx >= k || (jj > 0 && idx <= before)) bad = true;
+      else atomicOr(&cls[idx >> 5], 1u << (idx & 31));
+    }
+    last = __shfl_sync(kFull, idx, 31);
+  }
+  // the unary section [fixed, nbits) in 32-bit windows, one per lane: zero offsets by rank
+  const uint32_t nwin = (nbits - fixed + 31) >> 5;
+  uint32_t zeros = 0, ones = 0;
+  for (uint32_t t0 = 0; t0 < nwin; t0 += 32) {
+    const uint32_t t = t0 + lane;
+    uint32_t zm = 0;
+    if (t < nwin) {
+      const uint32_t at = fixed + 32 * t, avail = nbits - at;
+      const uint32_t valid = avail >= 32 ? 0xFFFFFFFFu : (1u << avail) - 1u;
+      const uint32_t wd = at >> 5;
+      const uint32_t win = __funnelshift_r(sw[wd], sw[wd + 1], at & 31);
+      zm = ~win & valid;
+      ones += __popc(win & valid);
+    }
+    const uint32_t cz = __popc(zm), incl = warp_incl_scan(cz);
+    uint32_t r = zeros + incl - cz;
+    for (; zm != 0 && r < k; zm &= zm - 1, r++) ent[r] = 32 * t + __ffs(zm) - 1;
+    zeros += __shfl_sync(kFull, incl, 31);
+  }
+  ones = (uint32_t)warp_sum64(ones);
+  __syncwarp();
+  if (__any_sync(kFull, bad) || zeros < k) return true;
+  const uint32_t zlast = ent[k - 1];                  // offset of the k-th zero
+  const uint32_t used = fixed + zlast + 1;
+  if ((used + 7) / 8 != nb || ones != zlast + 1 - k) return true;
+  // the changes, 32 at a time
+  uint32_t carry = 0xFFFFFFFFu, zprev = 0xFFFFFFFFu, mr = 0, rr = 0;
+  const uint32_t rem0 = kRiceIdxBits * R;
+  for (uint32_t b0 = 0; b0 < k; b0 += 32) {
+    const uint32_t i = b0 + lane;
+    const bool in = i < k;
+    const uint32_t z = in ? ent[i] : 0u;
+    uint32_t zp = __shfl_up_sync(kFull, z, 1);
+    if (lane == 0) zp = zprev;
+    zprev = __shfl_sync(kFull, z, 31);
+    const uint32_t g = in ? ((z - zp - 1) << K) | field(rem0 + K * i, K) : 0u;
+    const bool isR = in && ((cls[i >> 5] >> (i & 31)) & 1u);
+    const uint32_t bR = __ballot_sync(kFull, isR), bM = __ballot_sync(kFull, in && !isR);
+    uint32_t v = 0;
+    if (isR) {
+      const uint32_t r = rr + __popc(bR & lt);
+      if (r < R) v = rvals[r]; else bad = true;
+    } else if (in) {
+      const uint32_t m = mr + __popc(bM & lt);
+      if (m < M) v = mant_at(mbytes, s0, m); else bad = true;
+    }
+    rr += __popc(bR);
+    mr += __popc(bM);
+    if (in && g == 0) bad = true;
+    __syncwarp();   // every lane has read its zero offset before the entries replace them
+    const uint32_t p = carry + warp_incl_scan(g);
+    carry = __shfl_sync(kFull, p, 31);
+    if (in) {
+      if (!ow && (isR ? (v & kSignExp) == 0 : v == 0)) bad = true;
+      if (p >= L) bad = true;
+      if (!bad) ent[i] = (isR ? kEntRare : 0u) | (p << 16) | v;
+    }
+  }
+  return __any_sync(kFull, bad);
+}
+
 // Asks L2 for the 128-byte line holding p when p lies before end (a hint: nothing waits for
 // it, and nothing is asked past the end of the payload).
 __device__ __forceinline__ void prefetch_l2_before(const uint8_t* p, const uint8_t* end) {
@@ -659,7 +814,8 @@ k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
                uint32_t* __restrict__ list, uint8_t* __restrict__ ck_base) {
   if ((list_count[kFlagV3Word] != 0) != V3) return;   // the other build runs this call
   __shared__ uint32_t s_ent[kWarps][kEntMax];       // pos << 16 | XOR value
-  __shared__ uint4 s_bits[kWarps][kChunk / 128];    // mantissa-only positions, 512 B
+  // mantissa-only positions (512 B); in the general build also a version-4 staging area
+  __shared__ uint4 s_bits[kWarps][V3 ? kRiceWords / 4 : kChunk / 128];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   uint32_t* ent = s_ent[w];
   uint32_t* bits = reinterpret_cast<uint32_t*>(s_bits[w]);
@@ -708,7 +864,9 @@ k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
       const bool both = M > 0 && R > 0;
       const bool ow = V3 && (I.flags & kFlagOverwrite) != 0;
       bool bad = false;
-      if (V3 && cc.compact) {
+      if (V3 && cc.rice) {
+        bad = decode_rice(mlist, cc.nb, cc.K, mbytes, s0, rvals, M, R, L, ow, bits, ent);
+      } else if (V3 && cc.compact) {
         bad = decode_compact<4>(mlist,
                              reinterpret_cast<const uint16_t*>(payload + I.x_start) + pre.e + lc.w,
                              cc.E, mbytes, s0, rvals, M, R, L, ow, ent);
@@ -833,7 +991,8 @@ k_apply_incr(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
   // another build runs this call
   if ((list_count[kFlagV3Word] != 0) != V3 || (list_count[kFlagOwWord] != 0) != OW) return;
   __shared__ uint32_t s_ent[kWarps][kEntMax];       // pos << 16 | XOR value
-  __shared__ uint4 s_bits[kWarps][kChunk / 128];    // mantissa-only positions, 512 B
+  // mantissa-only positions (512 B); in the general build also a version-4 staging area
+  __shared__ uint4 s_bits[kWarps][V3 ? kRiceWords / 4 : kChunk / 128];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   uint32_t* ent = s_ent[w];
   uint32_t* bits = reinterpret_cast<uint32_t*>(s_bits[w]);
@@ -882,7 +1041,9 @@ k_apply_incr(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
     const bool both = M > 0 && R > 0;
     const bool ow = OW && (I.flags & kFlagOverwrite) != 0;
     bool bad = false;
-    if (V3 && cc.compact) {
+    if (V3 && cc.rice) {
+      bad = decode_rice(mlist, cc.nb, cc.K, mbytes, s0, rvals, M, R, L, ow, bits, ent);
+    } else if (V3 && cc.compact) {
       bad = decode_compact<0>(mlist,
                            reinterpret_cast<const uint16_t*>(payload + I.x_start) + pre.e + lc.w,
                            cc.E, mbytes, s0, rvals, M, R, L, ow, ent);

@@ -1,6 +1,6 @@
 // bd_internal.cuh -- device-side definitions shared by the kernels of libbf16delta.
 //
-// Everything here follows the BF16DLT1 format (versions 1 to 3) described in include/bf16delta.h.
+// Everything here follows the BF16DLT1 format (versions 1 to 4) described in include/bf16delta.h.
 // The field split comes from "Every byte counts: ARCv3 and the case for cross-region RL"
 // (figure "How ARCv3 encodes a block of weights"); the XOR algebra from "GPU-accelerated
 // Weight Teleportation", section "Delta update algebra".
@@ -55,17 +55,35 @@ __host__ __device__ __forceinline__ bool choose_compact(uint32_t M, uint32_t R, 
          compact_bytes(k) + 2 * E < block_bytes(M, B) + block_bytes(R, B);
 }
 
+// Version 4: compact blocks coded with a Golomb-Rice code instead (no X stream).  A compact
+// entry holds M in bits 0..8, R in 9..17, the Rice parameter K in 18..20 and the block's bytes
+// in 21..30 (M + R in 1..508, at least one byte).  The block is a bit stream read LSB-first
+// from its first byte: the merged-list indices of the R rare changes (9 bits each, strictly
+// ascending, below M + R), the K-bit remainders g mod 2^K of the gaps, then the quotients
+// g >> K in unary (ones closed by a zero), then zero pad bits up to the block's last byte.
+constexpr uint32_t kRiceIdxBits = 9;
+
 // One count-table entry, decoded for the payload's version.
 struct ChunkCount {
-  uint32_t M, R, E;   // mantissa-only and rare changes, escaped gaps (compact only)
+  uint32_t M, R, E;   // mantissa-only and rare changes, escaped gaps (version-3 compact only)
+  uint32_t K, nb;     // version-4 compact only: Rice parameter, block bytes
   bool compact;
+  bool rice;          // a compact chunk of version 4
   bool bad;           // unused bits set, or a compact entry out of range
 };
 __host__ __device__ __forceinline__ ChunkCount parse_count(uint32_t v, uint32_t version) {
-  ChunkCount c{0, 0, 0, false, false};
+  ChunkCount c{0, 0, 0, 0, 0, false, false, false};
   if (version < 3) {
     c.M = v & 0xFFFFu;
     c.R = v >> 16;
+  } else if ((v & kCompactFlag) && version == 4) {
+    c.compact = true;
+    c.rice = true;
+    c.M = v & 0x1FFu;
+    c.R = (v >> 9) & 0x1FFu;
+    c.K = (v >> 18) & 0x7u;
+    c.nb = (v >> 21) & 0x3FFu;
+    c.bad = c.M + c.R == 0 || c.M + c.R > kCompactMax || c.nb == 0;
   } else if (v & kCompactFlag) {
     c.compact = true;
     c.M = v & 0x1FFu;
@@ -82,6 +100,7 @@ __host__ __device__ __forceinline__ ChunkCount parse_count(uint32_t v, uint32_t 
 }
 // Position-section bytes of a chunk whose bitmap has B bytes.
 __host__ __device__ __forceinline__ uint32_t chunk_pos_bytes(const ChunkCount& c, uint32_t B) {
+  if (c.rice) return c.nb;
   return c.compact ? compact_bytes(c.M + c.R) : block_bytes(c.M, B) + block_bytes(c.R, B);
 }
 // The count-table entry written by compress.
@@ -92,7 +111,7 @@ __host__ __device__ __forceinline__ uint32_t count_entry(uint32_t version, uint3
   return M | (R << 15);
 }
 
-// Header flags (the u64 at byte 72 of a version-2 or -3 header).  kFlagOverwrite: the streams
+// Header flags (the u64 at byte 72 of a header of version 2 or later).  kFlagOverwrite: the streams
 // carry new field values (the whole value of a rare change, the mantissa of a mantissa-only
 // change) that overwrite the weights instead of XOR masks; every other bit is zero.
 constexpr uint32_t kFlagOverwrite = 1;
@@ -209,9 +228,9 @@ struct CJob {
   uint64_t chunk_base;  // global index of this tensor's chunk 0
   uint64_t nchunks;     // C = ceil(n / 4096)
   uint64_t tile_base;   // global index of this tensor's first scan tile
-  const uint64_t* d_base;   // versions 2 and 3: the base checksum to bind to (NULL: version 1)
+  const uint64_t* d_base;   // versions 2 to 4: the base checksum to bind to (NULL: version 1)
   uint32_t version;         // payload version written: 1, 2 or 3 (compact position blocks)
-  uint32_t flags;           // header flags written (versions 2 and 3): kFlagOverwrite
+  uint32_t flags;           // header flags written (versions 2 to 4): kFlagOverwrite
   uint64_t pad[3];
 };
 static_assert(sizeof(CJob) == 128, "CJob layout");
@@ -241,7 +260,7 @@ struct JobInfo {
   int32_t status;      // set by the scan phase; constant while later kernels run
   int32_t chunk_err;   // set by the apply kernel when a chunk is malformed
   uint32_t version;    // payload version (set by the scan phase)
-  uint32_t flags;      // header flags (versions 2 and 3; set by the scan phase)
+  uint32_t flags;      // header flags (versions 2 to 4; set by the scan phase)
   uint64_t pad;
 };
 static_assert(sizeof(JobInfo) == 96, "JobInfo layout");

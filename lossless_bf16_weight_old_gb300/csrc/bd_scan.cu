@@ -2,7 +2,7 @@
 //
 // The payload sections are laid out chunk-major, so every chunk needs the exclusive prefix of
 // four per-chunk quantities over the chunks before it in its tensor: position-section bytes
-// P_c (two version-1 blocks, or a version-3 compact block), mantissa-only count M_c, rare
+// P_c (two version-1 blocks, or a compact block of version 3 or 4), mantissa-only count M_c, rare
 // count R_c and escaped gaps E_c (X-stream values of a compact block, else 0).
 //   scan_tiles  one CTA per tile of 1024 chunks: per-chunk prefix inside the tile, tile total.
 //               Compress decides here which chunks of a version-3 payload are compact.  For
@@ -91,7 +91,7 @@ k_scan_tiles(const void* __restrict__ jobs, const uint64_t* __restrict__ tile_st
         const uint64_t L64 = J.n - c * kChunk;
         const uint32_t L = L64 < kChunk ? (uint32_t)L64 : kChunk;
         const uint32_t B = (L + 7) >> 3;
-        ChunkCount cc;
+        ChunkCount cc{};
         if (DEC) {
           cc = parse_count(v, version);
           if (cc.bad || cc.M + cc.R > L) bad = true;
@@ -214,7 +214,7 @@ k_scan_jobs(const void* __restrict__ jobs, const uint64_t* __restrict__ tile_sta
                                  ? reinterpret_cast<const uint64_t*>(J.payload)[9] : 0;
       I.flags = (uint32_t)(flags & kFlagOverwrite);
       // the general apply build decodes compact blocks and applies overwrites
-      if (version == 3 || I.flags != 0) *v3_flag = 1u;
+      if (version >= 3 || I.flags != 0) *v3_flag = 1u;
       if (I.flags != 0) v3_flag[kFlagOwWord - kFlagV3Word] = 1u;
       I.r_start = hdr + 4 * J.nchunks;
       I.x_start = I.r_start + 2 * rR;
@@ -225,7 +225,7 @@ k_scan_jobs(const void* __restrict__ jobs, const uint64_t* __restrict__ tile_sta
         st = BD_ERR_FORMAT;
       } else if (st == BD_OK) {
         const uint64_t* h = reinterpret_cast<const uint64_t*>(J.payload);
-        const bool ok = h[0] == kMagic && version >= 1 && version <= 3 &&
+        const bool ok = h[0] == kMagic && version >= 1 && version <= 4 &&
                         h[1] == ((uint64_t)version | ((uint64_t)kChunk << 32)) &&
                         h[2] == J.n && h[3] == J.nchunks && h[4] == rM && h[5] == rR &&
                         h[6] == rP && h[7] == J.size && I.total == J.size &&
