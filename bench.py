@@ -592,6 +592,32 @@ def run_ours(args) -> None:
             i3_ms = ms
     del c3b, d3, i3
 
+    # version 4 (Rice-coded compact position blocks) of the same update, timed as version 3
+    c4 = bd.CompressBatch(olds, news, base_checksums=ck_old, rice=True)
+    c4.run(stream)
+    torch.cuda.synchronize()
+    s4 = [int(v) for v in c4.sizes.tolist()]
+    c4b = bd.CompressBatch(news, olds, caps=s4, base_checksums=ck_new, rice=True)
+    c4b.run(stream)
+    torch.cuda.synchronize()
+    if int(c4.status.item()) != bd.OK or int(c4b.status.item()) != bd.OK:
+        raise RuntimeError("version-4 compress failed")
+    p4_bytes = sum(s4)
+    c4_ms, _ = timed(lambda: c4.run(stream), args.steps)
+    d4 = {True: bd.DecompressBatch(rolls, c4.payloads, s4, ck_old),
+          False: bd.DecompressBatch(rolls, c4.payloads, s4, ck_new)}
+    i4 = {True: bd.IncrementalBatch(rolls, c4b.payloads, s4, ck_new, ck_old),
+          False: bd.IncrementalBatch(rolls, c4.payloads, s4, ck_old, ck_new)}
+    rice_res = {}
+    for name, table in (("apply", d4), ("incremental", i4)):
+        ms, last4 = timed(alternate(table), args.steps)
+        want = N if state["new"] else O
+        if int(last4.status.item()) != bd.OK or not torch.equal(Rb.view(torch.int16),
+                                                                 want.view(torch.int16)):
+            raise RuntimeError(f"version-4 {name} did not verify")
+        rice_res[name] = ms
+    del c4, c4b, d4, i4
+
     # overwrite payloads (version 3, header flag bit 0) of the same update, both directions
     cof = bd.CompressBatch(olds, news, caps=s3, base_checksums=ck_old, compact=True,
                            overwrite=True)
@@ -736,6 +762,19 @@ def run_ours(args) -> None:
                     "what": "version-3 payloads (compact position blocks) of the same update: "
                             "bd_compress_versioned_batch format 3, bd_decompress_batch in "
                             "place, bd_decompress_incremental_batch in place"},
+                "rice": {
+                    "payload_pct": round(100 * p4_bytes / raw, 4),
+                    "payload_vs_v1": round(p4_bytes / payload_bytes, 4),
+                    "payload_vs_v3": round(p4_bytes / p3_bytes, 4),
+                    "compress_ms": round(c4_ms, 4), "apply_ms": round(rice_res["apply"], 4),
+                    "incremental_ms": round(rice_res["incremental"], 4),
+                    "compress_roofline_frac": round((4 * n_total + p4_bytes) / (c4_ms * 1e-3)
+                                                    / 1e9 / peak, 4),
+                    "apply_roofline_frac": round((2 * n_total + p4_bytes + 32 * touched)
+                                                 / (rice_res["apply"] * 1e-3) / 1e9 / peak, 4),
+                    "what": "version-4 payloads (Rice-coded compact position blocks) of the same "
+                            "update: bd_compress_versioned_batch format 4, bd_decompress_batch "
+                            "in place, bd_decompress_incremental_batch in place"},
                 "overwrite": {
                     "compress_ms": round(ow_ms, 4), "apply_ms": round(ow_res["apply"], 4),
                     "incremental_ms": round(ow_res["incremental"], 4),

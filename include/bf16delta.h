@@ -199,15 +199,16 @@ BD_API int bd_compress_batch(const bd_compress_item* h_items, uint32_t k, void* 
                       uint64_t ws_bytes, int32_t* d_status, void* stream);
 
 /* bd_compress writing a payload bound to its base version: format 2 (the version-1 payload
- * with the 80-byte header) or 3 (compact position blocks, see above), either optionally OR-ed
- * with BD_FORMAT_OVERWRITE for an overwrite payload; any other format is BD_ERR_INVALID_ARG.  Not on the pages: the NeMo-DCR page binds the installed weights to
+ * with the 80-byte header), 3 (compact position blocks, see above) or 4 (Rice-coded compact
+ * position blocks), each optionally OR-ed with BD_FORMAT_OVERWRITE for an overwrite payload;
+ * any other format is BD_ERR_INVALID_ARG.  Not on the pages: the NeMo-DCR page binds the installed weights to
  * the baseline of the next delta so that mismatched versions cannot enter silently.
  * *d_base_checksum (device, required) is the checksum of d_old as the caller knows it -- in
  * a steady update loop, the checksum of the previous update's new weights; it is stored in
  * the header, not recomputed.  The incremental apply refuses the payload with BD_ERR_BASE
  * when the receiver's checksum of its weights differs; bd_payload_info exposes the base for
  * a check on the host before a full apply.  Sizes, capacity and workspace as bd_compress
- * (bd_compress_bound covers both formats). */
+ * (bd_compress_bound covers every format). */
 BD_API int bd_compress_versioned(const uint16_t* d_old, const uint16_t* d_new, uint64_t n,
                                  void* d_payload, uint64_t cap, void* d_ws, uint64_t ws_bytes,
                                  uint64_t* d_size, uint64_t* d_checksum,

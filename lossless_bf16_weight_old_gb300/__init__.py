@@ -171,23 +171,28 @@ def _workspace(nbytes: int, device, workspace) -> torch.Tensor:
 FORMAT_OVERWRITE = 0x100   # BD_FORMAT_OVERWRITE
 
 
-def _format_arg(compact: bool, overwrite: bool) -> int:
+def _format_arg(compact: bool, overwrite: bool, rice: bool = False) -> int:
     """The format argument of bd_compress_versioned(_batch)."""
-    return (3 if compact else 2) | (FORMAT_OVERWRITE if overwrite else 0)
+    if compact and rice:
+        raise ValueError("compact (version 3) and rice (version 4) exclude each other")
+    return (4 if rice else 3 if compact else 2) | (FORMAT_OVERWRITE if overwrite else 0)
 
 
 def compress(old: torch.Tensor, new: torch.Tensor, *, payload: torch.Tensor | None = None,
              workspace: torch.Tensor | None = None, base_checksum=None, compact: bool = False,
-             overwrite: bool = False, stream=None):
+             overwrite: bool = False, rice: bool = False, stream=None):
     """Encodes old -> new on the GPU.  Returns device tensors
     (payload uint8[cap], size int64[1], checksum int64[1] (unsigned bits), status int32[1]),
     all written asynchronously on the stream.  With base_checksum (an int or int64[1] device
     tensor: the checksum of old as the caller knows it) the payload is bound to that base
-    (bd_compress_versioned): version 2, or version 3 (compact position blocks) when
-    `compact` is set; with `overwrite` the payload carries new values instead of XOR masks
-    (applying it again, to weights it has wholly or partly updated, gives the same result)."""
-    if (compact or overwrite) and base_checksum is None:
-        raise ValueError("compact and overwrite payloads are bound to a base: pass base_checksum")
+    (bd_compress_versioned): version 2, version 3 (compact position blocks) when `compact` is
+    set, or version 4 (Rice-coded compact position blocks) when `rice` is set; with
+    `overwrite` the payload carries new values instead of XOR masks (applying it again, to
+    weights it has wholly or partly updated, gives the same result)."""
+    if (compact or overwrite or rice) and base_checksum is None:
+        raise ValueError("compact, Rice and overwrite payloads are bound to a base: "
+                         "pass base_checksum")
+    fmt = _format_arg(compact, overwrite, rice)
     po, n = _bits(old, "old")
     pn, n2 = _bits(new, "new")
     if n != n2:
@@ -210,7 +215,7 @@ def compress(old: torch.Tensor, new: torch.Tensor, *, payload: torch.Tensor | No
         rc = _lib.load().bd_compress_versioned(po, pn, n, payload.data_ptr(), payload.numel(),
                                                ws.data_ptr(), ws.numel(), size.data_ptr(),
                                                ck.data_ptr(), base_checksum.data_ptr(),
-                                               _format_arg(compact, overwrite), st.data_ptr(),
+                                               fmt, st.data_ptr(),
                                                _stream(stream))
         _check(rc, "bd_compress_versioned")
     return payload, size, ck, st
@@ -273,14 +278,15 @@ class CompressBatch:
 
     def __init__(self, olds: Sequence[torch.Tensor], news: Sequence[torch.Tensor],
                  caps: Sequence[int] | None = None, base_checksums: torch.Tensor | None = None,
-                 compact: bool = False, overwrite: bool = False):
+                 compact: bool = False, overwrite: bool = False, rice: bool = False):
         """base_checksums (int64[k] device tensor, optional): payloads bound to these base
-        checksums (bd_compress_versioned_batch), version 2, or version 3 (compact position
-        blocks) when `compact` is set, overwrite payloads when `overwrite` is set."""
-        if (compact or overwrite) and base_checksums is None:
-            raise ValueError("compact and overwrite payloads are bound to a base: "
+        checksums (bd_compress_versioned_batch), version 2, version 3 (compact position
+        blocks) when `compact` is set or version 4 (Rice-coded ones) when `rice` is set,
+        overwrite payloads when `overwrite` is set."""
+        if (compact or overwrite or rice) and base_checksums is None:
+            raise ValueError("compact, Rice and overwrite payloads are bound to a base: "
                              "pass base_checksums")
-        self.format = _format_arg(compact, overwrite)
+        self.format = _format_arg(compact, overwrite, rice)
         if len(olds) != len(news):
             raise ValueError("olds and news differ in length")
         k = len(olds)

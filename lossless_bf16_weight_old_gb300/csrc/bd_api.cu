@@ -117,14 +117,14 @@ inline bool overlaps(const void* a, uint64_t na, const void* b, uint64_t nb) {
 int check(cudaError_t e) { return e == cudaSuccess ? BD_OK : BD_ERR_CUDA; }
 
 // -------------------------------------------------------------------------------- compress
-// bases == nullptr: version 1; else version `format & 0xFF` (2, or 3 with compact position
-// blocks), an overwrite payload when format has BD_FORMAT_OVERWRITE.
+// bases == nullptr: version 1; else version `format & 0xFF` (2, or 3 or 4 with compact
+// position blocks), an overwrite payload when format has BD_FORMAT_OVERWRITE.
 int compress_impl(const bd_compress_item* items, const uint64_t* const* bases, uint32_t format,
                   uint32_t k, void* ws, uint64_t ws_bytes, int32_t* status_all, cudaStream_t s) {
   if (k > 0 && items == nullptr) return BD_ERR_INVALID_ARG;
   const uint32_t vfmt = format & 0xFFu;
   const bool overwrite = bases && (format & BD_FORMAT_OVERWRITE) != 0;
-  if (bases && ((vfmt != 2 && vfmt != 3) || (format & ~(0xFFu | BD_FORMAT_OVERWRITE)) != 0))
+  if (bases && (vfmt < 2 || vfmt > 4 || (format & ~(0xFFu | BD_FORMAT_OVERWRITE)) != 0))
     return BD_ERR_INVALID_ARG;
   const uint32_t version = bases ? vfmt : 1;
   if (bases)
@@ -190,11 +190,13 @@ int compress_impl(const bd_compress_item* items, const uint64_t* const* bases, u
   if (status_all && (rc = check(cudaMemsetAsync(status_all, 0, sizeof(int32_t), s)))) return rc;
   if (k == 0) return BD_OK;
   if ((rc = check(upload(host, w + lay.jobs, s)))) return rc;
-  const bool general = version == 3 || overwrite;   // the general kernel builds
-  if ((rc = check(launch_encode_slots(c, general, overwrite)))) return rc;
+  // the kernel builds: version 4, version 3 (also every overwrite payload of version 2), or
+  // the XOR payloads of versions 1 and 2
+  const uint32_t fmt = version == 4 ? 4u : (version == 3 || overwrite) ? 3u : 0u;
+  if ((rc = check(launch_encode_slots(c, fmt, overwrite)))) return rc;
   if ((rc = check(launch_scan_tiles(c, false)))) return rc;
   if ((rc = check(launch_scan_jobs(c, false, status_all)))) return rc;
-  if ((rc = check(launch_emit(c, general, overwrite)))) return rc;
+  if ((rc = check(launch_emit(c, fmt, overwrite)))) return rc;
   return check(launch_emit_dense(c));
 }
 

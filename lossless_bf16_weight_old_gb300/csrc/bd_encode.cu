@@ -126,12 +126,90 @@ __device__ __noinline__ uint32_t chunk_escapes(const uint16_t* __restrict__ old,
   return esc;
 }
 
-// GEN: the general build (version 3, overwrite payloads): the chunk's escaped gaps counted.
+// Version 4: the Rice statistics of a chunk from its k >= 1 slot entries (position order, either
+// layout): the packed sums of g >> K (rice_terms) over its gaps, and in sum0 the sum of the gaps
+// (its last position + 1).
+__device__ __forceinline__ uint64_t slot_rice(const uint32_t* __restrict__ entries, uint32_t k,
+                                           uint32_t* sum0) {
+  const int lane = threadIdx.x & 31;
+  int32_t carry = -1;
+  uint64_t acc = 0;
+  for (uint32_t i0 = 0; i0 < k; i0 += 32) {
+    const uint32_t i = i0 + lane;
+    const int32_t pos = i < k ? (int32_t)ent_pos(entries[i]) : 0;
+    int32_t prev = __shfl_up_sync(0xFFFFFFFFu, pos, 1);
+    if (lane == 0) prev = carry;
+    if (i < k) acc += rice_terms((uint32_t)(pos - prev));
+    carry = __shfl_sync(0xFFFFFFFFu, pos, 31);
+  }
+  *sum0 = ent_pos(entries[k - 1]) + 1;
+  return warp_sum64(acc);
+}
+
+// The same statistics for a chunk whose changes did not fit its slot, from old and new again
+// (512 elements per step, 16 per lane): a lane's first change follows the last change of the
+// nearest lower lane that has one, or of the steps before; its others follow one another.
+template <bool FULL>
+__device__ __noinline__ uint64_t chunk_rice(const uint16_t* __restrict__ old,
+                                            const uint16_t* __restrict__ neu, uint64_t n,
+                                            uint64_t e0, uint32_t* sum0) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t lt = (1u << lane) - 1;
+  int32_t lastp = -1;
+  uint64_t acc = 0;
+  for (int s = 0; s < 8; s++) {
+    const uint32_t eloc = s * 512 + lane * 16;
+    const uint64_t e = e0 + eloc;
+    uint4 o0, o1, n0, n1;
+    if (FULL) {
+      o0 = __ldg(reinterpret_cast<const uint4*>(old + e));
+      o1 = __ldg(reinterpret_cast<const uint4*>(old + e + 8));
+      n0 = __ldg(reinterpret_cast<const uint4*>(neu + e));
+      n1 = __ldg(reinterpret_cast<const uint4*>(neu + e + 8));
+    } else {
+      o0 = load8(old, e, n); o1 = load8(old, e + 8, n);
+      n0 = load8(neu, e, n); n1 = load8(neu, e + 8, n);
+    }
+    const uint32_t nz = nz_mask16(xor4(o0, n0), xor4(o1, n1));
+    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, nz != 0);
+    if (bal == 0) continue;
+    const int32_t last = (int32_t)(eloc + 31 - __clz(nz));   // meaningful where nz != 0
+    const uint32_t lower = bal & lt;
+    const int32_t below = __shfl_sync(0xFFFFFFFFu, last, lower ? 31 - __clz(lower) : 0);
+    int32_t prev = lower ? below : lastp;
+    for (uint32_t bits = nz; bits; bits &= bits - 1) {
+      const int32_t p = (int32_t)(eloc + __ffs(bits) - 1);
+      acc += rice_terms((uint32_t)(p - prev));
+      prev = p;
+    }
+    lastp = __shfl_sync(0xFFFFFFFFu, last, 31 - __clz(bal));
+  }
+  *sum0 = (uint32_t)(lastp + 1);
+  return warp_sum64(acc);
+}
+
+// The compress workspace word of a version-4 chunk with M + R (1..508) changes, from its slot
+// entries or, when they did not fit, from old and new.  One call for both (two calls from the
+// encode loop spilled there).
+template <bool FULL>
+__device__ __noinline__ uint32_t rice_count(const uint32_t* entries, bool overflow,
+                                            const uint16_t* old, const uint16_t* neu, uint64_t n,
+                                            uint64_t e0, uint32_t M, uint32_t R) {
+  uint32_t sum0;
+  uint64_t packed;
+  if (!overflow) packed = slot_rice(entries, M + R, &sum0);
+  else packed = chunk_rice<FULL>(old, neu, n, e0, &sum0);
+  return rice_word(M, R, sum0, packed);
+}
+
+// FMT: the payload kinds of the build -- 0: XOR payloads of versions 1 and 2; 3: version 3 (the
+// chunk's escaped gaps counted) and overwrite payloads of version 2; 4: version 4 (the chunk's
+// Rice statistics gathered, its K and block bytes chosen).
 // OW: slot entries in the general layout (kEntRare | pos << 16 | value) with the new field
 // values (the new value of a rare change, the new mantissa of a mantissa-only one), read back
 // from a per-lane shared copy of the step's new values; otherwise pos << 16 | x (the class
 // follows from x).
-template <bool FULL, bool GEN, bool OW>
+template <bool FULL, int FMT, bool OW>
 __device__ __forceinline__ void encode_chunk(const uint16_t* __restrict__ old,
                                              const uint16_t* __restrict__ neu, uint64_t n,
                                              uint64_t e0, uint32_t* __restrict__ slot,
@@ -226,24 +304,30 @@ __device__ __forceinline__ void encode_chunk(const uint16_t* __restrict__ old,
   const uint32_t runR = __shfl_sync(0xFFFFFFFFu, rl, 31);
   const uint32_t runM = __shfl_sync(0xFFFFFFFFu, nl, 31) - runR;
   const bool overflow = runM + runR > kSlotEntries;
-  uint32_t esc = 0;   // GEN: gaps above 255 in the chunk's merged position list
-  if (GEN && runM + runR <= kCompactMax) {
+  uint32_t word = wcount(runM, runR, 0);
+  if (FMT == 3 && runM + runR <= kCompactMax) {   // gaps above 255 in the merged list
+    uint32_t esc;
     if (!overflow) {
       __syncwarp();   // the slot entries written by every lane are visible to the warp
       esc = slot_escapes(entries, runM + runR);
     } else {
       esc = chunk_escapes<FULL>(old, neu, n, e0);
     }
+    word = wcount(runM, runR, esc);
+  }
+  if (FMT == 4 && runM + runR > 0 && runM + runR <= kCompactMax) {
+    __syncwarp();   // the slot entries written by every lane are visible to the warp
+    word = rice_count<FULL>(entries, overflow, old, neu, n, e0, runM, runR);
   }
   if (lane == 0) {
     slot[0] = overflow ? kSlotOverflow : slot_info(runM, runR);
     slot[1] = fm;
-    counts[g] = wcount(runM, runR, esc);
+    counts[g] = word;
     if (overflow) list[atomicAdd(list_count, 1u)] = (uint32_t)g;
   }
 }
 
-template <bool GEN, bool OW>
+template <int FMT, bool OW>
 __global__ void __launch_bounds__(kThreads, 4)
 k_encode_slots(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
                uint32_t k, uint64_t total_chunks, uint32_t* __restrict__ counts,
@@ -278,10 +362,10 @@ k_encode_slots(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
     }
     uint4* ns = s_ns[OW ? threadIdx.x : 0];
     if (e0 + kChunk <= n)
-      encode_chunk<true, GEN, OW>(jobs[j].old, jobs[j].neu, n, e0, slot, ck, g, counts,
+      encode_chunk<true, FMT, OW>(jobs[j].old, jobs[j].neu, n, e0, slot, ck, g, counts,
                                   list_count, list, s_xs[threadIdx.x], ns);
     else
-      encode_chunk<false, GEN, OW>(jobs[j].old, jobs[j].neu, n, e0, slot, ck, g, counts,
+      encode_chunk<false, FMT, OW>(jobs[j].old, jobs[j].neu, n, e0, slot, ck, g, counts,
                                    list_count, list, s_xs[threadIdx.x], ns);
   }
   if (cur != 0xFFFFFFFFu) {
@@ -401,15 +485,17 @@ __device__ __forceinline__ void store_bitmap(uint8_t* dst, const uint32_t* bm, u
 // Position of the first mantissa value after chunk g (in g's tensor, ending at g_end) and
 // its value, for the last owned byte of g that reaches past g's own values.  `cnt_next` and
 // `aux_next` are the counts and slot aux word of chunk g + 1, already loaded.
+template <bool V4>
 __device__ __forceinline__ uint32_t next_mant_value(uint64_t g, uint64_t g_end, uint32_t cnt_next,
                                                     uint32_t aux_next,
                                                     const uint32_t* __restrict__ counts,
                                                     const uint8_t* __restrict__ slots) {
   const int lane = threadIdx.x & 31;
-  if (g + 1 < g_end && wcount_m(cnt_next) != 0) return aux_next & kMant;
+  if (g + 1 < g_end && (V4 ? v4count_m(cnt_next) : wcount_m(cnt_next)) != 0)
+    return aux_next & kMant;
   for (uint64_t gg = g + 2; gg < g_end; gg += 32) {  // rare: chunks without mantissa values
     const uint64_t q = gg + lane;
-    const bool has = q < g_end && wcount_m(counts[q]) != 0;
+    const bool has = q < g_end && (V4 ? v4count_m(counts[q]) : wcount_m(counts[q])) != 0;
     const uint32_t bal = __ballot_sync(0xFFFFFFFFu, has);
     if (bal) {
       const uint64_t gn = gg + __ffs(bal) - 1;
@@ -467,6 +553,79 @@ __device__ __forceinline__ void compact_batch(uint32_t e, bool valid, CompactSta
   cs.x += __popc(bE);
 }
 
+// Output of a version-4 compact chunk: its block is assembled in shared memory (zeroed words,
+// set by atomic ORs, every field in its own bits) and copied out afterwards.
+struct RiceOut {
+  uint32_t* bits;      // shared: the block, 32-bit words, bit b of the stream = bit b%32 of word b/32
+  uint16_t* rstream;   // R stream at the chunk's first rare value
+  uint8_t* mv;         // shared: the chunk's 7-bit mantissa values by chunk-local rank
+  uint32_t K;          // Rice parameter
+  uint32_t rem0;       // first remainder bit: 9R
+  uint32_t u0;         // first unary bit: 9R + K(M+R)
+};
+struct RiceState {
+  uint32_t prev;       // position of the last change emitted (0xFFFFFFFF before the first)
+  uint32_t i, m, r;    // changes, mantissa-only values, rare values emitted
+  uint32_t z;          // unary bits emitted
+};
+
+// Sets the bits of v (below 2^9) at stream bit `at`: one word, or two when v straddles them.
+__device__ __forceinline__ void or_bits(uint32_t* bits, uint32_t at, uint32_t v) {
+  if (v == 0) return;
+  const uint64_t t = (uint64_t)v << (at & 31);
+  atomicOr(&bits[at >> 5], (uint32_t)t);
+  if (t >> 32) atomicOr(&bits[(at >> 5) + 1], (uint32_t)(t >> 32));
+}
+// Sets the q bits [at, at + q).
+__device__ __forceinline__ void ones_run(uint32_t* bits, uint32_t at, uint32_t q) {
+  while (q > 0) {
+    const uint32_t off = at & 31, take = min(q, 32 - off);
+    atomicOr(&bits[at >> 5], (take == 32 ? 0xFFFFFFFFu : (1u << take) - 1u) << off);
+    at += take;
+    q -= take;
+  }
+}
+
+// Emits the 32 changes rs.i .. rs.i+31 of a version-4 compact chunk in position order, lane l
+// holding change rs.i + l as a slot entry (OW: the general layout; else pos << 16 | x) when
+// `valid` (the valid lanes are a prefix).  Change i with gap g (pos + 1 for the first) puts
+// g mod 2^K at bit 9R + K*i, its quotient g >> K as that many ones ending before its unary
+// zero (the zeros of changes 0..i close the first i+1 unary codes), and, when rare, its index
+// i at bit 9*(its rank among the rare changes).
+template <bool OW>
+__device__ __forceinline__ void rice_batch(uint32_t e, bool valid, RiceState& rs,
+                                           const RiceOut& o) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t lt = (1u << lane) - 1;
+  const uint32_t pos = ent_pos(e), x = e & 0xFFFFu;
+  uint32_t prev = __shfl_up_sync(0xFFFFFFFFu, pos, 1);
+  if (lane == 0) prev = rs.prev;
+  const uint32_t gap = pos - prev;
+  const bool rare = OW ? (e & kEntRare) != 0 : (x & kSignExp) != 0;
+  const bool isR = valid && rare;
+  const bool isM = valid && !rare;
+  const uint32_t bM = __ballot_sync(0xFFFFFFFFu, isM), bR = __ballot_sync(0xFFFFFFFFu, isR);
+  const uint32_t q = valid ? gap >> o.K : 0u;
+  const uint32_t incl = warp_incl_scan(valid ? q + 1 : 0u);   // unary bits up to change i
+  if (valid) {
+    const uint32_t i = rs.i + lane;
+    ones_run(o.bits, o.u0 + rs.z + incl - 1 - q, q);
+    or_bits(o.bits, o.rem0 + o.K * i, gap & ((1u << o.K) - 1u));
+    if (isR) {
+      const uint32_t jr = rs.r + __popc(bR & lt);
+      or_bits(o.bits, kRiceIdxBits * jr, i);
+      o.rstream[jr] = (uint16_t)x;
+    } else {
+      o.mv[rs.m + __popc(bM & lt)] = (uint8_t)(x & kMant);
+    }
+  }
+  rs.prev = __shfl_sync(0xFFFFFFFFu, pos, 31);
+  rs.i += 32;
+  rs.m += __popc(bM);
+  rs.r += __popc(bR);
+  rs.z += __shfl_sync(0xFFFFFFFFu, incl, 31);
+}
+
 // Sets up the output pointers of chunk c (counts M, R, exclusive prefixes Pex / Rex).
 __device__ __forceinline__ void emit_ctx(EmitCtx& cx, uint8_t* payload, const JobInfo& I,
                                          uint32_t M, uint32_t R, uint32_t B, uint64_t Pex,
@@ -484,9 +643,10 @@ __device__ __forceinline__ void emit_ctx(EmitCtx& cx, uint8_t* payload, const Jo
 
 // Chunks whose changes fit their slot: the slot's single position-ordered list is split by
 // class 32 entries at a time with ballots (rank = set lanes below; the previous element of
-// the same class, for the delta, is the nearest such lane below or the carry).  GEN: the
-// general build (version-3 compact blocks); OW: slot entries in the general layout.
-template <bool GEN, bool OW>
+// the same class, for the delta, is the nearest such lane below or the carry).  FMT as in
+// encode_slots: 3 writes version-3 compact blocks, 4 version-4 ones; OW: slot entries in the
+// general layout.
+template <int FMT, bool OW>
 __global__ void __launch_bounds__(kThreads, 4)
 k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
        const uint64_t* __restrict__ tile_start, uint32_t k, uint64_t total_chunks,
@@ -522,6 +682,7 @@ k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
     const uint64_t c = g - chunk_start[j];
     const uint64_t g_job_end = chunk_start[j + 1];
     const TileSum pre = tile_pre[tile_start[j] + c / kTileChunks];
+    constexpr bool GEN = FMT != 0;
     const uint32_t cnt_here = GEN ? counts[g] : 0u;
     const uint32_t cnt_next = g + 1 < g_job_end ? counts[g + 1] : 0u;
     const uint32_t aux_next =
@@ -548,13 +709,32 @@ k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
     const uint32_t B = (L + 7) >> 3;
     const uint64_t Pex = pre.p + lc.x, Mex = pre.m + lc.y, Rex = pre.r + lc.z;
     const uint32_t nesc = wcount_e(cnt_here);
-    const bool compact = GEN && I.version == 3 && choose_compact(M, R, nesc, B);
+    const bool rice = FMT == 4 && I.version == 4 && rice_compact(cnt_here, B);
+    const bool compact = rice || (FMT == 3 && I.version == 3 && choose_compact(M, R, nesc, B));
     if (lane == 0)
       reinterpret_cast<uint32_t*>(payload + count_table_offset(I.r_start, jobs[j].nchunks))[c] =
-          count_entry(GEN ? I.version : 1u, M, R, nesc, compact);
+          rice ? cnt_here : count_entry(GEN ? I.version : 1u, M, R, nesc, compact);
     EmitCtx cx;
     emit_ctx(cx, payload, I, M, R, B, Pex, Rex, sm);
-    if (GEN && compact) {
+    if constexpr (FMT == 4) {
+      if (rice) {
+        cx.listM = cx.listR = true;   // no bitmap
+        const uint32_t nb = (cnt_here >> 21) & 0x3FFu, K = (cnt_here >> 18) & 0x7u;
+        for (uint32_t i = lane; i < (nb + 3) / 4; i += 32) sm->bm[i] = 0;
+        __syncwarp();
+        const RiceOut o{sm->bm, cx.rstream, sm->mv, K, kRiceIdxBits * R,
+                        kRiceIdxBits * R + K * kk};
+        RiceState rs{0xFFFFFFFFu, 0, 0, 0, 0};
+#pragma unroll
+        for (int q = 0; q < 8; q++) {
+          if (32u * q >= kk) break;
+          rice_batch<OW>(ent[q], 32u * q + lane < kk, rs, o);
+        }
+        __syncwarp();
+        store_bitmap(payload + I.p_start + Pex, sm->bm, nb);
+      }
+    }
+    if (FMT == 3 && compact) {
       cx.listM = cx.listR = true;   // no bitmap
       const CompactOut o{payload + I.p_start + Pex,
                          reinterpret_cast<uint16_t*>(payload + I.x_start) + pre.e + lc.w,
@@ -632,7 +812,7 @@ k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
       // from the chunk's first mantissa bit is below 7*M + 8)
       const uint32_t jl_last = (uint32_t)(8 * (b_hi - 1) - 7 * Mex) / 7;
       if (jl_last + 1 == M && Mex + M < I.sum_m)
-        after = next_mant_value(g, g_job_end, cnt_next, aux_next, counts, slots);
+        after = next_mant_value<FMT == 4>(g, g_job_end, cnt_next, aux_next, counts, slots);
       put_mant_bytes(payload + I.m_start, b_lo, b_hi, Mex, M, after, cx);
     }
     if (!cx.listM || !cx.listR) {
@@ -644,11 +824,32 @@ k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
   }
 }
 
+// Emits a version-4 compact chunk from its position-ordered list of changes lst (count word
+// cnt; ow: entries in the general layout) and copies its block to dst.  Called, not inlined:
+// inlined, emit_dense spilled.
+__device__ __noinline__ void emit_rice_list(const uint32_t* lst, uint32_t cnt, bool ow,
+                                            uint16_t* rstream, EmitSmem* sm, uint8_t* dst) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t M = cnt & 0x1FFu, R = (cnt >> 9) & 0x1FFu, kk = M + R;
+  const uint32_t nb = (cnt >> 21) & 0x3FFu, K = (cnt >> 18) & 0x7u;
+  for (uint32_t i = lane; i < (nb + 3) / 4; i += 32) sm->bm[i] = 0;
+  __syncwarp();
+  const RiceOut o{sm->bm, rstream, sm->mv, K, kRiceIdxBits * R, kRiceIdxBits * R + K * kk};
+  RiceState rs{0xFFFFFFFFu, 0, 0, 0, 0};
+  for (uint32_t i0 = 0; i0 < kk; i0 += 32) {
+    const bool valid = i0 + lane < kk;
+    if (ow) rice_batch<true>(valid ? lst[i0 + lane] : 0u, valid, rs, o);
+    else rice_batch<false>(valid ? lst[i0 + lane] : 0u, valid, rs, o);
+  }
+  __syncwarp();
+  store_bitmap(dst, sm->bm, nb);
+}
+
 // Chunks with more changes than a slot holds (listed by encode_slots): the changes are derived
 // again from old and new, 512 elements per step; after each step the mantissa-stream bytes
 // whose two values are known are written and the value window keeps only its last value.
-// A version-3 compact chunk (at most kCompactMax changes) first gathers its changes in
-// position order into a shared list, then emits them 32 at a time as emit does.
+// A compact chunk (at most kCompactMax changes) first gathers its changes in position order
+// into a shared list, then emits them 32 at a time as emit does.
 __global__ void __launch_bounds__(kThreads)
 k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
              const uint64_t* __restrict__ tile_start, uint32_t k,
@@ -677,16 +878,18 @@ k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
     const uint32_t L = (n - e0) < kChunk ? (uint32_t)(n - e0) : kChunk;
     const uint32_t B = (L + 7) >> 3;
     const uint32_t cnt = counts[g];
-    const uint32_t M = wcount_m(cnt), R = wcount_r(cnt), E = wcount_e(cnt);
+    const uint32_t M = v4count_m(cnt), R = v4count_r(cnt);
+    const uint32_t E = I.version == 3 ? wcount_e(cnt) : 0u;
     const TileSum pre = tile_pre[tile_start[j] + c / kTileChunks];
     const uint4 lc = loc[g];
     const uint64_t Pex = pre.p + lc.x, Mex = pre.m + lc.y, Rex = pre.r + lc.z;
-    const bool compact = I.version == 3 && choose_compact(M, R, E, B);
+    const bool rice = I.version == 4 && rice_compact(cnt, B);
+    const bool compact = rice || (I.version == 3 && choose_compact(M, R, E, B));
     const bool ow = (J.flags & kFlagOverwrite) != 0;
     uint8_t* payload = J.payload;
     if (lane == 0)
       reinterpret_cast<uint32_t*>(payload + count_table_offset(I.r_start, jobs[j].nchunks))[c] =
-          count_entry(I.version, M, R, E, compact);
+          rice ? cnt : count_entry(I.version, M, R, E, compact);
     EmitCtx cx;
     emit_ctx(cx, payload, I, M, R, B, Pex, Rex, sm);
     if (compact) cx.listM = cx.listR = true;   // no bitmap
@@ -728,14 +931,18 @@ k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
       }
       __syncwarp();
       const uint32_t kk = M + R;
-      const CompactOut o{payload + I.p_start + Pex,
-                         reinterpret_cast<uint16_t*>(payload + I.x_start) + pre.e + lc.w,
-                         cx.rstream, sm->mv, kk};
-      CompactState cs{0xFFFFFFFFu, 0, 0, 0, 0};
-      for (uint32_t i0 = 0; i0 < kk; i0 += 32) {
-        const bool valid = i0 + lane < kk;
-        if (ow) compact_batch<true>(valid ? lst[i0 + lane] : 0u, valid, cs, o);
-        else compact_batch<false>(valid ? lst[i0 + lane] : 0u, valid, cs, o);
+      if (rice) {
+        emit_rice_list(lst, cnt, ow, cx.rstream, sm, payload + I.p_start + Pex);
+      } else {
+        const CompactOut o{payload + I.p_start + Pex,
+                           reinterpret_cast<uint16_t*>(payload + I.x_start) + pre.e + lc.w,
+                           cx.rstream, sm->mv, kk};
+        CompactState cs{0xFFFFFFFFu, 0, 0, 0, 0};
+        for (uint32_t i0 = 0; i0 < kk; i0 += 32) {
+          const bool valid = i0 + lane < kk;
+          if (ow) compact_batch<true>(valid ? lst[i0 + lane] : 0u, valid, cs, o);
+          else compact_batch<false>(valid ? lst[i0 + lane] : 0u, valid, cs, o);
+        }
       }
     }
     for (int s = 0; s < 8 && !compact; s++) {
@@ -774,7 +981,8 @@ k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
         const uint32_t cnt_next = g + 1 < g_job_end ? counts[g + 1] : 0u;
         const uint32_t aux_next =
             g + 1 < g_job_end ? reinterpret_cast<const uint32_t*>(slots + (g + 1) * kSlotBytes)[1] : 0u;
-        after = next_mant_value(g, g_job_end, cnt_next, aux_next, counts, slots);
+        // (the reader of both count-word layouts: versions 1 to 3 never set bit 31)
+        after = next_mant_value<true>(g, g_job_end, cnt_next, aux_next, counts, slots);
       }
       put_mant_bytes(mout, b_next, b_hi, Mex, M, after, cx);
     }
@@ -803,15 +1011,29 @@ uint64_t cap_grid(uint64_t want, uint64_t work_items_per_block, uint64_t items) 
 
 }  // namespace
 
-cudaError_t launch_encode_slots(const LaunchCtx& c, bool general, bool overwrite) {
+// The build of a compress kernel for the payload kind (fmt 0, 3 or 4 and overwrite), with its
+// blocks per SM.
+template <typename K>
+struct Builds {
+  K k[5];   // <0,false> <3,false> <3,true> <4,false> <4,true>
+  int per_sm[5];
+  int pick(uint32_t fmt, bool overwrite) const {
+    return fmt == 4 ? (overwrite ? 4 : 3) : (overwrite ? 2 : fmt == 3 ? 1 : 0);
+  }
+};
+
+cudaError_t launch_encode_slots(const LaunchCtx& c, uint32_t fmt, bool overwrite) {
   if (c.chunks == 0) return cudaSuccess;
-  static const int per_sm = blocks_per_sm(k_encode_slots<false, false>, kThreads);
-  static const int per_sm_g = blocks_per_sm(k_encode_slots<true, false>, kThreads);
-  static const int per_sm_o = blocks_per_sm(k_encode_slots<true, true>, kThreads);
-  const int bps = overwrite ? per_sm_o : general ? per_sm_g : per_sm;
-  const uint64_t grid = cap_grid((uint64_t)bps * c.sms, kWarps, c.chunks);
-  auto kernel = overwrite ? k_encode_slots<true, true>
-                          : general ? k_encode_slots<true, false> : k_encode_slots<false, false>;
+  using KT = decltype(&k_encode_slots<0, false>);
+  static const Builds<KT> b = [] {
+    Builds<KT> r{{k_encode_slots<0, false>, k_encode_slots<3, false>, k_encode_slots<3, true>,
+                  k_encode_slots<4, false>, k_encode_slots<4, true>}, {}};
+    for (int i = 0; i < 5; i++) r.per_sm[i] = blocks_per_sm(r.k[i], kThreads);
+    return r;
+  }();
+  const int w = b.pick(fmt, overwrite);
+  const uint64_t grid = cap_grid((uint64_t)b.per_sm[w] * c.sms, kWarps, c.chunks);
+  auto kernel = b.k[w];
   kernel<<<(unsigned)grid, kThreads, 0, c.stream>>>(
       reinterpret_cast<const CJob*>(c.ws + c.lay.jobs),
       reinterpret_cast<const uint64_t*>(c.ws + c.lay.chunk_start), c.k, c.chunks,
@@ -838,14 +1060,18 @@ cudaError_t launch_emit_dense(const LaunchCtx& c) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_emit(const LaunchCtx& c, bool general, bool overwrite) {
+cudaError_t launch_emit(const LaunchCtx& c, uint32_t fmt, bool overwrite) {
   if (c.chunks == 0) return cudaSuccess;
-  static const int per_sm = blocks_per_sm(k_emit<false, false>, kThreads);
-  static const int per_sm_g = blocks_per_sm(k_emit<true, false>, kThreads);
-  static const int per_sm_o = blocks_per_sm(k_emit<true, true>, kThreads);
-  const int bps = overwrite ? per_sm_o : general ? per_sm_g : per_sm;
-  const uint64_t grid = cap_grid((uint64_t)bps * c.sms, kWarps, c.chunks);
-  auto kernel = overwrite ? k_emit<true, true> : general ? k_emit<true, false> : k_emit<false, false>;
+  using KT = decltype(&k_emit<0, false>);
+  static const Builds<KT> b = [] {
+    Builds<KT> r{{k_emit<0, false>, k_emit<3, false>, k_emit<3, true>, k_emit<4, false>,
+                  k_emit<4, true>}, {}};
+    for (int i = 0; i < 5; i++) r.per_sm[i] = blocks_per_sm(r.k[i], kThreads);
+    return r;
+  }();
+  const int w = b.pick(fmt, overwrite);
+  const uint64_t grid = cap_grid((uint64_t)b.per_sm[w] * c.sms, kWarps, c.chunks);
+  auto kernel = b.k[w];
   kernel<<<(unsigned)grid, kThreads, 0, c.stream>>>(
       reinterpret_cast<const CJob*>(c.ws + c.lay.jobs),
       reinterpret_cast<const uint64_t*>(c.ws + c.lay.chunk_start),

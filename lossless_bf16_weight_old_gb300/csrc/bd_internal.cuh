@@ -124,13 +124,58 @@ constexpr uint32_t kEntRare = 0x80000000u;
 __host__ __device__ __forceinline__ uint32_t ent_pos(uint32_t e) { return (e >> 16) & 0xFFFu; }
 
 // Compress workspace word of a chunk's counts: M in bits 0..12, R in 13..25, E (gaps above 255
-// in the merged position list, counted only for version 3) in 26..30.
+// in the merged position list, counted only for version 3) in 26..30, bit 31 clear.  Version 4
+// writes a chunk of 1..508 changes whose Rice block fits in 1023 bytes as the compact count
+// entry it would have (bit 31 set, M, R, K, block bytes); the scan keeps it compact when the
+// block is smaller than the version-1 blocks.  The wcount_* readers take the first layout
+// only; the v4count_* readers take both.
 __host__ __device__ __forceinline__ uint32_t wcount(uint32_t M, uint32_t R, uint32_t E) {
   return M | (R << 13) | (E << 26);
 }
 __host__ __device__ __forceinline__ uint32_t wcount_m(uint32_t v) { return v & 0x1FFFu; }
 __host__ __device__ __forceinline__ uint32_t wcount_r(uint32_t v) { return (v >> 13) & 0x1FFFu; }
 __host__ __device__ __forceinline__ uint32_t wcount_e(uint32_t v) { return (v >> 26) & 0x1Fu; }
+__host__ __device__ __forceinline__ uint32_t v4count_m(uint32_t v) {
+  return (v & kCompactFlag) ? v & 0x1FFu : v & 0x1FFFu;
+}
+__host__ __device__ __forceinline__ uint32_t v4count_r(uint32_t v) {
+  return (v & kCompactFlag) ? (v >> 9) & 0x1FFu : (v >> 13) & 0x1FFFu;
+}
+// Version 4: whether the chunk (bitmap bytes B) is coded compactly.
+__host__ __device__ __forceinline__ bool rice_compact(uint32_t v, uint32_t B) {
+  if ((v & kCompactFlag) == 0) return false;
+  const uint32_t M = v & 0x1FFu, R = (v >> 9) & 0x1FFu;
+  return ((v >> 21) & 0x3FFu) < block_bytes(M, B) + block_bytes(R, B);
+}
+
+// Sums over a chunk's gaps of g >> K for K = 1..7, packed in one u64: fields of 12, 11, 10, 9,
+// 8, 7 and 6 bits at bits 0, 12, 23, 33, 42, 50 and 57.  The gaps of a chunk add up to its last
+// position + 1 <= 4096, so the sum for K is at most 4096 >> K and no field carries into the next.
+__device__ __forceinline__ uint64_t rice_terms(uint32_t g) {
+  return (uint64_t)(g >> 1) | ((uint64_t)(g >> 2) << 12) | ((uint64_t)(g >> 3) << 23) |
+         ((uint64_t)(g >> 4) << 33) | ((uint64_t)(g >> 5) << 42) | ((uint64_t)(g >> 6) << 50) |
+         ((uint64_t)(g >> 7) << 57);
+}
+// The compress workspace word of a version-4 chunk with M + R changes: sum0 = the sum of the
+// gaps (last position + 1), packed = their rice_terms.  K takes the fewest bits
+// (9R + K(M+R) + (M+R) + sum of g >> K), the smallest K on a tie.
+__device__ __forceinline__ uint32_t rice_word(uint32_t M, uint32_t R, uint32_t sum0,
+                                              uint64_t packed) {
+  const uint32_t k = M + R;
+  if (k == 0 || k > kCompactMax) return wcount(M, R, 0);
+  constexpr uint32_t off[8] = {0, 0, 12, 23, 33, 42, 50, 57};
+  constexpr uint32_t wid[8] = {0, 12, 11, 10, 9, 8, 7, 6};
+  uint32_t bestK = 0, best = k + sum0;
+#pragma unroll
+  for (uint32_t K = 1; K < 8; K++) {
+    const uint32_t s = (uint32_t)(packed >> off[K]) & ((1u << wid[K]) - 1u);
+    const uint32_t bits = K * k + k + s;
+    if (bits < best) { best = bits; bestK = K; }
+  }
+  const uint32_t nb = (9 * R + best + 7) / 8;
+  if (nb > 1023) return wcount(M, R, 0);
+  return kCompactFlag | M | (R << 9) | (bestK << 18) | (nb << 21);
+}
 
 // SplitMix64 output function (Steele, Lea & Flood 2014) applied to a position-keyed word.
 __device__ __forceinline__ uint64_t mix64(uint64_t z) {
@@ -420,10 +465,12 @@ struct LaunchCtx {
   uint64_t tiles;      // total scan tiles
 };
 
-cudaError_t launch_encode_slots(const LaunchCtx& c, bool general, bool overwrite);
+// fmt: 0 (XOR payloads of versions 1 and 2), 3 (version 3, and overwrite payloads of version
+// 2), 4 (version 4); overwrite: the payloads carry new values.
+cudaError_t launch_encode_slots(const LaunchCtx& c, uint32_t fmt, bool overwrite);
 cudaError_t launch_scan_tiles(const LaunchCtx& c, bool decompress);
 cudaError_t launch_scan_jobs(const LaunchCtx& c, bool decompress, int32_t* d_status_all);
-cudaError_t launch_emit(const LaunchCtx& c, bool general, bool overwrite);
+cudaError_t launch_emit(const LaunchCtx& c, uint32_t fmt, bool overwrite);
 cudaError_t launch_emit_dense(const LaunchCtx& c);
 cudaError_t launch_apply_chunks(const LaunchCtx& c);
 cudaError_t launch_apply_incremental(const LaunchCtx& c);

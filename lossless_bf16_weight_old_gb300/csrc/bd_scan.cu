@@ -5,7 +5,7 @@
 // P_c (two version-1 blocks, or a compact block of version 3 or 4), mantissa-only count M_c, rare
 // count R_c and escaped gaps E_c (X-stream values of a compact block, else 0).
 //   scan_tiles  one CTA per tile of 1024 chunks: per-chunk prefix inside the tile, tile total.
-//               Compress decides here which chunks of a version-3 payload are compact.  For
+//               Compress decides here which chunks of a version-3 or -4 payload are compact.  For
 //               decompress the counts come from the untrusted payload, so it also checks
 //               that the count table lies inside the payload, that each entry is well formed
 //               for the version and that M_c + R_c <= L_c.
@@ -98,8 +98,15 @@ k_scan_tiles(const void* __restrict__ jobs, const uint64_t* __restrict__ tile_st
         } else {
           cc.M = wcount_m(v);
           cc.R = wcount_r(v);
-          cc.compact = version == 3 && choose_compact(cc.M, cc.R, wcount_e(v), B);
-          cc.E = cc.compact ? wcount_e(v) : 0;
+          if (version == 4) {
+            cc.M = v4count_m(v);
+            cc.R = v4count_r(v);
+            cc.compact = cc.rice = rice_compact(v, B);
+            cc.nb = (v >> 21) & 0x3FFu;
+          } else {
+            cc.compact = version == 3 && choose_compact(cc.M, cc.R, wcount_e(v), B);
+            cc.E = cc.compact ? wcount_e(v) : 0;
+          }
         }
         vM[i] = cc.M;
         vR[i] = cc.R;

@@ -171,16 +171,44 @@ def test_payload_info_reports_overwrite_flag(cuda_lib):
         assert cuda_lib.bd_payload_info(b, 80, ctypes.byref(info)) == 3
 
 
+def test_payload_info_parses_version_4_headers(cuda_lib):
+    rng = np.random.default_rng(15)
+    old = rng.integers(0, 1 << 16, 5 * 4096 + 9).astype(np.uint16)
+    new = old.copy()
+    new[:3 * 4096:37] ^= np.uint16(3)
+    new[4096:2 * 4096:700] ^= np.uint16(0x8001)
+    info = _lib.PayloadInfo()
+    for ow in (False, True):
+        p, _ = oracle.encode(old, new, base=99, rice=True, overwrite=ow)
+        table = p[80:80 + 4 * 6].view(np.uint32)
+        assert ((table >> 31) == 1).any()
+        h = (ctypes.c_uint8 * 80).from_buffer_copy(p[:80].tobytes())
+        assert cuda_lib.bd_payload_info(h, 80, ctypes.byref(info)) == 0
+        assert info.version == 4 and info.base_checksum == 99 and info.n_escapes == 0
+        assert info.total_size == p.size and info.flags == int(ow)
+        # no X stream: the total is exactly the sections
+        bad = bytearray(p[:80].tobytes())
+        bad[56:64] = (p.size + 2).to_bytes(8, "little")
+        b = (ctypes.c_uint8 * 80).from_buffer_copy(bytes(bad))
+        assert cuda_lib.bd_payload_info(b, 80, ctypes.byref(info)) == 3
+    bad = bytearray(p[:80].tobytes())
+    bad[8] = 5
+    b = (ctypes.c_uint8 * 80).from_buffer_copy(bytes(bad))
+    assert cuda_lib.bd_payload_info(b, 80, ctypes.byref(info)) == 3
+
+
 def test_version_3_bound(cuda_lib):
-    """bd_compress_bound covers version 3: never longer than version 2 of the same update."""
+    """bd_compress_bound covers versions 3 and 4: never longer than version 2 of the same
+    update."""
     rng = np.random.default_rng(13)
     for n in (1, 4097, 3 * 4096 + 5):
         old = rng.integers(0, 1 << 16, n).astype(np.uint16)
         for rate in (0.001, 0.05, 0.5, 1.0):
             new = old ^ np.where(rng.random(n) < rate, rng.integers(1, 1 << 16, n), 0).astype(np.uint16)
             p3, _ = oracle.encode(old, new, base=1, compact=True)
+            p4, _ = oracle.encode(old, new, base=1, rice=True)
             p2, _ = oracle.encode(old, new, base=1)
-            assert p3.size <= p2.size <= cuda_lib.bd_compress_bound(n)
+            assert max(p3.size, p4.size) <= p2.size <= cuda_lib.bd_compress_bound(n)
 
 
 def test_argument_checks_need_no_gpu(cuda_lib):
@@ -203,8 +231,8 @@ def test_argument_checks_need_no_gpu(cuda_lib):
     assert cuda_lib.bd_decompress(ctypes.c_void_p(1 << 20), 1000, ctypes.c_void_p(1 << 24),
                                   100, dummy, ctypes.c_void_p((1 << 20) + 16),
                                   ctypes.c_void_p(1 << 26), 1 << 20, dummy, None) == 1
-    # the versioned compress takes format 2 or 3 only, optionally with the overwrite bit
-    for fmt in (0, 1, 4, 0x102 | 0x200, 0x101, 0x104):
+    # the versioned compress takes format 2, 3 or 4 only, optionally with the overwrite bit
+    for fmt in (0, 1, 5, 0x102 | 0x200, 0x101, 0x105):
         assert cuda_lib.bd_compress_versioned(dummy, dummy, 10, ctypes.c_void_p(1 << 20), 100,
                                               ctypes.c_void_p(1 << 24), 1 << 20, dummy, dummy,
                                               dummy, fmt, None, None) == 1

@@ -3,8 +3,8 @@
 Every call enqueues its work on the given stream without synchronising the host (the tensor
 table travels as kernel parameters), so a compress and the applies that follow can be captured
 once and replayed: an update loop then costs one graph launch per phase.  Replays must give the
-oracle's payload bytes and restore the weights exactly, in both directions, for version 1 and
-version 3 payloads, with the full and with the incremental apply.
+oracle's payload bytes and restore the weights exactly, in both directions, for payloads of
+versions 1, 3 and 4, with the full and with the incremental apply.
 """
 import numpy as np
 import pytest
@@ -44,16 +44,17 @@ def _capture(fn, stream):
     return g
 
 
-@pytest.mark.parametrize("compact", [False, True])
-def test_compress_and_applies_replayed_from_graphs(compact):
+@pytest.mark.parametrize("version", [1, 3, 4])
+def test_compress_and_applies_replayed_from_graphs(version):
     pairs = _pairs()
     olds = [from_np_u16(p[0]) for p in pairs]
     news = [from_np_u16(p[1]) for p in pairs]
     cks_old = [oracle.checksum(p[0]) for p in pairs]
-    refs = [oracle.encode(o, nw, base=cks_old[i], compact=True) if compact else oracle.encode(o, nw)
+    fmt = {1: {}, 3: dict(compact=True), 4: dict(rice=True)}[version]
+    refs = [oracle.encode(o, nw, base=cks_old[i], **fmt) if fmt else oracle.encode(o, nw)
             for i, (o, nw) in enumerate(pairs)]
     ck_old_t = bd._u64_tensor(cks_old, "cuda")
-    kw = dict(base_checksums=ck_old_t, compact=True) if compact else {}
+    kw = dict(base_checksums=ck_old_t, **fmt) if fmt else {}
     comp = bd.CompressBatch(olds, news, **kw)
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())

@@ -289,3 +289,152 @@ def test_rice_on_bf16_workload_tensor(clustered):
     assert ref.size < ref3.size
     got = _statuses(o, ref, ck, base)
     assert got == (oracle.OK, oracle.OK, oracle.OK)
+
+
+# ---- compress (format 4) -------------------------------------------------------------------
+
+def _compress4(o, nw, base, overwrite=False):
+    old, new = from_np_u16(o), from_np_u16(nw)
+    payload, size, ck, st = bd.compress(old, new, base_checksum=base, rice=True,
+                                        overwrite=overwrite)
+    torch.cuda.synchronize()
+    assert int(st.item()) == bd.OK
+    return old, new, payload, int(size.item()), bd.u64(ck)[0]
+
+
+@pytest.mark.parametrize("overwrite", [False, True])
+@pytest.mark.parametrize("n", [1, 5, 4095, 4096, 4097, 3 * 4096 + 77, 40 * 4096 + 13])
+@pytest.mark.parametrize("rate", [0.0, 0.00085, 0.003, 0.02, 0.05, 0.09, 0.12, 0.3, 1.0])
+def test_compress_writes_the_oracle_bytes(n, rate, overwrite):
+    o, nw = _pair(n, rate, seed=n * 11 + int(rate * 1e5), rare=0.05)
+    base = oracle.checksum(o)
+    ref, ck_ref = oracle.encode(o, nw, base=base, rice=True, overwrite=overwrite)
+    old, new, payload, size, ck = _compress4(o, nw, base, overwrite)
+    assert size == ref.size and ck == ck_ref
+    assert np.array_equal(payload[:size].cpu().numpy(), ref)
+    w = old.clone()
+    st, ck2 = bd.decompress_incremental(w, payload, size, base, bd._u64_tensor([ck], "cuda"))
+    torch.cuda.synchronize()
+    assert int(st.item()) == bd.OK and bd.u64(ck2)[0] == ck_ref
+    assert torch.equal(w.view(torch.int16), new.view(torch.int16))
+
+
+def test_every_chunk_coding_appears():
+    """Chunks that stay plain, compact chunks within a compress slot (<= 252 changes), compact
+    chunks beyond it (253..508, emitted by the dense path) and chunks too dense for a block."""
+    parts, rates = [], [0.0005, 0.02, 0.09, 0.4]
+    for i, r in enumerate(rates):
+        parts.append(_pair(8 * 4096, r, seed=200 + i))
+    o = np.concatenate([p[0] for p in parts])
+    nw = np.concatenate([p[1] for p in parts])
+    base = oracle.checksum(o)
+    for overwrite in (False, True):
+        ref, _ = oracle.encode(o, nw, base=base, rice=True, overwrite=overwrite)
+        C = (o.size + 4095) // 4096
+        table = ref[80:80 + 4 * C].view(np.uint32)
+        compact = (table >> 31) == 1
+        k = np.where(compact, (table & 0x1FF) + ((table >> 9) & 0x1FF), 0)
+        assert (~compact).any() and (compact & (k <= 252)).any() and (compact & (k > 252)).any()
+        _, _, payload, size, _ = _compress4(o, nw, base, overwrite)
+        assert np.array_equal(payload[:size].cpu().numpy(), ref)
+
+
+def test_gap_extremes():
+    """Single changes at the chunk's end (first gap 4096), gaps at powers of two around every
+    K, a chunk of exactly 508 changes and one of 509, rare-only and mantissa-only chunks."""
+    n = 10 * 4096 + 100
+    rng = np.random.default_rng(31)
+    o = rng.integers(0, 1 << 16, n, dtype=np.uint16)
+    nw = o.copy()
+    nw[4095] ^= 0x0001
+    p = 4096
+    for g in (1, 2, 3, 4, 7, 8, 15, 16, 31, 32, 63, 64, 127, 128, 255, 256, 511, 512, 1023):
+        p += g
+        nw[p] ^= 0x8001 if g % 3 == 0 else 0x0011
+    for c, k in ((2, 508), (3, 509)):
+        pos = np.sort(rng.choice(4096, k, replace=False)) + c * 4096
+        nw[pos] ^= 0x0003
+    nw[4 * 4096:5 * 4096:97] ^= 0x8000                     # rare only
+    nw[5 * 4096 + 1:6 * 4096:53] ^= 0x0040                 # mantissa only
+    nw[6 * 4096 + 5:6 * 4096 + 300] ^= 0x0002              # a run of 295
+    nw[9 * 4096 + 7] ^= 0x0100                             # tail chunk of 4096 too
+    nw[n - 1] ^= 0x0005                                    # and the ragged last chunk
+    base = oracle.checksum(o)
+    for overwrite in (False, True):
+        ref, ck_ref = oracle.encode(o, nw, base=base, rice=True, overwrite=overwrite)
+        old, new, payload, size, ck = _compress4(o, nw, base, overwrite)
+        assert size == ref.size and ck == ck_ref
+        assert np.array_equal(payload[:size].cpu().numpy(), ref)
+        out = torch.empty_like(old)
+        st = bd.decompress(old, payload, size, bd._u64_tensor([ck], "cuda"), out=out)
+        torch.cuda.synchronize()
+        assert int(st.item()) == bd.OK
+        assert torch.equal(out.view(torch.int16), new.view(torch.int16))
+
+
+def test_rice_compress_batch():
+    sizes = [5, 4096 * 10, 12345, 70001, 4096 * 3]
+    rates = [0.3, 0.02, 1.0, 0.05, 0.1]
+    pairs = [_pair(n, r, seed=240 + i) for i, (n, r) in enumerate(zip(sizes, rates))]
+    olds = [from_np_u16(p[0]) for p in pairs]
+    news = [from_np_u16(p[1]) for p in pairs]
+    cks_old = [oracle.checksum(p[0]) for p in pairs]
+    for overwrite in (False, True):
+        b4 = bd.CompressBatch(olds, news, base_checksums=bd._u64_tensor(cks_old, "cuda"),
+                              rice=True, overwrite=overwrite)
+        b4.run()
+        torch.cuda.synchronize()
+        assert int(b4.status.item()) == bd.OK
+        s4 = [int(v) for v in b4.sizes.tolist()]
+        for i, (o, nw) in enumerate(pairs):
+            ref, _ = oracle.encode(o, nw, base=cks_old[i], rice=True, overwrite=overwrite)
+            assert np.array_equal(b4.payloads[i][:s4[i]].cpu().numpy(), ref), i
+        ws = [o.clone() for o in olds]
+        inc = bd.IncrementalBatch(ws, b4.payloads, s4, bd._u64_tensor(cks_old, "cuda"),
+                                  b4.checksums)
+        inc.run()
+        torch.cuda.synchronize()
+        assert int(inc.status.item()) == bd.OK
+        for i in range(len(sizes)):
+            assert torch.equal(ws[i].view(torch.int16), news[i].view(torch.int16)), i
+
+
+def test_compress_on_bf16_workload_tensor():
+    old, new = W.make_pair(W.Spec("t", (4096 * 64 + 300,), rate=0.02, tid=79), device="cuda")
+    old, new = old.reshape(-1), new.reshape(-1)
+    o, nw = to_np_u16(old), to_np_u16(new)
+    base = oracle.checksum(o)
+    ref, ck_ref = oracle.encode(o, nw, base=base, rice=True)
+    payload, size, ck, st = bd.compress(old, new, base_checksum=base, rice=True)
+    torch.cuda.synchronize()
+    assert int(st.item()) == bd.OK and int(size.item()) == ref.size
+    assert np.array_equal(payload[:ref.size].cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("overwrite", [False, True])
+def test_full_size_1gib_and_sweep_workloads(overwrite):
+    """The 1 GiB N(0,1) tensor (about 22% changed) and the 14336x4096 tensor at every rate of
+    the sweep, in version 4: bytes identical to the oracle's, and every apply restores."""
+    for spec in W.dense1g() + W.sweep14336():
+        old, new = W.make_pair(spec, device="cuda")
+        old, new = old.reshape(-1), new.reshape(-1)
+        o, nw = to_np_u16(old), to_np_u16(new)
+        base = oracle.checksum(o)
+        ref, ck_ref = oracle.encode(o, nw, base=base, rice=True, overwrite=overwrite)
+        payload, size, ck, st = bd.compress(old, new, base_checksum=base, rice=True,
+                                            overwrite=overwrite)
+        torch.cuda.synchronize()
+        assert int(st.item()) == bd.OK, spec.name
+        size = int(size.item())
+        assert size == ref.size and bd.u64(ck)[0] == ck_ref, spec.name
+        assert np.array_equal(payload[:size].cpu().numpy(), ref), spec.name
+        w = old.clone()
+        st2 = bd.decompress(w, payload, size, ck, out=w)
+        w2 = old.clone()
+        st3, ck3 = bd.decompress_incremental(w2, payload, size, base, ck)
+        torch.cuda.synchronize()
+        assert int(st2.item()) == bd.OK and int(st3.item()) == bd.OK, spec.name
+        assert bd.u64(ck3)[0] == ck_ref, spec.name
+        assert torch.equal(w.view(torch.int16), new.view(torch.int16)), spec.name
+        assert torch.equal(w2.view(torch.int16), new.view(torch.int16)), spec.name
+        del old, new, w, w2, payload
