@@ -37,10 +37,14 @@ constexpr int kWarps = kThreads / 32;
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 // Words of a warp's staging area for a version-4 block: the block (at most 1023 bytes, 256
-// words) and a zero guard word, then the 512-bit class bitmap of the merged list.
+// words) and a zero guard word, the 512-bit class bitmap of the merged list, the first 128
+// mantissa-only values (bytes) and the first 32 rare values (u16) of the chunk.
 constexpr uint32_t kRiceCls = 260;
-constexpr uint32_t kRiceWords = kRiceCls + 16;
+constexpr uint32_t kRiceMv = kRiceCls + 16;
+constexpr uint32_t kRiceRv = kRiceMv + 32;
+constexpr uint32_t kRiceWords = kRiceRv + 16;
 
+template <int PRE>
 __device__ __forceinline__ bool decode_rice(const uint8_t* __restrict__ blk, uint32_t nb,
                                             uint32_t K, const uint8_t* __restrict__ mbytes,
                                             uint32_t s0, const uint16_t* __restrict__ rvals,
@@ -54,7 +58,7 @@ __device__ __noinline__ bool decode_rice_call(const uint8_t* blk, uint32_t nb, u
                                               const uint8_t* mbytes, uint32_t s0,
                                               const uint16_t* rvals, uint32_t M, uint32_t R,
                                               uint32_t L, bool ow, uint32_t* sw, uint32_t* ent) {
-  return decode_rice(blk, nb, K, mbytes, s0, rvals, M, R, L, ow, sw, ent);
+  return decode_rice<4>(blk, nb, K, mbytes, s0, rvals, M, R, L, ow, sw, ent);
 }
 
 // 7-bit value j of an M stream.  The caller guarantees j < number of M values, so the
@@ -662,7 +666,10 @@ __device__ __forceinline__ bool decode_compact(const uint8_t* __restrict__ blk,
 // rare indices strictly ascend below k; k zeros in the unary section; the bits used end in
 // the block's last byte and the pad bits after them are zero (the ones of the section are
 // exactly the quotients' ones); every gap is at least 1 and every position below L; the value
-// rules of apply_chunks.  Returns whether the chunk is malformed (the same on every lane).
+// rules of apply_chunks.  The first 32*PRE mantissa-only values and, when PRE > 0, the first
+// 32 rare values are requested with the block (PRE <= 4).  Returns whether the chunk is
+// malformed (the same on every lane).
+template <int PRE>
 __device__ __forceinline__ bool decode_rice(const uint8_t* __restrict__ blk, uint32_t nb,
                                             uint32_t K, const uint8_t* __restrict__ mbytes,
                                             uint32_t s0, const uint16_t* __restrict__ rvals,
@@ -673,6 +680,23 @@ __device__ __forceinline__ bool decode_rice(const uint8_t* __restrict__ blk, uin
   const uint32_t lt = (1u << lane) - 1;
   const uint32_t k = M + R, nbits = 8 * nb, nw = (nb + 3) >> 2;   // nw <= 256
   uint32_t* __restrict__ cls = sw + kRiceCls;
+  uint8_t* __restrict__ smv = reinterpret_cast<uint8_t*>(sw + kRiceMv);
+  uint16_t* __restrict__ srv = reinterpret_cast<uint16_t*>(sw + kRiceRv);
+  // the first 128 mantissa-only and 32 rare values are requested with the block, so that the
+  // whole decode waits for one round of loads
+  constexpr int NQ = PRE > 0 ? PRE : 1;   // (arrays of size 0 are not allowed)
+  uint32_t mraw[NQ];
+#pragma unroll
+  for (int q = 0; q < PRE; q++) {
+    const uint32_t m = 32 * q + lane;
+    mraw[q] = 0;
+    if (m < M) {
+      const uint32_t bit = s0 + 7 * m;
+      mraw[q] = mbytes[bit >> 3];
+      if ((bit & 7) > 1) mraw[q] |= (uint32_t)mbytes[(bit >> 3) + 1] << 8;
+    }
+  }
+  const uint32_t rv0 = PRE > 0 && (uint32_t)lane < R ? (uint32_t)rvals[lane] : 0u;
   // the block as little-endian words, bytes past it zero, and the guard word
   for (uint32_t i = lane; i <= nw; i += 32) {
     uint32_t v = 0;
@@ -682,6 +706,10 @@ __device__ __forceinline__ bool decode_rice(const uint8_t* __restrict__ blk, uin
     sw[i] = v;
   }
   if (lane < 16) cls[lane] = 0;
+#pragma unroll
+  for (int q = 0; q < PRE; q++)
+    smv[32 * q + lane] = (uint8_t)((mraw[q] >> ((s0 + 7 * (32 * q + lane)) & 7)) & kMant);
+  if (PRE > 0) srv[lane] = (uint16_t)rv0;
   __syncwarp();
   // nbits-bit field at bit `at` of the block (at < 32 * nw, so the second word exists)
   auto field = [&](uint32_t at, uint32_t bits) -> uint32_t {
@@ -705,26 +733,43 @@ __device__ __forceinline__ bool decode_rice(const uint8_t* __restrict__ blk, uin
     }
     last = __shfl_sync(kFull, idx, 31);
   }
-  // the unary section [fixed, nbits) in 32-bit windows, one per lane: zero offsets by rank
+  // the unary section [fixed, nbits): the offsets of its zeros by rank into ent, and the count
+  // of its ones.  A short section is read 32 bits at a time, the same word on every lane (lane
+  // l ranks bit l); a long one (over 12 words, only in dense chunks) one word per lane, each
+  // lane listing the zeros of its word.
   const uint32_t nwin = (nbits - fixed + 31) >> 5;
   uint32_t zeros = 0, ones = 0;
-  for (uint32_t t0 = 0; t0 < nwin; t0 += 32) {
-    const uint32_t t = t0 + lane;
-    uint32_t zm = 0;
-    if (t < nwin) {
-      const uint32_t at = fixed + 32 * t, avail = nbits - at;
+  if (nwin <= 12) {
+    for (uint32_t at = fixed; at < nbits; at += 32) {
+      const uint32_t avail = nbits - at;
       const uint32_t valid = avail >= 32 ? 0xFFFFFFFFu : (1u << avail) - 1u;
       const uint32_t wd = at >> 5;
       const uint32_t win = __funnelshift_r(sw[wd], sw[wd + 1], at & 31);
-      zm = ~win & valid;
+      const uint32_t zm = ~win & valid;
       ones += __popc(win & valid);
+      const uint32_t r = zeros + __popc(zm & lt);
+      if (((zm >> lane) & 1u) && r < k) ent[r] = at - fixed + lane;
+      zeros += __popc(zm);
     }
-    const uint32_t cz = __popc(zm), incl = warp_incl_scan(cz);
-    uint32_t r = zeros + incl - cz;
-    for (; zm != 0 && r < k; zm &= zm - 1, r++) ent[r] = 32 * t + __ffs(zm) - 1;
-    zeros += __shfl_sync(kFull, incl, 31);
+  } else {
+    for (uint32_t t0 = 0; t0 < nwin; t0 += 32) {
+      const uint32_t t = t0 + lane;
+      uint32_t zm = 0;
+      if (t < nwin) {
+        const uint32_t at = fixed + 32 * t, avail = nbits - at;
+        const uint32_t valid = avail >= 32 ? 0xFFFFFFFFu : (1u << avail) - 1u;
+        const uint32_t wd = at >> 5;
+        const uint32_t win = __funnelshift_r(sw[wd], sw[wd + 1], at & 31);
+        zm = ~win & valid;
+        ones += __popc(win & valid);
+      }
+      const uint32_t cz = __popc(zm), incl = warp_incl_scan(cz);
+      uint32_t r = zeros + incl - cz;
+      for (; zm != 0 && r < k; zm &= zm - 1, r++) ent[r] = 32 * t + __ffs(zm) - 1;
+      zeros += __shfl_sync(kFull, incl, 31);
+    }
+    ones = __reduce_add_sync(kFull, ones);
   }
-  ones = (uint32_t)warp_sum64(ones);
   __syncwarp();
   if (__any_sync(kFull, bad) || zeros < k) return true;
   const uint32_t zlast = ent[k - 1];                  // offset of the k-th zero
@@ -746,10 +791,14 @@ __device__ __forceinline__ bool decode_rice(const uint8_t* __restrict__ blk, uin
     uint32_t v = 0;
     if (isR) {
       const uint32_t r = rr + __popc(bR & lt);
-      if (r < R) v = rvals[r]; else bad = true;
+      if (PRE > 0 && r < 32) v = srv[r];
+      else if (r < R) v = rvals[r];
+      else bad = true;
     } else if (in) {
       const uint32_t m = mr + __popc(bM & lt);
-      if (m < M) v = mant_at(mbytes, s0, m); else bad = true;
+      if (PRE > 0 && m < 32u * PRE) v = smv[m];
+      else if (m < M) v = mant_at(mbytes, s0, m);
+      else bad = true;
     }
     rr += __popc(bR);
     mr += __popc(bM);
@@ -865,7 +914,7 @@ k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
       const bool ow = V3 && (I.flags & kFlagOverwrite) != 0;
       bool bad = false;
       if (V3 && cc.rice) {
-        bad = decode_rice(mlist, cc.nb, cc.K, mbytes, s0, rvals, M, R, L, ow, bits, ent);
+        bad = decode_rice<4>(mlist, cc.nb, cc.K, mbytes, s0, rvals, M, R, L, ow, bits, ent);
       } else if (V3 && cc.compact) {
         bad = decode_compact<4>(mlist,
                              reinterpret_cast<const uint16_t*>(payload + I.x_start) + pre.e + lc.w,
@@ -1042,7 +1091,8 @@ k_apply_incr(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
     const bool ow = OW && (I.flags & kFlagOverwrite) != 0;
     bool bad = false;
     if (V3 && cc.rice) {
-      bad = decode_rice(mlist, cc.nb, cc.K, mbytes, s0, rvals, M, R, L, ow, bits, ent);
+      bad = decode_rice<0>(mlist, cc.nb, cc.K, mbytes, s0, rvals, M, R, L, ow, bits,
+                                    ent);
     } else if (V3 && cc.compact) {
       bad = decode_compact<0>(mlist,
                            reinterpret_cast<const uint16_t*>(payload + I.x_start) + pre.e + lc.w,

@@ -127,36 +127,36 @@ __device__ __noinline__ uint32_t chunk_escapes(const uint16_t* __restrict__ old,
 }
 
 // Version 4: the Rice statistics of a chunk from its k >= 1 slot entries (position order, either
-// layout): the packed sums of g >> K (rice_terms) over its gaps, and in sum0 the sum of the gaps
-// (its last position + 1).
-__device__ __forceinline__ uint64_t slot_rice(const uint32_t* __restrict__ entries, uint32_t k,
-                                           uint32_t* sum0) {
+// layout): the sums of g >> K over its gaps (the warp's totals), and in sum0 the sum of the
+// gaps (its last position + 1).
+__device__ __forceinline__ RiceSums slot_rice(const uint32_t* __restrict__ entries, uint32_t k,
+                                              uint32_t* sum0) {
   const int lane = threadIdx.x & 31;
   int32_t carry = -1;
-  uint64_t acc = 0;
+  RiceSums acc{0, 0};
   for (uint32_t i0 = 0; i0 < k; i0 += 32) {
     const uint32_t i = i0 + lane;
     const int32_t pos = i < k ? (int32_t)ent_pos(entries[i]) : 0;
     int32_t prev = __shfl_up_sync(0xFFFFFFFFu, pos, 1);
     if (lane == 0) prev = carry;
-    if (i < k) acc += rice_terms((uint32_t)(pos - prev));
+    if (i < k) rice_add(acc, (uint32_t)(pos - prev));
     carry = __shfl_sync(0xFFFFFFFFu, pos, 31);
   }
   *sum0 = ent_pos(entries[k - 1]) + 1;
-  return warp_sum64(acc);
+  return RiceSums{__reduce_add_sync(0xFFFFFFFFu, acc.a), __reduce_add_sync(0xFFFFFFFFu, acc.b)};
 }
 
 // The same statistics for a chunk whose changes did not fit its slot, from old and new again
 // (512 elements per step, 16 per lane): a lane's first change follows the last change of the
 // nearest lower lane that has one, or of the steps before; its others follow one another.
 template <bool FULL>
-__device__ __noinline__ uint64_t chunk_rice(const uint16_t* __restrict__ old,
+__device__ __noinline__ RiceSums chunk_rice(const uint16_t* __restrict__ old,
                                             const uint16_t* __restrict__ neu, uint64_t n,
                                             uint64_t e0, uint32_t* sum0) {
   const int lane = threadIdx.x & 31;
   const uint32_t lt = (1u << lane) - 1;
   int32_t lastp = -1;
-  uint64_t acc = 0;
+  RiceSums acc{0, 0};
   for (int s = 0; s < 8; s++) {
     const uint32_t eloc = s * 512 + lane * 16;
     const uint64_t e = e0 + eloc;
@@ -179,13 +179,13 @@ __device__ __noinline__ uint64_t chunk_rice(const uint16_t* __restrict__ old,
     int32_t prev = lower ? below : lastp;
     for (uint32_t bits = nz; bits; bits &= bits - 1) {
       const int32_t p = (int32_t)(eloc + __ffs(bits) - 1);
-      acc += rice_terms((uint32_t)(p - prev));
+      rice_add(acc, (uint32_t)(p - prev));
       prev = p;
     }
     lastp = __shfl_sync(0xFFFFFFFFu, last, 31 - __clz(bal));
   }
   *sum0 = (uint32_t)(lastp + 1);
-  return warp_sum64(acc);
+  return RiceSums{__reduce_add_sync(0xFFFFFFFFu, acc.a), __reduce_add_sync(0xFFFFFFFFu, acc.b)};
 }
 
 // The compress workspace word of a version-4 chunk with M + R (1..508) changes, from its slot
@@ -196,10 +196,9 @@ __device__ __noinline__ uint32_t rice_count(const uint32_t* entries, bool overfl
                                             const uint16_t* old, const uint16_t* neu, uint64_t n,
                                             uint64_t e0, uint32_t M, uint32_t R) {
   uint32_t sum0;
-  uint64_t packed;
-  if (!overflow) packed = slot_rice(entries, M + R, &sum0);
-  else packed = chunk_rice<FULL>(old, neu, n, e0, &sum0);
-  return rice_word(M, R, sum0, packed);
+  const RiceSums sums = !overflow ? slot_rice(entries, M + R, &sum0)
+                                  : chunk_rice<FULL>(old, neu, n, e0, &sum0);
+  return rice_word(M, R, sum0, sums);
 }
 
 // FMT: the payload kinds of the build -- 0: XOR payloads of versions 1 and 2; 3: version 3 (the
@@ -553,28 +552,24 @@ __device__ __forceinline__ void compact_batch(uint32_t e, bool valid, CompactSta
   cs.x += __popc(bE);
 }
 
-// Output of a version-4 compact chunk: its block is assembled in shared memory (zeroed words,
-// set by atomic ORs, every field in its own bits) and copied out afterwards.
-struct RiceOut {
-  uint32_t* bits;      // shared: the block, 32-bit words, bit b of the stream = bit b%32 of word b/32
-  uint16_t* rstream;   // R stream at the chunk's first rare value
-  uint8_t* mv;         // shared: the chunk's 7-bit mantissa values by chunk-local rank
-  uint32_t K;          // Rice parameter
-  uint32_t rem0;       // first remainder bit: 9R
-  uint32_t u0;         // first unary bit: 9R + K(M+R)
-};
-struct RiceState {
-  uint32_t prev;       // position of the last change emitted (0xFFFFFFFF before the first)
-  uint32_t i, m, r;    // changes, mantissa-only values, rare values emitted
-  uint32_t z;          // unary bits emitted
-};
-
 // Sets the bits of v (below 2^9) at stream bit `at`: one word, or two when v straddles them.
 __device__ __forceinline__ void or_bits(uint32_t* bits, uint32_t at, uint32_t v) {
   if (v == 0) return;
   const uint64_t t = (uint64_t)v << (at & 31);
   atomicOr(&bits[at >> 5], (uint32_t)t);
   if (t >> 32) atomicOr(&bits[(at >> 5) + 1], (uint32_t)(t >> 32));
+}
+// Sets the bits of the n-bit value v (n <= 64, no bits above them) at stream bit `at`: up to
+// three words.
+__device__ __forceinline__ void or_bits64(uint32_t* bits, uint32_t at, uint64_t v, uint32_t n) {
+  const uint32_t w = at >> 5, s = at & 31;
+  const uint32_t lo = (uint32_t)(v << s), mid = (uint32_t)(v >> (32 - s));
+  if (lo) atomicOr(&bits[w], lo);
+  if (n + s > 32 && mid) atomicOr(&bits[w + 1], mid);
+  if (n + s > 64) {   // then s > 0
+    const uint32_t hi = (uint32_t)(v >> (64 - s));
+    if (hi) atomicOr(&bits[w + 2], hi);
+  }
 }
 // Sets the q bits [at, at + q).
 __device__ __forceinline__ void ones_run(uint32_t* bits, uint32_t at, uint32_t q) {
@@ -586,44 +581,76 @@ __device__ __forceinline__ void ones_run(uint32_t* bits, uint32_t at, uint32_t q
   }
 }
 
-// Emits the 32 changes rs.i .. rs.i+31 of a version-4 compact chunk in position order, lane l
-// holding change rs.i + l as a slot entry (OW: the general layout; else pos << 16 | x) when
-// `valid` (the valid lanes are a prefix).  Change i with gap g (pos + 1 for the first) puts
-// g mod 2^K at bit 9R + K*i, its quotient g >> K as that many ones ending before its unary
-// zero (the zeros of changes 0..i close the first i+1 unary codes), and, when rare, its index
-// i at bit 9*(its rank among the rare changes).
+// Emits a version-4 compact chunk: its k = M + R changes in position order in list (OW: the
+// general layout; else pos << 16 | x), Rice parameter K.  The block is assembled in `bits`
+// (shared, zeroed words; stream bit b = bit b%32 of word b/32); the rare values go to rstream
+// and the 7-bit mantissa values to mv by class rank.  Each lane takes a contiguous range of
+// ceil(k/32) changes: a first pass counts its unary bits and its changes of each class, one
+// warp scan places every lane's fields, and a second pass writes them -- the remainder g mod
+// 2^K of change i at bit 9R + K*i, the quotient g >> K as that many ones ending before the
+// change's unary zero, and for a rare change its index i at bit 9*(its rare rank).  A lane
+// gathers its unary codes and its remainders in two 64-bit registers and writes each run with
+// one to three atomic ORs (a quotient that does not fit is written on its own); lanes write
+// disjoint bit ranges, so their ORs meet only on the words two ranges share.
 template <bool OW>
-__device__ __forceinline__ void rice_batch(uint32_t e, bool valid, RiceState& rs,
-                                           const RiceOut& o) {
+__device__ __forceinline__ void rice_write(const uint32_t* list, uint32_t k, uint32_t R,
+                                           uint32_t K, uint32_t* bits, uint16_t* rstream,
+                                           uint8_t* mv) {
   const int lane = threadIdx.x & 31;
-  const uint32_t lt = (1u << lane) - 1;
-  const uint32_t pos = ent_pos(e), x = e & 0xFFFFu;
-  uint32_t prev = __shfl_up_sync(0xFFFFFFFFu, pos, 1);
-  if (lane == 0) prev = rs.prev;
-  const uint32_t gap = pos - prev;
-  const bool rare = OW ? (e & kEntRare) != 0 : (x & kSignExp) != 0;
-  const bool isR = valid && rare;
-  const bool isM = valid && !rare;
-  const uint32_t bM = __ballot_sync(0xFFFFFFFFu, isM), bR = __ballot_sync(0xFFFFFFFFu, isR);
-  const uint32_t q = valid ? gap >> o.K : 0u;
-  const uint32_t incl = warp_incl_scan(valid ? q + 1 : 0u);   // unary bits up to change i
-  if (valid) {
-    const uint32_t i = rs.i + lane;
-    ones_run(o.bits, o.u0 + rs.z + incl - 1 - q, q);
-    or_bits(o.bits, o.rem0 + o.K * i, gap & ((1u << o.K) - 1u));
-    if (isR) {
-      const uint32_t jr = rs.r + __popc(bR & lt);
-      or_bits(o.bits, kRiceIdxBits * jr, i);
-      o.rstream[jr] = (uint16_t)x;
+  const uint32_t per = (k + 31) >> 5;
+  const uint32_t i0 = min(lane * per, k), i1 = min(i0 + per, k);
+  const uint32_t last = i1 > i0 ? ent_pos(list[i1 - 1]) : 0u;
+  uint32_t prev0 = __shfl_up_sync(0xFFFFFFFFu, last, 1);
+  if (lane == 0) prev0 = 0xFFFFFFFFu;   // the first gap is the position + 1
+  uint32_t U = 0, nr = 0, p = prev0;
+  for (uint32_t i = i0; i < i1; i++) {
+    const uint32_t e = list[i], pos = ent_pos(e);
+    U += ((pos - p) >> K) + 1;
+    nr += OW ? (e >> 31) : ((e & kSignExp) != 0);
+    p = pos;
+  }
+  // unary bits (at most 8184), rare and mantissa-only counts (at most 508 each) in one scan
+  const uint32_t mine = U | (nr << 14) | ((i1 - i0 - nr) << 23);
+  const uint32_t excl = warp_incl_scan(mine) - mine;
+  uint32_t ubit = kRiceIdxBits * R + K * k + (excl & 0x3FFFu);
+  uint32_t rr = (excl >> 14) & 0x1FFu, mm = excl >> 23;
+  const uint32_t rmask = (1u << K) - 1u;
+  uint32_t rbit = kRiceIdxBits * R + K * i0;
+  uint64_t ua = 0, ra = 0;   // pending unary bits (un of them) and remainder bits (rn)
+  uint32_t un = 0, rn = 0;
+  p = prev0;
+  for (uint32_t i = i0; i < i1; i++) {
+    const uint32_t e = list[i], pos = ent_pos(e), g = pos - p, x = e & 0xFFFFu;
+    p = pos;
+    const uint32_t q = g >> K;
+    if (un + q + 1 <= 64) {
+      ua |= ((1ull << q) - 1ull) << un;
+      un += q + 1;
     } else {
-      o.mv[rs.m + __popc(bM & lt)] = (uint8_t)(x & kMant);
+      or_bits64(bits, ubit, ua, un);
+      ubit += un;
+      ua = 0;
+      un = 0;
+      ones_run(bits, ubit, q);
+      ubit += q + 1;
+    }
+    if (rn + K > 64) {
+      or_bits64(bits, rbit, ra, rn);
+      rbit += rn;
+      ra = 0;
+      rn = 0;
+    }
+    ra |= (uint64_t)(g & rmask) << rn;
+    rn += K;
+    if (OW ? (e >> 31) != 0 : (x & kSignExp) != 0) {
+      or_bits(bits, kRiceIdxBits * rr, i);
+      rstream[rr++] = (uint16_t)x;
+    } else {
+      mv[mm++] = (uint8_t)(x & kMant);
     }
   }
-  rs.prev = __shfl_sync(0xFFFFFFFFu, pos, 31);
-  rs.i += 32;
-  rs.m += __popc(bM);
-  rs.r += __popc(bR);
-  rs.z += __shfl_sync(0xFFFFFFFFu, incl, 31);
+  or_bits64(bits, ubit, ua, un);
+  or_bits64(bits, rbit, ra, rn);
 }
 
 // Sets up the output pointers of chunk c (counts M, R, exclusive prefixes Pex / Rex).
@@ -722,14 +749,7 @@ k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
         const uint32_t nb = (cnt_here >> 21) & 0x3FFu, K = (cnt_here >> 18) & 0x7u;
         for (uint32_t i = lane; i < (nb + 3) / 4; i += 32) sm->bm[i] = 0;
         __syncwarp();
-        const RiceOut o{sm->bm, cx.rstream, sm->mv, K, kRiceIdxBits * R,
-                        kRiceIdxBits * R + K * kk};
-        RiceState rs{0xFFFFFFFFu, 0, 0, 0, 0};
-#pragma unroll
-        for (int q = 0; q < 8; q++) {
-          if (32u * q >= kk) break;
-          rice_batch<OW>(ent[q], 32u * q + lane < kk, rs, o);
-        }
+        rice_write<OW>(E, kk, R, K, sm->bm, cx.rstream, sm->mv);
         __syncwarp();
         store_bitmap(payload + I.p_start + Pex, sm->bm, nb);
       }
@@ -834,13 +854,8 @@ __device__ __noinline__ void emit_rice_list(const uint32_t* lst, uint32_t cnt, b
   const uint32_t nb = (cnt >> 21) & 0x3FFu, K = (cnt >> 18) & 0x7u;
   for (uint32_t i = lane; i < (nb + 3) / 4; i += 32) sm->bm[i] = 0;
   __syncwarp();
-  const RiceOut o{sm->bm, rstream, sm->mv, K, kRiceIdxBits * R, kRiceIdxBits * R + K * kk};
-  RiceState rs{0xFFFFFFFFu, 0, 0, 0, 0};
-  for (uint32_t i0 = 0; i0 < kk; i0 += 32) {
-    const bool valid = i0 + lane < kk;
-    if (ow) rice_batch<true>(valid ? lst[i0 + lane] : 0u, valid, rs, o);
-    else rice_batch<false>(valid ? lst[i0 + lane] : 0u, valid, rs, o);
-  }
+  if (ow) rice_write<true>(lst, kk, R, K, sm->bm, rstream, sm->mv);
+  else rice_write<false>(lst, kk, R, K, sm->bm, rstream, sm->mv);
   __syncwarp();
   store_bitmap(dst, sm->bm, nb);
 }

@@ -148,28 +148,40 @@ __host__ __device__ __forceinline__ bool rice_compact(uint32_t v, uint32_t B) {
   return ((v >> 21) & 0x3FFu) < block_bytes(M, B) + block_bytes(R, B);
 }
 
-// Sums over a chunk's gaps of g >> K for K = 1..7, packed in one u64: fields of 12, 11, 10, 9,
-// 8, 7 and 6 bits at bits 0, 12, 23, 33, 42, 50 and 57.  The gaps of a chunk add up to its last
-// position + 1 <= 4096, so the sum for K is at most 4096 >> K and no field carries into the next.
-__device__ __forceinline__ uint64_t rice_terms(uint32_t g) {
-  return (uint64_t)(g >> 1) | ((uint64_t)(g >> 2) << 12) | ((uint64_t)(g >> 3) << 23) |
-         ((uint64_t)(g >> 4) << 33) | ((uint64_t)(g >> 5) << 42) | ((uint64_t)(g >> 6) << 50) |
-         ((uint64_t)(g >> 7) << 57);
+// Sums over a chunk's gaps of g >> K for K = 1..7, packed in two words: a holds the sums for
+// K = 1, 2 and 4 in fields of 12, 11 and 9 bits at bits 0, 12 and 23; b those for K = 3, 5, 6
+// and 7 in fields of 10, 8, 7 and 6 bits at bits 0, 10, 18 and 25.  The gaps of a chunk add
+// up to its last position + 1 <= 4096, so the sum for K is at most 4096 >> K and no field
+// carries into the next, in a lane's partial sums or in the warp's total.
+struct RiceSums {
+  uint32_t a, b;
+};
+__device__ __forceinline__ void rice_add(RiceSums& s, uint32_t g) {
+  s.a += (g >> 1) | ((g >> 2) << 12) | ((g >> 4) << 23);
+  s.b += (g >> 3) | ((g >> 5) << 10) | ((g >> 6) << 18) | ((g >> 7) << 25);
+}
+__device__ __forceinline__ uint32_t rice_sum(const RiceSums& s, uint32_t K) {
+  switch (K) {
+    case 1: return s.a & 0xFFFu;
+    case 2: return (s.a >> 12) & 0x7FFu;
+    case 3: return s.b & 0x3FFu;
+    case 4: return s.a >> 23;
+    case 5: return (s.b >> 10) & 0xFFu;
+    case 6: return (s.b >> 18) & 0x7Fu;
+    default: return s.b >> 25;
+  }
 }
 // The compress workspace word of a version-4 chunk with M + R changes: sum0 = the sum of the
-// gaps (last position + 1), packed = their rice_terms.  K takes the fewest bits
+// gaps (last position + 1), s = their sums for K = 1..7.  K takes the fewest bits
 // (9R + K(M+R) + (M+R) + sum of g >> K), the smallest K on a tie.
 __device__ __forceinline__ uint32_t rice_word(uint32_t M, uint32_t R, uint32_t sum0,
-                                              uint64_t packed) {
+                                              const RiceSums& s) {
   const uint32_t k = M + R;
   if (k == 0 || k > kCompactMax) return wcount(M, R, 0);
-  constexpr uint32_t off[8] = {0, 0, 12, 23, 33, 42, 50, 57};
-  constexpr uint32_t wid[8] = {0, 12, 11, 10, 9, 8, 7, 6};
   uint32_t bestK = 0, best = k + sum0;
 #pragma unroll
   for (uint32_t K = 1; K < 8; K++) {
-    const uint32_t s = (uint32_t)(packed >> off[K]) & ((1u << wid[K]) - 1u);
-    const uint32_t bits = K * k + k + s;
+    const uint32_t bits = K * k + k + rice_sum(s, K);
     if (bits < best) { best = bits; bestK = K; }
   }
   const uint32_t nb = (9 * R + best + 7) / 8;
