@@ -37,12 +37,12 @@ constexpr int kWarps = kThreads / 32;
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 // Words of a warp's staging area for a version-4 block: the block (at most 1023 bytes, 256
-// words) and a zero guard word, the 512-bit class bitmap of the merged list, the first 128
-// mantissa-only values (bytes) and the first 32 rare values (u16) of the chunk.
+// words) and a zero guard word, the 512-bit class bitmap of the merged list, then the chunk's
+// first values as u16: mantissa-only values 0..127 at [0, 128), rare values 0..31 at
+// [128, 160).
 constexpr uint32_t kRiceCls = 260;
-constexpr uint32_t kRiceMv = kRiceCls + 16;
-constexpr uint32_t kRiceRv = kRiceMv + 32;
-constexpr uint32_t kRiceWords = kRiceRv + 16;
+constexpr uint32_t kRiceVals = kRiceCls + 16;
+constexpr uint32_t kRiceWords = kRiceVals + 80;
 
 template <int PRE>
 __device__ __forceinline__ bool decode_rice(const uint8_t* __restrict__ blk, uint32_t nb,
@@ -680,8 +680,7 @@ __device__ __forceinline__ bool decode_rice(const uint8_t* __restrict__ blk, uin
   const uint32_t lt = (1u << lane) - 1;
   const uint32_t k = M + R, nbits = 8 * nb, nw = (nb + 3) >> 2;   // nw <= 256
   uint32_t* __restrict__ cls = sw + kRiceCls;
-  uint8_t* __restrict__ smv = reinterpret_cast<uint8_t*>(sw + kRiceMv);
-  uint16_t* __restrict__ srv = reinterpret_cast<uint16_t*>(sw + kRiceRv);
+  uint16_t* __restrict__ sv = reinterpret_cast<uint16_t*>(sw + kRiceVals);
   // the first 128 mantissa-only and 32 rare values are requested with the block, so that the
   // whole decode waits for one round of loads
   constexpr int NQ = PRE > 0 ? PRE : 1;   // (arrays of size 0 are not allowed)
@@ -708,8 +707,8 @@ __device__ __forceinline__ bool decode_rice(const uint8_t* __restrict__ blk, uin
   if (lane < 16) cls[lane] = 0;
 #pragma unroll
   for (int q = 0; q < PRE; q++)
-    smv[32 * q + lane] = (uint8_t)((mraw[q] >> ((s0 + 7 * (32 * q + lane)) & 7)) & kMant);
-  if (PRE > 0) srv[lane] = (uint16_t)rv0;
+    sv[32 * q + lane] = (uint16_t)((mraw[q] >> ((s0 + 7 * (32 * q + lane)) & 7)) & kMant);
+  if (PRE > 0) sv[128 + lane] = (uint16_t)rv0;
   __syncwarp();
   // nbits-bit field at bit `at` of the block (at < 32 * nw, so the second word exists)
   auto field = [&](uint32_t at, uint32_t bits) -> uint32_t {
@@ -778,6 +777,9 @@ __device__ __forceinline__ bool decode_rice(const uint8_t* __restrict__ blk, uin
   // the changes, 32 at a time
   uint32_t carry = 0xFFFFFFFFu, zprev = 0xFFFFFFFFu, mr = 0, rr = 0;
   const uint32_t rem0 = kRiceIdxBits * R;
+  // every value staged (the same on every lane): one shared load per change, no range checks
+  // (the rare indices checked above make exactly R changes rare)
+  const bool staged = PRE > 0 && M <= 32u * PRE && R <= 32;
   for (uint32_t b0 = 0; b0 < k; b0 += 32) {
     const uint32_t i = b0 + lane;
     const bool in = i < k;
@@ -789,14 +791,16 @@ __device__ __forceinline__ bool decode_rice(const uint8_t* __restrict__ blk, uin
     const bool isR = in && ((cls[i >> 5] >> (i & 31)) & 1u);
     const uint32_t bR = __ballot_sync(kFull, isR), bM = __ballot_sync(kFull, in && !isR);
     uint32_t v = 0;
-    if (isR) {
+    if (staged) {
+      if (in) v = sv[isR ? 128u + rr + __popc(bR & lt) : mr + __popc(bM & lt)];
+    } else if (isR) {
       const uint32_t r = rr + __popc(bR & lt);
-      if (PRE > 0 && r < 32) v = srv[r];
+      if (PRE > 0 && r < 32) v = sv[128 + r];
       else if (r < R) v = rvals[r];
       else bad = true;
     } else if (in) {
       const uint32_t m = mr + __popc(bM & lt);
-      if (PRE > 0 && m < 32u * PRE) v = smv[m];
+      if (PRE > 0 && m < 32u * PRE) v = sv[m];
       else if (m < M) v = mant_at(mbytes, s0, m);
       else bad = true;
     }
