@@ -12,6 +12,11 @@ of one checkpoint divided by compress+apply time), summed over ranks for N > 1 (
 replicas, weak scaling).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload dense7b] [--impl reference]
+
+`--profile-case embed|formats` runs a fixed small program for an ncu capture instead (no timing,
+no JSON line): `embed` compresses the 32000x4096 embedding tensor of dense7b in versions 1, 3
+and 4 and applies each payload, two rounds; `formats` does the same with versions 3 and 4 on the
+whole workload, with the incremental apply too.
 """
 from __future__ import annotations
 
@@ -794,6 +799,65 @@ def run_ours(args) -> None:
         dist.destroy_process_group()
 
 
+def run_profile_case(args) -> None:
+    """The fixed programs that the committed ncu summaries were captured from (one GPU)."""
+    import lossless_bf16_weight_old_gb300 as bd
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if args.profile_case == "embed":
+        spec = [s for s in W.dense7b() if s.name == "embed"][0]
+        a, b = W.make_pair(spec, device=dev)
+        olds, news = [a.reshape(-1)], [b.reshape(-1)]
+        versions = (1, 3, 4)
+    else:
+        specs = _workload_specs(args.workload)
+        olds, news = [], []
+        for s in specs:
+            a, b = W.make_pair(s, device=dev)
+            olds.append(a.reshape(-1))
+            news.append(b.reshape(-1))
+        versions = (3, 4)
+    rolls = [o.clone() for o in olds]
+    ck_old = torch.cat([bd.checksum(o).reshape(1) for o in olds])
+    comp = {v: (bd.CompressBatch(olds, news) if v == 1 else
+                bd.CompressBatch(olds, news, base_checksums=ck_old, compact=v == 3, rice=v == 4))
+            for v in versions}
+    sizes = {}
+    for rnd in range(2):
+        for v in versions:
+            comp[v].run()
+        torch.cuda.synchronize()
+        for v in versions:
+            sizes[v] = [int(x) for x in comp[v].sizes.tolist()]
+        ck_new = comp[versions[0]].checksums
+        state_new = False
+        for r, o in zip(rolls, olds):
+            r.copy_(o)
+        done = []
+        for v in versions:   # alternately to new and back to old
+            dec = bd.DecompressBatch(rolls, comp[v].payloads, sizes[v],
+                                     ck_old if state_new else ck_new)
+            dec.run()
+            done.append(dec)
+            state_new = not state_new
+        if args.profile_case == "formats":
+            for v in versions:
+                for r, o in zip(rolls, olds):
+                    r.copy_(o)
+                inc = bd.IncrementalBatch(rolls, comp[v].payloads, sizes[v], ck_old, ck_new)
+                inc.run()
+                done.append(inc)
+                state_new = True
+        torch.cuda.synchronize()
+        want = news if state_new else olds
+        if any(int(x.status.item()) != bd.OK for x in done) or not all(
+                torch.equal(r.view(torch.int16), w.view(torch.int16))
+                for r, w in zip(rolls, want)):
+            raise RuntimeError("profile case did not verify")
+    print("profile case", args.profile_case, "ok:",
+          {v: sum(sizes[v]) for v in versions}, "payload bytes", flush=True)
+
+
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -805,7 +869,12 @@ def main(argv=None):
                    help="elements of the workload the CPU oracle baseline encodes+decodes")
     p.add_argument("--ref-sample-elems", type=int, default=400_000_000,
                    help="elements per step of the --impl reference arm")
+    p.add_argument("--profile-case", choices=["embed", "formats"], default=None,
+                   help="run a fixed small program for an ncu capture instead of the bench")
     args = p.parse_args(argv)
+    if args.profile_case:
+        run_profile_case(args)
+        return
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")
     if args.impl == "reference":
