@@ -438,3 +438,26 @@ def test_full_size_1gib_and_sweep_workloads(overwrite):
         assert torch.equal(w.view(torch.int16), new.view(torch.int16)), spec.name
         assert torch.equal(w2.view(torch.int16), new.view(torch.int16)), spec.name
         del old, new, w, w2, payload
+
+
+@pytest.mark.parametrize("kind", [dict(), dict(compact=True), dict(rice=True),
+                                  dict(overwrite=True), dict(compact=True, overwrite=True),
+                                  dict(rice=True, overwrite=True)])
+def test_empty_tensor_in_every_bound_format(kind):
+    """n = 0: the 80-byte header alone (C = 0, checksum 0) in versions 2 to 4, applied in full
+    and incrementally."""
+    o = np.zeros(0, dtype=np.uint16)
+    base = oracle.checksum(o)   # 0
+    assert oracle.decode_incremental(o, oracle.encode(o, o, base=base, **kind)[0], base, 0)[0] \
+        == oracle.OK
+    ref, ck_ref = oracle.encode(o, o, base=base, **kind)
+    assert ref.size == 80 and ck_ref == 0
+    old = torch.empty(0, dtype=torch.bfloat16, device="cuda")
+    payload, size, ck, st = bd.compress(old, old, base_checksum=base, **kind)
+    torch.cuda.synchronize()
+    assert int(st.item()) == bd.OK and int(size.item()) == 80 and bd.u64(ck)[0] == 0
+    assert np.array_equal(payload[:80].cpu().numpy(), ref)
+    st1 = bd.decompress(old, payload, 80, 0, out=old)
+    st2, ck2 = bd.decompress_incremental(old, payload, 80, base, bd._u64_tensor([0], "cuda"))
+    torch.cuda.synchronize()
+    assert int(st1.item()) == bd.OK and int(st2.item()) == bd.OK and bd.u64(ck2)[0] == 0
