@@ -18,17 +18,28 @@ constexpr uint64_t kAlign = 256;
 inline uint64_t up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
 
 struct Sizes {
-  uint64_t chunks = 0, tiles = 0;
+  uint64_t chunks = 0, tiles = 0, batches = 0;
+  uint32_t bchunks = 1;
 };
 
-bool sizes_of(const uint64_t* ns, uint32_t k, Sizes& s) {
+// Chunks per batch of the fused compress: as many as keep about four batches per resident warp
+// (32 per SM), at most kMaxBatchChunks.  Fewer, larger batches cost less to hand out and to
+// publish; small calls keep one warp per chunk.  The workspace size assumes the smallest.
+uint32_t batch_chunks(uint64_t chunks, int sms) {
+  const uint64_t per = chunks / ((uint64_t)(sms > 0 ? sms : 1) * 32 * 4);
+  return (uint32_t)(per < 1 ? 1 : per > kMaxBatchChunks ? kMaxBatchChunks : per);
+}
+
+bool sizes_of(const uint64_t* ns, uint32_t k, Sizes& s, uint32_t bchunks = 1) {
   s = Sizes{};
+  s.bchunks = bchunks;
   for (uint32_t i = 0; i < k; i++) {
     const uint64_t n = ns[i];
     if (n > BD_MAX_ELEMS) return false;
     const uint64_t C = (n + kChunk - 1) / kChunk;
     s.chunks += C;
     s.tiles += (C + kTileChunks - 1) / kTileChunks;
+    s.batches += tensor_batches(C, bchunks);
   }
   return true;
 }
@@ -41,8 +52,12 @@ WsLayout make_layout(uint32_t k, const Sizes& s, bool compress) {
   off = up(off + (uint64_t)k * kCkBytes, kAlign);
   L.info = off;
   off = up(off + (uint64_t)k * sizeof(JobInfo), kAlign);
-  L.overflow = off;  // decompress: count of chunks listed for the dense apply
+  L.overflow = off;  // count of chunks listed for the dense kernels (+ selection words)
   off = up(off + 16, kAlign);
+  if (compress) {
+    L.fused_ctl = off;
+    off = up(off + ((uint64_t)kCtlTensors + 2 * (uint64_t)k) * 4, kAlign);
+  }
   L.state_bytes = off - L.state;
   L.jobs = off;
   off = up(off + (uint64_t)k * 128, kAlign);
@@ -50,6 +65,10 @@ WsLayout make_layout(uint32_t k, const Sizes& s, bool compress) {
   off = up(off + ((uint64_t)k + 1) * 8, kAlign);
   L.tile_start = off;
   off = up(off + ((uint64_t)k + 1) * 8, kAlign);
+  if (compress) {   // uploaded with the tensor table
+    L.batch_start = off;
+    off = up(off + ((uint64_t)k + 1) * 8, kAlign);
+  }
   L.loc = off;
   off = up(off + s.chunks * 16, kAlign);
   L.tile_tot = off;
@@ -63,6 +82,10 @@ WsLayout make_layout(uint32_t k, const Sizes& s, bool compress) {
     off = up(off + s.chunks * kSlotBytes, kAlign);
     L.counts = off;
     off = up(off + s.chunks * 4, kAlign);
+    L.batch_tot = off;
+    off = up(off + s.batches * 16, kAlign);
+    L.batch_pre = off;
+    off = up(off + s.batches * sizeof(TileSum), kAlign);
   }
   L.total = off;
   return L;
@@ -143,6 +166,7 @@ int compress_impl(const bd_compress_item* items, const uint64_t* const* bases, u
       return BD_ERR_INVALID_ARG;
     ns[i] = it.n;
   }
+  // (the layout for one-chunk batches, the most there can be, is the size the caller was told)
   Sizes sz;
   if (!sizes_of(ns.data(), k, sz)) return BD_ERR_INVALID_ARG;
   const WsLayout lay = make_layout(k, sz, true);
@@ -151,13 +175,15 @@ int compress_impl(const bd_compress_item* items, const uint64_t* const* bases, u
     if (overlaps(items[i].d_payload, items[i].cap, ws, lay.total)) return BD_ERR_INVALID_ARG;
   const int sms = sm_count();
   if (sms <= 0) return BD_ERR_CUDA;
+  const uint32_t bchunks = batch_chunks(sz.chunks, sms);
 
   // tensor table
   std::vector<uint8_t> host(lay.loc - lay.jobs, 0);
   CJob* jobs = reinterpret_cast<CJob*>(host.data());
   uint64_t* cstart = reinterpret_cast<uint64_t*>(host.data() + (lay.chunk_start - lay.jobs));
   uint64_t* tstart = reinterpret_cast<uint64_t*>(host.data() + (lay.tile_start - lay.jobs));
-  uint64_t cb = 0, tb = 0;
+  uint64_t* bstart = reinterpret_cast<uint64_t*>(host.data() + (lay.batch_start - lay.jobs));
+  uint64_t cb = 0, tb = 0, bb = 0;
   for (uint32_t i = 0; i < k; i++) {
     const bd_compress_item& it = items[i];
     CJob& J = jobs[i];
@@ -177,14 +203,17 @@ int compress_impl(const bd_compress_item* items, const uint64_t* const* bases, u
     J.tile_base = tb;
     cstart[i] = cb;
     tstart[i] = tb;
+    bstart[i] = bb;
     cb += J.nchunks;
     tb += (J.nchunks + kTileChunks - 1) / kTileChunks;
+    bb += tensor_batches(J.nchunks, bchunks);
   }
   cstart[k] = cb;
   tstart[k] = tb;
+  bstart[k] = bb;
 
   uint8_t* w = static_cast<uint8_t*>(ws);
-  LaunchCtx c{s, sms, w, lay, k, sz.chunks, sz.tiles};
+  LaunchCtx c{s, sms, w, lay, k, sz.chunks, sz.tiles, bb, bchunks};
   int rc;
   if ((rc = check(cudaMemsetAsync(w + lay.state, 0, lay.state_bytes, s)))) return rc;
   if (status_all && (rc = check(cudaMemsetAsync(status_all, 0, sizeof(int32_t), s)))) return rc;
@@ -193,6 +222,10 @@ int compress_impl(const bd_compress_item* items, const uint64_t* const* bases, u
   // the kernel builds: version 4, version 3 (also every overwrite payload of version 2), or
   // the XOR payloads of versions 1 and 2
   const uint32_t fmt = version == 4 ? 4u : (version == 3 || overwrite) ? 3u : 0u;
+  if (fmt == 0) {   // XOR payloads of versions 1 and 2: the fused compress
+    if ((rc = check(launch_compress_fused(c, status_all)))) return rc;
+    return check(launch_emit_dense(c, true));
+  }
   if ((rc = check(launch_encode_slots(c, fmt, overwrite)))) return rc;
   if ((rc = check(launch_scan_tiles(c, false)))) return rc;
   if ((rc = check(launch_scan_jobs(c, false, status_all)))) return rc;

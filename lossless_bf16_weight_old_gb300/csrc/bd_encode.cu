@@ -209,7 +209,7 @@ __device__ __noinline__ uint32_t rice_count(const uint32_t* entries, bool overfl
 // from a per-lane shared copy of the step's new values; otherwise pos << 16 | x (the class
 // follows from x).
 template <bool FULL, int FMT, bool OW>
-__device__ __forceinline__ void encode_chunk(const uint16_t* __restrict__ old,
+__device__ __forceinline__ uint32_t encode_chunk(const uint16_t* __restrict__ old,
                                              const uint16_t* __restrict__ neu, uint64_t n,
                                              uint64_t e0, uint32_t* __restrict__ slot,
                                              uint64_t& ck, uint64_t g,
@@ -324,6 +324,7 @@ __device__ __forceinline__ void encode_chunk(const uint16_t* __restrict__ old,
     counts[g] = word;
     if (overflow) list[atomicAdd(list_count, 1u)] = (uint32_t)g;
   }
+  return word;   // the same on every lane
 }
 
 template <int FMT, bool OW>
@@ -668,11 +669,169 @@ __device__ __forceinline__ void emit_ctx(EmitCtx& cx, uint8_t* payload, const Jo
   cx.wbase = 0;
 }
 
-// Chunks whose changes fit their slot: the slot's single position-ordered list is split by
-// class 32 entries at a time with ballots (rank = set lanes below; the previous element of
-// the same class, for the delta, is the nearest such lane below or the carry).  FMT as in
-// encode_slots: 3 writes version-3 compact blocks, 4 version-4 ones; OW: slot entries in the
-// general layout.
+// The emit work of chunk g (chunk c of tensor j, whose chunks end at g_job_end) once the offsets
+// of its tensor's sections (I) and the chunk's exclusive prefixes are known: Pex, Mex, Rex, Xex
+// = position bytes, mantissa-only values, rare values and escaped gaps of the chunks before it
+// in its tensor.  The slot's single position-ordered list is split by class 32 entries at a
+// time with ballots (rank = set lanes below; the previous element of the same class, for the
+// delta, is the nearest such lane below or the carry).  FMT as in encode_slots: 3 writes
+// version-3 compact blocks, 4 version-4 ones; OW: slot entries in the general layout.
+// prefetch_next: ask L2 for the next chunk's slot header and first 96 entries meanwhile.
+template <int FMT, bool OW>
+__device__ __forceinline__ void emit_chunk(const CJob* __restrict__ jobs, uint64_t g, uint32_t j,
+                                           uint64_t c, uint64_t g_job_end, bool prefetch_next,
+                                           const JobInfo& I, uint64_t Pex, uint64_t Mex,
+                                           uint64_t Rex, uint64_t Xex,
+                                           const uint32_t* __restrict__ counts,
+                                           const uint8_t* __restrict__ slots, EmitSmem* sm) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t lt = (1u << lane) - 1;
+  // level 1: everything addressed by g and j alone, requested together
+  const uint8_t* slot = slots + g * kSlotBytes;
+  if (prefetch_next && lane < 4)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(slot + kSlotBytes + 128 * lane));
+  const uint32_t* E = reinterpret_cast<const uint32_t*>(slot + kSlotHeader);
+  const uint32_t hdr = *reinterpret_cast<const uint32_t*>(slot);
+  uint32_t ent[8];
+  // the first 96 entries are read with the header (a slot always has room for them); they
+  // cover the whole list of most sparse chunks
+  ent[0] = E[lane];
+  ent[1] = E[32 + lane];
+  ent[2] = E[64 + lane];
+  constexpr bool GEN = FMT != 0;
+  const uint32_t cnt_here = GEN ? counts[g] : 0u;
+  const uint32_t cnt_next = g + 1 < g_job_end ? counts[g + 1] : 0u;
+  const uint32_t aux_next =
+      g + 1 < g_job_end ? reinterpret_cast<const uint32_t*>(slot + kSlotBytes)[1] : 0u;
+  uint8_t* payload = jobs[j].payload;
+  const uint64_t n = jobs[j].n;
+  if (I.status != BD_OK || (hdr & kSlotOverflow)) return;
+
+  // level 2: the rest of the list
+  const uint32_t M = hdr & 0xFFFu, R = (hdr >> 12) & 0xFFFu, kk = M + R;
+#pragma unroll
+  for (int q = 3; q < 8; q++) ent[q] = 0u;
+  if (kk > 96) {
+#pragma unroll
+    for (int q = 3; q < 8; q++) {
+      const uint32_t i = 32 * q + lane;
+      if (i < kk) ent[q] = E[i];
+    }
+  }
+
+  const uint64_t e0 = c * kChunk;
+  const uint32_t L = (n - e0) < kChunk ? (uint32_t)(n - e0) : kChunk;
+  const uint32_t B = (L + 7) >> 3;
+  const uint32_t nesc = wcount_e(cnt_here);
+  const bool rice = FMT == 4 && I.version == 4 && rice_compact(cnt_here, B);
+  const bool compact = rice || (FMT == 3 && I.version == 3 && choose_compact(M, R, nesc, B));
+  if (lane == 0)
+    reinterpret_cast<uint32_t*>(payload + count_table_offset(I.r_start, jobs[j].nchunks))[c] =
+        rice ? cnt_here : count_entry(GEN ? I.version : 1u, M, R, nesc, compact);
+  EmitCtx cx;
+  emit_ctx(cx, payload, I, M, R, B, Pex, Rex, sm);
+  if constexpr (FMT == 4) {
+    if (rice) {
+      cx.listM = cx.listR = true;   // no bitmap
+      const uint32_t nb = (cnt_here >> 21) & 0x3FFu, K = (cnt_here >> 18) & 0x7u;
+      for (uint32_t i = lane; i < (nb + 3) / 4; i += 32) sm->bm[i] = 0;
+      __syncwarp();
+      rice_write<OW>(E, kk, R, K, sm->bm, cx.rstream, sm->mv);
+      __syncwarp();
+      store_bitmap(payload + I.p_start + Pex, sm->bm, nb);
+    }
+  }
+  if (FMT == 3 && compact) {
+    cx.listM = cx.listR = true;   // no bitmap
+    const CompactOut o{payload + I.p_start + Pex,
+                       reinterpret_cast<uint16_t*>(payload + I.x_start) + Xex,
+                       cx.rstream, sm->mv, kk};
+    CompactState cs{0xFFFFFFFFu, 0, 0, 0, 0};
+#pragma unroll
+    for (int q = 0; q < 8; q++) {
+      if (32u * q >= kk) break;
+      compact_batch<OW>(ent[q], 32u * q + lane < kk, cs, o);
+    }
+  }
+  if (!cx.listM || !cx.listR) {
+    for (int i = lane; i < 256; i += 32) sm->bm[i] = 0;
+    __syncwarp();
+  }
+  uint32_t baseM = 0, baseR = 0, carryM = 0, carryR = 0;
+#pragma unroll
+  for (int q = 0; q < 8; q++) {
+    if (compact || 32u * q >= kk) break;
+    const uint32_t e = ent[q], pos = OW ? ent_pos(e) : e >> 16, x = e & 0xFFFFu;
+    const bool valid = 32u * q + lane < kk;
+    const bool rare = OW ? (e & kEntRare) != 0 : (x & kSignExp) != 0;
+    const bool isR = valid && rare;
+    const bool isM = valid && !rare;
+    const uint32_t bM = __ballot_sync(0xFFFFFFFFu, isM), bR = __ballot_sync(0xFFFFFFFFu, isR);
+    // (In versions 1 and 2 every M block starts at an even offset; after an odd-length
+    // compact block of version 3 it may not, hence the alignment-checking stores there.)
+    if (bR == 0 && cx.listM) {
+      // no rare entry in this batch: the mantissa-only entries are the first lanes in order
+      const uint32_t prevL = __shfl_up_sync(0xFFFFFFFFu, pos, 1);
+      if (isM) {
+        const uint32_t r = baseM + lane;
+        const uint32_t prev = lane ? prevL : carryM;
+        if (GEN) store_u16(cx.mblk + 2 * r, (uint16_t)(pos - prev));
+        else reinterpret_cast<uint16_t*>(cx.mblk)[r] = (uint16_t)(pos - prev);
+        sm->mv[r] = (uint8_t)(x & kMant);
+      }
+      const uint32_t cntM = __popc(bM);
+      carryM = __shfl_sync(0xFFFFFFFFu, pos, cntM - 1);
+      baseM += cntM;
+      continue;
+    }
+    const uint32_t lowM = bM & lt, lowR = bR & lt;
+    const uint32_t pM = __shfl_sync(0xFFFFFFFFu, pos, lowM ? 31 - __clz(lowM) : lane);
+    const uint32_t pR = __shfl_sync(0xFFFFFFFFu, pos, lowR ? 31 - __clz(lowR) : lane);
+    if (isM) {
+      const uint32_t r = baseM + __popc(lowM);
+      const uint32_t prev = lowM ? pM : carryM;
+      if (cx.listM && GEN) store_u16(cx.mblk + 2 * r, (uint16_t)(pos - prev));
+      else if (cx.listM) reinterpret_cast<uint16_t*>(cx.mblk)[r] = (uint16_t)(pos - prev);
+      else atomicOr(&sm->bm[pos >> 5], 1u << (pos & 31));
+      sm->mv[r] = (uint8_t)(x & kMant);
+    }
+    if (isR) {
+      const uint32_t r = baseR + __popc(lowR);
+      const uint32_t prev = lowR ? pR : carryR;
+      if (cx.listR) store_u16(cx.rblk + 2 * r, (uint16_t)(pos - prev));
+      else atomicOr(&sm->bm[128 + (pos >> 5)], 1u << (pos & 31));
+      cx.rstream[r] = (uint16_t)x;
+    }
+    // carries: position of the last element of each class so far
+    const uint32_t topM = __shfl_sync(0xFFFFFFFFu, pos, bM ? 31 - __clz(bM) : 0);
+    const uint32_t topR = __shfl_sync(0xFFFFFFFFu, pos, bR ? 31 - __clz(bR) : 0);
+    if (bM) carryM = topM;
+    if (bR) carryR = topR;
+    baseM += __popc(bM);
+    baseR += __popc(bR);
+  }
+  __syncwarp();
+  // the mantissa-stream bytes owned by this chunk (first bit in one of its values)
+  const uint64_t b_lo = (7 * Mex + 7) >> 3, b_hi = (7 * (Mex + M) + 7) >> 3;
+  if (b_hi > b_lo) {
+    uint32_t after = 0;
+    // chunk-local value holding the first bit of the last owned byte (32-bit: the offset
+    // from the chunk's first mantissa bit is below 7*M + 8)
+    const uint32_t jl_last = (uint32_t)(8 * (b_hi - 1) - 7 * Mex) / 7;
+    if (jl_last + 1 == M && Mex + M < I.sum_m)
+      after = next_mant_value<FMT == 4>(g, g_job_end, cnt_next, aux_next, counts, slots);
+    put_mant_bytes(payload + I.m_start, b_lo, b_hi, Mex, M, after, cx);
+  }
+  if (!cx.listM || !cx.listR) {
+    __syncwarp();
+    if (!cx.listM) store_bitmap(cx.mblk, sm->bm, B);
+    if (!cx.listR) store_bitmap(cx.rblk, sm->bm + 128, B);
+  }
+  __syncwarp();
+}
+
+// Chunks whose changes fit their slot, each warp a contiguous range; the prefixes come from the
+// count scan (tile prefix + chunk prefix inside the tile).
 template <int FMT, bool OW>
 __global__ void __launch_bounds__(kThreads, 4)
 k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
@@ -681,166 +840,20 @@ k_emit(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
        const uint4* __restrict__ loc, const TileSum* __restrict__ tile_pre,
        const JobInfo* __restrict__ info) {
   __shared__ EmitSmem s_em[kWarps];
-  const int lane = threadIdx.x & 31;
-  const uint32_t lt = (1u << lane) - 1;
   const uint64_t gwarp = ((uint64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
   const uint64_t nwarps = ((uint64_t)gridDim.x * kThreads) >> 5;
   EmitSmem* sm = &s_em[threadIdx.x >> 5];
-
   uint32_t j = 0xFFFFFFFFu;
   uint64_t g_begin, g_end;
   warp_range(total_chunks, gwarp, nwarps, g_begin, g_end);
   for (uint64_t g = g_begin; g < g_end; g++) {
     j = advance_job(chunk_start, k, j, g);
-    // level 1: everything addressed by g and j alone, requested together
-    const uint8_t* slot = slots + g * kSlotBytes;
-    // the next chunk's slot header and first 96 entries into L2 while this one is emitted
-    if (g + 1 < g_end && lane < 4)
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(slot + kSlotBytes + 128 * lane));
-    const uint32_t* E = reinterpret_cast<const uint32_t*>(slot + kSlotHeader);
-    const uint32_t hdr = *reinterpret_cast<const uint32_t*>(slot);
-    uint32_t ent[8];
-    // the first 96 entries are read with the header (a slot always has room for them); they
-    // cover the whole list of most sparse chunks
-    ent[0] = E[lane];
-    ent[1] = E[32 + lane];
-    ent[2] = E[64 + lane];
     const uint4 lc = loc[g];
     const uint64_t c = g - chunk_start[j];
-    const uint64_t g_job_end = chunk_start[j + 1];
     const TileSum pre = tile_pre[tile_start[j] + c / kTileChunks];
-    constexpr bool GEN = FMT != 0;
-    const uint32_t cnt_here = GEN ? counts[g] : 0u;
-    const uint32_t cnt_next = g + 1 < g_job_end ? counts[g + 1] : 0u;
-    const uint32_t aux_next =
-        g + 1 < g_job_end ? reinterpret_cast<const uint32_t*>(slot + kSlotBytes)[1] : 0u;
     const JobInfo I = info[j];
-    uint8_t* payload = jobs[j].payload;
-    const uint64_t n = jobs[j].n;
-    if (I.status != BD_OK || (hdr & kSlotOverflow)) continue;
-
-    // level 2: the rest of the list
-    const uint32_t M = hdr & 0xFFFu, R = (hdr >> 12) & 0xFFFu, kk = M + R;
-#pragma unroll
-    for (int q = 3; q < 8; q++) ent[q] = 0u;
-    if (kk > 96) {
-#pragma unroll
-      for (int q = 3; q < 8; q++) {
-        const uint32_t i = 32 * q + lane;
-        if (i < kk) ent[q] = E[i];
-      }
-    }
-
-    const uint64_t e0 = c * kChunk;
-    const uint32_t L = (n - e0) < kChunk ? (uint32_t)(n - e0) : kChunk;
-    const uint32_t B = (L + 7) >> 3;
-    const uint64_t Pex = pre.p + lc.x, Mex = pre.m + lc.y, Rex = pre.r + lc.z;
-    const uint32_t nesc = wcount_e(cnt_here);
-    const bool rice = FMT == 4 && I.version == 4 && rice_compact(cnt_here, B);
-    const bool compact = rice || (FMT == 3 && I.version == 3 && choose_compact(M, R, nesc, B));
-    if (lane == 0)
-      reinterpret_cast<uint32_t*>(payload + count_table_offset(I.r_start, jobs[j].nchunks))[c] =
-          rice ? cnt_here : count_entry(GEN ? I.version : 1u, M, R, nesc, compact);
-    EmitCtx cx;
-    emit_ctx(cx, payload, I, M, R, B, Pex, Rex, sm);
-    if constexpr (FMT == 4) {
-      if (rice) {
-        cx.listM = cx.listR = true;   // no bitmap
-        const uint32_t nb = (cnt_here >> 21) & 0x3FFu, K = (cnt_here >> 18) & 0x7u;
-        for (uint32_t i = lane; i < (nb + 3) / 4; i += 32) sm->bm[i] = 0;
-        __syncwarp();
-        rice_write<OW>(E, kk, R, K, sm->bm, cx.rstream, sm->mv);
-        __syncwarp();
-        store_bitmap(payload + I.p_start + Pex, sm->bm, nb);
-      }
-    }
-    if (FMT == 3 && compact) {
-      cx.listM = cx.listR = true;   // no bitmap
-      const CompactOut o{payload + I.p_start + Pex,
-                         reinterpret_cast<uint16_t*>(payload + I.x_start) + pre.e + lc.w,
-                         cx.rstream, sm->mv, kk};
-      CompactState cs{0xFFFFFFFFu, 0, 0, 0, 0};
-#pragma unroll
-      for (int q = 0; q < 8; q++) {
-        if (32u * q >= kk) break;
-        compact_batch<OW>(ent[q], 32u * q + lane < kk, cs, o);
-      }
-    }
-    if (!cx.listM || !cx.listR) {
-      for (int i = lane; i < 256; i += 32) sm->bm[i] = 0;
-      __syncwarp();
-    }
-    uint32_t baseM = 0, baseR = 0, carryM = 0, carryR = 0;
-#pragma unroll
-    for (int q = 0; q < 8; q++) {
-      if (compact || 32u * q >= kk) break;
-      const uint32_t e = ent[q], pos = OW ? ent_pos(e) : e >> 16, x = e & 0xFFFFu;
-      const bool valid = 32u * q + lane < kk;
-      const bool rare = OW ? (e & kEntRare) != 0 : (x & kSignExp) != 0;
-      const bool isR = valid && rare;
-      const bool isM = valid && !rare;
-      const uint32_t bM = __ballot_sync(0xFFFFFFFFu, isM), bR = __ballot_sync(0xFFFFFFFFu, isR);
-      // (In versions 1 and 2 every M block starts at an even offset; after an odd-length
-      // compact block of version 3 it may not, hence the alignment-checking stores there.)
-      if (bR == 0 && cx.listM) {
-        // no rare entry in this batch: the mantissa-only entries are the first lanes in order
-        const uint32_t prevL = __shfl_up_sync(0xFFFFFFFFu, pos, 1);
-        if (isM) {
-          const uint32_t r = baseM + lane;
-          const uint32_t prev = lane ? prevL : carryM;
-          if (GEN) store_u16(cx.mblk + 2 * r, (uint16_t)(pos - prev));
-          else reinterpret_cast<uint16_t*>(cx.mblk)[r] = (uint16_t)(pos - prev);
-          sm->mv[r] = (uint8_t)(x & kMant);
-        }
-        const uint32_t cntM = __popc(bM);
-        carryM = __shfl_sync(0xFFFFFFFFu, pos, cntM - 1);
-        baseM += cntM;
-        continue;
-      }
-      const uint32_t lowM = bM & lt, lowR = bR & lt;
-      const uint32_t pM = __shfl_sync(0xFFFFFFFFu, pos, lowM ? 31 - __clz(lowM) : lane);
-      const uint32_t pR = __shfl_sync(0xFFFFFFFFu, pos, lowR ? 31 - __clz(lowR) : lane);
-      if (isM) {
-        const uint32_t r = baseM + __popc(lowM);
-        const uint32_t prev = lowM ? pM : carryM;
-        if (cx.listM && GEN) store_u16(cx.mblk + 2 * r, (uint16_t)(pos - prev));
-        else if (cx.listM) reinterpret_cast<uint16_t*>(cx.mblk)[r] = (uint16_t)(pos - prev);
-        else atomicOr(&sm->bm[pos >> 5], 1u << (pos & 31));
-        sm->mv[r] = (uint8_t)(x & kMant);
-      }
-      if (isR) {
-        const uint32_t r = baseR + __popc(lowR);
-        const uint32_t prev = lowR ? pR : carryR;
-        if (cx.listR) store_u16(cx.rblk + 2 * r, (uint16_t)(pos - prev));
-        else atomicOr(&sm->bm[128 + (pos >> 5)], 1u << (pos & 31));
-        cx.rstream[r] = (uint16_t)x;
-      }
-      // carries: position of the last element of each class so far
-      const uint32_t topM = __shfl_sync(0xFFFFFFFFu, pos, bM ? 31 - __clz(bM) : 0);
-      const uint32_t topR = __shfl_sync(0xFFFFFFFFu, pos, bR ? 31 - __clz(bR) : 0);
-      if (bM) carryM = topM;
-      if (bR) carryR = topR;
-      baseM += __popc(bM);
-      baseR += __popc(bR);
-    }
-    __syncwarp();
-    // the mantissa-stream bytes owned by this chunk (first bit in one of its values)
-    const uint64_t b_lo = (7 * Mex + 7) >> 3, b_hi = (7 * (Mex + M) + 7) >> 3;
-    if (b_hi > b_lo) {
-      uint32_t after = 0;
-      // chunk-local value holding the first bit of the last owned byte (32-bit: the offset
-      // from the chunk's first mantissa bit is below 7*M + 8)
-      const uint32_t jl_last = (uint32_t)(8 * (b_hi - 1) - 7 * Mex) / 7;
-      if (jl_last + 1 == M && Mex + M < I.sum_m)
-        after = next_mant_value<FMT == 4>(g, g_job_end, cnt_next, aux_next, counts, slots);
-      put_mant_bytes(payload + I.m_start, b_lo, b_hi, Mex, M, after, cx);
-    }
-    if (!cx.listM || !cx.listR) {
-      __syncwarp();
-      if (!cx.listM) store_bitmap(cx.mblk, sm->bm, B);
-      if (!cx.listR) store_bitmap(cx.rblk, sm->bm + 128, B);
-    }
-    __syncwarp();
+    emit_chunk<FMT, OW>(jobs, g, j, c, chunk_start[j + 1], g + 1 < g_end, I, pre.p + lc.x,
+                        pre.m + lc.y, pre.r + lc.z, pre.e + lc.w, counts, slots, sm);
   }
 }
 
@@ -865,13 +878,17 @@ __device__ __noinline__ void emit_rice_list(const uint32_t* lst, uint32_t cnt, b
 // whose two values are known are written and the value window keeps only its last value.
 // A compact chunk (at most kCompactMax changes) first gathers its changes in position order
 // into a shared list, then emits them 32 at a time as emit does.
+// FUSED: after the fused compress, which leaves per-batch prefixes (batch_pre, batches of
+// bchunks chunks from batch_start) instead of the count scan's tile and chunk prefixes.
+template <bool FUSED>
 __global__ void __launch_bounds__(kThreads)
 k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
              const uint64_t* __restrict__ tile_start, uint32_t k,
              const uint32_t* __restrict__ list_count, const uint32_t* __restrict__ list,
              const uint32_t* __restrict__ counts, const uint8_t* __restrict__ slots,
              const uint4* __restrict__ loc, const TileSum* __restrict__ tile_pre,
-             const JobInfo* __restrict__ info) {
+             const JobInfo* __restrict__ info, const uint64_t* __restrict__ batch_start,
+             const TileSum* __restrict__ batch_pre, uint32_t bchunks) {
   __shared__ EmitSmem s_em[kWarps];
   __shared__ uint32_t s_list[kWarps][kCompactMax];   // compact chunks: pos << 16 | x
   const int lane = threadIdx.x & 31;
@@ -895,9 +912,28 @@ k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
     const uint32_t cnt = counts[g];
     const uint32_t M = v4count_m(cnt), R = v4count_r(cnt);
     const uint32_t E = I.version == 3 ? wcount_e(cnt) : 0u;
-    const TileSum pre = tile_pre[tile_start[j] + c / kTileChunks];
-    const uint4 lc = loc[g];
-    const uint64_t Pex = pre.p + lc.x, Mex = pre.m + lc.y, Rex = pre.r + lc.z;
+    uint64_t Pex, Mex, Rex, Xex;
+    if (FUSED) {   // the batch's prefix plus the full chunks before this one in its batch
+      const uint64_t cb = c - c % bchunks;
+      const TileSum pre = batch_pre[batch_start[j] + c / bchunks];
+      Pex = pre.p;
+      Mex = pre.m;
+      Rex = pre.r;
+      Xex = 0;
+      for (uint64_t c2 = cb; c2 < c; c2++) {
+        const uint32_t w = counts[chunk_start[j] + c2];
+        Pex += block_bytes(wcount_m(w), kChunkBitmap) + block_bytes(wcount_r(w), kChunkBitmap);
+        Mex += wcount_m(w);
+        Rex += wcount_r(w);
+      }
+    } else {
+      const TileSum pre = tile_pre[tile_start[j] + c / kTileChunks];
+      const uint4 lc = loc[g];
+      Pex = pre.p + lc.x;
+      Mex = pre.m + lc.y;
+      Rex = pre.r + lc.z;
+      Xex = pre.e + lc.w;
+    }
     const bool rice = I.version == 4 && rice_compact(cnt, B);
     const bool compact = rice || (I.version == 3 && choose_compact(M, R, E, B));
     const bool ow = (J.flags & kFlagOverwrite) != 0;
@@ -950,7 +986,7 @@ k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
         emit_rice_list(lst, cnt, ow, cx.rstream, sm, payload + I.p_start + Pex);
       } else {
         const CompactOut o{payload + I.p_start + Pex,
-                           reinterpret_cast<uint16_t*>(payload + I.x_start) + pre.e + lc.w,
+                           reinterpret_cast<uint16_t*>(payload + I.x_start) + Xex,
                            cx.rstream, sm->mv, kk};
         CompactState cs{0xFFFFFFFFu, 0, 0, 0, 0};
         for (uint32_t i0 = 0; i0 < kk; i0 += 32) {
@@ -1010,6 +1046,219 @@ k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
   }
 }
 
+// ------------------------------------------------------------------------ fused compress
+//
+// XOR payloads of versions 1 and 2 in one persistent kernel instead of encode_slots, the count
+// scan and emit.  Warps claim batches of consecutive chunks of one tensor (up to 32, per call) in
+// order and encode them (encode_chunk, as encode_slots does); the warp that completes the last
+// batch of a tensor scans the tensor's batch totals, finishes it (offsets, size, checksum,
+// header) and publishes it.  Every batch is claimed a second time, in the same order, as emit
+// work, which writes it into the payload (emit_chunk, as emit does): one warp in
+// kEmitterEvery takes emit work whenever the next emit batch belongs to a published tensor,
+// the others encode until no encode batch is left, then all emit.  A warp that has claimed an
+// emit batch of a tensor not yet published encodes further batches while it waits.  Against
+// the separate kernels this saves the count-scan launches and the gaps between kernels (a
+// schedule that emits only after all encoding measured almost the same as this one).  Every claimed encode batch is held by a warp that is
+// running it, and encoding and finishing never wait, so every wait ends, whether or not all
+// blocks are resident; the waits are bounded all the same (kWaitLimit idle polls), after which
+// the warp reports BD_ERR_CUDA for the tensor and the call and stops.
+constexpr uint32_t kWaitLimit = 1u << 24;
+constexpr uint32_t kEmitterEvery = 6;
+
+struct FusedArgs {
+  const CJob* jobs;
+  const uint64_t* chunk_start;
+  const uint64_t* batch_start;
+  uint32_t* counts;
+  uint8_t* slots;
+  uint8_t* ck_base;
+  uint32_t* list_count;
+  uint32_t* list;
+  uint4* batch_tot;
+  TileSum* batch_pre;
+  JobInfo* info;
+  uint32_t* ctl;
+  int32_t* status_all;
+  uint64_t batches;
+  uint32_t k;
+  uint32_t bchunks;   // chunks per batch
+};
+
+// A u32 that other warps change, read by lane 0 and given to the whole warp.
+__device__ __forceinline__ uint32_t warp_read(const uint32_t* p) {
+  uint32_t v = 0;
+  if ((threadIdx.x & 31) == 0) v = *reinterpret_cast<const volatile uint32_t*>(p);
+  return __shfl_sync(0xFFFFFFFFu, v, 0);
+}
+// The next value of a work counter, claimed for the whole warp.
+__device__ __forceinline__ uint32_t warp_claim(uint32_t* ctr) {
+  uint32_t v = 0;
+  if ((threadIdx.x & 31) == 0) v = atomicAdd(ctr, 1u);
+  return __shfl_sync(0xFFFFFFFFu, v, 0);
+}
+
+// Scans the batch totals of tensor j (all of its batches encoded) into exclusive prefixes,
+// finishes the tensor and publishes it.
+__device__ __noinline__ void fused_finish(const FusedArgs& a, uint32_t j) {
+  const int lane = threadIdx.x & 31;
+  __threadfence();   // the totals, counts, slots and checksum terms of the other batches
+  const uint64_t b0 = a.batch_start[j], nb = a.batch_start[j + 1] - b0;
+  uint64_t rP = 0, rM = 0, rR = 0;
+  for (uint64_t i0 = 0; i0 < nb; i0 += 32) {
+    uint4 t = make_uint4(0, 0, 0, 0);
+    if (i0 + lane < nb) t = __ldcg(&a.batch_tot[b0 + i0 + lane]);
+    // per batch at most 32 chunks (32 KiB of positions, 131072 values): 32 batches fit in
+    // 32 bits
+    const uint32_t iP = warp_incl_scan(t.x), iM = warp_incl_scan(t.y), iR = warp_incl_scan(t.z);
+    if (i0 + lane < nb)
+      a.batch_pre[b0 + i0 + lane] = TileSum{rP + iP - t.x, rM + iM - t.y, rR + iR - t.z, 0};
+    rP += __shfl_sync(0xFFFFFFFFu, iP, 31);
+    rM += __shfl_sync(0xFFFFFFFFu, iM, 31);
+    rR += __shfl_sync(0xFFFFFFFFu, iR, 31);
+  }
+  __threadfence();
+  __syncwarp();
+  if (lane == 0) {
+    JobInfo I{};
+    I.sum_p = rP;
+    I.sum_m = rM;
+    I.sum_r = rR;
+    I.sum_e = 0;
+    I.chunk_err = 0;
+    finish_compress_job(a.jobs[j], j, I, a.ck_base, a.info, a.status_all);
+    __threadfence();   // the prefixes, the tensor's info and header before the flag
+    *reinterpret_cast<volatile uint32_t*>(&a.ctl[kCtlTensors + 2 * j + 1]) = 1u;
+  }
+  __syncwarp();
+}
+
+// Encodes batch b; the warp completing its tensor finishes it.
+__device__ __forceinline__ void fused_encode(const FusedArgs& a, uint32_t b, uint4* xs) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t j = find_job(a.batch_start, a.k, b);
+  const CJob& J = a.jobs[j];
+  const uint64_t n = J.n;
+  const uint64_t c0 = (b - a.batch_start[j]) * a.bchunks;
+  const uint64_t c1 = min(c0 + a.bchunks, J.nchunks);
+  uint64_t ck = 0;
+  uint32_t sP = 0, sM = 0, sR = 0;
+  for (uint64_t c = c0; c < c1; c++) {
+    const uint64_t g = J.chunk_base + c, e0 = c * kChunk;
+    uint32_t* slot = reinterpret_cast<uint32_t*>(a.slots + g * kSlotBytes);
+    uint32_t word;
+    if (e0 + kChunk <= n) {   // the chunk of old and new into L2 ahead of the step loads
+      prefetch_chunk_l2(J.old + e0);
+      prefetch_chunk_l2(J.neu + e0);
+      word = encode_chunk<true, 0, false>(J.old, J.neu, n, e0, slot, ck, g, a.counts,
+                                          a.list_count, a.list, xs, xs);
+    } else {
+      word = encode_chunk<false, 0, false>(J.old, J.neu, n, e0, slot, ck, g, a.counts,
+                                           a.list_count, a.list, xs, xs);
+    }
+    const uint32_t M = wcount_m(word), R = wcount_r(word);
+    const uint32_t L = (n - e0) < kChunk ? (uint32_t)(n - e0) : kChunk, B = (L + 7) >> 3;
+    sP += block_bytes(M, B) + block_bytes(R, B);
+    sM += M;
+    sR += R;
+  }
+  const uint64_t s = warp_sum64(ck);
+  if (lane == 0) {
+    if (c1 > c0) atomicAdd(ck_slot(a.ck_base, j, b), (unsigned long long)s);
+    a.batch_tot[b] = make_uint4(sP, sM, sR, 0);
+  }
+  __threadfence();   // this batch's slots, counts, total and checksum terms before its count
+  __syncwarp();
+  uint32_t fin = 0;
+  if (lane == 0) {
+    const uint32_t cnt = (uint32_t)(c1 - c0);
+    fin = atomicAdd(&a.ctl[kCtlTensors + 2 * j], cnt) + cnt == (uint32_t)J.nchunks;
+  }
+  if (__shfl_sync(0xFFFFFFFFu, fin, 0)) fused_finish(a, j);
+}
+
+// Emits batch e of a published tensor.
+__device__ __forceinline__ void fused_emit(const FusedArgs& a, uint32_t e, EmitSmem* sm) {
+  const uint32_t j = find_job(a.batch_start, a.k, e);
+  const CJob& J = a.jobs[j];
+  const uint64_t c0 = (e - a.batch_start[j]) * a.bchunks;
+  const uint64_t c1 = min(c0 + a.bchunks, J.nchunks);
+  const JobInfo I = a.info[j];
+  if (c1 <= c0 || I.status != BD_OK) return;
+  const TileSum pre = a.batch_pre[e];
+  uint64_t Pex = pre.p, Mex = pre.m, Rex = pre.r;
+  const uint64_t g_job_end = J.chunk_base + J.nchunks;
+  for (uint64_t c = c0; c < c1; c++) {
+    const uint64_t g = J.chunk_base + c;
+    const uint32_t w = a.counts[g];
+    emit_chunk<0, false>(a.jobs, g, j, c, g_job_end, c + 1 < c1, I, Pex, Mex, Rex, 0, a.counts,
+                         a.slots, sm);
+    const uint64_t e0 = c * kChunk;
+    const uint32_t L = (J.n - e0) < kChunk ? (uint32_t)(J.n - e0) : kChunk, B = (L + 7) >> 3;
+    Pex += block_bytes(wcount_m(w), B) + block_bytes(wcount_r(w), B);
+    Mex += wcount_m(w);
+    Rex += wcount_r(w);
+  }
+}
+
+// Waits until the tensor of emit batch e is published, encoding unclaimed batches meanwhile.
+// Returns false when it gave up (reported as BD_ERR_CUDA).
+__device__ __noinline__ bool fused_wait(const FusedArgs& a, uint32_t e, uint4* xs) {
+  const uint32_t j = find_job(a.batch_start, a.k, e);
+  const uint32_t nbatches = (uint32_t)a.batches;
+  uint32_t idle = 0;
+  while (warp_read(&a.ctl[kCtlTensors + 2 * j + 1]) == 0) {
+    if (warp_read(&a.ctl[0]) < nbatches) {
+      const uint32_t b = warp_claim(&a.ctl[0]);
+      if (b < nbatches) {
+        fused_encode(a, b, xs);
+        continue;
+      }
+    }
+    if (++idle > kWaitLimit) {
+      if ((threadIdx.x & 31) == 0) {
+        if (a.jobs[j].d_status) *a.jobs[j].d_status = BD_ERR_CUDA;
+        if (a.status_all) atomicMax(reinterpret_cast<int*>(a.status_all), (int)BD_ERR_CUDA);
+      }
+      return false;
+    }
+    __nanosleep(256);
+  }
+  __threadfence();   // the tensor's prefixes, info, counts and slots after its flag
+  return true;
+}
+
+__global__ void __launch_bounds__(kThreads, 4) k_compress_fused(const FusedArgs a) {
+  __shared__ uint4 s_xs[kThreads][2];   // encode: the 16 XOR values of a thread's step
+  __shared__ EmitSmem s_em[kWarps];     // emit: per-warp bitmaps and mantissa values
+  uint4* xs = s_xs[threadIdx.x];
+  EmitSmem* sm = &s_em[threadIdx.x >> 5];
+  const uint32_t nbatches = (uint32_t)a.batches;
+  // While batches remain to be encoded, one warp in kEmitterEvery takes emit work: all warps
+  // switching to emit as soon as a tensor is published drained the DRAM stream of the encoding
+  // (slower than the separate kernels); a few emitters keep it flowing.
+  const bool emitter = ((((uint64_t)blockIdx.x * kThreads + threadIdx.x) >> 5) % kEmitterEvery) == 0;
+  for (;;) {
+    // emit work first, when the next emit batch belongs to a published tensor
+    const uint32_t peek = emitter ? warp_read(&a.ctl[1]) : nbatches;
+    bool emit = false;
+    if (peek < nbatches) {
+      const uint32_t jp = find_job(a.batch_start, a.k, peek);
+      emit = warp_read(&a.ctl[kCtlTensors + 2 * jp + 1]) != 0;
+    }
+    if (!emit) {
+      const uint32_t b = warp_claim(&a.ctl[0]);
+      if (b < nbatches) {
+        fused_encode(a, b, xs);
+        continue;
+      }
+    }
+    const uint32_t e = warp_claim(&a.ctl[1]);   // (once encoding is all handed out, only this)
+    if (e >= nbatches) break;
+    if (!fused_wait(a, e, xs)) return;
+    fused_emit(a, e, sm);
+  }
+}
+
 template <typename K>
 int blocks_per_sm(K kernel, int threads) {
   int per_sm = 0;
@@ -1058,11 +1307,11 @@ cudaError_t launch_encode_slots(const LaunchCtx& c, uint32_t fmt, bool overwrite
   return cudaGetLastError();
 }
 
-cudaError_t launch_emit_dense(const LaunchCtx& c) {
+cudaError_t launch_emit_dense(const LaunchCtx& c, bool fused) {
   if (c.chunks == 0) return cudaSuccess;
-  static const int per_sm = blocks_per_sm(k_emit_dense, kThreads);
+  static const int per_sm = blocks_per_sm(k_emit_dense<false>, kThreads);
   const uint64_t grid = cap_grid((uint64_t)per_sm * c.sms, kWarps, c.chunks);
-  k_emit_dense<<<(unsigned)grid, kThreads, 0, c.stream>>>(
+  (fused ? k_emit_dense<true> : k_emit_dense<false>)<<<(unsigned)grid, kThreads, 0, c.stream>>>(
       reinterpret_cast<const CJob*>(c.ws + c.lay.jobs),
       reinterpret_cast<const uint64_t*>(c.ws + c.lay.chunk_start),
       reinterpret_cast<const uint64_t*>(c.ws + c.lay.tile_start), c.k,
@@ -1071,7 +1320,35 @@ cudaError_t launch_emit_dense(const LaunchCtx& c) {
       reinterpret_cast<const uint32_t*>(c.ws + c.lay.counts), c.ws + c.lay.slots,
       reinterpret_cast<const uint4*>(c.ws + c.lay.loc),
       reinterpret_cast<const TileSum*>(c.ws + c.lay.tile_pre),
-      reinterpret_cast<const JobInfo*>(c.ws + c.lay.info));
+      reinterpret_cast<const JobInfo*>(c.ws + c.lay.info),
+      reinterpret_cast<const uint64_t*>(c.ws + c.lay.batch_start),
+      reinterpret_cast<const TileSum*>(c.ws + c.lay.batch_pre), c.bchunks);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_compress_fused(const LaunchCtx& c, int32_t* d_status_all) {
+  if (c.batches == 0) return cudaSuccess;
+  static const int per_sm = blocks_per_sm(k_compress_fused, kThreads);
+  // persistent: one wave of resident blocks (fewer when there is little work)
+  const uint64_t grid = cap_grid((uint64_t)per_sm * c.sms, kWarps, c.batches);
+  FusedArgs a;
+  a.jobs = reinterpret_cast<const CJob*>(c.ws + c.lay.jobs);
+  a.chunk_start = reinterpret_cast<const uint64_t*>(c.ws + c.lay.chunk_start);
+  a.batch_start = reinterpret_cast<const uint64_t*>(c.ws + c.lay.batch_start);
+  a.counts = reinterpret_cast<uint32_t*>(c.ws + c.lay.counts);
+  a.slots = c.ws + c.lay.slots;
+  a.ck_base = c.ws + c.lay.ck;
+  a.list_count = reinterpret_cast<uint32_t*>(c.ws + c.lay.overflow);
+  a.list = reinterpret_cast<uint32_t*>(c.ws + c.lay.ovf_list);
+  a.batch_tot = reinterpret_cast<uint4*>(c.ws + c.lay.batch_tot);
+  a.batch_pre = reinterpret_cast<TileSum*>(c.ws + c.lay.batch_pre);
+  a.info = reinterpret_cast<JobInfo*>(c.ws + c.lay.info);
+  a.ctl = reinterpret_cast<uint32_t*>(c.ws + c.lay.fused_ctl);
+  a.status_all = d_status_all;
+  a.batches = c.batches;
+  a.k = c.k;
+  a.bchunks = c.bchunks;
+  k_compress_fused<<<(unsigned)grid, kThreads, 0, c.stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -328,8 +328,65 @@ constexpr int kCkSlots = 8;
 constexpr int kCkStride = 8;  // u64 per slot
 constexpr int kCkBytes = kCkSlots * kCkStride * 8;
 
+constexpr uint64_t kMagic = 0x31544C4436314642ull;  // "BF16DLT1" little-endian
+__host__ __device__ __forceinline__ uint64_t header_bytes(uint32_t version) {
+  return version >= 2 ? kHeaderV2 : kHeader;
+}
+
+// The end of a compress for tensor j, one thread, once its totals are in I (sum_p, sum_m,
+// sum_r, sum_e) and its checksum terms in its accumulators: section offsets, size and status
+// (capacity), the checksum, the header (only when the payload fits), the per-tensor outputs,
+// info[j] and the call's largest status.
+__device__ __forceinline__ void finish_compress_job(const CJob& J, uint32_t j, JobInfo& I,
+                                                    const uint8_t* ck_base, JobInfo* info,
+                                                    int32_t* status_all) {
+  I.version = J.version;
+  I.flags = J.flags;
+  I.r_start = header_bytes(J.version) + 4 * J.nchunks;
+  I.x_start = I.r_start + 2 * I.sum_r;
+  I.p_start = I.x_start + 2 * I.sum_e;
+  I.m_start = I.p_start + I.sum_p;
+  I.total = I.m_start + (7 * I.sum_m + 7) / 8;
+  I.status = I.total > J.cap ? BD_ERR_CAPACITY : BD_OK;
+  const uint64_t* ck = reinterpret_cast<const uint64_t*>(ck_base + (uint64_t)j * kCkBytes);
+  uint64_t sum = 0;
+  for (int s = 0; s < kCkSlots; s++) sum += ck[s * kCkStride];
+  *J.d_size = I.total;
+  *J.d_checksum = sum;
+  if (I.status == BD_OK) {
+    uint64_t* h = reinterpret_cast<uint64_t*>(J.payload);
+    h[0] = kMagic;
+    h[1] = (uint64_t)J.version | ((uint64_t)kChunk << 32);
+    h[2] = J.n;
+    h[3] = J.nchunks;
+    h[4] = I.sum_m;
+    h[5] = I.sum_r;
+    h[6] = I.sum_p;
+    h[7] = I.total;
+    if (J.version >= 2) {   // the base this payload applies to, and the flags
+      h[8] = *J.d_base;
+      h[9] = J.flags;
+    }
+  }
+  if (J.d_status) *J.d_status = I.status;
+  info[j] = I;
+  if (status_all) atomicMax(reinterpret_cast<int*>(status_all), I.status);
+}
+
 // Scan tiles: chunks per tile of the count scan.
 constexpr uint32_t kTileChunks = 1024;
+
+// Fused compress (XOR payloads of versions 1 and 2): batches of up to `bchunks` consecutive
+// chunks of one tensor (chosen per call, at most kMaxBatchChunks; an empty tensor has one
+// empty batch, so that its header is written), and control words in the zeroed state: [0] the
+// next encode batch to hand out, [1] the next emit batch, then per tensor j
+// [kCtlTensors + 2j] its chunks encoded so far and [kCtlTensors + 2j + 1] its flag "scanned,
+// emit may start".
+constexpr uint32_t kMaxBatchChunks = 32;
+constexpr uint32_t kCtlTensors = 4;
+__host__ __device__ __forceinline__ uint64_t tensor_batches(uint64_t nchunks, uint32_t bchunks) {
+  return nchunks ? (nchunks + bchunks - 1) / bchunks : 1;
+}
 
 struct TileSum {   // totals of one scan tile (or their exclusive prefix)
   uint64_t p, m, r, e;   // position bytes, M, R, escaped gaps (X-stream values)
@@ -388,6 +445,10 @@ struct WsLayout {
   uint64_t overflow;     // decompress: u32 words in the zeroed state -- the count of listed
                          // chunks, then kFlagV3Word ...
   uint64_t ovf_list;     // ... and Ctot u32 chunk indices handled by the block-level apply
+  uint64_t fused_ctl;    // compress: fused-compress control words (zeroed state)
+  uint64_t batch_start;  // compress: (k+1) u64, global index of tensor j's first batch
+  uint64_t batch_tot;    // compress: per batch uint4 (position bytes, M, R, 0)
+  uint64_t batch_pre;    // compress: per batch TileSum, exclusive prefix inside its tensor
   uint64_t total;
 };
 
@@ -475,6 +536,8 @@ struct LaunchCtx {
   uint32_t k;          // jobs
   uint64_t chunks;     // total chunks
   uint64_t tiles;      // total scan tiles
+  uint64_t batches;    // total fused-compress batches
+  uint32_t bchunks;    // chunks per fused-compress batch
 };
 
 // fmt: 0 (XOR payloads of versions 1 and 2), 3 (version 3, and overwrite payloads of version
@@ -483,7 +546,10 @@ cudaError_t launch_encode_slots(const LaunchCtx& c, uint32_t fmt, bool overwrite
 cudaError_t launch_scan_tiles(const LaunchCtx& c, bool decompress);
 cudaError_t launch_scan_jobs(const LaunchCtx& c, bool decompress, int32_t* d_status_all);
 cudaError_t launch_emit(const LaunchCtx& c, uint32_t fmt, bool overwrite);
-cudaError_t launch_emit_dense(const LaunchCtx& c);
+cudaError_t launch_emit_dense(const LaunchCtx& c, bool fused = false);
+// The fused compress of XOR payloads of versions 1 and 2 (encode, scan and emit in one
+// persistent kernel; emit_dense follows it).
+cudaError_t launch_compress_fused(const LaunchCtx& c, int32_t* d_status_all);
 cudaError_t launch_apply_chunks(const LaunchCtx& c);
 cudaError_t launch_apply_incremental(const LaunchCtx& c);
 cudaError_t launch_copy_jobs(const LaunchCtx& c);

@@ -20,7 +20,6 @@ namespace bd {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr uint64_t kMagic = 0x31544C4436314642ull;  // "BF16DLT1" little-endian
 
 struct JobView {
   uint64_t n, nchunks, chunk_base;
@@ -46,9 +45,6 @@ __device__ __forceinline__ JobView view(const void* jobs, uint32_t j) {
 // Version of a payload as the scan reads it (0 when too short to hold one).
 __device__ __forceinline__ uint32_t payload_version(const uint8_t* payload, uint64_t size) {
   return size >= 16 ? reinterpret_cast<const uint32_t*>(payload)[2] : 0;
-}
-__host__ __device__ __forceinline__ uint64_t header_bytes(uint32_t version) {
-  return version >= 2 ? kHeaderV2 : kHeader;
 }
 
 template <bool DEC>
@@ -179,38 +175,8 @@ k_scan_jobs(const void* __restrict__ jobs, const uint64_t* __restrict__ tile_sta
     I.sum_p = rP; I.sum_m = rM; I.sum_r = rR; I.sum_e = rE;
     I.chunk_err = 0;
     if (!DEC) {
-      const CJob& J = reinterpret_cast<const CJob*>(jobs)[j];
-      I.version = J.version;
-      I.flags = J.flags;
-      I.r_start = header_bytes(J.version) + 4 * J.nchunks;
-      I.x_start = I.r_start + 2 * rR;
-      I.p_start = I.x_start + 2 * rE;
-      I.m_start = I.p_start + rP;
-      I.total = I.m_start + (7 * rM + 7) / 8;
-      I.status = I.total > J.cap ? BD_ERR_CAPACITY : BD_OK;
-      const uint64_t* ck = reinterpret_cast<const uint64_t*>(ck_base + (uint64_t)j * kCkBytes);
-      uint64_t sum = 0;
-      for (int s = 0; s < kCkSlots; s++) sum += ck[s * kCkStride];
-      *J.d_size = I.total;
-      *J.d_checksum = sum;
-      if (I.status == BD_OK) {
-        uint64_t* h = reinterpret_cast<uint64_t*>(J.payload);
-        h[0] = kMagic;
-        h[1] = (uint64_t)J.version | ((uint64_t)kChunk << 32);
-        h[2] = J.n;
-        h[3] = J.nchunks;
-        h[4] = rM;
-        h[5] = rR;
-        h[6] = rP;
-        h[7] = I.total;
-        if (J.version >= 2) {   // the base this payload applies to, and the flags
-          h[8] = *J.d_base;
-          h[9] = J.flags;
-        }
-      }
-      if (J.d_status) *J.d_status = I.status;
-      info[j] = I;
-      if (status_all) atomicMax(reinterpret_cast<int*>(status_all), I.status);
+      finish_compress_job(reinterpret_cast<const CJob*>(jobs)[j], j, I, ck_base, info,
+                          status_all);
     } else {
       const DJob& J = reinterpret_cast<const DJob*>(jobs)[j];
       int32_t st = info[j].status;
