@@ -661,8 +661,8 @@ def run_ours(args) -> None:
     app_ach = app_bytes / (ma * 1e-3) / 1e9
     dom = "compress" if mc >= ma else "apply"
     roof = {"bound": "hbm",
-            "kernel": ("compress phase (bd_compress_batch: encode_slots + count scan + emit + "
-                       "emit_dense)" if dom == "compress" else
+            "kernel": ("compress phase (bd_compress_batch: the fused compress kernel, then "
+                       "emit_dense for the chunks too dense for a slot)" if dom == "compress" else
                        "apply phase (bd_decompress_batch: count scan + apply_chunks + apply_dense "
                        "+ apply_finish)"),
             "achieved": round(comp_ach if dom == "compress" else app_ach, 1),
@@ -723,10 +723,14 @@ def run_ours(args) -> None:
         cpu = oracle_baseline(specs, args.cpu_sample_elems, dev)
         cpu["fanout"] = oracle_fanout(specs, args.cpu_sample_elems)
 
-    blobs_c = -(-(128 * len(specs) + 2 * 8 * (len(specs) + 1) + 1024) // 30720)
-    # compress: tensor-table uploads + encode, scan x2, emit, emit_dense; decompress: uploads +
-    # scan x2, both builds of apply_chunks (one returns at once), apply_dense, apply_finish
-    launches_per_step = (blobs_c + 5) + (blobs_c + 6)
+    # tensor-table uploads (30 KiB each): the tensor table and the chunk, tile and (compress)
+    # batch start arrays, each section 256-byte aligned
+    k = len(specs)
+    blobs_c = -(-(128 * k + 3 * 8 * (k + 1) + 3 * 256) // 30720)
+    blobs_d = -(-(128 * k + 2 * 8 * (k + 1) + 2 * 256) // 30720)
+    # compress: uploads + the fused compress + emit_dense; decompress: uploads + scan x2, both
+    # builds of apply_chunks (one returns at once), apply_dense, apply_finish
+    launches_per_step = (blobs_c + 2) + (blobs_d + 6)
 
     if rank == 0:
         line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
