@@ -5,6 +5,7 @@
 // delta_compress(src, dst) -> (compressed_diff, checksum); delta_decompress(src,
 // compressed_diff, checksum) -> restored) and "GPU-accelerated Weight Teleportation",
 // section "Delta update algebra" (old XOR mask = new).
+#include <algorithm>
 #include <cstring>
 #include <memory>
 #include <vector>
@@ -183,7 +184,7 @@ int compress_impl(const bd_compress_item* items, const uint64_t* const* bases, u
   uint64_t* cstart = reinterpret_cast<uint64_t*>(host.data() + (lay.chunk_start - lay.jobs));
   uint64_t* tstart = reinterpret_cast<uint64_t*>(host.data() + (lay.tile_start - lay.jobs));
   uint64_t* bstart = reinterpret_cast<uint64_t*>(host.data() + (lay.batch_start - lay.jobs));
-  uint64_t cb = 0, tb = 0, bb = 0;
+  uint64_t cb = 0, tb = 0, bb = 0, most_batches = 0;
   for (uint32_t i = 0; i < k; i++) {
     const bd_compress_item& it = items[i];
     CJob& J = jobs[i];
@@ -207,6 +208,7 @@ int compress_impl(const bd_compress_item* items, const uint64_t* const* bases, u
     cb += J.nchunks;
     tb += (J.nchunks + kTileChunks - 1) / kTileChunks;
     bb += tensor_batches(J.nchunks, bchunks);
+    most_batches = std::max(most_batches, tensor_batches(J.nchunks, bchunks));
   }
   cstart[k] = cb;
   tstart[k] = tb;
@@ -222,7 +224,7 @@ int compress_impl(const bd_compress_item* items, const uint64_t* const* bases, u
   // the kernel builds: version 4, version 3 (also every overwrite payload of version 2), or
   // the XOR payloads of versions 1 and 2
   const uint32_t fmt = version == 4 ? 4u : (version == 3 || overwrite) ? 3u : 0u;
-  if (fmt == 0) {   // XOR payloads of versions 1 and 2: the fused compress
+  if (fmt == 0 && most_batches <= kMaxFusedBatches) {   // XOR payloads of versions 1 and 2
     if ((rc = check(launch_compress_fused(c, status_all)))) return rc;
     return check(launch_emit_dense(c, true));
   }

@@ -1098,24 +1098,36 @@ __device__ __forceinline__ uint32_t warp_claim(uint32_t* ctr) {
 }
 
 // Scans the batch totals of tensor j (all of its batches encoded) into exclusive prefixes,
-// finishes the tensor and publishes it.
+// finishes the tensor and publishes it.  Each lane sums a contiguous segment of the batches
+// (independent loads, in flight together), one warp scan places the segments, and each lane
+// writes its segment's prefixes.  The host takes this path only for tensors of at most
+// kMaxFusedBatches batches of at most kMaxBatchChunks chunks, so every sum fits in 32 bits
+// (4096 batches x 32 chunks x 4096 values < 2^32).
 __device__ __noinline__ void fused_finish(const FusedArgs& a, uint32_t j) {
   const int lane = threadIdx.x & 31;
   __threadfence();   // the totals, counts, slots and checksum terms of the other batches
   const uint64_t b0 = a.batch_start[j], nb = a.batch_start[j + 1] - b0;
-  uint64_t rP = 0, rM = 0, rR = 0;
-  for (uint64_t i0 = 0; i0 < nb; i0 += 32) {
-    uint4 t = make_uint4(0, 0, 0, 0);
-    if (i0 + lane < nb) t = __ldcg(&a.batch_tot[b0 + i0 + lane]);
-    // per batch at most 32 chunks (32 KiB of positions, 131072 values): 32 batches fit in
-    // 32 bits
-    const uint32_t iP = warp_incl_scan(t.x), iM = warp_incl_scan(t.y), iR = warp_incl_scan(t.z);
-    if (i0 + lane < nb)
-      a.batch_pre[b0 + i0 + lane] = TileSum{rP + iP - t.x, rM + iM - t.y, rR + iR - t.z, 0};
-    rP += __shfl_sync(0xFFFFFFFFu, iP, 31);
-    rM += __shfl_sync(0xFFFFFFFFu, iM, 31);
-    rR += __shfl_sync(0xFFFFFFFFu, iR, 31);
+  const uint64_t per = (nb + 31) / 32;
+  const uint64_t s0 = min((uint64_t)lane * per, nb), s1 = min(s0 + per, nb);
+  uint32_t sP = 0, sM = 0, sR = 0;
+#pragma unroll 4
+  for (uint64_t i = s0; i < s1; i++) {
+    const uint4 t = __ldcg(&a.batch_tot[b0 + i]);
+    sP += t.x;
+    sM += t.y;
+    sR += t.z;
   }
+  const uint32_t iP = warp_incl_scan(sP), iM = warp_incl_scan(sM), iR = warp_incl_scan(sR);
+  uint64_t p = iP - sP, m = iM - sM, r = iR - sR;
+  for (uint64_t i = s0; i < s1; i++) {
+    const uint4 t = __ldcg(&a.batch_tot[b0 + i]);
+    a.batch_pre[b0 + i] = TileSum{p, m, r, 0};
+    p += t.x;
+    m += t.y;
+    r += t.z;
+  }
+  const uint64_t rP = __shfl_sync(0xFFFFFFFFu, iP, 31), rM = __shfl_sync(0xFFFFFFFFu, iM, 31),
+                 rR = __shfl_sync(0xFFFFFFFFu, iR, 31);
   __threadfence();
   __syncwarp();
   if (lane == 0) {

@@ -383,6 +383,11 @@ constexpr uint32_t kTileChunks = 1024;
 // [kCtlTensors + 2j] its chunks encoded so far and [kCtlTensors + 2j + 1] its flag "scanned,
 // emit may start".
 constexpr uint32_t kMaxBatchChunks = 32;
+// The fused compress serves calls whose tensors have at most this many batches each: the warp
+// finishing a tensor scans its batch totals alone, so a tensor of many small batches (a single
+// large tensor, whose batches are kept small for parallelism) would hold every warp waiting on
+// that one scan; such calls take the separate kernels.
+constexpr uint64_t kMaxFusedBatches = 4096;
 constexpr uint32_t kCtlTensors = 4;
 __host__ __device__ __forceinline__ uint64_t tensor_batches(uint64_t nchunks, uint32_t bchunks) {
   return nchunks ? (nchunks + bchunks - 1) / bchunks : 1;
