@@ -13,10 +13,11 @@ replicas, weak scaling).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload dense7b] [--impl reference]
 
-`--profile-case embed|formats` runs a fixed small program for an ncu capture instead (no timing,
-no JSON line): `embed` compresses the 32000x4096 embedding tensor of dense7b in versions 1, 3
-and 4 and applies each payload, two rounds; `formats` does the same with versions 3 and 4 on the
-whole workload, with the incremental apply too.
+`--profile-case embed|layers|formats` runs a fixed small program for an ncu capture instead (no
+timing, no JSON line): `embed` compresses the 32000x4096 embedding tensor of dense7b in versions
+1, 3 and 4 and applies each payload, two rounds; `layers` does the same in version 1 with the
+18 tensors of dense7b's first two layers (a batch the fused compress takes); `formats` with
+versions 3 and 4 on the whole workload, with the incremental apply too.
 """
 from __future__ import annotations
 
@@ -808,11 +809,18 @@ def run_profile_case(args) -> None:
     import lossless_bf16_weight_old_gb300 as bd
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    if args.profile_case == "embed":
-        spec = [s for s in W.dense7b() if s.name == "embed"][0]
-        a, b = W.make_pair(spec, device=dev)
-        olds, news = [a.reshape(-1)], [b.reshape(-1)]
-        versions = (1, 3, 4)
+    if args.profile_case in ("embed", "layers"):
+        if args.profile_case == "embed":
+            specs = [s for s in W.dense7b() if s.name == "embed"]
+            versions = (1, 3, 4)
+        else:
+            specs = [s for s in W.dense7b() if s.name.startswith(("layers.0.", "layers.1."))]
+            versions = (1,)
+        olds, news = [], []
+        for s in specs:
+            a, b = W.make_pair(s, device=dev)
+            olds.append(a.reshape(-1))
+            news.append(b.reshape(-1))
     else:
         specs = _workload_specs(args.workload)
         olds, news = [], []
@@ -873,7 +881,7 @@ def main(argv=None):
                    help="elements of the workload the CPU oracle baseline encodes+decodes")
     p.add_argument("--ref-sample-elems", type=int, default=400_000_000,
                    help="elements per step of the --impl reference arm")
-    p.add_argument("--profile-case", choices=["embed", "formats"], default=None,
+    p.add_argument("--profile-case", choices=["embed", "layers", "formats"], default=None,
                    help="run a fixed small program for an ncu capture instead of the bench")
     args = p.parse_args(argv)
     if args.profile_case:
