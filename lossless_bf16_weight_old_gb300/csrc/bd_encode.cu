@@ -5,7 +5,10 @@
 // values, keep only the mantissa bits of mantissa-only changes and pack exponent/sign changes
 // separately as one block; the API returns a checksum beside the payload.
 //
-// Two passes around the count scan (bd_scan.cu), neither of which waits on another CTA:
+// XOR payloads of versions 1 and 2 go through one persistent kernel, the fused compress at the
+// end of this file (its parts are the kernels below).  Versions 3 and 4 and overwrite payloads,
+// and calls with a tensor too large for the fused compress, take two passes around the count
+// scan (bd_scan.cu), neither of which waits on another CTA:
 //   encode_slots  the only full-size read of old and new.  One warp per 4096-element chunk
 //                 (each warp a contiguous range of chunks, each chunk prefetched into L2 as
 //                 the warp starts it): branch-free classification, per-chunk class counts,
