@@ -113,7 +113,9 @@ typedef enum bd_status {
   BD_ERR_FORMAT = 3,      /* decompress: not a canonical BF16DLT1 payload for n elements */
   BD_ERR_CHECKSUM = 4,    /* decompress: checksum of the result differs from the expected */
   BD_ERR_CUDA = 5,        /* a CUDA runtime call or kernel launch failed (as a device status:
-                             a wait inside the compress gave up, which its design excludes) */
+                             a wait inside the compress gave up, which its design excludes;
+                             then the call and every tensor of it report this code, see
+                             bf16delta_debug.h) */
   BD_ERR_BASE = 6         /* incremental apply: a payload of version 2 or later whose base checksum
                              is not the checksum of the weights it is applied to */
 } bd_status;

@@ -340,6 +340,19 @@ class CompressBatch:
         _check(rc, "bd_compress_batch")
 
 
+
+def debug_compress_stall(batch: CompressBatch, stall: int, stream=None) -> None:
+    """bd_debug_compress_stall on a CompressBatch of version-1 payloads: tensor `stall` is
+    never published, so the persistent compress's bounded wait runs out; afterwards
+    ``batch.status`` and every entry of ``batch.statuses`` hold ERR_CUDA.  Fault injection
+    for tests of that error path."""
+    if batch.bases is not None:
+        raise ValueError("debug_compress_stall takes a batch of version-1 payloads")
+    rc = _lib.load().bd_debug_compress_stall(batch.items, batch.k, int(stall),
+                                             batch.workspace.data_ptr(), batch.workspace.numel(),
+                                             batch.status.data_ptr(), _stream(stream))
+    _check(rc, "bd_debug_compress_stall")
+
 class DecompressBatch:
     """Device buffers and the C item table of one batched decompress over fixed tensors."""
 

@@ -34,7 +34,7 @@ class PayloadInfo(ctypes.Structure):
                 ("flags", c_u64)]
 
 
-# name -> (restype, argtypes); must match include/bf16delta.h
+# name -> (restype, argtypes); must match include/bf16delta.h and include/bf16delta_debug.h
 SIGNATURES = {
     "bd_compress_bound": (c_u64, [c_u64]),
     "bd_compress_workspace_size": (c_u64, [c_p, c_u32]),
@@ -54,6 +54,7 @@ SIGNATURES = {
     "bd_payload_info": (c_int, [c_p, c_u64, ctypes.POINTER(PayloadInfo)]),
     "bd_status_sync": (c_int, [c_p, c_p]),
     "bd_status_string": (ctypes.c_char_p, [c_int]),
+    "bd_debug_compress_stall": (c_int, [c_p, c_u32, c_u32, c_p, c_u64, c_p, c_p]),
 }
 
 _lib = None

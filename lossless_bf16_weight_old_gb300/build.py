@@ -1,7 +1,7 @@
 """In-tree build of libbf16delta.so for GB300 (sm_103a).
 
 Each CUDA translation unit is compiled in parallel with nvcc, then linked into one shared
-library next to this file.  Only the symbols declared in include/bf16delta.h are exported.
+library next to this file.  Only the symbols declared in include/*.h are exported.
 """
 from __future__ import annotations
 
@@ -33,7 +33,7 @@ def _nvcc() -> str:
 def _inputs() -> list[str]:
     files = [os.path.join(CSRC, s) for s in SOURCES]
     files += [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cuh")]
-    files.append(os.path.join(INCLUDE, "bf16delta.h"))
+    files += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
     return files
 
 

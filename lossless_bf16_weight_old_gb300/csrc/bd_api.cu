@@ -11,6 +11,7 @@
 #include <vector>
 
 #include "bd_internal.cuh"
+#include "bf16delta_debug.h"
 
 namespace bd {
 namespace {
@@ -142,9 +143,12 @@ int check(cudaError_t e) { return e == cudaSuccess ? BD_OK : BD_ERR_CUDA; }
 
 // -------------------------------------------------------------------------------- compress
 // bases == nullptr: version 1; else version `format & 0xFF` (2, or 3 or 4 with compact
-// position blocks), an overwrite payload when format has BD_FORMAT_OVERWRITE.
+// position blocks), an overwrite payload when format has BD_FORMAT_OVERWRITE.  stall < k: the
+// fused compress with tensor `stall` never published (bd_debug_compress_stall).
+constexpr uint32_t kNoStall = 0xFFFFFFFFu;
 int compress_impl(const bd_compress_item* items, const uint64_t* const* bases, uint32_t format,
-                  uint32_t k, void* ws, uint64_t ws_bytes, int32_t* status_all, cudaStream_t s) {
+                  uint32_t k, void* ws, uint64_t ws_bytes, int32_t* status_all, cudaStream_t s,
+                  uint32_t stall = kNoStall) {
   if (k > 0 && items == nullptr) return BD_ERR_INVALID_ARG;
   const uint32_t vfmt = format & 0xFFu;
   const bool overwrite = bases && (format & BD_FORMAT_OVERWRITE) != 0;
@@ -213,6 +217,8 @@ int compress_impl(const bd_compress_item* items, const uint64_t* const* bases, u
   cstart[k] = cb;
   tstart[k] = tb;
   bstart[k] = bb;
+  if (stall != kNoStall && (stall >= k || bases || most_batches > kMaxFusedBatches))
+    return BD_ERR_INVALID_ARG;   // (the hook needs a call that takes the fused compress)
 
   uint8_t* w = static_cast<uint8_t*>(ws);
   LaunchCtx c{s, sms, w, lay, k, sz.chunks, sz.tiles, bb, bchunks};
@@ -225,6 +231,11 @@ int compress_impl(const bd_compress_item* items, const uint64_t* const* bases, u
   // the XOR payloads of versions 1 and 2
   const uint32_t fmt = version == 4 ? 4u : (version == 3 || overwrite) ? 3u : 0u;
   if (fmt == 0 && most_batches <= kMaxFusedBatches) {   // XOR payloads of versions 1 and 2
+    // the hook: tensor `stall` starts with a chunk count that never reaches its chunks
+    if (stall != kNoStall &&
+        (rc = check(cudaMemsetAsync(w + lay.fused_ctl + 4 * (kCtlTensors + 2 * (uint64_t)stall),
+                                    0x80, 4, s))))
+      return rc;
     if ((rc = check(launch_compress_fused(c, status_all)))) return rc;
     return check(launch_emit_dense(c, true));
   }
@@ -377,6 +388,13 @@ int bd_compress_batch(const bd_compress_item* h_items, uint32_t k, void* d_ws,
                       uint64_t ws_bytes, int32_t* d_status, void* stream) {
   return compress_impl(h_items, nullptr, 1, k, d_ws, ws_bytes, d_status,
                        static_cast<cudaStream_t>(stream));
+}
+
+int bd_debug_compress_stall(const bd_compress_item* h_items, uint32_t k, uint32_t stall,
+                            void* d_ws, uint64_t ws_bytes, int32_t* d_status, void* stream) {
+  if (stall >= k) return BD_ERR_INVALID_ARG;
+  return compress_impl(h_items, nullptr, 1, k, d_ws, ws_bytes, d_status,
+                       static_cast<cudaStream_t>(stream), stall);
 }
 
 int bd_compress_versioned(const uint16_t* d_old, const uint16_t* d_new, uint64_t n,

@@ -882,7 +882,8 @@ __device__ __noinline__ void emit_rice_list(const uint32_t* lst, uint32_t cnt, b
 // A compact chunk (at most kCompactMax changes) first gathers its changes in position order
 // into a shared list, then emits them 32 at a time as emit does.
 // FUSED: after the fused compress, which leaves per-batch prefixes (batch_pre, batches of
-// bchunks chunks from batch_start) instead of the count scan's tile and chunk prefixes.
+// bchunks chunks from batch_start) instead of the count scan's tile and chunk prefixes; if a
+// wait of the fused compress gave up (*abort), it emits nothing and fails every tensor.
 template <bool FUSED>
 __global__ void __launch_bounds__(kThreads)
 k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
@@ -891,7 +892,14 @@ k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
              const uint32_t* __restrict__ counts, const uint8_t* __restrict__ slots,
              const uint4* __restrict__ loc, const TileSum* __restrict__ tile_pre,
              const JobInfo* __restrict__ info, const uint64_t* __restrict__ batch_start,
-             const TileSum* __restrict__ batch_pre, uint32_t bchunks) {
+             const TileSum* __restrict__ batch_pre, uint32_t bchunks,
+             const uint32_t* __restrict__ abort) {
+  if (FUSED && *abort) {
+    if (blockIdx.x == 0)
+      for (uint32_t j = threadIdx.x; j < k; j += blockDim.x)
+        if (jobs[j].d_status) *jobs[j].d_status = BD_ERR_CUDA;
+    return;
+  }
   __shared__ EmitSmem s_em[kWarps];
   __shared__ uint32_t s_list[kWarps][kCompactMax];   // compact chunks: pos << 16 | x
   const int lane = threadIdx.x & 31;
@@ -1063,9 +1071,12 @@ k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
 // the separate kernels this saves the count-scan launches and the gaps between kernels (a
 // schedule that emits only after all encoding measured almost the same as this one).  Every claimed encode batch is held by a warp that is
 // running it, and encoding and finishing never wait, so every wait ends, whether or not all
-// blocks are resident; the waits are bounded all the same (kWaitLimit idle polls), after which
-// the warp reports BD_ERR_CUDA for the tensor and the call and stops.
-constexpr uint32_t kWaitLimit = 1u << 24;
+// blocks are resident; the waits are bounded all the same (kWaitLimit idle polls of 256 ns,
+// about a second; the longest wait the schedule allows is one batch being encoded plus one
+// tensor's scan, well under a millisecond), after which the warp reports BD_ERR_CUDA for the
+// tensor and the call, raises the abort word and stops; emit_dense, next on the stream, then
+// reports BD_ERR_CUDA for every tensor of the call, whose payloads may be incomplete.
+constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr uint32_t kEmitterEvery = 6;
 
 struct FusedArgs {
@@ -1233,6 +1244,7 @@ __device__ __noinline__ bool fused_wait(const FusedArgs& a, uint32_t e, uint4* x
       if ((threadIdx.x & 31) == 0) {
         if (a.jobs[j].d_status) *a.jobs[j].d_status = BD_ERR_CUDA;
         if (a.status_all) atomicMax(reinterpret_cast<int*>(a.status_all), (int)BD_ERR_CUDA);
+        atomicExch(&a.ctl[kCtlAbort], 1u);
       }
       return false;
     }
@@ -1337,7 +1349,8 @@ cudaError_t launch_emit_dense(const LaunchCtx& c, bool fused) {
       reinterpret_cast<const TileSum*>(c.ws + c.lay.tile_pre),
       reinterpret_cast<const JobInfo*>(c.ws + c.lay.info),
       reinterpret_cast<const uint64_t*>(c.ws + c.lay.batch_start),
-      reinterpret_cast<const TileSum*>(c.ws + c.lay.batch_pre), c.bchunks);
+      reinterpret_cast<const TileSum*>(c.ws + c.lay.batch_pre), c.bchunks,
+      reinterpret_cast<const uint32_t*>(c.ws + c.lay.fused_ctl) + kCtlAbort);
   return cudaGetLastError();
 }
 

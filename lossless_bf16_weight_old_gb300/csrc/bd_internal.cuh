@@ -379,15 +379,16 @@ constexpr uint32_t kTileChunks = 1024;
 // Fused compress (XOR payloads of versions 1 and 2): batches of up to `bchunks` consecutive
 // chunks of one tensor (chosen per call, at most kMaxBatchChunks; an empty tensor has one
 // empty batch, so that its header is written), and control words in the zeroed state: [0] the
-// next encode batch to hand out, [1] the next emit batch, then per tensor j
-// [kCtlTensors + 2j] its chunks encoded so far and [kCtlTensors + 2j + 1] its flag "scanned,
-// emit may start".
+// next encode batch to hand out, [1] the next emit batch, [kCtlAbort] set when a wait gave up
+// (emit_dense then fails every tensor of the call), then per tensor j [kCtlTensors + 2j] its
+// chunks encoded so far and [kCtlTensors + 2j + 1] its flag "scanned, emit may start".
 constexpr uint32_t kMaxBatchChunks = 32;
 // The fused compress serves calls whose tensors have at most this many batches each: the warp
 // finishing a tensor scans its batch totals alone, so a tensor of many small batches (a single
 // large tensor, whose batches are kept small for parallelism) would hold every warp waiting on
 // that one scan; such calls take the separate kernels.
 constexpr uint64_t kMaxFusedBatches = 4096;
+constexpr uint32_t kCtlAbort = 2;
 constexpr uint32_t kCtlTensors = 4;
 __host__ __device__ __forceinline__ uint64_t tensor_batches(uint64_t nchunks, uint32_t bchunks) {
   return nchunks ? (nchunks + bchunks - 1) / bchunks : 1;

@@ -1,5 +1,5 @@
 """CPU tests of the C-ABI boundary: the library builds for sm_103a, loads without a GPU,
-exports exactly what include/bf16delta.h declares, and its host-only logic (size bounds,
+exports exactly what include/bf16delta.h and include/bf16delta_debug.h declare, and its host-only logic (size bounds,
 workspace sizes, header parsing, argument checks) behaves as documented.  No call here
 launches GPU work."""
 import ctypes
@@ -14,17 +14,23 @@ import oracle
 from lossless_bf16_weight_old_gb300 import _lib, build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "bf16delta.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in ("bf16delta.h", "bf16delta_debug.h")]
 
 
 def _declared() -> set[str]:
-    src = open(HEADER).read()
+    src = "".join(open(h).read() for h in HEADERS)
     return set(re.findall(r"^BD_API\s+[\w\s\*]*?\b(bd_\w+)\s*\(", src, flags=re.M))
+
+
+def test_headers_are_all_listed():
+    inc = os.path.join(ROOT, "include")
+    assert sorted(os.path.join(inc, f) for f in os.listdir(inc) if f.endswith(".h")) == \
+        sorted(HEADERS)
 
 
 def test_library_exports_every_declared_symbol(cuda_lib):
     names = _declared()
-    assert len(names) == 16
+    assert len(names) == 17
     for name in names:
         assert hasattr(cuda_lib, name), name
     out = subprocess.run(["nm", "-D", "--defined-only", _lib.path()], capture_output=True,
@@ -241,6 +247,13 @@ def test_argument_checks_need_no_gpu(cuda_lib):
                                                 1 << 20, None, None) == 1
     assert cuda_lib.bd_checksum(None, 5, dummy, None) == 1
     assert cuda_lib.bd_status_sync(None, None) == 1
+    # the fault-injection hook stalls a tensor of the call, no other
+    items = (_lib.CompressItem * 2)()
+    for stall in (2, 3, 1 << 31):
+        assert cuda_lib.bd_debug_compress_stall(items, 2, stall, ctypes.c_void_p(1 << 24),
+                                                1 << 20, None, None) == 1
+    assert cuda_lib.bd_debug_compress_stall(None, 0, 0, ctypes.c_void_p(1 << 24), 1 << 20,
+                                            None, None) == 1
     del one
 
 
