@@ -2,7 +2,7 @@
 the launch configuration the benchmark times: one batched compress over every tensor of the
 checkpoint (held in one flat buffer per checkpoint, tensors at 256-byte aligned offsets), then
 one batched in-place apply on a copy of old; the dense checkpoint also in version 3 (compact
-position blocks).
+position blocks) and version 4 (Rice-coded compact position blocks).
 
 The oracle checks a sample of tensors one by one (payload bytes, size, checksum; integer work,
 tolerance 0).  Every tensor is checked by properties that hold at any size: each status is OK,
@@ -54,23 +54,25 @@ def _cap_estimate(spec) -> int:
     return min(bd.compress_bound(n), 64 + 4 * C + per_chunk * C + int(3 * spec.rate * n) + 4096)
 
 
-def _check_workload(specs, sample, compact=False):
+def _check_workload(specs, sample, compact=False, rice=False):
     dev = torch.device("cuda")
     O, N, offs, ns = _flat(specs, dev)
     olds = [O[off:off + n] for off, n in zip(offs, ns)]
     news = [N[off:off + n] for off, n in zip(offs, ns)]
     ck_old = torch.cat([bd.checksum(a).reshape(1) for a in olds])
-    bases = ck_old if compact else None   # version 3 payloads are bound to checksum(old)
+    kw = dict(compact=compact, rice=rice)
+    bound = compact or rice
+    bases = ck_old if bound else None   # versions 3 and 4 are bound to checksum(old)
     # payload room from the change rate (the worst-case bound of a 30B checkpoint would not fit
     # beside it); a tensor that needs more reports its size and the batch is run again
     caps = [_cap_estimate(s) for s in specs]
-    comp = bd.CompressBatch(olds, news, caps, base_checksums=bases, compact=compact)
+    comp = bd.CompressBatch(olds, news, caps, base_checksums=bases, **kw)
     comp.run()
     torch.cuda.synchronize()
     if int(comp.status.item()) == bd.ERR_CAPACITY:
         need = [int(v) for v in comp.sizes.tolist()]
         del comp
-        comp = bd.CompressBatch(olds, news, need, base_checksums=bases, compact=compact)
+        comp = bd.CompressBatch(olds, news, need, base_checksums=bases, **kw)
         comp.run()
         torch.cuda.synchronize()
     assert int(comp.status.item()) == bd.OK
@@ -80,9 +82,9 @@ def _check_workload(specs, sample, compact=False):
     # sampled tensors against the oracle, byte for byte
     ck_old_list = bd.u64(ck_old)
     for i in sample:
-        if compact:
+        if bound:
             ref, ref_ck = oracle.encode(to_np_u16(olds[i]), to_np_u16(news[i]),
-                                        base=ck_old_list[i], compact=True)
+                                        base=ck_old_list[i], **kw)
         else:
             ref, ref_ck = oracle_pair(olds[i], news[i])
         assert sizes[i] == ref.size, specs[i].name
@@ -113,7 +115,7 @@ def _check_workload(specs, sample, compact=False):
     assert bd.u64(inc.checksums) == cks
     assert torch.equal(R.view(torch.int16), N.view(torch.int16))
     back_payloads, back_sizes = comp.payloads, sizes
-    if compact:
+    if bound:
         # a payload bound to checksum(old) is refused from new, leaving the weights alone; the
         # way back is the reverse update's payload, bound to checksum(new)
         refused = bd.IncrementalBatch(rolls, comp.payloads, sizes, comp.checksums, ck_old)
@@ -123,7 +125,7 @@ def _check_workload(specs, sample, compact=False):
         assert torch.equal(R.view(torch.int16), N.view(torch.int16))
         comp.workspace = None   # (the forward compress is done: room for the reverse one)
         torch.cuda.empty_cache()
-        rev = bd.CompressBatch(news, olds, sizes, base_checksums=comp.checksums, compact=True)
+        rev = bd.CompressBatch(news, olds, sizes, base_checksums=comp.checksums, **kw)
         rev.run()
         torch.cuda.synchronize()
         assert int(rev.status.item()) == bd.OK
@@ -152,6 +154,15 @@ def test_dense7b_full_size_compact():
     sample = [names[x] for x in ("embed", "layers.0.q", "layers.0.down", "layers.0.norm1",
                                  "norm", "lm_head")]
     _check_workload(specs, sample, compact=True)
+
+
+def test_dense7b_full_size_rice():
+    """The same checkpoint in version 4 (Rice-coded compact position blocks)."""
+    specs = W.dense7b()
+    names = {s.name: i for i, s in enumerate(specs)}
+    sample = [names[x] for x in ("embed", "layers.0.k", "layers.0.up", "layers.0.norm2",
+                                 "layers.31.o", "norm")]
+    _check_workload(specs, sample, rice=True)
 
 
 def test_moe30b_full_size_compact():

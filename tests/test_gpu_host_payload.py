@@ -80,15 +80,17 @@ def test_batched_apply_from_host_payloads():
         assert torch.equal(o.view(torch.int16), nw.view(torch.int16))
 
 
+@pytest.mark.parametrize("version", [3, 4])
 @pytest.mark.parametrize("overwrite", [False, True])
-def test_version_3_payloads_from_host_memory(overwrite):
-    """Version-3 payloads (XOR and overwrite) read from mapped host memory by the full, the
-    incremental and the no-workspace apply: the oracle's result in every case."""
+def test_versioned_payloads_from_host_memory(overwrite, version):
+    """Version-3 and version-4 payloads (XOR and overwrite) read from mapped host memory by the
+    full, the incremental and the no-workspace apply: the oracle's result in every case."""
     old, new = W.make_pair(W.Spec("h3", (4096 * 90 + 321,), rate=0.04, tid=13), device="cuda")
     old, new = old.reshape(-1), new.reshape(-1)
     o, nw = to_np_u16(old), to_np_u16(new)
     base = oracle.checksum(o)
-    ref, ck = oracle.encode(o, nw, base=base, compact=True, overwrite=overwrite)
+    ref, ck = oracle.encode(o, nw, base=base, compact=version == 3, rice=version == 4,
+                            overwrite=overwrite)
     buf = bd.MappedHostBuffer(ref.size)
     buf.numpy()[:] = ref
     out = torch.empty_like(old)
