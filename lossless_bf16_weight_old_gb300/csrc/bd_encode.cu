@@ -1077,7 +1077,7 @@ k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
 // tensor and the call, raises the abort word and stops; emit_dense, next on the stream, then
 // reports BD_ERR_CUDA for every tensor of the call, whose payloads may be incomplete.
 constexpr uint32_t kWaitLimit = 1u << 22;
-constexpr uint32_t kEmitterEvery = 6;
+constexpr uint32_t kEmitterEvery = 4;   // two warps of each block of eight
 
 struct FusedArgs {
   const CJob* jobs;
@@ -1254,7 +1254,9 @@ __device__ __noinline__ bool fused_wait(const FusedArgs& a, uint32_t e, uint4* x
   return true;
 }
 
-__global__ void __launch_bounds__(kThreads, 4) k_compress_fused(const FusedArgs a) {
+// Three blocks per SM (80 registers): at four (64 registers) the inlined encoder and emitter
+// spilled 132 bytes a thread and the kernel was 1.2% slower.
+__global__ void __launch_bounds__(kThreads, 3) k_compress_fused(const FusedArgs a) {
   __shared__ uint4 s_xs[kThreads][2];   // encode: the 16 XOR values of a thread's step
   __shared__ EmitSmem s_em[kWarps];     // emit: per-warp bitmaps and mantissa values
   uint4* xs = s_xs[threadIdx.x];
@@ -1262,7 +1264,9 @@ __global__ void __launch_bounds__(kThreads, 4) k_compress_fused(const FusedArgs 
   const uint32_t nbatches = (uint32_t)a.batches;
   // While batches remain to be encoded, one warp in kEmitterEvery takes emit work: all warps
   // switching to emit as soon as a tensor is published drained the DRAM stream of the encoding
-  // (slower than the separate kernels); a few emitters keep it flowing.
+  // (slower than the separate kernels); a few emitters keep it flowing.  The same number in
+  // every block measured best (one in four: 4.97 ms on dense7b; one in eight 4.99; one in
+  // three, five or six, which give blocks one or two, 5.03-5.10; one in two 5.10).
   const bool emitter = ((((uint64_t)blockIdx.x * kThreads + threadIdx.x) >> 5) % kEmitterEvery) == 0;
   for (;;) {
     // emit work first, when the next emit batch belongs to a published tensor
