@@ -230,13 +230,13 @@ int compress_impl(const bd_compress_item* items, const uint64_t* const* bases, u
   // the kernel builds: version 4, version 3 (also every overwrite payload of version 2), or
   // the XOR payloads of versions 1 and 2
   const uint32_t fmt = version == 4 ? 4u : (version == 3 || overwrite) ? 3u : 0u;
-  if (fmt == 0 && most_batches <= kMaxFusedBatches) {   // XOR payloads of versions 1 and 2
+  if (most_batches <= kMaxFusedBatches) {   // the fused compress, then the dense chunks
     // the hook: tensor `stall` starts with a chunk count that never reaches its chunks
     if (stall != kNoStall &&
         (rc = check(cudaMemsetAsync(w + lay.fused_ctl + 4 * (kCtlTensors + 2 * (uint64_t)stall),
                                     0x80, 4, s))))
       return rc;
-    if ((rc = check(launch_compress_fused(c, status_all)))) return rc;
+    if ((rc = check(launch_compress_fused(c, fmt, overwrite, status_all)))) return rc;
     return check(launch_emit_dense(c, true));
   }
   if ((rc = check(launch_encode_slots(c, fmt, overwrite)))) return rc;

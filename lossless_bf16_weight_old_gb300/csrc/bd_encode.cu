@@ -5,10 +5,10 @@
 // values, keep only the mantissa bits of mantissa-only changes and pack exponent/sign changes
 // separately as one block; the API returns a checksum beside the payload.
 //
-// XOR payloads of versions 1 and 2 go through one persistent kernel, the fused compress at the
-// end of this file (its parts are the kernels below).  Versions 3 and 4 and overwrite payloads,
-// and calls with a tensor too large for the fused compress, take two passes around the count
-// scan (bd_scan.cu), neither of which waits on another CTA:
+// A call goes through one persistent kernel, the fused compress at the end of this file (its
+// parts are the kernels below), in one build per payload kind.  A call with a tensor too large
+// for it takes two passes around the count scan (bd_scan.cu), neither of which waits on
+// another CTA:
 //   encode_slots  the only full-size read of old and new.  One warp per 4096-element chunk
 //                 (each warp a contiguous range of chunks, each chunk prefetched into L2 as
 //                 the warp starts it): branch-free classification, per-chunk class counts,
@@ -930,12 +930,13 @@ k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
       Pex = pre.p;
       Mex = pre.m;
       Rex = pre.r;
-      Xex = 0;
+      Xex = pre.e;
       for (uint64_t c2 = cb; c2 < c; c2++) {
-        const uint32_t w = counts[chunk_start[j] + c2];
-        Pex += block_bytes(wcount_m(w), kChunkBitmap) + block_bytes(wcount_r(w), kChunkBitmap);
-        Mex += wcount_m(w);
-        Rex += wcount_r(w);
+        const ChunkCount cc = chunk_layout(counts[chunk_start[j] + c2], kChunk, I.version);
+        Pex += chunk_pos_bytes(cc, kChunkBitmap);
+        Mex += cc.M;
+        Rex += cc.R;
+        Xex += cc.E;
       }
     } else {
       const TileSum pre = tile_pre[tile_start[j] + c / kTileChunks];
@@ -1059,8 +1060,8 @@ k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
 
 // ------------------------------------------------------------------------ fused compress
 //
-// XOR payloads of versions 1 and 2 in one persistent kernel instead of encode_slots, the count
-// scan and emit.  Warps claim batches of consecutive chunks of one tensor (up to 32, per call) in
+// Every payload kind (one build per kind, as encode_slots and emit have) in one persistent
+// kernel instead of encode_slots, the count scan and emit.  Warps claim batches of consecutive chunks of one tensor (up to 32, per call) in
 // order and encode them (encode_chunk, as encode_slots does); the warp that completes the last
 // batch of a tensor scans the tensor's batch totals, finishes it (offsets, size, checksum,
 // header) and publishes it.  Every batch is claimed a second time, in the same order, as emit
@@ -1069,8 +1070,8 @@ k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
 // the others encode until no encode batch is left, then all emit.  A warp that has claimed an
 // emit batch of a tensor not yet published encodes further batches while it waits.  Against
 // the separate kernels this saves the count-scan launches and the gaps between kernels (a
-// schedule that emits only after all encoding measured almost the same as this one).  Every claimed encode batch is held by a warp that is
-// running it, and encoding and finishing never wait, so every wait ends, whether or not all
+// schedule that emits only after all encoding measured almost the same as this one).  Every
+// claimed encode batch is held by a warp that is running it, and encoding and finishing never wait, so every wait ends, whether or not all
 // blocks are resident; the waits are bounded all the same (kWaitLimit idle polls of 256 ns,
 // about a second; the longest wait the schedule allows is one batch being encoded plus one
 // tensor's scan, well under a millisecond), after which the warp reports BD_ERR_CUDA for the
@@ -1116,32 +1117,38 @@ __device__ __forceinline__ uint32_t warp_claim(uint32_t* ctr) {
 // (independent loads, in flight together), one warp scan places the segments, and each lane
 // writes its segment's prefixes.  The host takes this path only for tensors of at most
 // kMaxFusedBatches batches of at most kMaxBatchChunks chunks, so every sum fits in 32 bits
-// (4096 batches x 32 chunks x 4096 values < 2^32).
+// (4096 batches x 32 chunks x 4096 values < 2^32).  X: the payloads have an X stream
+// (version 3), whose values are scanned too.
+template <bool X>
 __device__ __noinline__ void fused_finish(const FusedArgs& a, uint32_t j) {
   const int lane = threadIdx.x & 31;
   __threadfence();   // the totals, counts, slots and checksum terms of the other batches
   const uint64_t b0 = a.batch_start[j], nb = a.batch_start[j + 1] - b0;
   const uint64_t per = (nb + 31) / 32;
   const uint64_t s0 = min((uint64_t)lane * per, nb), s1 = min(s0 + per, nb);
-  uint32_t sP = 0, sM = 0, sR = 0;
+  uint32_t sP = 0, sM = 0, sR = 0, sE = 0;
 #pragma unroll 4
   for (uint64_t i = s0; i < s1; i++) {
     const uint4 t = __ldcg(&a.batch_tot[b0 + i]);
     sP += t.x;
     sM += t.y;
     sR += t.z;
+    if (X) sE += t.w;
   }
-  const uint32_t iP = warp_incl_scan(sP), iM = warp_incl_scan(sM), iR = warp_incl_scan(sR);
-  uint64_t p = iP - sP, m = iM - sM, r = iR - sR;
+  const uint32_t iP = warp_incl_scan(sP), iM = warp_incl_scan(sM), iR = warp_incl_scan(sR),
+                 iE = X ? warp_incl_scan(sE) : 0u;
+  uint64_t p = iP - sP, m = iM - sM, r = iR - sR, x = iE - sE;
   for (uint64_t i = s0; i < s1; i++) {
     const uint4 t = __ldcg(&a.batch_tot[b0 + i]);
-    a.batch_pre[b0 + i] = TileSum{p, m, r, 0};
+    a.batch_pre[b0 + i] = TileSum{p, m, r, x};
     p += t.x;
     m += t.y;
     r += t.z;
+    if (X) x += t.w;
   }
   const uint64_t rP = __shfl_sync(0xFFFFFFFFu, iP, 31), rM = __shfl_sync(0xFFFFFFFFu, iM, 31),
-                 rR = __shfl_sync(0xFFFFFFFFu, iR, 31);
+                 rR = __shfl_sync(0xFFFFFFFFu, iR, 31),
+                 rE = X ? __shfl_sync(0xFFFFFFFFu, iE, 31) : 0u;
   __threadfence();
   __syncwarp();
   if (lane == 0) {
@@ -1149,7 +1156,7 @@ __device__ __noinline__ void fused_finish(const FusedArgs& a, uint32_t j) {
     I.sum_p = rP;
     I.sum_m = rM;
     I.sum_r = rR;
-    I.sum_e = 0;
+    I.sum_e = rE;
     I.chunk_err = 0;
     finish_compress_job(a.jobs[j], j, I, a.ck_base, a.info, a.status_all);
     __threadfence();   // the prefixes, the tensor's info and header before the flag
@@ -1158,8 +1165,18 @@ __device__ __noinline__ void fused_finish(const FusedArgs& a, uint32_t j) {
   __syncwarp();
 }
 
+// chunk_layout for the build FMT, which fixes the version (FMT 3 also serves the overwrite
+// payloads of version 2, so there the tensor's version decides).  The version-1 build keeps its
+// own plain sums in fused_encode and fused_emit: through this helper it measured 0.6% slower.
+template <int FMT>
+__device__ __forceinline__ ChunkCount layout_of(uint32_t w, uint32_t L, uint32_t version) {
+  return chunk_layout(w, L, FMT == 0 ? 1u : FMT == 4 ? 4u : version);
+}
+
 // Encodes batch b; the warp completing its tensor finishes it.
+template <int FMT, bool OW>
 __device__ __forceinline__ void fused_encode(const FusedArgs& a, uint32_t b, uint4* xs) {
+  uint4* ns = OW ? xs + 2 : xs;   // OW: the step's new values after its XOR values
   const int lane = threadIdx.x & 31;
   const uint32_t j = find_job(a.batch_start, a.k, b);
   const CJob& J = a.jobs[j];
@@ -1167,7 +1184,7 @@ __device__ __forceinline__ void fused_encode(const FusedArgs& a, uint32_t b, uin
   const uint64_t c0 = (b - a.batch_start[j]) * a.bchunks;
   const uint64_t c1 = min(c0 + a.bchunks, J.nchunks);
   uint64_t ck = 0;
-  uint32_t sP = 0, sM = 0, sR = 0;
+  uint32_t sP = 0, sM = 0, sR = 0, sE = 0;
   for (uint64_t c = c0; c < c1; c++) {
     const uint64_t g = J.chunk_base + c, e0 = c * kChunk;
     uint32_t* slot = reinterpret_cast<uint32_t*>(a.slots + g * kSlotBytes);
@@ -1175,22 +1192,30 @@ __device__ __forceinline__ void fused_encode(const FusedArgs& a, uint32_t b, uin
     if (e0 + kChunk <= n) {   // the chunk of old and new into L2 ahead of the step loads
       prefetch_chunk_l2(J.old + e0);
       prefetch_chunk_l2(J.neu + e0);
-      word = encode_chunk<true, 0, false>(J.old, J.neu, n, e0, slot, ck, g, a.counts,
-                                          a.list_count, a.list, xs, xs);
+      word = encode_chunk<true, FMT, OW>(J.old, J.neu, n, e0, slot, ck, g, a.counts,
+                                         a.list_count, a.list, xs, ns);
     } else {
-      word = encode_chunk<false, 0, false>(J.old, J.neu, n, e0, slot, ck, g, a.counts,
-                                           a.list_count, a.list, xs, xs);
+      word = encode_chunk<false, FMT, OW>(J.old, J.neu, n, e0, slot, ck, g, a.counts,
+                                          a.list_count, a.list, xs, ns);
     }
-    const uint32_t M = wcount_m(word), R = wcount_r(word);
-    const uint32_t L = (n - e0) < kChunk ? (uint32_t)(n - e0) : kChunk, B = (L + 7) >> 3;
-    sP += block_bytes(M, B) + block_bytes(R, B);
-    sM += M;
-    sR += R;
+    const uint32_t L = (n - e0) < kChunk ? (uint32_t)(n - e0) : kChunk;
+    if constexpr (FMT == 0) {
+      const uint32_t M = wcount_m(word), R = wcount_r(word), B = (L + 7) >> 3;
+      sP += block_bytes(M, B) + block_bytes(R, B);
+      sM += M;
+      sR += R;
+    } else {
+      const ChunkCount cc = layout_of<FMT>(word, L, J.version);
+      sP += chunk_pos_bytes(cc, (L + 7) >> 3);
+      sM += cc.M;
+      sR += cc.R;
+      sE += cc.E;
+    }
   }
   const uint64_t s = warp_sum64(ck);
   if (lane == 0) {
     if (c1 > c0) atomicAdd(ck_slot(a.ck_base, j, b), (unsigned long long)s);
-    a.batch_tot[b] = make_uint4(sP, sM, sR, 0);
+    a.batch_tot[b] = make_uint4(sP, sM, sR, sE);
   }
   __threadfence();   // this batch's slots, counts, total and checksum terms before its count
   __syncwarp();
@@ -1199,10 +1224,11 @@ __device__ __forceinline__ void fused_encode(const FusedArgs& a, uint32_t b, uin
     const uint32_t cnt = (uint32_t)(c1 - c0);
     fin = atomicAdd(&a.ctl[kCtlTensors + 2 * j], cnt) + cnt == (uint32_t)J.nchunks;
   }
-  if (__shfl_sync(0xFFFFFFFFu, fin, 0)) fused_finish(a, j);
+  if (__shfl_sync(0xFFFFFFFFu, fin, 0)) fused_finish<FMT != 0>(a, j);
 }
 
 // Emits batch e of a published tensor.
+template <int FMT, bool OW>
 __device__ __forceinline__ void fused_emit(const FusedArgs& a, uint32_t e, EmitSmem* sm) {
   const uint32_t j = find_job(a.batch_start, a.k, e);
   const CJob& J = a.jobs[j];
@@ -1211,23 +1237,33 @@ __device__ __forceinline__ void fused_emit(const FusedArgs& a, uint32_t e, EmitS
   const JobInfo I = a.info[j];
   if (c1 <= c0 || I.status != BD_OK) return;
   const TileSum pre = a.batch_pre[e];
-  uint64_t Pex = pre.p, Mex = pre.m, Rex = pre.r;
+  uint64_t Pex = pre.p, Mex = pre.m, Rex = pre.r, Xex = FMT == 0 ? 0 : pre.e;
   const uint64_t g_job_end = J.chunk_base + J.nchunks;
   for (uint64_t c = c0; c < c1; c++) {
     const uint64_t g = J.chunk_base + c;
     const uint32_t w = a.counts[g];
-    emit_chunk<0, false>(a.jobs, g, j, c, g_job_end, c + 1 < c1, I, Pex, Mex, Rex, 0, a.counts,
-                         a.slots, sm);
+    emit_chunk<FMT, OW>(a.jobs, g, j, c, g_job_end, c + 1 < c1, I, Pex, Mex, Rex, Xex, a.counts,
+                        a.slots, sm);
     const uint64_t e0 = c * kChunk;
-    const uint32_t L = (J.n - e0) < kChunk ? (uint32_t)(J.n - e0) : kChunk, B = (L + 7) >> 3;
-    Pex += block_bytes(wcount_m(w), B) + block_bytes(wcount_r(w), B);
-    Mex += wcount_m(w);
-    Rex += wcount_r(w);
+    const uint32_t L = (J.n - e0) < kChunk ? (uint32_t)(J.n - e0) : kChunk;
+    if constexpr (FMT == 0) {
+      const uint32_t B = (L + 7) >> 3;
+      Pex += block_bytes(wcount_m(w), B) + block_bytes(wcount_r(w), B);
+      Mex += wcount_m(w);
+      Rex += wcount_r(w);
+    } else {
+      const ChunkCount cc = layout_of<FMT>(w, L, I.version);
+      Pex += chunk_pos_bytes(cc, (L + 7) >> 3);
+      Mex += cc.M;
+      Rex += cc.R;
+      Xex += cc.E;
+    }
   }
 }
 
 // Waits until the tensor of emit batch e is published, encoding unclaimed batches meanwhile.
 // Returns false when it gave up (reported as BD_ERR_CUDA).
+template <int FMT, bool OW>
 __device__ __noinline__ bool fused_wait(const FusedArgs& a, uint32_t e, uint4* xs) {
   const uint32_t j = find_job(a.batch_start, a.k, e);
   const uint32_t nbatches = (uint32_t)a.batches;
@@ -1236,7 +1272,7 @@ __device__ __noinline__ bool fused_wait(const FusedArgs& a, uint32_t e, uint4* x
     if (warp_read(&a.ctl[0]) < nbatches) {
       const uint32_t b = warp_claim(&a.ctl[0]);
       if (b < nbatches) {
-        fused_encode(a, b, xs);
+        fused_encode<FMT, OW>(a, b, xs);
         continue;
       }
     }
@@ -1254,11 +1290,13 @@ __device__ __noinline__ bool fused_wait(const FusedArgs& a, uint32_t e, uint4* x
   return true;
 }
 
-// Three blocks per SM (80 registers): at four (64 registers) the inlined encoder and emitter
-// spilled 132 bytes a thread and the kernel was 1.2% slower.
+// Three blocks per SM (80 registers, at most 24 bytes of spills in any build): at four (64
+// registers) the inlined encoder and emitter spilled 130-250 bytes a thread; the version-1
+// build was 1.2% slower there, and the other builds slower than the separate kernels.
+template <int FMT, bool OW>
 __global__ void __launch_bounds__(kThreads, 3) k_compress_fused(const FusedArgs a) {
-  __shared__ uint4 s_xs[kThreads][2];   // encode: the 16 XOR values of a thread's step
-  __shared__ EmitSmem s_em[kWarps];     // emit: per-warp bitmaps and mantissa values
+  __shared__ uint4 s_xs[kThreads][OW ? 4 : 2];   // encode: a thread's step (OW: + new values)
+  __shared__ EmitSmem s_em[kWarps];               // emit: per-warp bitmaps and mantissa values
   uint4* xs = s_xs[threadIdx.x];
   EmitSmem* sm = &s_em[threadIdx.x >> 5];
   const uint32_t nbatches = (uint32_t)a.batches;
@@ -1279,14 +1317,14 @@ __global__ void __launch_bounds__(kThreads, 3) k_compress_fused(const FusedArgs 
     if (!emit) {
       const uint32_t b = warp_claim(&a.ctl[0]);
       if (b < nbatches) {
-        fused_encode(a, b, xs);
+        fused_encode<FMT, OW>(a, b, xs);
         continue;
       }
     }
     const uint32_t e = warp_claim(&a.ctl[1]);   // (once encoding is all handed out, only this)
     if (e >= nbatches) break;
-    if (!fused_wait(a, e, xs)) return;
-    fused_emit(a, e, sm);
+    if (!fused_wait<FMT, OW>(a, e, xs)) return;
+    fused_emit<FMT, OW>(a, e, sm);
   }
 }
 
@@ -1358,9 +1396,19 @@ cudaError_t launch_emit_dense(const LaunchCtx& c, bool fused) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_compress_fused(const LaunchCtx& c, int32_t* d_status_all) {
+cudaError_t launch_compress_fused(const LaunchCtx& c, uint32_t fmt, bool overwrite,
+                                  int32_t* d_status_all) {
   if (c.batches == 0) return cudaSuccess;
-  static const int per_sm = blocks_per_sm(k_compress_fused, kThreads);
+  using KT = decltype(&k_compress_fused<0, false>);
+  static const Builds<KT> bl = [] {
+    Builds<KT> r{{k_compress_fused<0, false>, k_compress_fused<3, false>,
+                  k_compress_fused<3, true>, k_compress_fused<4, false>,
+                  k_compress_fused<4, true>}, {}};
+    for (int i = 0; i < 5; i++) r.per_sm[i] = blocks_per_sm(r.k[i], kThreads);
+    return r;
+  }();
+  const int wsel = bl.pick(fmt, overwrite);
+  const int per_sm = bl.per_sm[wsel];
   // persistent: one wave of resident blocks (fewer when there is little work)
   const uint64_t grid = cap_grid((uint64_t)per_sm * c.sms, kWarps, c.batches);
   FusedArgs a;
@@ -1380,7 +1428,8 @@ cudaError_t launch_compress_fused(const LaunchCtx& c, int32_t* d_status_all) {
   a.batches = c.batches;
   a.k = c.k;
   a.bchunks = c.bchunks;
-  k_compress_fused<<<(unsigned)grid, kThreads, 0, c.stream>>>(a);
+  auto kernel = bl.k[wsel];
+  kernel<<<(unsigned)grid, kThreads, 0, c.stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -148,6 +148,28 @@ __host__ __device__ __forceinline__ bool rice_compact(uint32_t v, uint32_t B) {
   return ((v >> 21) & 0x3FFu) < block_bytes(M, B) + block_bytes(R, B);
 }
 
+// How compress lays out a chunk of length L in a payload of `version`, from the chunk's count
+// word w in the compress workspace: its counts, whether its positions take a compact block and
+// the X-stream values E that block needs (version 3); its position bytes are chunk_pos_bytes.
+// The count scan and the fused compress take the same decisions through this.
+__host__ __device__ __forceinline__ ChunkCount chunk_layout(uint32_t w, uint32_t L,
+                                                            uint32_t version) {
+  const uint32_t B = (L + 7) >> 3;
+  ChunkCount cc{};
+  if (version == 4) {
+    cc.M = v4count_m(w);
+    cc.R = v4count_r(w);
+    cc.compact = cc.rice = rice_compact(w, B);
+    cc.nb = (w >> 21) & 0x3FFu;
+  } else {
+    cc.M = wcount_m(w);
+    cc.R = wcount_r(w);
+    cc.compact = version == 3 && choose_compact(cc.M, cc.R, wcount_e(w), B);
+    cc.E = cc.compact ? wcount_e(w) : 0;
+  }
+  return cc;
+}
+
 // Sums over a chunk's gaps of g >> K for K = 1..7, packed in two words: a holds the sums for
 // K = 1, 2 and 4 in fields of 12, 11 and 9 bits at bits 0, 12 and 23; b those for K = 3, 5, 6
 // and 7 in fields of 10, 8, 7 and 6 bits at bits 0, 10, 18 and 25.  The gaps of a chunk add
@@ -376,7 +398,7 @@ __device__ __forceinline__ void finish_compress_job(const CJob& J, uint32_t j, J
 // Scan tiles: chunks per tile of the count scan.
 constexpr uint32_t kTileChunks = 1024;
 
-// Fused compress (XOR payloads of versions 1 and 2): batches of up to `bchunks` consecutive
+// Fused compress (every payload kind): batches of up to `bchunks` consecutive
 // chunks of one tensor (chosen per call, at most kMaxBatchChunks; an empty tensor has one
 // empty batch, so that its header is written), and control words in the zeroed state: [0] the
 // next encode batch to hand out, [1] the next emit batch, [kCtlAbort] set when a wait gave up
@@ -553,9 +575,10 @@ cudaError_t launch_scan_tiles(const LaunchCtx& c, bool decompress);
 cudaError_t launch_scan_jobs(const LaunchCtx& c, bool decompress, int32_t* d_status_all);
 cudaError_t launch_emit(const LaunchCtx& c, uint32_t fmt, bool overwrite);
 cudaError_t launch_emit_dense(const LaunchCtx& c, bool fused = false);
-// The fused compress of XOR payloads of versions 1 and 2 (encode, scan and emit in one
-// persistent kernel; emit_dense follows it).
-cudaError_t launch_compress_fused(const LaunchCtx& c, int32_t* d_status_all);
+// The fused compress (encode, scan and emit in one persistent kernel; emit_dense follows it),
+// in the same builds as encode_slots and emit.
+cudaError_t launch_compress_fused(const LaunchCtx& c, uint32_t fmt, bool overwrite,
+                                  int32_t* d_status_all);
 cudaError_t launch_apply_chunks(const LaunchCtx& c);
 cudaError_t launch_apply_incremental(const LaunchCtx& c);
 cudaError_t launch_copy_jobs(const LaunchCtx& c);
