@@ -892,6 +892,10 @@ k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
     const uint32_t L = (n - e0) < kChunk ? (uint32_t)(n - e0) : kChunk;
     const uint32_t B = (L + 7) >> 3;
     const uint8_t* __restrict__ payload = J.payload;
+    // the chunk's prefix sums are requested with its count word, not after it (one dependent
+    // round trip fewer: 0.5-1% on the dense apply)
+    const TileSum pre = tile_pre[tile_start[j] + c / kTileChunks];
+    const uint4 lc = loc[g];
     const ChunkCount cc = parse_count(reinterpret_cast<const uint32_t*>(
         payload + count_table_offset(info[j].r_start, J.nchunks))[c], V3 ? I.version : 1u);
     const uint32_t M = cc.M, R = cc.R;
@@ -902,8 +906,6 @@ k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
     if (e0 + kChunk <= n) prefetch_chunk_l2(J.out + e0);   // in L2 by the time it is read
 
     if (M + R > 0) {
-      const TileSum pre = tile_pre[tile_start[j] + c / kTileChunks];
-      const uint4 lc = loc[g];
       const uint64_t Pex = pre.p + lc.x, Mex = pre.m + lc.y, Rex = pre.r + lc.z;
       // The rare values are 2-byte aligned (the R stream starts at the even offset
       // header + 4C); the delta lists are too in versions 1 and 2, but may start at an odd
