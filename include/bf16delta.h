@@ -177,12 +177,14 @@ typedef struct bd_payload_info_t {
 #define BD_FLAG_OVERWRITE 1u
 #define BD_FORMAT_OVERWRITE 0x100u
 
-/* Largest payload compress can produce for n elements (every chunk at its worst split, with
- * the version-2 header).  Returns 0 for n > BD_MAX_ELEMS. */
+/* Library utility: no passage on the pages.  Largest payload compress can produce for n
+ * elements (every chunk at its worst split, with the version-2 header), so a caller can size
+ * a payload buffer before the first call.  Returns 0 for n > BD_MAX_ELEMS. */
 BD_API uint64_t bd_compress_bound(uint64_t n);
 
-/* Workspace bytes needed by bd_compress_batch / bd_decompress_batch for k tensors of
- * h_n[0..k) elements (k = 1 for the single-tensor calls).  Returns 0 on bad arguments. */
+/* Library utility: no passage on the pages.  Workspace bytes needed by bd_compress_batch /
+ * bd_decompress_batch for k tensors of h_n[0..k) elements (k = 1 for the single-tensor
+ * calls); h_n is a host array read during the call.  Returns 0 on bad arguments. */
 BD_API uint64_t bd_compress_workspace_size(const uint64_t* h_n, uint32_t k);
 BD_API uint64_t bd_decompress_workspace_size(const uint64_t* h_n, uint32_t k);
 
@@ -291,27 +293,38 @@ BD_API int bd_decompress_incremental_batch(const bd_incremental_item* h_items, u
  *   - all calls share the one scratch array (it keeps the last call's contents; each call
  *     clears what must start at zero), so two calls that may overlap on the GPU race:
  *     issue them on one stream, or order them with events;
- *   - the first call on a device looks up the array's device address (once per device, with
- *     that device current); make that first call before any stream capture begins.
+ *   - every call looks up the array's device address on the current device (a host call,
+ *     no allocation; so a device reset leaves no stale address behind); the first call on a
+ *     device also loads the library's module there, so make that first call before any
+ *     stream capture begins;
+ *   - d_expected must be 8-byte and d_status 4-byte aligned, as for bd_decompress.
  * It allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine. */
 BD_API int bd_decompress_noalloc(const uint16_t* d_old, uint64_t n, const void* d_payload,
                                  uint64_t size, const uint64_t* d_expected, uint16_t* d_out,
                                  int32_t* d_status, void* stream);
 
-/* The checksum above of n BF16 values, written to *d_out.  Needs no workspace. */
+/* [ARCv3], the paragraph on encoding the mantissa/exponent asymmetry: the rollout side
+ * checksums the restored weights against the trainer's original.  The page names no formula;
+ * this computes the one given at the top of this header (sum of position-keyed SplitMix64
+ * word terms) over the n BF16 values at d_w and writes it to *d_out, asynchronously on
+ * stream.  n = 0 gives 0.  Needs no workspace; d_w 16-byte aligned, d_out 8-byte aligned. */
 BD_API int bd_checksum(const uint16_t* d_w, uint64_t n, uint64_t* d_out, void* stream);
 
-/* Parses and checks a payload header held in host memory (bytes >= 64; >= 80 for versions 2
+/* Library utility: no passage on the pages (the header layout is this library's format).
+ * Parses and checks a payload header held in host memory (bytes >= 64; >= 80 for versions 2
  * to 4).  Checks magic, version, chunk size and the internal consistency of the header
  * fields (for version 3 the total leaves an even number of bytes, at most 2 * 508 per chunk,
  * for the X stream); returns BD_OK, BD_ERR_FORMAT or BD_ERR_INVALID_ARG.  Does not touch the
  * GPU. */
 BD_API int bd_payload_info(const void* h_header, uint64_t bytes, bd_payload_info_t* out);
 
-/* Waits for `stream` and returns the int32 status word at d_status (or BD_ERR_CUDA). */
+/* Library utility: no passage on the pages.  Waits for `stream` (the host blocks) and
+ * returns the int32 status word at d_status, which must be device-readable and 4-byte
+ * aligned (or BD_ERR_CUDA when the wait or the read fails). */
 BD_API int bd_status_sync(const int32_t* d_status, void* stream);
 
-/* Static description of a status code. */
+/* Library utility: no passage on the pages.  Static description of a status code (never
+ * NULL; unknown codes give a generic string). */
 BD_API const char* bd_status_string(int code);
 
 #ifdef __cplusplus

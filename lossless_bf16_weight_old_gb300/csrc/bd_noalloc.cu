@@ -7,7 +7,6 @@
 // workspace argument.  It runs the same scan kernels as bd_decompress and applies every
 // chunk with the block-level decoder, which needs only a few bytes of scratch per chunk.
 #include <algorithm>
-#include <mutex>
 
 #include "bd_internal.cuh"
 
@@ -18,23 +17,15 @@ namespace {
 // address: the device address is looked up with cudaGetSymbolAddress below.
 static __device__ __align__(256) uint8_t g_scratch[BD_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 128;
-std::mutex g_mutex;
-uint8_t* g_scratch_addr[kMaxDevices];  // device address per device, set on first use
-
-// Device address of the scratch array on the current device (looked up once per device,
-// with that device current).
+// Device address of the scratch array on the current device.  It is looked up on every call
+// (a cheap host call) rather than cached, so that a device reset or a re-created primary
+// context never leaves a stale address behind; the first lookup on a device also loads the
+// library's module there.
 int scratch_address(uint8_t** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return BD_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_mutex);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
-    if (e != cudaSuccess || p == nullptr) return BD_ERR_CUDA;
-    g_scratch_addr[dev] = static_cast<uint8_t*>(p);
-  }
-  *out = g_scratch_addr[dev];
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
+  if (e != cudaSuccess || p == nullptr) return BD_ERR_CUDA;
+  *out = static_cast<uint8_t*>(p);
   return BD_OK;
 }
 
@@ -112,7 +103,8 @@ extern "C" int bd_decompress_noalloc(const uint16_t* d_old, uint64_t n, const vo
                                      uint64_t size, const uint64_t* d_expected, uint16_t* d_out,
                                      int32_t* d_status, void* stream) {
   if (n > BD_NOALLOC_MAX_ELEMS) return BD_ERR_INVALID_ARG;  // larger than the scratch covers
-  if (!d_status || !aligned(d_status, 4) || !d_expected) return BD_ERR_INVALID_ARG;
+  if (!d_status || !aligned(d_status, 4) || !d_expected || !aligned(d_expected, 8))
+    return BD_ERR_INVALID_ARG;
   if (n > 0 && (!d_old || !d_out || !aligned(d_old, 16) || !aligned(d_out, 16)))
     return BD_ERR_INVALID_ARG;
   if (d_out != d_old && overlaps(d_out, 2 * n, d_old, 2 * n)) return BD_ERR_INVALID_ARG;

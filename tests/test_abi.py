@@ -246,6 +246,16 @@ def test_argument_checks_need_no_gpu(cuda_lib):
     assert cuda_lib.bd_compress_versioned_batch(None, base_ptrs, 0, 7, ctypes.c_void_p(1 << 24),
                                                 1 << 20, None, None) == 1
     assert cuda_lib.bd_checksum(None, 5, dummy, None) == 1
+    # the no-workspace apply: an expected checksum or status word off its alignment, a missing
+    # status word and a tensor beyond its scratch are rejected before anything is enqueued
+    base = 1 << 20
+    for exp, st in ((ctypes.c_void_p(base + 4), dummy), (dummy, ctypes.c_void_p(base + 2)),
+                    (dummy, None), (None, dummy)):
+        assert cuda_lib.bd_decompress_noalloc(ctypes.c_void_p(1 << 24), 4096,
+                                              ctypes.c_void_p(1 << 26), 64, exp,
+                                              ctypes.c_void_p(1 << 24), st, None) == 1
+    assert cuda_lib.bd_decompress_noalloc(dummy, (1 << 27) + 1, dummy, 64, dummy, dummy, dummy,
+                                          None) == 1
     assert cuda_lib.bd_status_sync(None, None) == 1
     # the fault-injection hook stalls a tensor of the call, no other
     items = (_lib.CompressItem * 2)()

@@ -70,6 +70,23 @@ def test_noalloc_matches_workspace_entry_point(lib, call):
     assert int(st_bad.item()) == int(st_bad_ref.item()) == bd.ERR_CHECKSUM
 
 
+def test_noalloc_empty_tensor(lib):
+    # n = 0: the 64-byte header alone, checksum 0; twice in a row, as above
+    old = torch.empty(0, dtype=torch.bfloat16, device="cuda")
+    payload, size_t, ck, st = bd.compress(old, old)
+    torch.cuda.synchronize()
+    assert int(st.item()) == bd.OK
+    size = int(size_t.item())
+    for _ in range(2):
+        out = torch.empty_like(old)
+        st_ref = bd.decompress(old, payload, size, ck, out=out)
+        st_got = _noalloc(lib, old, payload, size, ck, out)
+        st_bad = _noalloc(lib, old, payload, size, ck ^ 1, out)
+        torch.cuda.synchronize()
+        assert int(st_ref.item()) == int(st_got.item()) == bd.OK
+        assert int(st_bad.item()) == bd.ERR_CHECKSUM
+
+
 def test_noalloc_rejects_tensors_beyond_its_scratch(lib):
     limit = 1 << 27
     dummy = ctypes.c_void_p(1 << 20)
