@@ -379,6 +379,29 @@ def run_reference(args) -> None:
 
 # ------------------------------------------------------------------------ GPU arm
 
+def _host_mem_available() -> int:
+    """Bytes of host memory this process may still use (the smaller of the free physical
+    memory and the room left under a cgroup limit)."""
+    try:
+        avail = os.sysconf("SC_AVPHYS_PAGES") * os.sysconf("SC_PAGE_SIZE")
+    except (ValueError, OSError, AttributeError):
+        avail = 1 << 62
+    try:
+        with open("/sys/fs/cgroup/memory.max") as f:
+            lim = f.read().strip()
+        with open("/sys/fs/cgroup/memory.current") as f:
+            cur = int(f.read().strip())
+        if lim != "max":
+            avail = min(avail, int(lim) - cur)
+    except (OSError, ValueError):
+        pass
+    return avail
+
+
+L2_FLUSH_BYTES = 256 << 20     # twice the GB300's L2
+FLUSH_BELOW = 1 << 30          # flush L2 between timed runs when old + new are under 1 GiB
+
+
 def run_ours(args) -> None:
     import lossless_bf16_weight_old_gb300 as bd
 
@@ -395,6 +418,7 @@ def run_ours(args) -> None:
     specs = _workload_specs(args.workload)
     ns = [s.numel for s in specs]
     n_total = sum(ns)
+    k = len(specs)
     # flat buffers: old (trainer before), new (trainer after), rollout copy
     offs, o = [], 0
     for n in ns:
@@ -413,42 +437,69 @@ def run_ours(args) -> None:
     rolls = [Rb[off:off + n] for off, n in zip(offs, ns)]
     torch.cuda.synchronize()
 
+    # small workloads: flush L2 (write twice its size) before every timed phase, outside the
+    # phase's events; larger ones stream more than L2 by themselves
+    flush = 4 * n_total < FLUSH_BELOW
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev) if flush else None
+
     # touched 32-byte sectors (16 elements) -- algorithmic write bytes of the in-place apply
     touched = 0
     for a, b in zip(olds, news):
         m = len(a) // 16 * 16
         diff = a.view(torch.int16) != b.view(torch.int16)
         touched += int(diff[:m].view(-1, 16).any(1).sum().item()) + int(diff[m:].any().item())
+        del diff
 
     stream = torch.cuda.current_stream()
-    comp = bd.CompressBatch(olds, news)
-    comp.run(stream)
-    torch.cuda.synchronize()
-    if int(comp.status.item()) != bd.OK:
-        raise RuntimeError(f"compress status {int(comp.status.item())}")
-    sizes = [int(v) for v in comp.sizes.tolist()]
+    # one workspace per direction, shared by every batch below (they run one after another)
+    ws_c = torch.empty(max(bd.compress_workspace_size(ns), 256), dtype=torch.uint8, device=dev)
+    ws_d = torch.empty(max(bd.decompress_workspace_size(ns), 256), dtype=torch.uint8,
+                       device=dev)
+
+    def sized_batch(src, dst, **kw):
+        """A compress batch whose payload buffers have exactly the sizes the update needs
+        (a first run with no room reports them)."""
+        probe = bd.CompressBatch(src, dst, caps=[0] * k, workspace=ws_c, **kw)
+        probe.run(stream)
+        torch.cuda.synchronize()
+        need = [int(v) for v in probe.sizes.tolist()]
+        del probe
+        b = bd.CompressBatch(src, dst, caps=need, workspace=ws_c, **kw)
+        b.run(stream)
+        torch.cuda.synchronize()
+        if int(b.status.item()) != bd.OK:
+            raise RuntimeError(f"compress status {int(b.status.item())}")
+        return b, need
+
+    comp, sizes = sized_batch(olds, news)
     payload_bytes = sum(sizes)
     ck_new = comp.checksums.clone()
     ck_old = torch.empty_like(ck_new)
     for i, a in enumerate(olds):
         ck_old[i:i + 1].copy_(bd.checksum(a))
-    dec_to_new = bd.DecompressBatch(rolls, comp.payloads, sizes, ck_new)
-    dec_to_old = bd.DecompressBatch(rolls, comp.payloads, sizes, ck_old)
+    dec_to_new = bd.DecompressBatch(rolls, comp.payloads, sizes, ck_new, workspace=ws_d)
+    dec_to_old = bd.DecompressBatch(rolls, comp.payloads, sizes, ck_old, workspace=ws_d)
     torch.cuda.synchronize()
 
     state = {"new": False}
 
-    def step(evs=None):
+    def step(evs=None, flush_l2=flush):
+        if flush_l2:
+            flush_buf.zero_()
         if evs is not None:
             evs[0].record(stream)
         comp.run(stream)
         if evs is not None:
             evs[1].record(stream)
+        if flush_l2:
+            flush_buf.zero_()
+        if evs is not None:
+            evs[2].record(stream)
         d = dec_to_old if state["new"] else dec_to_new
         d.run(stream)
         state["new"] = not state["new"]
         if evs is not None:
-            evs[2].record(stream)
+            evs[3].record(stream)
         return d
 
     clocks = ClockSampler(_smi_id(dev, local))
@@ -458,7 +509,7 @@ def run_ours(args) -> None:
     torch.cuda.synchronize()
     barrier(world, dev)
     torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
     last = None
@@ -471,7 +522,7 @@ def run_ours(args) -> None:
     clk = clocks.stop()
     total_ms = start.elapsed_time(end)
     t_comp = [e[0].elapsed_time(e[1]) for e in evs]
-    t_app = [e[1].elapsed_time(e[2]) for e in evs]
+    t_app = [e[2].elapsed_time(e[3]) for e in evs]
 
     # correctness of the timed work (outside the timed region)
     st_c, st_d = int(comp.status.item()), int(last.status.item())
@@ -479,34 +530,55 @@ def run_ours(args) -> None:
     if st_c != bd.OK or st_d != bd.OK or not torch.equal(Rb.view(torch.int16), want.view(torch.int16)):
         raise RuntimeError(f"timed steps did not verify: compress {st_c}, apply {st_d}")
 
+    def timed(fn, steps):
+        """Mean device time of fn over `steps` runs after the warm-up; with the L2 flushed
+        before each run (outside its events) for small workloads."""
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        if flush:
+            spans, out = [], None
+            for _ in range(steps):
+                flush_buf.zero_()
+                t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                t0.record(stream)
+                out = fn()
+                t1.record(stream)
+                spans.append((t0, t1))
+            torch.cuda.synchronize()
+            ms = sum(a.elapsed_time(b) for a, b in spans)
+        else:
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+            for _ in range(steps):
+                out = fn()
+            t1.record(stream)
+            torch.cuda.synchronize()
+            ms = t0.elapsed_time(t1)
+        return reduce_max(ms, world, dev) / steps, out
+
+    def alternate(table):
+        def run():
+            b = table[state["new"]]
+            b.run(stream)
+            state["new"] = not state["new"]
+            return b
+        return run
+
+    def verified(name, last_batch):
+        want = N if state["new"] else O
+        if int(last_batch.status.item()) != bd.OK or not torch.equal(Rb.view(torch.int16),
+                                                                     want.view(torch.int16)):
+            raise RuntimeError(f"{name} did not verify")
+
     # the incremental apply (verified from the checksum of the resident weights; reads and
     # writes only the touched sectors), timed on its own after the step, alternating
     # directions like the step's apply
-    inc_fwd = bd.IncrementalBatch(rolls, comp.payloads, sizes, ck_old, ck_new)
-    inc_bwd = bd.IncrementalBatch(rolls, comp.payloads, sizes, ck_new, ck_old)
-    inc_state = {"new": state["new"]}
-
-    def inc_step():
-        b = inc_bwd if inc_state["new"] else inc_fwd
-        b.run(stream)
-        inc_state["new"] = not inc_state["new"]
-        return b
-
-    for _ in range(args.warmup):
-        inc_step()
-    torch.cuda.synchronize()
-    i0, i1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    i0.record(stream)
-    for _ in range(args.steps):
-        last_inc = inc_step()
-    i1.record(stream)
-    torch.cuda.synchronize()
-    inc_ms = reduce_max(i0.elapsed_time(i1), world, dev) / args.steps
-    want = N if inc_state["new"] else O
-    if int(last_inc.status.item()) != bd.OK or not torch.equal(Rb.view(torch.int16),
-                                                                want.view(torch.int16)):
-        raise RuntimeError("incremental apply did not verify")
-    state["new"] = inc_state["new"]   # the rollout copy now holds this side
+    inc = {True: bd.IncrementalBatch(rolls, comp.payloads, sizes, ck_new, ck_old, workspace=ws_d),
+           False: bd.IncrementalBatch(rolls, comp.payloads, sizes, ck_old, ck_new, workspace=ws_d)}
+    inc_ms, last_inc = timed(alternate(inc), args.steps)
+    verified("incremental apply", last_inc)
+    del inc
 
     # the full verified apply reading its payloads straight from mapped pinned host memory
     # (over the CPU-GPU link, no host-to-device copy), timed on its own
@@ -519,138 +591,44 @@ def run_ours(args) -> None:
     for p, o, sz in zip(comp.payloads, h_offs, sizes):
         hview[o:o + sz] = p[:sz].cpu().numpy()
     h_addrs = [hbuf.device_ptr + o for o in h_offs]
-    hd_new = bd.DecompressBatch(rolls, h_addrs, sizes, ck_new)
-    hd_old = bd.DecompressBatch(rolls, h_addrs, sizes, ck_old)
-    h_state = {"new": state["new"]}
-
-    def host_step():
-        d = hd_old if h_state["new"] else hd_new
-        d.run(stream)
-        h_state["new"] = not h_state["new"]
-        return d
-
-    for _ in range(args.warmup):
-        host_step()
-    torch.cuda.synchronize()
-    h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    h0.record(stream)
-    for _ in range(args.steps):
-        last_h = host_step()
-    h1.record(stream)
-    torch.cuda.synchronize()
-    host_ms = reduce_max(h0.elapsed_time(h1), world, dev) / args.steps
-    want = N if h_state["new"] else O
-    if int(last_h.status.item()) != bd.OK or not torch.equal(Rb.view(torch.int16),
-                                                              want.view(torch.int16)):
-        raise RuntimeError("apply from host payloads did not verify")
-    state["new"] = h_state["new"]
-    del hd_new, hd_old, hbuf
+    hd = {True: bd.DecompressBatch(rolls, h_addrs, sizes, ck_old, workspace=ws_d),
+          False: bd.DecompressBatch(rolls, h_addrs, sizes, ck_new, workspace=ws_d)}
+    host_ms, last_h = timed(alternate(hd), args.steps)
+    verified("apply from host payloads", last_h)
+    del hd, hbuf
 
     # version 3 (compact position blocks) of the same update: compress bound to checksum(old),
     # the full verified apply, and the incremental apply -- backwards from a second payload of
     # the reverse update bound to checksum(new), so that both directions pass the base check
-    c3 = bd.CompressBatch(olds, news, base_checksums=ck_old, compact=True)
-    c3.run(stream)
-    torch.cuda.synchronize()
-    s3 = [int(v) for v in c3.sizes.tolist()]
-    c3b = bd.CompressBatch(news, olds, caps=s3, base_checksums=ck_new, compact=True)
-    c3b.run(stream)
-    torch.cuda.synchronize()
-    if int(c3.status.item()) != bd.OK or int(c3b.status.item()) != bd.OK:
-        raise RuntimeError("version-3 compress failed")
-    p3_bytes = sum(s3)
+    def bound_format(**kw):
+        fwd, s_f = sized_batch(olds, news, base_checksums=ck_old, **kw)
+        bwd, s_b = sized_batch(news, olds, base_checksums=ck_new, **kw)
+        c_ms, _ = timed(lambda: fwd.run(stream), args.steps)
+        res = {"compress_ms": c_ms, "bytes": sum(s_f)}
+        dec = {True: bd.DecompressBatch(rolls, bwd.payloads, s_b, ck_old, workspace=ws_d),
+               False: bd.DecompressBatch(rolls, fwd.payloads, s_f, ck_new, workspace=ws_d)}
+        incb = {True: bd.IncrementalBatch(rolls, bwd.payloads, s_b, ck_new, ck_old,
+                                          workspace=ws_d),
+                False: bd.IncrementalBatch(rolls, fwd.payloads, s_f, ck_old, ck_new,
+                                           workspace=ws_d)}
+        for name, table in (("apply", dec), ("incremental", incb)):
+            ms, lastb = timed(alternate(table), args.steps)
+            verified(f"{kw} {name}", lastb)
+            res[name + "_ms"] = ms
+        del fwd, bwd, dec, incb
+        return res
 
-    def timed(fn, steps):
-        for _ in range(args.warmup):
-            fn()
-        torch.cuda.synchronize()
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        for _ in range(steps):
-            out = fn()
-        t1.record(stream)
-        torch.cuda.synchronize()
-        return reduce_max(t0.elapsed_time(t1), world, dev) / steps, out
+    v3 = bound_format(compact=True)
+    v4 = bound_format(rice=True)
+    ow = bound_format(compact=True, overwrite=True)
+    p3_bytes, p4_bytes = v3["bytes"], v4["bytes"]
 
-    c3_ms, _ = timed(lambda: c3.run(stream), args.steps)
-    d3 = {True: bd.DecompressBatch(rolls, c3.payloads, s3, ck_old),
-          False: bd.DecompressBatch(rolls, c3.payloads, s3, ck_new)}
-    i3 = {True: bd.IncrementalBatch(rolls, c3b.payloads, s3, ck_new, ck_old),
-          False: bd.IncrementalBatch(rolls, c3.payloads, s3, ck_old, ck_new)}
-
-    def alternate(table):
-        def run():
-            b = table[state["new"]]
-            b.run(stream)
-            state["new"] = not state["new"]
-            return b
-        return run
-
-    for name, table in (("apply", d3), ("incremental", i3)):
-        ms, last3 = timed(alternate(table), args.steps)
-        want = N if state["new"] else O
-        if int(last3.status.item()) != bd.OK or not torch.equal(Rb.view(torch.int16),
-                                                                 want.view(torch.int16)):
-            raise RuntimeError(f"version-3 {name} did not verify")
-        if name == "apply":
-            a3_ms = ms
-        else:
-            i3_ms = ms
-    del c3b, d3, i3
-
-    # version 4 (Rice-coded compact position blocks) of the same update, timed as version 3
-    c4 = bd.CompressBatch(olds, news, base_checksums=ck_old, rice=True)
-    c4.run(stream)
-    torch.cuda.synchronize()
-    s4 = [int(v) for v in c4.sizes.tolist()]
-    c4b = bd.CompressBatch(news, olds, caps=s4, base_checksums=ck_new, rice=True)
-    c4b.run(stream)
-    torch.cuda.synchronize()
-    if int(c4.status.item()) != bd.OK or int(c4b.status.item()) != bd.OK:
-        raise RuntimeError("version-4 compress failed")
-    p4_bytes = sum(s4)
-    c4_ms, _ = timed(lambda: c4.run(stream), args.steps)
-    d4 = {True: bd.DecompressBatch(rolls, c4.payloads, s4, ck_old),
-          False: bd.DecompressBatch(rolls, c4.payloads, s4, ck_new)}
-    i4 = {True: bd.IncrementalBatch(rolls, c4b.payloads, s4, ck_new, ck_old),
-          False: bd.IncrementalBatch(rolls, c4.payloads, s4, ck_old, ck_new)}
-    rice_res = {}
-    for name, table in (("apply", d4), ("incremental", i4)):
-        ms, last4 = timed(alternate(table), args.steps)
-        want = N if state["new"] else O
-        if int(last4.status.item()) != bd.OK or not torch.equal(Rb.view(torch.int16),
-                                                                 want.view(torch.int16)):
-            raise RuntimeError(f"version-4 {name} did not verify")
-        rice_res[name] = ms
-    del c4, c4b, d4, i4
-
-    # overwrite payloads (version 3, header flag bit 0) of the same update, both directions
-    cof = bd.CompressBatch(olds, news, caps=s3, base_checksums=ck_old, compact=True,
-                           overwrite=True)
-    cob = bd.CompressBatch(news, olds, caps=s3, base_checksums=ck_new, compact=True,
-                           overwrite=True)
-    cof.run(stream)
-    cob.run(stream)
-    torch.cuda.synchronize()
-    if int(cof.status.item()) != bd.OK or int(cob.status.item()) != bd.OK:
-        raise RuntimeError("overwrite compress failed")
-    ow_ms, _ = timed(lambda: cof.run(stream), args.steps)
-    dow = {True: bd.DecompressBatch(rolls, cob.payloads, s3, ck_old),
-           False: bd.DecompressBatch(rolls, cof.payloads, s3, ck_new)}
-    iow = {True: bd.IncrementalBatch(rolls, cob.payloads, s3, ck_new, ck_old),
-           False: bd.IncrementalBatch(rolls, cof.payloads, s3, ck_old, ck_new)}
-    ow_res = {}
-    for name, table in (("apply", dow), ("incremental", iow)):
-        ms, lastw = timed(alternate(table), args.steps)
-        want = N if state["new"] else O
-        if int(lastw.status.item()) != bd.OK or not torch.equal(Rb.view(torch.int16),
-                                                                 want.view(torch.int16)):
-            raise RuntimeError(f"overwrite {name} did not verify")
-        ow_res[name] = ms
-    del cof, cob, dow, iow
-
-    total_ms = reduce_max(total_ms, world, dev)
-    ms_step = total_ms / args.steps
+    if flush:
+        ms_step = statistics.mean(t_comp) + statistics.mean(t_app)
+        ms_step = reduce_max(ms_step, world, dev)
+    else:
+        total_ms = reduce_max(total_ms, world, dev)
+        ms_step = total_ms / args.steps
     raw = 2 * n_total
     value = world * raw / (ms_step * 1e-3) / 1e9
     peak, peak_kind = _peak_hbm()
@@ -675,7 +653,12 @@ def run_ours(args) -> None:
     # e2e through the public API with host buffers: H2D old+new from pinned memory, compress,
     # verified apply, D2H of payloads + checksums + statuses
     e2e = None
-    if True:
+    host_need = 4 * n_total + payload_bytes
+    if host_need > _host_mem_available() // 2:
+        e2e = {"value": None, "unit": "GB/s",
+               "unavailable": f"pinned host copies of old and new ({host_need / 1e9:.0f} GB) "
+                              f"exceed half of the host memory free to this process"}
+    else:
         hO = torch.empty(O.shape, dtype=O.dtype, pin_memory=True)
         hN = torch.empty(N.shape, dtype=N.dtype, pin_memory=True)
         hO.copy_(O)
@@ -692,7 +675,7 @@ def run_ours(args) -> None:
         def e2e_step():
             O.copy_(hO, non_blocking=True)
             N.copy_(hN, non_blocking=True)
-            d = step()
+            d = step(flush_l2=False)
             for p, hoff, sz in regions:
                 hP[hoff:hoff + sz].copy_(p[:sz], non_blocking=True)
             hS[:len(specs)].copy_(comp.sizes, non_blocking=True)
@@ -726,21 +709,44 @@ def run_ours(args) -> None:
 
     # tensor-table uploads (30 KiB each): the tensor table and the chunk, tile and (compress)
     # batch start arrays, each section 256-byte aligned
-    k = len(specs)
     blobs_c = -(-(128 * k + 3 * 8 * (k + 1) + 3 * 256) // 30720)
     blobs_d = -(-(128 * k + 2 * 8 * (k + 1) + 2 * 256) // 30720)
     # compress: uploads + the fused compress + emit_dense; decompress: uploads + scan x2, both
     # builds of apply_chunks (one returns at once), apply_dense, apply_finish
     launches_per_step = (blobs_c + 2) + (blobs_d + 6)
 
+    def frac(nbytes, ms):
+        return round(nbytes / (ms * 1e-3) / 1e9 / peak, 4)
+
+    def fmt_block(res, what, nbytes_payload=None):
+        out = {"compress_ms": round(res["compress_ms"], 4), "apply_ms": round(res["apply_ms"], 4),
+               "incremental_ms": round(res["incremental_ms"], 4), "what": what}
+        if nbytes_payload is not None:
+            out.update({
+                "payload_pct": round(100 * nbytes_payload / raw, 4),
+                "payload_vs_v1": round(nbytes_payload / payload_bytes, 4),
+                "compress_roofline_frac": frac(4 * n_total + nbytes_payload, res["compress_ms"]),
+                "apply_roofline_frac": frac(2 * n_total + nbytes_payload + 32 * touched,
+                                            res["apply_ms"]),
+                "incremental_roofline_frac": frac(nbytes_payload + 2 * 32 * touched,
+                                                  res["incremental_ms"])})
+        return out
+
     if rank == 0:
+        rice = fmt_block(v4, "version-4 payloads (Rice-coded compact position blocks) of the "
+                             "same update: bd_compress_versioned_batch format 4, "
+                             "bd_decompress_batch in place, bd_decompress_incremental_batch in "
+                             "place", p4_bytes)
+        rice["payload_vs_v3"] = round(p4_bytes / p3_bytes, 4)
         line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "u16", "data": "synthetic",
                 "config": {"workload": _describe(args.workload, specs),
-                           "l2": "inputs larger than L2 (no flush needed)"
-                           if 4 * n_total > 129e6 else "inputs fit in L2",
+                           "l2": (f"flushed before every timed phase ({L2_FLUSH_BYTES >> 20} MiB "
+                                  "write outside the phase events); ms_per_step = compress + "
+                                  "apply phase times") if flush else
+                                 "inputs larger than L2 (no flush needed)",
                            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
                 "compress_gbs": round(raw / (mc * 1e-3) / 1e9, 2),
                 "apply_gbs": round(raw / (ma * 1e-3) / 1e9, 2),
@@ -760,39 +766,17 @@ def run_ours(args) -> None:
                     "what": "bd_decompress_incremental_batch in place: verified from the "
                             "checksums of the resident weights; algorithmic bytes = payload + "
                             "read and write of each touched 32-byte sector"},
-                "compact": {
-                    "payload_pct": round(100 * p3_bytes / raw, 4),
-                    "payload_vs_v1": round(p3_bytes / payload_bytes, 4),
-                    "compress_ms": round(c3_ms, 4), "apply_ms": round(a3_ms, 4),
-                    "incremental_ms": round(i3_ms, 4),
-                    "compress_roofline_frac": round((4 * n_total + p3_bytes) / (c3_ms * 1e-3)
-                                                    / 1e9 / peak, 4),
-                    "apply_roofline_frac": round((2 * n_total + p3_bytes + 32 * touched)
-                                                 / (a3_ms * 1e-3) / 1e9 / peak, 4),
-                    "what": "version-3 payloads (compact position blocks) of the same update: "
-                            "bd_compress_versioned_batch format 3, bd_decompress_batch in "
-                            "place, bd_decompress_incremental_batch in place"},
-                "rice": {
-                    "payload_pct": round(100 * p4_bytes / raw, 4),
-                    "payload_vs_v1": round(p4_bytes / payload_bytes, 4),
-                    "payload_vs_v3": round(p4_bytes / p3_bytes, 4),
-                    "compress_ms": round(c4_ms, 4), "apply_ms": round(rice_res["apply"], 4),
-                    "incremental_ms": round(rice_res["incremental"], 4),
-                    "compress_roofline_frac": round((4 * n_total + p4_bytes) / (c4_ms * 1e-3)
-                                                    / 1e9 / peak, 4),
-                    "apply_roofline_frac": round((2 * n_total + p4_bytes + 32 * touched)
-                                                 / (rice_res["apply"] * 1e-3) / 1e9 / peak, 4),
-                    "what": "version-4 payloads (Rice-coded compact position blocks) of the same "
-                            "update: bd_compress_versioned_batch format 4, bd_decompress_batch "
-                            "in place, bd_decompress_incremental_batch in place"},
-                "overwrite": {
-                    "compress_ms": round(ow_ms, 4), "apply_ms": round(ow_res["apply"], 4),
-                    "incremental_ms": round(ow_res["incremental"], 4),
-                    "what": "version-3 overwrite payloads (new field values instead of XOR "
-                            "masks; same size as the version-3 XOR payload) of the same update "
-                            "and of its reverse: bd_compress_versioned_batch format 3 | "
-                            "BD_FORMAT_OVERWRITE, bd_decompress_batch and "
-                            "bd_decompress_incremental_batch in place"},
+                "compact": fmt_block(v3, "version-3 payloads (compact position blocks) of the "
+                                         "same update: bd_compress_versioned_batch format 3, "
+                                         "bd_decompress_batch in place, "
+                                         "bd_decompress_incremental_batch in place", p3_bytes),
+                "rice": rice,
+                "overwrite": fmt_block(ow, "version-3 overwrite payloads (new field values "
+                                           "instead of XOR masks; same size as the version-3 "
+                                           "XOR payload) of the same update and of its reverse: "
+                                           "bd_compress_versioned_batch format 3 | "
+                                           "BD_FORMAT_OVERWRITE, bd_decompress_batch and "
+                                           "bd_decompress_incremental_batch in place"),
                 "compress_algorithmic_bytes": comp_bytes, "apply_algorithmic_bytes": app_bytes,
                 "payload_pct": round(100 * payload_bytes / raw, 4),
                 "touched_sector_pct": round(100 * touched / (raw / 32), 3),

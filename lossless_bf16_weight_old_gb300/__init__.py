@@ -278,11 +278,14 @@ class CompressBatch:
 
     def __init__(self, olds: Sequence[torch.Tensor], news: Sequence[torch.Tensor],
                  caps: Sequence[int] | None = None, base_checksums: torch.Tensor | None = None,
-                 compact: bool = False, overwrite: bool = False, rice: bool = False):
+                 compact: bool = False, overwrite: bool = False, rice: bool = False,
+                 workspace: torch.Tensor | None = None):
         """base_checksums (int64[k] device tensor, optional): payloads bound to these base
         checksums (bd_compress_versioned_batch), version 2, version 3 (compact position
         blocks) when `compact` is set or version 4 (Rice-coded ones) when `rice` is set,
-        overwrite payloads when `overwrite` is set."""
+        overwrite payloads when `overwrite` is set.  workspace (optional, uint8 device tensor
+        of at least compress_workspace_size bytes) may be shared by batches whose runs never
+        overlap on the GPU; one is allocated otherwise."""
         if (compact or overwrite or rice) and base_checksums is None:
             raise ValueError("compact, Rice and overwrite payloads are bound to a base: "
                              "pass base_checksums")
@@ -308,8 +311,7 @@ class CompressBatch:
         self.checksums = torch.zeros(k, dtype=torch.int64, device=dev)
         self.statuses = torch.zeros(k, dtype=torch.int32, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.workspace = torch.empty(max(compress_workspace_size(ns), 256), dtype=torch.uint8,
-                                     device=dev)
+        self.workspace = _workspace(compress_workspace_size(ns), dev, workspace)
         items = (_lib.CompressItem * max(1, k))()
         for i in range(k):
             items[i].d_old = _bits(olds[i], "old")[0]
@@ -358,15 +360,16 @@ class DecompressBatch:
 
     def __init__(self, olds: Sequence[torch.Tensor], payloads: Sequence[torch.Tensor],
                  sizes: Sequence[int], expected: torch.Tensor,
-                 outs: Sequence[torch.Tensor] | None = None):
+                 outs: Sequence[torch.Tensor] | None = None,
+                 workspace: torch.Tensor | None = None):
+        """workspace: as for CompressBatch (decompress_workspace_size bytes)."""
         k = len(olds)
         dev = olds[0].device
         outs = list(outs) if outs is not None else list(olds)
         ns = [o.numel() for o in olds]
         self.statuses = torch.zeros(k, dtype=torch.int32, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.workspace = torch.empty(max(decompress_workspace_size(ns), 256),
-                                     dtype=torch.uint8, device=dev)
+        self.workspace = _workspace(decompress_workspace_size(ns), dev, workspace)
         self.expected = expected
         items = (_lib.DecompressItem * max(1, k))()
         for i in range(k):
@@ -396,15 +399,16 @@ class IncrementalBatch:
     """Item table of one batched incremental apply over fixed tensors (in place)."""
 
     def __init__(self, ws: Sequence[torch.Tensor], payloads: Sequence[torch.Tensor],
-                 sizes: Sequence[int], ck_old: torch.Tensor, expected: torch.Tensor):
+                 sizes: Sequence[int], ck_old: torch.Tensor, expected: torch.Tensor,
+                 workspace: torch.Tensor | None = None):
+        """workspace: as for CompressBatch (decompress_workspace_size bytes)."""
         k = len(ws)
         dev = ws[0].device
         ns = [w.numel() for w in ws]
         self.statuses = torch.zeros(k, dtype=torch.int32, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.checksums = torch.zeros(k, dtype=torch.int64, device=dev)
-        self.workspace = torch.empty(max(decompress_workspace_size(ns), 256),
-                                     dtype=torch.uint8, device=dev)
+        self.workspace = _workspace(decompress_workspace_size(ns), dev, workspace)
         items = (_lib.IncrementalItem * max(1, k))()
         for i in range(k):
             items[i].d_w = _bits(ws[i], "w")[0]

@@ -79,13 +79,16 @@ def checksum(w) -> int:
 
 
 def encode(old, new, base: int | None = None, compact: bool = False,
-           overwrite: bool = False, rice: bool = False) -> tuple[np.ndarray, int]:
+           overwrite: bool = False, rice: bool = False,
+           cap: int | None = None) -> tuple[np.ndarray, int]:
     """Returns (payload bytes as a uint8 array, checksum of new).  With `base` (the checksum of
     old as the caller knows it) the payload is version 2, bound to that base; with compact=True
     (which needs a base) it is version 3, with compact position lists; with rice=True (which
     needs a base, and excludes compact) it is version 4, with Rice-coded compact position
     blocks; with overwrite=True (which needs a base) its streams hold new values instead of XOR
-    masks."""
+    masks.  `cap` only saves time: when given, the encoder first writes into a buffer of that
+    many bytes in one pass and is run again with the exact size only if the payload is
+    larger; the result is the same either way."""
     old, new = _u16(old), _u16(new)
     if old.size != new.size:
         raise ValueError("old and new must have the same number of elements")
@@ -110,9 +113,17 @@ def encode(old, new, base: int | None = None, compact: bool = False,
               (True, True): lib.orc_encode_compact_overwrite}[(bool(compact), bool(overwrite))]
         call = lambda out, cap: fn(old.ctypes.data, new.ctypes.data, old.size, b, out, cap,
                                    ctypes.byref(size), ctypes.byref(ck))
-    rc = call(None, 0)
-    if rc not in (OK, ERR_CAPACITY):
-        raise RuntimeError(f"orc_encode failed with {rc}")
+    if cap is not None:
+        out = np.zeros(max(int(cap), 1), dtype=np.uint8)
+        rc = call(out.ctypes.data, out.size)
+        if rc == OK:
+            return out[:size.value].copy(), int(ck.value)
+        if rc != ERR_CAPACITY:
+            raise RuntimeError(f"orc_encode failed with {rc}")
+    else:
+        rc = call(None, 0)
+        if rc not in (OK, ERR_CAPACITY):
+            raise RuntimeError(f"orc_encode failed with {rc}")
     out = np.zeros(size.value, dtype=np.uint8)
     rc = call(out.ctypes.data, out.size)
     if rc != OK:

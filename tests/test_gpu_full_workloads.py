@@ -1,21 +1,29 @@
 """Parity at full size on the 7B-shaped dense checkpoint and the 30B-shaped MoE checkpoint, in
 the launch configuration the benchmark times: one batched compress over every tensor of the
 checkpoint (held in one flat buffer per checkpoint, tensors at 256-byte aligned offsets), then
-one batched in-place apply on a copy of old; the dense checkpoint also in version 3 (compact
+one batched in-place apply on a copy of old; both checkpoints in version 1, version 3 (compact
 position blocks) and version 4 (Rice-coded compact position blocks).
 
-The oracle checks a sample of tensors one by one (payload bytes, size, checksum; integer work,
-tolerance 0).  Every tensor is checked by properties that hold at any size: each status is OK,
-the restored checkpoint equals new bit for bit, and applying the same payloads again with the
-checksums of old restores old exactly.
+The oracle checks EVERY tensor of the checkpoint one by one: payload bytes, size and checksum
+(integer work, tolerance 0).  Byte equality matters beyond "restored == new" because the
+decoders of versions 3 and 4 accept codings the encoder never writes (another Rice parameter,
+a chunk kept on version-1 blocks), so a wrong choice would still restore.  The oracle runs
+one tensor per host thread (its C calls release the interpreter lock), fed by device-to-host
+copies of one tensor at a time with a bound on the host memory in flight.  Every tensor is
+also checked by properties of the apply: each status is OK, the restored checkpoint equals new
+bit for bit, and applying the same payloads again with the checksums of old restores old.
 """
+import collections
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import pytest
 import torch
 
 import oracle
 import workloads as W
-from tests.gpu_util import oracle_pair, to_np_u16
+from tests.gpu_util import to_np_u16
 
 pytestmark = pytest.mark.gpu
 
@@ -54,7 +62,62 @@ def _cap_estimate(spec) -> int:
     return min(bd.compress_bound(n), 64 + 4 * C + per_chunk * C + int(3 * spec.rate * n) + 4096)
 
 
-def _check_workload(specs, sample, compact=False, rice=False):
+def _host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _oracle_one(name, o, nw, got, ck, base, kw):
+    """The oracle's payload for one tensor, compared with the GPU's (a message, or None)."""
+    ref, ref_ck = oracle.encode(o, nw, base=base, cap=got.size, **kw)
+    if ref.size != got.size:
+        return f"{name}: size {got.size} != oracle {ref.size}"
+    if ref_ck != ck:
+        return f"{name}: checksum {ck:#x} != oracle {ref_ck:#x}"
+    if not np.array_equal(ref, got):
+        at = int(np.flatnonzero(ref != got)[0])
+        return f"{name}: payload differs from the oracle's first at byte {at}"
+    return None
+
+
+def _oracle_every_tensor(specs, olds, news, payloads, sizes, cks, bases, kw):
+    """Compares every tensor's payload, size and checksum with the oracle's, one tensor per
+    host thread; at most `limit` bytes of host copies are in flight."""
+    largest = max(4 * s.numel for s in specs)
+    limit = max(6 << 30, 3 * largest)
+    pending = collections.deque()
+    in_flight = 0
+    errors = []
+    checked = 0
+
+    def drain_one():
+        nonlocal in_flight, checked
+        fut, nbytes = pending.popleft()
+        msg = fut.result()
+        in_flight -= nbytes
+        checked += 1
+        if msg is not None:
+            errors.append(msg)
+
+    with ThreadPoolExecutor(max_workers=min(_host_cores(), 64)) as ex:
+        for i, s in enumerate(specs):
+            nbytes = 4 * s.numel + sizes[i]
+            while pending and in_flight + nbytes > limit:
+                drain_one()
+            o, nw = to_np_u16(olds[i]), to_np_u16(news[i])
+            got = payloads[i][:sizes[i]].cpu().numpy()
+            base = None if bases is None else bases[i]
+            pending.append((ex.submit(_oracle_one, s.name, o, nw, got, cks[i], base, kw), nbytes))
+            in_flight += nbytes
+        while pending:
+            drain_one()
+    assert checked == len(specs)
+    assert not errors, f"{len(errors)} of {len(specs)} tensors differ: {errors[:5]}"
+
+
+def _check_workload(specs, compact=False, rice=False):
     dev = torch.device("cuda")
     O, N, offs, ns = _flat(specs, dev)
     olds = [O[off:off + n] for off, n in zip(offs, ns)]
@@ -79,18 +142,9 @@ def _check_workload(specs, sample, compact=False, rice=False):
     sizes = [int(v) for v in comp.sizes.tolist()]
     cks = bd.u64(comp.checksums)
 
-    # sampled tensors against the oracle, byte for byte
-    ck_old_list = bd.u64(ck_old)
-    for i in sample:
-        if bound:
-            ref, ref_ck = oracle.encode(to_np_u16(olds[i]), to_np_u16(news[i]),
-                                        base=ck_old_list[i], **kw)
-        else:
-            ref, ref_ck = oracle_pair(olds[i], news[i])
-        assert sizes[i] == ref.size, specs[i].name
-        assert cks[i] == ref_ck, specs[i].name
-        got = comp.payloads[i][:sizes[i]].cpu().numpy()
-        assert np.array_equal(got, ref), specs[i].name
+    # every tensor against the oracle, byte for byte
+    _oracle_every_tensor(specs, olds, news, comp.payloads, sizes, cks,
+                         bd.u64(ck_old) if bound else None, kw)
 
     # every tensor: in-place apply restores new, applying again with checksum(old) restores old
     R = O.clone()
@@ -140,46 +194,31 @@ def _check_workload(specs, sample, compact=False, rice=False):
 
 
 def test_dense7b_full_size_batched():
-    specs = W.dense7b()
-    names = {s.name: i for i, s in enumerate(specs)}
-    sample = [names[x] for x in ("embed", "layers.0.q", "layers.0.gate", "layers.0.down",
-                                 "layers.0.norm1", "layers.31.up", "norm", "lm_head")]
-    _check_workload(specs, sample)
+    _check_workload(W.dense7b())
 
 
 def test_dense7b_full_size_compact():
     """The same checkpoint in version 3 (compact position blocks), bound to checksum(old)."""
-    specs = W.dense7b()
-    names = {s.name: i for i, s in enumerate(specs)}
-    sample = [names[x] for x in ("embed", "layers.0.q", "layers.0.down", "layers.0.norm1",
-                                 "norm", "lm_head")]
-    _check_workload(specs, sample, compact=True)
+    _check_workload(W.dense7b(), compact=True)
 
 
 def test_dense7b_full_size_rice():
     """The same checkpoint in version 4 (Rice-coded compact position blocks)."""
-    specs = W.dense7b()
-    names = {s.name: i for i, s in enumerate(specs)}
-    sample = [names[x] for x in ("embed", "layers.0.k", "layers.0.up", "layers.0.norm2",
-                                 "layers.31.o", "norm")]
-    _check_workload(specs, sample, rice=True)
-
-
-def test_moe30b_full_size_compact():
-    """The MoE checkpoint in version 3: hot experts with dense chunks (version-1 bitmaps and
-    compact chunks of 253..508 changes through the dense emit) beside sparse cold experts."""
-    specs = W.moe30b()
-    names = {s.name: i for i, s in enumerate(specs)}
-    hot = max(range(len(specs)), key=lambda i: specs[i].rate)
-    sample = [names["embed"], hot, names["layers.0.q"], names["lm_head"]]
-    _check_workload(specs, sample, compact=True)
+    _check_workload(W.dense7b(), rice=True)
 
 
 def test_moe30b_full_size_batched():
-    specs = W.moe30b()
-    names = {s.name: i for i, s in enumerate(specs)}
-    hot = max(range(len(specs)), key=lambda i: specs[i].rate)   # a hot expert (bitmap chunks)
-    cold = next(i for i, s in enumerate(specs) if ".experts." in s.name and s.rate < specs[hot].rate)
-    sample = [names["embed"], hot, cold, names["layers.0.q"], names["layers.0.k"],
-              names["layers.47.router"], names["lm_head"]]
-    _check_workload(specs, sample)
+    """The MoE checkpoint: hot experts with dense chunks (bitmaps, the dense emit and apply)
+    beside sparse cold experts, attention, routers, embedding and head."""
+    _check_workload(W.moe30b())
+
+
+def test_moe30b_full_size_compact():
+    """The MoE checkpoint in version 3: compact chunks of 253..508 changes through the dense
+    emit beside version-1 bitmaps."""
+    _check_workload(W.moe30b(), compact=True)
+
+
+def test_moe30b_full_size_rice():
+    """The MoE checkpoint in version 4."""
+    _check_workload(W.moe30b(), rice=True)

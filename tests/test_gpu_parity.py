@@ -241,8 +241,9 @@ def test_inplace_rollback_after_error():
 
 def test_pages_api_snippet():
     """delta_compress / delta_decompress as in the API listing of the ARCv3 page."""
-    src = torch.randn(1024, 1024, dtype=torch.bfloat16, device="cuda")
-    dst = src + 1e-3 * torch.randn_like(src)
+    g = torch.Generator(device="cuda").manual_seed(0x5EED)
+    src = torch.randn(1024, 1024, dtype=torch.bfloat16, device="cuda", generator=g)
+    dst = src + 1e-3 * torch.randn(src.shape, dtype=src.dtype, device="cuda", generator=g)
     compressed_diff, checksum = bd.delta_compress(src=src, dst=dst)
     restored = bd.delta_decompress(src=src, compressed_diff=compressed_diff, checksum=checksum)
     assert torch.equal(restored.view(torch.uint8), dst.view(torch.uint8))
