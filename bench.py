@@ -13,11 +13,14 @@ replicas, weak scaling).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload dense7b] [--impl reference]
 
-`--profile-case embed|layers|formats` runs a fixed small program for an ncu capture instead (no
-timing, no JSON line): `embed` compresses the 32000x4096 embedding tensor of dense7b in versions
-1, 3 and 4 and applies each payload, two rounds; `layers` does the same in version 1 with the
-18 tensors of dense7b's first two layers (a batch the fused compress takes); `formats` with
-versions 3 and 4 on the whole workload, with the incremental apply too.
+`--profile-case embed|layers|dense|formats` runs a fixed small program for an ncu capture
+instead (no timing, no JSON line), two rounds of: compress in each version, the full verified
+apply and the incremental apply of each payload.  `embed`: the 32000x4096 embedding tensor of
+dense7b in versions 1, 3 and 4 (the separate compress kernels), plus the standalone checksum and
+an out-of-place apply; `layers`: the 18 tensors of dense7b's first two layers in versions 1, 3
+and 4 (the fused compress); `dense`: a 2^26-element tensor made by the 1 GiB workload's rule
+(22% changed: the dense emit and apply) in versions 1 and 3, plus the checksum and an
+out-of-place apply; `formats`: the whole --workload in versions 3 and 4.
 """
 from __future__ import annotations
 
@@ -789,31 +792,36 @@ def run_ours(args) -> None:
 
 
 def run_profile_case(args) -> None:
-    """The fixed programs that the committed ncu summaries were captured from (one GPU)."""
+    """The fixed programs that the committed ncu summaries were captured from (one GPU).
+
+    Each round of every case: compress in each version, the full verified apply of each
+    payload in place (alternately to new and back to old), and the incremental apply of each
+    payload from old; `embed` and `dense` also run the standalone checksum of old and one
+    out-of-place full apply (the copy kernel).  Two rounds, so that a capture can skip the
+    first."""
     import lossless_bf16_weight_old_gb300 as bd
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    if args.profile_case in ("embed", "layers"):
-        if args.profile_case == "embed":
-            specs = [s for s in W.dense7b() if s.name == "embed"]
-            versions = (1, 3, 4)
-        else:
-            specs = [s for s in W.dense7b() if s.name.startswith(("layers.0.", "layers.1."))]
-            versions = (1,)
-        olds, news = [], []
-        for s in specs:
-            a, b = W.make_pair(s, device=dev)
-            olds.append(a.reshape(-1))
-            news.append(b.reshape(-1))
-    else:
+    case = args.profile_case
+    if case == "embed":        # one 32000x4096 tensor: the separate compress kernels
+        specs = [s for s in W.dense7b() if s.name == "embed"]
+        versions = (1, 3, 4)
+    elif case == "layers":     # dense7b's first two layers: the fused compress
+        specs = [s for s in W.dense7b() if s.name.startswith(("layers.0.", "layers.1."))]
+        versions = (1, 3, 4)
+    elif case == "dense":      # a 2^26-element slice of the 1 GiB workload: the dense kernels
+        specs = [W.Spec("w", (1 << 26,), kind="additive", tid=0)]
+        versions = (1, 3)
+    else:                      # "formats": a whole workload in versions 3 and 4
         specs = _workload_specs(args.workload)
-        olds, news = [], []
-        for s in specs:
-            a, b = W.make_pair(s, device=dev)
-            olds.append(a.reshape(-1))
-            news.append(b.reshape(-1))
         versions = (3, 4)
+    olds, news = [], []
+    for s in specs:
+        a, b = W.make_pair(s, device=dev)
+        olds.append(a.reshape(-1))
+        news.append(b.reshape(-1))
     rolls = [o.clone() for o in olds]
+    outs = [torch.empty_like(o) for o in olds] if case in ("embed", "dense") else None
     ck_old = torch.cat([bd.checksum(o).reshape(1) for o in olds])
     comp = {v: (bd.CompressBatch(olds, news) if v == 1 else
                 bd.CompressBatch(olds, news, base_checksums=ck_old, compact=v == 3, rice=v == 4))
@@ -836,21 +844,34 @@ def run_profile_case(args) -> None:
             dec.run()
             done.append(dec)
             state_new = not state_new
-        if args.profile_case == "formats":
-            for v in versions:
-                for r, o in zip(rolls, olds):
-                    r.copy_(o)
-                inc = bd.IncrementalBatch(rolls, comp[v].payloads, sizes[v], ck_old, ck_new)
-                inc.run()
-                done.append(inc)
-                state_new = True
         torch.cuda.synchronize()
         want = news if state_new else olds
         if any(int(x.status.item()) != bd.OK for x in done) or not all(
                 torch.equal(r.view(torch.int16), w.view(torch.int16))
                 for r, w in zip(rolls, want)):
-            raise RuntimeError("profile case did not verify")
-    print("profile case", args.profile_case, "ok:",
+            raise RuntimeError("profile case did not verify (full apply)")
+        done = []
+        for v in versions:
+            for r, o in zip(rolls, olds):
+                r.copy_(o)
+            inc = bd.IncrementalBatch(rolls, comp[v].payloads, sizes[v], ck_old, ck_new)
+            inc.run()
+            done.append(inc)
+        torch.cuda.synchronize()
+        if any(int(x.status.item()) != bd.OK for x in done) or not all(
+                torch.equal(r.view(torch.int16), w.view(torch.int16))
+                for r, w in zip(rolls, news)):
+            raise RuntimeError("profile case did not verify (incremental apply)")
+        if outs is not None:
+            cks = torch.cat([bd.checksum(o).reshape(1) for o in olds])
+            oop = bd.DecompressBatch(olds, comp[1].payloads, sizes[1], ck_new, outs=outs)
+            oop.run()
+            torch.cuda.synchronize()
+            if (bd.u64(cks) != bd.u64(ck_old) or int(oop.status.item()) != bd.OK or not all(
+                    torch.equal(r.view(torch.int16), w.view(torch.int16))
+                    for r, w in zip(outs, news))):
+                raise RuntimeError("profile case did not verify (checksum, out of place)")
+    print("profile case", case, "ok:",
           {v: sum(sizes[v]) for v in versions}, "payload bytes", flush=True)
 
 
@@ -865,7 +886,8 @@ def main(argv=None):
                    help="elements of the workload the CPU oracle baseline encodes+decodes")
     p.add_argument("--ref-sample-elems", type=int, default=400_000_000,
                    help="elements per step of the --impl reference arm")
-    p.add_argument("--profile-case", choices=["embed", "layers", "formats"], default=None,
+    p.add_argument("--profile-case", choices=["embed", "layers", "dense", "formats"],
+                   default=None,
                    help="run a fixed small program for an ncu capture instead of the bench")
     args = p.parse_args(argv)
     if args.profile_case:

@@ -335,7 +335,7 @@ int decompress_impl(const DecItem* items, uint32_t k, void* ws, uint64_t ws_byte
   } else {
     if ((rc = check(launch_apply_chunks(c)))) return rc;
   }
-  if ((rc = check(launch_apply(c, incremental)))) return rc;
+  if ((rc = check(launch_apply_bitmap(c, incremental)))) return rc;
   return check(launch_apply_finish(c, status_all));
 }
 

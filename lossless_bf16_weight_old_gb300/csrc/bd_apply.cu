@@ -1231,6 +1231,236 @@ k_apply_incr(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
   if (cur != kNone) flush_ck(ck_base, cur, gwarp, ck);
 }
 
+// ------------------------------------------------------------------------ apply_bitmap
+
+// Little-endian u32 at the 4-byte aligned address p; bytes at or past `end` read as zero
+// (nothing past the payload is read).
+__device__ __forceinline__ uint32_t ld_u32_upto(const uint8_t* p, const uint8_t* end) {
+  if (p + 4 <= end) return __ldg(reinterpret_cast<const uint32_t*>(p));
+  uint32_t v = 0;
+  for (int i = 0; i < 4; i++)
+    if (p + i < end) v |= (uint32_t)p[i] << (8 * i);
+  return v;
+}
+
+// The 64 stream bits from bit `bit` of the byte stream s on (bit b = bit b%8 of byte b/8;
+// bits at or past `end` read as zero).
+__device__ __forceinline__ uint64_t bits64_at(const uint8_t* s, uint64_t bit, const uint8_t* end) {
+  const uint8_t* p = s + (bit >> 3);
+  const uint8_t* a = reinterpret_cast<const uint8_t*>(reinterpret_cast<uintptr_t>(p) & ~(uintptr_t)3);
+  const uint32_t sh = (uint32_t)((p - a) * 8 + (bit & 7));   // 0..31
+  const uint64_t lo = (uint64_t)ld_u32_upto(a, end) | ((uint64_t)ld_u32_upto(a + 4, end) << 32);
+  const uint64_t hi = ld_u32_upto(a + 8, end);
+  return sh ? (lo >> sh) | (hi << (64 - sh)) : lo;
+}
+
+// The value v repeated in each of nine 7-bit fields (bits 7f .. 7f+6, f = 0..8).
+constexpr uint64_t fields9(uint64_t v) {
+  uint64_t r = 0;
+  for (int f = 0; f < 9; f++) r |= v << (7 * f);
+  return r;
+}
+constexpr uint64_t kField6 = fields9(0x3F), kField7 = fields9(0x40);
+
+// Per-warp shared state of apply_bitmap: the chunk's two position blocks as bitmaps (a block
+// that is a bitmap in the payload is copied as the aligned words covering it, read from byte
+// offset `off`; a delta list is decoded into a bitmap at offset 0).
+struct BitmapSmem {
+  uint32_t w[2][130];   // [0]: mantissa-only, [1]: rare
+};
+
+// Byte q (0 <= q < 512) of the class-c bitmap; bytes past the chunk's B read as zero.
+__device__ __forceinline__ uint32_t bm_byte(const BitmapSmem* sm, int c, uint32_t off,
+                                            uint32_t q, uint32_t B) {
+  return q < B ? reinterpret_cast<const uint8_t*>(sm->w[c])[off + q] : 0u;
+}
+// Word i of the class-c bitmap (positions 32i .. 32i+31), bytes past B as zero.
+__device__ __forceinline__ uint32_t bm_word(const BitmapSmem* sm, int c, uint32_t off,
+                                            uint32_t i, uint32_t B) {
+  const uint32_t a = sm->w[c][(off >> 2) + i], b = sm->w[c][(off >> 2) + i + 1];
+  uint32_t v = (off & 3) ? __funnelshift_r(a, b, 8 * (off & 3)) : a;
+  if (4 * i + 4 > B) v &= 4 * i >= B ? 0u : (0xFFFFFFFFu >> (8 * (4 * i + 4 - B)));
+  return v;
+}
+
+// Reads one position block of a chunk into a bitmap of sm: a delta list of k entries at blk
+// (deltas of at least 1 after the first, positions below L) or a B-byte bitmap at blk.
+// Returns the byte offset to read it from; sets bad for a malformed list.
+__device__ __forceinline__ uint32_t load_block(BitmapSmem* sm, int c, const uint8_t* blk,
+                                               uint32_t k, uint32_t B, uint32_t L, bool list,
+                                               const uint8_t* end, bool& bad) {
+  const int lane = threadIdx.x & 31;
+  uint32_t* w = sm->w[c];
+  if (!list) {
+    const uint8_t* a = reinterpret_cast<const uint8_t*>(reinterpret_cast<uintptr_t>(blk) & ~(uintptr_t)3);
+    const uint32_t off = (uint32_t)(blk - a);
+    const uint32_t nw = (off + B + 3) / 4;
+    for (uint32_t i = lane; i < nw; i += 32) w[i] = ld_u32_upto(a + 4 * i, end);
+    if ((uint32_t)lane < 130 - nw && nw + lane < 130) w[nw + lane] = 0;   // guard words
+    return off;
+  }
+  for (uint32_t i = lane; i < 130; i += 32) w[i] = 0;
+  __syncwarp();
+  uint32_t carry = 0;
+  for (uint32_t b0 = 0; b0 < k; b0 += 32) {
+    const uint32_t i = b0 + lane;
+    const bool in = i < k;
+    const uint32_t d = in ? load_u16(blk + 2 * i) : 0u;
+    if (in && i > 0 && d == 0) bad = true;
+    const uint32_t p = carry + warp_incl_scan(d);
+    carry = __shfl_sync(kFull, p, 31);
+    if (in) {
+      if (p >= L) bad = true;
+      else atomicOr(&w[p >> 5], 1u << (p & 31));
+    }
+  }
+  return 0;
+}
+
+// One warp per listed chunk (a chunk with at least one bitmap block; compact chunks never have
+// one), each warp taking every nwarps-th entry of the list.  The chunk is checked in full
+// first -- the blocks (list deltas, positions below L, bitmap counts equal to M and R, no bit at
+// or past L, no position in both classes) and, for an XOR payload, every value (a nonzero
+// mantissa mask, a rare mask with a sign or exponent bit) -- and left unwritten when
+// malformed.  Then 16 steps of 256 elements, lane l taking the 8-element group 32s + l: the
+// ranks of the group's first values come from one warp scan of the two classes' bit counts,
+// its mantissa-only values from one 64-bit window of the M stream, its rare values from the R
+// stream; the group is XORed (an overwrite payload: its records written in place of the
+// fields), stored when it changed, and its checksum terms added (INCR: new minus old terms of
+// the changed groups).  The chunk is prefetched into L2 while its payload is checked, and
+// each step's group loads are issued one step ahead.
+template <bool INCR>
+__global__ void __launch_bounds__(kThreads, 4)
+k_apply_bitmap(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
+               const uint64_t* __restrict__ tile_start, uint32_t k,
+               const uint32_t* __restrict__ list_count, const uint32_t* __restrict__ list,
+               const uint4* __restrict__ loc, const TileSum* __restrict__ tile_pre,
+               JobInfo* __restrict__ info, uint8_t* __restrict__ ck_base) {
+  __shared__ BitmapSmem s_bm[kWarps];
+  const int lane = threadIdx.x & 31;
+  BitmapSmem* sm = &s_bm[threadIdx.x >> 5];
+  const uint64_t gwarp = ((uint64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+  const uint64_t nwarps = ((uint64_t)gridDim.x * kThreads) >> 5;
+  const uint32_t listed = *list_count;
+  uint32_t cur = kNone;
+  uint64_t ck = 0;
+  for (uint64_t li = gwarp; li < listed; li += nwarps) {
+    const uint64_t g = list[li];
+    const uint32_t j = find_job(chunk_start, k, g);
+    const JobInfo& I = info[j];
+    if (I.status != BD_OK) continue;
+    if (j != cur) {
+      if (cur != kNone) flush_ck(ck_base, cur, gwarp, ck);
+      cur = j;
+      ck = 0;
+    }
+    const DJob& J = jobs[j];
+    const uint64_t n = J.n, c = g - chunk_start[j], e0 = c * kChunk;
+    uint16_t* __restrict__ out = J.out;
+    if (e0 + kChunk <= n) prefetch_chunk_l2(out + e0);   // in L2 by the time it is read
+    const uint32_t L = (n - e0) < kChunk ? (uint32_t)(n - e0) : kChunk;
+    const uint32_t B = (L + 7) >> 3;
+    const uint8_t* __restrict__ payload = J.payload;
+    const uint8_t* end = payload + J.size;
+    const TileSum pre = tile_pre[tile_start[j] + c / kTileChunks];
+    const uint4 lc = loc[g];
+    const ChunkCount cc = parse_count(reinterpret_cast<const uint32_t*>(
+        payload + count_table_offset(I.r_start, J.nchunks))[c], I.version);
+    const uint32_t M = cc.M, R = cc.R;
+    const uint64_t Pex = pre.p + lc.x, Mex = pre.m + lc.y, Rex = pre.r + lc.z;
+    const bool listM = 2 * M < B, listR = 2 * R < B;
+    const uint8_t* mblk = payload + I.p_start + Pex;
+    const uint8_t* rblk = mblk + block_bytes(M, B);
+    const uint8_t* mstream = payload + I.m_start;
+    const uint16_t* rstream = reinterpret_cast<const uint16_t*>(payload + I.r_start) + Rex;
+    const bool ow = (I.flags & kFlagOverwrite) != 0;
+
+    // ---- check the whole chunk before anything is written
+    bool bad = cc.compact;   // (never listed)
+    const uint32_t offM = load_block(sm, 0, mblk, M, B, L, listM, end, bad);
+    const uint32_t offR = load_block(sm, 1, rblk, R, B, L, listR, end, bad);
+    __syncwarp();
+    uint32_t cM = 0, cR = 0;
+    for (uint32_t i = lane; 4 * i < B; i += 32) {
+      const uint32_t wM = bm_word(sm, 0, offM, i, B), wR = bm_word(sm, 1, offR, i, B);
+      const uint32_t valid = 32 * i + 32 <= L ? 0xFFFFFFFFu : (0xFFFFFFFFu >> (32 * i + 32 - L));
+      if ((wM & wR) != 0 || ((wM | wR) & ~valid) != 0) bad = true;
+      cM += __popc(wM);
+      cR += __popc(wR);
+    }
+    cM = __reduce_add_sync(kFull, cM);
+    cR = __reduce_add_sync(kFull, cR);
+    if (cM != M || cR != R) bad = true;
+    if (!ow) {
+      // every 7-bit mantissa mask nonzero: nine fields per 63-bit window, field f nonzero
+      // exactly when bit 6 of ((f & 0x3F) + 0x3F) | f is set (the add cannot carry out of it)
+      for (uint32_t v0 = 9 * lane; v0 < M; v0 += 9 * 32) {
+        const uint32_t nf = M - v0 < 9 ? M - v0 : 9;
+        const uint64_t x = bits64_at(mstream, 7 * (Mex + v0), end);
+        const uint64_t keep = kField7 & ((1ull << (7 * nf)) - 1);
+        if (((((x & kField6) + kField6) | x) & keep) != keep) bad = true;
+      }
+      for (uint32_t i = lane; i < R; i += 32)
+        if ((rstream[i] & kSignExp) == 0) bad = true;
+    }
+    if (__any_sync(kFull, bad)) {
+      if (lane == 0) record_status(&info[j].chunk_err, BD_ERR_FORMAT);
+      __syncwarp();
+      continue;
+    }
+
+    // ---- apply, 16 steps of 256 elements
+    const uint64_t words = (n + 3) >> 2;
+    uint32_t rM = 0, rR = 0;   // ranks of the values before this step
+    uint64_t ea = e0 + 8 * (uint64_t)lane;
+    uint4 nxt = load8(out, ea, n);
+#pragma unroll 1
+    for (uint32_t s = 0; s < 16; s++, ea += 256) {
+      const uint4 now = nxt;
+      if (s < 15) nxt = load8(out, ea + 256, n);
+      const uint32_t q = 32 * s + lane;
+      const uint32_t bm = bm_byte(sm, 0, offM, q, B), br = bm_byte(sm, 1, offR, q, B);
+      const uint32_t packed = __popc(bm) | (__popc(br) << 16);
+      const uint32_t incl = warp_incl_scan(packed), excl = incl - packed;
+      const uint32_t tot = __shfl_sync(kFull, incl, 31);
+      uint64_t t0 = 0, t1 = 0;   // the group's values (XOR masks or overwrite targets)
+      if (bm) {
+        uint64_t win = bits64_at(mstream, 7 * (Mex + rM + (excl & 0xFFFFu)), end);
+        for (uint32_t b = bm; b; b &= b - 1) {
+          const uint32_t i = __ffs(b) - 1;
+          const uint64_t v = (win & kMant) << (16 * (i & 3));
+          if (i < 4) t0 |= v; else t1 |= v;
+          win >>= 7;
+        }
+      }
+      if (br) {
+        uint32_t r = rR + (excl >> 16);
+        for (uint32_t b = br; b; b &= b - 1, r++) {
+          const uint32_t i = __ffs(b) - 1;
+          const uint64_t v = (uint64_t)rstream[r] << (16 * (i & 3));
+          if (i < 4) t0 |= v; else t1 |= v;
+        }
+      }
+      rM += tot & 0xFFFFu;
+      rR += tot >> 16;
+      uint4 m = make_uint4((uint32_t)t0, (uint32_t)(t0 >> 32), (uint32_t)t1, (uint32_t)(t1 >> 32));
+      if (ow) m = overwrite_mask(m, now, bm, br);
+      const bool ch = (m.x | m.y | m.z | m.w) != 0;
+      const uint4 res = make_uint4(now.x ^ m.x, now.y ^ m.y, now.z ^ m.z, now.w ^ m.w);
+      if (ch && ea < n) {
+        if (ea + 8 <= n) *reinterpret_cast<uint4*>(out + ea) = res;
+        else for (int i = 0; ea + i < n; i++) out[ea + i] = (uint16_t)elem_of(res, i);
+      }
+      if (INCR) {
+        if (ch) ck += group_hash(res, ea >> 3, words) - group_hash(now, ea >> 3, words);
+      } else {
+        ck += group_hash(res, ea >> 3, words);
+      }
+    }
+  }
+  if (cur != kNone) flush_ck(ck_base, cur, gwarp, ck);
+}
+
 // Out-of-place apply: copies old to out (warp per chunk) for the tensors with out != old.
 __global__ void __launch_bounds__(kThreads)
 k_copy_jobs(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start, uint32_t k,
@@ -1349,6 +1579,25 @@ cudaError_t launch_apply(const LaunchCtx& c, bool incremental) {
   static const int per_sm = blocks_per_sm(k_apply_dense<false>);
   const uint64_t grid = std::min<uint64_t>(c.chunks, (uint64_t)per_sm * c.sms);
   auto kernel = incremental ? k_apply_dense<true> : k_apply_dense<false>;
+  kernel<<<(unsigned)grid, kThreads, 0, c.stream>>>(
+      reinterpret_cast<const DJob*>(c.ws + c.lay.jobs),
+      reinterpret_cast<const uint64_t*>(c.ws + c.lay.chunk_start),
+      reinterpret_cast<const uint64_t*>(c.ws + c.lay.tile_start), c.k,
+      reinterpret_cast<const uint32_t*>(c.ws + c.lay.overflow),
+      reinterpret_cast<const uint32_t*>(c.ws + c.lay.ovf_list),
+      reinterpret_cast<const uint4*>(c.ws + c.lay.loc),
+      reinterpret_cast<const TileSum*>(c.ws + c.lay.tile_pre),
+      reinterpret_cast<JobInfo*>(c.ws + c.lay.info), c.ws + c.lay.ck);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_apply_bitmap(const LaunchCtx& c, bool incremental) {
+  if (c.chunks == 0) return cudaSuccess;
+  static const int per_sm = blocks_per_sm(k_apply_bitmap<false>);
+  static const int per_sm_i = blocks_per_sm(k_apply_bitmap<true>);
+  const uint64_t grid = std::min<uint64_t>((c.chunks + kWarps - 1) / kWarps,
+                                           (uint64_t)(incremental ? per_sm_i : per_sm) * c.sms);
+  auto kernel = incremental ? k_apply_bitmap<true> : k_apply_bitmap<false>;
   kernel<<<(unsigned)grid, kThreads, 0, c.stream>>>(
       reinterpret_cast<const DJob*>(c.ws + c.lay.jobs),
       reinterpret_cast<const uint64_t*>(c.ws + c.lay.chunk_start),

@@ -583,6 +583,8 @@ cudaError_t launch_apply_chunks(const LaunchCtx& c);
 cudaError_t launch_apply_incremental(const LaunchCtx& c);
 cudaError_t launch_copy_jobs(const LaunchCtx& c);
 cudaError_t launch_apply(const LaunchCtx& c, bool incremental = false);
+// The listed chunks (those with a bitmap block) of a call with a workspace, one warp each.
+cudaError_t launch_apply_bitmap(const LaunchCtx& c, bool incremental);
 cudaError_t launch_apply_finish(const LaunchCtx& c, int32_t* d_status_all);
 cudaError_t launch_checksum(const uint16_t* w, uint64_t n, uint64_t* out, cudaStream_t s,
                             int sms);
