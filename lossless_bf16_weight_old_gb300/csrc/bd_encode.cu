@@ -876,11 +876,157 @@ __device__ __noinline__ void emit_rice_list(const uint32_t* lst, uint32_t cnt, b
   store_bitmap(dst, sm->bm, nb);
 }
 
+// Positions of one class in a delta list: lane holds the changes at p0 + b for the set bits b of
+// mask, the class's first rank `rank` of them; `last` is the class's last position before this
+// step (0 at the start of the chunk, so that the first delta is the position itself).
+__device__ __forceinline__ void list_deltas(uint8_t* blk, uint32_t mask, uint32_t p0,
+                                            uint32_t rank, uint32_t k, int32_t& last) {
+  const int lane = threadIdx.x & 31;
+  const int32_t mine = mask ? (int32_t)(p0 + 31 - __clz(mask)) : -1;
+  const int32_t incl = warp_incl_max(mine);
+  int32_t prev = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
+  if (lane == 0) prev = -1;
+  prev = max(prev, last);
+  for (uint32_t b = mask; b; b &= b - 1, rank++) {
+    const uint32_t pos = p0 + __ffs(b) - 1;
+    if (rank < k) store_u16(blk + 2 * rank, (uint16_t)(pos - (uint32_t)prev));
+    prev = (int32_t)pos;
+  }
+  last = max(last, __shfl_sync(0xFFFFFFFFu, incl, 31));
+}
+
+// A chunk too dense for a slot, with plain (version-1) blocks, one warp: 8 steps of 512 elements
+// (lane l: elements 512s + 16l .. +15, the next step's loads in flight).  A bitmap block is
+// written straight from the lane's 16-bit class mask (two bytes per lane and step), a delta
+// list from the positions; rare values go to the R stream by rank.  The lane's mantissa-only
+// values are packed 7 bits each and ORed into a shared bit buffer at their stream offset
+// (buffer bit 0 = stream bit 8 * b_next); after each step the complete bytes are written to the
+// M stream and the buffer keeps the bits of the last, incomplete byte.  Only the bytes
+// [b_lo, b_hi) belong to the chunk: the bits of its first value that fall in byte b_lo - 1 are
+// the previous chunk's to write, and its last byte takes the low bits of the next mantissa
+// value of the tensor, `after`.
+__device__ __forceinline__ void emit_dense_plain(const uint16_t* __restrict__ old,
+                                                 const uint16_t* __restrict__ neu, uint64_t n,
+                                                 uint64_t e0, uint32_t B, uint32_t M, uint32_t R,
+                                                 uint64_t Mex, const EmitCtx& cx, bool ow,
+                                                 uint8_t* __restrict__ mout, uint64_t b_lo,
+                                                 uint64_t b_hi, uint32_t* __restrict__ sb,
+                                                 uint64_t g, uint64_t g_job_end, uint64_t sum_m,
+                                                 const uint32_t* __restrict__ counts,
+                                                 const uint8_t* __restrict__ slots) {
+  const int lane = threadIdx.x & 31;
+  uint8_t* sbb = reinterpret_cast<uint8_t*>(sb);
+  for (int i = lane; i < 256; i += 32) sb[i] = 0;
+  __syncwarp();
+  uint64_t b_next = b_lo;
+  uint32_t rM = 0, rR = 0;
+  int32_t lastM = 0, lastR = 0;
+  uint64_t e = e0 + 16 * (uint64_t)lane;
+  uint4 o0 = load8(old, e, n), o1 = load8(old, e + 8, n);
+  uint4 n0 = load8(neu, e, n), n1 = load8(neu, e + 8, n);
+#pragma unroll 1
+  for (uint32_t s = 0; s < 8; s++, e += 512) {
+    const uint4 x0 = xor4(o0, n0), x1 = xor4(o1, n1);
+    const uint4 w0 = ow ? n0 : x0, w1 = ow ? n1 : x1;   // the values written
+    if (s < 7) {
+      o0 = load8(old, e + 512, n);
+      o1 = load8(old, e + 520, n);
+      n0 = load8(neu, e + 512, n);
+      n1 = load8(neu, e + 520, n);
+    }
+    const uint32_t rm = rare_mask16(x0, x1);
+    const uint32_t mm = nz_mask16(x0, x1) & ~rm;
+    const uint32_t packed = __popc(mm) | (__popc(rm) << 16);
+    const uint32_t incl = warp_incl_scan(packed), excl = incl - packed;
+    const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    const uint32_t p0 = 512 * s + 16 * lane;
+    const uint32_t q = 64 * s + 2 * lane;   // the lane's first bitmap byte
+    // positions
+    if (!cx.listM) {
+      if (q + 1 < B) store_u16(cx.mblk + q, (uint16_t)mm);
+      else if (q < B) cx.mblk[q] = (uint8_t)mm;
+    } else {
+      list_deltas(cx.mblk, mm, p0, rM + (excl & 0xFFFFu), M, lastM);
+    }
+    if (!cx.listR) {
+      if (q + 1 < B) store_u16(cx.rblk + q, (uint16_t)rm);
+      else if (q < B) cx.rblk[q] = (uint8_t)rm;
+    } else {
+      list_deltas(cx.rblk, rm, p0, rR + (excl >> 16), R, lastR);
+    }
+    // rare values
+    {
+      uint32_t r = rR + (excl >> 16);
+      for (uint32_t b = rm; b; b &= b - 1, r++) {
+        const int i = __ffs(b) - 1;
+        if (r < R) cx.rstream[r] = (uint16_t)elem_of(i < 8 ? w0 : w1, i & 7);
+      }
+    }
+    // mantissa-only values into the bit buffer
+    if (mm) {
+      uint64_t lo = 0, hi = 0;
+      uint32_t kk = 0;
+      for (uint32_t b = mm; b; b &= b - 1, kk++) {
+        const int i = __ffs(b) - 1;
+        const uint64_t v = elem_of(i < 8 ? w0 : w1, i & 7) & kMant;
+        if (kk < 9) lo |= v << (7 * kk);
+        else hi |= v << (7 * (kk - 9));
+      }
+      // 128-bit value (a3:a2:a1:a0) of the lane's 7 * kk bits
+      uint64_t A = lo | (hi << 63), Bh = hi >> 1;
+      int64_t rel = (int64_t)(7 * (Mex + rM + (excl & 0xFFFFu))) - (int64_t)(8 * b_next);
+      if (rel < 0) {   // the chunk's first value: its bits below byte b_lo are not ours
+        const uint32_t d = (uint32_t)(-rel);
+        A = (A >> d) | (Bh << (64 - d));
+        Bh >>= d;
+        rel = 0;
+      }
+      const uint32_t wd = (uint32_t)rel >> 5, sh = (uint32_t)rel & 31;
+      const uint32_t a0 = (uint32_t)A, a1 = (uint32_t)(A >> 32), a2 = (uint32_t)Bh,
+                     a3 = (uint32_t)(Bh >> 32);
+      const uint32_t o[5] = {a0 << sh, __funnelshift_l(a0, a1, sh), __funnelshift_l(a1, a2, sh),
+                             __funnelshift_l(a2, a3, sh), __funnelshift_l(a3, 0u, sh)};
+#pragma unroll
+      for (int i = 0; i < 5; i++)
+        if (o[i]) atomicOr(&sb[wd + i], o[i]);
+    }
+    rM += tot & 0xFFFFu;
+    rR += tot >> 16;
+    __syncwarp();
+    // write the complete bytes, keep the incomplete one (the buffer holds `avail` bits; before
+    // the chunk's first value it can be up to 7 short of byte b_lo)
+    const int64_t avail = (int64_t)(7 * (Mex + rM)) - (int64_t)(8 * b_next);
+    uint64_t nbytes = avail > 0 ? (uint64_t)avail >> 3 : 0;
+    if (nbytes > b_hi - b_next) nbytes = b_hi - b_next;
+    for (uint32_t t = lane; t < (uint32_t)nbytes; t += 32) mout[b_next + t] = sbb[t];
+    const uint32_t keep = avail > (int64_t)(8 * nbytes) ? sbb[nbytes] : 0u;
+    __syncwarp();
+    const uint32_t used = avail > 0 ? (uint32_t)((avail + 31) >> 5) + 1 : 1u;
+    for (uint32_t i = lane; i < used && i < 256; i += 32) sb[i] = 0;
+    __syncwarp();
+    if (lane == 0) sb[0] = keep;
+    __syncwarp();
+    b_next += nbytes;
+  }
+  if (b_hi > b_next) {   // the last byte: its high bits start the next value of the tensor
+    uint32_t after = 0;
+    if (Mex + M < sum_m) {   // (warp-uniform: every lane takes part in the search)
+      const uint32_t cnt_next = g + 1 < g_job_end ? counts[g + 1] : 0u;
+      const uint32_t aux_next =
+          g + 1 < g_job_end ? reinterpret_cast<const uint32_t*>(slots + (g + 1) * kSlotBytes)[1] : 0u;
+      after = next_mant_value<true>(g, g_job_end, cnt_next, aux_next, counts, slots);
+    }
+    const uint32_t bits = (uint32_t)(7 * (Mex + M) - 8 * b_next);   // 1..7
+    if (lane == 0) mout[b_next] = (uint8_t)(sbb[0] | (after << bits));
+  }
+  __syncwarp();
+}
+
 // Chunks with more changes than a slot holds (listed by encode_slots): the changes are derived
-// again from old and new, 512 elements per step; after each step the mantissa-stream bytes
-// whose two values are known are written and the value window keeps only its last value.
-// A compact chunk (at most kCompactMax changes) first gathers its changes in position order
-// into a shared list, then emits them 32 at a time as emit does.
+// again from old and new, 512 elements per step, the whole chunk requested into L2 first.  A
+// chunk with version-1 blocks goes through emit_dense_plain; a compact chunk (at most
+// kCompactMax changes) first gathers its changes in position order into a shared list, then
+// emits them 32 at a time as emit does.
 // FUSED: after the fused compress, which leaves per-batch prefixes (batch_pre, batches of
 // bchunks chunks from batch_start) instead of the count scan's tile and chunk prefixes; if a
 // wait of the fused compress gave up (*abort), it emits nothing and fails every tensor.
@@ -956,16 +1102,17 @@ k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
     EmitCtx cx;
     emit_ctx(cx, payload, I, M, R, B, Pex, Rex, sm);
     if (compact) cx.listM = cx.listR = true;   // no bitmap
-    if (!cx.listM || !cx.listR) {
-      for (int i = lane; i < 256; i += 32) sm->bm[i] = 0;
-      __syncwarp();
-    }
     uint8_t* mout = payload + I.m_start;
     const uint64_t b_lo = (7 * Mex + 7) >> 3, b_hi = (7 * (Mex + M) + 7) >> 3;
-    uint64_t b_next = b_lo;
-    EmitState st{0, 0, 0, 0};
+    const uint64_t b_next = b_lo;
     const uint16_t* __restrict__ old = J.old;
     const uint16_t* __restrict__ neu = J.neu;
+    // the whole chunk of old and new requested from DRAM at once (16 KiB); the steps below
+    // then find it in L2 instead of waiting for one step's 2 KiB at a time
+    if (e0 + kChunk <= n) {
+      prefetch_chunk_l2(old + e0);
+      prefetch_chunk_l2(neu + e0);
+    }
     if (compact) {
       // the chunk's changes in position order (M + R <= kCompactMax of them)
       uint32_t base = 0;
@@ -1008,34 +1155,12 @@ k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
         }
       }
     }
-    for (int s = 0; s < 8 && !compact; s++) {
-      const uint32_t eloc = s * 512 + lane * 16;
-      const uint64_t e = e0 + eloc;
-      const uint4 n0 = load8(neu, e, n), n1 = load8(neu, e + 8, n);
-      const uint4 x0 = xor4(load8(old, e, n), n0);
-      const uint4 x1 = xor4(load8(old, e + 8, n), n1);
-      const uint32_t rare = rare_mask16(x0, x1);
-      // the value emitted: the XOR mask, or with overwrite the new value (the M stream keeps
-      // its mantissa bits)
-      const uint4 v0 = ow ? n0 : x0, v1 = ow ? n1 : x1;
-      emit_batch(eloc, nz_mask16(x0, x1) & ~rare, rare,
-                 [v0, v1](int b) { return elem_of(b < 8 ? v0 : v1, b & 7); }, st, cx);
-      __syncwarp();
-      const uint32_t known = min(st.rankM, M);  // values with rank < known are in the window
-      if (known > cx.wbase) {
-        // byte b is complete when floor(8b/7) + 1 <= Mex + known - 1
-        const uint64_t b_full = (7 * (Mex + known - 1) + 7) >> 3;
-        const uint64_t b_end = min(b_full, b_hi);
-        if (b_end > b_next) {
-          put_mant_bytes(mout, b_next, b_end, Mex, M, 0, cx);
-          b_next = b_end;
-        }
-        __syncwarp();
-        if (lane == 0) sm->mv[0] = sm->mv[known - 1 - cx.wbase];
-        __syncwarp();
-        cx.wbase = known - 1;
-      }
+    if (!compact) {
+      emit_dense_plain(old, neu, n, e0, B, M, R, Mex, cx, ow, mout, b_lo, b_hi, sm->bm, g,
+                       g_job_end, I.sum_m, counts, slots);
+      continue;
     }
+    // a compact chunk: the mantissa-stream bytes it owns, from its values in sm->mv
     __syncwarp();
     if (b_hi > b_next) {
       uint32_t after = 0;
@@ -1048,11 +1173,6 @@ k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
         after = next_mant_value<true>(g, g_job_end, cnt_next, aux_next, counts, slots);
       }
       put_mant_bytes(mout, b_next, b_hi, Mex, M, after, cx);
-    }
-    if (!cx.listM || !cx.listR) {
-      __syncwarp();
-      if (!cx.listM) store_bitmap(cx.mblk, sm->bm, B);
-      if (!cx.listR) store_bitmap(cx.rblk, sm->bm + 128, B);
     }
     __syncwarp();
   }
