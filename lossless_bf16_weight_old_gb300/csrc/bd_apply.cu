@@ -1243,17 +1243,6 @@ __device__ __forceinline__ uint32_t ld_u32_upto(const uint8_t* p, const uint8_t*
   return v;
 }
 
-// The 64 stream bits from bit `bit` of the byte stream s on (bit b = bit b%8 of byte b/8;
-// bits at or past `end` read as zero).
-__device__ __forceinline__ uint64_t bits64_at(const uint8_t* s, uint64_t bit, const uint8_t* end) {
-  const uint8_t* p = s + (bit >> 3);
-  const uint8_t* a = reinterpret_cast<const uint8_t*>(reinterpret_cast<uintptr_t>(p) & ~(uintptr_t)3);
-  const uint32_t sh = (uint32_t)((p - a) * 8 + (bit & 7));   // 0..31
-  const uint64_t lo = (uint64_t)ld_u32_upto(a, end) | ((uint64_t)ld_u32_upto(a + 4, end) << 32);
-  const uint64_t hi = ld_u32_upto(a + 8, end);
-  return sh ? (lo >> sh) | (hi << (64 - sh)) : lo;
-}
-
 // The value v repeated in each of nine 7-bit fields (bits 7f .. 7f+6, f = 0..8).
 constexpr uint64_t fields9(uint64_t v) {
   uint64_t r = 0;
@@ -1262,17 +1251,53 @@ constexpr uint64_t fields9(uint64_t v) {
 }
 constexpr uint64_t kField6 = fields9(0x3F), kField7 = fields9(0x40);
 
+// 8 BF16 values at the 16-byte aligned p (a plain load: p is written by this kernel).
+__device__ __forceinline__ uint4 ld_plain(const uint16_t* p) {
+  return *reinterpret_cast<const uint4*>(p);
+}
+// Checksum terms of a group of 8 values whose first word has key `key` (both words below n).
+__device__ __forceinline__ uint64_t hash_pair(uint4 v, uint64_t key) {
+  return mix64(((uint64_t)v.x | ((uint64_t)v.y << 32)) ^ key) +
+         mix64(((uint64_t)v.z | ((uint64_t)v.w << 32)) ^ (key + kGamma));
+}
+
 // Per-warp shared state of apply_bitmap: the chunk's two position blocks as bitmaps (a block
 // that is a bitmap in the payload is copied as the aligned words covering it, read from byte
 // offset `off`; a delta list is decoded into a bitmap at offset 0).
 struct BitmapSmem {
   uint32_t w[2][130];   // [0]: mantissa-only, [1]: rare
+  uint32_t mw[902];     // the chunk's M-stream bytes, as the aligned words covering them
 };
+
+// Copies the M-stream bits of a chunk's M values (7 bits each, stream bit 7*Mex on) into
+// sm->mw; returns the buffer bit of the chunk's first value bit.
+__device__ __forceinline__ uint32_t stage_mstream(BitmapSmem* sm, const uint8_t* mstream,
+                                                  uint64_t Mex, uint32_t M, const uint8_t* end) {
+  const int lane = threadIdx.x & 31;
+  const uint8_t* p = mstream + ((7 * Mex) >> 3);
+  const uint8_t* a = reinterpret_cast<const uint8_t*>(reinterpret_cast<uintptr_t>(p) & ~(uintptr_t)3);
+  const uint32_t first = (uint32_t)(p - a) * 8 + (uint32_t)((7 * Mex) & 7);
+  const uint32_t nw = (first + 7 * M + 31) / 32;   // <= 898
+  for (uint32_t i = lane; i < nw + 2; i += 32) sm->mw[i] = i < nw ? ld_u32_upto(a + 4 * i, end) : 0u;
+  return first;
+}
+
+// The 64 buffer bits from buffer bit `bit` on.
+__device__ __forceinline__ uint64_t mw_bits64(const BitmapSmem* sm, uint32_t bit) {
+  const uint32_t w = bit >> 5, sh = bit & 31;
+  const uint64_t lo = (uint64_t)sm->mw[w] | ((uint64_t)sm->mw[w + 1] << 32);
+  return sh ? (lo >> sh) | ((uint64_t)sm->mw[w + 2] << (64 - sh)) : lo;
+}
 
 // Byte q (0 <= q < 512) of the class-c bitmap; bytes past the chunk's B read as zero.
 __device__ __forceinline__ uint32_t bm_byte(const BitmapSmem* sm, int c, uint32_t off,
                                             uint32_t q, uint32_t B) {
   return q < B ? reinterpret_cast<const uint8_t*>(sm->w[c])[off + q] : 0u;
+}
+// The same for a full chunk (B = 512).
+__device__ __forceinline__ uint32_t bm_byte_full(const BitmapSmem* sm, int c, uint32_t off,
+                                                 uint32_t q) {
+  return reinterpret_cast<const uint8_t*>(sm->w[c])[off + q];
 }
 // Word i of the class-c bitmap (positions 32i .. 32i+31), bytes past B as zero.
 __device__ __forceinline__ uint32_t bm_word(const BitmapSmem* sm, int c, uint32_t off,
@@ -1317,6 +1342,85 @@ __device__ __forceinline__ uint32_t load_block(BitmapSmem* sm, int c, const uint
   return 0;
 }
 
+// The values of one 8-element group (XOR masks or overwrite targets) with class masks bm, br:
+// its mantissa-only values are the next popc(bm) of the M stream (from buffer bit `mbit`),
+// spread to bytes and permuted into their elements' places by the selectors of bm; its rare
+// values are the next popc(br) of the R stream from rank r.
+__device__ __forceinline__ uint4 group_values(const BitmapSmem* sm, const uint4* s_esel,
+                                              uint32_t bm, uint32_t br, uint32_t mbit,
+                                              const uint16_t* __restrict__ rstream, uint32_t r) {
+  uint4 m = make_uint4(0, 0, 0, 0);
+  if (bm) {
+    const uint64_t win = mw_bits64(sm, mbit);
+    const uint32_t a = unpack7x4((uint32_t)win), b = unpack7x4((uint32_t)(win >> 28));
+    const uint4 sel = s_esel[bm];
+    m = make_uint4(prmt(a, b, sel.x), prmt(a, b, sel.y), prmt(a, b, sel.z), prmt(a, b, sel.w));
+  }
+  if (br) {
+    for (uint32_t b = br; b; b &= b - 1, r++) {   // mostly a single rare change
+      const uint32_t i = __ffs(b) - 1;
+      const uint32_t v = (uint32_t)rstream[r] << (16 * (i & 1));
+      if (i < 2) m.x |= v;
+      else if (i < 4) m.y |= v;
+      else if (i < 6) m.z |= v;
+      else m.w |= v;
+    }
+  }
+  return m;
+}
+
+// The apply steps of one checked chunk (elements e0 .. e0 + 4095 of w, clipped at n): step s,
+// lane l takes group 32s + l; returns the checksum terms (INCR: new minus old terms of the
+// changed groups).  FULL: the whole chunk lies below n -- no bounds on loads, stores and terms,
+// and the checksum keys advance by a constant per step.
+template <bool FULL, bool INCR>
+__device__ __forceinline__ uint64_t bitmap_steps(const BitmapSmem* sm, const uint4* s_esel,
+                                                 uint16_t* __restrict__ w, uint64_t e0, uint64_t n,
+                                                 uint32_t offM, uint32_t offR, uint32_t B,
+                                                 uint32_t mbit0,
+                                                 const uint16_t* __restrict__ rstream, bool ow) {
+  const int lane = threadIdx.x & 31;
+  const uint64_t words = (n + 3) >> 2;
+  uint64_t ck = 0;
+  uint32_t rM = 0, rR = 0;   // ranks of the values before this step
+  uint32_t el = 8 * lane;    // chunk-local element of the lane's group
+  uint64_t key = (((e0 + el) >> 2) + 1) * kGamma;   // FULL: key of the group's first word
+  uint4 nxt = FULL ? ld_plain(w + el) : load8(w - e0, e0 + el, n);
+#pragma unroll 1
+  for (uint32_t s = 0; s < 16; s++, el += 256) {
+    const uint4 now = nxt;
+    if (s < 15) nxt = FULL ? ld_plain(w + el + 256) : load8(w - e0, e0 + el + 256, n);
+    const uint32_t q = 32 * s + lane;
+    const uint32_t bm = FULL ? bm_byte_full(sm, 0, offM, q) : bm_byte(sm, 0, offM, q, B);
+    const uint32_t br = FULL ? bm_byte_full(sm, 1, offR, q) : bm_byte(sm, 1, offR, q, B);
+    const uint32_t packed = __popc(bm) | (__popc(br) << 16);
+    const uint32_t incl = warp_incl_scan(packed), excl = incl - packed;
+    const uint32_t tot = __shfl_sync(kFull, incl, 31);
+    uint4 m = group_values(sm, s_esel, bm, br, mbit0 + 7 * (rM + (excl & 0xFFFFu)), rstream,
+                           rR + (excl >> 16));
+    rM += tot & 0xFFFFu;
+    rR += tot >> 16;
+    if (ow) m = overwrite_mask(m, now, bm, br);
+    const bool ch = (m.x | m.y | m.z | m.w) != 0;
+    const uint4 res = make_uint4(now.x ^ m.x, now.y ^ m.y, now.z ^ m.z, now.w ^ m.w);
+    const uint64_t e = e0 + el;
+    if (FULL) {
+      if (ch) *reinterpret_cast<uint4*>(w + el) = res;
+      if (!INCR) ck += hash_pair(res, key);
+      else if (ch) ck += hash_pair(res, key) - hash_pair(now, key);
+      key += 64 * kGamma;
+    } else {
+      if (ch && e < n) {
+        if (e + 8 <= n) *reinterpret_cast<uint4*>(w + el) = res;
+        else for (int i = 0; e + i < n; i++) w[el + i] = (uint16_t)elem_of(res, i);
+      }
+      if (!INCR) ck += group_hash(res, e >> 3, words);
+      else if (ch) ck += group_hash(res, e >> 3, words) - group_hash(now, e >> 3, words);
+    }
+  }
+  return ck;
+}
+
 // One warp per listed chunk (a chunk with at least one bitmap block; compact chunks never have
 // one), each warp taking every nwarps-th entry of the list.  The chunk is checked in full
 // first -- the blocks (list deltas, positions below L, bitmap counts equal to M and R, no bit at
@@ -1324,11 +1428,13 @@ __device__ __forceinline__ uint32_t load_block(BitmapSmem* sm, int c, const uint
 // mantissa mask, a rare mask with a sign or exponent bit) -- and left unwritten when
 // malformed.  Then 16 steps of 256 elements, lane l taking the 8-element group 32s + l: the
 // ranks of the group's first values come from one warp scan of the two classes' bit counts,
-// its mantissa-only values from one 64-bit window of the M stream, its rare values from the R
+// its mantissa-only values from one 64-bit window of the M stream (spread to bytes and put in
+// place by four byte permutes chosen by the group's class mask), its rare values from the R
 // stream; the group is XORed (an overwrite payload: its records written in place of the
 // fields), stored when it changed, and its checksum terms added (INCR: new minus old terms of
 // the changed groups).  The chunk is prefetched into L2 while its payload is checked, and
-// each step's group loads are issued one step ahead.
+// each step's group loads are issued one step ahead; the chunk's M-stream bytes are staged in
+// shared memory with its blocks.
 template <bool INCR>
 __global__ void __launch_bounds__(kThreads, 4)
 k_apply_bitmap(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
@@ -1337,10 +1443,15 @@ k_apply_bitmap(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
                const uint4* __restrict__ loc, const TileSum* __restrict__ tile_pre,
                JobInfo* __restrict__ info, uint8_t* __restrict__ ck_base) {
   __shared__ BitmapSmem s_bm[kWarps];
+  __shared__ uint4 s_esel[256];   // expand selectors by class mask
   const int lane = threadIdx.x & 31;
   BitmapSmem* sm = &s_bm[threadIdx.x >> 5];
   const uint64_t gwarp = ((uint64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
   const uint64_t nwarps = ((uint64_t)gridDim.x * kThreads) >> 5;
+  static_assert(kThreads == 256, "one selector entry per thread");
+  s_esel[threadIdx.x] = make_uint4(expand_sel(threadIdx.x, 0), expand_sel(threadIdx.x, 1),
+                                   expand_sel(threadIdx.x, 2), expand_sel(threadIdx.x, 3));
+  __syncthreads();
   const uint32_t listed = *list_count;
   uint32_t cur = kNone;
   uint64_t ck = 0;
@@ -1379,6 +1490,7 @@ k_apply_bitmap(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
     bool bad = cc.compact;   // (never listed)
     const uint32_t offM = load_block(sm, 0, mblk, M, B, L, listM, end, bad);
     const uint32_t offR = load_block(sm, 1, rblk, R, B, L, listR, end, bad);
+    const uint32_t mbit0 = stage_mstream(sm, mstream, Mex, M, end);
     __syncwarp();
     uint32_t cM = 0, cR = 0;
     for (uint32_t i = lane; 4 * i < B; i += 32) {
@@ -1396,7 +1508,7 @@ k_apply_bitmap(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
       // exactly when bit 6 of ((f & 0x3F) + 0x3F) | f is set (the add cannot carry out of it)
       for (uint32_t v0 = 9 * lane; v0 < M; v0 += 9 * 32) {
         const uint32_t nf = M - v0 < 9 ? M - v0 : 9;
-        const uint64_t x = bits64_at(mstream, 7 * (Mex + v0), end);
+        const uint64_t x = mw_bits64(sm, mbit0 + 7 * v0);
         const uint64_t keep = kField7 & ((1ull << (7 * nf)) - 1);
         if (((((x & kField6) + kField6) | x) & keep) != keep) bad = true;
       }
@@ -1410,53 +1522,10 @@ k_apply_bitmap(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
     }
 
     // ---- apply, 16 steps of 256 elements
-    const uint64_t words = (n + 3) >> 2;
-    uint32_t rM = 0, rR = 0;   // ranks of the values before this step
-    uint64_t ea = e0 + 8 * (uint64_t)lane;
-    uint4 nxt = load8(out, ea, n);
-#pragma unroll 1
-    for (uint32_t s = 0; s < 16; s++, ea += 256) {
-      const uint4 now = nxt;
-      if (s < 15) nxt = load8(out, ea + 256, n);
-      const uint32_t q = 32 * s + lane;
-      const uint32_t bm = bm_byte(sm, 0, offM, q, B), br = bm_byte(sm, 1, offR, q, B);
-      const uint32_t packed = __popc(bm) | (__popc(br) << 16);
-      const uint32_t incl = warp_incl_scan(packed), excl = incl - packed;
-      const uint32_t tot = __shfl_sync(kFull, incl, 31);
-      uint64_t t0 = 0, t1 = 0;   // the group's values (XOR masks or overwrite targets)
-      if (bm) {
-        uint64_t win = bits64_at(mstream, 7 * (Mex + rM + (excl & 0xFFFFu)), end);
-        for (uint32_t b = bm; b; b &= b - 1) {
-          const uint32_t i = __ffs(b) - 1;
-          const uint64_t v = (win & kMant) << (16 * (i & 3));
-          if (i < 4) t0 |= v; else t1 |= v;
-          win >>= 7;
-        }
-      }
-      if (br) {
-        uint32_t r = rR + (excl >> 16);
-        for (uint32_t b = br; b; b &= b - 1, r++) {
-          const uint32_t i = __ffs(b) - 1;
-          const uint64_t v = (uint64_t)rstream[r] << (16 * (i & 3));
-          if (i < 4) t0 |= v; else t1 |= v;
-        }
-      }
-      rM += tot & 0xFFFFu;
-      rR += tot >> 16;
-      uint4 m = make_uint4((uint32_t)t0, (uint32_t)(t0 >> 32), (uint32_t)t1, (uint32_t)(t1 >> 32));
-      if (ow) m = overwrite_mask(m, now, bm, br);
-      const bool ch = (m.x | m.y | m.z | m.w) != 0;
-      const uint4 res = make_uint4(now.x ^ m.x, now.y ^ m.y, now.z ^ m.z, now.w ^ m.w);
-      if (ch && ea < n) {
-        if (ea + 8 <= n) *reinterpret_cast<uint4*>(out + ea) = res;
-        else for (int i = 0; ea + i < n; i++) out[ea + i] = (uint16_t)elem_of(res, i);
-      }
-      if (INCR) {
-        if (ch) ck += group_hash(res, ea >> 3, words) - group_hash(now, ea >> 3, words);
-      } else {
-        ck += group_hash(res, ea >> 3, words);
-      }
-    }
+    if (e0 + kChunk <= n)
+      ck += bitmap_steps<true, INCR>(sm, s_esel, out + e0, e0, n, offM, offR, B, mbit0, rstream, ow);
+    else
+      ck += bitmap_steps<false, INCR>(sm, s_esel, out + e0, e0, n, offM, offR, B, mbit0, rstream, ow);
   }
   if (cur != kNone) flush_ck(ck_base, cur, gwarp, ck);
 }

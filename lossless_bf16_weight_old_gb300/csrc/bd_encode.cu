@@ -899,12 +899,14 @@ __device__ __forceinline__ void list_deltas(uint8_t* blk, uint32_t mask, uint32_
 // (lane l: elements 512s + 16l .. +15, the next step's loads in flight).  A bitmap block is
 // written straight from the lane's 16-bit class mask (two bytes per lane and step), a delta
 // list from the positions; rare values go to the R stream by rank.  The lane's mantissa-only
-// values are packed 7 bits each and ORed into a shared bit buffer at their stream offset
+// values (moved to the front of each 8-element half by byte permutes chosen by the half's
+// mask) are packed 7 bits each and ORed into a shared bit buffer at their stream offset
 // (buffer bit 0 = stream bit 8 * b_next); after each step the complete bytes are written to the
 // M stream and the buffer keeps the bits of the last, incomplete byte.  Only the bytes
 // [b_lo, b_hi) belong to the chunk: the bits of its first value that fall in byte b_lo - 1 are
 // the previous chunk's to write, and its last byte takes the low bits of the next mantissa
 // value of the tensor, `after`.
+template <bool FULL>
 __device__ __forceinline__ void emit_dense_plain(const uint16_t* __restrict__ old,
                                                  const uint16_t* __restrict__ neu, uint64_t n,
                                                  uint64_t e0, uint32_t B, uint32_t M, uint32_t R,
@@ -913,7 +915,8 @@ __device__ __forceinline__ void emit_dense_plain(const uint16_t* __restrict__ ol
                                                  uint64_t b_hi, uint32_t* __restrict__ sb,
                                                  uint64_t g, uint64_t g_job_end, uint64_t sum_m,
                                                  const uint32_t* __restrict__ counts,
-                                                 const uint8_t* __restrict__ slots) {
+                                                 const uint8_t* __restrict__ slots,
+                                                 const uint2* __restrict__ csel) {
   const int lane = threadIdx.x & 31;
   uint8_t* sbb = reinterpret_cast<uint8_t*>(sb);
   for (int i = lane; i < 256; i += 32) sb[i] = 0;
@@ -922,17 +925,21 @@ __device__ __forceinline__ void emit_dense_plain(const uint16_t* __restrict__ ol
   uint32_t rM = 0, rR = 0;
   int32_t lastM = 0, lastR = 0;
   uint64_t e = e0 + 16 * (uint64_t)lane;
-  uint4 o0 = load8(old, e, n), o1 = load8(old, e + 8, n);
-  uint4 n0 = load8(neu, e, n), n1 = load8(neu, e + 8, n);
+  // FULL: the chunk lies below n (no bounds on loads, every bitmap byte exists)
+  auto ld = [n](const uint16_t* p, uint64_t at) {
+    return FULL ? __ldg(reinterpret_cast<const uint4*>(p + at)) : load8(p, at, n);
+  };
+  uint4 o0 = ld(old, e), o1 = ld(old, e + 8);
+  uint4 n0 = ld(neu, e), n1 = ld(neu, e + 8);
 #pragma unroll 1
   for (uint32_t s = 0; s < 8; s++, e += 512) {
     const uint4 x0 = xor4(o0, n0), x1 = xor4(o1, n1);
     const uint4 w0 = ow ? n0 : x0, w1 = ow ? n1 : x1;   // the values written
     if (s < 7) {
-      o0 = load8(old, e + 512, n);
-      o1 = load8(old, e + 520, n);
-      n0 = load8(neu, e + 512, n);
-      n1 = load8(neu, e + 520, n);
+      o0 = ld(old, e + 512);
+      o1 = ld(old, e + 520);
+      n0 = ld(neu, e + 512);
+      n1 = ld(neu, e + 520);
     }
     const uint32_t rm = rare_mask16(x0, x1);
     const uint32_t mm = nz_mask16(x0, x1) & ~rm;
@@ -943,13 +950,13 @@ __device__ __forceinline__ void emit_dense_plain(const uint16_t* __restrict__ ol
     const uint32_t q = 64 * s + 2 * lane;   // the lane's first bitmap byte
     // positions
     if (!cx.listM) {
-      if (q + 1 < B) store_u16(cx.mblk + q, (uint16_t)mm);
+      if (FULL || q + 1 < B) store_u16(cx.mblk + q, (uint16_t)mm);
       else if (q < B) cx.mblk[q] = (uint8_t)mm;
     } else {
       list_deltas(cx.mblk, mm, p0, rM + (excl & 0xFFFFu), M, lastM);
     }
     if (!cx.listR) {
-      if (q + 1 < B) store_u16(cx.rblk + q, (uint16_t)rm);
+      if (FULL || q + 1 < B) store_u16(cx.rblk + q, (uint16_t)rm);
       else if (q < B) cx.rblk[q] = (uint8_t)rm;
     } else {
       list_deltas(cx.rblk, rm, p0, rR + (excl >> 16), R, lastR);
@@ -962,18 +969,21 @@ __device__ __forceinline__ void emit_dense_plain(const uint16_t* __restrict__ ol
         if (r < R) cx.rstream[r] = (uint16_t)elem_of(i < 8 ? w0 : w1, i & 7);
       }
     }
-    // mantissa-only values into the bit buffer
+    // mantissa-only values into the bit buffer: the 16 mantissas as bytes, the ones in mm
+    // moved to the front of each half by byte permutes chosen by its 8-bit mask, then packed
+    // 7 bits each
     if (mm) {
-      uint64_t lo = 0, hi = 0;
-      uint32_t kk = 0;
-      for (uint32_t b = mm; b; b &= b - 1, kk++) {
-        const int i = __ffs(b) - 1;
-        const uint64_t v = elem_of(i < 8 ? w0 : w1, i & 7) & kMant;
-        if (kk < 9) lo |= v << (7 * kk);
-        else hi |= v << (7 * (kk - 9));
-      }
-      // 128-bit value (a3:a2:a1:a0) of the lane's 7 * kk bits
-      uint64_t A = lo | (hi << 63), Bh = hi >> 1;
+      const uint32_t lo8 = mm & 0xFFu, hi8 = mm >> 8;
+      const uint32_t m0 = prmt(w0.x, w0.y, 0x6420u) & 0x7F7F7F7Fu;
+      const uint32_t m1 = prmt(w0.z, w0.w, 0x6420u) & 0x7F7F7F7Fu;
+      const uint32_t m2 = prmt(w1.x, w1.y, 0x6420u) & 0x7F7F7F7Fu;
+      const uint32_t m3 = prmt(w1.z, w1.w, 0x6420u) & 0x7F7F7F7Fu;
+      const uint2 sl = csel[lo8], sh8 = csel[hi8];
+      const uint64_t lo = pack7x4(prmt(m0, m1, sl.x)) | ((uint64_t)pack7x4(prmt(m0, m1, sl.y)) << 28);
+      const uint64_t hi = pack7x4(prmt(m2, m3, sh8.x)) | ((uint64_t)pack7x4(prmt(m2, m3, sh8.y)) << 28);
+      // 128-bit value (Bh:A) of the lane's 7 * popc(mm) bits
+      const uint32_t s0 = 7 * __popc(lo8);   // 0..56
+      uint64_t A = lo | (hi << s0), Bh = s0 ? hi >> (64 - s0) : 0;
       int64_t rel = (int64_t)(7 * (Mex + rM + (excl & 0xFFFFu))) - (int64_t)(8 * b_next);
       if (rel < 0) {   // the chunk's first value: its bits below byte b_lo are not ours
         const uint32_t d = (uint32_t)(-rel);
@@ -1031,7 +1041,7 @@ __device__ __forceinline__ void emit_dense_plain(const uint16_t* __restrict__ ol
 // bchunks chunks from batch_start) instead of the count scan's tile and chunk prefixes; if a
 // wait of the fused compress gave up (*abort), it emits nothing and fails every tensor.
 template <bool FUSED>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 3)
 k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
              const uint64_t* __restrict__ tile_start, uint32_t k,
              const uint32_t* __restrict__ list_count, const uint32_t* __restrict__ list,
@@ -1048,6 +1058,10 @@ k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
   }
   __shared__ EmitSmem s_em[kWarps];
   __shared__ uint32_t s_list[kWarps][kCompactMax];   // compact chunks: pos << 16 | x
+  __shared__ uint2 s_csel[256];                      // compress selectors by class mask
+  static_assert(kThreads == 256, "one selector entry per thread");
+  s_csel[threadIdx.x] = make_uint2(compress_sel(threadIdx.x, 0), compress_sel(threadIdx.x, 1));
+  __syncthreads();
   const int lane = threadIdx.x & 31;
   const uint64_t gwarp = ((uint64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
   const uint64_t nwarps = ((uint64_t)gridDim.x * kThreads) >> 5;
@@ -1156,8 +1170,12 @@ k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
       }
     }
     if (!compact) {
-      emit_dense_plain(old, neu, n, e0, B, M, R, Mex, cx, ow, mout, b_lo, b_hi, sm->bm, g,
-                       g_job_end, I.sum_m, counts, slots);
+      if (e0 + kChunk <= n)
+        emit_dense_plain<true>(old, neu, n, e0, B, M, R, Mex, cx, ow, mout, b_lo, b_hi, sm->bm,
+                               g, g_job_end, I.sum_m, counts, slots, s_csel);
+      else
+        emit_dense_plain<false>(old, neu, n, e0, B, M, R, Mex, cx, ow, mout, b_lo, b_hi, sm->bm,
+                                g, g_job_end, I.sum_m, counts, slots, s_csel);
       continue;
     }
     // a compact chunk: the mantissa-stream bytes it owns, from its values in sm->mv

@@ -232,6 +232,59 @@ __device__ __forceinline__ uint64_t group_hash(uint4 v, uint64_t q, uint64_t wor
   return h;
 }
 
+// ---------------------------------------------------------------------------- byte permutes
+// The dense kernels move a group's 7-bit mantissa values between their packed stream order and
+// their element positions with byte permutes driven by small tables indexed by the group's
+// 8-bit class mask, instead of a loop over the set bits.
+
+// PTX prmt in its default mode: byte n of the result is byte (s >> 4n) & 7 of the pair b:a;
+// when bit 3 of that selector nibble is set, the selected byte's top bit is replicated instead
+// (0x00 for a byte below 0x80, as every 7-bit value byte is).
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t s) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(s));
+  return d;
+}
+// The four 7-bit fields at bits 0..27 of v spread to bytes 0..3, and back.
+__device__ __forceinline__ uint32_t unpack7x4(uint32_t v) {
+  return (v & 0x7Fu) | ((v << 1) & 0x7F00u) | ((v << 2) & 0x7F0000u) | ((v << 3) & 0x7F000000u);
+}
+__device__ __forceinline__ uint32_t pack7x4(uint32_t v) {
+  return (v & 0x7Fu) | ((v >> 1) & 0x3F80u) | ((v >> 2) & 0x1FC000u) | ((v >> 3) & 0xFE00000u);
+}
+// Expand selectors of an 8-element group with class mask m: for word w (elements 2w, 2w+1),
+// the selector that takes, from the bytes of the group's values in stream order, the value
+// of element 2w into byte 0 and that of element 2w+1 into byte 2 (their ranks among the set
+// bits of m), and 0x00 into the other bytes and for elements not in m.
+__host__ __device__ __forceinline__ uint32_t expand_sel(uint32_t m, uint32_t w) {
+  uint32_t sel = 0x8080u;
+  for (uint32_t h = 0; h < 2; h++) {
+    const uint32_t e = 2 * w + h;
+    uint32_t nib = 8;
+    if ((m >> e) & 1u) {
+      nib = 0;
+      for (uint32_t i = 0; i < e; i++) nib += (m >> i) & 1u;
+    }
+    sel |= nib << (8 * h);
+  }
+  return sel;
+}
+// Compress selectors of an 8-element group with class mask m: for half h, the selector that
+// puts into byte k of the result (k = 0..3) the byte of the group's (4h + k)-th element in m,
+// and 0x00 past the last one.
+__host__ __device__ __forceinline__ uint32_t compress_sel(uint32_t m, uint32_t h) {
+  uint32_t sel = 0, k = 0;
+  for (uint32_t e = 0; e < 8; e++) {
+    if ((m >> e) & 1u) {
+      if (k >= 4 * h && k < 4 * h + 4) sel |= e << (4 * (k - 4 * h));
+      k++;
+    }
+  }
+  for (; k < 4 * h + 4; k++)
+    if (k >= 4 * h) sel |= 8u << (4 * (k - 4 * h));
+  return sel;
+}
+
 // Per-element class masks of the 8 XOR values in x (bit e <-> element e of the group).
 __device__ __forceinline__ void classify8(uint4 x, uint32_t& mmask, uint32_t& rmask) {
   mmask = 0;
