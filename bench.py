@@ -16,8 +16,8 @@ replicas, weak scaling).
 `--profile-case embed|layers|dense|formats` runs a fixed small program for an ncu capture
 instead (no timing, no JSON line), two rounds of: compress in each version, the full verified
 apply and the incremental apply of each payload.  `embed`: the 32000x4096 embedding tensor of
-dense7b in versions 1, 3 and 4 (the separate compress kernels), plus the standalone checksum and
-an out-of-place apply; `layers`: the 18 tensors of dense7b's first two layers in versions 1, 3
+dense7b in versions 1, 3 and 4 (the separate compress kernels), plus the standalone checksum, an
+out-of-place apply and the apply without a workspace; `layers`: the 18 tensors of dense7b's first two layers in versions 1, 3
 and 4 (the fused compress); `dense`: a 2^26-element tensor made by the 1 GiB workload's rule
 (22% changed: the dense emit and apply) in versions 1 and 3, plus the checksum and an
 out-of-place apply; `formats`: the whole --workload in versions 3 and 4.
@@ -402,6 +402,7 @@ def _host_mem_available() -> int:
 
 
 L2_FLUSH_BYTES = 256 << 20     # twice the GB300's L2
+E2E_GROUP_BYTES = 1 << 30      # old + new bytes per group of the e2e pipeline
 FLUSH_BELOW = 1 << 30          # flush L2 between timed runs when old + new are under 1 GiB
 
 
@@ -666,24 +667,60 @@ def run_ours(args) -> None:
         hN = torch.empty(N.shape, dtype=N.dtype, pin_memory=True)
         hO.copy_(O)
         hN.copy_(N)
-        hP = torch.empty(max(payload_bytes, 1), dtype=torch.uint8, pin_memory=True)
-        hS = torch.empty(len(specs) * 3, dtype=torch.int64, pin_memory=True)
+        # groups of consecutive tensors (about E2E_GROUP_BYTES of old + new each): group g's
+        # host-to-device copy runs on its own stream while group g-1 is compressed and applied,
+        # and its payloads come back on a third stream once it is done
+        groups, i0, acc = [], 0, 0
+        for i, n in enumerate(ns):
+            acc += 4 * n
+            if acc >= E2E_GROUP_BYTES or i == k - 1:
+                groups.append((i0, i + 1))
+                i0, acc = i + 1, 0
+        g_comp, g_dec, g_span, g_pay = [], [], [], []
+        hoff = 0
+        for (a0, a1) in groups:
+            c = bd.CompressBatch(olds[a0:a1], news[a0:a1], caps=sizes[a0:a1], workspace=ws_c)
+            g_comp.append(c)
+            g_dec.append({False: bd.DecompressBatch(rolls[a0:a1], c.payloads, sizes[a0:a1],
+                                                    ck_new[a0:a1], workspace=ws_d),
+                          True: bd.DecompressBatch(rolls[a0:a1], c.payloads, sizes[a0:a1],
+                                                   ck_old[a0:a1], workspace=ws_d)})
+            g_span.append((offs[a0], offs[a1 - 1] + ns[a1 - 1]))
+            pb = (c.payloads[-1].data_ptr() - c.payload_buf.data_ptr()) + sizes[a1 - 1]
+            g_pay.append((hoff, pb))
+            hoff += pb
+        hP = torch.empty(max(hoff, 1), dtype=torch.uint8, pin_memory=True)
+        hS = torch.empty(3 * k, dtype=torch.int64, pin_memory=True)
+        # old and new come in on two streams (two copy engines), payloads go out on a third
+        s_in = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
+        s_out = torch.cuda.Stream(device=dev)
+        ev_in = [[torch.cuda.Event() for _ in groups] for _ in s_in]
+        ev_done = [torch.cuda.Event() for _ in groups]
         torch.cuda.synchronize()
-        # payload bytes of every tensor, packed one after another in host memory
-        regions, hoff = [], 0
-        for p, sz in zip(comp.payloads, sizes):
-            regions.append((p, hoff, sz))
-            hoff += sz
 
         def e2e_step():
-            O.copy_(hO, non_blocking=True)
-            N.copy_(hN, non_blocking=True)
-            d = step(flush_l2=False)
-            for p, hoff, sz in regions:
-                hP[hoff:hoff + sz].copy_(p[:sz], non_blocking=True)
-            hS[:len(specs)].copy_(comp.sizes, non_blocking=True)
-            hS[len(specs):2 * len(specs)].copy_(comp.checksums, non_blocking=True)
-            hS[2 * len(specs):2 * len(specs) + 1].copy_(d.status.to(torch.int64), non_blocking=True)
+            for si in s_in:
+                si.wait_stream(stream)   # the previous step's compute has read old and new
+            for g, (a0, a1) in enumerate(groups):
+                lo, hi = g_span[g]
+                for si, ev, dst, src in zip(s_in, ev_in, (O, N), (hO, hN)):
+                    with torch.cuda.stream(si):
+                        dst[lo:hi].copy_(src[lo:hi], non_blocking=True)
+                        ev[g].record(si)
+                    stream.wait_event(ev[g])
+                g_comp[g].run(stream)
+                g_dec[g][state["new"]].run(stream)
+                ev_done[g].record(stream)
+                s_out.wait_event(ev_done[g])
+                with torch.cuda.stream(s_out):
+                    h0, pb = g_pay[g]
+                    hP[h0:h0 + pb].copy_(g_comp[g].payload_buf[:pb], non_blocking=True)
+                    hS[a0:a1].copy_(g_comp[g].sizes, non_blocking=True)
+                    hS[k + a0:k + a1].copy_(g_comp[g].checksums, non_blocking=True)
+                    hS[2 * k + a0:2 * k + a1].copy_(g_dec[g][state["new"]].statuses.to(torch.int64),
+                                                    non_blocking=True)
+            state["new"] = not state["new"]
+            stream.wait_stream(s_out)
 
         for _ in range(2):
             e2e_step()
@@ -697,13 +734,31 @@ def run_ours(args) -> None:
         e1.record(stream)
         torch.cuda.synchronize()
         e_ms = reduce_max(e0.elapsed_time(e1), world, dev) / e2e_steps
-        if int(hS[2 * len(specs)].item()) != bd.OK:
+        if any(int(v) != bd.OK for v in hS[2 * k:3 * k].tolist()):
             raise RuntimeError("e2e apply did not verify")
+        want = N if state["new"] else O
+        if not torch.equal(Rb.view(torch.int16), want.view(torch.int16)):
+            raise RuntimeError("e2e apply did not restore")
+        # the host link on its own in the same run: old and new copied in, both streams
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        p0.record(stream)
+        for si in s_in:
+            si.wait_stream(stream)
+        for si, dst, src in zip(s_in, (O, N), (hO, hN)):
+            with torch.cuda.stream(si):
+                dst.copy_(src, non_blocking=True)
+        for si in s_in:
+            stream.wait_stream(si)
+        p1.record(stream)
+        torch.cuda.synchronize()
+        h2d_gbs = 4 * n_total / (p0.elapsed_time(p1) * 1e-3) / 1e9
         e2e = {"value": round(world * raw / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                "ms_per_step": round(e_ms, 3), "steps": e2e_steps,
-               "h2d_bytes_per_step": 4 * n_total, "d2h_bytes_per_step":
-               payload_bytes + 8 * 2 * len(specs) + 8}
-        del hO, hN, hP
+               "h2d_alone_gbs": round(h2d_gbs, 1),
+               "h2d_bytes_per_step": 4 * n_total, "d2h_bytes_per_step": hoff + 8 * 3 * k,
+               "overlap": f"{len(groups)} groups of tensors: old and new in on two streams, "
+                          "compress + apply, payloads out on a third"}
+        del hO, hN, hP, g_comp, g_dec
 
     cpu = None
     if rank == 0:
@@ -871,6 +926,23 @@ def run_profile_case(args) -> None:
                     torch.equal(r.view(torch.int16), w.view(torch.int16))
                     for r, w in zip(outs, news))):
                 raise RuntimeError("profile case did not verify (checksum, out of place)")
+            # the entry point without a workspace (block-level decoder), out of place
+            if case == "embed":
+                lib = bd._lib.load()
+                st = torch.full((1,), -1, dtype=torch.int32, device=dev)
+                for o, p_, sz, ck, out in zip(olds, comp[1].payloads, sizes[1],
+                                             torch.split(ck_new, 1), outs):
+                    out.zero_()
+                    rc = lib.bd_decompress_noalloc(o.data_ptr(), o.numel(), p_.data_ptr(), sz,
+                                                   ck.data_ptr(), out.data_ptr(), st.data_ptr(),
+                                                   torch.cuda.current_stream().cuda_stream)
+                    if rc != bd.OK:
+                        raise RuntimeError(f"bd_decompress_noalloc returned {rc}")
+                torch.cuda.synchronize()
+                if int(st.item()) != bd.OK or not all(
+                        torch.equal(r.view(torch.int16), w.view(torch.int16))
+                        for r, w in zip(outs, news)):
+                    raise RuntimeError("profile case did not verify (no workspace)")
     print("profile case", case, "ok:",
           {v: sum(sizes[v]) for v in versions}, "payload bytes", flush=True)
 
