@@ -65,34 +65,37 @@ def _describe(name: str, specs: list[W.Spec]) -> str:
     return f"{name}: {len(specs)} BF16 tensors, {n:,} elements ({2 * n / 1e9:.2f} GB per checkpoint)"
 
 
-def _source_hash() -> str:
-    """Hash of the CUDA sources, to tell whether stored ncu counters still apply."""
+def _source_hash(files) -> str:
+    """Hash of the named CUDA sources, to tell whether stored ncu counters still apply."""
     import hashlib
     h = hashlib.sha256()
     d = os.path.join(ROOT, "lossless_bf16_weight_old_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
-        if f.endswith((".cu", ".cuh")):
-            h.update(f.encode())
-            with open(os.path.join(d, f), "rb") as fh:
-                h.update(fh.read())
+    for f in sorted(files):
+        h.update(f.encode())
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def _traffic(workload: str, phase: str):
-    """DRAM bytes (read + write) per call of `phase` from the committed ncu summary, or None
-    when there is none for this workload or the kernels changed since it was taken."""
+def _traffic(workload: str, phase: str, n_total: int):
+    """DRAM bytes (read + write) of one call of `phase` on this workload, from the committed
+    ncu capture of the same kernels on a smaller case of the same kind, scaled by elements
+    (profiles/dram_traffic.json); None when there is none for this workload or the kernels'
+    sources changed since it was taken."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
-            data = json.load(f)
+            entry = json.load(f).get("phases", {}).get(phase, {})
     except (OSError, ValueError):
         return None
-    if data.get("source_hash") != _source_hash():
+    if workload not in entry.get("scales_to", []):
         return None
-    entry = data.get("phases", {}).get(phase, {})
-    if entry.get("workload") != workload:
+    try:
+        if entry.get("source_hash") != _source_hash(entry["sources"]):
+            return None
+    except (OSError, KeyError):
         return None
-    return entry.get("dram_bytes_per_call")
+    return int(round(entry["bytes_per_element"] * n_total))
 
 
 # ------------------------------------------------------------------------ multi-rank helpers
@@ -651,7 +654,7 @@ def run_ours(args) -> None:
             "achieved": round(comp_ach if dom == "compress" else app_ach, 1),
             "peak": peak, "unit": "GB/s",
             "frac": round((comp_ach if dom == "compress" else app_ach) / peak, 4),
-            "traffic": _traffic(args.workload, dom), "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+            "traffic": _traffic(args.workload, dom, n_total), "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
             if peak_kind == "measured" else "fallback"}
 
     # e2e through the public API with host buffers: H2D old+new from pinned memory, compress,

@@ -839,6 +839,30 @@ __device__ __forceinline__ void prefetch_next_payload(const uint8_t* pos_next,
   else if (lane == 7) prefetch_l2_before(x_next, end);
 }
 
+// Listing a chunk for the bitmap kernel through a per-warp buffer of 32 entries in shared
+// memory: every 32 entries (and at the end) the warp reserves their places with one atomic
+// instead of one per chunk (all chunks of a call meet on the one counter).  Both are called by
+// the whole warp.
+__device__ __forceinline__ void list_flush(uint32_t* wbuf, uint32_t& nbuf,
+                                           uint32_t* __restrict__ list_count,
+                                           uint32_t* __restrict__ list) {
+  const int lane = threadIdx.x & 31;
+  if (nbuf == 0) return;
+  __syncwarp();
+  uint32_t base = 0;
+  if (lane == 0) base = atomicAdd(list_count, nbuf);
+  base = __shfl_sync(kFull, base, 0);
+  if ((uint32_t)lane < nbuf) list[base + lane] = wbuf[lane];
+  __syncwarp();
+  nbuf = 0;
+}
+__device__ __forceinline__ void list_append(uint32_t* wbuf, uint32_t& nbuf, uint64_t g,
+                                            uint32_t* __restrict__ list_count,
+                                            uint32_t* __restrict__ list) {
+  if ((threadIdx.x & 31) == 0) wbuf[nbuf] = (uint32_t)g;
+  if (++nbuf == 32) list_flush(wbuf, nbuf, list_count, list);
+}
+
 // Entry i of a u16 delta list.  Versions 1 and 2 place every list at an even offset; after an
 // odd-length compact block of version 3 one may start at an odd offset.
 template <bool V3>
@@ -869,12 +893,13 @@ k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
   __shared__ uint32_t s_ent[kWarps][kEntMax];       // pos << 16 | XOR value
   // mantissa-only positions (512 B); in the general build also a version-4 staging area
   __shared__ uint4 s_bits[kWarps][V3 ? kRiceWords / 4 : kChunk / 128];
+  __shared__ uint32_t s_lbuf[kWarps][32];   // chunks to list, not yet appended
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   uint32_t* ent = s_ent[w];
   uint32_t* bits = reinterpret_cast<uint32_t*>(s_bits[w]);
   const uint64_t gwarp = ((uint64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
   const uint64_t nwarps = ((uint64_t)gridDim.x * kThreads) >> 5;
-  uint32_t j = kNone, cur = kNone;
+  uint32_t j = kNone, cur = kNone, nbuf = 0;
   uint64_t ck = 0;
   uint64_t g_begin, g_end;
   warp_range(total_chunks, gwarp, nwarps, g_begin, g_end);
@@ -900,7 +925,7 @@ k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
         payload + count_table_offset(info[j].r_start, J.nchunks))[c], V3 ? I.version : 1u);
     const uint32_t M = cc.M, R = cc.R;
     if (!cc.compact && (2 * M >= B || 2 * R >= B)) {
-      if (lane == 0) list[atomicAdd(list_count, 1u)] = (uint32_t)g;
+      list_append(s_lbuf[w], nbuf, g, list_count, list);
       continue;
     }
     if (e0 + kChunk <= n) prefetch_chunk_l2(J.out + e0);   // in L2 by the time it is read
@@ -1025,6 +1050,7 @@ k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
     if (e0 + kChunk <= n) ck += hash_chunk<true>(J.out, n, e0);
     else ck += hash_chunk<false>(J.out, n, e0);
   }
+  list_flush(s_lbuf[w], nbuf, list_count, list);
   if (cur != kNone) flush_ck(ck_base, cur, gwarp, ck);
 }
 
@@ -1048,12 +1074,13 @@ k_apply_incr(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
   __shared__ uint32_t s_ent[kWarps][kEntMax];       // pos << 16 | XOR value
   // mantissa-only positions (512 B); in the general build also a version-4 staging area
   __shared__ uint4 s_bits[kWarps][V3 ? kRiceWords / 4 : kChunk / 128];
+  __shared__ uint32_t s_lbuf[kWarps][32];   // chunks to list, not yet appended
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   uint32_t* ent = s_ent[w];
   uint32_t* bits = reinterpret_cast<uint32_t*>(s_bits[w]);
   const uint64_t gwarp = ((uint64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
   const uint64_t nwarps = ((uint64_t)gridDim.x * kThreads) >> 5;
-  uint32_t j = kNone, cur = kNone;
+  uint32_t j = kNone, cur = kNone, nbuf = 0;
   uint64_t ck = 0;
   uint64_t g_begin, g_end;
   warp_range(total_chunks, gwarp, nwarps, g_begin, g_end);
@@ -1075,7 +1102,7 @@ k_apply_incr(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
         payload + count_table_offset(info[j].r_start, J.nchunks))[c], V3 ? I.version : 1u);
     const uint32_t M = cc.M, R = cc.R;
     if (!cc.compact && (2 * M >= B || 2 * R >= B)) {
-      if (lane == 0) list[atomicAdd(list_count, 1u)] = (uint32_t)g;
+      list_append(s_lbuf[w], nbuf, g, list_count, list);
       continue;
     }
     if (M + R == 0) continue;
@@ -1228,6 +1255,7 @@ k_apply_incr(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
     }
     __syncwarp();
   }
+  list_flush(s_lbuf[w], nbuf, list_count, list);
   if (cur != kNone) flush_ck(ck_base, cur, gwarp, ck);
 }
 
