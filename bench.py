@@ -772,9 +772,16 @@ def run_ours(args) -> None:
     # batch start arrays, each section 256-byte aligned
     blobs_c = -(-(128 * k + 3 * 8 * (k + 1) + 3 * 256) // 30720)
     blobs_d = -(-(128 * k + 2 * 8 * (k + 1) + 2 * 256) // 30720)
-    # compress: uploads + the fused compress + emit_dense; decompress: uploads + scan x2, both
-    # builds of apply_chunks (one returns at once), apply_dense, apply_finish
-    launches_per_step = (blobs_c + 2) + (blobs_d + 6)
+    # compress: uploads + the fused compress + emit_dense, or (a call with a tensor of more
+    # batches than the fused compress takes -- the library's choice restated: about four
+    # batches of up to 32 chunks per resident warp, at most 4096 batches per tensor) uploads +
+    # encode_slots, two scans, emit and emit_dense; decompress: uploads + scan x2, both builds of
+    # apply_chunks (one returns at once), apply_bitmap, apply_finish
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    chunks = [(n + 4095) // 4096 for n in ns]
+    bch = max(1, min(32, sum(chunks) // (sms * 32 * 4)))
+    fused = -(-max(chunks) // bch) <= 4096
+    launches_per_step = (blobs_c + (2 if fused else 5)) + (blobs_d + 6)
 
     def frac(nbytes, ms):
         return round(nbytes / (ms * 1e-3) / 1e9 / peak, 4)
