@@ -13,14 +13,16 @@ replicas, weak scaling).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload dense7b] [--impl reference]
 
-`--profile-case embed|layers|dense|formats` runs a fixed small program for an ncu capture
+`--profile-case embed|layers|moe|dense|formats` runs a fixed small program for an ncu capture
 instead (no timing, no JSON line), two rounds of: compress in each version, the full verified
 apply and the incremental apply of each payload.  `embed`: the 32000x4096 embedding tensor of
 dense7b in versions 1, 3 and 4 (the separate compress kernels), plus the standalone checksum, an
 out-of-place apply and the apply without a workspace; `layers`: the 18 tensors of dense7b's first two layers in versions 1, 3
 and 4 (the fused compress); `dense`: a 2^26-element tensor made by the 1 GiB workload's rule
 (22% changed: the dense emit and apply) in versions 1 and 3, plus the checksum and an
-out-of-place apply; `formats`: the whole --workload in versions 3 and 4.
+out-of-place apply; `moe`: the 389 tensors of moe30b's layer 0 (cold experts with 0.64% of
+their elements changed, 8 hot ones with 40%) in versions 1, 3 and 4; `formats`: the whole
+--workload in versions 3 and 4.
 """
 from __future__ import annotations
 
@@ -932,6 +934,9 @@ def run_profile_case(args) -> None:
     elif case == "layers":     # dense7b's first two layers: the fused compress
         specs = [s for s in W.dense7b() if s.name.startswith(("layers.0.", "layers.1."))]
         versions = (1, 3, 4)
+    elif case == "moe":        # moe30b's layer 0: sparse cold experts beside dense hot ones
+        specs = [s for s in W.moe30b() if s.name.startswith("layers.0.")]
+        versions = (1, 3, 4)
     elif case == "dense":      # a 2^26-element slice of the 1 GiB workload: the dense kernels
         specs = [W.Spec("w", (1 << 26,), kind="additive", tid=0)]
         versions = (1, 3)
@@ -1026,7 +1031,7 @@ def main(argv=None):
                    help="elements of the workload the CPU oracle baseline encodes+decodes")
     p.add_argument("--ref-sample-elems", type=int, default=400_000_000,
                    help="elements per step of the --impl reference arm")
-    p.add_argument("--profile-case", choices=["embed", "layers", "dense", "formats"],
+    p.add_argument("--profile-case", choices=["embed", "layers", "moe", "dense", "formats"],
                    default=None,
                    help="run a fixed small program for an ncu capture instead of the bench")
     args = p.parse_args(argv)

@@ -79,6 +79,8 @@ WsLayout make_layout(uint32_t k, const Sizes& s, bool compress) {
   off = up(off + s.tiles * sizeof(TileSum), kAlign);
   L.ovf_list = off;  // chunks too dense for a slot / for the thread-level apply
   off = up(off + s.chunks * 4, kAlign);
+  L.ovf_job = off;   // their tensors
+  off = up(off + s.chunks * 4, kAlign);
   if (compress) {
     L.slots = off;
     off = up(off + s.chunks * kSlotBytes, kAlign);
@@ -103,8 +105,12 @@ struct Blob {
   uint4 data[kBlobWords];
 };
 
+// One 16-byte word per thread, spread over several blocks: the words of the parameter blob
+// differ from thread to thread and the constant cache serves one address at a time, so a
+// single block looping over a 30 KiB blob took about 8 µs per launch.
 __global__ void k_put(const __grid_constant__ Blob b, uint4* __restrict__ dst) {
-  for (uint32_t i = threadIdx.x; i < b.words; i += blockDim.x) dst[i] = b.data[i];
+  const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < b.words) dst[i] = b.data[i];
 }
 
 cudaError_t upload(const std::vector<uint8_t>& host, uint8_t* dst, cudaStream_t s) {
@@ -115,7 +121,7 @@ cudaError_t upload(const std::vector<uint8_t>& host, uint8_t* dst, cudaStream_t 
     const uint32_t cnt = (uint32_t)((words - w0) < kBlobWords ? (words - w0) : kBlobWords);
     b->words = cnt;
     std::memcpy(b->data, host.data() + w0 * 16, (size_t)cnt * 16);
-    k_put<<<1, 256, 0, s>>>(*b, reinterpret_cast<uint4*>(dst) + w0);
+    k_put<<<(cnt + 127) / 128, 128, 0, s>>>(*b, reinterpret_cast<uint4*>(dst) + w0);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

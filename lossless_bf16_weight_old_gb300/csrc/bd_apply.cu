@@ -841,26 +841,34 @@ __device__ __forceinline__ void prefetch_next_payload(const uint8_t* pos_next,
 
 // Listing a chunk for the bitmap kernel through a per-warp buffer of 32 entries in shared
 // memory: every 32 entries (and at the end) the warp reserves their places with one atomic
-// instead of one per chunk (all chunks of a call meet on the one counter).  Both are called by
+// instead of one per chunk (all chunks of a call meet on the one counter).  Entry i is the
+// chunk's global index in list[i] and its tensor in list_job[i], so that the bitmap kernel,
+// whose warps take scattered entries, needs no search of the tensor table.  Both are called by
 // the whole warp.
-__device__ __forceinline__ void list_flush(uint32_t* wbuf, uint32_t& nbuf,
+__device__ __forceinline__ void list_flush(uint2* wbuf, uint32_t& nbuf,
                                            uint32_t* __restrict__ list_count,
-                                           uint32_t* __restrict__ list) {
+                                           uint32_t* __restrict__ list,
+                                           uint32_t* __restrict__ list_job) {
   const int lane = threadIdx.x & 31;
   if (nbuf == 0) return;
   __syncwarp();
   uint32_t base = 0;
   if (lane == 0) base = atomicAdd(list_count, nbuf);
   base = __shfl_sync(kFull, base, 0);
-  if ((uint32_t)lane < nbuf) list[base + lane] = wbuf[lane];
+  if ((uint32_t)lane < nbuf) {
+    const uint2 e = wbuf[lane];
+    list[base + lane] = e.x;
+    list_job[base + lane] = e.y;
+  }
   __syncwarp();
   nbuf = 0;
 }
-__device__ __forceinline__ void list_append(uint32_t* wbuf, uint32_t& nbuf, uint64_t g,
+__device__ __forceinline__ void list_append(uint2* wbuf, uint32_t& nbuf, uint64_t g, uint32_t j,
                                             uint32_t* __restrict__ list_count,
-                                            uint32_t* __restrict__ list) {
-  if ((threadIdx.x & 31) == 0) wbuf[nbuf] = (uint32_t)g;
-  if (++nbuf == 32) list_flush(wbuf, nbuf, list_count, list);
+                                            uint32_t* __restrict__ list,
+                                            uint32_t* __restrict__ list_job) {
+  if ((threadIdx.x & 31) == 0) wbuf[nbuf] = make_uint2((uint32_t)g, j);
+  if (++nbuf == 32) list_flush(wbuf, nbuf, list_count, list, list_job);
 }
 
 // Entry i of a u16 delta list.  Versions 1 and 2 place every list at an even offset; after an
@@ -888,12 +896,13 @@ k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
                const uint64_t* __restrict__ tile_start, uint32_t k, uint64_t total_chunks,
                const uint4* __restrict__ loc, const TileSum* __restrict__ tile_pre,
                JobInfo* __restrict__ info, uint32_t* __restrict__ list_count,
-               uint32_t* __restrict__ list, uint8_t* __restrict__ ck_base) {
+               uint32_t* __restrict__ list, uint32_t* __restrict__ list_job,
+               uint8_t* __restrict__ ck_base) {
   if ((list_count[kFlagV3Word] != 0) != V3) return;   // the other build runs this call
   __shared__ uint32_t s_ent[kWarps][kEntMax];       // pos << 16 | XOR value
   // mantissa-only positions (512 B); in the general build also a version-4 staging area
   __shared__ uint4 s_bits[kWarps][V3 ? kRiceWords / 4 : kChunk / 128];
-  __shared__ uint32_t s_lbuf[kWarps][32];   // chunks to list, not yet appended
+  __shared__ uint2 s_lbuf[kWarps][32];   // chunks to list (index, tensor), not yet appended
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   uint32_t* ent = s_ent[w];
   uint32_t* bits = reinterpret_cast<uint32_t*>(s_bits[w]);
@@ -925,7 +934,7 @@ k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
         payload + count_table_offset(info[j].r_start, J.nchunks))[c], V3 ? I.version : 1u);
     const uint32_t M = cc.M, R = cc.R;
     if (!cc.compact && (2 * M >= B || 2 * R >= B)) {
-      list_append(s_lbuf[w], nbuf, g, list_count, list);
+      list_append(s_lbuf[w], nbuf, g, j, list_count, list, list_job);
       continue;
     }
     if (e0 + kChunk <= n) prefetch_chunk_l2(J.out + e0);   // in L2 by the time it is read
@@ -1050,7 +1059,7 @@ k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
     if (e0 + kChunk <= n) ck += hash_chunk<true>(J.out, n, e0);
     else ck += hash_chunk<false>(J.out, n, e0);
   }
-  list_flush(s_lbuf[w], nbuf, list_count, list);
+  list_flush(s_lbuf[w], nbuf, list_count, list, list_job);
   if (cur != kNone) flush_ck(ck_base, cur, gwarp, ck);
 }
 
@@ -1068,13 +1077,14 @@ k_apply_incr(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
              const uint64_t* __restrict__ tile_start, uint32_t k, uint64_t total_chunks,
              const uint4* __restrict__ loc, const TileSum* __restrict__ tile_pre,
              JobInfo* __restrict__ info, uint32_t* __restrict__ list_count,
-             uint32_t* __restrict__ list, uint8_t* __restrict__ ck_base) {
+             uint32_t* __restrict__ list, uint32_t* __restrict__ list_job,
+             uint8_t* __restrict__ ck_base) {
   // another build runs this call
   if ((list_count[kFlagV3Word] != 0) != V3 || (list_count[kFlagOwWord] != 0) != OW) return;
   __shared__ uint32_t s_ent[kWarps][kEntMax];       // pos << 16 | XOR value
   // mantissa-only positions (512 B); in the general build also a version-4 staging area
   __shared__ uint4 s_bits[kWarps][V3 ? kRiceWords / 4 : kChunk / 128];
-  __shared__ uint32_t s_lbuf[kWarps][32];   // chunks to list, not yet appended
+  __shared__ uint2 s_lbuf[kWarps][32];   // chunks to list (index, tensor), not yet appended
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   uint32_t* ent = s_ent[w];
   uint32_t* bits = reinterpret_cast<uint32_t*>(s_bits[w]);
@@ -1102,7 +1112,7 @@ k_apply_incr(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
         payload + count_table_offset(info[j].r_start, J.nchunks))[c], V3 ? I.version : 1u);
     const uint32_t M = cc.M, R = cc.R;
     if (!cc.compact && (2 * M >= B || 2 * R >= B)) {
-      list_append(s_lbuf[w], nbuf, g, list_count, list);
+      list_append(s_lbuf[w], nbuf, g, j, list_count, list, list_job);
       continue;
     }
     if (M + R == 0) continue;
@@ -1255,7 +1265,7 @@ k_apply_incr(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
     }
     __syncwarp();
   }
-  list_flush(s_lbuf[w], nbuf, list_count, list);
+  list_flush(s_lbuf[w], nbuf, list_count, list, list_job);
   if (cur != kNone) flush_ck(ck_base, cur, gwarp, ck);
 }
 
@@ -1468,8 +1478,9 @@ __global__ void __launch_bounds__(kThreads, 4)
 k_apply_bitmap(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
                const uint64_t* __restrict__ tile_start, uint32_t k,
                const uint32_t* __restrict__ list_count, const uint32_t* __restrict__ list,
-               const uint4* __restrict__ loc, const TileSum* __restrict__ tile_pre,
-               JobInfo* __restrict__ info, uint8_t* __restrict__ ck_base) {
+               const uint32_t* __restrict__ list_job, const uint4* __restrict__ loc,
+               const TileSum* __restrict__ tile_pre, JobInfo* __restrict__ info,
+               uint8_t* __restrict__ ck_base) {
   __shared__ BitmapSmem s_bm[kWarps];
   __shared__ uint4 s_esel[256];   // expand selectors by class mask
   const int lane = threadIdx.x & 31;
@@ -1485,7 +1496,7 @@ k_apply_bitmap(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
   uint64_t ck = 0;
   for (uint64_t li = gwarp; li < listed; li += nwarps) {
     const uint64_t g = list[li];
-    const uint32_t j = find_job(chunk_start, k, g);
+    const uint32_t j = list_job[li];
     const JobInfo& I = info[j];
     if (I.status != BD_OK) continue;
     if (j != cur) {
@@ -1635,7 +1646,8 @@ cudaError_t launch_both(const LaunchCtx& c, K k12, int per_sm12, K k3, int per_s
         reinterpret_cast<const TileSum*>(c.ws + c.lay.tile_pre),
         reinterpret_cast<JobInfo*>(c.ws + c.lay.info),
         reinterpret_cast<uint32_t*>(c.ws + c.lay.overflow),
-        reinterpret_cast<uint32_t*>(c.ws + c.lay.ovf_list), c.ws + c.lay.ck);
+        reinterpret_cast<uint32_t*>(c.ws + c.lay.ovf_list),
+        reinterpret_cast<uint32_t*>(c.ws + c.lay.ovf_job), c.ws + c.lay.ck);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -1701,6 +1713,7 @@ cudaError_t launch_apply_bitmap(const LaunchCtx& c, bool incremental) {
       reinterpret_cast<const uint64_t*>(c.ws + c.lay.tile_start), c.k,
       reinterpret_cast<const uint32_t*>(c.ws + c.lay.overflow),
       reinterpret_cast<const uint32_t*>(c.ws + c.lay.ovf_list),
+      reinterpret_cast<const uint32_t*>(c.ws + c.lay.ovf_job),
       reinterpret_cast<const uint4*>(c.ws + c.lay.loc),
       reinterpret_cast<const TileSum*>(c.ws + c.lay.tile_pre),
       reinterpret_cast<JobInfo*>(c.ws + c.lay.info), c.ws + c.lay.ck);

@@ -219,6 +219,7 @@ __device__ __forceinline__ uint32_t encode_chunk(const uint16_t* __restrict__ ol
                                              uint32_t* __restrict__ counts,
                                              uint32_t* __restrict__ list_count,
                                              uint32_t* __restrict__ list,
+                                             uint32_t* __restrict__ list_job, uint32_t j,
                                              uint4* __restrict__ xs, uint4* __restrict__ ns) {
   const int lane = threadIdx.x & 31;
   const uint16_t* xs16 = reinterpret_cast<const uint16_t*>(xs);
@@ -325,7 +326,11 @@ __device__ __forceinline__ uint32_t encode_chunk(const uint16_t* __restrict__ ol
     slot[0] = overflow ? kSlotOverflow : slot_info(runM, runR);
     slot[1] = fm;
     counts[g] = word;
-    if (overflow) list[atomicAdd(list_count, 1u)] = (uint32_t)g;
+    if (overflow) {   // listed for emit_dense, with its tensor
+      const uint32_t at = atomicAdd(list_count, 1u);
+      list[at] = (uint32_t)g;
+      list_job[at] = j;
+    }
   }
   return word;   // the same on every lane
 }
@@ -335,7 +340,8 @@ __global__ void __launch_bounds__(kThreads, 4)
 k_encode_slots(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
                uint32_t k, uint64_t total_chunks, uint32_t* __restrict__ counts,
                uint8_t* __restrict__ slots, uint8_t* __restrict__ ck_base,
-               uint32_t* __restrict__ list_count, uint32_t* __restrict__ list) {
+               uint32_t* __restrict__ list_count, uint32_t* __restrict__ list,
+               uint32_t* __restrict__ list_job) {
   __shared__ uint4 s_xs[kThreads][2];   // per thread: the 16 XOR values of its current step
   __shared__ uint4 s_ns[OW ? kThreads : 1][2];   // OW: its 16 new values
   const int lane = threadIdx.x & 31;
@@ -366,10 +372,10 @@ k_encode_slots(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk
     uint4* ns = s_ns[OW ? threadIdx.x : 0];
     if (e0 + kChunk <= n)
       encode_chunk<true, FMT, OW>(jobs[j].old, jobs[j].neu, n, e0, slot, ck, g, counts,
-                                  list_count, list, s_xs[threadIdx.x], ns);
+                                  list_count, list, list_job, j, s_xs[threadIdx.x], ns);
     else
       encode_chunk<false, FMT, OW>(jobs[j].old, jobs[j].neu, n, e0, slot, ck, g, counts,
-                                   list_count, list, s_xs[threadIdx.x], ns);
+                                   list_count, list, list_job, j, s_xs[threadIdx.x], ns);
   }
   if (cur != 0xFFFFFFFFu) {
     const uint64_t s = warp_sum64(ck);
@@ -1045,6 +1051,7 @@ __global__ void __launch_bounds__(kThreads, 3)
 k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,
              const uint64_t* __restrict__ tile_start, uint32_t k,
              const uint32_t* __restrict__ list_count, const uint32_t* __restrict__ list,
+             const uint32_t* __restrict__ list_job,
              const uint32_t* __restrict__ counts, const uint8_t* __restrict__ slots,
              const uint4* __restrict__ loc, const TileSum* __restrict__ tile_pre,
              const JobInfo* __restrict__ info, const uint64_t* __restrict__ batch_start,
@@ -1070,7 +1077,7 @@ k_emit_dense(const CJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_s
   const uint32_t listed = *list_count;
   for (uint64_t li = gwarp; li < listed; li += nwarps) {
     const uint64_t g = list[li];
-    const uint32_t j = find_job(chunk_start, k, g);
+    const uint32_t j = list_job[li];
     const JobInfo I = info[j];
     if (I.status != BD_OK) continue;
     const CJob& J = jobs[j];
@@ -1227,6 +1234,7 @@ struct FusedArgs {
   uint8_t* ck_base;
   uint32_t* list_count;
   uint32_t* list;
+  uint32_t* list_job;
   uint4* batch_tot;
   TileSum* batch_pre;
   JobInfo* info;
@@ -1331,10 +1339,10 @@ __device__ __forceinline__ void fused_encode(const FusedArgs& a, uint32_t b, uin
       prefetch_chunk_l2(J.old + e0);
       prefetch_chunk_l2(J.neu + e0);
       word = encode_chunk<true, FMT, OW>(J.old, J.neu, n, e0, slot, ck, g, a.counts,
-                                         a.list_count, a.list, xs, ns);
+                                         a.list_count, a.list, a.list_job, j, xs, ns);
     } else {
       word = encode_chunk<false, FMT, OW>(J.old, J.neu, n, e0, slot, ck, g, a.counts,
-                                          a.list_count, a.list, xs, ns);
+                                          a.list_count, a.list, a.list_job, j, xs, ns);
     }
     const uint32_t L = (n - e0) < kChunk ? (uint32_t)(n - e0) : kChunk;
     if constexpr (FMT == 0) {
@@ -1510,7 +1518,8 @@ cudaError_t launch_encode_slots(const LaunchCtx& c, uint32_t fmt, bool overwrite
       reinterpret_cast<const uint64_t*>(c.ws + c.lay.chunk_start), c.k, c.chunks,
       reinterpret_cast<uint32_t*>(c.ws + c.lay.counts), c.ws + c.lay.slots, c.ws + c.lay.ck,
       reinterpret_cast<uint32_t*>(c.ws + c.lay.overflow),
-      reinterpret_cast<uint32_t*>(c.ws + c.lay.ovf_list));
+      reinterpret_cast<uint32_t*>(c.ws + c.lay.ovf_list),
+      reinterpret_cast<uint32_t*>(c.ws + c.lay.ovf_job));
   return cudaGetLastError();
 }
 
@@ -1524,6 +1533,7 @@ cudaError_t launch_emit_dense(const LaunchCtx& c, bool fused) {
       reinterpret_cast<const uint64_t*>(c.ws + c.lay.tile_start), c.k,
       reinterpret_cast<const uint32_t*>(c.ws + c.lay.overflow),
       reinterpret_cast<const uint32_t*>(c.ws + c.lay.ovf_list),
+      reinterpret_cast<const uint32_t*>(c.ws + c.lay.ovf_job),
       reinterpret_cast<const uint32_t*>(c.ws + c.lay.counts), c.ws + c.lay.slots,
       reinterpret_cast<const uint4*>(c.ws + c.lay.loc),
       reinterpret_cast<const TileSum*>(c.ws + c.lay.tile_pre),
@@ -1558,6 +1568,7 @@ cudaError_t launch_compress_fused(const LaunchCtx& c, uint32_t fmt, bool overwri
   a.ck_base = c.ws + c.lay.ck;
   a.list_count = reinterpret_cast<uint32_t*>(c.ws + c.lay.overflow);
   a.list = reinterpret_cast<uint32_t*>(c.ws + c.lay.ovf_list);
+  a.list_job = reinterpret_cast<uint32_t*>(c.ws + c.lay.ovf_job);
   a.batch_tot = reinterpret_cast<uint4*>(c.ws + c.lay.batch_tot);
   a.batch_pre = reinterpret_cast<TileSum*>(c.ws + c.lay.batch_pre);
   a.info = reinterpret_cast<JobInfo*>(c.ws + c.lay.info);

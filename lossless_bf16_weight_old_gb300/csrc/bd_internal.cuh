@@ -526,6 +526,8 @@ struct WsLayout {
   uint64_t overflow;     // decompress: u32 words in the zeroed state -- the count of listed
                          // chunks, then kFlagV3Word ...
   uint64_t ovf_list;     // ... and Ctot u32 chunk indices handled by the block-level apply
+  uint64_t ovf_job;      // Ctot u32: the tensor of each listed chunk (not in the no-workspace
+                         // layout, whose one tensor needs none)
   uint64_t fused_ctl;    // compress: fused-compress control words (zeroed state)
   uint64_t batch_start;  // compress: (k+1) u64, global index of tensor j's first batch
   uint64_t batch_tot;    // compress: per batch uint4 (position bytes, M, R, 0)
