@@ -242,6 +242,31 @@ BD_API int bd_decompress(const uint16_t* d_old, uint64_t n, const void* d_payloa
 BD_API int bd_decompress_batch(const bd_decompress_item* h_items, uint32_t k, void* d_ws,
                         uint64_t ws_bytes, int32_t* d_status, void* stream);
 
+/* bd_decompress_batch with every payload in HOST memory, streamed through two device slots:
+ * the SM-only analog of the double-buffered pipeline of [WT], section "Double compression with
+ * heterogeneous decompression" (payloads staged in pinned host RAM; one of two layer-sized
+ * buffers is filled while the GPU applies from the other, so no device copy of the whole
+ * update is needed).  Here the copy engines fill a slot instead of the decompression engine.
+ * The items are cut, in order, into groups whose payloads (each placed at a 256-byte
+ * boundary) fit in slot_bytes; group g's payloads are copied into slot g % 2 of d_staging on
+ * copy_stream while group g - 1 is applied on stream, and a slot is refilled only after the
+ * apply that read it.  Each item's d_payload is a HOST address (page-locked memory, e.g.
+ * cudaHostAlloc, for the copies to overlap; pageable memory works but each copy may block the
+ * host); it must stay valid and unchanged until stream has passed the call.
+ * d_staging: device, 256-byte aligned, 2 * slot_bytes bytes, slot_bytes a multiple of 256
+ * and at least the largest payload rounded up to 256; it may not overlap any output or the
+ * workspace.  copy_stream: a stream other than stream (use non-blocking streams: the legacy
+ * default stream would serialise the copies with the applies).  The workspace is
+ * bd_decompress_workspace_size of all k tensors.  Results, per-tensor statuses and *d_status
+ * (required; the largest status over all tensors) are those of bd_decompress_batch on the
+ * same items with device payloads.  Every argument is checked before anything is enqueued:
+ * BD_ERR_INVALID_ARG otherwise (also for a payload larger than a slot); BD_ERR_CUDA when the
+ * runtime refuses an event, copy or launch, with earlier groups possibly enqueued. */
+BD_API int bd_decompress_batch_streamed(const bd_decompress_item* h_items, uint32_t k,
+                                        void* d_staging, uint64_t slot_bytes, void* d_ws,
+                                        uint64_t ws_bytes, int32_t* d_status, void* stream,
+                                        void* copy_stream);
+
 /* In-place apply verified incrementally.  Not on the pages, which verify by checksumming the
  * restored weights: a rollout process that applies updates one after another already holds
  * a verified checksum of its current weights (the expected checksum of its previous update),

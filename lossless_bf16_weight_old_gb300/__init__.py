@@ -30,7 +30,7 @@ __all__ = [
     "delta_compress", "delta_decompress", "compress", "decompress", "compress_batch",
     "decompress_batch", "decompress_incremental", "IncrementalBatch", "checksum",
     "compress_bound", "compress_workspace_size", "decompress_workspace_size", "payload_info",
-    "DeltaError", "status_name", "MappedHostBuffer",
+    "DeltaError", "status_name", "MappedHostBuffer", "StreamedDecompressBatch",
 ]
 
 
@@ -117,6 +117,7 @@ class MappedHostBuffer:
             self._host = None
             raise RuntimeError(f"cudaHostGetDevicePointer failed ({rc})")
         self.device_ptr = int(dev.value)
+        self.host_ptr = int(self._host.value)
 
     def numpy(self):
         import numpy as np
@@ -393,6 +394,54 @@ class DecompressBatch:
                                              self.workspace.numel(), self.status.data_ptr(),
                                              _stream(stream))
         _check(rc, "bd_decompress_batch")
+
+
+class StreamedDecompressBatch:
+    """Item table of one bd_decompress_batch_streamed call: the payloads lie in page-locked
+    host memory (a MappedHostBuffer, or a pinned CPU uint8 tensor) at byte offsets `offsets`,
+    and are copied through two device slots of `slot_bytes` each while the previous slot's
+    tensors are applied."""
+
+    def __init__(self, olds: Sequence[torch.Tensor], host_payloads, offsets: Sequence[int],
+                 sizes: Sequence[int], expected: torch.Tensor, slot_bytes: int | None = None,
+                 outs: Sequence[torch.Tensor] | None = None,
+                 workspace: torch.Tensor | None = None):
+        k = len(olds)
+        dev = olds[0].device
+        outs = list(outs) if outs is not None else list(olds)
+        ns = [o.numel() for o in olds]
+        if isinstance(host_payloads, MappedHostBuffer):
+            host = host_payloads.host_ptr
+        elif isinstance(host_payloads, torch.Tensor) and not host_payloads.is_cuda:
+            host = host_payloads.data_ptr()
+        else:
+            raise ValueError("host_payloads must be a MappedHostBuffer or a CPU tensor")
+        largest = max([(int(z) + 255) // 256 * 256 for z in sizes] + [256])
+        self.slot_bytes = int(slot_bytes) if slot_bytes is not None else max(64 << 20, largest)
+        self.staging = torch.empty(2 * self.slot_bytes, dtype=torch.uint8, device=dev)
+        self.statuses = torch.zeros(k, dtype=torch.int32, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.workspace = _workspace(decompress_workspace_size(ns), dev, workspace)
+        self.copy_stream = torch.cuda.Stream(device=dev)
+        items = (_lib.DecompressItem * max(1, k))()
+        for i in range(k):
+            items[i].d_old = _bits(olds[i], "old")[0]
+            items[i].d_out = _bits(outs[i], "out")[0]
+            items[i].n = ns[i]
+            items[i].d_payload = host + int(offsets[i])
+            items[i].size = int(sizes[i])
+            items[i].d_expected = expected.data_ptr() + 8 * i
+            items[i].d_status = self.statuses.data_ptr() + 4 * i
+        self._keep = (list(olds), host_payloads, outs, expected)
+        self.items, self.k = items, k
+
+    def run(self, stream=None, copy_stream=None) -> None:
+        cs = copy_stream if copy_stream is not None else self.copy_stream
+        rc = _lib.load().bd_decompress_batch_streamed(
+            self.items, self.k, self.staging.data_ptr(), self.slot_bytes,
+            self.workspace.data_ptr(), self.workspace.numel(), self.status.data_ptr(),
+            _stream(stream), _stream(cs))
+        _check(rc, "bd_decompress_batch_streamed")
 
 
 class IncrementalBatch:

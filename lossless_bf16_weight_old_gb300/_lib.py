@@ -46,6 +46,7 @@ SIGNATURES = {
     "bd_compress_versioned_batch": (c_int, [c_p, c_p, c_u32, c_u32, c_p, c_u64, c_p, c_p]),
     "bd_decompress": (c_int, [c_p, c_u64, c_p, c_u64, c_p, c_p, c_p, c_u64, c_p, c_p]),
     "bd_decompress_batch": (c_int, [c_p, c_u32, c_p, c_u64, c_p, c_p]),
+    "bd_decompress_batch_streamed": (c_int, [c_p, c_u32, c_p, c_u64, c_p, c_u64, c_p, c_p, c_p]),
     "bd_decompress_noalloc": (c_int, [c_p, c_u64, c_p, c_u64, c_p, c_p, c_p, c_p]),
     "bd_decompress_incremental": (c_int, [c_p, c_u64, c_p, c_u64, c_p, c_p, c_p, c_p, c_u64, c_p,
                                           c_p]),

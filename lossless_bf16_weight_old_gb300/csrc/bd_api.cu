@@ -267,7 +267,8 @@ struct DecItem {
 };
 
 int decompress_impl(const DecItem* items, uint32_t k, void* ws, uint64_t ws_bytes,
-                    int32_t* status_all, cudaStream_t s, bool incremental) {
+                    int32_t* status_all, cudaStream_t s, bool incremental,
+                    bool clear_status = true) {
   if (k > 0 && items == nullptr) return BD_ERR_INVALID_ARG;
   if (!status_all || !aligned(status_all, 4)) return BD_ERR_INVALID_ARG;
   std::vector<uint64_t> ns(k);
@@ -330,7 +331,7 @@ int decompress_impl(const DecItem* items, uint32_t k, void* ws, uint64_t ws_byte
   LaunchCtx c{s, sms, w, lay, k, sz.chunks, sz.tiles};
   int rc;
   if ((rc = check(cudaMemsetAsync(w + lay.state, 0, lay.state_bytes, s)))) return rc;
-  if ((rc = check(cudaMemsetAsync(status_all, 0, sizeof(int32_t), s)))) return rc;
+  if (clear_status && (rc = check(cudaMemsetAsync(status_all, 0, sizeof(int32_t), s)))) return rc;
   if (k == 0) return BD_OK;
   if ((rc = check(upload(host, w + lay.jobs, s)))) return rc;
   if ((rc = check(launch_scan_tiles(c, true)))) return rc;
@@ -343,6 +344,102 @@ int decompress_impl(const DecItem* items, uint32_t k, void* ws, uint64_t ws_byte
   }
   if ((rc = check(launch_apply_bitmap(c, incremental)))) return rc;
   return check(launch_apply_finish(c, status_all));
+}
+
+// Events of one streamed decompress, destroyed when the call returns (the runtime releases an
+// event's resources once the work recorded on it has completed).
+struct StreamEvents {
+  cudaEvent_t e[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
+  ~StreamEvents() {
+    for (cudaEvent_t& x : e)
+      if (x) cudaEventDestroy(x);
+  }
+  cudaError_t create() {
+    for (cudaEvent_t& x : e) {
+      const cudaError_t r = cudaEventCreateWithFlags(&x, cudaEventDisableTiming);
+      if (r != cudaSuccess) return r;
+    }
+    return cudaSuccess;
+  }
+};
+
+// bd_decompress_batch with the payloads in host memory, streamed through two device slots:
+// the items are cut, in order, into groups whose payloads (each at a 256-byte boundary) fit
+// one slot; group g's payloads are copied into slot g % 2 on the copy stream while the apply
+// of group g - 1 runs on the compute stream, and group g's apply waits for its copies only.
+// A slot is refilled (group g + 2) once the apply that read it is done.
+int decompress_streamed_impl(const bd_decompress_item* items, uint32_t k, void* staging,
+                             uint64_t slot_bytes, void* ws, uint64_t ws_bytes,
+                             int32_t* status_all, cudaStream_t s, cudaStream_t cs) {
+  if (k > 0 && !items) return BD_ERR_INVALID_ARG;
+  if (!status_all || !aligned(status_all, 4)) return BD_ERR_INVALID_ARG;
+  if (!cs || cs == s) return BD_ERR_INVALID_ARG;   // a stream of its own for the copies
+  if (k > 0 && (!staging || !aligned(staging, kAlign) || slot_bytes == 0 || slot_bytes % 256 != 0))
+    return BD_ERR_INVALID_ARG;
+  // everything checked before anything is enqueued (the per-group calls then cannot refuse)
+  std::vector<uint64_t> ns(k);
+  std::vector<uint32_t> group_start;
+  uint64_t used = 0;
+  for (uint32_t i = 0; i < k; i++) {
+    const bd_decompress_item& it = items[i];
+    if (it.n > BD_MAX_ELEMS) return BD_ERR_INVALID_ARG;
+    if (it.n > 0 && (!it.d_old || !it.d_out || !aligned(it.d_old, 16) || !aligned(it.d_out, 16)))
+      return BD_ERR_INVALID_ARG;
+    if (it.d_out != it.d_old && overlaps(it.d_out, 2 * it.n, it.d_old, 2 * it.n))
+      return BD_ERR_INVALID_ARG;
+    if (it.size > 0 && !it.d_payload) return BD_ERR_INVALID_ARG;
+    if (!it.d_expected || !aligned(it.d_expected, 8)) return BD_ERR_INVALID_ARG;
+    if (overlaps(it.d_out, 2 * it.n, staging, 2 * slot_bytes)) return BD_ERR_INVALID_ARG;
+    const uint64_t need = up(it.size, 256);
+    if (need > slot_bytes) return BD_ERR_INVALID_ARG;   // a payload larger than a slot
+    if (i == 0 || used + need > slot_bytes) {
+      group_start.push_back(i);
+      used = 0;
+    }
+    used += need;
+    ns[i] = it.n;
+  }
+  group_start.push_back(k);
+  Sizes sz;
+  if (!sizes_of(ns.data(), k, sz)) return BD_ERR_INVALID_ARG;
+  const WsLayout lay = make_layout(k, sz, false);   // covers the layout of every group
+  if (!ws || !aligned(ws, kAlign) || ws_bytes < lay.total) return BD_ERR_INVALID_ARG;
+  if (k > 0 && overlaps(ws, lay.total, staging, 2 * slot_bytes)) return BD_ERR_INVALID_ARG;
+  for (uint32_t i = 0; i < k; i++)
+    if (overlaps(items[i].d_out, 2 * items[i].n, ws, lay.total)) return BD_ERR_INVALID_ARG;
+
+  int rc;
+  if ((rc = check(cudaMemsetAsync(status_all, 0, sizeof(int32_t), s)))) return rc;
+  if (k == 0) return BD_OK;
+  StreamEvents ev;   // 0, 1: slot copied; 2, 3: slot free; 4: the call's start
+  if ((rc = check(ev.create()))) return rc;
+  // the copies may not overwrite a slot that work enqueued before this call still reads
+  if ((rc = check(cudaEventRecord(ev.e[4], s)))) return rc;
+  if ((rc = check(cudaStreamWaitEvent(cs, ev.e[4], 0)))) return rc;
+  uint8_t* const base = static_cast<uint8_t*>(staging);
+  std::vector<DecItem> dec;
+  for (size_t g = 0; g + 1 < group_start.size(); g++) {
+    const uint32_t slot = (uint32_t)(g & 1), i0 = group_start[g], i1 = group_start[g + 1];
+    uint8_t* const sb = base + slot * slot_bytes;
+    if (g >= 2 && (rc = check(cudaStreamWaitEvent(cs, ev.e[2 + slot], 0)))) return rc;
+    dec.clear();
+    uint64_t off = 0;
+    for (uint32_t i = i0; i < i1; i++) {
+      const bd_decompress_item& x = items[i];
+      if (x.size > 0 &&
+          (rc = check(cudaMemcpyAsync(sb + off, x.d_payload, x.size, cudaMemcpyHostToDevice, cs))))
+        return rc;
+      dec.push_back(DecItem{x.d_old, x.d_out, x.n, sb + off, x.size, x.d_expected, nullptr,
+                            nullptr, x.d_status});
+      off += up(x.size, 256);
+    }
+    if ((rc = check(cudaEventRecord(ev.e[slot], cs)))) return rc;
+    if ((rc = check(cudaStreamWaitEvent(s, ev.e[slot], 0)))) return rc;
+    if ((rc = decompress_impl(dec.data(), i1 - i0, ws, ws_bytes, status_all, s, false, false)))
+      return rc;
+    if ((rc = check(cudaEventRecord(ev.e[2 + slot], s)))) return rc;
+  }
+  return BD_OK;
 }
 
 uint64_t le64(const uint8_t* p) {
@@ -442,6 +539,14 @@ int bd_decompress_batch(const bd_decompress_item* h_items, uint32_t k, void* d_w
   }
   return decompress_impl(it.data(), k, d_ws, ws_bytes, d_status,
                          static_cast<cudaStream_t>(stream), false);
+}
+
+int bd_decompress_batch_streamed(const bd_decompress_item* h_items, uint32_t k, void* d_staging,
+                                 uint64_t slot_bytes, void* d_ws, uint64_t ws_bytes,
+                                 int32_t* d_status, void* stream, void* copy_stream) {
+  return decompress_streamed_impl(h_items, k, d_staging, slot_bytes, d_ws, ws_bytes, d_status,
+                                  static_cast<cudaStream_t>(stream),
+                                  static_cast<cudaStream_t>(copy_stream));
 }
 
 int bd_decompress_incremental(uint16_t* d_w, uint64_t n, const void* d_payload, uint64_t size,

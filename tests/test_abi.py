@@ -30,7 +30,7 @@ def test_headers_are_all_listed():
 
 def test_library_exports_every_declared_symbol(cuda_lib):
     names = _declared()
-    assert len(names) == 17
+    assert len(names) == 18
     for name in names:
         assert hasattr(cuda_lib, name), name
     out = subprocess.run(["nm", "-D", "--defined-only", _lib.path()], capture_output=True,
@@ -257,6 +257,28 @@ def test_argument_checks_need_no_gpu(cuda_lib):
     assert cuda_lib.bd_decompress_noalloc(dummy, (1 << 27) + 1, dummy, 64, dummy, dummy, dummy,
                                           None) == 1
     assert cuda_lib.bd_status_sync(None, None) == 1
+    # the streamed apply: every argument is checked before anything is enqueued
+    it = (_lib.DecompressItem * 1)()
+    it[0].d_old = it[0].d_out = 1 << 24
+    it[0].n = 4096
+    it[0].d_payload = 1 << 12   # (a host address; never read here)
+    it[0].size = 1000
+    it[0].d_expected = 4096
+    ws, stg, st = ctypes.c_void_p(1 << 28), ctypes.c_void_p(1 << 30), ctypes.c_void_p(1 << 26)
+    s1, s2 = ctypes.c_void_p(0x5000), ctypes.c_void_p(0x6000)
+    streamed = cuda_lib.bd_decompress_batch_streamed
+    assert streamed(it, 1, stg, 1024, ws, 1 << 20, st, s1, None) == 1      # no copy stream
+    assert streamed(it, 1, stg, 1024, ws, 1 << 20, st, s1, s1) == 1        # the same stream
+    assert streamed(it, 1, stg, 768, ws, 1 << 20, st, s1, s2) == 1         # payload > slot
+    assert streamed(it, 1, stg, 1000, ws, 1 << 20, st, s1, s2) == 1        # slot not 256k
+    assert streamed(it, 1, ctypes.c_void_p((1 << 30) + 16), 1024, ws, 1 << 20, st, s1,
+                    s2) == 1                                                 # staging alignment
+    assert streamed(it, 1, ctypes.c_void_p((1 << 24) + 4096), 1024, ws, 1 << 20, st, s1,
+                    s2) == 1                                                 # staging over out
+    assert streamed(it, 1, stg, 1024, ws, 16, st, s1, s2) == 1              # workspace too small
+    assert streamed(it, 1, stg, 1024, ws, 1 << 20, None, s1, s2) == 1      # no status word
+    it[0].d_payload = None
+    assert streamed(it, 1, stg, 1024, ws, 1 << 20, st, s1, s2) == 1        # no payload
     # the fault-injection hook stalls a tensor of the call, no other
     items = (_lib.CompressItem * 2)()
     for stall in (2, 3, 1 << 31):
