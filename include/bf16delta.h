@@ -254,14 +254,15 @@ BD_API int bd_decompress_batch(const bd_decompress_item* h_items, uint32_t k, vo
  * cudaHostAlloc, for the copies to overlap; pageable memory works but each copy may block the
  * host); it must stay valid and unchanged until stream has passed the call.
  * d_staging: device, 256-byte aligned, 2 * slot_bytes bytes, slot_bytes a multiple of 256
- * and at least the largest payload rounded up to 256; it may not overlap any output or the
- * workspace.  copy_stream: a stream other than stream (use non-blocking streams: the legacy
- * default stream would serialise the copies with the applies).  The workspace is
+ * (at most 2^40) and at least the largest payload rounded up to 256; it may not overlap any
+ * output or the workspace.  copy_stream: a stream other than stream (use non-blocking streams:
+ * the legacy default stream would serialise the copies with the applies).  The workspace is
  * bd_decompress_workspace_size of all k tensors.  Results, per-tensor statuses and *d_status
  * (required; the largest status over all tensors) are those of bd_decompress_batch on the
  * same items with device payloads.  Every argument is checked before anything is enqueued:
  * BD_ERR_INVALID_ARG otherwise (also for a payload larger than a slot); BD_ERR_CUDA when the
- * runtime refuses an event, copy or launch, with earlier groups possibly enqueued. */
+ * runtime refuses an event, copy or launch, with earlier groups possibly enqueued.  The call
+ * creates five CUDA events and destroys them before it returns (no memory is allocated). */
 BD_API int bd_decompress_batch_streamed(const bd_decompress_item* h_items, uint32_t k,
                                         void* d_staging, uint64_t slot_bytes, void* d_ws,
                                         uint64_t ws_bytes, int32_t* d_status, void* stream,

@@ -374,7 +374,8 @@ int decompress_streamed_impl(const bd_decompress_item* items, uint32_t k, void* 
   if (k > 0 && !items) return BD_ERR_INVALID_ARG;
   if (!status_all || !aligned(status_all, 4)) return BD_ERR_INVALID_ARG;
   if (!cs || cs == s) return BD_ERR_INVALID_ARG;   // a stream of its own for the copies
-  if (k > 0 && (!staging || !aligned(staging, kAlign) || slot_bytes == 0 || slot_bytes % 256 != 0))
+  if (k > 0 && (!staging || !aligned(staging, kAlign) || slot_bytes == 0 ||
+                slot_bytes % 256 != 0 || slot_bytes > (1ull << 40)))
     return BD_ERR_INVALID_ARG;
   // everything checked before anything is enqueued (the per-group calls then cannot refuse)
   std::vector<uint64_t> ns(k);

@@ -71,7 +71,7 @@ def test_workspace_sizes(cuda_lib):
     assert 0 < a < b
     assert a % 256 == 0
     # O(chunks) scratch: compress a 1 KiB slot plus ~30 bytes per 4096-element chunk,
-    # decompress ~20 bytes per chunk
+    # decompress ~24 bytes per chunk
     d = ws(cuda_lib.bd_decompress_workspace_size, [1 << 24])
     c = ws(cuda_lib.bd_compress_workspace_size, [1 << 24])
     chunks = (1 << 24) // 4096
@@ -271,6 +271,7 @@ def test_argument_checks_need_no_gpu(cuda_lib):
     assert streamed(it, 1, stg, 1024, ws, 1 << 20, st, s1, s1) == 1        # the same stream
     assert streamed(it, 1, stg, 768, ws, 1 << 20, st, s1, s2) == 1         # payload > slot
     assert streamed(it, 1, stg, 1000, ws, 1 << 20, st, s1, s2) == 1        # slot not 256k
+    assert streamed(it, 1, stg, 1 << 62, ws, 1 << 20, st, s1, s2) == 1     # slot too large
     assert streamed(it, 1, ctypes.c_void_p((1 << 30) + 16), 1024, ws, 1 << 20, st, s1,
                     s2) == 1                                                 # staging alignment
     assert streamed(it, 1, ctypes.c_void_p((1 << 24) + 4096), 1024, ws, 1 << 20, st, s1,
