@@ -252,7 +252,9 @@ BD_API int bd_decompress_batch(const bd_decompress_item* h_items, uint32_t k, vo
  * copy_stream while group g - 1 is applied on stream, and a slot is refilled only after the
  * apply that read it.  Each item's d_payload is a HOST address (page-locked memory, e.g.
  * cudaHostAlloc, for the copies to overlap; pageable memory works but each copy may block the
- * host); it must stay valid and unchanged until stream has passed the call.
+ * host); it must stay valid and unchanged until stream has passed the call.  Payloads that
+ * lie in host memory at the distances they take in the slot are copied together, with the
+ * bytes between them.
  * d_staging: device, 256-byte aligned, 2 * slot_bytes bytes, slot_bytes a multiple of 256
  * (at most 2^40) and at least the largest payload rounded up to 256; it may not overlap any
  * output or the workspace.  copy_stream: a stream other than stream (use non-blocking streams:

@@ -424,16 +424,33 @@ int decompress_streamed_impl(const bd_decompress_item* items, uint32_t k, void* 
     uint8_t* const sb = base + slot * slot_bytes;
     if (g >= 2 && (rc = check(cudaStreamWaitEvent(cs, ev.e[2 + slot], 0)))) return rc;
     dec.clear();
-    uint64_t off = 0;
+    // one copy per run of payloads laid out in host memory as they go into the slot (each at
+    // the slot offset's distance from the run's first): thousands of small tensors would
+    // otherwise cost one host call each
+    uint64_t off = 0, run_off = 0, run_len = 0;
+    const uint8_t* run_src = nullptr;
     for (uint32_t i = i0; i < i1; i++) {
       const bd_decompress_item& x = items[i];
-      if (x.size > 0 &&
-          (rc = check(cudaMemcpyAsync(sb + off, x.d_payload, x.size, cudaMemcpyHostToDevice, cs))))
-        return rc;
+      const uint8_t* src = static_cast<const uint8_t*>(x.d_payload);
+      if (x.size > 0) {
+        if (run_src && src == run_src + (off - run_off)) {
+          run_len = off - run_off + x.size;
+        } else {
+          if (run_src && (rc = check(cudaMemcpyAsync(sb + run_off, run_src, run_len,
+                                                     cudaMemcpyHostToDevice, cs))))
+            return rc;
+          run_src = src;
+          run_off = off;
+          run_len = x.size;
+        }
+      }
       dec.push_back(DecItem{x.d_old, x.d_out, x.n, sb + off, x.size, x.d_expected, nullptr,
                             nullptr, x.d_status});
       off += up(x.size, 256);
     }
+    if (run_src &&
+        (rc = check(cudaMemcpyAsync(sb + run_off, run_src, run_len, cudaMemcpyHostToDevice, cs))))
+      return rc;
     if ((rc = check(cudaEventRecord(ev.e[slot], cs)))) return rc;
     if ((rc = check(cudaStreamWaitEvent(s, ev.e[slot], 0)))) return rc;
     if ((rc = decompress_impl(dec.data(), i1 - i0, ws, ws_bytes, status_all, s, false, false)))

@@ -891,8 +891,9 @@ __device__ __forceinline__ uint32_t list_entry(const uint8_t* __restrict__ list,
 // there (prefetching a later chunk instead thrashes L2 and was much slower).  Chunks with a
 // bitmap block are listed for apply_dense, which also adds their checksum terms.
 // The version-1/2 build runs at three blocks per SM (75 registers; four measured no better), the
-// general build at four (64 registers, no spills: 3% faster on version-3 payloads, 6% on
-// overwrite payloads, the same on version 4, whose decode is bound by instruction issue).
+// general build at four (64 registers, no spills: 6% faster on overwrite payloads, whose apply
+// waits on a read of each changed element; version 3 the same or up to 3% faster, version 4
+// the same -- its decode is bound by instruction issue).
 template <bool V3>
 __global__ void __launch_bounds__(kThreads, V3 ? 4 : 3)
 k_apply_chunks(const DJob* __restrict__ jobs, const uint64_t* __restrict__ chunk_start,

@@ -54,22 +54,24 @@ def _groups(sizes, slot):
 
 
 def _host_layout(refs, gap=37):
-    """Host buffer holding the payloads back to back at odd offsets (not 256-aligned)."""
-    offs, o = [], gap
+    """Host buffer holding the payloads back to back at odd offsets (not 256-aligned), or with
+    gap=None at 256-byte boundaries -- the slot's own layout, so that the call copies each
+    group's payloads together."""
+    offs, o = [], (gap or 0)
     for r in refs:
         offs.append(o)
-        o += r.size + gap
+        o += (r.size + 255) // 256 * 256 if gap is None else r.size + gap
     return offs, o
 
 
-@pytest.mark.parametrize("host_kind", ["mapped", "pinned"])
-def test_streamed_apply_matches_oracle(host_kind):
+@pytest.mark.parametrize("host_kind,gap", [("mapped", 37), ("pinned", 37), ("pinned", None)])
+def test_streamed_apply_matches_oracle(host_kind, gap):
     olds, news = _tensors()
     pairs = [oracle_pair(o, nw) for o, nw in zip(olds, news)]
     refs = [p[0] for p in pairs]
     cks = [p[1] for p in pairs]
     ck_old = [oracle.checksum(to_np_u16(o)) for o in olds]
-    offs, total = _host_layout(refs)
+    offs, total = _host_layout(refs, gap)
     if host_kind == "mapped":
         host = bd.MappedHostBuffer(total)
         view = host.numpy()
